@@ -1,0 +1,221 @@
+/*
+ * okls.h -- C ABI of the GB300 Online KL Shampoo (OKLS) preconditioner step.
+ *
+ * What the library computes (page "Online KL Shampoo", README of the
+ * tilde-research release, section "How it works"): for every matrix gradient
+ * G (m x n) of a batch of same-shape parameters W,
+ *
+ *   S_a <- beta2 S_a + (1-beta2)/n (G P_b)(G P_b)^T + eps I          (m x m)
+ *   S_b <- beta2 S_b + (1-beta2)/m (P_a G)^T (P_a G) + eps I          (n x n)
+ *   P_a <- S_a^(-1/2),  P_b <- S_b^(-1/2)      (same step; coupled Newton-
+ *          Schulz, 10 iterations, 27 binary16 GEMMs, fp32 accumulation)
+ *   N   = Nesterov momentum with variance correction
+ *   U   = P_a N P_b
+ *   W   <- W - lr wd (lr/lr_peak) W - lr c_shape U,
+ *          c_shape = sqrt(m/n) / (sqrt(m) + sqrt(n)).
+ *
+ * Conventions used by every entry point
+ *   - Matrices are row-major and contiguous; a batch is `batch` matrices
+ *     back to back (the 3-D (N, m, n) parameter of the README's "Batched
+ *     matrices" section).  m = rows = fan-out, n = columns = fan-in.
+ *   - Pointers named *_dev are device pointers; they must be 256-byte aligned
+ *     (any cudaMalloc / PyTorch CUDA allocation is).  The caller owns every
+ *     buffer: the library never allocates device memory in okls_step.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *     okls_step and the state calls are asynchronous on that stream.
+ *   - Every function returns an okls_status; on failure a message is kept
+ *     per thread and returned by okls_last_error().  No C++ exception ever
+ *     crosses this boundary.
+ */
+#ifndef OKLS_H_
+#define OKLS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OKLS_ABI_VERSION 1
+
+typedef enum okls_status {
+  OKLS_OK = 0,
+  OKLS_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad hyperparameter  */
+  OKLS_ERR_UNSUPPORTED = 2,  /* shape/dtype/alignment the kernels can't take */
+  OKLS_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed            */
+  OKLS_ERR_NONFINITE = 4,    /* device flag: non-finite input or iterate     */
+  OKLS_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up           */
+  OKLS_ERR_NO_DEVICE = 6     /* no CUDA device / wrong architecture          */
+} okls_status;
+
+/* Element types of W and G. */
+typedef enum okls_dtype { OKLS_F32 = 0, OKLS_BF16 = 1 } okls_dtype;
+
+/* Which piece of state okls_get_state / okls_set_state move. */
+typedef enum okls_state_part {
+  OKLS_STATE_M = 0,   /* momentum,                 batch x m x n, fp32 */
+  OKLS_STATE_SA = 1,  /* left factor S_a,          batch x m x m, fp32 */
+  OKLS_STATE_SB = 2,  /* right factor S_b,         batch x n x n, fp32 */
+  OKLS_STATE_PA = 3,  /* left root P_a = S_a^-1/2, batch x m x m, fp32 */
+  OKLS_STATE_PB = 4   /* right root P_b,           batch x n x n, fp32 */
+} okls_state_part;
+
+/* Bits of the device status word (okls_query_status). */
+#define OKLS_DEV_NONFINITE_INPUT 0x1u  /* G (or the momentum) not finite   */
+#define OKLS_DEV_NONFINITE_ITER 0x2u   /* a Newton-Schulz iterate overflowed */
+#define OKLS_DEV_NONFINITE_UPDATE 0x4u /* the new W holds a non-finite value */
+#define OKLS_DEV_TIMEOUT 0x8u          /* a bounded pipeline wait expired   */
+
+/*
+ * Hyperparameters of one same-shape batch.  Defaults (okls_config_default)
+ * are those of the README's "Hyperparameters" table: lr 0.09434 (also
+ * lr_peak), beta1 0.9684, beta2 0.9482, eps 1e-9, weight_decay 0.0303, and
+ * 10 Newton-Schulz iterations.
+ *
+ *   ns_split_iters  0: every Newton-Schulz GEMM takes plain binary16 operands
+ *                   (27 GEMMs, the README's design).  s > 0: iterations
+ *                   0..s-1 carry each operand as a (hi, lo) binary16 pair and
+ *                   multiply hi*hi + hi*lo + lo*hi (three GEMMs per product),
+ *                   for factors whose condition number exceeds ~1e3.
+ *   ns_lo           lower end l_0 of the sqrt-eigenvalue interval the
+ *                   coefficient schedule is optimised for (default 1e-3:
+ *                   eigenvalues down to 1e-6 ||S||_F converge).
+ *   ridge           rho >= 0: the root is taken of S + rho ||S||_F I.
+ *   variance_correction  1: N_t is divided by its standard deviation under
+ *                   iid unit-variance gradients; 0: plain Nesterov.
+ *   eps_every_update 1: +eps I in every factor update (and S_0 = eps I);
+ *                   0: only S_0 = eps I.
+ */
+typedef struct okls_config {
+  int64_t batch;
+  int64_t m;
+  int64_t n;
+  int32_t param_dtype; /* okls_dtype of W */
+  int32_t grad_dtype;  /* okls_dtype of G */
+  float lr_peak;
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+  int32_t ns_iters;
+  int32_t ns_split_iters;
+  float ns_lo;
+  float ridge;
+  int32_t variance_correction;
+  int32_t eps_every_update;
+  int32_t reserved[8]; /* must be zero */
+} okls_config;
+
+typedef struct okls_handle_s *okls_handle;
+
+/* Library ABI version (OKLS_ABI_VERSION). */
+int32_t okls_abi_version(void);
+
+/* Message of the last failed call on this thread ("" if none).  The pointer
+ * stays valid until the next failing call on the same thread. */
+const char *okls_last_error(void);
+
+/* Fill *cfg with the README defaults for a batch of `batch` m x n matrices. */
+okls_status okls_config_default(okls_config *cfg, int64_t batch, int64_t m,
+                                int64_t n);
+
+/* Bytes of persistent state (M, S_a, S_b, P_a, P_b, fp32, layout owned by the
+ * library) and of workspace the caller must provide to okls_create.  The
+ * workspace also persists between steps (binary16 copies of P, scales). */
+okls_status okls_state_bytes(const okls_config *cfg, size_t *state_bytes,
+                             size_t *workspace_bytes);
+
+/*
+ * Bind a handle to caller-owned device memory.  Validates cfg, builds the TMA
+ * descriptors and the launch plan on the host, and uploads them with one
+ * synchronous cudaMemcpy; allocates no device memory of its own except the
+ * small descriptor table (freed by okls_destroy).  The state is NOT
+ * initialised: call okls_reset_state (or okls_set_state for every part).
+ * The current CUDA device must be the one that owns the buffers.
+ */
+okls_status okls_create(const okls_config *cfg, void *state_dev,
+                        size_t state_bytes, void *workspace_dev,
+                        size_t workspace_bytes, okls_handle *out);
+
+/* M = 0, S_a = eps I, S_b = eps I, P_a = I, P_b = I, step counter t = 0
+ * (README: eps is added at factor initialisation; P_0 = I is this library's
+ * reading of the first step).  Asynchronous on `stream`. */
+okls_status okls_reset_state(okls_handle h, void *stream);
+
+/*
+ * One OKLS step over the whole batch, asynchronous on `stream`.
+ *   W_dev  batch x m x n, param_dtype, updated in place.
+ *   G_dev  batch x m x n, grad_dtype, read only.
+ *   lr     current learning rate (finite, >= 0); lr_peak is fixed in cfg.
+ * Increments the step counter t on the host.  Device-side failures (non-
+ * finite inputs or iterates, an expired wait) are recorded in the device
+ * status word and reported by okls_query_status; once the word is non-zero
+ * the remaining stages of the step skip their writes, and the W update is
+ * skipped whenever an earlier stage flagged (a flag raised by the update
+ * itself still lets that step's other tiles land).
+ */
+okls_status okls_step(okls_handle h, void *W_dev, const void *G_dev, float lr,
+                      void *stream);
+
+/* Synchronise `stream`, read the device status word into *dev_status (may be
+ * NULL) and clear it.  Returns OKLS_ERR_NONFINITE / OKLS_ERR_TIMEOUT when the
+ * corresponding bits were set, OKLS_OK otherwise. */
+okls_status okls_query_status(okls_handle h, void *stream,
+                              uint32_t *dev_status);
+
+/* Copy one part of the fp32 state to / from a caller device buffer of the
+ * part's size (see okls_state_part), asynchronously on `stream`.  Setting
+ * OKLS_STATE_PA / PB also refreshes the binary16 copies the GEMMs read. */
+okls_status okls_get_state(okls_handle h, int32_t part, void *dst_dev,
+                           void *stream);
+okls_status okls_set_state(okls_handle h, int32_t part, const void *src_dev,
+                           void *stream);
+
+/* Host-side step counter t (the number of completed steps). */
+okls_status okls_get_step(okls_handle h, int64_t *t);
+okls_status okls_set_step(okls_handle h, int64_t t);
+
+/* Release the handle and its descriptor table (not the caller's buffers).
+ * Synchronises the device first.  NULL is accepted. */
+okls_status okls_destroy(okls_handle h);
+
+/*
+ * Coefficient schedule the library uses (host computation, no GPU needed):
+ * for k < iters, a[k], b[k] of T_k = a_k I + b_k Z_k Y_k, the minimax odd
+ * cubic on [l_k, u_k] (l_0 = lo, u_0 = 1), and for k <= iters the exponent
+ * zexp[k] = ceil(log2(prod_{j<k} a_j)) of the per-step binary16 scale.
+ * Arrays must hold iters (a, b) and iters+1 (zexp) entries.
+ */
+okls_status okls_ns_schedule(int32_t iters, double lo, double *a, double *b,
+                             int32_t *zexp);
+
+/*
+ * Debug / test entry: inverse square roots of `count` symmetric d x d fp32
+ * matrices S_dev by the library's Newton-Schulz chain (same kernels, schedule
+ * and precision mode as okls_step with the given iters / split / lo / ridge).
+ *   P_dev     out, count x d x d fp32: S^(-1/2).
+ *   root_dev  optional out (NULL to skip), count x d x d fp32: S^(1/2) (one
+ *             extra GEMM per iteration-9 factor).
+ *   trace_dev optional out (NULL to skip), binary16, count x (3*iters+1) x d
+ *             x d: for k = 0..iters-1 the stored iterates Y^_k, Z^_k, T^_k (Z^_0
+ *             is written as zeros), then Z^_iters; row-major, unpadded.
+ *   workspace_dev / workspace_bytes: from okls_inv_root_workspace_bytes.
+ * Asynchronous on `stream`; errors of the device status word are reported by
+ * the returned status only after an explicit synchronisation, so the call
+ * itself synchronises `stream` at the end and reads it.
+ */
+okls_status okls_inv_root_workspace_bytes(int64_t d, int64_t count,
+                                          int32_t iters, int32_t split_iters,
+                                          size_t *workspace_bytes);
+okls_status okls_inv_root(const float *S_dev, float *P_dev, float *root_dev,
+                          uint16_t *trace_dev, int64_t d, int64_t count,
+                          int32_t iters, int32_t split_iters, float lo,
+                          float ridge, void *workspace_dev,
+                          size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OKLS_H_ */

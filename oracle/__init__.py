@@ -1,0 +1,29 @@
+"""Float64 CPU oracle for the Online KL Shampoo (OKLS) preconditioner step.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may use it.  It shares no code, table or constant generator with
+the CUDA library; where both sides need the same number (the Newton-Schulz
+coefficient schedule, the momentum variance correction) each side derives it
+independently from the same written definition.
+
+Parity status per function (the pins live in ``tests/test_oracle_pins.py``):
+
+* ``sym_power`` / ``inv_root_exact``      pinned (Shampoo 2x3 hand example,
+  Problem 14, eigen-identities).
+* ``cans_schedule``                        pinned (textbook Newton-Schulz special
+  case, brute-force minimax, equioscillation).
+* ``ns_exact``, ``ns_replay``             pinned (scalar-polynomial identity,
+  convergence bound, fp16 rounding checks).
+* ``factor_ema``                           pinned (hand example L = G G^T,
+  brute-force loops).
+* ``okls_step`` / ``okls_run``             pinned (square fixed-gradient polar
+  limit, descent sign, closed-form weight decay).
+* ``variance_correction``                  pinned by Monte Carlo against its
+  definition (variance of the Nesterov combination for iid unit gradients);
+  the *choice* of this reading is not printed on the pages.
+* AdamC correction factor lr/lr_peak       parity unpinned (closed-form scalar,
+  only the reading is documented; the G = 0 decay test fixes its arithmetic).
+"""
+
+from .okls_oracle import *  # noqa: F401,F403

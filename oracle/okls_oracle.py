@@ -1,0 +1,441 @@
+"""Plain float64 restatement of the Online KL Shampoo step (test infrastructure).
+
+Sources (page title, then section / equation):
+
+* "Online KL Shampoo" (tilde-research release README), section "How it works":
+  the KL-form factor EMAs, the fresh inverse roots, the two-sided whitening and
+  the muP shape multiplier; bullet list under the title: 10-step "Scaled CANS
+  Coupled Newton-Schulz", 27 FP16 GEMMs, FP32 accumulation, Nesterov momentum
+  with variance correction, AdamC decoupled weight decay; section
+  "Hyperparameters": defaults and the meaning of eps; section "Learning-rate
+  schedule": lr_peak is the initial lr kept for the AdamC correction.
+* "Shampoo" chapter of the optim-book (section "2 x 3 gradient by hand" and
+  Problem 14): worked numbers used as pins.
+
+Readings of points the pages leave open (each is listed, with its reason, in
+the design notes of the repository):
+
+r1  P_0 = I at the first step (the EMAs use the previous roots).
+r2  eps is added to both factors at initialisation (S_0 = eps*I) and at every
+    update (+ eps*I).
+r3  the factors are built from the raw gradient G, not from the momentum.
+r4  Nesterov form: M_t = b1*M_{t-1} + (1-b1)*G_t,  N_t = b1*M_t + (1-b1)*G_t.
+r5  "variance correction": N_t is divided by the standard deviation it would
+    have for iid unit-variance gradients (``variance_correction``).
+r6  AdamC: decoupled decay lr*wd*(lr/lr_peak)*W_{t-1}.
+r7  W_t = W_{t-1} - decay - lr*c_shape*U_t, m = rows, n = cols.
+r8  Chebyshev (CANS) coefficients are not printed: each step applies the odd
+    cubic q(s) = a*s + b*s^3 that is the minimax approximation of 1 on the
+    current interval [l, u] of sqrt-eigenvalues (``cans_schedule``).
+r9  per-step scales are powers of two derived from the schedule alone.
+r10 an optional relative ridge rho: the root is taken of S + rho*||S||_F*I.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+__all__ = [
+    "Hyper", "OklsState", "c_shape", "variance_correction", "adamc_decay",
+    "sym_power", "inv_root_exact", "cans_schedule", "ns_exponents",
+    "ns_scalar_map", "ns_exact", "ns_matrix_float64", "f16", "split16",
+    "ns_replay", "ns_replay_iteration", "factor_ema", "init_state",
+    "okls_step", "okls_run", "rel_fro", "NS_HEADROOM", "NS_MARGIN",
+]
+
+# Power-of-two headroom of the stored binary16 operands (reading r9): Y and T
+# are stored times 2**12, Z times 2**(12 - z_k).  |Y| <= 2, |T| <= a_k <= 5.2
+# and |Z| <= 2**z_k bound the entries, so the stored values stay below 2.2e4
+# (binary16 max 65504) while typical entries, and the low halves of split
+# pairs, stay above the subnormal range (6.1e-5).
+NS_HEADROOM = 12
+# Normalisation margin: Y_0 = S_reg / (||S||_F (1+rho) (1+2**-8)), so that the
+# largest sqrt-eigenvalue sits strictly inside the first interval even after
+# binary16 rounding of Y_0.
+NS_MARGIN = 2.0 ** -8
+
+
+@dataclass
+class Hyper:
+    """Hyperparameters; defaults from the 'Hyperparameters' table of the
+    Online KL Shampoo README."""
+    lr: float = 0.09434
+    beta1: float = 0.9684
+    beta2: float = 0.9482
+    eps: float = 1e-9
+    weight_decay: float = 0.0303
+    lr_peak: float | None = None      # None -> lr (the initial lr is lr_peak)
+    ns_iters: int = 10
+    ns_lo: float = 1e-3               # l_0 of the coefficient schedule (r8)
+    ridge: float = 0.0                # rho of reading r10
+    variance_correction: bool = True  # reading r5
+    eps_every_update: bool = True     # reading r2
+
+    @property
+    def peak(self) -> float:
+        return self.lr if self.lr_peak is None else self.lr_peak
+
+
+@dataclass
+class OklsState:
+    """Per-matrix state as listed under 'Hyperparameters' of the README: one
+    (m,n) momentum and two copies each of the (m,m) and (n,n) shapes."""
+    M: np.ndarray
+    Sa: np.ndarray
+    Sb: np.ndarray
+    Pa: np.ndarray
+    Pb: np.ndarray
+    t: int = 0
+    extra: dict = field(default_factory=dict)
+
+
+# ---------------------------------------------------------------- scalars ---
+
+def c_shape(m: int, n: int) -> float:
+    """muP shape multiplier sqrt(m/n) / (sqrt(m) + sqrt(n)) ('How it works')."""
+    return math.sqrt(m / n) / (math.sqrt(m) + math.sqrt(n))
+
+
+def variance_correction(beta1: float, t: int) -> float:
+    """kappa_t of reading r5.
+
+    With M_0 = 0 and unrolled momentum,
+        N_t = (1-b1) [ (1+b1) G_t + sum_{j=1}^{t-1} b1^(t-j+1) G_j ],
+    so for iid unit-variance G_j its variance is
+        v_t = (1-b1)^2 [ (1+b1)^2 + sum_{k=2}^{t} b1^(2k) ].
+    The correction multiplies N_t by v_t^(-1/2).
+    """
+    if t < 1:
+        raise ValueError("step index starts at 1")
+    b = float(beta1)
+    tail = 0.0
+    for k in range(2, t + 1):
+        tail += b ** (2 * k)
+    v = (1.0 - b) ** 2 * ((1.0 + b) ** 2 + tail)
+    return 1.0 / math.sqrt(v)
+
+
+def adamc_decay(lr: float, lr_peak: float, wd: float) -> float:
+    """Decoupled AdamC decay coefficient lr * wd * (lr / lr_peak) (r6)."""
+    return lr * wd * (lr / lr_peak)
+
+
+# ------------------------------------------------------------ exact roots ---
+
+def _sym(S: np.ndarray) -> np.ndarray:
+    S = np.asarray(S, dtype=np.float64)
+    return 0.5 * (S + S.T)
+
+
+def sym_power(S: np.ndarray, p: float, rcond: float | None = None) -> np.ndarray:
+    """S^p of a symmetric PSD matrix by eigendecomposition.
+
+    For p < 0, eigenvalues <= rcond * lambda_max are treated as zero (pseudo
+    inverse), which is how a rank-deficient Shampoo factor is inverted in the
+    optim-book's worked example.  rcond=None keeps every eigenvalue.
+    """
+    lam, Q = np.linalg.eigh(_sym(S))
+    lam = np.maximum(lam, 0.0)
+    out = np.zeros_like(lam)
+    if p < 0:
+        keep = lam > (0.0 if rcond is None else rcond * lam.max())
+        out[keep] = lam[keep] ** p
+    else:
+        out = lam ** p
+    return (Q * out) @ Q.T
+
+
+def inv_root_exact(S: np.ndarray, ridge: float = 0.0) -> np.ndarray:
+    """P = (S + ridge*||S||_F*I)^(-1/2), the exact root ('How it works':
+    P_{a,t} = S_{a,t}^{-1/2}); ridge 0 is the plain root."""
+    S = _sym(S)
+    c = math.sqrt(float(np.sum(S * S)))
+    return sym_power(S + ridge * c * np.eye(S.shape[0]), -0.5)
+
+
+# -------------------------------------------------- Newton-Schulz schedule ---
+
+def cans_schedule(iters: int = 10, lo: float = 1e-3, hi: float = 1.0):
+    """Coefficients (a_k, b_k) and intervals [l_k, u_k] of reading r8.
+
+    Coupled Newton-Schulz keeps Y_k, Z_k polynomials in S; with T_k = a I + b
+    Z_k Y_k, an eigen-pair (y, z) of (Y_k, Z_k) moves to (y t, z t), t = a +
+    b y z, so s = sqrt(y z) maps by the odd cubic q(s) = a s + b s^3 and the
+    iteration converges when s -> 1 (then z -> lambda^(-1/2)).
+
+    Each step picks the q minimising max |1 - q(s)| on [l, u].  Its error
+    equioscillates at l, at the interior maximum s* = sqrt(-a/(3b)) and at u:
+      q(l) = q(u)            gives  a = -b (u^2 + u l + l^2) = -b D,
+      q(l) + q(s*) = 2       gives  a = 2 / (l u (u + l)/D + (2/3) sqrt(D/3)),
+    and the next interval is [q(l), q(s*)].  For l = u = 1 this is the
+    textbook (3/2, -1/2) step.
+    """
+    out = []
+    l, u = float(lo), float(hi)
+    for _ in range(iters):
+        D = u * u + u * l + l * l
+        a = 2.0 / (l * u * (u + l) / D + (2.0 / 3.0) * math.sqrt(D / 3.0))
+        b = -a / D
+        out.append((a, b, l, u))
+        s_star = math.sqrt(D / 3.0)
+        l, u = a * l + b * l ** 3, a * s_star + b * s_star ** 3
+    return out
+
+
+def ns_exponents(schedule) -> list[int]:
+    """z_k = ceil(log2(prod_{j<k} a_j)), z_0 = 0 (reading r9).
+
+    Every eigenvalue of Z_k is a product of factors t_j = a_j + b_j s^2 <= a_j
+    (b_j < 0), so |Z_k| entries are bounded by 2**z_k; the stored operand is
+    Z_k * 2**(headroom - z_k).  One entry per iterate k = 0..iters.
+    """
+    z = [0]
+    prod = 1.0
+    for (a, _b, _l, _u) in schedule:
+        prod *= a
+        z.append(int(math.ceil(math.log2(prod))))
+    return z
+
+
+def ns_scalar_map(mu: np.ndarray, schedule) -> tuple[np.ndarray, np.ndarray]:
+    """Exact-arithmetic NS on eigenvalues mu of Y_0: returns (y_K, z_K)."""
+    y = np.asarray(mu, dtype=np.float64).copy()
+    z = np.ones_like(y)
+    for (a, b, _l, _u) in schedule:
+        t = a + b * y * z
+        y, z = y * t, z * t
+    return y, z
+
+
+def _normaliser(S: np.ndarray, ridge: float) -> tuple[float, np.ndarray]:
+    c = math.sqrt(float(np.sum(S * S)))
+    cp = c * (1.0 + ridge) * (1.0 + NS_MARGIN)
+    Y0 = (S + ridge * c * np.eye(S.shape[0])) / cp
+    return cp, Y0
+
+
+def ns_exact(S: np.ndarray, schedule, ridge: float = 0.0):
+    """What the K-step iteration computes in exact arithmetic:
+    P = Q diag(z_K(mu)) Q^T / sqrt(c'), root = Q diag(y_K(mu)) Q^T sqrt(c')."""
+    S = _sym(S)
+    cp, Y0 = _normaliser(S, ridge)
+    mu, Q = np.linalg.eigh(Y0)
+    y, z = ns_scalar_map(mu, schedule)
+    return (Q * z) @ Q.T / math.sqrt(cp), (Q * y) @ Q.T * math.sqrt(cp)
+
+
+def ns_matrix_float64(S: np.ndarray, schedule, ridge: float = 0.0):
+    """The coupled matrix iteration in plain float64 (no rounding, no scales):
+    T_k = a_k I + b_k Z_k Y_k; Y_{k+1} = Y_k T_k; Z_{k+1} = T_k Z_k."""
+    S = _sym(S)
+    d = S.shape[0]
+    cp, Y = _normaliser(S, ridge)
+    Z = np.eye(d)
+    for (a, b, _l, _u) in schedule:
+        T = a * np.eye(d) + b * (Z @ Y)
+        Y, Z = Y @ T, T @ Z
+    return Z / math.sqrt(cp), Y * math.sqrt(cp)
+
+
+# ------------------------------------------------ binary16 replay of the NS ---
+
+def f16(x) -> np.ndarray:
+    """Round to IEEE binary16, round-to-nearest-even, back to float64."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def split16(x) -> tuple[np.ndarray, np.ndarray]:
+    """hi = r16(x), lo = r16(x - hi): a pair of binary16 numbers whose sum
+    carries about 22 significant bits (used by the split precision mode)."""
+    hi = f16(x)
+    return hi, f16(np.asarray(x, dtype=np.float64) - hi)
+
+
+def _ns_consts(schedule, headroom=NS_HEADROOM):
+    z = ns_exponents(schedule)
+    return z, headroom, headroom, headroom
+
+
+def _prod(A, B, split: bool):
+    """A @ B for stored operands; in split mode A, B are (hi, lo) pairs and
+    the product keeps hi*hi + hi*lo + lo*hi (lo*lo is below the precision)."""
+    if not split:
+        return A @ B
+    return A[0] @ B[0] + A[0] @ B[1] + A[1] @ B[0]
+
+
+def ns_replay(S: np.ndarray, schedule, ridge: float = 0.0, rounding: bool = True,
+              trace: bool = False, split_iters: int = 0):
+    """Float64 replay of the coupled iteration as the GPU orders it, with every
+    GEMM operand rounded to binary16 (rounding=False keeps float64 operands).
+
+    Stored operands carry power-of-two scales (reading r9): Y^ = Y 2^h,
+    Z^ = Z 2^(h - z_k), T^ = T 2^h.  Order of operations (27 products for 10
+    steps, the count the README gives):
+      k = 0:      Y0^ = r(Y_0 2^h);  T0^ = r(2^h a_0 I + b_0 Y0^)   (M_0 = Y_0)
+                  Z1^ = r(T0^ 2^(-z_1));     Y1^ = r((Y0^ T0^) 2^-h)
+      k = 1..K-1: T^  = r(2^h a_k I + b_k 2^(z_k - 2h + h) (Z^ Y^))
+                  Y^' = r((Y^ T^) 2^-h)                  (not at k = K-1)
+                  Z^' = r((T^ Z^) 2^(z_k - z_{k+1} - h))
+      P = (T^_{K-1} Z^_{K-1}) 2^(z_{K-1} - 2h) / sqrt(c')
+    This is the standard coupled order (M = Z Y, Y <- Y T, Z <- T Z).  Other
+    orders that are equal in exact arithmetic (M = Y Z, Z <- Z T, mirroring a
+    triangle) diverge under binary16 rounding, so the GPU keeps this one.
+
+    split_iters > 0: the operands of iterations k < split_iters are (hi, lo)
+    binary16 pairs (``split16``) and each product is hi*hi + hi*lo + lo*hi.
+
+    Returns dict with P, P_hat (binary16 copy of Z_K^), pi (P ~ pi * P_hat),
+    c_prime and, if trace, the lists Y, Z, T of stored iterates (index k is
+    the operand of iteration k; Z[0] is None, Z_0 = I is never stored).
+    """
+    ident = (lambda x: np.asarray(x, dtype=np.float64))
+    r = f16 if rounding else ident
+
+    def rs(x, split):
+        if split and rounding:
+            return split16(x)
+        if split:
+            return (ident(x), np.zeros_like(x))
+        return r(x)
+
+    def val(x):
+        return x[0] + x[1] if isinstance(x, tuple) else x
+
+    S = _sym(S)
+    d = S.shape[0]
+    K = len(schedule)
+    z, h, _, _ = _ns_consts(schedule)
+    I = np.eye(d)
+    cp, Y0 = _normaliser(S, ridge)
+    Ys, Zs, Ts = [], [], []
+    sp = split_iters > 0
+    Yh = rs(Y0 * 2.0 ** h, sp)
+    a0, b0 = schedule[0][0], schedule[0][1]
+    Th = rs(2.0 ** h * a0 * I + b0 * val(Yh), sp)
+    sp1 = split_iters > 1
+    Zh = rs(val(Th) * 2.0 ** (-z[1]), sp1)
+    Ys.append(Yh); Zs.append(None); Ts.append(Th)
+    Yh = rs(_prod(Yh, Th, sp) * 2.0 ** -h, sp1)
+    Zacc = None
+    for k in range(1, K):
+        spk = split_iters > k
+        spn = split_iters > k + 1
+        a, b = schedule[k][0], schedule[k][1]
+        Ys.append(Yh); Zs.append(Zh)
+        Mfac = b * 2.0 ** (z[k] - h)
+        Th = rs(2.0 ** h * a * I + Mfac * _prod(Zh, Yh, spk), spk)
+        Ts.append(Th)
+        Zacc = _prod(Th, Zh, spk)
+        if k < K - 1:
+            Yh = rs(_prod(Yh, Th, spk) * 2.0 ** -h, spn)
+            Zh = rs(Zacc * 2.0 ** (z[k] - z[k + 1] - h), spn)
+    k = K - 1
+    P = Zacc * 2.0 ** (z[k] - 2 * h) / math.sqrt(cp)
+    P_hat = r(Zacc * 2.0 ** (z[k] - z[k + 1] - h))
+    pi = 2.0 ** (z[K] - h) / math.sqrt(cp)
+    out = {"P": P, "P_hat": P_hat, "pi": pi, "c_prime": cp}
+    if trace:
+        out.update(Y=Ys, Z=Zs, T=Ts)
+    return out
+
+
+def ns_replay_iteration(k: int, Yh: np.ndarray, Zh: np.ndarray, schedule,
+                        rounding: bool = True):
+    """One step k >= 1 of ``ns_replay`` (binary16 operands) from given stored
+    iterates (Y^_k, Z^_k): returns (T^_k, Y^_{k+1} or None, Z^_{k+1}).  Used
+    for the per-iteration teacher-forced comparison with the GPU iterates."""
+    r = f16 if rounding else (lambda x: np.asarray(x, dtype=np.float64))
+    K = len(schedule)
+    z, h, _, _ = _ns_consts(schedule)
+    d = Yh.shape[0]
+    a, b = schedule[k][0], schedule[k][1]
+    Th = r(2.0 ** h * a * np.eye(d) + b * 2.0 ** (z[k] - h) * (Zh @ Yh))
+    Zn = r((Th @ Zh) * 2.0 ** (z[k] - z[k + 1] - h))
+    Yn = r((Yh @ Th) * 2.0 ** -h) if k < K - 1 else None
+    return Th, Yn, Zn
+
+
+# ----------------------------------------------------------- the OKLS step ---
+
+def factor_ema(S_prev: np.ndarray, X: np.ndarray, beta2: float, count: int,
+               eps: float) -> np.ndarray:
+    """S <- beta2 S + (1-beta2)/count * X X^T + eps I  ('How it works').
+
+    Left factor: X = G P_b, count = n.  Right factor: X = (P_a G)^T, count = m.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    d = X.shape[0]
+    return beta2 * S_prev + (1.0 - beta2) / count * (X @ X.T) + eps * np.eye(d)
+
+
+def init_state(m: int, n: int, hp: Hyper) -> OklsState:
+    """M_0 = 0, S_0 = eps I (README: eps is added at factor initialisation),
+    P_0 = I (reading r1)."""
+    return OklsState(
+        M=np.zeros((m, n)),
+        Sa=hp.eps * np.eye(m), Sb=hp.eps * np.eye(n),
+        Pa=np.eye(m), Pb=np.eye(n), t=0)
+
+
+def okls_step(state: OklsState, W: np.ndarray, G: np.ndarray, lr: float,
+              hp: Hyper, root: str = "exact"):
+    """One OKLS step for one matrix in float64.  Returns (new_state, W_new, U).
+
+    root: "exact" (eigendecomposition), "ns_exact" (the K-step polynomial in
+    exact arithmetic) or "replay" (binary16 replay of the GPU iteration).
+    """
+    G = np.asarray(G, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    m, n = G.shape
+    t = state.t + 1
+    b1, b2 = hp.beta1, hp.beta2
+    # momentum, reading r4/r5
+    M = b1 * state.M + (1.0 - b1) * G
+    kappa = variance_correction(b1, t) if hp.variance_correction else 1.0
+    N = kappa * (b1 * M + (1.0 - b1) * G)
+    # factor EMAs with the previous roots (r3; 'How it works')
+    eps_upd = hp.eps if hp.eps_every_update else 0.0
+    Sa = factor_ema(state.Sa, G @ state.Pb, b2, n, eps_upd)
+    Sb = factor_ema(state.Sb, (state.Pa @ G).T, b2, m, eps_upd)
+    # fresh roots in the same step
+    if root == "exact":
+        Pa, Pb = inv_root_exact(Sa, hp.ridge), inv_root_exact(Sb, hp.ridge)
+    elif root == "ns_exact":
+        sch = cans_schedule(hp.ns_iters, hp.ns_lo)
+        Pa, Pb = ns_exact(Sa, sch, hp.ridge)[0], ns_exact(Sb, sch, hp.ridge)[0]
+    elif root == "replay":
+        sch = cans_schedule(hp.ns_iters, hp.ns_lo)
+        Pa = ns_replay(Sa, sch, hp.ridge)["P"]
+        Pb = ns_replay(Sb, sch, hp.ridge)["P"]
+    else:
+        raise ValueError(root)
+    # two-sided whitening and update, readings r6/r7
+    U = Pa @ N @ Pb
+    decay = adamc_decay(lr, hp.peak, hp.weight_decay)
+    W_new = W - decay * W - lr * c_shape(m, n) * U
+    return OklsState(M=M, Sa=Sa, Sb=Sb, Pa=Pa, Pb=Pb, t=t), W_new, U
+
+
+def okls_run(W0: np.ndarray, grads, hp: Hyper, lrs=None, root: str = "exact"):
+    """Free-running OKLS over a gradient sequence; returns (state, W, Us)."""
+    m, n = np.asarray(W0).shape
+    st = init_state(m, n, hp)
+    W = np.asarray(W0, dtype=np.float64)
+    Us = []
+    for i, G in enumerate(grads):
+        lr = hp.lr if lrs is None else lrs[i]
+        st, W, U = okls_step(st, W, G, lr, hp, root=root)
+        Us.append(U)
+    return st, W, Us
+
+
+def rel_fro(A: np.ndarray, B: np.ndarray) -> float:
+    """||A - B||_F / ||B||_F."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    nb = float(np.linalg.norm(B))
+    return float(np.linalg.norm(A - B)) / (nb if nb > 0 else 1.0)

@@ -1,0 +1,341 @@
+"""Pins of the float64 oracle against what the pages and mathematics fix.
+
+Each test targets a mistake that would otherwise go unnoticed in the oracle
+(a dropped term, a transposed operand, a wrong exponent or sign); none of them
+re-types the function it checks.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "shampoo_hand_example.json")
+
+
+@pytest.fixture(scope="module")
+def hand():
+    with open(GOLD) as f:
+        return json.load(f)
+
+
+def _sv(X):
+    return np.sort(np.linalg.svd(np.asarray(X, dtype=np.float64), compute_uv=False))[::-1]
+
+
+# --------------------------------------------------------------- hand example
+
+def test_hand_example_factors(hand):
+    """L = G G^T printed on the page; the factor EMA with beta2 = 0, P = I,
+    eps = 0 must give n S_a = G G^T and m S_b = G^T G."""
+    G = np.array(hand["G"], dtype=np.float64)
+    m, n = G.shape
+    Sa = O.factor_ema(np.zeros((m, m)), G @ np.eye(n), 0.0, n, 0.0)
+    Sb = O.factor_ema(np.zeros((n, n)), (np.eye(m) @ G).T, 0.0, m, 0.0)
+    assert np.array_equal(n * Sa, np.array(hand["L_equals_GGt"], dtype=np.float64))
+    # G^T G of the page's G, entry by entry
+    assert np.allclose(m * Sb, [[10, 2, 3], [2, 4, 0], [3, 0, 1]], atol=1e-12)
+    assert np.allclose(_sv(G), hand["singular_values_G"], atol=hand["printed_precision"])
+
+
+@pytest.mark.parametrize("acc,key", [(1, "shampoo_quarter_root_step_singular_values"),
+                                     (4, "shampoo_quarter_root_after_4_accumulations"),
+                                     (100, "shampoo_quarter_root_after_100_accumulations")])
+def test_hand_example_quarter_root(hand, acc, key):
+    """sigma(L^-1/4 G R^-1/4) = 1, 1 for one gradient, 0.5 after four identical
+    accumulations and 0.1 after a hundred (R is rank 2: pseudo-inverse)."""
+    G = np.array(hand["G"], dtype=np.float64)
+    L, R = acc * (G @ G.T), acc * (G.T @ G)
+    step = O.sym_power(L, -0.25, rcond=1e-12) @ G @ O.sym_power(R, -0.25, rcond=1e-12)
+    assert np.allclose(_sv(step)[:2], hand[key], atol=hand["printed_precision"])
+
+
+def test_problem14_half_roots(hand):
+    """Problem 14: with -1/2 on both sides the step's singular values are
+    0.527 / 0.296, and 0.0527 / 0.0296 for 10 G; with -1/4, 10 G keeps 1, 1."""
+    G = np.array(hand["G"], dtype=np.float64)
+    tol = hand["printed_precision"]
+    for c, key in [(1.0, "problem14_half_root_G"), (10.0, "problem14_half_root_10G")]:
+        Gc = c * G
+        L, R = Gc @ Gc.T, Gc.T @ Gc
+        step = O.inv_root_exact(L) @ Gc @ O.sym_power(R, -0.5, rcond=1e-12)
+        want = np.array(hand[key])
+        assert np.allclose(_sv(step)[:2], want, rtol=tol / want.min() * 0.6)
+    G10 = 10 * G
+    step = (O.sym_power(G10 @ G10.T, -0.25) @ G10
+            @ O.sym_power(G10.T @ G10, -0.25, rcond=1e-12))
+    assert np.allclose(_sv(step)[:2], hand["problem14_quarter_root_10G"], atol=tol)
+
+
+def test_eps_regularised_rank_deficient_right_factor(hand):
+    """With +eps I instead of a pseudo-inverse, G annihilates R's null
+    direction, so the -1/2 step keeps Problem 14's singular values."""
+    G = np.array(hand["G"], dtype=np.float64)
+    R = G.T @ G + 1e-9 * np.eye(3)
+    step = O.inv_root_exact(G @ G.T) @ G @ O.inv_root_exact(R)
+    assert np.allclose(_sv(step)[:2], [0.527, 0.296], atol=1e-3)
+
+
+# --------------------------------------------------------------- schedule
+
+def test_schedule_textbook_special_case():
+    """On [1, 1] the minimax cubic is the textbook Newton-Schulz step."""
+    (a, b, _l, _u), = O.cans_schedule(1, lo=1.0, hi=1.0)
+    assert abs(a - 1.5) < 1e-15 and abs(b + 0.5) < 1e-15
+
+
+def test_schedule_is_minimax_by_brute_force():
+    """For each step, no (a, b) on a fine grid around the schedule's pair has
+    a smaller worst error max|1 - q(s)| on [l, u], and the error
+    equioscillates at l, s* and u."""
+    sch = O.cans_schedule(10, 1e-3)
+    for (a, b, l, u) in sch[:6]:
+        s = np.concatenate([np.linspace(l, u, 20001), np.geomspace(l, u, 20001)])
+        err = lambda A, B: np.max(np.abs(1 - (A * s + B * s ** 3)))  # noqa: E731
+        e0 = err(a, b)
+        for da in np.linspace(-0.02, 0.02, 21):
+            for db in np.linspace(-0.02, 0.02, 21):
+                if da == 0 and db == 0:
+                    continue
+                assert err(a * (1 + da), b * (1 + db)) >= e0 - 1e-12
+        s_star = math.sqrt(-a / (3 * b))
+        e_l, e_s, e_u = 1 - (a * l + b * l ** 3), 1 - (a * s_star + b * s_star ** 3), \
+            1 - (a * u + b * u ** 3)
+        assert abs(e_l - e_u) < 1e-9 and abs(e_l + e_s) < 1e-9
+
+
+def test_schedule_convergence_window():
+    """After ten steps from [1e-3, 1] every sqrt-eigenvalue lies within 1e-5
+    of 1 (scalar map checked on a dense grid, independent of the interval
+    bookkeeping)."""
+    sch = O.cans_schedule(10, 1e-3)
+    s = np.geomspace(1e-3, 1.0, 200001)
+    mu = s ** 2
+    y, z = O.ns_scalar_map(mu, sch)
+    assert np.max(np.abs(np.sqrt(y * z) - 1)) < 1e-5
+    # z converges to mu^-1/2 with the same relative error
+    assert np.max(np.abs(z * np.sqrt(mu) - 1)) < 1e-5
+
+
+def test_scale_exponents_bound_z():
+    """Entries of Z_k of the float64 iteration never exceed 2**z_k."""
+    rng = np.random.default_rng(3)
+    sch = O.cans_schedule(10, 1e-3)
+    z = O.ns_exponents(sch)
+    d = 24
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    S = (Q * np.geomspace(1e-6, 1, d)) @ Q.T
+    cp = np.linalg.norm(S) * (1 + O.NS_MARGIN)
+    Y, Z = S / cp, np.eye(d)
+    for k, (a, b, _l, _u) in enumerate(sch):
+        assert np.max(np.abs(Z)) <= 2.0 ** z[k]
+        T = a * np.eye(d) + b * Z @ Y
+        Y, Z = Y @ T, T @ Z
+    assert np.max(np.abs(Z)) <= 2.0 ** z[len(sch)]
+
+
+# --------------------------------------------------------------- NS chain
+
+def _spd(d, cond, seed):
+    rng = np.random.default_rng(seed)
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    w = np.geomspace(1.0, cond, d)
+    return (Q * w) @ Q.T
+
+
+def test_matrix_iteration_equals_scalar_polynomial():
+    """Coupled matrix iteration (float64) = eigen-wise scalar recursion."""
+    S = _spd(40, 1e3, 1)
+    sch = O.cans_schedule(10, 1e-3)
+    P1, R1 = O.ns_matrix_float64(S, sch)
+    P2, R2 = O.ns_exact(S, sch)
+    assert O.rel_fro(P1, P2) < 1e-10 and O.rel_fro(R1, R2) < 1e-10
+
+
+def test_ns_reaches_exact_root_within_schedule_bound():
+    """For spectra inside the converging window the 10-step result equals
+    S^-1/2 and S^1/2 (eigendecomposition) within the schedule's error."""
+    sch = O.cans_schedule(10, 1e-3)
+    for cond in [1.0, 1e2, 1e4]:
+        S = _spd(32, cond, 2)
+        P, R = O.ns_exact(S, sch)
+        assert O.rel_fro(P, O.inv_root_exact(S)) < 2e-5
+        assert O.rel_fro(R, O.sym_power(S, 0.5)) < 2e-5
+        assert np.allclose(P @ S @ P, np.eye(32), atol=5e-5)
+
+
+def test_ridge_is_root_of_shifted_matrix():
+    S = _spd(20, 1e5, 4)
+    rho = 1e-3
+    c = np.linalg.norm(S)
+    want = O.sym_power(S + rho * c * np.eye(20), -0.5)
+    assert O.rel_fro(O.inv_root_exact(S, rho), want) < 1e-12
+    assert O.rel_fro(O.ns_exact(S, O.cans_schedule(10, 1e-3), rho)[0], want) < 2e-5
+
+
+def test_replay_without_rounding_is_the_float64_iteration():
+    S = _spd(48, 1e3, 5)
+    sch = O.cans_schedule(10, 1e-3)
+    r = O.ns_replay(S, sch, rounding=False)
+    assert O.rel_fro(r["P"], O.ns_matrix_float64(S, sch)[0]) < 1e-11
+    assert O.rel_fro(r["pi"] * r["P_hat"], r["P"]) < 1e-12
+    rs = O.ns_replay(S, sch, rounding=False, split_iters=4)
+    assert O.rel_fro(rs["P"], r["P"]) < 1e-11
+
+
+def test_replay_with_binary16_rounding_is_accurate_when_well_conditioned():
+    sch = O.cans_schedule(10, 1e-3)
+    S = _spd(64, 10.0, 6)
+    r = O.ns_replay(S, sch)
+    assert 1e-6 < O.rel_fro(r["P"], O.inv_root_exact(S)) < 5e-3
+    # the split mode cuts the error of an ill-conditioned factor
+    S4 = _spd(64, 1e4, 7)
+    e0 = O.rel_fro(O.ns_replay(S4, sch)["P"], O.inv_root_exact(S4))
+    e3 = O.rel_fro(O.ns_replay(S4, sch, split_iters=3)["P"], O.inv_root_exact(S4))
+    assert e3 < 1e-2 and e3 < 0.5 * e0
+
+
+def test_replay_iteration_matches_trace():
+    sch = O.cans_schedule(10, 1e-3)
+    S = _spd(32, 1e2, 8)
+    r = O.ns_replay(S, sch, trace=True)
+    for k in range(1, 10):
+        T, Yn, Zn = O.ns_replay_iteration(k, r["Y"][k], r["Z"][k], sch)
+        assert np.array_equal(T, r["T"][k])
+        if k < 9:
+            assert np.array_equal(Yn, r["Y"][k + 1]) and np.array_equal(Zn, r["Z"][k + 1])
+        else:
+            assert np.array_equal(Zn, r["P_hat"])
+
+
+def test_binary16_rounding_is_round_to_nearest_even():
+    one = 1.0
+    assert O.f16(one + 2 ** -11) == 1.0                      # tie -> even
+    assert O.f16(one + 3 * 2 ** -11) == one + 2 ** -9        # tie -> even
+    assert O.f16(one + 2 ** -11 + 2 ** -40) == one + 2 ** -10  # no double rounding
+    assert O.f16(65519.0) == 65504.0 and np.isinf(O.f16(65520.0))
+    assert O.f16(2 ** -25) == 0.0 and O.f16(3 * 2 ** -25) == 2 ** -23  # subnormals
+    # at the operands' headroom scale (2**12) the low half stays normal and
+    # the pair carries ~22 bits
+    x = np.random.default_rng(0).standard_normal(1000) * 2.0 ** 12
+    x = x[np.abs(x) > 1.0]
+    hi, lo = O.split16(x)
+    assert np.max(np.abs(hi + lo - x) / np.abs(x)) < 2 ** -21
+
+
+# --------------------------------------------------------------- step pieces
+
+def test_factor_ema_brute_force_loops():
+    """Element-by-element sums on tiny inputs, including non-identity roots."""
+    rng = np.random.default_rng(9)
+    m, n = 4, 3
+    G = rng.standard_normal((m, n))
+    Pa = _spd(m, 5.0, 10)
+    Pb = _spd(n, 3.0, 11)
+    Sa0, Sb0 = _spd(m, 2.0, 12), _spd(n, 2.0, 13)
+    b2, eps = 0.7, 1e-3
+    Sa = np.zeros((m, m))
+    for i in range(m):
+        for j in range(m):
+            acc = 0.0
+            for k in range(n):
+                xi = sum(G[i, l] * Pb[l, k] for l in range(n))
+                xj = sum(G[j, l] * Pb[l, k] for l in range(n))
+                acc += xi * xj
+            Sa[i, j] = b2 * Sa0[i, j] + (1 - b2) / n * acc + (eps if i == j else 0.0)
+    Sb = np.zeros((n, n))
+    for i in range(n):
+        for j in range(n):
+            acc = 0.0
+            for k in range(m):
+                xi = sum(Pa[k, l] * G[l, i] for l in range(m))
+                xj = sum(Pa[k, l] * G[l, j] for l in range(m))
+                acc += xi * xj
+            Sb[i, j] = b2 * Sb0[i, j] + (1 - b2) / m * acc + (eps if i == j else 0.0)
+    assert np.allclose(O.factor_ema(Sa0, G @ Pb, b2, n, eps), Sa, atol=1e-12)
+    assert np.allclose(O.factor_ema(Sb0, (Pa @ G).T, b2, m, eps), Sb, atol=1e-12)
+
+
+def test_c_shape_closed_forms():
+    assert abs(O.c_shape(16, 16) - 1 / (2 * 4)) < 1e-15
+    assert abs(O.c_shape(4, 1) - 2 / 3) < 1e-15
+    assert abs(O.c_shape(1, 4) - (0.5 / 3)) < 1e-15
+
+
+def test_variance_correction_monte_carlo():
+    """N_t * kappa_t has unit variance for iid unit gradients (the reading's
+    definition), checked by simulation, not by the closed form."""
+    rng = np.random.default_rng(14)
+    b1 = 0.9684
+    trials, T = 200000, 12
+    M = np.zeros(trials)
+    for t in range(1, T + 1):
+        g = rng.standard_normal(trials)
+        M = b1 * M + (1 - b1) * g
+        N = b1 * M + (1 - b1) * g
+        std = np.std(N * O.variance_correction(b1, t))
+        assert abs(std - 1) < 0.01
+    assert O.variance_correction(0.0, 5) == 1.0
+
+
+def test_hyperparameter_defaults_are_the_readme_table():
+    hp = O.Hyper()
+    assert (hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay) == \
+        (0.09434, 0.9684, 0.9482, 1e-9, 0.0303)
+    assert hp.ns_iters == 10
+
+
+def test_weight_decay_closed_form_with_zero_gradients():
+    """G = 0: U = 0, so W_t = W_0 prod_t (1 - lr_t^2 wd / lr_peak)."""
+    hp = O.Hyper(lr=0.1)
+    rng = np.random.default_rng(15)
+    W0 = rng.standard_normal((6, 5))
+    lrs = [0.1, 0.05, 0.08, 0.1]
+    _st, W, Us = O.okls_run(W0, [np.zeros((6, 5))] * 4, hp, lrs=lrs)
+    f = np.prod([1 - l * l * hp.weight_decay / 0.1 for l in lrs])
+    assert np.allclose(W, W0 * f, atol=1e-14)
+    assert all(np.all(U == 0) for U in Us)
+
+
+def test_first_step_is_a_descent_direction():
+    """<W_1 - (1 - decay) W_0, G> < 0: the update moves against G."""
+    hp = O.Hyper()
+    rng = np.random.default_rng(16)
+    G = rng.standard_normal((7, 5))
+    W0 = rng.standard_normal((7, 5))
+    _st, W1, _U = O.okls_step(O.init_state(7, 5, hp), W0, G, hp.lr, hp)
+    decay = O.adamc_decay(hp.lr, hp.peak, hp.weight_decay)
+    assert np.sum((W1 - (1 - decay) * W0) * G) < 0
+
+
+@pytest.mark.parametrize("beta2,steps", [(0.5, 300), (0.9482, 1500)])
+def test_square_fixed_gradient_reaches_scaled_polar_factor(beta2, steps):
+    """Fed one square G forever, the KL factors reach a fixed point where
+    P_a G P_b = sqrt(n) U V^T (G = U Sigma V^T).  A transposed operand, a
+    swapped side or a wrong 1/n breaks this limit."""
+    rng = np.random.default_rng(17)
+    n = 12
+    G = rng.standard_normal((n, n))
+    hp = O.Hyper(beta1=0.0, beta2=beta2, eps=0.0, lr=0.0, lr_peak=1.0)
+    st = O.init_state(n, n, hp)
+    st.Sa, st.Sb = np.eye(n) * 1e-3, np.eye(n) * 1e-3
+    W = np.zeros((n, n))
+    for _ in range(steps):
+        st, W, U = O.okls_step(st, W, G, 0.0, hp)
+    u, _s, vt = np.linalg.svd(G)
+    assert O.rel_fro(st.Pa @ G @ st.Pb, math.sqrt(n) * (u @ vt)) < 1e-8
+    assert O.rel_fro(U, math.sqrt(n) * (u @ vt)) < 1e-8
+
+
+def test_step_root_modes_agree_on_a_benign_case():
+    rng = np.random.default_rng(18)
+    hp = O.Hyper()
+    G = [rng.standard_normal((24, 16)) for _ in range(4)]
+    W0 = rng.standard_normal((24, 16)) * 0.01
+    _s1, W1, U1 = O.okls_run(W0, G, hp, root="exact")
+    _s2, W2, U2 = O.okls_run(W0, G, hp, root="ns_exact")
+    assert O.rel_fro(U2[0], U1[0]) < 1e-3
