@@ -71,7 +71,7 @@ typedef enum okls_state_part {
  * Hyperparameters of one same-shape batch.  Defaults (okls_config_default)
  * are those of the README's "Hyperparameters" table: lr 0.09434 (also
  * lr_peak), beta1 0.9684, beta2 0.9482, eps 1e-9, weight_decay 0.0303, and
- * 10 Newton-Schulz iterations.
+ * 10 Newton-Schulz iterations with plain binary16 operands and ridge 1e-3.
  *
  *   ns_split_iters  0: every Newton-Schulz GEMM takes plain binary16 operands
  *                   (27 GEMMs, the README's design).  s > 0: iterations
@@ -81,7 +81,13 @@ typedef enum okls_state_part {
  *   ns_lo           lower end l_0 of the sqrt-eigenvalue interval the
  *                   coefficient schedule is optimised for (default 1e-3:
  *                   eigenvalues down to 1e-6 ||S||_F converge).
- *   ridge           rho >= 0: the root is taken of S + rho ||S||_F I.
+ *   ridge           rho >= 0: the root is taken of S + rho ||S||_F I
+ *                   (default 1e-3).  Binary16 rounding of Y_0 = S/||S||_F
+ *                   perturbs eigenvalues by ~2^-12; without a ridge above
+ *                   that floor, rank-deficient factors (every m != n matrix
+ *                   at its first step) get negative eigenvalues that the
+ *                   cubic drives to overflow.  With ns_split_iters = 3 a
+ *                   ridge of 1e-4 suffices.
  *   variance_correction  1: N_t is divided by its standard deviation under
  *                   iid unit-variance gradients; 0: plain Nesterov.
  *   eps_every_update 1: +eps I in every factor update (and S_0 = eps I);
@@ -128,11 +134,11 @@ okls_status okls_state_bytes(const okls_config *cfg, size_t *state_bytes,
 
 /*
  * Bind a handle to caller-owned device memory.  Validates cfg, builds the TMA
- * descriptors and the launch plan on the host, and uploads them with one
- * synchronous cudaMemcpy; allocates no device memory of its own except the
- * small descriptor table (freed by okls_destroy).  The state is NOT
- * initialised: call okls_reset_state (or okls_set_state for every part).
- * The current CUDA device must be the one that owns the buffers.
+ * descriptors on the host and uploads them with one synchronous cudaMemcpy
+ * into the head of the workspace; allocates no device memory.  The state is
+ * NOT initialised: call okls_reset_state (or okls_set_state for every part).
+ * The current CUDA device must be the one that owns the buffers, and it must
+ * be an sm_103 GPU (OKLS_ERR_NO_DEVICE otherwise).
  */
 okls_status okls_create(const okls_config *cfg, void *state_dev,
                         size_t state_bytes, void *workspace_dev,
@@ -176,8 +182,9 @@ okls_status okls_set_state(okls_handle h, int32_t part, const void *src_dev,
 okls_status okls_get_step(okls_handle h, int64_t *t);
 okls_status okls_set_step(okls_handle h, int64_t t);
 
-/* Release the handle and its descriptor table (not the caller's buffers).
- * Synchronises the device first.  NULL is accepted. */
+/* Release the handle (its descriptor table lives in the caller's workspace,
+ * so nothing on the device is freed).  The caller must not free state or
+ * workspace while work of this handle is still queued.  NULL is accepted. */
 okls_status okls_destroy(okls_handle h);
 
 /*
@@ -197,9 +204,11 @@ okls_status okls_ns_schedule(int32_t iters, double lo, double *a, double *b,
  *   P_dev     out, count x d x d fp32: S^(-1/2).
  *   root_dev  optional out (NULL to skip), count x d x d fp32: S^(1/2) (one
  *             extra GEMM per iteration-9 factor).
- *   trace_dev optional out (NULL to skip), binary16, count x (3*iters+1) x d
- *             x d: for k = 0..iters-1 the stored iterates Y^_k, Z^_k, T^_k (Z^_0
- *             is written as zeros), then Z^_iters; row-major, unpadded.
+ *   trace_dev optional out (NULL to skip), binary16, (3*iters+1) x count x d
+ *             x d: slice 3k, 3k+1, 3k+2 holds the stored iterates Y^_k, Z^_k,
+ *             T^_k of iteration k (Z^_0 = I is written as zeros), slice
+ *             3*iters holds Z^_iters; row-major, unpadded.  In split mode the
+ *             slices hold the high halves.
  *   workspace_dev / workspace_bytes: from okls_inv_root_workspace_bytes.
  * Asynchronous on `stream`; errors of the device status word are reported by
  * the returned status only after an explicit synchronisation, so the call

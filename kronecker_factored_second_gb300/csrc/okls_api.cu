@@ -1,0 +1,966 @@
+// C ABI of the OKLS step: validation, workspace planning, TMA descriptors and
+// the launch sequence of one step (see include/okls.h for the contract).
+//
+// Step (page "Online KL Shampoo", "How it works"), per same-shape batch:
+//   1. momentum statistics          k_momentum_stats, k_coeffs_pre
+//   2. M_t, Ghat, Ghat^T, Nhat^T    k_pack
+//   3. X_b = G P_b, X_a^T = G^T P_a^T             GEMM (EPI_X16)
+//   4. S_a, S_b EMAs (+ ||S||_F^2)                 GEMM (EPI_SYRK, upper tiles)
+//   5. normalisers, Y_0, T_0, Z_1                  k_coeffs_post, k_normalise
+//   6. coupled Newton-Schulz, both factors         19 GEMM launches, 27 products
+//   7. Q = P_a N                                    GEMM (EPI_X16)
+//   8. U = Q P_b and the parameter update          GEMM (EPI_UPDATE)
+#include <cudaTypedefs.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/okls.h"
+#include "okls_internal.h"
+#include "okls_kernels.h"
+
+using namespace okls;
+
+namespace {
+
+thread_local std::string g_err;
+
+okls_status fail(okls_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+#define OKLS_CK(call)                                                                   \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(OKLS_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                  __FILE__, __LINE__);                                                  \
+  } while (0)
+
+// ------------------------------------------------------------------ schedule
+// Minimax odd cubic q(s) = a s + b s^3 of 1 on [l, u] (equioscillation at l,
+// sqrt(D/3), u with D = u^2 + u l + l^2), next interval [q(l), q(sqrt(D/3))];
+// exponents z_k = ceil(log2(prod_{j<k} a_j)).
+struct Sched {
+  int iters = 0;
+  std::vector<double> a, b;
+  std::vector<int> z;
+};
+
+Sched make_schedule(int iters, double lo) {
+  Sched s;
+  s.iters = iters;
+  double l = lo, u = 1.0, prod = 1.0;
+  s.z.push_back(0);
+  for (int k = 0; k < iters; ++k) {
+    const double D = u * u + u * l + l * l;
+    const double a = 2.0 / (l * u * (u + l) / D + (2.0 / 3.0) * std::sqrt(D / 3.0));
+    const double b = -a / D;
+    s.a.push_back(a);
+    s.b.push_back(b);
+    prod *= a;
+    s.z.push_back(static_cast<int>(std::ceil(std::log2(prod))));
+    const double ss = std::sqrt(D / 3.0);
+    const double nl = a * l + b * l * l * l, nu = a * ss + b * ss * ss * ss;
+    l = nl;
+    u = nu;
+  }
+  return s;
+}
+
+// variance of the Nesterov combination for iid unit-variance gradients:
+// v_t = (1-b)^2 [ (1+b)^2 + sum_{k=2}^{t} b^{2k} ]; kappa = v_t^-1/2
+double variance_kappa(double b, int64_t t) {
+  const double b2 = b * b;
+  double tail = 0.0;
+  if (t >= 2) tail = (b2 < 1.0) ? b2 * b2 * (1.0 - std::pow(b2, static_cast<double>(t - 1))) / (1.0 - b2) : 0.0;
+  const double v = (1.0 - b) * (1.0 - b) * ((1.0 + b) * (1.0 + b) + tail);
+  return 1.0 / std::sqrt(v);
+}
+
+// ------------------------------------------------------------ TMA encoding
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxMaps = 128;
+constexpr size_t kMapTableBytes = kMaxMaps * sizeof(CUtensorMap);
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// A batch of binary16 matrices (rows x cols, row pitch ld) with two TMA
+// descriptors: box 128 rows (A operand) and box 256 rows (B operand).
+struct Buf {
+  __half* p = nullptr;
+  int64_t rows = 0, cols = 0, ld = 0, batch = 0;
+  int mapA = -1, mapB = -1;
+  int64_t mat() const { return rows * ld; }
+};
+
+struct Planner {
+  uint8_t* base = nullptr;  // null: sizing pass
+  size_t off = 0;
+  std::vector<CUtensorMap> maps;
+  okls_status err = OKLS_OK;
+
+  void* take(size_t bytes, size_t align = 256) {
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off), static_cast<int64_t>(align)));
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+
+  int make_map(void* ptr, int64_t rows, int64_t cols, int64_t ld, int64_t batch, int box_rows) {
+    if (!base) return 0;
+    if (static_cast<int>(maps.size()) >= kMaxMaps) {
+      err = fail(OKLS_ERR_UNSUPPORTED, "descriptor table full");
+      return -1;
+    }
+    auto fn = encode_fn();
+    if (!fn) {
+      err = fail(OKLS_ERR_NO_DEVICE, "cuTensorMapEncodeTiled unavailable");
+      return -1;
+    }
+    CUtensorMap m;
+    memset(&m, 0, sizeof(m));
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(rows * ld * 2)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, ptr, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      err = fail(OKLS_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d) rows=%lld cols=%lld ld=%lld",
+                 static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols),
+                 static_cast<long long>(ld));
+      return -1;
+    }
+    maps.push_back(m);
+    return static_cast<int>(maps.size()) - 1;
+  }
+
+  Buf buf16(int64_t rows, int64_t cols, int64_t batch) {
+    Buf b;
+    b.rows = rows;
+    b.cols = cols;
+    b.ld = round_up(cols, 8);
+    b.batch = batch;
+    b.p = static_cast<__half*>(take(static_cast<size_t>(b.mat() * batch * 2)));
+    b.mapA = make_map(b.p, rows, cols, b.ld, batch, kBM);
+    b.mapB = make_map(b.p, rows, cols, b.ld, batch, kBN);
+    return b;
+  }
+};
+
+// One Newton-Schulz factor (a batch of d x d matrices).
+struct Factor {
+  int d = 0;
+  int batch = 0;
+  float* S = nullptr;       // fp32 input
+  float* P32 = nullptr;     // fp32 output
+  float* root32 = nullptr;  // debug root output
+  Buf Ph[2], PhT[2];                                      // binary16 P (hi, lo)
+  Buf Y[2][2], YT[2][2], Z[2][2], ZT[2][2], T[2], TT[2];  // [ping-pong][hi, lo]
+  bool split = false;
+  int slot_sumsq = 0, slot_cprime = 0, slot_pi = 0, slot_pscale = 0, slot_rscale = 0;
+};
+
+void plan_factor(Planner& pl, Factor& f, int d, int batch, bool split) {
+  f.d = d;
+  f.batch = batch;
+  f.split = split;
+  const int nl = split ? 2 : 1;
+  for (int l = 0; l < nl; ++l) {
+    f.Ph[l] = pl.buf16(d, d, batch);
+    f.PhT[l] = pl.buf16(d, d, batch);
+  }
+  for (int pp = 0; pp < 2; ++pp)
+    for (int l = 0; l < nl; ++l) {
+      f.Y[pp][l] = pl.buf16(d, d, batch);
+      f.YT[pp][l] = pl.buf16(d, d, batch);
+      f.Z[pp][l] = pl.buf16(d, d, batch);
+      f.ZT[pp][l] = pl.buf16(d, d, batch);
+    }
+  for (int l = 0; l < nl; ++l) {
+    f.T[l] = pl.buf16(d, d, batch);
+    f.TT[l] = pl.buf16(d, d, batch);
+  }
+}
+
+int g_num_sms[64] = {0};
+
+okls_status device_sms(int* out) {
+  int dev = 0;
+  OKLS_CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(OKLS_ERR_NO_DEVICE, "device index %d", dev);
+  if (g_num_sms[dev] == 0) {
+    int major = 0, minor = 0, sms = 0;
+    OKLS_CK(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    OKLS_CK(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    OKLS_CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (major != 10 || minor != 3)
+      return fail(OKLS_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, major,
+                  minor);
+    g_num_sms[dev] = sms;
+  }
+  *out = g_num_sms[dev];
+  return OKLS_OK;
+}
+
+// ------------------------------------------------------------ GEMM launches
+// Output buffers must cover the problem's rows x cols (and cols x rows for the
+// transposed copy, which shares the pitch); a violation is a planning bug.
+thread_local bool g_plan_error = false;
+
+struct LaunchBuilder {
+  GemmLaunch L;
+  LaunchBuilder() { memset(&L, 0, sizeof(L)); }
+
+  // D = sum over segments of A_seg * B_seg^T; split: (hi,hi), (hi,lo), (lo,hi)
+  GemmProblem& add(const Buf* A, const Buf* B, bool split, int rows, int cols, int K, int batch, int epi,
+                   bool sym) {
+    GemmProblem& p = L.prob[L.nprob++];
+    memset(&p, 0, sizeof(p));
+    p.nseg = split ? 3 : 1;
+    p.amap[0] = A[0].mapA;
+    p.bmap[0] = B[0].mapB;
+    if (split) {
+      p.amap[1] = A[0].mapA;
+      p.bmap[1] = B[1].mapB;
+      p.amap[2] = A[1].mapA;
+      p.bmap[2] = B[0].mapB;
+    }
+    p.rows = rows;
+    p.cols = cols;
+    p.K = K;
+    p.batch = batch;
+    p.tiles_m = (rows + kBM - 1) / kBM;
+    p.tiles_n = (cols + kBN - 1) / kBN;
+    p.sym = sym ? 1 : 0;
+    p.epi = epi;
+    if (sym) {
+      int64_t cnt = 0;
+      for (int tm = 0; tm < p.tiles_m; ++tm) cnt += p.tiles_n - tm / 2;
+      p.tiles_per_mat = cnt;
+    } else {
+      p.tiles_per_mat = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    }
+    return p;
+  }
+
+  // D = A * (B_hi + B_lo)^T: two K segments when `split`, else one
+  GemmProblem& add_bsplit(const Buf& A, const Buf* B, bool split, int rows, int cols, int K, int batch,
+                          int epi) {
+    GemmProblem& p = add(&A, B, false, rows, cols, K, batch, epi, false);
+    if (split) {
+      p.nseg = 2;
+      p.amap[1] = A.mapA;
+      p.bmap[1] = B[1].mapB;
+    }
+    return p;
+  }
+
+  // D = (A_hi + A_lo) * B^T
+  GemmProblem& add_asplit(const Buf* A, const Buf& B, bool split, int rows, int cols, int K, int batch,
+                          int epi) {
+    GemmProblem& p = add(A, &B, false, rows, cols, K, batch, epi, false);
+    if (split) {
+      p.nseg = 2;
+      p.amap[1] = A[1].mapA;
+      p.bmap[1] = B.mapB;
+    }
+    return p;
+  }
+
+  okls_status go(const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st) {
+    if (g_plan_error) {
+      g_plan_error = false;
+      return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: output buffer smaller than a GEMM problem");
+    }
+    for (int i = 0; i < L.nprob; ++i) {
+      const GemmProblem& p = L.prob[i];
+      if ((p.epi == EPI_SYRK || p.epi == EPI_NS_LAST || p.epi == EPI_ROOT) && (p.out32 == nullptr || p.ld32 < p.cols))
+        return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: fp32 output");
+      if (p.epi == EPI_UPDATE && (p.w == nullptr || p.ld32 < p.cols || p.mat32 < static_cast<int64_t>(p.rows) * p.ld32))
+        return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: parameter output");
+    }
+    // longest K first so the expensive tiles start in the first wave
+    std::stable_sort(L.prob, L.prob + L.nprob, [](const GemmProblem& x, const GemmProblem& y) {
+      return static_cast<int64_t>(x.K) * x.nseg > static_cast<int64_t>(y.K) * y.nseg;
+    });
+    int64_t t = 0;
+    for (int i = 0; i < L.nprob; ++i) {
+      L.prob[i].tile_begin = t;
+      t += L.prob[i].tiles_per_mat * L.prob[i].batch;
+    }
+    L.total_tiles = t;
+    L.maps = maps;
+    L.status = status;
+    OKLS_CK(launch_gemm(L, sms, st));
+    return OKLS_OK;
+  }
+};
+
+
+void check_out(const Buf& b, int64_t rows, int64_t cols, int64_t batch, int64_t ld) {
+  if (b.rows < rows || b.cols < cols || b.batch < batch || b.ld != ld || b.p == nullptr) g_plan_error = true;
+}
+
+void set_out16(GemmProblem& p, const Buf& hi, const Buf* hiT, const Buf* lo, const Buf* loT) {
+  check_out(hi, p.rows, p.cols, p.batch, hi.ld);
+  if (hiT) check_out(*hiT, p.cols, p.rows, p.batch, hi.ld);
+  if (lo) check_out(*lo, p.rows, p.cols, p.batch, hi.ld);
+  if (loT) check_out(*loT, p.cols, p.rows, p.batch, hi.ld);
+  p.out_hi = hi.p;
+  p.out_hi_t = hiT ? hiT->p : nullptr;
+  p.out_lo = lo ? lo->p : nullptr;
+  p.out_lo_t = loT ? loT->p : nullptr;
+  p.ld16 = hi.ld;
+  p.mat16 = hi.mat();
+  p.split_out = lo ? 1 : 0;
+}
+
+struct TraceOut {
+  uint16_t* base = nullptr;  // [(3K+1)][count][d][d]
+  int64_t count = 0, d = 0;
+};
+
+okls_status trace_copy(const TraceOut& tr, int slice, const Buf* b, cudaStream_t st) {
+  if (!tr.base) return OKLS_OK;
+  const int64_t dd = tr.d * tr.d;
+  uint16_t* dst = tr.base + static_cast<int64_t>(slice) * tr.count * dd;
+  if (!b) {
+    OKLS_CK(cudaMemsetAsync(dst, 0, static_cast<size_t>(tr.count * dd * 2), st));
+    return OKLS_OK;
+  }
+  OKLS_CK(cudaMemcpy2DAsync(dst, static_cast<size_t>(tr.d * 2), b->p, static_cast<size_t>(b->ld * 2),
+                            static_cast<size_t>(tr.d * 2), static_cast<size_t>(tr.d * tr.count),
+                            cudaMemcpyDeviceToDevice, st));
+  return OKLS_OK;
+}
+
+// Normalisation and the coupled Newton-Schulz chain for 1 or 2 factors.
+// The stable order is kept: M_k = Z_k Y_k, Y_{k+1} = Y_k T_k, Z_{k+1} = T_k Z_k.
+okls_status run_ns(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
+                   int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
+                   const TraceOut* tr) {
+  const int K = sc.iters;
+  const int h = kHeadroom;
+  for (int q = 0; q < nf; ++q) {
+    Factor& f = *fs[q];
+    NormaliseArgs A;
+    memset(&A, 0, sizeof(A));
+    A.S = f.S;
+    A.d = f.d;
+    A.ld16 = f.Y[0][0].ld;
+    A.mat16 = f.Y[0][0].mat();
+    A.Y = f.Y[0][0].p;
+    A.YT = f.YT[0][0].p;
+    A.T = f.T[0].p;
+    A.TT = f.TT[0].p;
+    A.Z = f.Z[1][0].p;
+    A.ZT = f.ZT[1][0].p;
+    A.split_y = split > 0;
+    A.split_t = split > 0;
+    A.split_z = split > 1;
+    if (A.split_y) {
+      A.Ylo = f.Y[0][1].p;
+      A.YTlo = f.YT[0][1].p;
+      A.Tlo = f.T[1].p;
+      A.TTlo = f.TT[1].p;
+    }
+    if (A.split_z) {
+      A.Zlo = f.Z[1][1].p;
+      A.ZTlo = f.ZT[1][1].p;
+    }
+    A.a0 = static_cast<float>(sc.a[0]);
+    A.b0 = static_cast<float>(sc.b[0]);
+    A.z1 = sc.z[1];
+    A.ridge = ridge;
+    A.scal = scal;
+    A.scal_ld = scal_ld;
+    A.slot_cprime = f.slot_cprime;
+    A.slot_sumsq = f.slot_sumsq;
+    A.status = status;
+    OKLS_CK(launch_normalise(A, f.batch, st));
+  }
+  if (tr && tr->base) {
+    okls_status s;
+    if ((s = trace_copy(*tr, 0, &fs[0]->Y[0][0], st)) != OKLS_OK) return s;
+    if ((s = trace_copy(*tr, 1, nullptr, st)) != OKLS_OK) return s;
+    if ((s = trace_copy(*tr, 2, &fs[0]->T[0], st)) != OKLS_OK) return s;
+  }
+  // k = 0: Y_1 = Y_0 T_0 (Z_1 = T_0 written by the normaliser)
+  {
+    LaunchBuilder lb;
+    const bool sp = split > 0, spo = split > 1;
+    for (int q = 0; q < nf; ++q) {
+      Factor& f = *fs[q];
+      GemmProblem& p = lb.add(f.Y[0], f.TT, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false);
+      set_out16(p, f.Y[1][0], &f.YT[1][0], spo ? &f.Y[1][1] : nullptr, spo ? &f.YT[1][1] : nullptr);
+      p.alpha = std::ldexp(1.0f, -h);
+    }
+    okls_status s = lb.go(maps, status, sms, st);
+    if (s != OKLS_OK) return s;
+  }
+  for (int k = 1; k < K; ++k) {
+    const int cur = k & 1, nxt = cur ^ 1;
+    const bool sp = split > k;       // operands of this iteration are pairs
+    const bool spo = split > k + 1;  // outputs feed a split iteration
+    {
+      LaunchBuilder lb;  // T_k = a_k I + b_k Z_k Y_k
+      for (int q = 0; q < nf; ++q) {
+        Factor& f = *fs[q];
+        GemmProblem& p = lb.add(f.Z[cur], f.YT[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_T, false);
+        set_out16(p, f.T[0], &f.TT[0], sp ? &f.T[1] : nullptr, sp ? &f.TT[1] : nullptr);
+        p.alpha = static_cast<float>(std::ldexp(sc.a[k], h));
+        p.beta = static_cast<float>(std::ldexp(sc.b[k], sc.z[k] - h));
+      }
+      okls_status s = lb.go(maps, status, sms, st);
+      if (s != OKLS_OK) return s;
+    }
+    if (tr && tr->base) {
+      okls_status s;
+      if ((s = trace_copy(*tr, 3 * k, &fs[0]->Y[cur][0], st)) != OKLS_OK) return s;
+      if ((s = trace_copy(*tr, 3 * k + 1, &fs[0]->Z[cur][0], st)) != OKLS_OK) return s;
+      if ((s = trace_copy(*tr, 3 * k + 2, &fs[0]->T[0], st)) != OKLS_OK) return s;
+    }
+    LaunchBuilder lb;
+    for (int q = 0; q < nf; ++q) {
+      Factor& f = *fs[q];
+      if (k < K - 1) {
+        GemmProblem& py = lb.add(f.Y[cur], f.TT, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false);
+        set_out16(py, f.Y[nxt][0], &f.YT[nxt][0], spo ? &f.Y[nxt][1] : nullptr, spo ? &f.YT[nxt][1] : nullptr);
+        py.alpha = std::ldexp(1.0f, -h);
+        GemmProblem& pz = lb.add(f.T, f.ZT[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false);
+        set_out16(pz, f.Z[nxt][0], &f.ZT[nxt][0], spo ? &f.Z[nxt][1] : nullptr, spo ? &f.ZT[nxt][1] : nullptr);
+        pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
+      } else {
+        GemmProblem& pz = lb.add(f.T, f.ZT[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_LAST, false);
+        // in split mode the copy of P read by the X and whitening products
+        // is a (hi, lo) pair as well
+        set_out16(pz, f.Ph[0], &f.PhT[0], f.split ? &f.Ph[1] : nullptr, f.split ? &f.PhT[1] : nullptr);
+        pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
+        pz.out32 = f.P32;
+        pz.ld32 = f.d;
+        pz.mat32 = static_cast<int64_t>(f.d) * f.d;
+        pz.scal = scal;
+        pz.scal_ld = scal_ld;
+        pz.scal_slot = f.slot_pscale;
+        if (f.root32) {
+          GemmProblem& pr = lb.add(f.Y[cur], f.TT, sp, f.d, f.d, f.d, f.batch, EPI_ROOT, false);
+          pr.out32 = f.root32;
+          pr.ld32 = f.d;
+          pr.mat32 = static_cast<int64_t>(f.d) * f.d;
+          pr.scal = scal;
+          pr.scal_ld = scal_ld;
+          pr.scal_slot = f.slot_rscale;
+        }
+      }
+    }
+    okls_status s = lb.go(maps, status, sms, st);
+    if (s != OKLS_OK) return s;
+  }
+  if (tr && tr->base) return trace_copy(*tr, 3 * K, &fs[0]->Ph[0], st);
+  return OKLS_OK;
+}
+
+}  // namespace
+
+// ====================================================================== handle
+struct okls_handle_s {
+  okls_config cfg;
+  int sms = 0;
+  Sched sched;
+  float *M = nullptr, *Sa = nullptr, *Sb = nullptr, *Pa = nullptr, *Pb = nullptr;
+  Factor fa, fb;
+  Buf Gh, GhT, NhT, Xb, XaT;
+  float* scal = nullptr;
+  uint32_t* status = nullptr;
+  CUtensorMap* maps = nullptr;
+  int64_t t = 0;
+};
+
+namespace {
+
+struct Layout {
+  size_t state_bytes = 0, ws_bytes = 0;
+};
+
+// Lays out state and workspace; with bases set, fills the handle too.
+okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_s* h, Layout* out) {
+  const int64_t B = c.batch, m = c.m, n = c.n;
+  Planner sp;
+  sp.base = state;
+  float* M = static_cast<float*>(sp.take(static_cast<size_t>(B * m * n * 4)));
+  float* Sa = static_cast<float*>(sp.take(static_cast<size_t>(B * m * m * 4)));
+  float* Sb = static_cast<float*>(sp.take(static_cast<size_t>(B * n * n * 4)));
+  float* Pa = static_cast<float*>(sp.take(static_cast<size_t>(B * m * m * 4)));
+  float* Pb = static_cast<float*>(sp.take(static_cast<size_t>(B * n * n * 4)));
+  Planner wp;
+  wp.base = ws;
+  CUtensorMap* maps = static_cast<CUtensorMap*>(wp.take(kMapTableBytes, 128));
+  float* scal = static_cast<float*>(wp.take(static_cast<size_t>(SC_COUNT * B * 4)));
+  uint32_t* status = static_cast<uint32_t*>(wp.take(256));
+  Buf Gh = wp.buf16(m, n, B), GhT = wp.buf16(n, m, B), NhT = wp.buf16(n, m, B);
+  Buf Xb = wp.buf16(m, n, B), XaT = wp.buf16(n, m, B);
+  Factor fa, fb;
+  const bool split = c.ns_split_iters > 0;
+  plan_factor(wp, fa, static_cast<int>(m), static_cast<int>(B), split);
+  plan_factor(wp, fb, static_cast<int>(n), static_cast<int>(B), split);
+  if (wp.err != OKLS_OK) return wp.err;
+  out->state_bytes = sp.off;
+  out->ws_bytes = wp.off;
+  if (h) {
+    h->M = M;
+    h->Sa = Sa;
+    h->Sb = Sb;
+    h->Pa = Pa;
+    h->Pb = Pb;
+    fa.S = Sa;
+    fa.P32 = Pa;
+    fa.slot_sumsq = SC_SUMSQ_SA;
+    fa.slot_cprime = SC_CPRIME_A;
+    fa.slot_pi = SC_PI_A;
+    fa.slot_pscale = SC_PSCALE_A;
+    fa.slot_rscale = SC_RSCALE_A;
+    fb.S = Sb;
+    fb.P32 = Pb;
+    fb.slot_sumsq = SC_SUMSQ_SB;
+    fb.slot_cprime = SC_CPRIME_B;
+    fb.slot_pi = SC_PI_B;
+    fb.slot_pscale = SC_PSCALE_B;
+    fb.slot_rscale = SC_RSCALE_B;
+    h->fa = fa;
+    h->fb = fb;
+    h->Gh = Gh;
+    h->GhT = GhT;
+    h->NhT = NhT;
+    h->Xb = Xb;
+    h->XaT = XaT;
+    h->scal = scal;
+    h->status = status;
+    h->maps = maps;
+    // upload the descriptor table once
+    if (!wp.maps.empty()) {
+      cudaError_t e = cudaMemcpy(maps, wp.maps.data(), wp.maps.size() * sizeof(CUtensorMap),
+                                 cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return fail(OKLS_ERR_CUDA, "descriptor upload: %s", cudaGetErrorString(e));
+    }
+  }
+  return OKLS_OK;
+}
+
+bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.0f; }
+
+okls_status validate(const okls_config* c) {
+  if (!c) return fail(OKLS_ERR_INVALID_ARG, "config is NULL");
+  if (c->batch < 1 || c->m < 1 || c->n < 1)
+    return fail(OKLS_ERR_INVALID_ARG, "batch, m, n must be >= 1 (got %lld, %lld, %lld)",
+                static_cast<long long>(c->batch), static_cast<long long>(c->m), static_cast<long long>(c->n));
+  if (c->m > 32768 || c->n > 32768 || c->batch > 65535)
+    return fail(OKLS_ERR_UNSUPPORTED, "m, n <= 32768 and batch <= 65535 supported");
+  if (c->param_dtype != OKLS_F32 && c->param_dtype != OKLS_BF16)
+    return fail(OKLS_ERR_INVALID_ARG, "param_dtype %d", c->param_dtype);
+  if (c->grad_dtype != OKLS_F32 && c->grad_dtype != OKLS_BF16)
+    return fail(OKLS_ERR_INVALID_ARG, "grad_dtype %d", c->grad_dtype);
+  if (!(c->lr_peak > 0.0f) || !std::isfinite(c->lr_peak)) return fail(OKLS_ERR_INVALID_ARG, "lr_peak must be > 0");
+  if (!(c->beta1 >= 0.0f && c->beta1 < 1.0f)) return fail(OKLS_ERR_INVALID_ARG, "beta1 must be in [0, 1)");
+  if (!(c->beta2 >= 0.0f && c->beta2 < 1.0f)) return fail(OKLS_ERR_INVALID_ARG, "beta2 must be in [0, 1)");
+  if (!finite_nonneg(c->eps)) return fail(OKLS_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (!finite_nonneg(c->weight_decay)) return fail(OKLS_ERR_INVALID_ARG, "weight_decay must be >= 0");
+  if (c->ns_iters < 2 || c->ns_iters > 32) return fail(OKLS_ERR_INVALID_ARG, "ns_iters must be in [2, 32]");
+  if (c->ns_split_iters < 0 || c->ns_split_iters > c->ns_iters)
+    return fail(OKLS_ERR_INVALID_ARG, "ns_split_iters must be in [0, ns_iters]");
+  if (!(c->ns_lo > 0.0f && c->ns_lo < 1.0f)) return fail(OKLS_ERR_INVALID_ARG, "ns_lo must be in (0, 1)");
+  if (!finite_nonneg(c->ridge)) return fail(OKLS_ERR_INVALID_ARG, "ridge must be finite and >= 0");
+  for (int i = 0; i < 8; ++i)
+    if (c->reserved[i] != 0) return fail(OKLS_ERR_INVALID_ARG, "reserved fields must be zero");
+  return OKLS_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+// ================================================================== C entries
+extern "C" {
+
+int32_t okls_abi_version(void) { return OKLS_ABI_VERSION; }
+
+const char* okls_last_error(void) { return g_err.c_str(); }
+
+okls_status okls_config_default(okls_config* cfg, int64_t batch, int64_t m, int64_t n) {
+  if (!cfg) return fail(OKLS_ERR_INVALID_ARG, "config is NULL");
+  memset(cfg, 0, sizeof(*cfg));
+  cfg->batch = batch;
+  cfg->m = m;
+  cfg->n = n;
+  cfg->param_dtype = OKLS_F32;
+  cfg->grad_dtype = OKLS_F32;
+  cfg->lr_peak = 0.09434f;
+  cfg->beta1 = 0.9684f;
+  cfg->beta2 = 0.9482f;
+  cfg->eps = 1e-9f;
+  cfg->weight_decay = 0.0303f;
+  cfg->ns_iters = 10;
+  cfg->ns_split_iters = 0;
+  cfg->ns_lo = 1e-3f;
+  cfg->ridge = 1e-3f;
+  cfg->variance_correction = 1;
+  cfg->eps_every_update = 1;
+  return OKLS_OK;
+}
+
+okls_status okls_state_bytes(const okls_config* cfg, size_t* state_bytes, size_t* workspace_bytes) {
+  okls_status s = validate(cfg);
+  if (s != OKLS_OK) return s;
+  Layout lay;
+  s = plan(*cfg, nullptr, nullptr, nullptr, &lay);
+  if (s != OKLS_OK) return s;
+  if (state_bytes) *state_bytes = lay.state_bytes;
+  if (workspace_bytes) *workspace_bytes = lay.ws_bytes;
+  return OKLS_OK;
+}
+
+okls_status okls_create(const okls_config* cfg, void* state_dev, size_t state_bytes, void* workspace_dev,
+                        size_t workspace_bytes, okls_handle* out) {
+  if (!out) return fail(OKLS_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  okls_status s = validate(cfg);
+  if (s != OKLS_OK) return s;
+  if (!state_dev || !workspace_dev) return fail(OKLS_ERR_INVALID_ARG, "state/workspace pointer is NULL");
+  if (!aligned(state_dev, 256) || !aligned(workspace_dev, 256))
+    return fail(OKLS_ERR_UNSUPPORTED, "state and workspace must be 256-byte aligned");
+  Layout lay;
+  s = plan(*cfg, nullptr, nullptr, nullptr, &lay);
+  if (s != OKLS_OK) return s;
+  if (state_bytes < lay.state_bytes || workspace_bytes < lay.ws_bytes)
+    return fail(OKLS_ERR_INVALID_ARG, "state needs %zu bytes, workspace %zu bytes", lay.state_bytes, lay.ws_bytes);
+  int sms = 0;
+  if ((s = device_sms(&sms)) != OKLS_OK) return s;
+  okls_handle_s* h = new okls_handle_s();
+  h->cfg = *cfg;
+  h->sms = sms;
+  h->sched = make_schedule(cfg->ns_iters, cfg->ns_lo);
+  s = plan(*cfg, static_cast<uint8_t*>(state_dev), static_cast<uint8_t*>(workspace_dev), h, &lay);
+  if (s != OKLS_OK) {
+    delete h;
+    return s;
+  }
+  *out = h;
+  return OKLS_OK;
+}
+
+okls_status okls_reset_state(okls_handle h, void* stream) {
+  if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const okls_config& c = h->cfg;
+  OKLS_CK(cudaMemsetAsync(h->M, 0, static_cast<size_t>(c.batch * c.m * c.n * 4), st));
+  OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(SC_COUNT * c.batch * 4), st));
+  OKLS_CK(cudaMemsetAsync(h->status, 0, 4, st));
+  OKLS_CK(launch_reset_factor(h->Sa, h->Pa, h->fa.Ph[0].p, h->fa.PhT[0].p, h->fa.Ph[1].p, h->fa.PhT[1].p,
+                              static_cast<int>(c.m), h->fa.Ph[0].ld, h->fa.Ph[0].mat(), static_cast<int>(c.batch),
+                              c.eps, h->scal,
+                              static_cast<int>(c.batch), SC_PI_A, st));
+  OKLS_CK(launch_reset_factor(h->Sb, h->Pb, h->fb.Ph[0].p, h->fb.PhT[0].p, h->fb.Ph[1].p, h->fb.PhT[1].p,
+                              static_cast<int>(c.n), h->fb.Ph[0].ld, h->fb.Ph[0].mat(), static_cast<int>(c.batch),
+                              c.eps, h->scal,
+                              static_cast<int>(c.batch), SC_PI_B, st));
+  h->t = 0;
+  return OKLS_OK;
+}
+
+okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* stream) {
+  if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
+  if (!W || !G) return fail(OKLS_ERR_INVALID_ARG, "W or G is NULL");
+  if (!aligned(W, 16) || !aligned(G, 16)) return fail(OKLS_ERR_UNSUPPORTED, "W and G must be 16-byte aligned");
+  if (!finite_nonneg(lr)) return fail(OKLS_ERR_INVALID_ARG, "lr must be finite and >= 0");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const okls_config& c = h->cfg;
+  const int B = static_cast<int>(c.batch), m = static_cast<int>(c.m), n = static_cast<int>(c.n);
+  const int sld = B;
+  const int64_t t1 = h->t + 1;
+  const float kappa = c.variance_correction ? static_cast<float>(variance_kappa(c.beta1, t1)) : 1.0f;
+  const int gbf = c.grad_dtype == OKLS_BF16;
+  const int h12 = kHeadroom;
+  okls_status s;
+
+  // 1-2. momentum, statistics, packed binary16 operands
+  OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(4 * B * 4), st));  // SC_SUMSQ_* slots
+  OKLS_CK(launch_momentum_stats(G, gbf, h->M, B, static_cast<int64_t>(m) * n, c.beta1, kappa, h->scal, sld,
+                                h->status, st));
+  OKLS_CK(launch_coeffs_pre(B, m, n, c.beta2, h->scal, sld, st));
+  // row pitches: Ghat is m x n (pitch ldn), Ghat^T and Nhat^T are n x m (pitch ldm)
+  if (h->Gh.ld < n || h->GhT.ld < m || h->NhT.ld != h->GhT.ld || h->Gh.rows != m || h->GhT.rows != n)
+    return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: packed operand pitches");
+  OKLS_CK(launch_pack(G, gbf, h->M, h->Gh.p, h->GhT.p, h->NhT.p, B, m, n, /*ldm=*/h->GhT.ld,
+                      /*ldn=*/h->Gh.ld, c.beta1, kappa, h->scal, sld, h->status, st));
+  // 3. X_b = G P_b and X_a^T = G^T P_a^T (previous roots)
+  {
+    LaunchBuilder lb;
+    GemmProblem& p0 = lb.add_bsplit(h->Gh, h->fb.PhT, h->fb.split, m, n, n, B, EPI_X16);
+    set_out16(p0, h->Xb, nullptr, nullptr, nullptr);
+    p0.alpha = std::ldexp(1.0f, -h12);
+    p0.check_finite = 1;
+    GemmProblem& p1 = lb.add_bsplit(h->GhT, h->fa.Ph, h->fa.split, n, m, m, B, EPI_X16);
+    set_out16(p1, h->XaT, nullptr, nullptr, nullptr);
+    p1.alpha = std::ldexp(1.0f, -h12);
+    p1.check_finite = 1;
+    if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
+  }
+  // 4. factor EMAs on upper tiles, mirrored, with ||S||_F^2
+  {
+    const float eps_u = c.eps_every_update ? c.eps : 0.0f;
+    LaunchBuilder lb;
+    GemmProblem& pa = lb.add(&h->Xb, &h->Xb, false, m, m, n, B, EPI_SYRK, true);
+    pa.out32 = h->Sa;
+    pa.ld32 = m;
+    pa.mat32 = static_cast<int64_t>(m) * m;
+    pa.scal = h->scal;
+    pa.scal_ld = sld;
+    pa.scal_slot = SC_ALPHA_SA;
+    pa.sum_slot = SC_SUMSQ_SA;
+    pa.beta = c.beta2;
+    pa.gamma = eps_u;
+    GemmProblem& pb = lb.add(&h->XaT, &h->XaT, false, n, n, m, B, EPI_SYRK, true);
+    pb.out32 = h->Sb;
+    pb.ld32 = n;
+    pb.mat32 = static_cast<int64_t>(n) * n;
+    pb.scal = h->scal;
+    pb.scal_ld = sld;
+    pb.scal_slot = SC_ALPHA_SB;
+    pb.sum_slot = SC_SUMSQ_SB;
+    pb.beta = c.beta2;
+    pb.gamma = eps_u;
+    if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
+  }
+  // 5-6. fresh inverse roots of both factors
+  const int K = h->sched.iters;
+  OKLS_CK(launch_coeffs_post(B, c.ridge, h->sched.z[K], h->sched.z[K - 1], h->scal, sld, 1, h->status, st));
+  {
+    Factor* fs[2] = {&h->fa, &h->fb};
+    if ((s = run_ns(fs, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
+                    nullptr)) != OKLS_OK)
+      return s;
+  }
+  // 7. Q = P_a N  (into the X_b buffer)
+  {
+    LaunchBuilder lb;
+    GemmProblem& p = lb.add_asplit(h->fa.Ph, h->NhT, h->fa.split, m, n, m, B, EPI_X16);
+    set_out16(p, h->Xb, nullptr, nullptr, nullptr);
+    p.alpha = std::ldexp(1.0f, -h12);
+    p.check_finite = 1;
+    if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
+  }
+  // 8. U = Q P_b, W <- W (1 - lr wd lr/lr_peak) - lr c_shape U
+  {
+    LaunchBuilder lb;
+    GemmProblem& p = lb.add_bsplit(h->Xb, h->fb.PhT, h->fb.split, m, n, n, B, EPI_UPDATE);
+    p.w = W;
+    p.w_bf16 = c.param_dtype == OKLS_BF16;
+    p.ld32 = n;
+    p.mat32 = static_cast<int64_t>(m) * n;
+    p.scal = h->scal;
+    p.scal_ld = sld;
+    p.scal_slot = SC_UCOEF;
+    const double cshape = std::sqrt(static_cast<double>(m) / n) / (std::sqrt(static_cast<double>(m)) + std::sqrt(static_cast<double>(n)));
+    p.alpha = static_cast<float>(1.0 - static_cast<double>(lr) * c.weight_decay * (static_cast<double>(lr) / c.lr_peak));
+    p.beta = static_cast<float>(static_cast<double>(lr) * cshape);
+    if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
+  }
+  h->t = t1;
+  return OKLS_OK;
+}
+
+okls_status okls_query_status(okls_handle h, void* stream, uint32_t* dev_status) {
+  if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  OKLS_CK(cudaStreamSynchronize(st));
+  OKLS_CK(cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost));
+  OKLS_CK(cudaMemset(h->status, 0, 4));
+  if (dev_status) *dev_status = v;
+  if (v & kStTimeout) return fail(OKLS_ERR_TIMEOUT, "a device-side wait expired (status 0x%x)", v);
+  if (v) return fail(OKLS_ERR_NONFINITE, "non-finite values in the step (status 0x%x)", v);
+  return OKLS_OK;
+}
+
+static okls_status part_ptr(okls_handle h, int32_t part, float** p, size_t* bytes) {
+  const okls_config& c = h->cfg;
+  switch (part) {
+    case OKLS_STATE_M: *p = h->M; *bytes = static_cast<size_t>(c.batch * c.m * c.n * 4); break;
+    case OKLS_STATE_SA: *p = h->Sa; *bytes = static_cast<size_t>(c.batch * c.m * c.m * 4); break;
+    case OKLS_STATE_SB: *p = h->Sb; *bytes = static_cast<size_t>(c.batch * c.n * c.n * 4); break;
+    case OKLS_STATE_PA: *p = h->Pa; *bytes = static_cast<size_t>(c.batch * c.m * c.m * 4); break;
+    case OKLS_STATE_PB: *p = h->Pb; *bytes = static_cast<size_t>(c.batch * c.n * c.n * 4); break;
+    default: return fail(OKLS_ERR_INVALID_ARG, "unknown state part %d", part);
+  }
+  return OKLS_OK;
+}
+
+okls_status okls_get_state(okls_handle h, int32_t part, void* dst, void* stream) {
+  if (!h || !dst) return fail(OKLS_ERR_INVALID_ARG, "handle or dst is NULL");
+  float* p = nullptr;
+  size_t bytes = 0;
+  okls_status s = part_ptr(h, part, &p, &bytes);
+  if (s != OKLS_OK) return s;
+  OKLS_CK(cudaMemcpyAsync(dst, p, bytes, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)));
+  return OKLS_OK;
+}
+
+okls_status okls_set_state(okls_handle h, int32_t part, const void* src, void* stream) {
+  if (!h || !src) return fail(OKLS_ERR_INVALID_ARG, "handle or src is NULL");
+  float* p = nullptr;
+  size_t bytes = 0;
+  okls_status s = part_ptr(h, part, &p, &bytes);
+  if (s != OKLS_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  OKLS_CK(cudaMemcpyAsync(p, src, bytes, cudaMemcpyDeviceToDevice, st));
+  const okls_config& c = h->cfg;
+  if (part == OKLS_STATE_PA)
+    OKLS_CK(launch_requant(h->Pa, static_cast<int>(c.batch), static_cast<int>(c.m), h->fa.Ph[0].p, h->fa.PhT[0].p,
+                           h->fa.Ph[1].p, h->fa.PhT[1].p, h->fa.Ph[0].ld, h->fa.Ph[0].mat(), h->scal,
+                           static_cast<int>(c.batch), SC_PI_A, st));
+  if (part == OKLS_STATE_PB)
+    OKLS_CK(launch_requant(h->Pb, static_cast<int>(c.batch), static_cast<int>(c.n), h->fb.Ph[0].p, h->fb.PhT[0].p,
+                           h->fb.Ph[1].p, h->fb.PhT[1].p, h->fb.Ph[0].ld, h->fb.Ph[0].mat(), h->scal,
+                           static_cast<int>(c.batch), SC_PI_B, st));
+  return OKLS_OK;
+}
+
+okls_status okls_get_step(okls_handle h, int64_t* t) {
+  if (!h || !t) return fail(OKLS_ERR_INVALID_ARG, "handle or t is NULL");
+  *t = h->t;
+  return OKLS_OK;
+}
+
+okls_status okls_set_step(okls_handle h, int64_t t) {
+  if (!h || t < 0) return fail(OKLS_ERR_INVALID_ARG, "bad handle or step");
+  h->t = t;
+  return OKLS_OK;
+}
+
+okls_status okls_destroy(okls_handle h) {
+  delete h;
+  return OKLS_OK;
+}
+
+okls_status okls_ns_schedule(int32_t iters, double lo, double* a, double* b, int32_t* zexp) {
+  if (iters < 1 || iters > 64 || !(lo > 0.0 && lo <= 1.0))
+    return fail(OKLS_ERR_INVALID_ARG, "iters in [1, 64], lo in (0, 1]");
+  Sched s = make_schedule(iters, lo);
+  for (int k = 0; k < iters; ++k) {
+    if (a) a[k] = s.a[k];
+    if (b) b[k] = s.b[k];
+  }
+  if (zexp)
+    for (int k = 0; k <= iters; ++k) zexp[k] = s.z[k];
+  return OKLS_OK;
+}
+
+// ------------------------------------------------------------ inverse roots
+static okls_status inv_plan(int64_t d, int64_t count, int32_t split, uint8_t* ws, Factor* f, float** scal,
+                            uint32_t** status, CUtensorMap** maps, size_t* bytes, std::vector<CUtensorMap>* mv) {
+  Planner wp;
+  wp.base = ws;
+  *maps = static_cast<CUtensorMap*>(wp.take(kMapTableBytes, 128));
+  *scal = static_cast<float*>(wp.take(static_cast<size_t>(SC_COUNT * count * 4)));
+  *status = static_cast<uint32_t*>(wp.take(256));
+  plan_factor(wp, *f, static_cast<int>(d), static_cast<int>(count), split > 0);
+  if (wp.err != OKLS_OK) return wp.err;
+  *bytes = wp.off;
+  if (mv) *mv = wp.maps;
+  return OKLS_OK;
+}
+
+okls_status okls_inv_root_workspace_bytes(int64_t d, int64_t count, int32_t iters, int32_t split_iters,
+                                          size_t* workspace_bytes) {
+  if (d < 1 || d > 32768 || count < 1 || count > 65535 || iters < 2 || iters > 32 || split_iters < 0 ||
+      split_iters > iters || !workspace_bytes)
+    return fail(OKLS_ERR_INVALID_ARG, "bad inverse-root arguments");
+  Factor f;
+  float* scal;
+  uint32_t* status;
+  CUtensorMap* maps;
+  return inv_plan(d, count, split_iters, nullptr, &f, &scal, &status, &maps, workspace_bytes, nullptr);
+}
+
+okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace, int64_t d, int64_t count,
+                          int32_t iters, int32_t split_iters, float lo, float ridge, void* ws, size_t ws_bytes,
+                          void* stream) {
+  size_t need = 0;
+  okls_status s = okls_inv_root_workspace_bytes(d, count, iters, split_iters, &need);
+  if (s != OKLS_OK) return s;
+  if (!S || !P || !ws) return fail(OKLS_ERR_INVALID_ARG, "S, P and workspace must be non-NULL");
+  if (ws_bytes < need) return fail(OKLS_ERR_INVALID_ARG, "workspace needs %zu bytes", need);
+  if (!aligned(ws, 256)) return fail(OKLS_ERR_UNSUPPORTED, "workspace must be 256-byte aligned");
+  if (!(lo > 0.0f && lo < 1.0f) || !finite_nonneg(ridge)) return fail(OKLS_ERR_INVALID_ARG, "bad lo or ridge");
+  int sms = 0;
+  if ((s = device_sms(&sms)) != OKLS_OK) return s;
+  Factor f;
+  float* scal;
+  uint32_t* status;
+  CUtensorMap* maps;
+  std::vector<CUtensorMap> mv;
+  if ((s = inv_plan(d, count, split_iters, static_cast<uint8_t*>(ws), &f, &scal, &status, &maps, &need, &mv)) !=
+      OKLS_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  OKLS_CK(cudaMemcpyAsync(maps, mv.data(), mv.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice, st));
+  OKLS_CK(cudaMemsetAsync(scal, 0, static_cast<size_t>(SC_COUNT * count * 4), st));
+  OKLS_CK(cudaMemsetAsync(status, 0, 4, st));
+  f.S = const_cast<float*>(S);
+  f.P32 = P;
+  f.root32 = root;
+  f.slot_sumsq = SC_SUMSQ_SA;
+  f.slot_cprime = SC_CPRIME_A;
+  f.slot_pi = SC_PI_A;
+  f.slot_pscale = SC_PSCALE_A;
+  f.slot_rscale = SC_RSCALE_A;
+  const Sched sc = make_schedule(iters, lo);
+  OKLS_CK(launch_sumsq(S, static_cast<int>(count), d * d, scal, static_cast<int>(count), SC_SUMSQ_SA, st));
+  OKLS_CK(launch_coeffs_post(static_cast<int>(count), ridge, sc.z[iters], sc.z[iters - 1], scal,
+                             static_cast<int>(count), 0, status, st));
+  TraceOut tr;
+  tr.base = trace;
+  tr.count = count;
+  tr.d = d;
+  Factor* fs[1] = {&f};
+  s = run_ns(fs, 1, sc, split_iters, ridge, scal, static_cast<int>(count), maps, status, sms, st, &tr);
+  // keep the host descriptor table alive until the upload has run
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (s != OKLS_OK) return s;
+  if (e != cudaSuccess) return fail(OKLS_ERR_CUDA, "inverse root: %s", cudaGetErrorString(e));
+  uint32_t v = 0;
+  OKLS_CK(cudaMemcpy(&v, status, 4, cudaMemcpyDeviceToHost));
+  if (v & kStTimeout) return fail(OKLS_ERR_TIMEOUT, "a device-side wait expired (status 0x%x)", v);
+  if (v) return fail(OKLS_ERR_NONFINITE, "non-finite Newton-Schulz iterate (status 0x%x)", v);
+  return OKLS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,432 @@
+// Bandwidth-bound kernels of the OKLS step (sm_103a).
+//
+//   k_momentum_stats  M_t = b1 M + (1-b1) G and N_t = kappa (b1 M_t + (1-b1) G)
+//                     evaluated on the fly to get sum G^2, sum N^2 per matrix
+//                     (page "Online KL Shampoo": Nesterov momentum with
+//                     variance correction); flags non-finite inputs.
+//   k_coeffs_pre      per-matrix power-of-two scales of G and N and the EMA
+//                     weights of both factors.
+//   k_pack            writes M_t, Ghat, Ghat^T and Nhat^T (binary16, scaled)
+//                     through 32x32 shared-memory tiles (coalesced both ways).
+//   k_coeffs_post     normaliser c' of each factor, the root scales pi and
+//                     the whitening coefficient.
+//   k_normalise       Y_0 = (S + rho c I)/c', T_0 = a_0 I + b_0 Y_0, Z_1 = T_0
+//                     (the first Newton-Schulz step needs no product).
+//   k_sumsq, k_amax, k_requant, k_reset_state: inverse-root entry and state
+//                     management.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "okls_internal.h"
+#include "okls_kernels.h"
+
+namespace okls {
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float s = 0.0f;
+  if (w == 0) {
+    s = (l < static_cast<int>(blockDim.x >> 5)) ? red[l] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  }
+  return s;  // valid in thread 0
+}
+
+// ------------------------------------------------------------ momentum stats
+template <typename GT>
+__global__ void k_momentum_stats(const GT* __restrict__ G, const float* __restrict__ M,
+                                 int64_t mn, float b1, float kappa, float* scal, int scal_ld,
+                                 uint32_t* status) {
+  __shared__ float red[32];
+  const int b = blockIdx.y;
+  const GT* g = G + static_cast<int64_t>(b) * mn;
+  const float* mo = M + static_cast<int64_t>(b) * mn;
+  float sg = 0.0f, sn = 0.0f;
+  bool bad = false;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < mn;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float gv = to_f(g[e]);
+    const float mv = mo[e];
+    const float mn1 = fmaf(b1, mv, (1.0f - b1) * gv);
+    const float nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
+    bad |= !isfinite(gv) || !isfinite(mv);
+    sg = fmaf(gv, gv, sg);
+    sn = fmaf(nv, nv, sn);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, kStNonfiniteInput);
+  const float tg = block_sum(sg, red);
+  const float tn = block_sum(sn, red);
+  if (threadIdx.x == 0) {
+    atomicAdd(scal + static_cast<int64_t>(SC_SUMSQ_G) * scal_ld + b, tg);
+    atomicAdd(scal + static_cast<int64_t>(SC_SUMSQ_N) * scal_ld + b, tn);
+  }
+}
+
+// power of two 2^e with rms * 2^e in [1, 2); 1 for an all-zero matrix
+__device__ __forceinline__ float pow2_rms_scale(float sumsq, double count) {
+  const float r = static_cast<float>(sqrt(static_cast<double>(sumsq) / count));
+  if (!(r > 0.0f) || !isfinite(r)) return 1.0f;
+  int e = -ilogbf(r);
+  e = max(-100, min(100, e));
+  return ldexpf(1.0f, e);
+}
+
+__global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal,
+                             int scal_ld) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  auto S = [&](int slot) -> float& { return scal[static_cast<int64_t>(slot) * scal_ld + b]; };
+  const double cnt = static_cast<double>(m) * static_cast<double>(n);
+  const float gs = pow2_rms_scale(S(SC_SUMSQ_G), cnt);
+  const float ns = pow2_rms_scale(S(SC_SUMSQ_N), cnt);
+  S(SC_GSCALE) = gs;
+  S(SC_NSCALE) = ns;
+  // X_b = G P_b = Xhat_b 2^h pi_b / gs  ->  S_a += (1-b2)/n (2^h pi_b / gs)^2 Xhat Xhat^T
+  const double h = ldexp(1.0, kHeadroom);
+  const double xa = h * S(SC_PI_B) / gs;
+  const double xb = h * S(SC_PI_A) / gs;
+  S(SC_ALPHA_SA) = static_cast<float>((1.0 - beta2) / static_cast<double>(n) * xa * xa);
+  S(SC_ALPHA_SB) = static_cast<float>((1.0 - beta2) / static_cast<double>(m) * xb * xb);
+}
+
+// ------------------------------------------------------------------ pack
+template <typename GT>
+__global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* __restrict__ Gh,
+                       __half* __restrict__ GhT, __half* __restrict__ NhT, int m, int n, int64_t ldm,
+                       int64_t ldn, float b1, float kappa, const float* scal, int scal_ld,
+                       const uint32_t* status) {
+  __shared__ float sg[32][33];
+  __shared__ float sn[32][33];
+  if (*reinterpret_cast<const volatile uint32_t*>(status) != 0u) return;
+  const int b = blockIdx.z;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const float gs = scal[static_cast<int64_t>(SC_GSCALE) * scal_ld + b];
+  const float ns = scal[static_cast<int64_t>(SC_NSCALE) * scal_ld + b];
+  const int64_t mn = static_cast<int64_t>(m) * n;
+  const GT* g = G + b * mn;
+  float* mo = M + b * mn;
+  __half* gh = Gh + b * static_cast<int64_t>(m) * ldn;
+  const int tx = threadIdx.x;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int i = r0 + r, j = c0 + tx;
+    float gv = 0.0f, nv = 0.0f;
+    if (i < m && j < n) {
+      const int64_t e = static_cast<int64_t>(i) * n + j;
+      gv = to_f(g[e]);
+      const float mn1 = fmaf(b1, mo[e], (1.0f - b1) * gv);
+      nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
+      mo[e] = mn1;
+      gh[static_cast<int64_t>(i) * ldn + j] = __float2half_rn(gv * gs);
+    }
+    sg[r][tx] = gv * gs;
+    sn[r][tx] = nv * ns;
+  }
+  __syncthreads();
+  __half* gt = GhT + b * static_cast<int64_t>(n) * ldm;
+  __half* nt = NhT + b * static_cast<int64_t>(n) * ldm;
+  for (int c = threadIdx.y; c < 32; c += 8) {
+    const int j = c0 + c, i = r0 + tx;
+    if (i < m && j < n) {
+      gt[static_cast<int64_t>(j) * ldm + i] = __float2half_rn(sg[tx][c]);
+      nt[static_cast<int64_t>(j) * ldm + i] = __float2half_rn(sn[tx][c]);
+    }
+  }
+}
+
+// -------------------------------------------------------------- post scalars
+__global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
+                              int with_update, const uint32_t* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  // a failed stage leaves the previous roots (and their scales) in force
+  if (*reinterpret_cast<const volatile uint32_t*>(status) != 0u) return;
+  auto S = [&](int slot) -> float& { return scal[static_cast<int64_t>(slot) * scal_ld + b]; };
+  const double margin = 1.0 + ldexp(1.0, -8);
+  const int h = kHeadroom;
+  for (int f = 0; f < 2; ++f) {
+    const int s_sum = f == 0 ? SC_SUMSQ_SA : SC_SUMSQ_SB;
+    double c = sqrt(static_cast<double>(S(s_sum)));
+    double cp = c * (1.0 + ridge) * margin;
+    if (!(cp > 1e-30)) cp = 1e-30;
+    const double rc = 1.0 / sqrt(cp);
+    S(f == 0 ? SC_CPRIME_A : SC_CPRIME_B) = static_cast<float>(cp);
+    S(f == 0 ? SC_PI_A : SC_PI_B) = static_cast<float>(ldexp(rc, zK - h));
+    S(f == 0 ? SC_PSCALE_A : SC_PSCALE_B) = static_cast<float>(ldexp(rc, zK1 - 2 * h));
+    S(f == 0 ? SC_RSCALE_A : SC_RSCALE_B) = static_cast<float>(ldexp(sqrt(cp), -2 * h));
+  }
+  if (with_update) {
+    const double pa = S(SC_PI_A), pb = S(SC_PI_B), ns = S(SC_NSCALE);
+    S(SC_UCOEF) = static_cast<float>(ldexp(pa * pb / ns, h));
+  }
+}
+
+// ---------------------------------------------------------------- normalise
+__global__ void k_normalise(NormaliseArgs A) {
+  __shared__ float t1[32][33];
+  __shared__ float t2[32][33];
+  if (A.status && *reinterpret_cast<const volatile uint32_t*>(A.status) != 0u) return;
+  const int b = blockIdx.z;
+  const int d = A.d;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const float* S = A.S + static_cast<int64_t>(b) * d * d;
+  const int tx = threadIdx.x;
+  // tile (r0, c0) and the transposed tile (c0, r0) for the symmetric part
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int i = r0 + r, j = c0 + tx;
+    t1[r][tx] = (i < d && j < d) ? S[static_cast<int64_t>(i) * d + j] : 0.0f;
+    const int i2 = c0 + r, j2 = r0 + tx;
+    t2[r][tx] = (i2 < d && j2 < d) ? S[static_cast<int64_t>(i2) * d + j2] : 0.0f;
+  }
+  __syncthreads();
+  const float cp = A.scal[static_cast<int64_t>(A.slot_cprime) * A.scal_ld + b];
+  const float c = sqrtf(A.scal[static_cast<int64_t>(A.slot_sumsq) * A.scal_ld + b]);
+  const float inv = ldexpf(1.0f, kHeadroom) / cp;
+  const float rc = A.ridge * c;
+  const float a0h = ldexpf(A.a0, kHeadroom);
+  const float zsc = ldexpf(1.0f, -A.z1);
+  const int64_t moff = static_cast<int64_t>(b) * A.mat16;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int i = r0 + r, j = c0 + tx;
+    if (i >= d || j >= d) continue;
+    const float s = 0.5f * (t1[r][tx] + t2[tx][r]);
+    const float y = (s + (i == j ? rc : 0.0f)) * inv;
+    const int64_t e = moff + static_cast<int64_t>(i) * A.ld16 + j;
+    const __half yh = __float2half_rn(y);
+    float yv = __half2float(yh);
+    if (A.split_y) {
+      const __half yl = __float2half_rn(y - yv);
+      A.Ylo[e] = yl;
+      A.YTlo[e] = yl;
+      yv += __half2float(yl);
+    }
+    A.Y[e] = yh;
+    A.YT[e] = yh;
+    const float t = fmaf(A.b0, yv, i == j ? a0h : 0.0f);
+    const __half th = __float2half_rn(t);
+    float tv = __half2float(th);
+    if (A.split_t) {
+      const __half tl = __float2half_rn(t - tv);
+      A.Tlo[e] = tl;
+      A.TTlo[e] = tl;
+      tv += __half2float(tl);
+    }
+    A.T[e] = th;
+    A.TT[e] = th;
+    const float z = tv * zsc;
+    const __half zh = __float2half_rn(z);
+    if (A.split_z) {
+      const __half zl = __float2half_rn(z - __half2float(zh));
+      A.Zlo[e] = zl;
+      A.ZTlo[e] = zl;
+    }
+    A.Z[e] = zh;
+    A.ZT[e] = zh;
+    if (!isfinite(y) && A.status) atomicOr(A.status, kStNonfiniteIter);
+  }
+}
+
+// ------------------------------------------------------------- small helpers
+__global__ void k_sumsq(const float* __restrict__ S, int64_t dd, float* scal, int scal_ld, int slot) {
+  __shared__ float red[32];
+  const int b = blockIdx.y;
+  const float* s = S + static_cast<int64_t>(b) * dd;
+  float acc = 0.0f;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < dd;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    acc = fmaf(s[e], s[e], acc);
+  const float t = block_sum(acc, red);
+  if (threadIdx.x == 0) atomicAdd(scal + static_cast<int64_t>(slot) * scal_ld + b, t);
+}
+
+__global__ void k_amax(const float* __restrict__ P, int64_t dd, float* scal, int scal_ld, int slot) {
+  __shared__ float red[32];
+  const int b = blockIdx.y;
+  const float* p = P + static_cast<int64_t>(b) * dd;
+  float acc = 0.0f;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < dd;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    acc = fmaxf(acc, fabsf(p[e]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc = fmaxf(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mx = 0.0f;
+    for (int q = 0; q < static_cast<int>(blockDim.x >> 5); ++q) mx = fmaxf(mx, red[q]);
+    // non-negative floats order like their bit patterns
+    atomicMax(reinterpret_cast<unsigned int*>(scal + static_cast<int64_t>(slot) * scal_ld + b),
+              __float_as_uint(mx));
+  }
+}
+
+// pi = 2^(ceil(log2 amax) - h); the amax slot is overwritten by pi.
+__global__ void k_requant_scale(int batch, float* scal, int scal_ld, int slot) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  float& s = scal[static_cast<int64_t>(slot) * scal_ld + b];
+  const float amax = s;
+  int e = 0;
+  if (amax > 0.0f && isfinite(amax)) {
+    e = ilogbf(amax);
+    if (ldexpf(1.0f, e) < amax) ++e;
+  }
+  s = ldexpf(1.0f, e - kHeadroom);
+}
+
+// Phat = P / pi (row-major and transposed, 32x32 tiles); optional lo halves
+__global__ void k_requant(const float* __restrict__ P, int d, __half* Ph, __half* PhT, __half* Pl,
+                          __half* PlT, int64_t ld16, int64_t mat16, const float* scal, int scal_ld, int slot) {
+  __shared__ float t[32][33];
+  const int b = blockIdx.z;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const float inv = 1.0f / scal[static_cast<int64_t>(slot) * scal_ld + b];
+  const float* p = P + static_cast<int64_t>(b) * d * d;
+  const int tx = threadIdx.x;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int i = r0 + r, j = c0 + tx;
+    float v = 0.0f;
+    if (i < d && j < d) {
+      v = p[static_cast<int64_t>(i) * d + j] * inv;
+      const __half hv = __float2half_rn(v);
+      Ph[b * mat16 + static_cast<int64_t>(i) * ld16 + j] = hv;
+      if (Pl) Pl[b * mat16 + static_cast<int64_t>(i) * ld16 + j] = __float2half_rn(v - __half2float(hv));
+    }
+    t[r][tx] = v;
+  }
+  __syncthreads();
+  for (int c = threadIdx.y; c < 32; c += 8) {
+    const int j = c0 + c, i = r0 + tx;
+    if (i < d && j < d) {
+      const float v = t[tx][c];
+      const __half hv = __float2half_rn(v);
+      PhT[b * mat16 + static_cast<int64_t>(j) * ld16 + i] = hv;
+      if (PlT) PlT[b * mat16 + static_cast<int64_t>(j) * ld16 + i] = __float2half_rn(v - __half2float(hv));
+    }
+  }
+}
+
+// M = 0, S = eps I, P = I; Phat = 2^h I (pi = 2^-h), low halves 0
+__global__ void k_reset_factor(float* S, float* P, __half* Ph, __half* PhT, __half* Pl, __half* PlT, int d,
+                               int64_t ld16, int64_t mat16, int batch, float eps) {
+  const int64_t dd = static_cast<int64_t>(d) * d;
+  const int64_t tot = dd * batch;
+  const __half one = __float2half_rn(ldexpf(1.0f, kHeadroom));
+  const __half zero = __float2half_rn(0.0f);
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < tot;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t b = e / dd, r = e % dd;
+    const int64_t i = r / d, j = r % d;
+    const bool diag = i == j;
+    S[e] = diag ? eps : 0.0f;
+    P[e] = diag ? 1.0f : 0.0f;
+    const int64_t o = b * mat16 + i * ld16 + j;
+    Ph[o] = diag ? one : zero;
+    PhT[o] = diag ? one : zero;
+    if (Pl) Pl[o] = zero;
+    if (PlT) PlT[o] = zero;
+  }
+}
+
+__global__ void k_fill_scal(float* scal, int scal_ld, int slot, int batch, float v) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < batch) scal[static_cast<int64_t>(slot) * scal_ld + b] = v;
+}
+
+// ---------------------------------------------------------------- launchers
+static int grid_for(int64_t n, int per_block, int cap) {
+  int64_t g = (n + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return static_cast<int>(g);
+}
+
+cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int batch, int64_t mn,
+                                  float b1, float kappa, float* scal, int scal_ld, uint32_t* status,
+                                  cudaStream_t st) {
+  const int per_mat = grid_for(mn, 256 * 8, 4096);
+  dim3 grid(per_mat, batch);
+  if (g_bf16)
+    k_momentum_stats<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(G), M, mn,
+                                                          b1, kappa, scal, scal_ld, status);
+  else
+    k_momentum_stats<float><<<grid, 256, 0, st>>>(static_cast<const float*>(G), M, mn, b1, kappa, scal,
+                                                  scal_ld, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal, int scal_ld,
+                              cudaStream_t st) {
+  k_coeffs_pre<<<(batch + 127) / 128, 128, 0, st>>>(batch, m, n, beta2, scal, scal_ld);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* NhT,
+                        int batch, int m, int n, int64_t ldm, int64_t ldn, float b1, float kappa,
+                        const float* scal, int scal_ld, const uint32_t* status, cudaStream_t st) {
+  dim3 grid((n + 31) / 32, (m + 31) / 32, batch), block(32, 8);
+  if (g_bf16)
+    k_pack<__nv_bfloat16><<<grid, block, 0, st>>>(static_cast<const __nv_bfloat16*>(G), M, Gh, GhT, NhT,
+                                                  m, n, ldm, ldn, b1, kappa, scal, scal_ld, status);
+  else
+    k_pack<float><<<grid, block, 0, st>>>(static_cast<const float*>(G), M, Gh, GhT, NhT, m, n, ldm, ldn,
+                                          b1, kappa, scal, scal_ld, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
+                               int with_update, const uint32_t* status, cudaStream_t st) {
+  k_coeffs_post<<<(batch + 127) / 128, 128, 0, st>>>(batch, ridge, zK, zK1, scal, scal_ld, with_update,
+                                                     status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_normalise(const NormaliseArgs& A, int batch, cudaStream_t st) {
+  dim3 grid((A.d + 31) / 32, (A.d + 31) / 32, batch), block(32, 8);
+  k_normalise<<<grid, block, 0, st>>>(A);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sumsq(const float* S, int batch, int64_t dd, float* scal, int scal_ld, int slot,
+                         cudaStream_t st) {
+  dim3 grid(grid_for(dd, 256 * 8, 1024), batch);
+  k_sumsq<<<grid, 256, 0, st>>>(S, dd, scal, scal_ld, slot);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_requant(const float* P, int batch, int d, __half* Ph, __half* PhT, __half* Pl, __half* PlT,
+                           int64_t ld16, int64_t mat16, float* scal, int scal_ld, int slot, cudaStream_t st) {
+  k_fill_scal<<<(batch + 127) / 128, 128, 0, st>>>(scal, scal_ld, slot, batch, 0.0f);
+  const int64_t dd = static_cast<int64_t>(d) * d;
+  dim3 g1(grid_for(dd, 256 * 8, 1024), batch);
+  k_amax<<<g1, 256, 0, st>>>(P, dd, scal, scal_ld, slot);
+  k_requant_scale<<<(batch + 127) / 128, 128, 0, st>>>(batch, scal, scal_ld, slot);
+  dim3 grid((d + 31) / 32, (d + 31) / 32, batch), block(32, 8);
+  k_requant<<<grid, block, 0, st>>>(P, d, Ph, PhT, Pl, PlT, ld16, mat16, scal, scal_ld, slot);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset_factor(float* S, float* P, __half* Ph, __half* PhT, __half* Pl, __half* PlT, int d,
+                                int64_t ld16, int64_t mat16, int batch, float eps, float* scal, int scal_ld,
+                                int pi_slot, cudaStream_t st) {
+  const int64_t tot = static_cast<int64_t>(d) * d * batch;
+  k_reset_factor<<<grid_for(tot, 256, 8192), 256, 0, st>>>(S, P, Ph, PhT, Pl, PlT, d, ld16, mat16, batch, eps);
+  k_fill_scal<<<(batch + 127) / 128, 128, 0, st>>>(scal, scal_ld, pi_slot, batch,
+                                                   ldexpf(1.0f, -kHeadroom));
+  return cudaGetLastError();
+}
+
+}  // namespace okls

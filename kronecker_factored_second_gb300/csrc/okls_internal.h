@@ -1,0 +1,109 @@
+// Internal structures shared by the host planner and the sm_103a kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace okls {
+
+// ----------------------------------------------------------------- tiling
+constexpr int kBM = 128;        // output rows per tile (UMMA M, one TMEM lane each)
+constexpr int kBN = 256;        // output cols per tile (UMMA N, TMEM columns)
+constexpr int kBK = 64;         // K per pipeline stage: 64 fp16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;      // K of one tcgen05.mma kind::f16
+constexpr int kStages = 4;      // smem ring depth
+constexpr int kStageABytes = kBM * kBK * 2;   // 16 KB
+constexpr int kStageBBytes = kBN * kBK * 2;   // 32 KB
+constexpr int kStageBytes = kStageABytes + kStageBBytes;
+constexpr int kGemmThreads = 192;             // warp0 TMA, warp1 MMA, warps2-5 epilogue
+constexpr int kTmemCols = 512;                // two 256-column fp32 accumulators
+constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kMaxProblems = 6;
+constexpr int kMaxSeg = 3;                    // K segments (split mode: hi*hi, hi*lo, lo*hi)
+constexpr int kGroupM = 8;                    // raster group height (tiles) for L2 reuse
+
+// Binary16 operand headroom (power of two) of the Newton-Schulz iterates.
+constexpr int kHeadroom = 12;
+
+// Per-matrix scalar slots (float), laid out [slot][batch].
+enum ScalarSlot {
+  SC_SUMSQ_G = 0,    // sum G^2 of this step            (zeroed every step)
+  SC_SUMSQ_N = 1,    // sum N^2                          (zeroed every step)
+  SC_SUMSQ_SA = 2,   // ||S_a||_F^2                      (zeroed every step)
+  SC_SUMSQ_SB = 3,   // ||S_b||_F^2                      (zeroed every step)
+  SC_GSCALE = 4,     // Ghat = G * gscale (power of two)
+  SC_NSCALE = 5,     // Nhat = N * nscale (power of two)
+  SC_ALPHA_SA = 6,   // S_a += alpha_a * (Xhat_b Xhat_b^T)
+  SC_ALPHA_SB = 7,   // S_b += alpha_b * (Xhat_a^T Xhat_a)
+  SC_PI_A = 8,       // P_a = pi_a * Phat_a              (persistent)
+  SC_PI_B = 9,       // P_b = pi_b * Phat_b              (persistent)
+  SC_CPRIME_A = 10,  // normaliser c' of S_a
+  SC_CPRIME_B = 11,
+  SC_PSCALE_A = 12,  // fp32 P_a = acc * pscale_a at the last product
+  SC_PSCALE_B = 13,
+  SC_RSCALE_A = 14,  // root S_a^1/2 = acc * rscale_a (debug root output)
+  SC_RSCALE_B = 15,
+  SC_UCOEF = 16,     // U = acc_U * ucoef
+  SC_COUNT = 17
+};
+
+// Status word bits (mirror of okls.h).
+constexpr uint32_t kStNonfiniteInput = 0x1u;
+constexpr uint32_t kStNonfiniteIter = 0x2u;
+constexpr uint32_t kStNonfiniteUpdate = 0x4u;
+constexpr uint32_t kStTimeout = 0x8u;
+
+// ----------------------------------------------------------------- epilogues
+enum EpiKind : int32_t {
+  EPI_X16 = 0,       // out16 = acc * alpha (row-major)          [X_b, X_a^T, Q]
+  EPI_SYRK = 1,      // S = beta2 S + alpha_b acc + eps I, symmetric tiles, sum S^2
+  EPI_NS_T = 2,      // T = a' I + b' acc  -> fp16 row + transposed (+lo)
+  EPI_NS_SCALE = 3,  // out = acc * alpha  -> fp16 row + transposed (+lo)
+  EPI_NS_LAST = 4,   // P32 = acc * pscale_b ; Phat = acc * alpha (row + transposed)
+  EPI_UPDATE = 5,    // W = W * decay - coef_b * acc
+  EPI_ROOT = 6       // root32 = acc * rscale_b (debug)
+};
+
+struct GemmProblem {
+  // operands: K segments, each a pair of tensor-map indices (A: box 128 rows,
+  // B: box 256 rows) into the handle's descriptor table
+  int32_t nseg;
+  int32_t amap[kMaxSeg];
+  int32_t bmap[kMaxSeg];
+  int32_t rows, cols, K;        // output rows (A rows), cols (B rows), K
+  int32_t batch;
+  int32_t tiles_m, tiles_n;
+  int32_t sym;                  // 1: only tiles touching the upper triangle
+  int32_t epi;
+  int64_t tiles_per_mat;
+  int64_t tile_begin;           // first linear tile of this problem in the launch
+  // epilogue
+  void* out_hi;                 // fp16 row-major
+  void* out_hi_t;               // fp16 transposed (may be null)
+  void* out_lo;                 // fp16 row-major low half (split outputs)
+  void* out_lo_t;
+  int64_t ld16;                 // row pitch (elements) of fp16 outputs
+  int64_t mat16;                // elements per matrix of fp16 outputs
+  float* out32;                 // fp32 output / state (S, P, W fp32)
+  void* w;                      // parameter (EPI_UPDATE), fp32 or bf16
+  int32_t w_bf16;
+  int64_t ld32, mat32;          // fp32 / W row pitch and matrix stride (elements)
+  float* scal;                  // per-matrix scalar table base [SC_COUNT][scal_ld]
+  int32_t scal_ld;              // matrices per slot row of the table
+  int32_t scal_slot;            // slot read by this epilogue (alpha_b, pscale, coef)
+  int32_t sum_slot;             // slot accumulated (EPI_SYRK)
+  float alpha, beta, gamma, delta;  // kind-specific constants
+  int32_t split_out;            // 1: also write lo halves
+  int32_t check_finite;         // 1: raise kStNonfiniteIter on non-finite acc
+};
+
+struct GemmLaunch {
+  GemmProblem prob[kMaxProblems];
+  int32_t nprob;
+  int64_t total_tiles;
+  const CUtensorMap* maps;      // device table of descriptors (64-byte aligned)
+  uint32_t* status;
+};
+
+}  // namespace okls

@@ -1,0 +1,49 @@
+// Host-side launchers of the library's kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "okls_internal.h"
+
+namespace okls {
+
+struct NormaliseArgs {
+  const float* S;   // batch x d x d fp32 (symmetrised on the fly)
+  int d;
+  int64_t ld16, mat16;
+  __half *Y, *YT, *Ylo, *YTlo;   // Y_0 (both layouts; equal by symmetry)
+  __half *T, *TT, *Tlo, *TTlo;   // T_0
+  __half *Z, *ZT, *Zlo, *ZTlo;   // Z_1 = T_0
+  int split_y, split_t, split_z;
+  float a0, b0;
+  int z1;
+  float ridge;
+  const float* scal;
+  int scal_ld;
+  int slot_cprime, slot_sumsq;
+  uint32_t* status;
+};
+
+cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int batch, int64_t mn,
+                                  float b1, float kappa, float* scal, int scal_ld, uint32_t* status,
+                                  cudaStream_t st);
+cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal, int scal_ld,
+                              cudaStream_t st);
+cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* NhT,
+                        int batch, int m, int n, int64_t ldm, int64_t ldn, float b1, float kappa,
+                        const float* scal, int scal_ld, const uint32_t* status, cudaStream_t st);
+cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
+                               int with_update, const uint32_t* status, cudaStream_t st);
+cudaError_t launch_normalise(const NormaliseArgs& A, int batch, cudaStream_t st);
+cudaError_t launch_sumsq(const float* S, int batch, int64_t dd, float* scal, int scal_ld, int slot,
+                         cudaStream_t st);
+cudaError_t launch_requant(const float* P, int batch, int d, __half* Ph, __half* PhT, __half* Pl, __half* PlT,
+                           int64_t ld16, int64_t mat16, float* scal, int scal_ld, int slot, cudaStream_t st);
+cudaError_t launch_reset_factor(float* S, float* P, __half* Ph, __half* PhT, __half* Pl, __half* PlT, int d,
+                                int64_t ld16, int64_t mat16, int batch, float eps, float* scal, int scal_ld,
+                                int pi_slot, cudaStream_t st);
+
+}  // namespace okls

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function the header declares, validates its arguments, and computes the
+same coefficient schedule as the oracle from the same definition."""
+
+import ctypes
+import os
+
+import numpy as np
+import pytest
+
+from kronecker_factored_second_gb300 import _lib as L
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        from kronecker_factored_second_gb300.build import build_library
+        build_library()
+    return L.lib()
+
+
+def test_library_exports_every_header_function(lib):
+    names = L.header_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(lib, name), name
+    assert lib.okls_abi_version() == 1
+
+
+def test_header_names_match_binding():
+    assert set(L.header_functions()) == set(L._SIGS)
+
+
+def test_config_defaults_are_readme_values(lib):
+    c = L.config_default(3, 128, 64)
+    assert (c.batch, c.m, c.n) == (3, 128, 64)
+    assert abs(c.lr_peak - 0.09434) < 1e-7 and abs(c.beta1 - 0.9684) < 1e-7
+    assert abs(c.beta2 - 0.9482) < 1e-7 and abs(c.eps - 1e-9) < 1e-15
+    assert abs(c.weight_decay - 0.0303) < 1e-7 and c.ns_iters == 10
+    assert c.variance_correction == 1 and c.eps_every_update == 1
+
+
+def test_state_bytes_layout(lib):
+    c = L.config_default(2, 128, 64)
+    sb, wb = L.state_bytes(c)
+    # M + S_a + S_b + P_a + P_b in fp32 (each block 256-byte aligned)
+    want = 4 * 2 * (128 * 64 + 2 * 128 * 128 + 2 * 64 * 64)
+    assert want <= sb <= want + 5 * 256
+    assert wb > 0
+    c.ns_split_iters = 3
+    _, wb3 = L.state_bytes(c)
+    assert wb3 > wb
+
+
+@pytest.mark.parametrize("field,value", [
+    ("batch", 0), ("m", 0), ("n", -1), ("beta1", 1.0), ("beta2", -0.1), ("eps", -1.0),
+    ("weight_decay", float("nan")), ("ns_iters", 1), ("ns_split_iters", 11), ("ns_lo", 0.0),
+    ("ridge", -1.0), ("lr_peak", 0.0), ("param_dtype", 7), ("m", 1 << 20)])
+def test_invalid_configs_rejected(lib, field, value):
+    c = L.config_default(1, 64, 32)
+    setattr(c, field, value)
+    s, w = ctypes.c_size_t(), ctypes.c_size_t()
+    code = lib.okls_state_bytes(ctypes.byref(c), ctypes.byref(s), ctypes.byref(w))
+    assert code in (L.OKLS_ERR_INVALID_ARG, L.OKLS_ERR_UNSUPPORTED)
+    assert L.last_error()
+
+
+def test_reserved_fields_must_be_zero(lib):
+    c = L.config_default(1, 64, 32)
+    c.reserved[3] = 1
+    assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_INVALID_ARG
+
+
+def test_null_arguments(lib):
+    assert lib.okls_state_bytes(None, None, None) == L.OKLS_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    c = L.config_default(1, 64, 32)
+    assert lib.okls_create(ctypes.byref(c), None, 0, None, 0, ctypes.byref(h)) == L.OKLS_ERR_INVALID_ARG
+    assert lib.okls_step(None, None, None, ctypes.c_float(0.1), None) == L.OKLS_ERR_INVALID_ARG
+    assert lib.okls_destroy(None) == L.OKLS_OK
+    assert lib.okls_ns_schedule(0, 1e-3, None, None, None) == L.OKLS_ERR_INVALID_ARG
+
+
+def test_schedule_matches_oracle_definition(lib):
+    """The library and the oracle derive the coefficients independently from
+    the same minimax definition; they must agree to rounding."""
+    import oracle as O
+    a, b, z = L.ns_schedule(10, 1e-3)
+    sch = O.cans_schedule(10, 1e-3)
+    assert np.allclose(a, [s[0] for s in sch], rtol=1e-13)
+    assert np.allclose(b, [s[1] for s in sch], rtol=1e-13)
+    assert z == O.ns_exponents(sch)
+    a1, b1, _ = L.ns_schedule(1, 1.0)
+    assert abs(a1[0] - 1.5) < 1e-15 and abs(b1[0] + 0.5) < 1e-15
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    c = L.config_default(1, 64, 32)
+    sb, wb = L.state_bytes(c)
+    buf = ctypes.create_string_buffer(sb + wb + 512)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    h = ctypes.c_void_p()
+    code = lib.okls_create(ctypes.byref(c), ctypes.c_void_p(base), sb, ctypes.c_void_p(base), wb,
+                           ctypes.byref(h))
+    assert code in (L.OKLS_ERR_NO_DEVICE, L.OKLS_ERR_CUDA)
+    assert not h.value
