@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Throughput of the OKLS step on one GB300 (or N replicas under torchrun).
+
+Metric: preconditioned matrices per second of okls_step (and dense TFLOP/s)
+on the 1.2B-shaped Llama layer set: 24 layers x {q,k,v,o 2048x2048;
+gate,up 5504x2048; down 2048x5504} = 168 matrices, bf16 W and G, fp32 state,
+Kronecker-structured gradients with condition number 1e3.  One step is one
+okls_step call per shape group over all 168 matrices.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl okls|reference]
+
+The JSON line carries the device-resident number (`value`), the end-to-end
+number through the public API with pinned host copies (`e2e`), the live
+per-launch roofline of the GEMM kernel (`roofline`), the float64 CPU oracle
+timed on a bounded sample (`cpu_baseline`) and the SM clocks seen during the
+timed region (`clocks`).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "preconditioned matrices/s per okls_step (TFLOP/s vs GB300 FP16 peak alongside)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def dense_flops(m: int, n: int) -> float:
+    """Dense algorithmic FLOPs of one matrix's step: 27 products of each
+    Newton-Schulz chain, the two factor products and the whitening."""
+    return 27 * 2.0 * (m ** 3 + n ** 3) + 4.0 * m * n * (m + n) + 2.0 * m * n * (m + n)
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- distributed
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_setup(ws: int, backend: str):
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """Largest value over ranks (the job's time is its slowest rank's)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU baseline
+def oracle_sample(seconds: float = 20.0, reps_max: int = 3) -> dict:
+    """The float64 oracle as it stands, one q/k/v/o-shaped (2048 x 2048)
+    matrix step per sample, repeated while within `seconds`."""
+    import numpy as np
+
+    import oracle as O
+    rng = np.random.default_rng(7)
+    m = n = 2048
+    hp = O.Hyper(ridge=1e-3)
+    st = O.init_state(m, n, hp)
+    W = rng.standard_normal((m, n)) * 1e-3
+    times = []
+    t_end = time.perf_counter() + seconds
+    for i in range(reps_max):
+        G = rng.standard_normal((m, n))
+        t0 = time.perf_counter()
+        st, W, _U = O.okls_step(st, W, G, hp.lr, hp)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end:
+            break
+    t = statistics.median(times)
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    return {"value": 1.0 / t, "unit": "matrices/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(times)} float64 oracle step(s) of one 2048x2048 q/k/v/o-shaped matrix "
+                      f"(eigendecomposition roots), median {t:.2f} s per matrix"}
+
+
+def run_reference(args):
+    """`--impl reference`: the float64 CPU oracle timed on the host cores on
+    a bounded sample of the same workload (one 2048x2048 matrix per step)."""
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle as O
+    rng = np.random.default_rng(11)
+    m = n = 2048
+    hp = O.Hyper(ridge=1e-3)
+    st = O.init_state(m, n, hp)
+    W = rng.standard_normal((m, n)) * 1e-3
+    Gs = [rng.standard_normal((m, n)) for _ in range(2)]
+    for i in range(args.warmup):
+        st, W, _ = O.okls_step(st, W, Gs[i % 2], hp.lr, hp)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        st, W, _ = O.okls_step(st, W, Gs[i % 2], hp.lr, hp)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    v = 1.0 / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "matrices/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama1.2b (bounded sample: one 2048x2048 q/k/v/o-shaped matrix per step)"},
+            "cpu_baseline": {"value": v, "unit": "matrices/s", "cores": cores, "kind": "oracle",
+                             "sample": "one float64 oracle step of one 2048x2048 matrix per timed step"},
+            "e2e": {"value": v, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm
+def run_okls(args):
+    import torch
+
+    from kronecker_factored_second_gb300.okls import OklsBatch
+    from kronecker_factored_second_gb300.workloads import GradientStream, workload
+
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_setup(ws, "nccl")
+    wl = workload(args.workload, layers=args.layers)
+    # every rank owns a full layer set of its own (weak scaling): seeds differ
+    wl.seed = wl.seed + 1000 * rank
+    gs = GradientStream(wl, dev)
+    n_distinct = max(2, min(wl.steps, args.distinct))
+    groups = []
+    for gi, g in enumerate(wl.groups):
+        ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=args.split, ridge=args.ridge,
+                       device=dev)
+        W = gs.init_weights(gi)
+        Gs = [gs.grad(gi, t + 1) for t in range(n_distinct)]
+        groups.append((g, ob, W, Gs))
+    del gs
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    matrices = wl.matrices
+    flops_step = sum(g.batch * dense_flops(g.m, g.n) for g in wl.groups)
+    in_bytes = sum(G[0].numel() * G[0].element_size() for (_g, _ob, _W, G) in groups)
+    state_bytes = sum(ob.state.numel() for (_g, ob, _W, _G) in groups)
+
+    def one_step(k):
+        for (g, ob, W, Gs) in groups:
+            ob.step(W, Gs[k % len(Gs)], args.lr)
+
+    for k in range(args.warmup):
+        one_step(k)
+    torch.cuda.synchronize()
+    for (_g, ob, _W, _G) in groups:
+        st = ob.status_nothrow()
+        if st[1]:
+            raise RuntimeError(f"device status 0x{st[1]:x} during warm-up")
+        ob.read_profile()
+        ob.profile(True)
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        gpu_uuid = None
+    clocks = ClockSampler(gpu_uuid) if rank == 0 else None
+    barrier(ws)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.5)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        one_step(args.warmup + k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    barrier(ws)
+    ms_total = e0.elapsed_time(e1)
+    ms_total = max_over_ranks(ms_total, ws, dev)
+    prof = {"kernel_launches": 0, "gemm_launches": 0, "gemm_flops": 0.0, "gemm_ms": 0.0, "ns_flops": 0.0,
+            "ns_ms": 0.0, "ns_launches": 0}
+    for (_g, ob, _W, _G) in groups:
+        p = ob.read_profile()
+        for k in prof:
+            prof[k] += p[k]
+        ob.profile(False)
+        st = ob.status_nothrow()
+        if st[1]:
+            raise RuntimeError(f"device status 0x{st[1]:x} in the timed region")
+    ms_step = ms_total / args.steps
+    total_matrices = sum_over_ranks(matrices * args.steps, ws, dev)
+    value = total_matrices / (ms_total / 1e3)
+    tflops = sum_over_ranks(flops_step * args.steps, ws, dev) / (ms_total / 1e3) / 1e12
+
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = prof["gemm_flops"] / (prof["gemm_ms"] / 1e3) / 1e12 if prof["gemm_ms"] > 0 else None
+    ns_achieved = prof["ns_flops"] / (prof["ns_ms"] / 1e3) / 1e12 if prof["ns_ms"] > 0 else None
+
+    # ---------------------------------------------- end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        hostG = []
+        for (g, ob, W, Gs) in groups:
+            hostG.append([Gs[i].cpu().pin_memory() for i in range(2)])
+        devG = [torch.empty_like(Gs[0]) for (_g, _ob, _W, Gs) in groups]
+        hostW = [torch.empty(W.shape, dtype=W.dtype, pin_memory=True) for (_g, _ob, W, _G) in groups]
+        h2d = sum(h[0].numel() * h[0].element_size() for h in hostG)
+        d2h = sum(h.numel() * h.element_size() for h in hostW)
+
+        def e2e_step(k):
+            for i, (g, ob, W, _Gs) in enumerate(groups):
+                devG[i].copy_(hostG[i][k % 2], non_blocking=True)
+                ob.step(W, devG[i], args.lr)
+                hostW[i].copy_(W, non_blocking=True)
+
+        for k in range(max(1, args.warmup // 2)):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(args.steps):
+            e2e_step(k)
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ms_e2e = max_over_ranks(a.elapsed_time(b), ws, dev)
+        e2e = {"value": sum_over_ranks(matrices * args.steps, ws, dev) / (ms_e2e / 1e3), "unit": "matrices/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e / args.steps}
+        del hostG, devG, hostW
+
+    # ------------------------------------------------ second precision mode
+    split_line = None
+    if args.also_split and args.split == 0:
+        torch.cuda.synchronize()
+        for i in range(len(groups)):
+            g, ob, W, Gs = groups[i]
+            ob.close()
+            groups[i] = (g, None, W, Gs)
+            del ob
+            torch.cuda.empty_cache()
+            groups[i] = (g, OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=3, ridge=1e-4,
+                                      device=dev), W, Gs)
+        for k in range(args.warmup):
+            one_step(k)
+        torch.cuda.synchronize()
+        for (_g, ob, _W, _G) in groups:
+            ob.read_profile()
+            ob.profile(True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(args.steps):
+            one_step(k)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms2 = max_over_ranks(a.elapsed_time(b), ws, dev)
+        gf, gm = 0.0, 0.0
+        for (_g, ob, _W, _G) in groups:
+            p = ob.read_profile()
+            gf += p["gemm_flops"]
+            gm += p["gemm_ms"]
+        split_line = {"mode": "iterations 0-2 split (hi/lo binary16), ridge 1e-4, 41 NS products per factor",
+                      "value": sum_over_ranks(matrices * args.steps, ws, dev) / (ms2 / 1e3),
+                      "unit": "matrices/s", "ms_per_step": ms2 / args.steps,
+                      "tflops_dense_27": sum_over_ranks(flops_step * args.steps, ws, dev) / (ms2 / 1e3) / 1e12,
+                      "gemm_tflops_executed": gf / (gm / 1e3) / 1e12 if gm > 0 else None}
+
+    cpu = None
+    if rank == 0 and ws >= 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+            "config": {
+                "workload": (f"{args.workload}: " + ", ".join(f"{g.batch} x {g.m}x{g.n} {g.name}" for g in wl.groups)
+                             + f" = {matrices} matrices, {wl.groups[0].dtype} W and G, fp32 state, "
+                             f"{wl.recipe} gradients (condition number {wl.cond:g})"),
+                "precision": f"binary16 Newton-Schulz operands, fp32 accumulation, split_iters={args.split}, "
+                             f"ridge={args.ridge:g}",
+                "l2": f"inputs larger than L2: {in_bytes / 1e9:.2f} GB of gradients and "
+                      f"{state_bytes / 1e9:.1f} GB of state per step",
+                "parallelism": f"owner-computes replicas x{ws} (each rank a full layer set)"},
+            "tflops": tflops,
+            "tflops_frac_of_peak": tflops / peak,
+            "roofline": {"bound": "tensor", "kernel": "okls_gemm_kernel (tcgen05, all products of the step)",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "peak_kind": f"{peak_kind} bf16 sustained (fp16 nominal ratio 1)",
+                         "launches": prof["gemm_launches"], "ms_per_launch": prof["gemm_ms"] / max(1, prof["gemm_launches"]),
+                         "ns_chain_tflops": ns_achieved,
+                         "ns_chain_frac": (ns_achieved / peak) if ns_achieved else None},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": prof["kernel_launches"],
+            "clocks": clk,
+        }
+        if split_line:
+            line["split_mode"] = split_line
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["okls", "reference"], default="okls")
+    ap.add_argument("--workload", default="llama1.2b")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling cases)")
+    ap.add_argument("--split", type=int, default=0)
+    ap.add_argument("--ridge", type=float, default=1e-3)
+    ap.add_argument("--lr", type=float, default=0.09434)
+    ap.add_argument("--distinct", type=int, default=4, help="distinct gradient batches kept on the device")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--also-split", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "okls":
+        print("note: at least 3 warm-up steps are used", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_okls(args)
+
+
+if __name__ == "__main__":
+    main()

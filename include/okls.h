@@ -188,6 +188,28 @@ okls_status okls_set_step(okls_handle h, int64_t t);
 okls_status okls_destroy(okls_handle h);
 
 /*
+ * Launch accounting of okls_step, for measurement.  Kernel launches are
+ * always counted; with timing enabled (okls_profile_enable(h, 1)) every GEMM
+ * launch is bracketed by two CUDA events recorded on the step's stream.
+ * okls_profile_read synchronises on those events, returns the sums since the
+ * previous read and resets them.  FLOPs are algorithmic: 2 M N K per K
+ * segment for dense products, M (M+1) K for the symmetric factor products.
+ */
+typedef struct okls_profile {
+  int64_t kernel_launches; /* all library kernels                         */
+  int64_t gemm_launches;   /* tcgen05 GEMM launches among them              */
+  double gemm_flops;
+  double gemm_ms;          /* summed event time of the timed GEMM launches */
+  int64_t timed_launches;
+  int64_t ns_launches;     /* the Newton-Schulz subset of the GEMMs         */
+  double ns_flops;
+  double ns_ms;
+} okls_profile;
+
+okls_status okls_profile_enable(okls_handle h, int32_t timing);
+okls_status okls_profile_read(okls_handle h, okls_profile *out);
+
+/*
  * Coefficient schedule the library uses (host computation, no GPU needed):
  * for k < iters, a[k], b[k] of T_k = a_k I + b_k Z_k Y_k, the minimax odd
  * cubic on [l_k, u_k] (l_0 = lo, u_0 = 1), and for k <= iters the exponent

@@ -56,6 +56,19 @@ class okls_config(ctypes.Structure):
     ]
 
 
+class okls_profile(ctypes.Structure):
+    _fields_ = [
+        ("kernel_launches", ctypes.c_int64),
+        ("gemm_launches", ctypes.c_int64),
+        ("gemm_flops", ctypes.c_double),
+        ("gemm_ms", ctypes.c_double),
+        ("timed_launches", ctypes.c_int64),
+        ("ns_launches", ctypes.c_int64),
+        ("ns_flops", ctypes.c_double),
+        ("ns_ms", ctypes.c_double),
+    ]
+
+
 class OklsError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"okls error {code}: {msg}")
@@ -84,6 +97,8 @@ _SIGS = {
     "okls_get_step": (_I32, [_P, ctypes.POINTER(_I64)]),
     "okls_set_step": (_I32, [_P, _I64]),
     "okls_destroy": (_I32, [_P]),
+    "okls_profile_enable": (_I32, [_P, _I32]),
+    "okls_profile_read": (_I32, [_P, ctypes.POINTER(okls_profile)]),
     "okls_ns_schedule": (_I32, [_I32, ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                                 ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I32)]),
     "okls_inv_root_workspace_bytes": (_I32, [_I64, _I64, _I32, _I32, ctypes.POINTER(_SZ)]),

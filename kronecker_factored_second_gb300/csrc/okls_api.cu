@@ -231,6 +231,49 @@ okls_status device_sms(int* out) {
   return OKLS_OK;
 }
 
+// ------------------------------------------------------------ profiling
+// Counts every kernel a step launches; with timing on, brackets each GEMM
+// launch with CUDA events on the launching stream and records its
+// algorithmic FLOPs (dense: 2 M N K per segment; symmetric: M (M+1) K, the
+// upper triangle only).
+struct Prof {
+  bool timing = false;
+  struct Rec {
+    cudaEvent_t a, b;
+    double flops;
+    bool ns;
+  };
+  std::vector<cudaEvent_t> pool;
+  size_t used = 0;
+  std::vector<Rec> recs;
+  int64_t kernels = 0, gemm_launches = 0, ns_launches = 0;
+  double gemm_flops = 0.0, ns_flops = 0.0;
+
+  cudaEvent_t next_event() {
+    if (used == pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      pool.push_back(e);
+    }
+    return pool[used++];
+  }
+  ~Prof() {
+    for (cudaEvent_t e : pool) cudaEventDestroy(e);
+  }
+};
+
+thread_local Prof* g_prof = nullptr;  // set for the duration of okls_step
+thread_local bool g_in_ns = false;
+
+void note_kernels(int n) {
+  if (g_prof) g_prof->kernels += n;
+}
+
+struct ProfScope {
+  explicit ProfScope(Prof* p) { g_prof = p; }
+  ~ProfScope() { g_prof = nullptr; }
+};
+
 // ------------------------------------------------------------ GEMM launches
 // Output buffers must cover the problem's rows x cols (and cols x rows for the
 // transposed copy, which shares the pitch); a violation is a planning bug.
@@ -320,7 +363,35 @@ struct LaunchBuilder {
     L.total_tiles = t;
     L.maps = maps;
     L.status = status;
+    Prof* pf = g_prof;
+    double flops = 0.0;
+    for (int i = 0; i < L.nprob; ++i) {
+      const GemmProblem& p = L.prob[i];
+      const double mn = p.sym ? static_cast<double>(p.rows) * (p.rows + 1) * 0.5 : static_cast<double>(p.rows) * p.cols;
+      flops += 2.0 * mn * p.K * p.batch * p.nseg;
+    }
+    cudaEvent_t ea = nullptr, eb = nullptr;
+    if (pf && pf->timing) {
+      ea = pf->next_event();
+      eb = pf->next_event();
+      if (ea) OKLS_CK(cudaEventRecord(ea, st));
+    }
     OKLS_CK(launch_gemm(L, sms, st));
+    if (pf) {
+      if (ea && eb) {
+        OKLS_CK(cudaEventRecord(eb, st));
+        pf->recs.push_back({ea, eb, flops, g_in_ns});
+      }
+      if (L.total_tiles > 0) {
+        pf->kernels += 1;
+        pf->gemm_launches += 1;
+        pf->gemm_flops += flops;
+        if (g_in_ns) {
+          pf->ns_launches += 1;
+          pf->ns_flops += flops;
+        }
+      }
+    }
     return OKLS_OK;
   }
 };
@@ -365,9 +436,22 @@ okls_status trace_copy(const TraceOut& tr, int slice, const Buf* b, cudaStream_t
 
 // Normalisation and the coupled Newton-Schulz chain for 1 or 2 factors.
 // The stable order is kept: M_k = Z_k Y_k, Y_{k+1} = Y_k T_k, Z_{k+1} = T_k Z_k.
+okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
+                        int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
+                        const TraceOut* tr);
+
 okls_status run_ns(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
                    int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
                    const TraceOut* tr) {
+  g_in_ns = true;
+  okls_status s = run_ns_body(fs, nf, sc, split, ridge, scal, scal_ld, maps, status, sms, st, tr);
+  g_in_ns = false;
+  return s;
+}
+
+okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
+                        int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
+                        const TraceOut* tr) {
   const int K = sc.iters;
   const int h = kHeadroom;
   for (int q = 0; q < nf; ++q) {
@@ -407,6 +491,7 @@ okls_status run_ns(Factor* const* fs, int nf, const Sched& sc, int split, float 
     A.slot_sumsq = f.slot_sumsq;
     A.status = status;
     OKLS_CK(launch_normalise(A, f.batch, st));
+    note_kernels(1);
   }
   if (tr && tr->base) {
     okls_status s;
@@ -503,6 +588,7 @@ struct okls_handle_s {
   uint32_t* status = nullptr;
   CUtensorMap* maps = nullptr;
   int64_t t = 0;
+  Prof prof;
 };
 
 namespace {
@@ -709,6 +795,8 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
   const int gbf = c.grad_dtype == OKLS_BF16;
   const int h12 = kHeadroom;
   okls_status s;
+  ProfScope scope(&h->prof);
+  note_kernels(4);  // momentum statistics, coefficients (2), pack
 
   // 1-2. momentum, statistics, packed binary16 operands
   OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(4 * B * 4), st));  // SC_SUMSQ_* slots
@@ -867,6 +955,36 @@ okls_status okls_set_step(okls_handle h, int64_t t) {
 
 okls_status okls_destroy(okls_handle h) {
   delete h;
+  return OKLS_OK;
+}
+
+okls_status okls_profile_enable(okls_handle h, int32_t timing) {
+  if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
+  h->prof.timing = timing != 0;
+  return OKLS_OK;
+}
+
+okls_status okls_profile_read(okls_handle h, okls_profile* out) {
+  if (!h || !out) return fail(OKLS_ERR_INVALID_ARG, "handle or out is NULL");
+  Prof& p = h->prof;
+  memset(out, 0, sizeof(*out));
+  out->kernel_launches = p.kernels;
+  out->gemm_launches = p.gemm_launches;
+  out->gemm_flops = p.gemm_flops;
+  out->ns_launches = p.ns_launches;
+  out->ns_flops = p.ns_flops;
+  for (const Prof::Rec& r : p.recs) {
+    OKLS_CK(cudaEventSynchronize(r.b));
+    float ms = 0.0f;
+    OKLS_CK(cudaEventElapsedTime(&ms, r.a, r.b));
+    out->gemm_ms += ms;
+    if (r.ns) out->ns_ms += ms;
+    out->timed_launches += 1;
+  }
+  p.recs.clear();
+  p.used = 0;
+  p.kernels = p.gemm_launches = p.ns_launches = 0;
+  p.gemm_flops = p.ns_flops = 0.0;
   return OKLS_OK;
 }
 

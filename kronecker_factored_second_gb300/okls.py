@@ -138,6 +138,17 @@ class OklsBatch:
     def t(self, value: int):
         L.check(L.lib().okls_set_step(self._h, int(value)))
 
+    def profile(self, timing: bool = True):
+        """Enable event timing of the GEMM launches of later steps."""
+        L.check(L.lib().okls_profile_enable(self._h, int(timing)))
+
+    def read_profile(self) -> dict:
+        """Launch counts, algorithmic FLOPs and event time since the last
+        read (synchronises on the recorded events)."""
+        p = L.okls_profile()
+        L.check(L.lib().okls_profile_read(self._h, ctypes.byref(p)))
+        return {k: getattr(p, k) for k, _ in L.okls_profile._fields_}
+
     def state_dict(self) -> dict:
         return {"t": self.t, **{k: self.get_state(p).cpu() for k, p in
                                 [("M", L.STATE_M), ("Sa", L.STATE_SA), ("Sb", L.STATE_SB),
