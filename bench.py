@@ -42,6 +42,34 @@ def dense_flops(m: int, n: int) -> float:
     return 27 * 2.0 * (m ** 3 + n ** 3) + 4.0 * m * n * (m + n) + 2.0 * m * n * (m + n)
 
 
+GEMM_SOURCES = ["kronecker_factored_second_gb300/csrc/okls_gemm.cu",
+                "kronecker_factored_second_gb300/csrc/okls_ptx.cuh",
+                "kronecker_factored_second_gb300/csrc/okls_internal.h"]
+TRAFFIC_PROFILE = "profiles/okls_gemm_kernel__llama1.2b_dram_per_launch.md"
+
+
+def gemm_traffic() -> float | None:
+    """DRAM bytes per GEMM launch from the committed ncu summary, or None
+    when the kernel sources changed since those counters were taken."""
+    import hashlib
+    try:
+        h = hashlib.sha256()
+        for f in GEMM_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        rec = {}
+        with open(os.path.join(ROOT, TRAFFIC_PROFILE)) as fh:
+            for line in fh:
+                if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch", "source_sha256"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("source_sha256") != h.hexdigest():
+            return None
+        return float(rec["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks() -> tuple[dict, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -393,7 +421,8 @@ def run_okls(args):
             "tflops_frac_of_peak": tflops / peak,
             "roofline": {"bound": "tensor", "kernel": "okls_gemm_kernel (tcgen05, all products of the step)",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "frac": (achieved / peak) if achieved else None, "traffic": gemm_traffic(),
+                         "traffic_unit": "bytes per launch (dram read + write, ncu, full-size step)",
                          "peak_kind": f"{peak_kind} bf16 sustained (fp16 nominal ratio 1)",
                          "launches": prof["gemm_launches"], "ms_per_launch": prof["gemm_ms"] / max(1, prof["gemm_launches"]),
                          "ns_chain_tflops": ns_achieved,
