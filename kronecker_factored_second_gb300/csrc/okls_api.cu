@@ -110,6 +110,22 @@ constexpr size_t kMapTableBytes = kMaxMaps * sizeof(CUtensorMap);
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
+// tiles of a symmetric (upper-triangle) d x d product: row block tm holds
+// column blocks floor(tm/2) .. tiles_n-1
+int64_t sym_tiles(int64_t d) {
+  const int64_t tm_n = (d + kBM - 1) / kBM, tn_n = (d + kBN - 1) / kBN;
+  int64_t c = 0;
+  for (int64_t tm = 0; tm < tm_n; ++tm) c += tn_n - tm / 2;
+  return c;
+}
+
+// fixed partial slots per matrix for ||S||_F^2 (SYRK tiles x 4 warps, or the
+// blocks of the standalone reduction)
+int64_t factor_parts(int64_t d) {
+  const int64_t a = 4 * sym_tiles(d), b = sumsq_parts(d * d);
+  return a > b ? a : b;
+}
+
 // A batch of binary16 matrices (rows x cols, row pitch ld) with two TMA
 // descriptors: box 128 rows (A operand) and box 256 rows (B operand).
 struct Buf {
@@ -587,6 +603,8 @@ struct okls_handle_s {
   float* scal = nullptr;
   uint32_t* status = nullptr;
   CUtensorMap* maps = nullptr;
+  float *part_g = nullptr, *part_a = nullptr, *part_b = nullptr;  // fixed-slot partial sums
+  int64_t part_g_ld = 0, part_a_ld = 0, part_b_ld = 0;
   int64_t t = 0;
   Prof prof;
 };
@@ -612,6 +630,10 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
   CUtensorMap* maps = static_cast<CUtensorMap*>(wp.take(kMapTableBytes, 128));
   float* scal = static_cast<float*>(wp.take(static_cast<size_t>(SC_COUNT * B * 4)));
   uint32_t* status = static_cast<uint32_t*>(wp.take(256));
+  const int64_t pg_ld = kMaxStatParts, pa_ld = factor_parts(m), pb_ld = factor_parts(n);
+  float* part_g = static_cast<float*>(wp.take(static_cast<size_t>(2 * B * pg_ld * 4)));
+  float* part_a = static_cast<float*>(wp.take(static_cast<size_t>(B * pa_ld * 4)));
+  float* part_b = static_cast<float*>(wp.take(static_cast<size_t>(B * pb_ld * 4)));
   Buf Gh = wp.buf16(m, n, B), GhT = wp.buf16(n, m, B), NhT = wp.buf16(n, m, B);
   Buf Xb = wp.buf16(m, n, B), XaT = wp.buf16(n, m, B);
   Factor fa, fb;
@@ -651,6 +673,12 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
     h->scal = scal;
     h->status = status;
     h->maps = maps;
+    h->part_g = part_g;
+    h->part_a = part_a;
+    h->part_b = part_b;
+    h->part_g_ld = pg_ld;
+    h->part_a_ld = pa_ld;
+    h->part_b_ld = pb_ld;
     // upload the descriptor table once
     if (!wp.maps.empty()) {
       cudaError_t e = cudaMemcpy(maps, wp.maps.data(), wp.maps.size() * sizeof(CUtensorMap),
@@ -800,9 +828,9 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
 
   // 1-2. momentum, statistics, packed binary16 operands
   OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(4 * B * 4), st));  // SC_SUMSQ_* slots
-  OKLS_CK(launch_momentum_stats(G, gbf, h->M, B, static_cast<int64_t>(m) * n, c.beta1, kappa, h->scal, sld,
-                                h->status, st));
-  OKLS_CK(launch_coeffs_pre(B, m, n, c.beta2, h->scal, sld, st));
+  OKLS_CK(launch_momentum_stats(G, gbf, h->M, B, static_cast<int64_t>(m) * n, c.beta1, kappa, h->part_g,
+                                h->part_g_ld, h->status, st));
+  OKLS_CK(launch_coeffs_pre(B, m, n, c.beta2, h->scal, sld, h->part_g, h->part_g_ld, st));
   // row pitches: Ghat is m x n (pitch ldn), Ghat^T and Nhat^T are n x m (pitch ldm)
   if (h->Gh.ld < n || h->GhT.ld < m || h->NhT.ld != h->GhT.ld || h->Gh.rows != m || h->GhT.rows != n)
     return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: packed operand pitches");
@@ -832,7 +860,8 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
     pa.scal = h->scal;
     pa.scal_ld = sld;
     pa.scal_slot = SC_ALPHA_SA;
-    pa.sum_slot = SC_SUMSQ_SA;
+    pa.part = h->part_a;
+    pa.part_ld = h->part_a_ld;
     pa.beta = c.beta2;
     pa.gamma = eps_u;
     GemmProblem& pb = lb.add(&h->XaT, &h->XaT, false, n, n, m, B, EPI_SYRK, true);
@@ -842,14 +871,16 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
     pb.scal = h->scal;
     pb.scal_ld = sld;
     pb.scal_slot = SC_ALPHA_SB;
-    pb.sum_slot = SC_SUMSQ_SB;
+    pb.part = h->part_b;
+    pb.part_ld = h->part_b_ld;
     pb.beta = c.beta2;
     pb.gamma = eps_u;
     if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
   }
   // 5-6. fresh inverse roots of both factors
   const int K = h->sched.iters;
-  OKLS_CK(launch_coeffs_post(B, c.ridge, h->sched.z[K], h->sched.z[K - 1], h->scal, sld, 1, h->status, st));
+  OKLS_CK(launch_coeffs_post(B, c.ridge, h->sched.z[K], h->sched.z[K - 1], h->scal, sld, 1, h->status, h->part_a,
+                             h->part_a_ld, 4 * sym_tiles(m), h->part_b, h->part_b_ld, 4 * sym_tiles(n), st));
   {
     Factor* fs[2] = {&h->fa, &h->fb};
     if ((s = run_ns(fs, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
@@ -1003,12 +1034,14 @@ okls_status okls_ns_schedule(int32_t iters, double lo, double* a, double* b, int
 
 // ------------------------------------------------------------ inverse roots
 static okls_status inv_plan(int64_t d, int64_t count, int32_t split, uint8_t* ws, Factor* f, float** scal,
-                            uint32_t** status, CUtensorMap** maps, size_t* bytes, std::vector<CUtensorMap>* mv) {
+                            uint32_t** status, CUtensorMap** maps, size_t* bytes, std::vector<CUtensorMap>* mv,
+                            float** part) {
   Planner wp;
   wp.base = ws;
   *maps = static_cast<CUtensorMap*>(wp.take(kMapTableBytes, 128));
   *scal = static_cast<float*>(wp.take(static_cast<size_t>(SC_COUNT * count * 4)));
   *status = static_cast<uint32_t*>(wp.take(256));
+  *part = static_cast<float*>(wp.take(static_cast<size_t>(count * factor_parts(d) * 4)));
   plan_factor(wp, *f, static_cast<int>(d), static_cast<int>(count), split > 0);
   if (wp.err != OKLS_OK) return wp.err;
   *bytes = wp.off;
@@ -1025,7 +1058,8 @@ okls_status okls_inv_root_workspace_bytes(int64_t d, int64_t count, int32_t iter
   float* scal;
   uint32_t* status;
   CUtensorMap* maps;
-  return inv_plan(d, count, split_iters, nullptr, &f, &scal, &status, &maps, workspace_bytes, nullptr);
+  float* part;
+  return inv_plan(d, count, split_iters, nullptr, &f, &scal, &status, &maps, workspace_bytes, nullptr, &part);
 }
 
 okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace, int64_t d, int64_t count,
@@ -1044,9 +1078,10 @@ okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace
   float* scal;
   uint32_t* status;
   CUtensorMap* maps;
+  float* part;
   std::vector<CUtensorMap> mv;
-  if ((s = inv_plan(d, count, split_iters, static_cast<uint8_t*>(ws), &f, &scal, &status, &maps, &need, &mv)) !=
-      OKLS_OK)
+  if ((s = inv_plan(d, count, split_iters, static_cast<uint8_t*>(ws), &f, &scal, &status, &maps, &need, &mv,
+                    &part)) != OKLS_OK)
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   OKLS_CK(cudaMemcpyAsync(maps, mv.data(), mv.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice, st));
@@ -1061,9 +1096,10 @@ okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace
   f.slot_pscale = SC_PSCALE_A;
   f.slot_rscale = SC_RSCALE_A;
   const Sched sc = make_schedule(iters, lo);
-  OKLS_CK(launch_sumsq(S, static_cast<int>(count), d * d, scal, static_cast<int>(count), SC_SUMSQ_SA, st));
+  OKLS_CK(launch_sumsq(S, static_cast<int>(count), d * d, part, factor_parts(d), st));
   OKLS_CK(launch_coeffs_post(static_cast<int>(count), ridge, sc.z[iters], sc.z[iters - 1], scal,
-                             static_cast<int>(count), 0, status, st));
+                             static_cast<int>(count), 0, status, part, factor_parts(d), sumsq_parts(d * d),
+                             nullptr, 0, 0, st));
   TraceOut tr;
   tr.base = trace;
   tr.count = count;

@@ -48,8 +48,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // ------------------------------------------------------------ momentum stats
 template <typename GT>
 __global__ void k_momentum_stats(const GT* __restrict__ G, const float* __restrict__ M,
-                                 int64_t mn, float b1, float kappa, float* scal, int scal_ld,
-                                 uint32_t* status) {
+                                 int64_t mn, float b1, float kappa, float* part, int64_t part_ld,
+                                 int batch, uint32_t* status) {
   __shared__ float red[32];
   const int b = blockIdx.y;
   const GT* g = G + static_cast<int64_t>(b) * mn;
@@ -69,10 +69,18 @@ __global__ void k_momentum_stats(const GT* __restrict__ G, const float* __restri
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, kStNonfiniteInput);
   const float tg = block_sum(sg, red);
   const float tn = block_sum(sn, red);
+  // per-block partials in fixed slots: [0: G, 1: N][batch][block]
   if (threadIdx.x == 0) {
-    atomicAdd(scal + static_cast<int64_t>(SC_SUMSQ_G) * scal_ld + b, tg);
-    atomicAdd(scal + static_cast<int64_t>(SC_SUMSQ_N) * scal_ld + b, tn);
+    part[static_cast<int64_t>(b) * part_ld + blockIdx.x] = tg;
+    part[(static_cast<int64_t>(batch) + b) * part_ld + blockIdx.x] = tn;
   }
+}
+
+// fixed-order double sum of n partials
+__device__ __forceinline__ double sum_parts(const float* p, int64_t n) {
+  double s = 0.0;
+  for (int64_t i = 0; i < n; ++i) s += static_cast<double>(p[i]);
+  return s;
 }
 
 // power of two 2^e with rms * 2^e in [1, 2); 1 for an all-zero matrix
@@ -85,10 +93,12 @@ __device__ __forceinline__ float pow2_rms_scale(float sumsq, double count) {
 }
 
 __global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal,
-                             int scal_ld) {
+                             int scal_ld, const float* part, int64_t part_ld, int nparts) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   auto S = [&](int slot) -> float& { return scal[static_cast<int64_t>(slot) * scal_ld + b]; };
+  S(SC_SUMSQ_G) = static_cast<float>(sum_parts(part + static_cast<int64_t>(b) * part_ld, nparts));
+  S(SC_SUMSQ_N) = static_cast<float>(sum_parts(part + (static_cast<int64_t>(batch) + b) * part_ld, nparts));
   const double cnt = static_cast<double>(m) * static_cast<double>(n);
   const float gs = pow2_rms_scale(S(SC_SUMSQ_G), cnt);
   const float ns = pow2_rms_scale(S(SC_SUMSQ_N), cnt);
@@ -148,12 +158,17 @@ __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* 
 
 // -------------------------------------------------------------- post scalars
 __global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                              int with_update, const uint32_t* status) {
+                              int with_update, const uint32_t* status, const float* part_a,
+                              int64_t part_a_ld, int64_t npart_a, const float* part_b, int64_t part_b_ld,
+                              int64_t npart_b) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   // a failed stage leaves the previous roots (and their scales) in force
   if (*reinterpret_cast<const volatile uint32_t*>(status) != 0u) return;
   auto S = [&](int slot) -> float& { return scal[static_cast<int64_t>(slot) * scal_ld + b]; };
+  // ||S||_F^2 of both factors from their fixed partial slots
+  if (part_a) S(SC_SUMSQ_SA) = static_cast<float>(sum_parts(part_a + b * part_a_ld, npart_a));
+  if (part_b) S(SC_SUMSQ_SB) = static_cast<float>(sum_parts(part_b + b * part_b_ld, npart_b));
   const double margin = 1.0 + ldexp(1.0, -8);
   const int h = kHeadroom;
   for (int f = 0; f < 2; ++f) {
@@ -239,7 +254,7 @@ __global__ void k_normalise(NormaliseArgs A) {
 }
 
 // ------------------------------------------------------------- small helpers
-__global__ void k_sumsq(const float* __restrict__ S, int64_t dd, float* scal, int scal_ld, int slot) {
+__global__ void k_sumsq(const float* __restrict__ S, int64_t dd, float* part, int64_t part_ld) {
   __shared__ float red[32];
   const int b = blockIdx.y;
   const float* s = S + static_cast<int64_t>(b) * dd;
@@ -248,7 +263,7 @@ __global__ void k_sumsq(const float* __restrict__ S, int64_t dd, float* scal, in
        e += static_cast<int64_t>(gridDim.x) * blockDim.x)
     acc = fmaf(s[e], s[e], acc);
   const float t = block_sum(acc, red);
-  if (threadIdx.x == 0) atomicAdd(scal + static_cast<int64_t>(slot) * scal_ld + b, t);
+  if (threadIdx.x == 0) part[static_cast<int64_t>(b) * part_ld + blockIdx.x] = t;
 }
 
 __global__ void k_amax(const float* __restrict__ P, int64_t dd, float* scal, int scal_ld, int slot) {
@@ -354,23 +369,27 @@ static int grid_for(int64_t n, int per_block, int cap) {
   return static_cast<int>(g);
 }
 
+int momentum_parts(int64_t mn) { return grid_for(mn, 256 * 8, kMaxStatParts); }
+
 cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int batch, int64_t mn,
-                                  float b1, float kappa, float* scal, int scal_ld, uint32_t* status,
+                                  float b1, float kappa, float* part, int64_t part_ld, uint32_t* status,
                                   cudaStream_t st) {
-  const int per_mat = grid_for(mn, 256 * 8, 4096);
+  const int per_mat = momentum_parts(mn);
+  if (per_mat > part_ld) return cudaErrorInvalidValue;
   dim3 grid(per_mat, batch);
   if (g_bf16)
     k_momentum_stats<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(G), M, mn,
-                                                          b1, kappa, scal, scal_ld, status);
+                                                          b1, kappa, part, part_ld, batch, status);
   else
-    k_momentum_stats<float><<<grid, 256, 0, st>>>(static_cast<const float*>(G), M, mn, b1, kappa, scal,
-                                                  scal_ld, status);
+    k_momentum_stats<float><<<grid, 256, 0, st>>>(static_cast<const float*>(G), M, mn, b1, kappa, part,
+                                                  part_ld, batch, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal, int scal_ld,
-                              cudaStream_t st) {
-  k_coeffs_pre<<<(batch + 127) / 128, 128, 0, st>>>(batch, m, n, beta2, scal, scal_ld);
+                              const float* part, int64_t part_ld, cudaStream_t st) {
+  k_coeffs_pre<<<(batch + 127) / 128, 128, 0, st>>>(batch, m, n, beta2, scal, scal_ld, part, part_ld,
+                                                    momentum_parts(m * n));
   return cudaGetLastError();
 }
 
@@ -388,9 +407,12 @@ cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half*
 }
 
 cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                               int with_update, const uint32_t* status, cudaStream_t st) {
+                               int with_update, const uint32_t* status, const float* part_a, int64_t part_a_ld,
+                               int64_t npart_a, const float* part_b, int64_t part_b_ld, int64_t npart_b,
+                               cudaStream_t st) {
   k_coeffs_post<<<(batch + 127) / 128, 128, 0, st>>>(batch, ridge, zK, zK1, scal, scal_ld, with_update,
-                                                     status);
+                                                     status, part_a, part_a_ld, npart_a, part_b, part_b_ld,
+                                                     npart_b);
   return cudaGetLastError();
 }
 
@@ -400,10 +422,13 @@ cudaError_t launch_normalise(const NormaliseArgs& A, int batch, cudaStream_t st)
   return cudaGetLastError();
 }
 
-cudaError_t launch_sumsq(const float* S, int batch, int64_t dd, float* scal, int scal_ld, int slot,
-                         cudaStream_t st) {
-  dim3 grid(grid_for(dd, 256 * 8, 1024), batch);
-  k_sumsq<<<grid, 256, 0, st>>>(S, dd, scal, scal_ld, slot);
+int sumsq_parts(int64_t dd) { return grid_for(dd, 256 * 8, kMaxStatParts); }
+
+cudaError_t launch_sumsq(const float* S, int batch, int64_t dd, float* part, int64_t part_ld, cudaStream_t st) {
+  const int per_mat = sumsq_parts(dd);
+  if (per_mat > part_ld) return cudaErrorInvalidValue;
+  dim3 grid(per_mat, batch);
+  k_sumsq<<<grid, 256, 0, st>>>(S, dd, part, part_ld);
   return cudaGetLastError();
 }
 

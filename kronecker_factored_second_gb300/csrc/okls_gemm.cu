@@ -30,6 +30,7 @@ namespace okls {
 
 struct TileCoord {
   int p, mat, tm, tn;
+  int64_t lt;  // tile index within its matrix
 };
 
 __device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t) {
@@ -41,6 +42,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t)
   c.p = p;
   c.mat = static_cast<int>(local / P.tiles_per_mat);
   int64_t r = local - static_cast<int64_t>(c.mat) * P.tiles_per_mat;
+  c.lt = r;
   if (P.sym) {
     // row block tm holds col blocks floor(tm/2) .. tiles_n-1 (BN = 2 BM)
     int tm = 0;
@@ -381,10 +383,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         epilogue_chunk(P, tc, i, tc.tn * kBN + c * 32, v, flags, sumsq);
       }
       if (P.epi == EPI_SYRK) {
+        // one partial per (tile, epilogue warp) in a fixed slot: the sum over
+        // slots is taken later in a fixed order, so ||S||_F is reproducible
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, o);
-        if (lane == 0 && sumsq != 0.0f)
-          atomicAdd(P.scal + static_cast<int64_t>(P.sum_slot) * P.scal_ld + tc.mat, sumsq);
+        if (lane == 0) P.part[static_cast<int64_t>(tc.mat) * P.part_ld + tc.lt * 4 + q] = sumsq;
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);

@@ -92,7 +92,8 @@ struct GemmProblem {
   float* scal;                  // per-matrix scalar table base [SC_COUNT][scal_ld]
   int32_t scal_ld;              // matrices per slot row of the table
   int32_t scal_slot;            // slot read by this epilogue (alpha_b, pscale, coef)
-  int32_t sum_slot;             // slot accumulated (EPI_SYRK)
+  float* part;                  // EPI_SYRK: per-(tile, warp) partial sums of S^2
+  int64_t part_ld;              // partial slots per matrix (>= 4 * tiles_per_mat)
   float alpha, beta, gamma, delta;  // kind-specific constants
   int32_t split_out;            // 1: also write lo halves
   int32_t check_finite;         // 1: raise kStNonfiniteIter on non-finite acc

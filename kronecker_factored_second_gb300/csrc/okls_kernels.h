@@ -27,19 +27,26 @@ struct NormaliseArgs {
 
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 
+// Reductions are deterministic: kernels write per-block (or per-tile) partials
+// into fixed slots and a single thread per matrix sums them in order.
+constexpr int kMaxStatParts = 1024;
+int momentum_parts(int64_t mn);
+int sumsq_parts(int64_t dd);
+
 cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int batch, int64_t mn,
-                                  float b1, float kappa, float* scal, int scal_ld, uint32_t* status,
+                                  float b1, float kappa, float* part, int64_t part_ld, uint32_t* status,
                                   cudaStream_t st);
 cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal, int scal_ld,
-                              cudaStream_t st);
+                              const float* part, int64_t part_ld, cudaStream_t st);
 cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* NhT,
                         int batch, int m, int n, int64_t ldm, int64_t ldn, float b1, float kappa,
                         const float* scal, int scal_ld, const uint32_t* status, cudaStream_t st);
 cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                               int with_update, const uint32_t* status, cudaStream_t st);
+                               int with_update, const uint32_t* status, const float* part_a, int64_t part_a_ld,
+                               int64_t npart_a, const float* part_b, int64_t part_b_ld, int64_t npart_b,
+                               cudaStream_t st);
 cudaError_t launch_normalise(const NormaliseArgs& A, int batch, cudaStream_t st);
-cudaError_t launch_sumsq(const float* S, int batch, int64_t dd, float* scal, int scal_ld, int slot,
-                         cudaStream_t st);
+cudaError_t launch_sumsq(const float* S, int batch, int64_t dd, float* part, int64_t part_ld, cudaStream_t st);
 cudaError_t launch_requant(const float* P, int batch, int d, __half* Ph, __half* PhT, __half* Pl, __half* PlT,
                            int64_t ld16, int64_t mat16, float* scal, int scal_ld, int slot, cudaStream_t st);
 cudaError_t launch_reset_factor(float* S, float* P, __half* Ph, __half* PhT, __half* Pl, __half* PlT, int d,

@@ -360,3 +360,26 @@ def test_ragged_shapes_and_tiny_dims(mode):
             assert worst["Sa"] < 1e-3 and worst["Sb"] < 1e-3, worst
             assert worst["Pa_exact"] < 1e-2 and worst["Pb_exact"] < 1e-2, worst
             assert worst["U"] < 2e-2 and worst["U_tf"] < 2e-2, worst
+
+
+def test_bitwise_reproducible():
+    """Same inputs, fresh handles: identical bits (every reduction sums its
+    partials in a fixed order; no floating-point atomics)."""
+    okls = _okls()
+    wl = workload("llama1.2b", scale=16, layers=1)
+    outs = []
+    for _rep in range(2):
+        gs = GradientStream(wl, "cpu")
+        g = wl.groups[1]
+        ob = okls.OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype)
+        W = gs.init_weights(1).cuda()
+        for t in range(1, 4):
+            ob.step(W, gs.grad(1, t).cuda(), 0.09434)
+        assert ob.query_status() == 0
+        outs.append((W.clone(), ob.get_state(L.STATE_PA), ob.get_state(L.STATE_SB)))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    S = torch.tensor(np.stack([spd(300, 50.0, 4), spd(300, 80.0, 5)]), dtype=torch.float32, device="cuda")
+    P1 = okls.inv_root(S)["P"]
+    P2 = okls.inv_root(S)["P"]
+    assert torch.equal(P1, P2)
