@@ -245,6 +245,38 @@ okls_status okls_inv_root(const float *S_dev, float *P_dev, float *root_dev,
                           float ridge, void *workspace_dev,
                           size_t workspace_bytes, void *stream);
 
+/*
+ * okls_inv_root without any device allocation.  The paper has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory
+ * when they need a root — code running while a CUDA graph is being captured,
+ * allocators that must not re-enter themselves, embedders whose device pool
+ * is fixed at start-up.  It computes the same S^(-1/2) as okls_inv_root
+ * (plain or split binary16 chain, same schedule, lo and ridge) but takes its
+ * scratch from one static device array inside the library instead of a
+ * workspace argument.
+ *   S_dev, P_dev  as okls_inv_root (count x d x d fp32, caller-owned).
+ *   Capacity      okls_inv_root_noalloc_capacity() bytes (32 MiB), held on
+ *                 every GPU that loads the library until the process exits;
+ *                 a request whose okls_inv_root_workspace_bytes exceeds it is
+ *                 rejected with OKLS_ERR_UNSUPPORTED (e.g. d = 1024 fits one
+ *                 matrix, d = 512 fits five).
+ *   First call    on each device looks up the array's device address
+ *                 (cudaGetSymbolAddress); make that first call before any
+ *                 stream capture.
+ *   Sharing       every call on a device uses the same array, which keeps the
+ *                 previous call's contents (the call clears what must start
+ *                 at zero).  Calls whose work overlaps on the GPU — two
+ *                 streams, two host threads — race on the array; serialise
+ *                 them.
+ * No cudaMalloc, cudaFree or other allocating routine is called.  The call
+ * synchronises `stream` before returning, like okls_inv_root.
+ */
+size_t okls_inv_root_noalloc_capacity(void);
+okls_status okls_inv_root_noalloc(const float *S_dev, float *P_dev, int64_t d,
+                                  int64_t count, int32_t iters,
+                                  int32_t split_iters, float lo, float ridge,
+                                  void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -103,6 +103,8 @@ _SIGS = {
                                 ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I32)]),
     "okls_inv_root_workspace_bytes": (_I32, [_I64, _I64, _I32, _I32, ctypes.POINTER(_SZ)]),
     "okls_inv_root": (_I32, [_P, _P, _P, _P, _I64, _I64, _I32, _I32, _F, _F, _P, _SZ, _P]),
+    "okls_inv_root_noalloc_capacity": (_SZ, []),
+    "okls_inv_root_noalloc": (_I32, [_P, _P, _I64, _I64, _I32, _I32, _F, _F, _P]),
 }
 
 

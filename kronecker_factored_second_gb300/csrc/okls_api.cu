@@ -1118,3 +1118,64 @@ okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace
 }
 
 }  // extern "C"
+
+// ===================================================== no-allocation variant
+// Some callers cannot allocate device memory at the moment they need an
+// inverse root: code running while a CUDA graph is being captured (a
+// cudaMalloc there breaks the capture), allocators that must not re-enter
+// themselves, and embedders whose memory pool is fixed at start-up.  For them
+// okls_inv_root_noalloc takes its scratch from this file-scope array instead
+// of a caller-provided workspace.  Every GPU that loads the library holds it
+// (32 MiB) until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the array's name in host code is only a host-side stand-in).
+okls_status noalloc_scratch(void** out) {
+  int dev = 0;
+  OKLS_CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(OKLS_ERR_NO_DEVICE, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(OKLS_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return OKLS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t okls_inv_root_noalloc_capacity(void) { return kNoAllocScratchBytes; }
+
+okls_status okls_inv_root_noalloc(const float* S, float* P, int64_t d, int64_t count, int32_t iters,
+                                  int32_t split_iters, float lo, float ridge, void* stream) {
+  size_t need = 0;
+  okls_status s = okls_inv_root_workspace_bytes(d, count, iters, split_iters, &need);
+  if (s != OKLS_OK) return s;
+  if (need > kNoAllocScratchBytes)
+    return fail(OKLS_ERR_UNSUPPORTED,
+                "okls_inv_root_noalloc: %lld matrices of %lld x %lld need %zu bytes of scratch; the static "
+                "scratch holds %zu bytes (use okls_inv_root with a workspace)",
+                static_cast<long long>(count), static_cast<long long>(d), static_cast<long long>(d), need,
+                kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != OKLS_OK) return s;
+  // the shared scratch keeps the previous call's contents; okls_inv_root
+  // clears the scalar sums and the status word it relies on
+  return okls_inv_root(S, P, nullptr, nullptr, d, count, iters, split_iters, lo, ridge, scratch,
+                       kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"
