@@ -12,6 +12,7 @@
 //   8. U = Q P_b and the parameter update          GEMM (EPI_UPDATE)
 #include <cudaTypedefs.h>
 #include <stdarg.h>
+#include <stdlib.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -110,20 +111,40 @@ constexpr size_t kMapTableBytes = kMaxMaps * sizeof(CUtensorMap);
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
+// Output tiles are tile_rows x 256: 128 rows for one CTA (default), 256 for
+// a CTA pair (okls_gemm2.cu, enabled with OKLS_GEMM_PAIR=1 for launches with a
+// problem taller than 128 rows).  On the power-capped GB300 the pair kernel
+// does ~10% more work per clock but runs ~10% lower clocks; end to end the
+// one-CTA kernel measured 2% faster on the 1.2B-shaped set.
+bool pair_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("OKLS_GEMM_PAIR");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+bool use_pair(int64_t max_rows) { return pair_enabled() && max_rows > kBM; }
+
 // tiles of a symmetric (upper-triangle) d x d product: row block tm holds
-// column blocks floor(tm/2) .. tiles_n-1
-int64_t sym_tiles(int64_t d) {
-  const int64_t tm_n = (d + kBM - 1) / kBM, tn_n = (d + kBN - 1) / kBN;
+// column blocks floor(tm * tile_rows / 256) .. tiles_n-1
+int64_t sym_tiles(int64_t d, int tile_rows) {
+  const int64_t tm_n = (d + tile_rows - 1) / tile_rows, tn_n = (d + kBN - 1) / kBN;
+  const int div = kBN / tile_rows;
   int64_t c = 0;
-  for (int64_t tm = 0; tm < tm_n; ++tm) c += tn_n - tm / 2;
+  for (int64_t tm = 0; tm < tm_n; ++tm) c += tn_n - tm / div;
   return c;
 }
 
-// fixed partial slots per matrix for ||S||_F^2 (SYRK tiles x 4 warps, or the
+// partial sums of S^2 one symmetric product writes: 4 epilogue warps per tile
+// (one CTA) or 8 (a pair)
+int64_t syrk_parts(int64_t d, bool pair) { return pair ? 8 * sym_tiles(d, 256) : 4 * sym_tiles(d, kBM); }
+
+// fixed partial slots per matrix for ||S||_F^2 (either tiling, or the
 // blocks of the standalone reduction)
 int64_t factor_parts(int64_t d) {
-  const int64_t a = 4 * sym_tiles(d), b = sumsq_parts(d * d);
-  return a > b ? a : b;
+  int64_t a = syrk_parts(d, false), b = syrk_parts(d, true), c = sumsq_parts(d * d);
+  return std::max(a, std::max(b, c));
 }
 
 // A batch of binary16 matrices (rows x cols, row pitch ld) with two TMA
@@ -139,6 +160,7 @@ struct Planner {
   uint8_t* base = nullptr;  // null: sizing pass
   size_t off = 0;
   std::vector<CUtensorMap> maps;
+  std::vector<int> boxes;  // rows of each descriptor's box (128 or 256)
   okls_status err = OKLS_OK;
 
   void* take(size_t bytes, size_t align = 256) {
@@ -176,6 +198,7 @@ struct Planner {
       return -1;
     }
     maps.push_back(m);
+    boxes.push_back(box_rows);
     return static_cast<int>(maps.size()) - 1;
   }
 
@@ -279,6 +302,7 @@ struct Prof {
 };
 
 thread_local Prof* g_prof = nullptr;  // set for the duration of okls_step
+thread_local const std::vector<int>* g_boxes = nullptr;  // box rows of each descriptor
 thread_local bool g_in_ns = false;
 
 void note_kernels(int n) {
@@ -288,6 +312,11 @@ void note_kernels(int n) {
 struct ProfScope {
   explicit ProfScope(Prof* p) { g_prof = p; }
   ~ProfScope() { g_prof = nullptr; }
+};
+
+struct BoxScope {
+  explicit BoxScope(const std::vector<int>* b) { g_boxes = b; }
+  ~BoxScope() { g_boxes = nullptr; }
 };
 
 // ------------------------------------------------------------ GEMM launches
@@ -307,27 +336,21 @@ struct LaunchBuilder {
     p.nseg = split ? 3 : 1;
     p.amap[0] = A[0].mapA;
     p.bmap[0] = B[0].mapB;
+    p.bmap_pair[0] = B[0].mapA;
     if (split) {
       p.amap[1] = A[0].mapA;
       p.bmap[1] = B[1].mapB;
+      p.bmap_pair[1] = B[1].mapA;
       p.amap[2] = A[1].mapA;
       p.bmap[2] = B[0].mapB;
+      p.bmap_pair[2] = B[0].mapA;
     }
     p.rows = rows;
     p.cols = cols;
     p.K = K;
     p.batch = batch;
-    p.tiles_m = (rows + kBM - 1) / kBM;
-    p.tiles_n = (cols + kBN - 1) / kBN;
     p.sym = sym ? 1 : 0;
     p.epi = epi;
-    if (sym) {
-      int64_t cnt = 0;
-      for (int tm = 0; tm < p.tiles_m; ++tm) cnt += p.tiles_n - tm / 2;
-      p.tiles_per_mat = cnt;
-    } else {
-      p.tiles_per_mat = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-    }
     return p;
   }
 
@@ -339,6 +362,7 @@ struct LaunchBuilder {
       p.nseg = 2;
       p.amap[1] = A.mapA;
       p.bmap[1] = B[1].mapB;
+      p.bmap_pair[1] = B[1].mapA;
     }
     return p;
   }
@@ -351,6 +375,7 @@ struct LaunchBuilder {
       p.nseg = 2;
       p.amap[1] = A[1].mapA;
       p.bmap[1] = B.mapB;
+      p.bmap_pair[1] = B.mapA;
     }
     return p;
   }
@@ -371,10 +396,32 @@ struct LaunchBuilder {
     std::stable_sort(L.prob, L.prob + L.nprob, [](const GemmProblem& x, const GemmProblem& y) {
       return static_cast<int64_t>(x.K) * x.nseg > static_cast<int64_t>(y.K) * y.nseg;
     });
+    int64_t max_rows = 0;
+    for (int i = 0; i < L.nprob; ++i) max_rows = std::max<int64_t>(max_rows, L.prob[i].rows);
+    const bool pair = use_pair(max_rows);
+    // every TMA box must match the ring slot it lands in
+    if (g_boxes) {
+      const int nb = static_cast<int>(g_boxes->size());
+      auto box = [&](int idx) { return (idx >= 0 && idx < nb) ? (*g_boxes)[idx] : -1; };
+      for (int i = 0; i < L.nprob; ++i)
+        for (int sg = 0; sg < L.prob[i].nseg; ++sg)
+          if (box(L.prob[i].amap[sg]) != kBM || box(L.prob[i].bmap[sg]) != kBN ||
+              box(L.prob[i].bmap_pair[sg]) != kBM)
+            return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: descriptor box sizes");
+    } else {
+      return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: descriptor table not bound");
+    }
+    const int tile_rows = pair ? 256 : kBM;
     int64_t t = 0;
     for (int i = 0; i < L.nprob; ++i) {
-      L.prob[i].tile_begin = t;
-      t += L.prob[i].tiles_per_mat * L.prob[i].batch;
+      GemmProblem& p = L.prob[i];
+      p.tiles_m = (p.rows + tile_rows - 1) / tile_rows;
+      p.tiles_n = (p.cols + kBN - 1) / kBN;
+      p.tiles_per_mat = p.sym ? sym_tiles(p.rows, tile_rows) : static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+      if (p.epi == EPI_SYRK && (p.part == nullptr || p.part_ld < syrk_parts(p.rows, pair)))
+        return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: partial-sum slots");
+      p.tile_begin = t;
+      t += p.tiles_per_mat * p.batch;
     }
     L.total_tiles = t;
     L.maps = maps;
@@ -383,7 +430,8 @@ struct LaunchBuilder {
     double flops = 0.0;
     for (int i = 0; i < L.nprob; ++i) {
       const GemmProblem& p = L.prob[i];
-      const double mn = p.sym ? static_cast<double>(p.rows) * (p.rows + 1) * 0.5 : static_cast<double>(p.rows) * p.cols;
+      const double mn =
+          p.sym ? static_cast<double>(p.rows) * (p.rows + 1) * 0.5 : static_cast<double>(p.rows) * p.cols;
       flops += 2.0 * mn * p.K * p.batch * p.nseg;
     }
     cudaEvent_t ea = nullptr, eb = nullptr;
@@ -392,7 +440,7 @@ struct LaunchBuilder {
       eb = pf->next_event();
       if (ea) OKLS_CK(cudaEventRecord(ea, st));
     }
-    OKLS_CK(launch_gemm(L, sms, st));
+    OKLS_CK(pair ? launch_gemm_pair(L, sms, st) : launch_gemm(L, sms, st));
     if (pf) {
       if (ea && eb) {
         OKLS_CK(cudaEventRecord(eb, st));
@@ -603,6 +651,7 @@ struct okls_handle_s {
   float* scal = nullptr;
   uint32_t* status = nullptr;
   CUtensorMap* maps = nullptr;
+  std::vector<int> boxes;  // box rows of each descriptor in the table
   float *part_g = nullptr, *part_a = nullptr, *part_b = nullptr;  // fixed-slot partial sums
   int64_t part_g_ld = 0, part_a_ld = 0, part_b_ld = 0;
   int64_t t = 0;
@@ -679,6 +728,7 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
     h->part_g_ld = pg_ld;
     h->part_a_ld = pa_ld;
     h->part_b_ld = pb_ld;
+    h->boxes = wp.boxes;
     // upload the descriptor table once
     if (!wp.maps.empty()) {
       cudaError_t e = cudaMemcpy(maps, wp.maps.data(), wp.maps.size() * sizeof(CUtensorMap),
@@ -824,6 +874,7 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
   const int h12 = kHeadroom;
   okls_status s;
   ProfScope scope(&h->prof);
+  BoxScope boxes(&h->boxes);
   note_kernels(4);  // momentum statistics, coefficients (2), pack
 
   // 1-2. momentum, statistics, packed binary16 operands
@@ -879,8 +930,11 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
   }
   // 5-6. fresh inverse roots of both factors
   const int K = h->sched.iters;
+  // the factor products ran as one launch: pair tiles iff either factor is taller than 128
+  const bool syrk_pair = use_pair(std::max(m, n));
   OKLS_CK(launch_coeffs_post(B, c.ridge, h->sched.z[K], h->sched.z[K - 1], h->scal, sld, 1, h->status, h->part_a,
-                             h->part_a_ld, 4 * sym_tiles(m), h->part_b, h->part_b_ld, 4 * sym_tiles(n), st));
+                             h->part_a_ld, syrk_parts(m, syrk_pair), h->part_b, h->part_b_ld,
+                             syrk_parts(n, syrk_pair), st));
   {
     Factor* fs[2] = {&h->fa, &h->fb};
     if ((s = run_ns(fs, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
@@ -1035,7 +1089,7 @@ okls_status okls_ns_schedule(int32_t iters, double lo, double* a, double* b, int
 // ------------------------------------------------------------ inverse roots
 static okls_status inv_plan(int64_t d, int64_t count, int32_t split, uint8_t* ws, Factor* f, float** scal,
                             uint32_t** status, CUtensorMap** maps, size_t* bytes, std::vector<CUtensorMap>* mv,
-                            float** part) {
+                            float** part, std::vector<int>* boxes = nullptr) {
   Planner wp;
   wp.base = ws;
   *maps = static_cast<CUtensorMap*>(wp.take(kMapTableBytes, 128));
@@ -1046,6 +1100,7 @@ static okls_status inv_plan(int64_t d, int64_t count, int32_t split, uint8_t* ws
   if (wp.err != OKLS_OK) return wp.err;
   *bytes = wp.off;
   if (mv) *mv = wp.maps;
+  if (boxes) *boxes = wp.boxes;
   return OKLS_OK;
 }
 
@@ -1080,9 +1135,11 @@ okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace
   CUtensorMap* maps;
   float* part;
   std::vector<CUtensorMap> mv;
+  std::vector<int> box_rows;
   if ((s = inv_plan(d, count, split_iters, static_cast<uint8_t*>(ws), &f, &scal, &status, &maps, &need, &mv,
-                    &part)) != OKLS_OK)
+                    &part, &box_rows)) != OKLS_OK)
     return s;
+  BoxScope boxes(&box_rows);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   OKLS_CK(cudaMemcpyAsync(maps, mv.data(), mv.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice, st));
   OKLS_CK(cudaMemsetAsync(scal, 0, static_cast<size_t>(SC_COUNT * count * 4), st));

@@ -1,0 +1,252 @@
+// Tile decoding and the fused OKLS epilogues shared by the one-CTA and the
+// CTA-pair tcgen05 GEMM kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "okls_internal.h"
+
+namespace okls {
+
+struct TileCoord {
+  int p, mat, tm, tn;
+  int64_t lt;  // tile index within its matrix
+};
+
+// Tile t of the launch's linear tile space.  Output tiles are tile_rows x 256
+// (tile_rows = 128 for one CTA, 256 for a CTA pair); symmetric problems keep
+// the tiles that touch the upper triangle: column block >= floor(tm * tile_rows / 256).
+template <int kTileRows>
+__device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t) {
+  constexpr int kDiv = kBN / kTileRows;
+  TileCoord c;
+  int p = 0;
+  while (p + 1 < L.nprob && t >= L.prob[p + 1].tile_begin) ++p;
+  const GemmProblem& P = L.prob[p];
+  const int64_t local = t - P.tile_begin;
+  c.p = p;
+  c.mat = static_cast<int>(local / P.tiles_per_mat);
+  int64_t r = local - static_cast<int64_t>(c.mat) * P.tiles_per_mat;
+  c.lt = r;
+  if (P.sym) {
+    int tm = 0;
+    for (;;) {
+      const int cnt = P.tiles_n - tm / kDiv;
+      if (r < cnt) break;
+      r -= cnt;
+      ++tm;
+    }
+    c.tm = tm;
+    c.tn = tm / kDiv + static_cast<int>(r);
+  } else {
+    const int64_t span = static_cast<int64_t>(kGroupM) * P.tiles_n;
+    const int g = static_cast<int>(r / span);
+    const int first = g * kGroupM;
+    const int gm = min(kGroupM, P.tiles_m - first);
+    const int64_t rr = r - static_cast<int64_t>(g) * span;
+    c.tm = first + static_cast<int>(rr % gm);
+    c.tn = static_cast<int>(rr / gm);
+  }
+  return c;
+}
+
+// Every loop below runs over the 32 values with a compile-time index and a
+// predicate for the ragged edge, so the values never leave registers.
+
+__device__ __forceinline__ void store_half32_row(__half* dst, const float (&x)[32], int nvalid) {
+  if (nvalid == 32) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __align__(16) __half2 h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(x[q * 8 + 2 * e], x[q * 8 + 2 * e + 1]);
+      *reinterpret_cast<uint4*>(dst + q * 8) = *reinterpret_cast<uint4*>(h);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (e < nvalid) dst[e] = __float2half_rn(x[e]);
+  }
+}
+
+// Split x into binary16 hi + lo (lo = r16(x - hi)).
+__device__ __forceinline__ void split_lo(const float (&x)[32], float (&lo)[32]) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) lo[e] = x[e] - __half2float(__float2half_rn(x[e]));
+}
+
+// Row-major and transposed binary16 stores of 32 values of row i, columns
+// j0..j0+31 of a square (ld16-pitched) output.
+__device__ __forceinline__ void store_both16(__half* row_base, __half* t_base, int64_t ld16, int i, int j0,
+                                             int cols, const float (&x)[32]) {
+  const int nvalid = min(32, cols - j0);
+  if (nvalid <= 0) return;
+  store_half32_row(row_base + static_cast<int64_t>(i) * ld16 + j0, x, nvalid);
+  if (t_base != nullptr) {
+    // thread i writes column i of rows j0..: consecutive lanes hit
+    // consecutive addresses of one row of the transposed output
+    __half* t = t_base + static_cast<int64_t>(j0) * ld16 + i;
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (e < nvalid) t[static_cast<int64_t>(e) * ld16] = __float2half_rn(x[e]);
+  }
+}
+
+__device__ __forceinline__ void store_f32_row(float* dst, const float (&x)[32], float scale, int nvalid,
+                                              bool vec_ok) {
+  if (vec_ok && nvalid == 32) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(dst + 4 * q) =
+          make_float4(x[4 * q] * scale, x[4 * q + 1] * scale, x[4 * q + 2] * scale, x[4 * q + 3] * scale);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (e < nvalid) dst[e] = x[e] * scale;
+  }
+}
+
+__device__ __forceinline__ float scal_at(const GemmProblem& P, int slot, int mat) {
+  return P.scal[static_cast<int64_t>(slot) * P.scal_ld + mat];
+}
+
+// Epilogue for one 32-column chunk of one accumulator row.
+__device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, const TileCoord& tc, int i, int j0,
+                                               float (&v)[32], uint32_t& flags, float& sumsq) {
+  if (i >= P.rows || j0 >= P.cols) return;
+  const int nvalid = min(32, P.cols - j0);
+  switch (P.epi) {
+    case EPI_X16: {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] *= P.alpha;
+      __half* dst = reinterpret_cast<__half*>(P.out_hi) + static_cast<int64_t>(tc.mat) * P.mat16 +
+                    static_cast<int64_t>(i) * P.ld16 + j0;
+      store_half32_row(dst, v, nvalid);
+      bool bad = false;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) bad |= !isfinite(v[e]);
+      if (bad && P.check_finite) flags |= kStNonfiniteIter;
+      break;
+    }
+    case EPI_NS_T:
+    case EPI_NS_SCALE:
+    case EPI_NS_LAST: {
+      if (P.epi == EPI_NS_LAST) {
+        float* dst = P.out32 + static_cast<int64_t>(tc.mat) * P.mat32 + static_cast<int64_t>(i) * P.ld32 + j0;
+        store_f32_row(dst, v, scal_at(P, P.scal_slot, tc.mat), nvalid, (P.ld32 & 3) == 0);
+      }
+      if (P.epi == EPI_NS_T) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = fmaf(P.beta, v[e], (i == j0 + e) ? P.alpha : 0.0f);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] *= P.alpha;
+      }
+      bool bad = false;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) bad |= !isfinite(v[e]) || fabsf(v[e]) > 65504.0f;
+      if (bad) flags |= kStNonfiniteIter;
+      const int64_t moff = static_cast<int64_t>(tc.mat) * P.mat16;
+      __half* hi = reinterpret_cast<__half*>(P.out_hi) + moff;
+      __half* hit = P.out_hi_t ? reinterpret_cast<__half*>(P.out_hi_t) + moff : nullptr;
+      if (P.split_out) {
+        float lo[32];
+        split_lo(v, lo);
+        store_both16(hi, hit, P.ld16, i, j0, P.cols, v);
+        __half* lob = reinterpret_cast<__half*>(P.out_lo) + moff;
+        __half* lot = P.out_lo_t ? reinterpret_cast<__half*>(P.out_lo_t) + moff : nullptr;
+        store_both16(lob, lot, P.ld16, i, j0, P.cols, lo);
+      } else {
+        store_both16(hi, hit, P.ld16, i, j0, P.cols, v);
+      }
+      break;
+    }
+    case EPI_SYRK: {
+      // only elements on or above the diagonal; mirrored below
+      const float alpha = scal_at(P, P.scal_slot, tc.mat);
+      float* S = P.out32 + static_cast<int64_t>(tc.mat) * P.mat32;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = j0 + e;
+        if (e < nvalid && j >= i) {
+          const int64_t a = static_cast<int64_t>(i) * P.ld32 + j;
+          float s = fmaf(P.beta, S[a], alpha * v[e]);
+          if (j == i) s += P.gamma;
+          S[a] = s;
+          if (j != i) S[static_cast<int64_t>(j) * P.ld32 + i] = s;
+          sumsq += (j == i ? 1.0f : 2.0f) * s * s;
+        }
+      }
+      break;
+    }
+    case EPI_UPDATE: {
+      const float coef = P.beta * scal_at(P, P.scal_slot, tc.mat);
+      const float decay = P.alpha;
+      const int64_t off = static_cast<int64_t>(tc.mat) * P.mat32 + static_cast<int64_t>(i) * P.ld32 + j0;
+      bool bad = false;
+      if (P.w_bf16) {
+        __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(P.w) + off;
+        if (nvalid == 32 && (P.ld32 & 7) == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 raw = *reinterpret_cast<const uint4*>(w + 8 * q);
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 o = __bfloat1622float2(h[e]);
+              const float n0 = fmaf(-coef, v[8 * q + 2 * e], decay * o.x);
+              const float n1 = fmaf(-coef, v[8 * q + 2 * e + 1], decay * o.y);
+              bad |= !isfinite(n0) || !isfinite(n1);
+              h[e] = __floats2bfloat162_rn(n0, n1);
+            }
+            *reinterpret_cast<uint4*>(w + 8 * q) = raw;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (e < nvalid) {
+              const float nw = fmaf(-coef, v[e], decay * __bfloat162float(w[e]));
+              bad |= !isfinite(nw);
+              w[e] = __float2bfloat16_rn(nw);
+            }
+          }
+        }
+      } else {
+        float* w = reinterpret_cast<float*>(P.w) + off;
+        if (nvalid == 32 && (P.ld32 & 3) == 0) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 o = *reinterpret_cast<float4*>(w + 4 * q);
+            o.x = fmaf(-coef, v[4 * q + 0], decay * o.x);
+            o.y = fmaf(-coef, v[4 * q + 1], decay * o.y);
+            o.z = fmaf(-coef, v[4 * q + 2], decay * o.z);
+            o.w = fmaf(-coef, v[4 * q + 3], decay * o.w);
+            bad |= !isfinite(o.x) || !isfinite(o.y) || !isfinite(o.z) || !isfinite(o.w);
+            *reinterpret_cast<float4*>(w + 4 * q) = o;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (e < nvalid) {
+              const float nw = fmaf(-coef, v[e], decay * w[e]);
+              bad |= !isfinite(nw);
+              w[e] = nw;
+            }
+          }
+        }
+      }
+      if (bad) flags |= kStNonfiniteUpdate;
+      break;
+    }
+    case EPI_ROOT: {
+      float* dst = P.out32 + static_cast<int64_t>(tc.mat) * P.mat32 + static_cast<int64_t>(i) * P.ld32 + j0;
+      store_f32_row(dst, v, scal_at(P, P.scal_slot, tc.mat), nvalid, (P.ld32 & 3) == 0);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+}  // namespace okls

@@ -69,8 +69,9 @@ struct GemmProblem {
   // operands: K segments, each a pair of tensor-map indices (A: box 128 rows,
   // B: box 256 rows) into the handle's descriptor table
   int32_t nseg;
-  int32_t amap[kMaxSeg];
-  int32_t bmap[kMaxSeg];
+  int32_t amap[kMaxSeg];        // A descriptors, 128-row boxes
+  int32_t bmap[kMaxSeg];        // B descriptors, 256-row boxes (one CTA per tile)
+  int32_t bmap_pair[kMaxSeg];   // B descriptors, 128-row boxes (CTA pairs: each loads half of B)
   int32_t rows, cols, K;        // output rows (A rows), cols (B rows), K
   int32_t batch;
   int32_t tiles_m, tiles_n;

@@ -26,6 +26,7 @@ struct NormaliseArgs {
 };
 
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_pair(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 
 // Reductions are deterministic: kernels write per-block (or per-tile) partials
 // into fixed slots and a single thread per matrix sums them in order.
