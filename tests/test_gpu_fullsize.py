@@ -1,0 +1,122 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py
+times (whole batches of every shape group on one GPU), on sampled outputs.
+
+For one matrix of each shape group, step 2 is checked teacher-forced from the
+GPU's own state after step 1 (so the factor products see a non-trivial P):
+  M            every entry, 1e-6
+  S_a, S_b     a 32 x 32 block: rows of G P_b / P_a G computed in float64
+               from the GPU's previous roots, 1e-3
+  P_a, P_b     against the eigendecomposition root of the GPU's own ridged S
+               (float64 on the host), 1e-2
+  U            64 sampled entries (from the change of W) against P_a N P_b with
+               the exact roots of the GPU's S and N from the float64 momentum,
+               2e-2; and against the same product with the GPU's own roots, 2e-2
+"""
+
+from __future__ import annotations
+
+import math
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_helpers import PARTS, hyper_of
+from kronecker_factored_second_gb300.workloads import GradientStream, workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def _matrix_state(ob, b: int) -> dict:
+    out = {}
+    for k, p in PARTS:
+        full = ob.get_state(p)
+        out[k] = full[b].double().cpu().numpy()
+        del full
+    return out
+
+
+def _check_group(wl_name, gi, g, gs, b, rng):
+    from kronecker_factored_second_gb300.okls import OklsBatch
+    ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype)
+    hp = hyper_of(ob)
+    W = gs.init_weights(gi)
+    ob.step(W, gs.grad(gi, 1), hp.lr)
+    assert ob.query_status() == 0
+    pre = _matrix_state(ob, b)
+    Wp = W[b].double().cpu().numpy()
+    G = gs.grad(gi, 2)
+    ob.step(W, G, hp.lr)
+    assert ob.query_status() == 0
+    post = _matrix_state(ob, b)
+    Wn = W[b].double().cpu().numpy()
+    Gb = G[b].double().cpu().numpy()
+    ob.close()
+    del ob, W, G
+    torch.cuda.empty_cache()
+
+    m, n = Gb.shape
+    b1, b2 = hp.beta1, hp.beta2
+    err = {}
+    # momentum
+    M = b1 * pre["M"] + (1 - b1) * Gb
+    err["M"] = O.rel_fro(post["M"], M)
+    # factor blocks
+    ia = np.sort(rng.choice(m, size=min(32, m), replace=False))
+    ja = np.sort(rng.choice(m, size=min(32, m), replace=False))
+    Xb_i, Xb_j = Gb[ia] @ pre["Pb"], Gb[ja] @ pre["Pb"]
+    Sa_blk = b2 * pre["Sa"][np.ix_(ia, ja)] + (1 - b2) / n * (Xb_i @ Xb_j.T) + hp.eps * (ia[:, None] == ja[None, :])
+    err["Sa"] = O.rel_fro(post["Sa"][np.ix_(ia, ja)], Sa_blk)
+    ib = np.sort(rng.choice(n, size=min(32, n), replace=False))
+    jb = np.sort(rng.choice(n, size=min(32, n), replace=False))
+    Xa_i, Xa_j = pre["Pa"] @ Gb[:, ib], pre["Pa"] @ Gb[:, jb]
+    Sb_blk = b2 * pre["Sb"][np.ix_(ib, jb)] + (1 - b2) / m * (Xa_i.T @ Xa_j) + hp.eps * (ib[:, None] == jb[None, :])
+    err["Sb"] = O.rel_fro(post["Sb"][np.ix_(ib, jb)], Sb_blk)
+    # roots against the exact root of the GPU's own ridged factors
+    t0 = time.time()
+    Pa_x = O.inv_root_exact(post["Sa"], hp.ridge)
+    Pb_x = O.inv_root_exact(post["Sb"], hp.ridge)
+    t_eigh = time.time() - t0
+    err["Pa"] = O.rel_fro(post["Pa"], Pa_x)
+    err["Pb"] = O.rel_fro(post["Pb"], Pb_x)
+    # sampled U entries
+    kappa = O.variance_correction(b1, 2)
+    N = kappa * (b1 * M + (1 - b1) * Gb)
+    ri = rng.choice(m, size=64)
+    ci = rng.choice(n, size=64)
+    decay = O.adamc_decay(hp.lr, hp.peak, hp.weight_decay)
+    c = O.c_shape(m, n)
+    U_gpu = ((1 - decay) * Wp[ri, ci] - Wn[ri, ci]) / (hp.lr * c)
+    left_x = Pa_x[ri] @ N
+    U_x = np.einsum("ij,ji->i", left_x, Pb_x[:, ci])
+    left_g = post["Pa"][ri] @ N
+    U_tf = np.einsum("ij,ji->i", left_g, post["Pb"][:, ci])
+    err["U"] = float(np.linalg.norm(U_gpu - U_x) / np.linalg.norm(U_x))
+    err["U_tf"] = float(np.linalg.norm(U_gpu - U_tf) / np.linalg.norm(U_tf))
+    print(f"{wl_name}/{g.name} b={b} ({m}x{n}) eigh {t_eigh:.1f}s", {k: f"{v:.2e}" for k, v in err.items()})
+    bf16 = g.dtype == torch.bfloat16
+    assert err["M"] < 1e-6, err
+    assert err["Sa"] < 1e-3 and err["Sb"] < 1e-3, err
+    assert err["Pa"] < 1e-2 and err["Pb"] < 1e-2, err
+    # bf16 parameters round the new W to 8 bits; the sampled U inherits that
+    u_tol = 3e-2 if bf16 else 2e-2
+    assert err["U"] < u_tol and err["U_tf"] < u_tol, err
+
+
+@pytest.mark.parametrize("name", ["batch16x512", "llama1.2b", "rect8192", "llama7b_slice"])
+def test_full_size_sampled_parity(name):
+    wl = workload(name)
+    gs = GradientStream(wl, "cuda")
+    rng = np.random.default_rng(31)
+    for gi, g in enumerate(wl.groups):
+        b = (7 * gi + 3) % g.batch
+        _check_group(name, gi, g, gs, b, rng)
