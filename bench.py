@@ -331,36 +331,66 @@ def run_okls(args):
     ns_achieved = prof["ns_flops"] / (prof["ns_ms"] / 1e3) / 1e12 if prof["ns_ms"] > 0 else None
 
     # ---------------------------------------------- end to end (host buffers)
+    # Every step copies that step's gradients from pinned host memory and
+    # reads the updated parameters back.  The copies run on their own stream
+    # and overlap the other shape groups' steps, as a training loop would:
+    # group i's step waits for its gradient copy, and its W read-back runs
+    # while group i+1 computes.  The timed region starts before the first
+    # copy and ends after the last read-back (both events on the copy stream).
     e2e = None
     if not args.no_e2e:
         hostG = []
         for (g, ob, W, Gs) in groups:
             hostG.append([Gs[i].cpu().pin_memory() for i in range(2)])
-        devG = [torch.empty_like(Gs[0]) for (_g, _ob, _W, Gs) in groups]
+        devG = [[torch.empty_like(Gs[0]) for _ in range(2)] for (_g, _ob, _W, Gs) in groups]
         hostW = [torch.empty(W.shape, dtype=W.dtype, pin_memory=True) for (_g, _ob, W, _G) in groups]
         h2d = sum(h[0].numel() * h[0].element_size() for h in hostG)
         d2h = sum(h.numel() * h.element_size() for h in hostW)
+        copy = torch.cuda.Stream(device=dev)
+        ng = len(groups)
+        g_ready = [[torch.cuda.Event() for _ in range(2)] for _ in range(ng)]
+        w_done = [torch.cuda.Event() for _ in range(ng)]
+        w_read = [torch.cuda.Event() for _ in range(ng)]
 
-        def e2e_step(k):
-            for i, (g, ob, W, _Gs) in enumerate(groups):
-                devG[i].copy_(hostG[i][k % 2], non_blocking=True)
-                ob.step(W, devG[i], args.lr)
-                hostW[i].copy_(W, non_blocking=True)
+        def e2e_steps(k0, count):
+            # prefetch the first step's gradients
+            with torch.cuda.stream(copy):
+                for i in range(ng):
+                    devG[i][k0 % 2].copy_(hostG[i][k0 % 2], non_blocking=True)
+                    g_ready[i][k0 % 2].record(copy)
+            for k in range(k0, k0 + count):
+                buf = k % 2
+                for i, (g, ob, W, _Gs) in enumerate(groups):
+                    stream.wait_event(g_ready[i][buf])
+                    if k > k0:
+                        stream.wait_event(w_read[i])   # W must be read back before it changes again
+                    ob.step(W, devG[i][buf], args.lr)
+                    w_done[i].record(stream)
+                    with torch.cuda.stream(copy):
+                        copy.wait_event(w_done[i])
+                        hostW[i].copy_(W, non_blocking=True)
+                        w_read[i].record(copy)
+                        if k + 1 < k0 + count:
+                            # next step's gradients into the other buffer (its last reader
+                            # was this group's previous step, finished before w_done)
+                            devG[i][1 - buf].copy_(hostG[i][(k + 1) % 2], non_blocking=True)
+                            g_ready[i][1 - buf].record(copy)
 
-        for k in range(max(1, args.warmup // 2)):
-            e2e_step(k)
+        e2e_steps(0, max(1, args.warmup // 2))
         torch.cuda.synchronize()
         barrier(ws)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for k in range(args.steps):
-            e2e_step(k)
-        b.record(stream)
+        a.record(copy)
+        stream.wait_event(a)
+        e2e_steps(0, args.steps)
+        copy.wait_stream(stream)
+        b.record(copy)
         torch.cuda.synchronize()
         barrier(ws)
         ms_e2e = max_over_ranks(a.elapsed_time(b), ws, dev)
         e2e = {"value": sum_over_ranks(matrices * args.steps, ws, dev) / (ms_e2e / 1e3), "unit": "matrices/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e / args.steps}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e / args.steps,
+               "copies": "pinned host, own stream, overlapped with the other groups' steps"}
         del hostG, devG, hostW
 
     # ------------------------------------------------ second precision mode
