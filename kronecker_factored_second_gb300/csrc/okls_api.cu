@@ -5,6 +5,8 @@
 //   1. momentum statistics          k_momentum_stats, k_coeffs_pre
 //   2. M_t, Ghat, Ghat^T, Nhat^T    k_pack
 //   3. X_b = G P_b, X_a^T = G^T P_a^T             GEMM (EPI_X16)
+//      (B operands stored K x N are read MN-major, so every binary16 matrix
+//      is kept in one row-major layout; only Ghat^T is materialised)
 //   4. S_a, S_b EMAs (+ ||S||_F^2)                 GEMM (EPI_SYRK, upper tiles)
 //   5. normalisers, Y_0, T_0, Z_1                  k_coeffs_post, k_normalise
 //   6. coupled Newton-Schulz, both factors         19 GEMM launches, 27 products
@@ -107,6 +109,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 constexpr int kMaxMaps = 128;
+constexpr int kMNBox = 64;  // descriptor code of a 64 x 64 MN-major box
 constexpr size_t kMapTableBytes = kMaxMaps * sizeof(CUtensorMap);
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -152,7 +155,8 @@ int64_t factor_parts(int64_t d) {
 struct Buf {
   __half* p = nullptr;
   int64_t rows = 0, cols = 0, ld = 0, batch = 0;
-  int mapA = -1, mapB = -1;
+  int mapA = -1, mapB = -1;  // K-major boxes: 128 and 256 rows of 64 columns
+  int mapMN = -1;            // MN-major box: 64 columns x 64 rows
   int64_t mat() const { return rows * ld; }
 };
 
@@ -170,6 +174,8 @@ struct Planner {
     return p;
   }
 
+  // box_rows 128 / 256: K-major operand tiles (64 columns); box_rows kMNBox:
+  // MN-major 64 x 64 tiles.  The recorded code is what the launch check reads.
   int make_map(void* ptr, int64_t rows, int64_t cols, int64_t ld, int64_t batch, int box_rows) {
     if (!base) return 0;
     if (static_cast<int>(maps.size()) >= kMaxMaps) {
@@ -186,7 +192,7 @@ struct Planner {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                           static_cast<cuuint64_t>(batch)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(rows * ld * 2)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows == kMNBox ? 64 : box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, ptr, dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -211,6 +217,7 @@ struct Planner {
     b.p = static_cast<__half*>(take(static_cast<size_t>(b.mat() * batch * 2)));
     b.mapA = make_map(b.p, rows, cols, b.ld, batch, kBM);
     b.mapB = make_map(b.p, rows, cols, b.ld, batch, kBN);
+    b.mapMN = make_map(b.p, rows, cols, b.ld, batch, kMNBox);
     return b;
   }
 };
@@ -222,8 +229,8 @@ struct Factor {
   float* S = nullptr;       // fp32 input
   float* P32 = nullptr;     // fp32 output
   float* root32 = nullptr;  // debug root output
-  Buf Ph[2], PhT[2];                                      // binary16 P (hi, lo)
-  Buf Y[2][2], YT[2][2], Z[2][2], ZT[2][2], T[2], TT[2];  // [ping-pong][hi, lo]
+  Buf Ph[2];                         // binary16 P (hi, lo), row-major
+  Buf Y[2][2], Z[2][2], T[2];        // iterates [ping-pong][hi, lo], row-major
   bool split = false;
   int slot_sumsq = 0, slot_cprime = 0, slot_pi = 0, slot_pscale = 0, slot_rscale = 0;
 };
@@ -233,21 +240,13 @@ void plan_factor(Planner& pl, Factor& f, int d, int batch, bool split) {
   f.batch = batch;
   f.split = split;
   const int nl = split ? 2 : 1;
-  for (int l = 0; l < nl; ++l) {
-    f.Ph[l] = pl.buf16(d, d, batch);
-    f.PhT[l] = pl.buf16(d, d, batch);
-  }
+  for (int l = 0; l < nl; ++l) f.Ph[l] = pl.buf16(d, d, batch);
   for (int pp = 0; pp < 2; ++pp)
     for (int l = 0; l < nl; ++l) {
       f.Y[pp][l] = pl.buf16(d, d, batch);
-      f.YT[pp][l] = pl.buf16(d, d, batch);
       f.Z[pp][l] = pl.buf16(d, d, batch);
-      f.ZT[pp][l] = pl.buf16(d, d, batch);
     }
-  for (int l = 0; l < nl; ++l) {
-    f.T[l] = pl.buf16(d, d, batch);
-    f.TT[l] = pl.buf16(d, d, batch);
-  }
+  for (int l = 0; l < nl; ++l) f.T[l] = pl.buf16(d, d, batch);
 }
 
 int g_num_sms[64] = {0};
@@ -328,22 +327,26 @@ struct LaunchBuilder {
   GemmLaunch L;
   LaunchBuilder() { memset(&L, 0, sizeof(L)); }
 
-  // D = sum over segments of A_seg * B_seg^T; split: (hi,hi), (hi,lo), (lo,hi)
+  // D = sum over segments of A_seg * op(B_seg); split: (hi,hi), (hi,lo), (lo,hi).
+  // op(B) = B^T for K-major B (stored N x K), B for MN-major B (stored K x N).
   GemmProblem& add(const Buf* A, const Buf* B, bool split, int rows, int cols, int K, int batch, int epi,
-                   bool sym) {
+                   bool sym, bool bmn = false) {
     GemmProblem& p = L.prob[L.nprob++];
     memset(&p, 0, sizeof(p));
+    p.bmn = bmn ? 1 : 0;
+    auto bm = [&](const Buf& x) { return bmn ? x.mapMN : x.mapB; };
+    auto bp = [&](const Buf& x) { return bmn ? x.mapMN : x.mapA; };
     p.nseg = split ? 3 : 1;
     p.amap[0] = A[0].mapA;
-    p.bmap[0] = B[0].mapB;
-    p.bmap_pair[0] = B[0].mapA;
+    p.bmap[0] = bm(B[0]);
+    p.bmap_pair[0] = bp(B[0]);
     if (split) {
       p.amap[1] = A[0].mapA;
-      p.bmap[1] = B[1].mapB;
-      p.bmap_pair[1] = B[1].mapA;
+      p.bmap[1] = bm(B[1]);
+      p.bmap_pair[1] = bp(B[1]);
       p.amap[2] = A[1].mapA;
-      p.bmap[2] = B[0].mapB;
-      p.bmap_pair[2] = B[0].mapA;
+      p.bmap[2] = bm(B[0]);
+      p.bmap_pair[2] = bp(B[0]);
     }
     p.rows = rows;
     p.cols = cols;
@@ -354,28 +357,28 @@ struct LaunchBuilder {
     return p;
   }
 
-  // D = A * (B_hi + B_lo)^T: two K segments when `split`, else one
-  GemmProblem& add_bsplit(const Buf& A, const Buf* B, bool split, int rows, int cols, int K, int batch,
-                          int epi) {
-    GemmProblem& p = add(&A, B, false, rows, cols, K, batch, epi, false);
+  // D = A * op(B_hi + B_lo): two K segments when `split`, else one
+  GemmProblem& add_bsplit(const Buf& A, const Buf* B, bool split, int rows, int cols, int K, int batch, int epi,
+                          bool bmn = false) {
+    GemmProblem& p = add(&A, B, false, rows, cols, K, batch, epi, false, bmn);
     if (split) {
       p.nseg = 2;
       p.amap[1] = A.mapA;
-      p.bmap[1] = B[1].mapB;
-      p.bmap_pair[1] = B[1].mapA;
+      p.bmap[1] = bmn ? B[1].mapMN : B[1].mapB;
+      p.bmap_pair[1] = bmn ? B[1].mapMN : B[1].mapA;
     }
     return p;
   }
 
-  // D = (A_hi + A_lo) * B^T
-  GemmProblem& add_asplit(const Buf* A, const Buf& B, bool split, int rows, int cols, int K, int batch,
-                          int epi) {
-    GemmProblem& p = add(A, &B, false, rows, cols, K, batch, epi, false);
+  // D = (A_hi + A_lo) * op(B)
+  GemmProblem& add_asplit(const Buf* A, const Buf& B, bool split, int rows, int cols, int K, int batch, int epi,
+                          bool bmn = false) {
+    GemmProblem& p = add(A, &B, false, rows, cols, K, batch, epi, false, bmn);
     if (split) {
       p.nseg = 2;
       p.amap[1] = A[1].mapA;
-      p.bmap[1] = B.mapB;
-      p.bmap_pair[1] = B.mapA;
+      p.bmap[1] = p.bmap[0];
+      p.bmap_pair[1] = p.bmap_pair[0];
     }
     return p;
   }
@@ -405,8 +408,9 @@ struct LaunchBuilder {
       auto box = [&](int idx) { return (idx >= 0 && idx < nb) ? (*g_boxes)[idx] : -1; };
       for (int i = 0; i < L.nprob; ++i)
         for (int sg = 0; sg < L.prob[i].nseg; ++sg)
-          if (box(L.prob[i].amap[sg]) != kBM || box(L.prob[i].bmap[sg]) != kBN ||
-              box(L.prob[i].bmap_pair[sg]) != kBM)
+          if (box(L.prob[i].amap[sg]) != kBM ||
+              box(L.prob[i].bmap[sg]) != (L.prob[i].bmn ? kMNBox : kBN) ||
+              box(L.prob[i].bmap_pair[sg]) != (L.prob[i].bmn ? kMNBox : kBM))
             return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: descriptor box sizes");
     } else {
       return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: descriptor table not bound");
@@ -527,23 +531,23 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
     A.ld16 = f.Y[0][0].ld;
     A.mat16 = f.Y[0][0].mat();
     A.Y = f.Y[0][0].p;
-    A.YT = f.YT[0][0].p;
+
     A.T = f.T[0].p;
-    A.TT = f.TT[0].p;
+
     A.Z = f.Z[1][0].p;
-    A.ZT = f.ZT[1][0].p;
+
     A.split_y = split > 0;
     A.split_t = split > 0;
     A.split_z = split > 1;
     if (A.split_y) {
       A.Ylo = f.Y[0][1].p;
-      A.YTlo = f.YT[0][1].p;
+
       A.Tlo = f.T[1].p;
-      A.TTlo = f.TT[1].p;
+
     }
     if (A.split_z) {
       A.Zlo = f.Z[1][1].p;
-      A.ZTlo = f.ZT[1][1].p;
+
     }
     A.a0 = static_cast<float>(sc.a[0]);
     A.b0 = static_cast<float>(sc.b[0]);
@@ -569,8 +573,8 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
     const bool sp = split > 0, spo = split > 1;
     for (int q = 0; q < nf; ++q) {
       Factor& f = *fs[q];
-      GemmProblem& p = lb.add(f.Y[0], f.TT, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false);
-      set_out16(p, f.Y[1][0], &f.YT[1][0], spo ? &f.Y[1][1] : nullptr, spo ? &f.YT[1][1] : nullptr);
+      GemmProblem& p = lb.add(f.Y[0], f.T, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
+      set_out16(p, f.Y[1][0], nullptr, spo ? &f.Y[1][1] : nullptr, nullptr);
       p.alpha = std::ldexp(1.0f, -h);
     }
     okls_status s = lb.go(maps, status, sms, st);
@@ -584,8 +588,8 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
       LaunchBuilder lb;  // T_k = a_k I + b_k Z_k Y_k
       for (int q = 0; q < nf; ++q) {
         Factor& f = *fs[q];
-        GemmProblem& p = lb.add(f.Z[cur], f.YT[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_T, false);
-        set_out16(p, f.T[0], &f.TT[0], sp ? &f.T[1] : nullptr, sp ? &f.TT[1] : nullptr);
+        GemmProblem& p = lb.add(f.Z[cur], f.Y[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_T, false, true);
+        set_out16(p, f.T[0], nullptr, sp ? &f.T[1] : nullptr, nullptr);
         p.alpha = static_cast<float>(std::ldexp(sc.a[k], h));
         p.beta = static_cast<float>(std::ldexp(sc.b[k], sc.z[k] - h));
       }
@@ -602,17 +606,17 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
     for (int q = 0; q < nf; ++q) {
       Factor& f = *fs[q];
       if (k < K - 1) {
-        GemmProblem& py = lb.add(f.Y[cur], f.TT, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false);
-        set_out16(py, f.Y[nxt][0], &f.YT[nxt][0], spo ? &f.Y[nxt][1] : nullptr, spo ? &f.YT[nxt][1] : nullptr);
+        GemmProblem& py = lb.add(f.Y[cur], f.T, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
+        set_out16(py, f.Y[nxt][0], nullptr, spo ? &f.Y[nxt][1] : nullptr, nullptr);
         py.alpha = std::ldexp(1.0f, -h);
-        GemmProblem& pz = lb.add(f.T, f.ZT[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false);
-        set_out16(pz, f.Z[nxt][0], &f.ZT[nxt][0], spo ? &f.Z[nxt][1] : nullptr, spo ? &f.ZT[nxt][1] : nullptr);
+        GemmProblem& pz = lb.add(f.T, f.Z[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
+        set_out16(pz, f.Z[nxt][0], nullptr, spo ? &f.Z[nxt][1] : nullptr, nullptr);
         pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
       } else {
-        GemmProblem& pz = lb.add(f.T, f.ZT[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_LAST, false);
+        GemmProblem& pz = lb.add(f.T, f.Z[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_LAST, false, true);
         // in split mode the copy of P read by the X and whitening products
         // is a (hi, lo) pair as well
-        set_out16(pz, f.Ph[0], &f.PhT[0], f.split ? &f.Ph[1] : nullptr, f.split ? &f.PhT[1] : nullptr);
+        set_out16(pz, f.Ph[0], nullptr, f.split ? &f.Ph[1] : nullptr, nullptr);
         pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
         pz.out32 = f.P32;
         pz.ld32 = f.d;
@@ -621,7 +625,7 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
         pz.scal_ld = scal_ld;
         pz.scal_slot = f.slot_pscale;
         if (f.root32) {
-          GemmProblem& pr = lb.add(f.Y[cur], f.TT, sp, f.d, f.d, f.d, f.batch, EPI_ROOT, false);
+          GemmProblem& pr = lb.add(f.Y[cur], f.T, sp, f.d, f.d, f.d, f.batch, EPI_ROOT, false, true);
           pr.out32 = f.root32;
           pr.ld32 = f.d;
           pr.mat32 = static_cast<int64_t>(f.d) * f.d;
@@ -647,7 +651,7 @@ struct okls_handle_s {
   Sched sched;
   float *M = nullptr, *Sa = nullptr, *Sb = nullptr, *Pa = nullptr, *Pb = nullptr;
   Factor fa, fb;
-  Buf Gh, GhT, NhT, Xb, XaT;
+  Buf Gh, GhT, Nh, Xb, XaT;  // Ghat (m x n), Ghat^T (n x m), Nhat (m x n), X_b / Q (m x n), X_a^T (n x m)
   float* scal = nullptr;
   uint32_t* status = nullptr;
   CUtensorMap* maps = nullptr;
@@ -683,7 +687,7 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
   float* part_g = static_cast<float*>(wp.take(static_cast<size_t>(2 * B * pg_ld * 4)));
   float* part_a = static_cast<float*>(wp.take(static_cast<size_t>(B * pa_ld * 4)));
   float* part_b = static_cast<float*>(wp.take(static_cast<size_t>(B * pb_ld * 4)));
-  Buf Gh = wp.buf16(m, n, B), GhT = wp.buf16(n, m, B), NhT = wp.buf16(n, m, B);
+  Buf Gh = wp.buf16(m, n, B), GhT = wp.buf16(n, m, B), Nh = wp.buf16(m, n, B);
   Buf Xb = wp.buf16(m, n, B), XaT = wp.buf16(n, m, B);
   Factor fa, fb;
   const bool split = c.ns_split_iters > 0;
@@ -716,7 +720,7 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
     h->fb = fb;
     h->Gh = Gh;
     h->GhT = GhT;
-    h->NhT = NhT;
+    h->Nh = Nh;
     h->Xb = Xb;
     h->XaT = XaT;
     h->scal = scal;
@@ -847,11 +851,11 @@ okls_status okls_reset_state(okls_handle h, void* stream) {
   OKLS_CK(cudaMemsetAsync(h->M, 0, static_cast<size_t>(c.batch * c.m * c.n * 4), st));
   OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(SC_COUNT * c.batch * 4), st));
   OKLS_CK(cudaMemsetAsync(h->status, 0, 4, st));
-  OKLS_CK(launch_reset_factor(h->Sa, h->Pa, h->fa.Ph[0].p, h->fa.PhT[0].p, h->fa.Ph[1].p, h->fa.PhT[1].p,
+  OKLS_CK(launch_reset_factor(h->Sa, h->Pa, h->fa.Ph[0].p, nullptr, h->fa.Ph[1].p, nullptr,
                               static_cast<int>(c.m), h->fa.Ph[0].ld, h->fa.Ph[0].mat(), static_cast<int>(c.batch),
                               c.eps, h->scal,
                               static_cast<int>(c.batch), SC_PI_A, st));
-  OKLS_CK(launch_reset_factor(h->Sb, h->Pb, h->fb.Ph[0].p, h->fb.PhT[0].p, h->fb.Ph[1].p, h->fb.PhT[1].p,
+  OKLS_CK(launch_reset_factor(h->Sb, h->Pb, h->fb.Ph[0].p, nullptr, h->fb.Ph[1].p, nullptr,
                               static_cast<int>(c.n), h->fb.Ph[0].ld, h->fb.Ph[0].mat(), static_cast<int>(c.batch),
                               c.eps, h->scal,
                               static_cast<int>(c.batch), SC_PI_B, st));
@@ -883,14 +887,14 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
                                 h->part_g_ld, h->status, st));
   OKLS_CK(launch_coeffs_pre(B, m, n, c.beta2, h->scal, sld, h->part_g, h->part_g_ld, st));
   // row pitches: Ghat is m x n (pitch ldn), Ghat^T and Nhat^T are n x m (pitch ldm)
-  if (h->Gh.ld < n || h->GhT.ld < m || h->NhT.ld != h->GhT.ld || h->Gh.rows != m || h->GhT.rows != n)
+  if (h->Gh.ld < n || h->GhT.ld < m || h->Nh.ld != h->Gh.ld || h->Gh.rows != m || h->GhT.rows != n)
     return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: packed operand pitches");
-  OKLS_CK(launch_pack(G, gbf, h->M, h->Gh.p, h->GhT.p, h->NhT.p, B, m, n, /*ldm=*/h->GhT.ld,
+  OKLS_CK(launch_pack(G, gbf, h->M, h->Gh.p, h->GhT.p, h->Nh.p, B, m, n, /*ldm=*/h->GhT.ld,
                       /*ldn=*/h->Gh.ld, c.beta1, kappa, h->scal, sld, h->status, st));
   // 3. X_b = G P_b and X_a^T = G^T P_a^T (previous roots)
   {
     LaunchBuilder lb;
-    GemmProblem& p0 = lb.add_bsplit(h->Gh, h->fb.PhT, h->fb.split, m, n, n, B, EPI_X16);
+    GemmProblem& p0 = lb.add_bsplit(h->Gh, h->fb.Ph, h->fb.split, m, n, n, B, EPI_X16, true);
     set_out16(p0, h->Xb, nullptr, nullptr, nullptr);
     p0.alpha = std::ldexp(1.0f, -h12);
     p0.check_finite = 1;
@@ -944,7 +948,7 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
   // 7. Q = P_a N  (into the X_b buffer)
   {
     LaunchBuilder lb;
-    GemmProblem& p = lb.add_asplit(h->fa.Ph, h->NhT, h->fa.split, m, n, m, B, EPI_X16);
+    GemmProblem& p = lb.add_asplit(h->fa.Ph, h->Nh, h->fa.split, m, n, m, B, EPI_X16, true);
     set_out16(p, h->Xb, nullptr, nullptr, nullptr);
     p.alpha = std::ldexp(1.0f, -h12);
     p.check_finite = 1;
@@ -953,7 +957,7 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
   // 8. U = Q P_b, W <- W (1 - lr wd lr/lr_peak) - lr c_shape U
   {
     LaunchBuilder lb;
-    GemmProblem& p = lb.add_bsplit(h->Xb, h->fb.PhT, h->fb.split, m, n, n, B, EPI_UPDATE);
+    GemmProblem& p = lb.add_bsplit(h->Xb, h->fb.Ph, h->fb.split, m, n, n, B, EPI_UPDATE, true);
     p.w = W;
     p.w_bf16 = c.param_dtype == OKLS_BF16;
     p.ld32 = n;
@@ -1016,12 +1020,12 @@ okls_status okls_set_state(okls_handle h, int32_t part, const void* src, void* s
   OKLS_CK(cudaMemcpyAsync(p, src, bytes, cudaMemcpyDeviceToDevice, st));
   const okls_config& c = h->cfg;
   if (part == OKLS_STATE_PA)
-    OKLS_CK(launch_requant(h->Pa, static_cast<int>(c.batch), static_cast<int>(c.m), h->fa.Ph[0].p, h->fa.PhT[0].p,
-                           h->fa.Ph[1].p, h->fa.PhT[1].p, h->fa.Ph[0].ld, h->fa.Ph[0].mat(), h->scal,
+    OKLS_CK(launch_requant(h->Pa, static_cast<int>(c.batch), static_cast<int>(c.m), h->fa.Ph[0].p, nullptr,
+                           h->fa.Ph[1].p, nullptr, h->fa.Ph[0].ld, h->fa.Ph[0].mat(), h->scal,
                            static_cast<int>(c.batch), SC_PI_A, st));
   if (part == OKLS_STATE_PB)
-    OKLS_CK(launch_requant(h->Pb, static_cast<int>(c.batch), static_cast<int>(c.n), h->fb.Ph[0].p, h->fb.PhT[0].p,
-                           h->fb.Ph[1].p, h->fb.PhT[1].p, h->fb.Ph[0].ld, h->fb.Ph[0].mat(), h->scal,
+    OKLS_CK(launch_requant(h->Pb, static_cast<int>(c.batch), static_cast<int>(c.n), h->fb.Ph[0].p, nullptr,
+                           h->fb.Ph[1].p, nullptr, h->fb.Ph[0].ld, h->fb.Ph[0].mat(), h->scal,
                            static_cast<int>(c.batch), SC_PI_B, st));
   return OKLS_OK;
 }

@@ -6,8 +6,8 @@
 //                     variance correction); flags non-finite inputs.
 //   k_coeffs_pre      per-matrix power-of-two scales of G and N and the EMA
 //                     weights of both factors.
-//   k_pack            writes M_t, Ghat, Ghat^T and Nhat^T (binary16, scaled)
-//                     through 32x32 shared-memory tiles (coalesced both ways).
+//   k_pack            writes M_t, Ghat, Nhat and Ghat^T (binary16, scaled);
+//                     the transpose goes through 32x32 shared-memory tiles.
 //   k_coeffs_post     normaliser c' of each factor, the root scales pi and
 //                     the whitening coefficient.
 //   k_normalise       Y_0 = (S + rho c I)/c', T_0 = a_0 I + b_0 Y_0, Z_1 = T_0
@@ -115,11 +115,10 @@ __global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float
 // ------------------------------------------------------------------ pack
 template <typename GT>
 __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* __restrict__ Gh,
-                       __half* __restrict__ GhT, __half* __restrict__ NhT, int m, int n, int64_t ldm,
+                       __half* __restrict__ GhT, __half* __restrict__ Nh, int m, int n, int64_t ldm,
                        int64_t ldn, float b1, float kappa, const float* scal, int scal_ld,
                        const uint32_t* status) {
   __shared__ float sg[32][33];
-  __shared__ float sn[32][33];
   if (*reinterpret_cast<const volatile uint32_t*>(status) != 0u) return;
   const int b = blockIdx.z;
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
@@ -129,6 +128,7 @@ __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* 
   const GT* g = G + b * mn;
   float* mo = M + b * mn;
   __half* gh = Gh + b * static_cast<int64_t>(m) * ldn;
+  __half* nh = Nh + b * static_cast<int64_t>(m) * ldn;
   const int tx = threadIdx.x;
   for (int r = threadIdx.y; r < 32; r += 8) {
     const int i = r0 + r, j = c0 + tx;
@@ -140,19 +140,15 @@ __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* 
       nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
       mo[e] = mn1;
       gh[static_cast<int64_t>(i) * ldn + j] = __float2half_rn(gv * gs);
+      nh[static_cast<int64_t>(i) * ldn + j] = __float2half_rn(nv * ns);
     }
     sg[r][tx] = gv * gs;
-    sn[r][tx] = nv * ns;
   }
   __syncthreads();
   __half* gt = GhT + b * static_cast<int64_t>(n) * ldm;
-  __half* nt = NhT + b * static_cast<int64_t>(n) * ldm;
   for (int c = threadIdx.y; c < 32; c += 8) {
     const int j = c0 + c, i = r0 + tx;
-    if (i < m && j < n) {
-      gt[static_cast<int64_t>(j) * ldm + i] = __float2half_rn(sg[tx][c]);
-      nt[static_cast<int64_t>(j) * ldm + i] = __float2half_rn(sn[tx][c]);
-    }
+    if (i < m && j < n) gt[static_cast<int64_t>(j) * ldm + i] = __float2half_rn(sg[tx][c]);
   }
 }
 
@@ -224,31 +220,31 @@ __global__ void k_normalise(NormaliseArgs A) {
     if (A.split_y) {
       const __half yl = __float2half_rn(y - yv);
       A.Ylo[e] = yl;
-      A.YTlo[e] = yl;
+      if (A.YTlo) A.YTlo[e] = yl;
       yv += __half2float(yl);
     }
     A.Y[e] = yh;
-    A.YT[e] = yh;
+    if (A.YT) A.YT[e] = yh;
     const float t = fmaf(A.b0, yv, i == j ? a0h : 0.0f);
     const __half th = __float2half_rn(t);
     float tv = __half2float(th);
     if (A.split_t) {
       const __half tl = __float2half_rn(t - tv);
       A.Tlo[e] = tl;
-      A.TTlo[e] = tl;
+      if (A.TTlo) A.TTlo[e] = tl;
       tv += __half2float(tl);
     }
     A.T[e] = th;
-    A.TT[e] = th;
+    if (A.TT) A.TT[e] = th;
     const float z = tv * zsc;
     const __half zh = __float2half_rn(z);
     if (A.split_z) {
       const __half zl = __float2half_rn(z - __half2float(zh));
       A.Zlo[e] = zl;
-      A.ZTlo[e] = zl;
+      if (A.ZTlo) A.ZTlo[e] = zl;
     }
     A.Z[e] = zh;
-    A.ZT[e] = zh;
+    if (A.ZT) A.ZT[e] = zh;
     if (!isfinite(y) && A.status) atomicOr(A.status, kStNonfiniteIter);
   }
 }
@@ -328,7 +324,7 @@ __global__ void k_requant(const float* __restrict__ P, int d, __half* Ph, __half
     if (i < d && j < d) {
       const float v = t[tx][c];
       const __half hv = __float2half_rn(v);
-      PhT[b * mat16 + static_cast<int64_t>(j) * ld16 + i] = hv;
+      if (PhT) PhT[b * mat16 + static_cast<int64_t>(j) * ld16 + i] = hv;
       if (PlT) PlT[b * mat16 + static_cast<int64_t>(j) * ld16 + i] = __float2half_rn(v - __half2float(hv));
     }
   }
@@ -350,7 +346,7 @@ __global__ void k_reset_factor(float* S, float* P, __half* Ph, __half* PhT, __ha
     P[e] = diag ? 1.0f : 0.0f;
     const int64_t o = b * mat16 + i * ld16 + j;
     Ph[o] = diag ? one : zero;
-    PhT[o] = diag ? one : zero;
+    if (PhT) PhT[o] = diag ? one : zero;
     if (Pl) Pl[o] = zero;
     if (PlT) PlT[o] = zero;
   }
@@ -393,15 +389,15 @@ cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, floa
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* NhT,
+cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* Nh,
                         int batch, int m, int n, int64_t ldm, int64_t ldn, float b1, float kappa,
                         const float* scal, int scal_ld, const uint32_t* status, cudaStream_t st) {
   dim3 grid((n + 31) / 32, (m + 31) / 32, batch), block(32, 8);
   if (g_bf16)
-    k_pack<__nv_bfloat16><<<grid, block, 0, st>>>(static_cast<const __nv_bfloat16*>(G), M, Gh, GhT, NhT,
+    k_pack<__nv_bfloat16><<<grid, block, 0, st>>>(static_cast<const __nv_bfloat16*>(G), M, Gh, GhT, Nh,
                                                   m, n, ldm, ldn, b1, kappa, scal, scal_ld, status);
   else
-    k_pack<float><<<grid, block, 0, st>>>(static_cast<const float*>(G), M, Gh, GhT, NhT, m, n, ldm, ldn,
+    k_pack<float><<<grid, block, 0, st>>>(static_cast<const float*>(G), M, Gh, GhT, Nh, m, n, ldm, ldn,
                                           b1, kappa, scal, scal_ld, status);
   return cudaGetLastError();
 }

@@ -96,7 +96,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
             uint8_t* sb = sa + kStageABytes;
             mbar_expect_tx(&full[stage], kStageBytes);
             tma_load_3d(sa, am, &full[stage], kb * kBK, tc.tm * kBM, tc.mat);
-            tma_load_3d(sb, bm, &full[stage], kb * kBK, tc.tn * kBN, tc.mat);
+            if (P.bmn) {
+              // B stored K x N: four 64 (N) x 64 (K) boxes, 8 KB apart
+#pragma unroll
+              for (int c = 0; c < kBN / 64; ++c)
+                tma_load_3d(sb + c * 8192, bm, &full[stage], tc.tn * kBN + c * 64, kb * kBK, tc.mat);
+            } else {
+              tma_load_3d(sb, bm, &full[stage], kb * kBK, tc.tn * kBN, tc.mat);
+            }
             ++issued;
             if (++stage == kStages) {
               stage = 0;
@@ -118,7 +125,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_f16_f32(kBM, kBN);
+      constexpr uint32_t idesc_k = idesc_f16_f32(kBM, kBN, false);
+      constexpr uint32_t idesc_mn = idesc_f16_f32(kBM, kBN, true);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x, ++it) {
@@ -138,10 +146,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
           const uint32_t b0 = a0 + kStageABytes;
+          if (P.bmn) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-            umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_desc(b0 + kk * kUmmaK * 2), idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+              umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_mn_desc(b0 + kk * kUmmaK * 128), idesc_mn,
+                       (kb | kk) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+              umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_desc(b0 + kk * kUmmaK * 2), idesc_k,
+                       (kb | kk) != 0 ? 1u : 0u);
+          }
           umma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;

@@ -108,7 +108,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             if (leader) mbar_expect_tx(&full[stage], 2 * kPairStageBytes);
             const uint32_t fb = full_leader + stage * 8u;
             tma_load_3d_pair(sa, am, fb, kb * kBK, row_a, tc.mat);
-            tma_load_3d_pair(sb, bm, fb, kb * kBK, row_b, tc.mat);
+            if (P.bmn) {
+              // this CTA's 128 columns of a K x N B: two 64 x 64 boxes, 8 KB apart
+              tma_load_3d_pair(sb, bm, fb, row_b, kb * kBK, tc.mat);
+              tma_load_3d_pair(sb + 8192, bm, fb, row_b + 64, kb * kBK, tc.mat);
+            } else {
+              tma_load_3d_pair(sb, bm, fb, kb * kBK, row_b, tc.mat);
+            }
             ++issued;
             if (++stage == kPairStages) {
               stage = 0;
@@ -133,7 +139,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------- MMA issuer (leader)
-      constexpr uint32_t idesc = idesc_f16_f32(256, kBN);
+      constexpr uint32_t idesc_k = idesc_f16_f32(256, kBN, false);
+      constexpr uint32_t idesc_mn = idesc_f16_f32(256, kBN, true);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int64_t t = pair_id; t < L.total_tiles && ok; t += npairs, ++it) {
@@ -153,10 +160,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + stage * kPairStageBytes);
           const uint32_t b0 = a0 + kPairStageA;
+          if (P.bmn) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-            umma_f16_pair(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_desc(b0 + kk * kUmmaK * 2), idesc,
-                          (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+              umma_f16_pair(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_mn_desc(b0 + kk * kUmmaK * 128), idesc_mn,
+                            (kb | kk) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+              umma_f16_pair(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_desc(b0 + kk * kUmmaK * 2), idesc_k,
+                            (kb | kk) != 0 ? 1u : 0u);
+          }
           umma_commit_pair(&empty[stage], 0x3);
           if (++stage == kPairStages) {
             stage = 0;

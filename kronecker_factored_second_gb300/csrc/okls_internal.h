@@ -70,8 +70,10 @@ struct GemmProblem {
   // B: box 256 rows) into the handle's descriptor table
   int32_t nseg;
   int32_t amap[kMaxSeg];        // A descriptors, 128-row boxes
-  int32_t bmap[kMaxSeg];        // B descriptors, 256-row boxes (one CTA per tile)
-  int32_t bmap_pair[kMaxSeg];   // B descriptors, 128-row boxes (CTA pairs: each loads half of B)
+  int32_t bmap[kMaxSeg];        // B descriptors: K-major 256-row boxes (one CTA per tile), or
+                                // MN-major 64x64 boxes when bmn
+  int32_t bmap_pair[kMaxSeg];   // B descriptors for CTA pairs: K-major 128-row boxes, or MN-major
+  int32_t bmn;                  // 1: B is stored K x N row-major (MN-major operand)
   int32_t rows, cols, K;        // output rows (A rows), cols (B rows), K
   int32_t batch;
   int32_t tiles_m, tiles_n;

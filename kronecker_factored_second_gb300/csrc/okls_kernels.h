@@ -39,7 +39,7 @@ cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int
                                   cudaStream_t st);
 cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal, int scal_ld,
                               const float* part, int64_t part_ld, cudaStream_t st);
-cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* NhT,
+cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* Nh,
                         int batch, int m, int n, int64_t ldm, int64_t ldn, float b1, float kappa,
                         const float* scal, int scal_ld, const uint32_t* status, cudaStream_t st);
 cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,

@@ -91,11 +91,23 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
+// Shared-memory descriptor of an MN-major operand written by TMA as 64 x 64
+// boxes with 128-byte swizzling: each k holds 64 consecutive MN elements
+// (128 B), 8 k form a 1024-byte atom (stride byte offset = 1024 between
+// 8-k groups), and the next 64-wide MN chunk starts 8 KB later (leading byte
+// offset).  Advancing K by 16 moves the start by 16 x 128 B.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(8192 >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B binary16 (format 0), both K-major, N >> 3 at bits 17-22,
-// M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// A and B binary16 (format 0), A K-major, B K-major or MN-major (bit 16),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn = false) {
+  return (1u << 4) | (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
