@@ -7,7 +7,8 @@
 //   3. X_b = G P_b, X_a^T = G^T P_a^T             GEMM (EPI_X16)
 //      (B operands stored K x N are read MN-major, so every binary16 matrix
 //      is kept in one row-major layout; only Ghat^T is materialised)
-//   4. S_a, S_b EMAs (+ ||S||_F^2)                 GEMM (EPI_SYRK, upper tiles)
+//   4. S_a, S_b EMAs (+ ||S||_F^2)                 GEMM (EPI_SYRK, upper triangle;
+//      the normaliser of step 5 writes the mirrored lower triangle)
 //   5. normalisers, Y_0, T_0, Z_1                  k_coeffs_post, k_normalise
 //   6. coupled Newton-Schulz, both factors         19 GEMM launches, 27 products
 //   7. Q = P_a N                                    GEMM (EPI_X16)
@@ -227,6 +228,7 @@ struct Factor {
   int d = 0;
   int batch = 0;
   float* S = nullptr;       // fp32 input
+  bool S_upper_only = false;  // S comes from the factor product: upper triangle only
   float* P32 = nullptr;     // fp32 output
   float* root32 = nullptr;  // debug root output
   Buf Ph[2];                         // binary16 P (hi, lo), row-major
@@ -527,6 +529,7 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
     NormaliseArgs A;
     memset(&A, 0, sizeof(A));
     A.S = f.S;
+    A.upper_only = f.S_upper_only ? 1 : 0;
     A.d = f.d;
     A.ld16 = f.Y[0][0].ld;
     A.mat16 = f.Y[0][0].mat();
@@ -703,6 +706,7 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
     h->Pa = Pa;
     h->Pb = Pb;
     fa.S = Sa;
+    fa.S_upper_only = true;
     fa.P32 = Pa;
     fa.slot_sumsq = SC_SUMSQ_SA;
     fa.slot_cprime = SC_CPRIME_A;
@@ -710,6 +714,7 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
     fa.slot_pscale = SC_PSCALE_A;
     fa.slot_rscale = SC_RSCALE_A;
     fb.S = Sb;
+    fb.S_upper_only = true;
     fb.P32 = Pb;
     fb.slot_sumsq = SC_SUMSQ_SB;
     fb.slot_cprime = SC_CPRIME_B;

@@ -192,9 +192,11 @@ __global__ void k_normalise(NormaliseArgs A) {
   const int b = blockIdx.z;
   const int d = A.d;
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  const float* S = A.S + static_cast<int64_t>(b) * d * d;
+  float* S = A.S + static_cast<int64_t>(b) * d * d;
   const int tx = threadIdx.x;
-  // tile (r0, c0) and the transposed tile (c0, r0) for the symmetric part
+  // tile (r0, c0) and the transposed tile (c0, r0); for upper-only input the
+  // value of (i, j) is read from whichever of the two holds it on or above the
+  // diagonal (only those elements are ever read, and only lower ones written)
   for (int r = threadIdx.y; r < 32; r += 8) {
     const int i = r0 + r, j = c0 + tx;
     t1[r][tx] = (i < d && j < d) ? S[static_cast<int64_t>(i) * d + j] : 0.0f;
@@ -212,7 +214,13 @@ __global__ void k_normalise(NormaliseArgs A) {
   for (int r = threadIdx.y; r < 32; r += 8) {
     const int i = r0 + r, j = c0 + tx;
     if (i >= d || j >= d) continue;
-    const float s = 0.5f * (t1[r][tx] + t2[tx][r]);
+    float s;
+    if (A.upper_only) {
+      s = (i <= j) ? t1[r][tx] : t2[tx][r];
+      if (i > j) S[static_cast<int64_t>(i) * d + j] = s;  // mirror into the state
+    } else {
+      s = 0.5f * (t1[r][tx] + t2[tx][r]);
+    }
     const float y = (s + (i == j ? rc : 0.0f)) * inv;
     const int64_t e = moff + static_cast<int64_t>(i) * A.ld16 + j;
     const __half yh = __float2half_rn(y);

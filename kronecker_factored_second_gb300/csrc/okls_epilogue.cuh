@@ -163,19 +163,32 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, const TileC
       break;
     }
     case EPI_SYRK: {
-      // only elements on or above the diagonal; mirrored below
+      // S <- beta2 S + alpha acc + gamma I on and above the diagonal only; the
+      // lower triangle is written later by the normaliser
       const float alpha = scal_at(P, P.scal_slot, tc.mat);
-      float* S = P.out32 + static_cast<int64_t>(tc.mat) * P.mat32;
+      float* S = P.out32 + static_cast<int64_t>(tc.mat) * P.mat32 + static_cast<int64_t>(i) * P.ld32 + j0;
+      if (j0 + 32 <= i) break;  // chunk entirely below the diagonal
+      if (j0 >= i + 1 && nvalid == 32 && (P.ld32 & 3) == 0) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = j0 + e;
-        if (e < nvalid && j >= i) {
-          const int64_t a = static_cast<int64_t>(i) * P.ld32 + j;
-          float s = fmaf(P.beta, S[a], alpha * v[e]);
-          if (j == i) s += P.gamma;
-          S[a] = s;
-          if (j != i) S[static_cast<int64_t>(j) * P.ld32 + i] = s;
-          sumsq += (j == i ? 1.0f : 2.0f) * s * s;
+        for (int q = 0; q < 8; ++q) {
+          float4 o = *reinterpret_cast<float4*>(S + 4 * q);
+          o.x = fmaf(P.beta, o.x, alpha * v[4 * q + 0]);
+          o.y = fmaf(P.beta, o.y, alpha * v[4 * q + 1]);
+          o.z = fmaf(P.beta, o.z, alpha * v[4 * q + 2]);
+          o.w = fmaf(P.beta, o.w, alpha * v[4 * q + 3]);
+          *reinterpret_cast<float4*>(S + 4 * q) = o;
+          sumsq += 2.0f * (o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = j0 + e;
+          if (e < nvalid && j >= i) {
+            float s = fmaf(P.beta, S[e], alpha * v[e]);
+            if (j == i) s += P.gamma;
+            S[e] = s;
+            sumsq += (j == i ? 1.0f : 2.0f) * s * s;
+          }
         }
       }
       break;

@@ -9,7 +9,10 @@
 namespace okls {
 
 struct NormaliseArgs {
-  const float* S;   // batch x d x d fp32 (symmetrised on the fly)
+  float* S;         // batch x d x d fp32
+  int upper_only;   // 1: only S's upper triangle is current (factor-product output):
+                    //    read it and write the mirrored lower triangle back;
+                    // 0: S is a full input, symmetrised as (S + S^T)/2, not written
   int d;
   int64_t ld16, mat16;
   __half *Y, *YT, *Ylo, *YTlo;   // Y_0 (both layouts; equal by symmetry)
