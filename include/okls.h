@@ -92,6 +92,12 @@ typedef enum okls_state_part {
  *                   iid unit-variance gradients; 0: plain Nesterov.
  *   eps_every_update 1: +eps I in every factor update (and S_0 = eps I);
  *                   0: only S_0 = eps I.
+ *   root_every      k >= 1 (0 means 1): fresh inverse roots at steps
+ *                   t = 1, 1+k, 1+2k, ...; the steps in between still update
+ *                   the factors and the momentum but whiten with the roots
+ *                   of the last refresh (the practice of recomputing Shampoo
+ *                   roots every 20-100 steps; k = 1 is the README's
+ *                   zero-staleness method).
  */
 typedef struct okls_config {
   int64_t batch;
@@ -110,7 +116,8 @@ typedef struct okls_config {
   float ridge;
   int32_t variance_correction;
   int32_t eps_every_update;
-  int32_t reserved[8]; /* must be zero */
+  int32_t root_every;
+  int32_t reserved[7]; /* must be zero */
 } okls_config;
 
 typedef struct okls_handle_s *okls_handle;

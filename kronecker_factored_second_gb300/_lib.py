@@ -52,7 +52,8 @@ class okls_config(ctypes.Structure):
         ("ridge", ctypes.c_float),
         ("variance_correction", ctypes.c_int32),
         ("eps_every_update", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 8),
+        ("root_every", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 7),
     ]
 
 

@@ -771,7 +771,8 @@ okls_status validate(const okls_config* c) {
     return fail(OKLS_ERR_INVALID_ARG, "ns_split_iters must be in [0, ns_iters]");
   if (!(c->ns_lo > 0.0f && c->ns_lo < 1.0f)) return fail(OKLS_ERR_INVALID_ARG, "ns_lo must be in (0, 1)");
   if (!finite_nonneg(c->ridge)) return fail(OKLS_ERR_INVALID_ARG, "ridge must be finite and >= 0");
-  for (int i = 0; i < 8; ++i)
+  if (c->root_every < 0) return fail(OKLS_ERR_INVALID_ARG, "root_every must be >= 0 (0 means 1)");
+  for (int i = 0; i < 7; ++i)
     if (c->reserved[i] != 0) return fail(OKLS_ERR_INVALID_ARG, "reserved fields must be zero");
   return OKLS_OK;
 }
@@ -806,6 +807,7 @@ okls_status okls_config_default(okls_config* cfg, int64_t batch, int64_t m, int6
   cfg->ridge = 1e-3f;
   cfg->variance_correction = 1;
   cfg->eps_every_update = 1;
+  cfg->root_every = 1;
   return OKLS_OK;
 }
 
@@ -937,18 +939,36 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
     pb.gamma = eps_u;
     if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
   }
-  // 5-6. fresh inverse roots of both factors
+  // 5-6. fresh inverse roots of both factors (every root_every-th step; the
+  // steps in between keep P, its binary16 copy and its scales)
   const int K = h->sched.iters;
+  const int64_t every = c.root_every > 1 ? c.root_every : 1;
+  const bool fresh = ((t1 - 1) % every) == 0;
   // the factor products ran as one launch: pair tiles iff either factor is taller than 128
   const bool syrk_pair = use_pair(std::max(m, n));
-  OKLS_CK(launch_coeffs_post(B, c.ridge, h->sched.z[K], h->sched.z[K - 1], h->scal, sld, 1, h->status, h->part_a,
-                             h->part_a_ld, syrk_parts(m, syrk_pair), h->part_b, h->part_b_ld,
-                             syrk_parts(n, syrk_pair), st));
-  {
+  OKLS_CK(launch_coeffs_post(B, c.ridge, h->sched.z[K], h->sched.z[K - 1], h->scal, sld, 1, fresh ? 1 : 0,
+                             h->status, h->part_a, h->part_a_ld, syrk_parts(m, syrk_pair), h->part_b,
+                             h->part_b_ld, syrk_parts(n, syrk_pair), st));
+  if (fresh) {
     Factor* fs[2] = {&h->fa, &h->fb};
     if ((s = run_ns(fs, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
                     nullptr)) != OKLS_OK)
       return s;
+  } else {
+    // keep the state symmetric: write the lower triangles of the new factors
+    for (Factor* f : {&h->fa, &h->fb}) {
+      NormaliseArgs A;
+      memset(&A, 0, sizeof(A));
+      A.S = f->S;
+      A.upper_only = 1;
+      A.mirror_only = 1;
+      A.d = f->d;
+      A.scal = h->scal;
+      A.scal_ld = sld;
+      A.status = h->status;
+      OKLS_CK(launch_normalise(A, f->batch, st));
+      note_kernels(1);
+    }
   }
   // 7. Q = P_a N  (into the X_b buffer)
   {
@@ -1164,7 +1184,7 @@ okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace
   const Sched sc = make_schedule(iters, lo);
   OKLS_CK(launch_sumsq(S, static_cast<int>(count), d * d, part, factor_parts(d), st));
   OKLS_CK(launch_coeffs_post(static_cast<int>(count), ridge, sc.z[iters], sc.z[iters - 1], scal,
-                             static_cast<int>(count), 0, status, part, factor_parts(d), sumsq_parts(d * d),
+                             static_cast<int>(count), 0, 1, status, part, factor_parts(d), sumsq_parts(d * d),
                              nullptr, 0, 0, st));
   TraceOut tr;
   tr.base = trace;

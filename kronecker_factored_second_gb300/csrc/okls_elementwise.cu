@@ -154,7 +154,7 @@ __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* 
 
 // -------------------------------------------------------------- post scalars
 __global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                              int with_update, const uint32_t* status, const float* part_a,
+                              int with_update, int with_roots, const uint32_t* status, const float* part_a,
                               int64_t part_a_ld, int64_t npart_a, const float* part_b, int64_t part_b_ld,
                               int64_t npart_b) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -167,7 +167,7 @@ __global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* sc
   if (part_b) S(SC_SUMSQ_SB) = static_cast<float>(sum_parts(part_b + b * part_b_ld, npart_b));
   const double margin = 1.0 + ldexp(1.0, -8);
   const int h = kHeadroom;
-  for (int f = 0; f < 2; ++f) {
+  for (int f = 0; f < 2 && with_roots; ++f) {
     const int s_sum = f == 0 ? SC_SUMSQ_SA : SC_SUMSQ_SB;
     double c = sqrt(static_cast<double>(S(s_sum)));
     double cp = c * (1.0 + ridge) * margin;
@@ -221,6 +221,7 @@ __global__ void k_normalise(NormaliseArgs A) {
     } else {
       s = 0.5f * (t1[r][tx] + t2[tx][r]);
     }
+    if (A.mirror_only) continue;
     const float y = (s + (i == j ? rc : 0.0f)) * inv;
     const int64_t e = moff + static_cast<int64_t>(i) * A.ld16 + j;
     const __half yh = __float2half_rn(y);
@@ -411,11 +412,12 @@ cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half*
 }
 
 cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                               int with_update, const uint32_t* status, const float* part_a, int64_t part_a_ld,
+                               int with_update, int with_roots, const uint32_t* status, const float* part_a,
+                               int64_t part_a_ld,
                                int64_t npart_a, const float* part_b, int64_t part_b_ld, int64_t npart_b,
                                cudaStream_t st) {
   k_coeffs_post<<<(batch + 127) / 128, 128, 0, st>>>(batch, ridge, zK, zK1, scal, scal_ld, with_update,
-                                                     status, part_a, part_a_ld, npart_a, part_b, part_b_ld,
+                                                     with_roots, status, part_a, part_a_ld, npart_a, part_b, part_b_ld,
                                                      npart_b);
   return cudaGetLastError();
 }

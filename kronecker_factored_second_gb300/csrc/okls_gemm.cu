@@ -125,8 +125,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
+      // a tile with at most 128 valid columns (the edge of a 5504-wide product)
+      // runs N = 128 MMAs; the epilogue never reads the unused columns
       constexpr uint32_t idesc_k = idesc_f16_f32(kBM, kBN, false);
       constexpr uint32_t idesc_mn = idesc_f16_f32(kBM, kBN, true);
+      constexpr uint32_t idesc_k_half = idesc_f16_f32(kBM, kBN / 2, false);
+      constexpr uint32_t idesc_mn_half = idesc_f16_f32(kBM, kBN / 2, true);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x, ++it) {
@@ -138,6 +142,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         if (!mbar_wait(&acc_empty[buf], aph ^ 1u, L.status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kBN;
+        const bool half_n = P.cols - tc.tn * kBN <= kBN / 2;
+        const uint32_t id_k = half_n ? idesc_k_half : idesc_k;
+        const uint32_t id_mn = half_n ? idesc_mn_half : idesc_mn;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, L.status)) {
             ok = false;
@@ -149,12 +156,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
           if (P.bmn) {
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-              umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_mn_desc(b0 + kk * kUmmaK * 128), idesc_mn,
+              umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_mn_desc(b0 + kk * kUmmaK * 128), id_mn,
                        (kb | kk) != 0 ? 1u : 0u);
           } else {
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-              umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_desc(b0 + kk * kUmmaK * 2), idesc_k,
+              umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_desc(b0 + kk * kUmmaK * 2), id_k,
                        (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit(&empty[stage]);

@@ -10,6 +10,7 @@ namespace okls {
 
 struct NormaliseArgs {
   float* S;         // batch x d x d fp32
+  int mirror_only;  // 1: only write S's mirrored lower triangle (steps that keep the roots)
   int upper_only;   // 1: only S's upper triangle is current (factor-product output):
                     //    read it and write the mirrored lower triangle back;
                     // 0: S is a full input, symmetrised as (S + S^T)/2, not written
@@ -46,7 +47,8 @@ cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half*
                         int batch, int m, int n, int64_t ldm, int64_t ldn, float b1, float kappa,
                         const float* scal, int scal_ld, const uint32_t* status, cudaStream_t st);
 cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                               int with_update, const uint32_t* status, const float* part_a, int64_t part_a_ld,
+                               int with_update, int with_roots, const uint32_t* status, const float* part_a,
+                               int64_t part_a_ld,
                                int64_t npart_a, const float* part_b, int64_t part_b_ld, int64_t npart_b,
                                cudaStream_t st);
 cudaError_t launch_normalise(const NormaliseArgs& A, int batch, cudaStream_t st);

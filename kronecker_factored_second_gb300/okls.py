@@ -45,7 +45,7 @@ class OklsBatch:
                  beta2: float = 0.9482, eps: float = 1e-9, weight_decay: float = 0.0303,
                  ns_iters: int = 10, ns_split_iters: int = 0, ns_lo: float = 1e-3,
                  ridge: float = 1e-3, variance_correction: bool = True,
-                 eps_every_update: bool = True, device=None):
+                 eps_every_update: bool = True, root_every: int = 1, device=None):
         lib = L.lib()
         cfg = L.config_default(batch, m, n)
         cfg.param_dtype = _DT[param_dtype]
@@ -55,6 +55,7 @@ class OklsBatch:
         cfg.ns_iters, cfg.ns_split_iters, cfg.ns_lo, cfg.ridge = ns_iters, ns_split_iters, ns_lo, ridge
         cfg.variance_correction = int(variance_correction)
         cfg.eps_every_update = int(eps_every_update)
+        cfg.root_every = int(root_every)
         self.cfg = cfg
         self.batch, self.m, self.n = batch, m, n
         self.param_dtype = param_dtype

@@ -73,6 +73,7 @@ class Hyper:
     ridge: float = 0.0                # rho of reading r10
     variance_correction: bool = True  # reading r5
     eps_every_update: bool = True     # reading r2
+    root_every: int = 1               # fresh roots at t = 1, 1+k, 1+2k, ... (1: every step)
 
     @property
     def peak(self) -> float:
@@ -401,8 +402,11 @@ def okls_step(state: OklsState, W: np.ndarray, G: np.ndarray, lr: float,
     eps_upd = hp.eps if hp.eps_every_update else 0.0
     Sa = factor_ema(state.Sa, G @ state.Pb, b2, n, eps_upd)
     Sb = factor_ema(state.Sb, (state.Pa @ G).T, b2, m, eps_upd)
-    # fresh roots in the same step
-    if root == "exact":
+    # fresh roots in the same step ('How it works'); with root_every = k > 1
+    # only at t = 1, 1+k, ... and the previous roots in between
+    if (t - 1) % max(1, hp.root_every) != 0:
+        Pa, Pb = state.Pa, state.Pb
+    elif root == "exact":
         Pa, Pb = inv_root_exact(Sa, hp.ridge), inv_root_exact(Sb, hp.ridge)
     elif root == "ns_exact":
         sch = cans_schedule(hp.ns_iters, hp.ns_lo)

@@ -149,13 +149,14 @@ def test_inv_root_root_output():
 MODES = [pytest.param((0, 1e-3), id="fp16-ridge1e-3"), pytest.param((3, 1e-4), id="split3-ridge1e-4")]
 
 
-def _run(wl, steps, mode=(0, 1e-3), sample=None, lr_sched=None):
+def _run(wl, steps, mode=(0, 1e-3), sample=None, lr_sched=None, root_every=1, check_stale=False):
     okls = _okls()
     split, ridge = mode
     gs = GradientStream(wl, "cpu")
     worst = {}
     for gi, g in enumerate(wl.groups):
-        ob = okls.OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=split, ridge=ridge)
+        ob = okls.OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=split, ridge=ridge,
+                            root_every=root_every)
         hp = hyper_of(ob)
         W = gs.init_weights(gi).cuda()
         mats = range(g.batch) if sample is None else [b for b in sample if b < g.batch]
@@ -169,6 +170,11 @@ def _run(wl, steps, mode=(0, 1e-3), sample=None, lr_sched=None):
             post = snapshot(ob)
             W_new = W.double().cpu().numpy()
             Gn = G.double().cpu().numpy()
+            if check_stale and (t - 1) % root_every != 0:
+                # roots kept bit for bit between refreshes; the factors still move
+                assert np.array_equal(post["Pa"], pre["Pa"]) and np.array_equal(post["Pb"], pre["Pb"])
+                assert not np.array_equal(post["Sa"], pre["Sa"])
+                assert np.array_equal(post["Sa"], np.swapaxes(post["Sa"], 1, 2))
             for b in mats:
                 e = compare_step(pre, post, b, W_prev[b], W_new[b], Gn[b], lr, hp, t - 1)
                 msg = (wl.name, g.name, t, b, {k: f"{v:.2e}" for k, v in e.items()})
@@ -253,6 +259,13 @@ def test_step_rectangular_extremes_scaled(mode):
 @pytest.mark.parametrize("mode", MODES)
 def test_step_heavy_tailed_scaled(mode):
     _run(workload("llama7b_slice", scale=32, layers=1), 3, mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_step_stale_roots_every_three(mode):
+    """Roots refreshed at t = 1, 4, 7 only; every step teacher-forced."""
+    _run(workload("single128x64"), 7, mode, root_every=3, check_stale=True)
+    _run(workload("llama1.2b", scale=16, layers=1), 5, mode, root_every=3, check_stale=True)
 
 
 def test_step_lr_schedule_and_decay():

@@ -339,3 +339,27 @@ def test_step_root_modes_agree_on_a_benign_case():
     _s1, W1, U1 = O.okls_run(W0, G, hp, root="exact")
     _s2, W2, U2 = O.okls_run(W0, G, hp, root="ns_exact")
     assert O.rel_fro(U2[0], U1[0]) < 1e-3
+
+
+def test_stale_roots_refresh_schedule():
+    """root_every = k: the roots are the eigendecomposition roots of the
+    current factors at t = 1, 1+k, ... and unchanged in between, while the
+    factors keep their per-step EMA; k = 1 is the default method."""
+    rng = np.random.default_rng(19)
+    G = [rng.standard_normal((10, 6)) for _ in range(7)]
+    W0 = rng.standard_normal((10, 6)) * 0.01
+    hp3 = O.Hyper(root_every=3)
+    st = O.init_state(10, 6, hp3)
+    W = W0
+    prev = None
+    for t, g in enumerate(G, start=1):
+        st, W, _U = O.okls_step(st, W, g, hp3.lr, hp3)
+        if (t - 1) % 3 == 0:
+            assert O.rel_fro(st.Pa, O.inv_root_exact(st.Sa)) < 1e-12
+        else:
+            assert np.array_equal(st.Pa, prev.Pa) and np.array_equal(st.Pb, prev.Pb)
+            assert not np.allclose(st.Sa, prev.Sa)
+        prev = st
+    _s1, W1, _ = O.okls_run(W0, G, O.Hyper())
+    _s2, W2, _ = O.okls_run(W0, G, O.Hyper(root_every=1))
+    assert np.array_equal(W1, W2)
