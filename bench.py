@@ -43,6 +43,7 @@ def dense_flops(m: int, n: int) -> float:
 
 
 GEMM_SOURCES = ["kronecker_factored_second_gb300/csrc/okls_gemm.cu",
+                "kronecker_factored_second_gb300/csrc/okls_epilogue.cuh",
                 "kronecker_factored_second_gb300/csrc/okls_ptx.cuh",
                 "kronecker_factored_second_gb300/csrc/okls_internal.h"]
 TRAFFIC_PROFILE = "profiles/okls_gemm_kernel__llama1.2b_dram_per_launch.md"
