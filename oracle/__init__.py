@@ -1,4 +1,5 @@
-"""Float64 CPU oracle for the Online KL Shampoo (OKLS) preconditioner step.
+"""Float64 CPU oracle for the Online KL Shampoo (OKLS) preconditioner step
+and the classic Shampoo step it refines.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this package:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
@@ -19,6 +20,12 @@ Parity status per function (the pins live in ``tests/test_oracle_pins.py``):
   brute-force loops).
 * ``okls_step`` / ``okls_run``             pinned (square fixed-gradient polar
   limit, descent sign, closed-form weight decay).
+* ``shampoo_step``                         pinned (the page's 2x3 gradient fed 1,
+  4 and 100 times: step singular values 1 / 0.5 / 0.1; scale invariance of
+  Problem 14; brute-force factor sums).
+* ``quarter_root_exact``, ``quarter_root_chain``  pinned (chained exact chains
+  equal the eigendecomposition quarter root, P^4 S = I; the replay's square
+  root equals the float64 iteration's).
 * ``variance_correction``                  pinned by Monte Carlo against its
   definition (variance of the Nesterov combination for iid unit gradients);
   the *choice* of this reading is not printed on the pages.

@@ -44,6 +44,7 @@ __all__ = [
     "ns_scalar_map", "ns_exact", "ns_matrix_float64", "f16", "split16",
     "ns_replay", "ns_replay_iteration", "factor_ema", "init_state",
     "okls_step", "okls_run", "rel_fro", "NS_HEADROOM", "NS_MARGIN",
+    "quarter_root_exact", "quarter_root_chain", "shampoo_init", "shampoo_step",
 ]
 
 # Power-of-two headroom of the stored binary16 operands (reading r9): Y and T
@@ -290,7 +291,8 @@ def ns_replay(S: np.ndarray, schedule, ridge: float = 0.0, rounding: bool = True
     binary16 pairs (``split16``) and each product is hi*hi + hi*lo + lo*hi.
 
     Returns dict with P, P_hat (binary16 copy of Z_K^), pi (P ~ pi * P_hat),
-    c_prime and, if trace, the lists Y, Z, T of stored iterates (index k is
+    c_prime, root (S^1/2 ~ Y_K sqrt(c') = (Y^_{K-1} T^_{K-1}) 2^(-2h) sqrt(c'))
+    and, if trace, the lists Y, Z, T of stored iterates (index k is
     the operand of iteration k; Z[0] is None, Z_0 = I is never stored).
     """
     ident = (lambda x: np.asarray(x, dtype=np.float64))
@@ -331,14 +333,17 @@ def ns_replay(S: np.ndarray, schedule, ridge: float = 0.0, rounding: bool = True
         Th = rs(2.0 ** h * a * I + Mfac * _prod(Zh, Yh, spk), spk)
         Ts.append(Th)
         Zacc = _prod(Th, Zh, spk)
+        Yacc = _prod(Yh, Th, spk)
         if k < K - 1:
-            Yh = rs(_prod(Yh, Th, spk) * 2.0 ** -h, spn)
+            Yh = rs(Yacc * 2.0 ** -h, spn)
             Zh = rs(Zacc * 2.0 ** (z[k] - z[k + 1] - h), spn)
     k = K - 1
     P = Zacc * 2.0 ** (z[k] - 2 * h) / math.sqrt(cp)
     P_hat = r(Zacc * 2.0 ** (z[k] - z[k + 1] - h))
     pi = 2.0 ** (z[K] - h) / math.sqrt(cp)
-    out = {"P": P, "P_hat": P_hat, "pi": pi, "c_prime": cp}
+    # the square root S^1/2 ~ Y_K sqrt(c'), formed from the last (Y^, T^)
+    root = Yacc * 2.0 ** (-2 * h) * math.sqrt(cp)
+    out = {"P": P, "P_hat": P_hat, "pi": pi, "c_prime": cp, "root": root}
     if trace:
         out.update(Y=Ys, Z=Zs, T=Ts)
     return out
@@ -435,6 +440,89 @@ def okls_run(W0: np.ndarray, grads, hp: Hyper, lrs=None, root: str = "exact"):
         st, W, U = okls_step(st, W, G, lr, hp, root=root)
         Us.append(U)
     return st, W, Us
+
+
+# ---------------------------------------------------- classic Shampoo ---
+#
+# "Shampoo" chapter of the optim-book, sections "2 x 3 gradient by hand" and
+# Problem 14: the row factor L and the column factor R are plain sums of
+# G G^T and G^T G over the steps, and the step multiplies the gradient by
+# L^-1/4 on the left and R^-1/4 on the right (the -1/4 makes the step
+# invariant to the scale of G).  Readings of what the chapter leaves open:
+#   s1  L_0 = R_0 = eps I (the README's eps at factor initialisation); no eps
+#       at later steps.
+#   s2  the step is W <- W - decay - lr U with U = L^-1/4 G R^-1/4: no
+#       momentum, no shape multiplier; decay is the same decoupled term as
+#       the OKLS step (weight_decay = 0 gives the chapter's plain step).
+#   s3  L^-1/4 = (L^1/2)^-1/2: the square root from one Newton-Schulz chain
+#       (ridge rho on L) is the input of a second chain without a ridge; its
+#       condition number is at most sqrt((1+rho)/rho).  The exact reference is
+#       (L + rho ||L||_F I)^-1/4.
+#   s4  roots are refreshed every root_every steps like the OKLS roots.
+
+def quarter_root_exact(S: np.ndarray, ridge: float = 0.0) -> np.ndarray:
+    """(S + rho ||S||_F I)^-1/4 by eigendecomposition (reading s3)."""
+    S = _sym(S)
+    c = math.sqrt(float(np.sum(S * S)))
+    return sym_power(S + ridge * c * np.eye(S.shape[0]), -0.25)
+
+
+def quarter_root_chain(S: np.ndarray, schedule, ridge: float = 0.0,
+                       mode: str = "ns_exact", split_iters: int = 0) -> np.ndarray:
+    """S^-1/4 as two chained K-step Newton-Schulz runs (reading s3).
+
+    mode "ns_exact": both chains in exact arithmetic (``ns_exact``).
+    mode "replay":   both chains as the binary16 replay (``ns_replay``); the
+                     square root between them is held in float32, as the GPU
+                     keeps it.
+    """
+    if mode == "ns_exact":
+        root = ns_exact(S, schedule, ridge)[1]
+        return ns_exact(root, schedule, 0.0)[0]
+    if mode == "replay":
+        root = ns_replay(S, schedule, ridge, split_iters=split_iters)["root"]
+        root = root.astype(np.float32).astype(np.float64)
+        return ns_replay(root, schedule, 0.0, split_iters=split_iters)["P"]
+    raise ValueError(mode)
+
+
+def shampoo_init(m: int, n: int, hp: Hyper) -> OklsState:
+    """L_0 = eps I, R_0 = eps I (reading s1), roots I; M is unused."""
+    return OklsState(
+        M=np.zeros((m, n)),
+        Sa=hp.eps * np.eye(m), Sb=hp.eps * np.eye(n),
+        Pa=np.eye(m), Pb=np.eye(n), t=0)
+
+
+def shampoo_step(state: OklsState, W: np.ndarray, G: np.ndarray, lr: float,
+                 hp: Hyper, root: str = "exact"):
+    """One classic Shampoo step for one matrix in float64 (Sa = L, Sb = R,
+    Pa = L^-1/4, Pb = R^-1/4).  Returns (new_state, W_new, U).
+
+    root: "exact" (eigendecomposition), "ns_exact" (two chained K-step
+    polynomials in exact arithmetic) or "replay" (two chained binary16
+    replays of the GPU iteration).
+    """
+    G = np.asarray(G, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    m, n = G.shape
+    t = state.t + 1
+    L = state.Sa + G @ G.T
+    R = state.Sb + G.T @ G
+    if (t - 1) % max(1, hp.root_every) != 0:
+        Pa, Pb = state.Pa, state.Pb
+    elif root == "exact":
+        Pa, Pb = quarter_root_exact(L, hp.ridge), quarter_root_exact(R, hp.ridge)
+    elif root in ("ns_exact", "replay"):
+        sch = cans_schedule(hp.ns_iters, hp.ns_lo)
+        Pa = quarter_root_chain(L, sch, hp.ridge, root)
+        Pb = quarter_root_chain(R, sch, hp.ridge, root)
+    else:
+        raise ValueError(root)
+    U = Pa @ G @ Pb
+    decay = adamc_decay(lr, hp.peak, hp.weight_decay)
+    W_new = W - decay * W - lr * U
+    return OklsState(M=state.M, Sa=L, Sb=R, Pa=Pa, Pb=Pb, t=t), W_new, U
 
 
 def rel_fro(A: np.ndarray, B: np.ndarray) -> float:

@@ -363,3 +363,132 @@ def test_stale_roots_refresh_schedule():
     _s1, W1, _ = O.okls_run(W0, G, O.Hyper())
     _s2, W2, _ = O.okls_run(W0, G, O.Hyper(root_every=1))
     assert np.array_equal(W1, W2)
+
+
+# ----------------------------------------------------------- classic Shampoo
+
+def _shampoo_run(G_seq, hp, root="exact", lr=1.0):
+    m, n = np.asarray(G_seq[0]).shape
+    st = O.shampoo_init(m, n, hp)
+    W = np.zeros((m, n))
+    Us = []
+    for G in G_seq:
+        st, W, U = O.shampoo_step(st, W, G, lr, hp, root=root)
+        Us.append(U)
+    return st, W, Us
+
+
+@pytest.mark.parametrize("steps,key", [(1, "shampoo_quarter_root_step_singular_values"),
+                                       (4, "shampoo_quarter_root_after_4_accumulations"),
+                                       (100, "shampoo_quarter_root_after_100_accumulations")])
+def test_shampoo_step_hand_example(hand, steps, key):
+    """The whole Shampoo step on the page's gradient, fed `steps` times: the
+    last step's singular values are 1, 1 / 0.5, 0.5 / 0.1, 0.1.  An EMA in
+    place of the plain sum, a -1/2 exponent or momentum in the middle would
+    all miss the 4- and 100-step values."""
+    G = np.array(hand["G"], dtype=np.float64)
+    hp = O.Hyper(eps=1e-9, ridge=0.0, weight_decay=0.0)
+    st, W, Us = _shampoo_run([G] * steps, hp)
+    assert np.allclose(_sv(Us[-1])[:2], hand[key], atol=hand["printed_precision"])
+    # the descent step itself: W moves by -lr U from W = 0 at the first step
+    _st1, W1, U1 = _shampoo_run([G], hp, lr=0.25)
+    assert np.allclose(W1, -0.25 * U1[0], atol=1e-15)
+
+
+def test_shampoo_step_is_scale_invariant(hand):
+    """Problem 14 (first part): 10 G gives the same step as G."""
+    G = np.array(hand["G"], dtype=np.float64)
+    hp = O.Hyper(eps=1e-9, ridge=0.0, weight_decay=0.0)
+    _s, _w, U1 = _shampoo_run([G], hp)
+    _s, _w, U10 = _shampoo_run([10.0 * G], hp)
+    assert np.allclose(_sv(U10[0])[:2], hand["problem14_quarter_root_10G"], atol=hand["printed_precision"])
+    assert O.rel_fro(U10[0], U1[0]) < 1e-6
+
+
+def test_shampoo_factor_sums_brute_force():
+    """L_t = eps I + sum_s G_s G_s^T and R_t = eps I + sum_s G_s^T G_s,
+    entry by entry with explicit loops, over three random gradients."""
+    rng = np.random.default_rng(21)
+    for m, n in [(2, 3), (4, 3)]:
+        Gs = [rng.standard_normal((m, n)) for _ in range(3)]
+        hp = O.Hyper(eps=0.5, ridge=0.0, weight_decay=0.0)
+        st, _W, _U = _shampoo_run(Gs, hp)
+        for i in range(m):
+            for j in range(m):
+                want = 0.5 * (i == j)
+                for G in Gs:
+                    for k in range(n):
+                        want += G[i, k] * G[j, k]
+                assert abs(st.Sa[i, j] - want) < 1e-12
+        for i in range(n):
+            for j in range(n):
+                want = 0.5 * (i == j)
+                for G in Gs:
+                    for k in range(m):
+                        want += G[k, i] * G[k, j]
+                assert abs(st.Sb[i, j] - want) < 1e-12
+
+
+def _spd(d, cond, seed):
+    rng = np.random.default_rng(seed)
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    w = np.exp(rng.uniform(0.0, math.log(cond), d))
+    w[0], w[-1] = 1.0, cond
+    return (Q * w) @ Q.T
+
+
+def test_replay_root_output_is_the_float64_square_root():
+    """The root output of the replay without rounding equals the plain
+    float64 coupled iteration's Y_K sqrt(c'), and squares back to S + rho c I
+    once converged (the scales 2^-2h and sqrt(c') are right)."""
+    sch = O.cans_schedule(10, 1e-3)
+    S = _spd(48, 100.0, 3)
+    for ridge in (0.0, 1e-3):
+        rep = O.ns_replay(S, sch, ridge, rounding=False)["root"]
+        ref = O.ns_matrix_float64(S, sch, ridge)[1]
+        assert O.rel_fro(rep, ref) < 1e-12
+        c = math.sqrt(float(np.sum(S * S)))
+        assert O.rel_fro(rep @ rep, S + ridge * c * np.eye(48)) < 1e-5
+
+
+@pytest.mark.parametrize("cond", [1e2, 1e4])
+@pytest.mark.parametrize("ridge", [0.0, 1e-3])
+def test_quarter_root_chain_reaches_the_eigendecomposition_root(cond, ridge):
+    """Two chained exact-arithmetic chains give (S + rho ||S||_F I)^-1/4, and
+    P^4 (S + rho c I) = I."""
+    sch = O.cans_schedule(10, 1e-3)
+    S = _spd(64, cond, 4)
+    P = O.quarter_root_chain(S, sch, ridge, "ns_exact")
+    assert O.rel_fro(P, O.quarter_root_exact(S, ridge)) < 1e-5
+    c = math.sqrt(float(np.sum(S * S)))
+    P2 = P @ P
+    assert O.rel_fro(P2 @ P2 @ (S + ridge * c * np.eye(64)), np.eye(64)) < 1e-4
+
+
+def test_quarter_root_replay_is_accurate_with_a_ridge():
+    """The binary16 replay of both chains stays within 5e-3 of the exact
+    quarter root of the ridged factor up to condition number 1e6."""
+    sch = O.cans_schedule(10, 1e-3)
+    for d, cond in [(64, 1e2), (128, 1e3), (96, 1e6)]:
+        S = _spd(d, cond, d)
+        P = O.quarter_root_chain(S, sch, 1e-3, "replay")
+        assert O.rel_fro(P, O.quarter_root_exact(S, 1e-3)) < 5e-3
+
+
+def test_shampoo_stale_roots():
+    """root_every = k: fresh quarter roots at t = 1, 1+k, ...; the sums and
+    the step still run every step."""
+    rng = np.random.default_rng(22)
+    Gs = [rng.standard_normal((6, 5)) for _ in range(5)]
+    hp = O.Hyper(eps=1e-3, ridge=0.0, weight_decay=0.0, root_every=2)
+    st = O.shampoo_init(6, 5, hp)
+    W = np.zeros((6, 5))
+    prev = None
+    for t, G in enumerate(Gs, start=1):
+        st, W, U = O.shampoo_step(st, W, G, 1.0, hp)
+        if (t - 1) % 2 == 0:
+            assert O.rel_fro(st.Pa, O.quarter_root_exact(st.Sa)) < 1e-12
+        else:
+            assert np.array_equal(st.Pa, prev.Pa) and np.array_equal(st.Pb, prev.Pb)
+            assert O.rel_fro(U, prev.Pa @ G @ prev.Pb) < 1e-14
+        prev = st
