@@ -14,6 +14,15 @@
  *   W   <- W - lr wd (lr/lr_peak) W - lr c_shape U,
  *          c_shape = sqrt(m/n) / (sqrt(m) + sqrt(n)).
  *
+ * With okls_config.method = OKLS_METHOD_SHAMPOO the same kernels run the
+ * classic Shampoo step the OKLS page refines (optim-book, "Shampoo" chapter,
+ * sections "2 x 3 gradient by hand" and Problem 14):
+ *
+ *   L <- L + G G^T,  R <- R + G^T G        (plain sums; L_0 = R_0 = eps I)
+ *   P_L <- L^(-1/4), P_R <- R^(-1/4)        (two chained Newton-Schulz runs:
+ *          the square root of the ridged factor, then its inverse square root)
+ *   W   <- W - lr wd (lr/lr_peak) W - lr P_L G P_R.
+ *
  * Conventions used by every entry point
  *   - Matrices are row-major and contiguous; a batch is `batch` matrices
  *     back to back (the 3-D (N, m, n) parameter of the README's "Batched
@@ -37,7 +46,7 @@
 extern "C" {
 #endif
 
-#define OKLS_ABI_VERSION 1
+#define OKLS_ABI_VERSION 2
 
 typedef enum okls_status {
   OKLS_OK = 0,
@@ -52,7 +61,15 @@ typedef enum okls_status {
 /* Element types of W and G. */
 typedef enum okls_dtype { OKLS_F32 = 0, OKLS_BF16 = 1 } okls_dtype;
 
-/* Which piece of state okls_get_state / okls_set_state move. */
+/* Preconditioner step computed by okls_step. */
+typedef enum okls_method {
+  OKLS_METHOD_OKLS = 0,    /* Online KL Shampoo (the default)              */
+  OKLS_METHOD_SHAMPOO = 1  /* classic Shampoo: summed factors, -1/4 roots */
+} okls_method;
+
+/* Which piece of state okls_get_state / okls_set_state move.  In Shampoo
+ * mode S_a / S_b hold the sums L / R and P_a / P_b their -1/4 roots; M is
+ * unused (left at zero). */
 typedef enum okls_state_part {
   OKLS_STATE_M = 0,   /* momentum,                 batch x m x n, fp32 */
   OKLS_STATE_SA = 1,  /* left factor S_a,          batch x m x m, fp32 */
@@ -98,6 +115,14 @@ typedef enum okls_state_part {
  *                   of the last refresh (the practice of recomputing Shampoo
  *                   roots every 20-100 steps; k = 1 is the README's
  *                   zero-staleness method).
+ *   method          okls_method.  OKLS_METHOD_SHAMPOO ignores beta1, beta2,
+ *                   variance_correction and eps_every_update (the sums add
+ *                   G G^T and G^T G with weight 1, eps enters only at reset,
+ *                   no momentum, no shape multiplier) and applies `ridge` to
+ *                   L and R before the first chain; the second chain takes
+ *                   no ridge (its input's condition number is at most
+ *                   sqrt((1 + ridge) / ridge)).  The workspace grows by one
+ *                   fp32 d x d square root per factor.
  */
 typedef struct okls_config {
   int64_t batch;
@@ -117,7 +142,8 @@ typedef struct okls_config {
   int32_t variance_correction;
   int32_t eps_every_update;
   int32_t root_every;
-  int32_t reserved[7]; /* must be zero */
+  int32_t method;      /* an okls_method value; 0 = OKLS */
+  int32_t reserved[6]; /* must be zero */
 } okls_config;
 
 typedef struct okls_handle_s *okls_handle;
@@ -157,7 +183,8 @@ okls_status okls_create(const okls_config *cfg, void *state_dev,
 okls_status okls_reset_state(okls_handle h, void *stream);
 
 /*
- * One OKLS step over the whole batch, asynchronous on `stream`.
+ * One OKLS (or, by cfg.method, classic Shampoo) step over the whole batch,
+ * asynchronous on `stream`.
  *   W_dev  batch x m x n, param_dtype, updated in place.
  *   G_dev  batch x m x n, grad_dtype, read only.
  *   lr     current learning rate (finite, >= 0); lr_peak is fixed in cfg.

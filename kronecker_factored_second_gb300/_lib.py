@@ -26,6 +26,9 @@ OKLS_ERR_NO_DEVICE = 6
 OKLS_F32 = 0
 OKLS_BF16 = 1
 
+METHOD_OKLS = 0
+METHOD_SHAMPOO = 1
+
 STATE_M, STATE_SA, STATE_SB, STATE_PA, STATE_PB = range(5)
 
 DEV_NONFINITE_INPUT = 0x1
@@ -53,7 +56,8 @@ class okls_config(ctypes.Structure):
         ("variance_correction", ctypes.c_int32),
         ("eps_every_update", ctypes.c_int32),
         ("root_every", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("method", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
     ]
 
 

@@ -506,22 +506,26 @@ okls_status trace_copy(const TraceOut& tr, int slice, const Buf* b, cudaStream_t
 
 // Normalisation and the coupled Newton-Schulz chain for 1 or 2 factors.
 // The stable order is kept: M_k = Z_k Y_k, Y_{k+1} = Y_k T_k, Z_{k+1} = T_k Z_k.
+// root_only: the last iteration forms only the square root (every factor
+// must have root32), not P, its binary16 copy or their scales.
 okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
                         int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
-                        const TraceOut* tr);
+                        const TraceOut* tr, bool root_only);
 
 okls_status run_ns(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
                    int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
-                   const TraceOut* tr) {
+                   const TraceOut* tr, bool root_only = false) {
+  for (int q = 0; q < nf && root_only; ++q)
+    if (!fs[q]->root32) return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: square-root output");
   g_in_ns = true;
-  okls_status s = run_ns_body(fs, nf, sc, split, ridge, scal, scal_ld, maps, status, sms, st, tr);
+  okls_status s = run_ns_body(fs, nf, sc, split, ridge, scal, scal_ld, maps, status, sms, st, tr, root_only);
   g_in_ns = false;
   return s;
 }
 
 okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
                         int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
-                        const TraceOut* tr) {
+                        const TraceOut* tr, bool root_only) {
   const int K = sc.iters;
   const int h = kHeadroom;
   for (int q = 0; q < nf; ++q) {
@@ -616,17 +620,19 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
         set_out16(pz, f.Z[nxt][0], nullptr, spo ? &f.Z[nxt][1] : nullptr, nullptr);
         pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
       } else {
-        GemmProblem& pz = lb.add(f.T, f.Z[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_LAST, false, true);
-        // in split mode the copy of P read by the X and whitening products
-        // is a (hi, lo) pair as well
-        set_out16(pz, f.Ph[0], nullptr, f.split ? &f.Ph[1] : nullptr, nullptr);
-        pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
-        pz.out32 = f.P32;
-        pz.ld32 = f.d;
-        pz.mat32 = static_cast<int64_t>(f.d) * f.d;
-        pz.scal = scal;
-        pz.scal_ld = scal_ld;
-        pz.scal_slot = f.slot_pscale;
+        if (!root_only) {
+          GemmProblem& pz = lb.add(f.T, f.Z[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_LAST, false, true);
+          // in split mode the copy of P read by the X and whitening products
+          // is a (hi, lo) pair as well
+          set_out16(pz, f.Ph[0], nullptr, f.split ? &f.Ph[1] : nullptr, nullptr);
+          pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
+          pz.out32 = f.P32;
+          pz.ld32 = f.d;
+          pz.mat32 = static_cast<int64_t>(f.d) * f.d;
+          pz.scal = scal;
+          pz.scal_ld = scal_ld;
+          pz.scal_slot = f.slot_pscale;
+        }
         if (f.root32) {
           GemmProblem& pr = lb.add(f.Y[cur], f.T, sp, f.d, f.d, f.d, f.batch, EPI_ROOT, false, true);
           pr.out32 = f.root32;
@@ -641,7 +647,7 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
     okls_status s = lb.go(maps, status, sms, st);
     if (s != OKLS_OK) return s;
   }
-  if (tr && tr->base) return trace_copy(*tr, 3 * K, &fs[0]->Ph[0], st);
+  if (tr && tr->base && !root_only) return trace_copy(*tr, 3 * K, &fs[0]->Ph[0], st);
   return OKLS_OK;
 }
 
@@ -655,6 +661,7 @@ struct okls_handle_s {
   float *M = nullptr, *Sa = nullptr, *Sb = nullptr, *Pa = nullptr, *Pb = nullptr;
   Factor fa, fb;
   Buf Gh, GhT, Nh, Xb, XaT;  // Ghat (m x n), Ghat^T (n x m), Nhat (m x n), X_b / Q (m x n), X_a^T (n x m)
+  float *sq_a = nullptr, *sq_b = nullptr;  // Shampoo: fp32 square roots L^1/2, R^1/2 between the chains
   float* scal = nullptr;
   uint32_t* status = nullptr;
   CUtensorMap* maps = nullptr;
@@ -690,8 +697,15 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
   float* part_g = static_cast<float*>(wp.take(static_cast<size_t>(2 * B * pg_ld * 4)));
   float* part_a = static_cast<float*>(wp.take(static_cast<size_t>(B * pa_ld * 4)));
   float* part_b = static_cast<float*>(wp.take(static_cast<size_t>(B * pb_ld * 4)));
-  Buf Gh = wp.buf16(m, n, B), GhT = wp.buf16(n, m, B), Nh = wp.buf16(m, n, B);
-  Buf Xb = wp.buf16(m, n, B), XaT = wp.buf16(n, m, B);
+  const bool shampoo = c.method == OKLS_METHOD_SHAMPOO;
+  // Shampoo has no momentum (N = G) and no preconditioned factor inputs, so
+  // Nhat and X_a^T are not needed; it keeps each factor's square root instead
+  Buf Gh = wp.buf16(m, n, B), GhT = wp.buf16(n, m, B);
+  Buf Nh = shampoo ? Buf() : wp.buf16(m, n, B);
+  Buf Xb = wp.buf16(m, n, B);
+  Buf XaT = shampoo ? Buf() : wp.buf16(n, m, B);
+  float* sq_a = shampoo ? static_cast<float*>(wp.take(static_cast<size_t>(B * m * m * 4))) : nullptr;
+  float* sq_b = shampoo ? static_cast<float*>(wp.take(static_cast<size_t>(B * n * n * 4))) : nullptr;
   Factor fa, fb;
   const bool split = c.ns_split_iters > 0;
   plan_factor(wp, fa, static_cast<int>(m), static_cast<int>(B), split);
@@ -728,6 +742,8 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
     h->Nh = Nh;
     h->Xb = Xb;
     h->XaT = XaT;
+    h->sq_a = sq_a;
+    h->sq_b = sq_b;
     h->scal = scal;
     h->status = status;
     h->maps = maps;
@@ -772,7 +788,9 @@ okls_status validate(const okls_config* c) {
   if (!(c->ns_lo > 0.0f && c->ns_lo < 1.0f)) return fail(OKLS_ERR_INVALID_ARG, "ns_lo must be in (0, 1)");
   if (!finite_nonneg(c->ridge)) return fail(OKLS_ERR_INVALID_ARG, "ridge must be finite and >= 0");
   if (c->root_every < 0) return fail(OKLS_ERR_INVALID_ARG, "root_every must be >= 0 (0 means 1)");
-  for (int i = 0; i < 7; ++i)
+  if (c->method != OKLS_METHOD_OKLS && c->method != OKLS_METHOD_SHAMPOO)
+    return fail(OKLS_ERR_INVALID_ARG, "method %d", c->method);
+  for (int i = 0; i < 6; ++i)
     if (c->reserved[i] != 0) return fail(OKLS_ERR_INVALID_ARG, "reserved fields must be zero");
   return OKLS_OK;
 }
@@ -877,29 +895,42 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
   if (!finite_nonneg(lr)) return fail(OKLS_ERR_INVALID_ARG, "lr must be finite and >= 0");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const okls_config& c = h->cfg;
+  const bool shampoo = c.method == OKLS_METHOD_SHAMPOO;
   const int B = static_cast<int>(c.batch), m = static_cast<int>(c.m), n = static_cast<int>(c.n);
   const int sld = B;
   const int64_t t1 = h->t + 1;
-  const float kappa = c.variance_correction ? static_cast<float>(variance_kappa(c.beta1, t1)) : 1.0f;
+  // Shampoo: no momentum, N = G
+  const float b1 = shampoo ? 0.0f : c.beta1;
+  const float kappa = (!shampoo && c.variance_correction) ? static_cast<float>(variance_kappa(c.beta1, t1)) : 1.0f;
+  float* M = shampoo ? nullptr : h->M;
   const int gbf = c.grad_dtype == OKLS_BF16;
   const int h12 = kHeadroom;
+  const int K = h->sched.iters;
+  const int zK = h->sched.z[K], zK1 = h->sched.z[K - 1];
   okls_status s;
   ProfScope scope(&h->prof);
   BoxScope boxes(&h->boxes);
-  note_kernels(4);  // momentum statistics, coefficients (2), pack
 
   // 1-2. momentum, statistics, packed binary16 operands
   OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(4 * B * 4), st));  // SC_SUMSQ_* slots
-  OKLS_CK(launch_momentum_stats(G, gbf, h->M, B, static_cast<int64_t>(m) * n, c.beta1, kappa, h->part_g,
-                                h->part_g_ld, h->status, st));
-  OKLS_CK(launch_coeffs_pre(B, m, n, c.beta2, h->scal, sld, h->part_g, h->part_g_ld, st));
-  // row pitches: Ghat is m x n (pitch ldn), Ghat^T and Nhat^T are n x m (pitch ldm)
-  if (h->Gh.ld < n || h->GhT.ld < m || h->Nh.ld != h->Gh.ld || h->Gh.rows != m || h->GhT.rows != n)
+  OKLS_CK(launch_momentum_stats(G, gbf, M, B, static_cast<int64_t>(m) * n, b1, kappa, h->part_g, h->part_g_ld,
+                                h->status, st));
+  OKLS_CK(launch_coeffs_pre(B, m, n, c.beta2, shampoo ? 1 : 0, h->scal, sld, h->part_g, h->part_g_ld, st));
+  // row pitches: Ghat and Nhat are m x n (pitch ldn), Ghat^T is n x m (pitch ldm)
+  if (h->Gh.ld < n || h->GhT.ld < m || h->Gh.rows != m || h->GhT.rows != n ||
+      (!shampoo && h->Nh.ld != h->Gh.ld))
     return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: packed operand pitches");
-  OKLS_CK(launch_pack(G, gbf, h->M, h->Gh.p, h->GhT.p, h->Nh.p, B, m, n, /*ldm=*/h->GhT.ld,
-                      /*ldn=*/h->Gh.ld, c.beta1, kappa, h->scal, sld, h->status, st));
-  // 3. X_b = G P_b and X_a^T = G^T P_a^T (previous roots)
-  {
+  OKLS_CK(launch_pack(G, gbf, M, h->Gh.p, h->GhT.p, shampoo ? nullptr : h->Nh.p, B, m, n, /*ldm=*/h->GhT.ld,
+                      /*ldn=*/h->Gh.ld, b1, kappa, h->scal, sld, h->status, st));
+  note_kernels(3);
+  // 3. OKLS: X_b = G P_b and X_a^T = G^T P_a^T (previous roots); Shampoo
+  //    feeds G itself to the factor products
+  const Buf* Xa = &h->XaT;
+  const Buf* Xl = &h->Xb;
+  if (shampoo) {
+    Xl = &h->Gh;
+    Xa = &h->GhT;
+  } else {
     LaunchBuilder lb;
     GemmProblem& p0 = lb.add_bsplit(h->Gh, h->fb.Ph, h->fb.split, m, n, n, B, EPI_X16, true);
     set_out16(p0, h->Xb, nullptr, nullptr, nullptr);
@@ -911,11 +942,13 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
     p1.check_finite = 1;
     if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
   }
-  // 4. factor EMAs on upper tiles, mirrored, with ||S||_F^2
+  // 4. factor updates on upper tiles (OKLS: EMA, + eps I; Shampoo: plain
+  //    sum), the lower triangle mirrored later, with ||S||_F^2 partials
   {
-    const float eps_u = c.eps_every_update ? c.eps : 0.0f;
+    const float beta = shampoo ? 1.0f : c.beta2;
+    const float eps_u = (!shampoo && c.eps_every_update) ? c.eps : 0.0f;
     LaunchBuilder lb;
-    GemmProblem& pa = lb.add(&h->Xb, &h->Xb, false, m, m, n, B, EPI_SYRK, true);
+    GemmProblem& pa = lb.add(Xl, Xl, false, m, m, n, B, EPI_SYRK, true);
     pa.out32 = h->Sa;
     pa.ld32 = m;
     pa.mat32 = static_cast<int64_t>(m) * m;
@@ -924,9 +957,9 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
     pa.scal_slot = SC_ALPHA_SA;
     pa.part = h->part_a;
     pa.part_ld = h->part_a_ld;
-    pa.beta = c.beta2;
+    pa.beta = beta;
     pa.gamma = eps_u;
-    GemmProblem& pb = lb.add(&h->XaT, &h->XaT, false, n, n, m, B, EPI_SYRK, true);
+    GemmProblem& pb = lb.add(Xa, Xa, false, n, n, m, B, EPI_SYRK, true);
     pb.out32 = h->Sb;
     pb.ld32 = n;
     pb.mat32 = static_cast<int64_t>(n) * n;
@@ -935,26 +968,59 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
     pb.scal_slot = SC_ALPHA_SB;
     pb.part = h->part_b;
     pb.part_ld = h->part_b_ld;
-    pb.beta = c.beta2;
+    pb.beta = beta;
     pb.gamma = eps_u;
     if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
   }
-  // 5-6. fresh inverse roots of both factors (every root_every-th step; the
-  // steps in between keep P, its binary16 copy and its scales)
-  const int K = h->sched.iters;
+  // 5-6. fresh roots of both factors (every root_every-th step; the steps in
+  // between keep P, its binary16 copy and its scales).  The scales pi of the
+  // new roots are committed only after the chain has run.
   const int64_t every = c.root_every > 1 ? c.root_every : 1;
   const bool fresh = ((t1 - 1) % every) == 0;
   // the factor products ran as one launch: pair tiles iff either factor is taller than 128
   const bool syrk_pair = use_pair(std::max(m, n));
-  OKLS_CK(launch_coeffs_post(B, c.ridge, h->sched.z[K], h->sched.z[K - 1], h->scal, sld, 1, fresh ? 1 : 0,
-                             h->status, h->part_a, h->part_a_ld, syrk_parts(m, syrk_pair), h->part_b,
-                             h->part_b_ld, syrk_parts(n, syrk_pair), st));
   if (fresh) {
-    Factor* fs[2] = {&h->fa, &h->fb};
-    if ((s = run_ns(fs, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
-                    nullptr)) != OKLS_OK)
-      return s;
+    OKLS_CK(launch_coeffs_post(B, c.ridge, zK, zK1, h->scal, sld, kPostRoots, h->status, h->part_a, h->part_a_ld,
+                               syrk_parts(m, syrk_pair), h->part_b, h->part_b_ld, syrk_parts(n, syrk_pair), st));
+    note_kernels(1);
+    if (shampoo) {
+      // L^-1/4 = (L^1/2)^-1/2: the first chain (ridge on L) forms only the
+      // square roots, the second (no ridge) their inverse square roots
+      Factor ra = h->fa, rb = h->fb;
+      ra.root32 = h->sq_a;
+      rb.root32 = h->sq_b;
+      Factor* f1[2] = {&ra, &rb};
+      if ((s = run_ns(f1, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
+                      nullptr, /*root_only=*/true)) != OKLS_OK)
+        return s;
+      OKLS_CK(launch_sumsq(h->sq_a, B, static_cast<int64_t>(m) * m, h->part_a, h->part_a_ld, st));
+      OKLS_CK(launch_sumsq(h->sq_b, B, static_cast<int64_t>(n) * n, h->part_b, h->part_b_ld, st));
+      OKLS_CK(launch_coeffs_post(B, 0.0f, zK, zK1, h->scal, sld, kPostRoots, h->status, h->part_a, h->part_a_ld,
+                                 sumsq_parts(static_cast<int64_t>(m) * m), h->part_b, h->part_b_ld,
+                                 sumsq_parts(static_cast<int64_t>(n) * n), st));
+      note_kernels(3);
+      Factor qa = h->fa, qb = h->fb;
+      qa.S = h->sq_a;
+      qa.S_upper_only = false;
+      qb.S = h->sq_b;
+      qb.S_upper_only = false;
+      Factor* f2[2] = {&qa, &qb};
+      if ((s = run_ns(f2, 2, h->sched, c.ns_split_iters, 0.0f, h->scal, sld, h->maps, h->status, h->sms, st,
+                      nullptr)) != OKLS_OK)
+        return s;
+    } else {
+      Factor* fs[2] = {&h->fa, &h->fb};
+      if ((s = run_ns(fs, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
+                      nullptr)) != OKLS_OK)
+        return s;
+    }
+    OKLS_CK(launch_coeffs_post(B, c.ridge, zK, zK1, h->scal, sld, kPostCommit | kPostUpdate, h->status, nullptr, 0,
+                               0, nullptr, 0, 0, st));
+    note_kernels(1);
   } else {
+    OKLS_CK(launch_coeffs_post(B, c.ridge, zK, zK1, h->scal, sld, kPostUpdate, h->status, nullptr, 0, 0, nullptr, 0,
+                               0, st));
+    note_kernels(1);
     // keep the state symmetric: write the lower triangles of the new factors
     for (Factor* f : {&h->fa, &h->fb}) {
       NormaliseArgs A;
@@ -970,16 +1036,16 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
       note_kernels(1);
     }
   }
-  // 7. Q = P_a N  (into the X_b buffer)
+  // 7. Q = P_a N (N = G for Shampoo) into the X_b buffer
   {
     LaunchBuilder lb;
-    GemmProblem& p = lb.add_asplit(h->fa.Ph, h->Nh, h->fa.split, m, n, m, B, EPI_X16, true);
+    GemmProblem& p = lb.add_asplit(h->fa.Ph, shampoo ? h->Gh : h->Nh, h->fa.split, m, n, m, B, EPI_X16, true);
     set_out16(p, h->Xb, nullptr, nullptr, nullptr);
     p.alpha = std::ldexp(1.0f, -h12);
     p.check_finite = 1;
     if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
   }
-  // 8. U = Q P_b, W <- W (1 - lr wd lr/lr_peak) - lr c_shape U
+  // 8. U = Q P_b, W <- W (1 - lr wd lr/lr_peak) - lr c_shape U (c_shape = 1 for Shampoo)
   {
     LaunchBuilder lb;
     GemmProblem& p = lb.add_bsplit(h->Xb, h->fb.Ph, h->fb.split, m, n, n, B, EPI_UPDATE, true);
@@ -990,7 +1056,9 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
     p.scal = h->scal;
     p.scal_ld = sld;
     p.scal_slot = SC_UCOEF;
-    const double cshape = std::sqrt(static_cast<double>(m) / n) / (std::sqrt(static_cast<double>(m)) + std::sqrt(static_cast<double>(n)));
+    const double cshape =
+        shampoo ? 1.0
+                : std::sqrt(static_cast<double>(m) / n) / (std::sqrt(static_cast<double>(m)) + std::sqrt(static_cast<double>(n)));
     p.alpha = static_cast<float>(1.0 - static_cast<double>(lr) * c.weight_decay * (static_cast<double>(lr) / c.lr_peak));
     p.beta = static_cast<float>(static_cast<double>(lr) * cshape);
     if ((s = lb.go(h->maps, h->status, h->sms, st)) != OKLS_OK) return s;
@@ -1184,7 +1252,7 @@ okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace
   const Sched sc = make_schedule(iters, lo);
   OKLS_CK(launch_sumsq(S, static_cast<int>(count), d * d, part, factor_parts(d), st));
   OKLS_CK(launch_coeffs_post(static_cast<int>(count), ridge, sc.z[iters], sc.z[iters - 1], scal,
-                             static_cast<int>(count), 0, 1, status, part, factor_parts(d), sumsq_parts(d * d),
+                             static_cast<int>(count), kPostRoots, status, part, factor_parts(d), sumsq_parts(d * d),
                              nullptr, 0, 0, st));
   TraceOut tr;
   tr.base = trace;

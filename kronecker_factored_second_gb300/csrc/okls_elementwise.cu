@@ -5,11 +5,13 @@
 //                     (page "Online KL Shampoo": Nesterov momentum with
 //                     variance correction); flags non-finite inputs.
 //   k_coeffs_pre      per-matrix power-of-two scales of G and N and the EMA
-//                     weights of both factors.
+//                     weights of both factors (the plain-sum weights of the
+//                     classic Shampoo factors in that mode).
 //   k_pack            writes M_t, Ghat, Nhat and Ghat^T (binary16, scaled);
 //                     the transpose goes through 32x32 shared-memory tiles.
-//   k_coeffs_post     normaliser c' of each factor, the root scales pi and
-//                     the whitening coefficient.
+//   k_coeffs_post     normaliser c' of each factor and the chain's output
+//                     scales; after the chain the root scales pi; the
+//                     whitening coefficient.
 //   k_normalise       Y_0 = (S + rho c I)/c', T_0 = a_0 I + b_0 Y_0, Z_1 = T_0
 //                     (the first Newton-Schulz step needs no product).
 //   k_sumsq, k_amax, k_requant, k_reset_state: inverse-root entry and state
@@ -53,13 +55,13 @@ __global__ void k_momentum_stats(const GT* __restrict__ G, const float* __restri
   __shared__ float red[32];
   const int b = blockIdx.y;
   const GT* g = G + static_cast<int64_t>(b) * mn;
-  const float* mo = M + static_cast<int64_t>(b) * mn;
+  const float* mo = M ? M + static_cast<int64_t>(b) * mn : nullptr;  // null: no momentum
   float sg = 0.0f, sn = 0.0f;
   bool bad = false;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < mn;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float gv = to_f(g[e]);
-    const float mv = mo[e];
+    const float mv = mo ? mo[e] : 0.0f;
     const float mn1 = fmaf(b1, mv, (1.0f - b1) * gv);
     const float nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
     bad |= !isfinite(gv) || !isfinite(mv);
@@ -92,7 +94,7 @@ __device__ __forceinline__ float pow2_rms_scale(float sumsq, double count) {
   return ldexpf(1.0f, e);
 }
 
-__global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal,
+__global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, int shampoo, float* scal,
                              int scal_ld, const float* part, int64_t part_ld, int nparts) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
@@ -104,6 +106,13 @@ __global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float
   const float ns = pow2_rms_scale(S(SC_SUMSQ_N), cnt);
   S(SC_GSCALE) = gs;
   S(SC_NSCALE) = ns;
+  if (shampoo) {
+    // L += G G^T = Ghat Ghat^T / gs^2 (and R likewise): weight 1, no roots
+    const double w = 1.0 / (static_cast<double>(gs) * gs);
+    S(SC_ALPHA_SA) = static_cast<float>(w);
+    S(SC_ALPHA_SB) = static_cast<float>(w);
+    return;
+  }
   // X_b = G P_b = Xhat_b 2^h pi_b / gs  ->  S_a += (1-b2)/n (2^h pi_b / gs)^2 Xhat Xhat^T
   const double h = ldexp(1.0, kHeadroom);
   const double xa = h * S(SC_PI_B) / gs;
@@ -126,9 +135,9 @@ __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* 
   const float ns = scal[static_cast<int64_t>(SC_NSCALE) * scal_ld + b];
   const int64_t mn = static_cast<int64_t>(m) * n;
   const GT* g = G + b * mn;
-  float* mo = M + b * mn;
+  float* mo = M ? M + b * mn : nullptr;  // null: no momentum (Shampoo)
   __half* gh = Gh + b * static_cast<int64_t>(m) * ldn;
-  __half* nh = Nh + b * static_cast<int64_t>(m) * ldn;
+  __half* nh = Nh ? Nh + b * static_cast<int64_t>(m) * ldn : nullptr;  // null: N = G
   const int tx = threadIdx.x;
   for (int r = threadIdx.y; r < 32; r += 8) {
     const int i = r0 + r, j = c0 + tx;
@@ -136,11 +145,13 @@ __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* 
     if (i < m && j < n) {
       const int64_t e = static_cast<int64_t>(i) * n + j;
       gv = to_f(g[e]);
-      const float mn1 = fmaf(b1, mo[e], (1.0f - b1) * gv);
-      nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
-      mo[e] = mn1;
       gh[static_cast<int64_t>(i) * ldn + j] = __float2half_rn(gv * gs);
-      nh[static_cast<int64_t>(i) * ldn + j] = __float2half_rn(nv * ns);
+      if (mo) {
+        const float mn1 = fmaf(b1, mo[e], (1.0f - b1) * gv);
+        nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
+        mo[e] = mn1;
+      }
+      if (nh) nh[static_cast<int64_t>(i) * ldn + j] = __float2half_rn(nv * ns);
     }
     sg[r][tx] = gv * gs;
   }
@@ -153,10 +164,13 @@ __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* 
 }
 
 // -------------------------------------------------------------- post scalars
-__global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                              int with_update, int with_roots, const uint32_t* status, const float* part_a,
-                              int64_t part_a_ld, int64_t npart_a, const float* part_b, int64_t part_b_ld,
-                              int64_t npart_b) {
+// mode bits: kPostRoots   c' and the chain's output scales from ||S||_F (before a chain)
+//            kPostCommit  pi of the new roots (after the chain, so a chain that
+//                         failed leaves P^ and pi of the previous roots together)
+//            kPostUpdate  the whitening coefficient from pi_a, pi_b and N's scale
+__global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld, int mode,
+                              const uint32_t* status, const float* part_a, int64_t part_a_ld, int64_t npart_a,
+                              const float* part_b, int64_t part_b_ld, int64_t npart_b) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   // a failed stage leaves the previous roots (and their scales) in force
@@ -167,18 +181,21 @@ __global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* sc
   if (part_b) S(SC_SUMSQ_SB) = static_cast<float>(sum_parts(part_b + b * part_b_ld, npart_b));
   const double margin = 1.0 + ldexp(1.0, -8);
   const int h = kHeadroom;
-  for (int f = 0; f < 2 && with_roots; ++f) {
+  for (int f = 0; f < 2 && (mode & kPostRoots); ++f) {
     const int s_sum = f == 0 ? SC_SUMSQ_SA : SC_SUMSQ_SB;
     double c = sqrt(static_cast<double>(S(s_sum)));
     double cp = c * (1.0 + ridge) * margin;
     if (!(cp > 1e-30)) cp = 1e-30;
     const double rc = 1.0 / sqrt(cp);
     S(f == 0 ? SC_CPRIME_A : SC_CPRIME_B) = static_cast<float>(cp);
-    S(f == 0 ? SC_PI_A : SC_PI_B) = static_cast<float>(ldexp(rc, zK - h));
     S(f == 0 ? SC_PSCALE_A : SC_PSCALE_B) = static_cast<float>(ldexp(rc, zK1 - 2 * h));
     S(f == 0 ? SC_RSCALE_A : SC_RSCALE_B) = static_cast<float>(ldexp(sqrt(cp), -2 * h));
   }
-  if (with_update) {
+  for (int f = 0; f < 2 && (mode & kPostCommit); ++f) {
+    const double cp = static_cast<double>(S(f == 0 ? SC_CPRIME_A : SC_CPRIME_B));
+    S(f == 0 ? SC_PI_A : SC_PI_B) = static_cast<float>(ldexp(1.0 / sqrt(cp), zK - h));
+  }
+  if (mode & kPostUpdate) {
     const double pa = S(SC_PI_A), pb = S(SC_PI_B), ns = S(SC_NSCALE);
     S(SC_UCOEF) = static_cast<float>(ldexp(pa * pb / ns, h));
   }
@@ -391,9 +408,9 @@ cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal, int scal_ld,
-                              const float* part, int64_t part_ld, cudaStream_t st) {
-  k_coeffs_pre<<<(batch + 127) / 128, 128, 0, st>>>(batch, m, n, beta2, scal, scal_ld, part, part_ld,
+cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, int shampoo, float* scal,
+                              int scal_ld, const float* part, int64_t part_ld, cudaStream_t st) {
+  k_coeffs_pre<<<(batch + 127) / 128, 128, 0, st>>>(batch, m, n, beta2, shampoo, scal, scal_ld, part, part_ld,
                                                     momentum_parts(m * n));
   return cudaGetLastError();
 }
@@ -411,14 +428,11 @@ cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half*
   return cudaGetLastError();
 }
 
-cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                               int with_update, int with_roots, const uint32_t* status, const float* part_a,
-                               int64_t part_a_ld,
-                               int64_t npart_a, const float* part_b, int64_t part_b_ld, int64_t npart_b,
-                               cudaStream_t st) {
-  k_coeffs_post<<<(batch + 127) / 128, 128, 0, st>>>(batch, ridge, zK, zK1, scal, scal_ld, with_update,
-                                                     with_roots, status, part_a, part_a_ld, npart_a, part_b, part_b_ld,
-                                                     npart_b);
+cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld, int mode,
+                               const uint32_t* status, const float* part_a, int64_t part_a_ld, int64_t npart_a,
+                               const float* part_b, int64_t part_b_ld, int64_t npart_b, cudaStream_t st) {
+  k_coeffs_post<<<(batch + 127) / 128, 128, 0, st>>>(batch, ridge, zK, zK1, scal, scal_ld, mode, status, part_a,
+                                                     part_a_ld, npart_a, part_b, part_b_ld, npart_b);
   return cudaGetLastError();
 }
 

@@ -41,16 +41,18 @@ int sumsq_parts(int64_t dd);
 cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int batch, int64_t mn,
                                   float b1, float kappa, float* part, int64_t part_ld, uint32_t* status,
                                   cudaStream_t st);
-cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, float* scal, int scal_ld,
-                              const float* part, int64_t part_ld, cudaStream_t st);
+// M may be null (no momentum: N = G); Nh may be null (N^ not needed).
+cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, int shampoo, float* scal,
+                              int scal_ld, const float* part, int64_t part_ld, cudaStream_t st);
 cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* Nh,
                         int batch, int m, int n, int64_t ldm, int64_t ldn, float b1, float kappa,
                         const float* scal, int scal_ld, const uint32_t* status, cudaStream_t st);
-cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld,
-                               int with_update, int with_roots, const uint32_t* status, const float* part_a,
-                               int64_t part_a_ld,
-                               int64_t npart_a, const float* part_b, int64_t part_b_ld, int64_t npart_b,
-                               cudaStream_t st);
+constexpr int kPostRoots = 1;   // c', P and root output scales of the coming chain
+constexpr int kPostCommit = 2;  // root scales pi of the chain that just ran
+constexpr int kPostUpdate = 4;  // whitening coefficient
+cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld, int mode,
+                               const uint32_t* status, const float* part_a, int64_t part_a_ld, int64_t npart_a,
+                               const float* part_b, int64_t part_b_ld, int64_t npart_b, cudaStream_t st);
 cudaError_t launch_normalise(const NormaliseArgs& A, int batch, cudaStream_t st);
 cudaError_t launch_sumsq(const float* S, int batch, int64_t dd, float* part, int64_t part_ld, cudaStream_t st);
 cudaError_t launch_requant(const float* P, int batch, int d, __half* Ph, __half* PhT, __half* Pl, __half* PlT,

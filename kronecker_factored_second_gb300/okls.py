@@ -7,6 +7,8 @@
 `OnlineKLShampoo`  a torch.optim.Optimizer with the README's constructor
                    (lr, beta1, beta2, eps, weight_decay), one OklsBatch per
                    2-D or 3-D parameter.
+`Shampoo`          the classic Shampoo step (summed factors, -1/4 roots)
+                   over the same kernels (method="shampoo").
 
 All arithmetic happens in libokls.so; nothing here computes on the CPU.
 """
@@ -45,8 +47,12 @@ class OklsBatch:
                  beta2: float = 0.9482, eps: float = 1e-9, weight_decay: float = 0.0303,
                  ns_iters: int = 10, ns_split_iters: int = 0, ns_lo: float = 1e-3,
                  ridge: float = 1e-3, variance_correction: bool = True,
-                 eps_every_update: bool = True, root_every: int = 1, device=None):
+                 eps_every_update: bool = True, root_every: int = 1, method: str = "okls",
+                 device=None):
         lib = L.lib()
+        methods = {"okls": L.METHOD_OKLS, "shampoo": L.METHOD_SHAMPOO}
+        if method not in methods:
+            raise ValueError(f"okls: method must be one of {sorted(methods)}")
         cfg = L.config_default(batch, m, n)
         cfg.param_dtype = _DT[param_dtype]
         cfg.grad_dtype = _DT[grad_dtype or param_dtype]
@@ -56,6 +62,8 @@ class OklsBatch:
         cfg.variance_correction = int(variance_correction)
         cfg.eps_every_update = int(eps_every_update)
         cfg.root_every = int(root_every)
+        cfg.method = methods[method]
+        self.method = method
         self.cfg = cfg
         self.batch, self.m, self.n = batch, m, n
         self.param_dtype = param_dtype
@@ -230,5 +238,39 @@ class OnlineKLShampoo(torch.optim.Optimizer):
                                            eps=g["eps"], weight_decay=g["weight_decay"],
                                            ns_split_iters=g["ns_split_iters"], ridge=g["ridge"],
                                            device=p.device)
+                st["okls"].step(p.data, p.grad.contiguous(), g["lr"])
+        return loss
+
+
+class Shampoo(torch.optim.Optimizer):
+    """Classic Shampoo (optim-book "Shampoo" chapter) over 2-D and 3-D CUDA
+    parameters: L += G G^T, R += G^T G, W -= lr L^-1/4 G R^-1/4, with the
+    roots refreshed every `root_every` steps (the chapter's 20-100)."""
+
+    def __init__(self, params, lr: float = 1e-2, eps: float = 1e-9, weight_decay: float = 0.0,
+                 root_every: int = 1, ns_split_iters: int = 0, ridge: float = 1e-3):
+        defaults = dict(lr=lr, eps=eps, weight_decay=weight_decay, root_every=root_every,
+                        ns_split_iters=ns_split_iters, ridge=ridge)
+        super().__init__(params, defaults)
+        for g in self.param_groups:
+            g.setdefault("lr_peak", g["lr"])
+
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = closure() if closure is not None else None
+        for g in self.param_groups:
+            for p in g["params"]:
+                if p.grad is None:
+                    continue
+                if p.dim() not in (2, 3):
+                    raise ValueError("Shampoo takes 2-D or 3-D matrix parameters only")
+                st = self.state[p]
+                if "okls" not in st:
+                    B = 1 if p.dim() == 2 else p.shape[0]
+                    m, n = p.shape[-2:]
+                    st["okls"] = OklsBatch(B, m, n, param_dtype=p.dtype, grad_dtype=p.grad.dtype,
+                                           lr=g["lr_peak"], eps=g["eps"], weight_decay=g["weight_decay"],
+                                           ns_split_iters=g["ns_split_iters"], ridge=g["ridge"],
+                                           root_every=g["root_every"], method="shampoo", device=p.device)
                 st["okls"].step(p.data, p.grad.contiguous(), g["lr"])
         return loss

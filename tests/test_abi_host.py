@@ -24,7 +24,7 @@ def test_library_exports_every_header_function(lib):
     assert len(names) >= 15
     for name in names:
         assert hasattr(lib, name), name
-    assert lib.okls_abi_version() == 1
+    assert lib.okls_abi_version() == 2
 
 
 def test_header_names_match_binding():
@@ -107,3 +107,19 @@ def test_create_without_gpu_fails_cleanly(lib):
                            ctypes.byref(h))
     assert code in (L.OKLS_ERR_NO_DEVICE, L.OKLS_ERR_CUDA)
     assert not h.value
+
+
+def test_method_is_validated_and_sizes_the_workspace(lib):
+    """Shampoo mode drops the N^ and X_a^T binary16 buffers and adds one fp32
+    square root per factor (all sizes here are multiples of the 256-byte
+    alignment, so the difference is exact)."""
+    c = L.config_default(2, 96, 40)
+    c.method = 2
+    assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_INVALID_ARG
+    c.method = L.METHOD_OKLS
+    s0, w0 = L.state_bytes(c)
+    c.method = L.METHOD_SHAMPOO
+    s1, w1 = L.state_bytes(c)
+    B, m, n = 2, 96, 40
+    assert s1 == s0
+    assert w1 - w0 == 4 * B * (m * m + n * n) - 2 * B * (m * n + n * m)
