@@ -36,9 +36,13 @@ METRIC = "preconditioned matrices/s per okls_step (TFLOP/s vs GB300 FP16 peak al
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def dense_flops(m: int, n: int) -> float:
-    """Dense algorithmic FLOPs of one matrix's step: 27 products of each
-    Newton-Schulz chain, the two factor products and the whitening."""
+def dense_flops(m: int, n: int, method: str = "okls") -> float:
+    """Dense algorithmic FLOPs of one matrix's step.  OKLS: 27 products of
+    each Newton-Schulz chain, the two preconditioned factor inputs and the
+    two factor products, the whitening.  Classic Shampoo: two chained chains
+    (54 products) per factor, the two factor products of G, the whitening."""
+    if method == "shampoo":
+        return 54 * 2.0 * (m ** 3 + n ** 3) + 2.0 * m * n * (m + n) + 2.0 * m * n * (m + n)
     return 27 * 2.0 * (m ** 3 + n ** 3) + 4.0 * m * n * (m + n) + 2.0 * m * n * (m + n)
 
 
@@ -262,7 +266,7 @@ def run_okls(args):
     groups = []
     for gi, g in enumerate(wl.groups):
         ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=args.split, ridge=args.ridge,
-                       device=dev)
+                       method=args.method, device=dev)
         W = gs.init_weights(gi)
         Gs = [gs.grad(gi, t + 1) for t in range(n_distinct)]
         groups.append((g, ob, W, Gs))
@@ -270,7 +274,7 @@ def run_okls(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     matrices = wl.matrices
-    flops_step = sum(g.batch * dense_flops(g.m, g.n) for g in wl.groups)
+    flops_step = sum(g.batch * dense_flops(g.m, g.n, args.method) for g in wl.groups)
     in_bytes = sum(G[0].numel() * G[0].element_size() for (_g, _ob, _W, G) in groups)
     state_bytes = sum(ob.state.numel() for (_g, ob, _W, _G) in groups)
 
@@ -394,9 +398,8 @@ def run_okls(args):
                "copies": "pinned host, own stream, overlapped with the other groups' steps"}
         del hostG, devG, hostW
 
-    # ------------------------------------------------ second precision mode
-    split_line = None
-    if args.also_split and args.split == 0:
+    # --------------------------------- other modes, timed the same way
+    def rebuild(**kw):
         torch.cuda.synchronize()
         for i in range(len(groups)):
             g, ob, W, Gs = groups[i]
@@ -404,12 +407,16 @@ def run_okls(args):
             groups[i] = (g, None, W, Gs)
             del ob
             torch.cuda.empty_cache()
-            groups[i] = (g, OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=3, ridge=1e-4,
-                                      device=dev), W, Gs)
+            groups[i] = (g, OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, device=dev, **kw), W, Gs)
+
+    def timed():
         for k in range(args.warmup):
             one_step(k)
         torch.cuda.synchronize()
         for (_g, ob, _W, _G) in groups:
+            st = ob.status_nothrow()
+            if st[1]:
+                raise RuntimeError(f"device status 0x{st[1]:x} during warm-up")
             ob.read_profile()
             ob.profile(True)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -418,17 +425,38 @@ def run_okls(args):
             one_step(k)
         b.record(stream)
         torch.cuda.synchronize()
-        ms2 = max_over_ranks(a.elapsed_time(b), ws, dev)
+        ms = max_over_ranks(a.elapsed_time(b), ws, dev)
         gf, gm = 0.0, 0.0
         for (_g, ob, _W, _G) in groups:
             p = ob.read_profile()
             gf += p["gemm_flops"]
             gm += p["gemm_ms"]
+            st = ob.status_nothrow()
+            if st[1]:
+                raise RuntimeError(f"device status 0x{st[1]:x} in the timed region")
+        return ms, (gf / (gm / 1e3) / 1e12 if gm > 0 else None)
+
+    split_line = None
+    if args.also_split and args.split == 0 and args.method == "okls":
+        rebuild(ns_split_iters=3, ridge=1e-4)
+        ms2, gt = timed()
         split_line = {"mode": "iterations 0-2 split (hi/lo binary16), ridge 1e-4, 41 NS products per factor",
                       "value": sum_over_ranks(matrices * args.steps, ws, dev) / (ms2 / 1e3),
                       "unit": "matrices/s", "ms_per_step": ms2 / args.steps,
                       "tflops_dense_27": sum_over_ranks(flops_step * args.steps, ws, dev) / (ms2 / 1e3) / 1e12,
-                      "gemm_tflops_executed": gf / (gm / 1e3) / 1e12 if gm > 0 else None}
+                      "gemm_tflops_executed": gt}
+    shampoo_line = None
+    if args.also_shampoo and args.method == "okls":
+        rebuild(ridge=args.ridge, method="shampoo", lr=args.lr, weight_decay=0.0)
+        ms3, gt = timed()
+        fs = sum(g.batch * dense_flops(g.m, g.n, "shampoo") for g in wl.groups)
+        shampoo_line = {"method": "classic Shampoo: summed factors, L^-1/4 G R^-1/4 by two chained "
+                                  "Newton-Schulz runs (54 binary16 products per factor), ridge "
+                                  f"{args.ridge:g}, roots every step",
+                        "value": sum_over_ranks(matrices * args.steps, ws, dev) / (ms3 / 1e3),
+                        "unit": "matrices/s", "ms_per_step": ms3 / args.steps,
+                        "tflops_dense": sum_over_ranks(fs * args.steps, ws, dev) / (ms3 / 1e3) / 1e12,
+                        "gemm_tflops": gt}
 
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline:
@@ -443,6 +471,7 @@ def run_okls(args):
                 "workload": (f"{args.workload}: " + ", ".join(f"{g.batch} x {g.m}x{g.n} {g.name}" for g in wl.groups)
                              + f" = {matrices} matrices, {wl.groups[0].dtype} W and G, fp32 state, "
                              f"{wl.recipe} gradients (condition number {wl.cond:g})"),
+                "method": args.method,
                 "precision": f"binary16 Newton-Schulz operands, fp32 accumulation, split_iters={args.split}, "
                              f"ridge={args.ridge:g}",
                 "l2": f"inputs larger than L2: {in_bytes / 1e9:.2f} GB of gradients and "
@@ -465,6 +494,8 @@ def run_okls(args):
         }
         if split_line:
             line["split_mode"] = split_line
+        if shampoo_line:
+            line["shampoo"] = shampoo_line
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -485,6 +516,8 @@ def main():
     ap.add_argument("--distinct", type=int, default=4, help="distinct gradient batches kept on the device")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--also-split", type=int, default=1)
+    ap.add_argument("--also-shampoo", type=int, default=1)
+    ap.add_argument("--method", choices=["okls", "shampoo"], default="okls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args()

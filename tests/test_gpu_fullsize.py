@@ -120,3 +120,65 @@ def test_full_size_sampled_parity(name):
     for gi, g in enumerate(wl.groups):
         b = (7 * gi + 3) % g.batch
         _check_group(name, gi, g, gs, b, rng)
+
+
+def _check_group_shampoo(wl_name, gi, g, gs, b, rng):
+    """Classic Shampoo mode at full size: step 2 teacher-forced from the GPU's
+    own state after step 1.  L, R on a 32 x 32 block (exact sums of the GPU's
+    previous factor and G G^T), 1e-3; P against the eigendecomposition
+    quarter root of the GPU's own ridged L, R, 1e-2; 64 sampled U entries
+    against P_exact G P_exact and against the GPU's own roots, 2e-2."""
+    from kronecker_factored_second_gb300.okls import OklsBatch
+    ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, method="shampoo", weight_decay=0.0)
+    hp = hyper_of(ob)
+    W = gs.init_weights(gi)
+    ob.step(W, gs.grad(gi, 1), hp.lr)
+    assert ob.query_status() == 0
+    pre = _matrix_state(ob, b)
+    Wp = W[b].double().cpu().numpy()
+    G = gs.grad(gi, 2)
+    ob.step(W, G, hp.lr)
+    assert ob.query_status() == 0
+    post = _matrix_state(ob, b)
+    Wn = W[b].double().cpu().numpy()
+    Gb = G[b].double().cpu().numpy()
+    ob.close()
+    del ob, W, G
+    torch.cuda.empty_cache()
+
+    m, n = Gb.shape
+    err = {}
+    ia = np.sort(rng.choice(m, size=min(32, m), replace=False))
+    ja = np.sort(rng.choice(m, size=min(32, m), replace=False))
+    err["Sa"] = O.rel_fro(post["Sa"][np.ix_(ia, ja)], pre["Sa"][np.ix_(ia, ja)] + Gb[ia] @ Gb[ja].T)
+    ib = np.sort(rng.choice(n, size=min(32, n), replace=False))
+    jb = np.sort(rng.choice(n, size=min(32, n), replace=False))
+    err["Sb"] = O.rel_fro(post["Sb"][np.ix_(ib, jb)], pre["Sb"][np.ix_(ib, jb)] + Gb[:, ib].T @ Gb[:, jb])
+    t0 = time.time()
+    Pa_x = O.quarter_root_exact(post["Sa"], hp.ridge)
+    Pb_x = O.quarter_root_exact(post["Sb"], hp.ridge)
+    t_eigh = time.time() - t0
+    err["Pa"] = O.rel_fro(post["Pa"], Pa_x)
+    err["Pb"] = O.rel_fro(post["Pb"], Pb_x)
+    ri = rng.choice(m, size=64)
+    ci = rng.choice(n, size=64)
+    U_gpu = (Wp[ri, ci] - Wn[ri, ci]) / hp.lr
+    U_x = np.einsum("ij,ji->i", Pa_x[ri] @ Gb, Pb_x[:, ci])
+    U_tf = np.einsum("ij,ji->i", post["Pa"][ri] @ Gb, post["Pb"][:, ci])
+    err["U"] = float(np.linalg.norm(U_gpu - U_x) / np.linalg.norm(U_x))
+    err["U_tf"] = float(np.linalg.norm(U_gpu - U_tf) / np.linalg.norm(U_tf))
+    print(f"shampoo {wl_name}/{g.name} b={b} ({m}x{n}) eigh {t_eigh:.1f}s", {k: f"{v:.2e}" for k, v in err.items()})
+    assert err["Sa"] < 1e-3 and err["Sb"] < 1e-3, err
+    assert err["Pa"] < 1e-2 and err["Pb"] < 1e-2, err
+    u_tol = 3e-2 if g.dtype == torch.bfloat16 else 2e-2
+    assert err["U"] < u_tol and err["U_tf"] < u_tol, err
+
+
+def test_full_size_sampled_parity_shampoo():
+    """The classic Shampoo leg of bench.py (the 1.2B-shaped set)."""
+    wl = workload("llama1.2b")
+    gs = GradientStream(wl, "cuda")
+    rng = np.random.default_rng(37)
+    for gi, g in enumerate(wl.groups):
+        b = (5 * gi + 1) % g.batch
+        _check_group_shampoo("llama1.2b", gi, g, gs, b, rng)
