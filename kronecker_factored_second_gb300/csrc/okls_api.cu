@@ -428,7 +428,11 @@ struct LaunchBuilder {
         return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: partial-sum slots");
       p.tile_begin = t;
       t += p.tiles_per_mat * p.batch;
+      fastdiv_make(static_cast<uint32_t>(p.tiles_per_mat), &p.tpm_mul, &p.tpm_shift);
+      fastdiv_make(static_cast<uint32_t>(kGroupM * p.tiles_n), &p.span_mul, &p.span_shift);
     }
+    // the kernels decode tile indices in 32 bits
+    if (t >= (int64_t(1) << 31)) return fail(OKLS_ERR_UNSUPPORTED, "more than 2^31 output tiles in one launch");
     L.total_tiles = t;
     L.maps = maps;
     L.status = status;

@@ -20,19 +20,23 @@ struct TileCoord {
 template <int kTileRows>
 __device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t) {
   constexpr int kDiv = kBN / kTileRows;
+  static_assert((kGroupM & (kGroupM - 1)) == 0, "raster group height must be a power of two");
   TileCoord c;
   int p = 0;
   while (p + 1 < L.nprob && t >= L.prob[p + 1].tile_begin) ++p;
   const GemmProblem& P = L.prob[p];
-  const int64_t local = t - P.tile_begin;
+  // tile indices of a launch stay below 2^31 (checked on the host), so the
+  // divisions run in 32 bits by multiplication
+  const uint32_t local = static_cast<uint32_t>(t - P.tile_begin);
   c.p = p;
-  c.mat = static_cast<int>(local / P.tiles_per_mat);
-  int64_t r = local - static_cast<int64_t>(c.mat) * P.tiles_per_mat;
+  const uint32_t mat = fastdiv(local, P.tpm_mul, P.tpm_shift);
+  c.mat = static_cast<int>(mat);
+  uint32_t r = local - mat * static_cast<uint32_t>(P.tiles_per_mat);
   c.lt = r;
   if (P.sym) {
     int tm = 0;
     for (;;) {
-      const int cnt = P.tiles_n - tm / kDiv;
+      const uint32_t cnt = static_cast<uint32_t>(P.tiles_n - tm / kDiv);
       if (r < cnt) break;
       r -= cnt;
       ++tm;
@@ -40,13 +44,17 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t)
     c.tm = tm;
     c.tn = tm / kDiv + static_cast<int>(r);
   } else {
-    const int64_t span = static_cast<int64_t>(kGroupM) * P.tiles_n;
-    const int g = static_cast<int>(r / span);
-    const int first = g * kGroupM;
+    const uint32_t g = fastdiv(r, P.span_mul, P.span_shift);
+    const int first = static_cast<int>(g) * kGroupM;
     const int gm = min(kGroupM, P.tiles_m - first);
-    const int64_t rr = r - static_cast<int64_t>(g) * span;
-    c.tm = first + static_cast<int>(rr % gm);
-    c.tn = static_cast<int>(rr / gm);
+    const uint32_t rr = r - g * static_cast<uint32_t>(kGroupM * P.tiles_n);
+    if (gm == kGroupM) {
+      c.tm = first + static_cast<int>(rr & (kGroupM - 1));
+      c.tn = static_cast<int>(rr / kGroupM);
+    } else {  // the last, shorter group of row blocks
+      c.tm = first + static_cast<int>(rr % static_cast<uint32_t>(gm));
+      c.tn = static_cast<int>(rr / static_cast<uint32_t>(gm));
+    }
   }
   return c;
 }

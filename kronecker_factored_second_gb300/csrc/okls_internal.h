@@ -81,6 +81,9 @@ struct GemmProblem {
   int32_t epi;
   int64_t tiles_per_mat;
   int64_t tile_begin;           // first linear tile of this problem in the launch
+  // exact division of tile indices (< 2^31) by tiles_per_mat and by the raster
+  // group span kGroupM * tiles_n: q = (n * mul) >> shift (host-computed)
+  uint32_t tpm_mul, tpm_shift, span_mul, span_shift;
   // epilogue
   void* out_hi;                 // fp16 row-major
   void* out_hi_t;               // fp16 transposed (may be null)
@@ -101,6 +104,23 @@ struct GemmProblem {
   int32_t split_out;            // 1: also write lo halves
   int32_t check_finite;         // 1: raise kStNonfiniteIter on non-finite acc
 };
+
+// Division by an invariant d >= 1 for dividends n < 2^31: with
+// s = ceil(log2 d) and mul = ceil(2^(31+s) / d) < 2^32, floor(n * mul / 2^(31+s))
+// = floor(n / d), because the rounding of mul adds less than n / 2^(31+s) < 2^-s
+// <= 1/d to n/d (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994).
+__host__ __device__ inline void fastdiv_make(uint32_t d, uint32_t* mul, uint32_t* shift) {
+  uint32_t s = 0;
+  while ((1ull << s) < d) ++s;
+  const unsigned long long num = 1ull << (31 + s);
+  *mul = static_cast<uint32_t>((num + d - 1) / d);
+  *shift = 31 + s;
+}
+
+__host__ __device__ __forceinline__ uint32_t fastdiv(uint32_t n, uint32_t mul, uint32_t shift) {
+  return static_cast<uint32_t>((static_cast<unsigned long long>(n) * mul) >> shift);
+}
 
 struct GemmLaunch {
   GemmProblem prob[kMaxProblems];
