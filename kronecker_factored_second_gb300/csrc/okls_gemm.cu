@@ -131,6 +131,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
       constexpr uint32_t idesc_mn = idesc_f16_f32(kBM, kBN, true);
       constexpr uint32_t idesc_k_half = idesc_f16_f32(kBM, kBN / 2, false);
       constexpr uint32_t idesc_mn_half = idesc_f16_f32(kBM, kBN / 2, true);
+      // descriptors of stage 0; stage s adds s * kStageBytes to the 16-byte
+      // address field (shared memory stays below 2^18 bytes, so it never carries)
+      const uint32_t s0 = smem_u32(smem);
+      const uint64_t adesc0 = sw128_desc(s0);
+      const uint64_t bdesc0_k = sw128_desc(s0 + kStageABytes);
+      const uint64_t bdesc0_mn = sw128_mn_desc(s0 + kStageABytes);
+      constexpr uint64_t kStageDesc = kStageBytes >> 4;
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x, ++it) {
@@ -143,27 +150,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kBN;
         const bool half_n = P.cols - tc.tn * kBN <= kBN / 2;
-        const uint32_t id_k = half_n ? idesc_k_half : idesc_k;
-        const uint32_t id_mn = half_n ? idesc_mn_half : idesc_mn;
+        const uint32_t id = P.bmn ? (half_n ? idesc_mn_half : idesc_mn) : (half_n ? idesc_k_half : idesc_k);
+        const uint64_t bdesc0 = P.bmn ? bdesc0_mn : bdesc0_k;
+        // K16 step of B: 16 rows of 128 B (MN-major) or 32 B (K-major)
+        const uint64_t bstep = P.bmn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, L.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
-          const uint32_t b0 = a0 + kStageABytes;
-          if (P.bmn) {
-#pragma unroll
-            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-              umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_mn_desc(b0 + kk * kUmmaK * 128), id_mn,
-                       (kb | kk) != 0 ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-              umma_f16(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_desc(b0 + kk * kUmmaK * 2), id_k,
-                       (kb | kk) != 0 ? 1u : 0u);
-          }
+          umma_f16_kblock(d, adesc0 + stage * kStageDesc, bdesc0 + stage * kStageDesc, bstep, id, kb != 0 ? 1u : 0u);
           umma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;

@@ -141,6 +141,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // ---------------------------------------------- MMA issuer (leader)
       constexpr uint32_t idesc_k = idesc_f16_f32(256, kBN, false);
       constexpr uint32_t idesc_mn = idesc_f16_f32(256, kBN, true);
+      const uint32_t s0 = smem_u32(smem);
+      const uint64_t adesc0 = sw128_desc(s0);
+      const uint64_t bdesc0_k = sw128_desc(s0 + kPairStageA);
+      const uint64_t bdesc0_mn = sw128_mn_desc(s0 + kPairStageA);
+      constexpr uint64_t kStageDesc = kPairStageBytes >> 4;
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int64_t t = pair_id; t < L.total_tiles && ok; t += npairs, ++it) {
@@ -158,19 +163,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + stage * kPairStageBytes);
-          const uint32_t b0 = a0 + kPairStageA;
-          if (P.bmn) {
-#pragma unroll
-            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-              umma_f16_pair(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_mn_desc(b0 + kk * kUmmaK * 128), idesc_mn,
-                            (kb | kk) != 0 ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-              umma_f16_pair(d, sw128_desc(a0 + kk * kUmmaK * 2), sw128_desc(b0 + kk * kUmmaK * 2), idesc_k,
-                            (kb | kk) != 0 ? 1u : 0u);
-          }
+          umma_f16_pair_kblock(d, adesc0 + stage * kStageDesc, (P.bmn ? bdesc0_mn : bdesc0_k) + stage * kStageDesc,
+                               P.bmn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4, P.bmn ? idesc_mn : idesc_k,
+                               kb != 0 ? 1u : 0u);
           umma_commit_pair(&empty[stage], 0x3);
           if (++stage == kPairStages) {
             stage = 0;

@@ -120,6 +120,32 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64
       : "memory");
 }
 
+// The four K16 MMAs of one 64-deep k-block, issued back to back from one asm
+// block: the issuing thread's instructions between MMAs delay the tensor
+// pipe, so the descriptors of steps 1-3 are the step-0 descriptors plus fixed
+// offsets (A: 32 B per K16 step, +2 in the 16-byte address field; B: `bstep`,
+// +2 K-major or +128 = 2048 B MN-major).  The accumulator is overwritten by
+// the first MMA when `accumulate` is 0.
+__device__ __forceinline__ void umma_f16_kblock(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint64_t bstep,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.eq.b32 q, %3, %3;\n\t"
+      "add.s64 a1, %1, 2;\n\t"
+      "add.s64 b1, %2, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.s64 a2, %1, 4;\n\t"
+      "add.s64 b2, b1, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n\t"
+      "add.s64 a3, %1, 6;\n\t"
+      "add.s64 b3, b2, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "l"(bstep), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -256,6 +282,27 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t tmem_d, uint64_t adesc, u
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// umma_f16_kblock for a CTA pair (M256 across both CTAs' shared memory).
+__device__ __forceinline__ void umma_f16_pair_kblock(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint64_t bstep,
+                                                     uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.eq.b32 q, %3, %3;\n\t"
+      "add.s64 a1, %1, 2;\n\t"
+      "add.s64 b1, %2, %4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.s64 a2, %1, 4;\n\t"
+      "add.s64 b2, b1, %4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, q;\n\t"
+      "add.s64 a3, %1, 6;\n\t"
+      "add.s64 b3, b2, %4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a2, b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a3, b3, %3, q;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "l"(bstep), "r"(accumulate)
       : "memory");
 }
 
