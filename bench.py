@@ -320,7 +320,7 @@ def run_okls(args):
     ms_total = e0.elapsed_time(e1)
     ms_total = max_over_ranks(ms_total, ws, dev)
     prof = {"kernel_launches": 0, "gemm_launches": 0, "gemm_flops": 0.0, "gemm_ms": 0.0, "ns_flops": 0.0,
-            "ns_ms": 0.0, "ns_launches": 0}
+            "ns_ms": 0.0, "ns_launches": 0, "bw_launches": 0, "bw_bytes": 0.0, "bw_ms": 0.0}
     for (_g, ob, _W, _G) in groups:
         p = ob.read_profile()
         for k in prof:
@@ -337,6 +337,15 @@ def run_okls(args):
     peaks, peak_kind = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     achieved = prof["gemm_flops"] / (prof["gemm_ms"] / 1e3) / 1e12 if prof["gemm_ms"] > 0 else None
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bw_gbs = prof["bw_bytes"] / (prof["bw_ms"] / 1e3) / 1e9 if prof["bw_ms"] > 0 else None
+    elementwise = {"kernels": "k_momentum_stats, k_pack, k_normalise (k_sumsq in Shampoo mode)",
+                   "bound": "hbm", "achieved": bw_gbs, "peak": hbm, "unit": "GB/s",
+                   "frac": (bw_gbs / hbm) if bw_gbs else None,
+                   "bytes_per_step": prof["bw_bytes"] / args.steps, "launches_per_step": prof["bw_launches"] / args.steps,
+                   "ms_per_step": prof["bw_ms"] / args.steps,
+                   "share_of_step": prof["bw_ms"] / ms_total if ms_total > 0 else None,
+                   "peak_kind": f"{peak_kind} copy bandwidth"}
     ns_achieved = prof["ns_flops"] / (prof["ns_ms"] / 1e3) / 1e12 if prof["ns_ms"] > 0 else None
 
     # ---------------------------------------------- end to end (host buffers)
@@ -491,6 +500,7 @@ def run_okls(args):
                          "launches": prof["gemm_launches"], "ms_per_launch": prof["gemm_ms"] / max(1, prof["gemm_launches"]),
                          "ns_chain_tflops": ns_achieved,
                          "ns_chain_frac": (ns_achieved / peak) if ns_achieved else None},
+            "elementwise": elementwise,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": prof["kernel_launches"],

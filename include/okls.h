@@ -224,7 +224,10 @@ okls_status okls_destroy(okls_handle h);
 /*
  * Launch accounting of okls_step, for measurement.  Kernel launches are
  * always counted; with timing enabled (okls_profile_enable(h, 1)) every GEMM
- * launch is bracketed by two CUDA events recorded on the step's stream.
+ * and bandwidth-kernel launch is bracketed by two CUDA events recorded on the
+ * step's stream.  Bandwidth bytes are algorithmic: each element read or
+ * written once per launch at its stored width (the per-matrix coefficient
+ * kernels are counted in kernel_launches only).
  * okls_profile_read synchronises on those events, returns the sums since the
  * previous read and resets them.  FLOPs are algorithmic: 2 M N K per K
  * segment for dense products, M (M+1) K for the symmetric factor products.
@@ -238,6 +241,10 @@ typedef struct okls_profile {
   int64_t ns_launches;     /* the Newton-Schulz subset of the GEMMs         */
   double ns_flops;
   double ns_ms;
+  int64_t bw_launches;     /* bandwidth kernels (momentum statistics, pack, */
+  double bw_bytes;         /* normalise, sums of squares): algorithmic DRAM */
+  double bw_ms;            /* bytes and summed event time                   */
+  int64_t bw_timed_launches;
 } okls_profile;
 
 okls_status okls_profile_enable(okls_handle h, int32_t timing);

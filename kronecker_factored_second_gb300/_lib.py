@@ -71,6 +71,10 @@ class okls_profile(ctypes.Structure):
         ("ns_launches", ctypes.c_int64),
         ("ns_flops", ctypes.c_double),
         ("ns_ms", ctypes.c_double),
+        ("bw_launches", ctypes.c_int64),
+        ("bw_bytes", ctypes.c_double),
+        ("bw_ms", ctypes.c_double),
+        ("bw_timed_launches", ctypes.c_int64),
     ]
 
 

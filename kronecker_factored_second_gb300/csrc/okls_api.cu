@@ -282,12 +282,13 @@ struct Prof {
     cudaEvent_t a, b;
     double flops;
     bool ns;
+    bool bw;  // a bandwidth kernel (time goes to bw_ms)
   };
   std::vector<cudaEvent_t> pool;
   size_t used = 0;
   std::vector<Rec> recs;
-  int64_t kernels = 0, gemm_launches = 0, ns_launches = 0;
-  double gemm_flops = 0.0, ns_flops = 0.0;
+  int64_t kernels = 0, gemm_launches = 0, ns_launches = 0, bw_launches = 0;
+  double gemm_flops = 0.0, ns_flops = 0.0, bw_bytes = 0.0;
 
   cudaEvent_t next_event() {
     if (used == pool.size()) {
@@ -308,6 +309,30 @@ thread_local bool g_in_ns = false;
 
 void note_kernels(int n) {
   if (g_prof) g_prof->kernels += n;
+}
+
+// Launch one bandwidth kernel through `launch` (returns cudaError_t), counting
+// it and its algorithmic DRAM bytes, bracketed by events when timing is on.
+template <class F>
+okls_status bw_launch(double bytes, cudaStream_t st, F&& launch) {
+  Prof* pf = g_prof;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  if (pf && pf->timing) {
+    ea = pf->next_event();
+    eb = pf->next_event();
+    if (ea) OKLS_CK(cudaEventRecord(ea, st));
+  }
+  OKLS_CK(launch());
+  if (pf) {
+    if (ea && eb) {
+      OKLS_CK(cudaEventRecord(eb, st));
+      pf->recs.push_back({ea, eb, 0.0, false, true});
+    }
+    pf->kernels += 1;
+    pf->bw_launches += 1;
+    pf->bw_bytes += bytes;
+  }
+  return OKLS_OK;
 }
 
 struct ProfScope {
@@ -454,7 +479,7 @@ struct LaunchBuilder {
     if (pf) {
       if (ea && eb) {
         OKLS_CK(cudaEventRecord(eb, st));
-        pf->recs.push_back({ea, eb, flops, g_in_ns});
+        pf->recs.push_back({ea, eb, flops, g_in_ns, false});
       }
       if (L.total_tiles > 0) {
         pf->kernels += 1;
@@ -569,8 +594,13 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
     A.slot_cprime = f.slot_cprime;
     A.slot_sumsq = f.slot_sumsq;
     A.status = status;
-    OKLS_CK(launch_normalise(A, f.batch, st));
-    note_kernels(1);
+    // per element: the upper triangle of S read and its mirror written
+    // (upper-only input) or all of S read (full input); Y_0, T_0, Z_1 (and
+    // low halves) written
+    const double per = 4.0 + 6.0 + 2.0 * (A.split_y + A.split_t + A.split_z);
+    okls_status s0 = bw_launch(per * f.batch * static_cast<double>(f.d) * f.d, st,
+                               [&] { return launch_normalise(A, f.batch, st); });
+    if (s0 != OKLS_OK) return s0;
   }
   if (tr && tr->base) {
     okls_status s;
@@ -917,16 +947,25 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
 
   // 1-2. momentum, statistics, packed binary16 operands
   OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(4 * B * 4), st));  // SC_SUMSQ_* slots
-  OKLS_CK(launch_momentum_stats(G, gbf, M, B, static_cast<int64_t>(m) * n, b1, kappa, h->part_g, h->part_g_ld,
-                                h->status, st));
+  const double elems = static_cast<double>(B) * m * n;
+  const double gsz = gbf ? 2.0 : 4.0;
+  if ((s = bw_launch(elems * (gsz + (M ? 4.0 : 0.0)), st, [&] {
+         return launch_momentum_stats(G, gbf, M, B, static_cast<int64_t>(m) * n, b1, kappa, h->part_g, h->part_g_ld,
+                                      h->status, st);
+       })) != OKLS_OK)
+    return s;
   OKLS_CK(launch_coeffs_pre(B, m, n, c.beta2, shampoo ? 1 : 0, h->scal, sld, h->part_g, h->part_g_ld, st));
+  note_kernels(1);
   // row pitches: Ghat and Nhat are m x n (pitch ldn), Ghat^T is n x m (pitch ldm)
   if (h->Gh.ld < n || h->GhT.ld < m || h->Gh.rows != m || h->GhT.rows != n ||
       (!shampoo && h->Nh.ld != h->Gh.ld))
     return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: packed operand pitches");
-  OKLS_CK(launch_pack(G, gbf, M, h->Gh.p, h->GhT.p, shampoo ? nullptr : h->Nh.p, B, m, n, /*ldm=*/h->GhT.ld,
-                      /*ldn=*/h->Gh.ld, b1, kappa, h->scal, sld, h->status, st));
-  note_kernels(3);
+  // G read; M read and written; Ghat, Ghat^T (and Nhat) written
+  if ((s = bw_launch(elems * (gsz + (M ? 8.0 : 0.0) + 4.0 + (shampoo ? 0.0 : 2.0)), st, [&] {
+         return launch_pack(G, gbf, M, h->Gh.p, h->GhT.p, shampoo ? nullptr : h->Nh.p, B, m, n,
+                            /*ldm=*/h->GhT.ld, /*ldn=*/h->Gh.ld, b1, kappa, h->scal, sld, h->status, st);
+       })) != OKLS_OK)
+    return s;
   // 3. OKLS: X_b = G P_b and X_a^T = G^T P_a^T (previous roots); Shampoo
   //    feeds G itself to the factor products
   const Buf* Xa = &h->XaT;
@@ -997,12 +1036,18 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
       if ((s = run_ns(f1, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
                       nullptr, /*root_only=*/true)) != OKLS_OK)
         return s;
-      OKLS_CK(launch_sumsq(h->sq_a, B, static_cast<int64_t>(m) * m, h->part_a, h->part_a_ld, st));
-      OKLS_CK(launch_sumsq(h->sq_b, B, static_cast<int64_t>(n) * n, h->part_b, h->part_b_ld, st));
+      if ((s = bw_launch(4.0 * B * static_cast<double>(m) * m, st, [&] {
+             return launch_sumsq(h->sq_a, B, static_cast<int64_t>(m) * m, h->part_a, h->part_a_ld, st);
+           })) != OKLS_OK)
+        return s;
+      if ((s = bw_launch(4.0 * B * static_cast<double>(n) * n, st, [&] {
+             return launch_sumsq(h->sq_b, B, static_cast<int64_t>(n) * n, h->part_b, h->part_b_ld, st);
+           })) != OKLS_OK)
+        return s;
       OKLS_CK(launch_coeffs_post(B, 0.0f, zK, zK1, h->scal, sld, kPostRoots, h->status, h->part_a, h->part_a_ld,
                                  sumsq_parts(static_cast<int64_t>(m) * m), h->part_b, h->part_b_ld,
                                  sumsq_parts(static_cast<int64_t>(n) * n), st));
-      note_kernels(3);
+      note_kernels(1);
       Factor qa = h->fa, qb = h->fb;
       qa.S = h->sq_a;
       qa.S_upper_only = false;
@@ -1036,8 +1081,10 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
       A.scal = h->scal;
       A.scal_ld = sld;
       A.status = h->status;
-      OKLS_CK(launch_normalise(A, f->batch, st));
-      note_kernels(1);
+      // the upper triangle of S read, the lower one written
+      if ((s = bw_launch(4.0 * f->batch * static_cast<double>(f->d) * f->d, st,
+                         [&] { return launch_normalise(A, f->batch, st); })) != OKLS_OK)
+        return s;
     }
   }
   // 7. Q = P_a N (N = G for Shampoo) into the X_b buffer
@@ -1159,18 +1206,25 @@ okls_status okls_profile_read(okls_handle h, okls_profile* out) {
   out->gemm_flops = p.gemm_flops;
   out->ns_launches = p.ns_launches;
   out->ns_flops = p.ns_flops;
+  out->bw_launches = p.bw_launches;
+  out->bw_bytes = p.bw_bytes;
   for (const Prof::Rec& r : p.recs) {
     OKLS_CK(cudaEventSynchronize(r.b));
     float ms = 0.0f;
     OKLS_CK(cudaEventElapsedTime(&ms, r.a, r.b));
+    if (r.bw) {
+      out->bw_ms += ms;
+      out->bw_timed_launches += 1;
+      continue;
+    }
     out->gemm_ms += ms;
     if (r.ns) out->ns_ms += ms;
     out->timed_launches += 1;
   }
   p.recs.clear();
   p.used = 0;
-  p.kernels = p.gemm_launches = p.ns_launches = 0;
-  p.gemm_flops = p.ns_flops = 0.0;
+  p.kernels = p.gemm_launches = p.ns_launches = p.bw_launches = 0;
+  p.gemm_flops = p.ns_flops = p.bw_bytes = 0.0;
   return OKLS_OK;
 }
 

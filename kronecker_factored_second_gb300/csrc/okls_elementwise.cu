@@ -48,7 +48,32 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // ------------------------------------------------------------ momentum stats
+// 8 consecutive elements of G (bf16 or fp32) and of M as floats
 template <typename GT>
+__device__ __forceinline__ void load8(const GT* p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
+  }
+}
+
+// Sums of G^2 and N^2 of one matrix per blockIdx.y, one fixed partial per
+// block.  kVec: 8 elements per thread and step with 16-byte loads (mn a
+// multiple of 8, so every matrix starts 16-byte aligned).
+template <typename GT, bool kVec>
 __global__ void k_momentum_stats(const GT* __restrict__ G, const float* __restrict__ M,
                                  int64_t mn, float b1, float kappa, float* part, int64_t part_ld,
                                  int batch, uint32_t* status) {
@@ -58,15 +83,36 @@ __global__ void k_momentum_stats(const GT* __restrict__ G, const float* __restri
   const float* mo = M ? M + static_cast<int64_t>(b) * mn : nullptr;  // null: no momentum
   float sg = 0.0f, sn = 0.0f;
   bool bad = false;
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < mn;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float gv = to_f(g[e]);
-    const float mv = mo ? mo[e] : 0.0f;
-    const float mn1 = fmaf(b1, mv, (1.0f - b1) * gv);
-    const float nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
-    bad |= !isfinite(gv) || !isfinite(mv);
-    sg = fmaf(gv, gv, sg);
-    sn = fmaf(nv, nv, sn);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  if (kVec) {
+    for (int64_t e8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e8 < mn / 8; e8 += stride) {
+      float gv[8], mv[8];
+      load8<GT>(g + e8 * 8, gv);
+      if (mo) {
+        load8<float>(mo + e8 * 8, mv);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mv[e] = 0.0f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float mn1 = fmaf(b1, mv[e], (1.0f - b1) * gv[e]);
+        const float nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv[e]);
+        bad |= !isfinite(gv[e]) || !isfinite(mv[e]);
+        sg = fmaf(gv[e], gv[e], sg);
+        sn = fmaf(nv, nv, sn);
+      }
+    }
+  } else {
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < mn; e += stride) {
+      const float gv = to_f(g[e]);
+      const float mv = mo ? mo[e] : 0.0f;
+      const float mn1 = fmaf(b1, mv, (1.0f - b1) * gv);
+      const float nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
+      bad |= !isfinite(gv) || !isfinite(mv);
+      sg = fmaf(gv, gv, sg);
+      sn = fmaf(nv, nv, sn);
+    }
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, kStNonfiniteInput);
   const float tg = block_sum(sg, red);
@@ -122,15 +168,22 @@ __global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, int s
 }
 
 // ------------------------------------------------------------------ pack
+// One block per 64 x 64 tile of one matrix: each thread takes 16 consecutive
+// columns of one row (16-byte loads and stores when n is a multiple of 8),
+// writes M_t, Ghat and Nhat row-major, and Ghat^T goes out through the
+// shared-memory tile, again as 16 consecutive elements per thread.
+constexpr int kPT = 64;
+
 template <typename GT>
-__global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* __restrict__ Gh,
-                       __half* __restrict__ GhT, __half* __restrict__ Nh, int m, int n, int64_t ldm,
-                       int64_t ldn, float b1, float kappa, const float* scal, int scal_ld,
-                       const uint32_t* status) {
-  __shared__ float sg[32][33];
+__global__ void __launch_bounds__(256) k_pack(const GT* __restrict__ G, float* __restrict__ M,
+                                              __half* __restrict__ Gh, __half* __restrict__ GhT,
+                                              __half* __restrict__ Nh, int m, int n, int64_t ldm, int64_t ldn,
+                                              float b1, float kappa, const float* scal, int scal_ld,
+                                              const uint32_t* status) {
+  __shared__ float sg[kPT][kPT + 1];
   if (*reinterpret_cast<const volatile uint32_t*>(status) != 0u) return;
   const int b = blockIdx.z;
-  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const int r0 = blockIdx.y * kPT, c0 = blockIdx.x * kPT;
   const float gs = scal[static_cast<int64_t>(SC_GSCALE) * scal_ld + b];
   const float ns = scal[static_cast<int64_t>(SC_NSCALE) * scal_ld + b];
   const int64_t mn = static_cast<int64_t>(m) * n;
@@ -138,28 +191,76 @@ __global__ void k_pack(const GT* __restrict__ G, float* __restrict__ M, __half* 
   float* mo = M ? M + b * mn : nullptr;  // null: no momentum (Shampoo)
   __half* gh = Gh + b * static_cast<int64_t>(m) * ldn;
   __half* nh = Nh ? Nh + b * static_cast<int64_t>(m) * ldn : nullptr;  // null: N = G
-  const int tx = threadIdx.x;
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int i = r0 + r, j = c0 + tx;
-    float gv = 0.0f, nv = 0.0f;
-    if (i < m && j < n) {
-      const int64_t e = static_cast<int64_t>(i) * n + j;
-      gv = to_f(g[e]);
-      gh[static_cast<int64_t>(i) * ldn + j] = __float2half_rn(gv * gs);
-      if (mo) {
-        const float mn1 = fmaf(b1, mo[e], (1.0f - b1) * gv);
-        nv = kappa * fmaf(b1, mn1, (1.0f - b1) * gv);
-        mo[e] = mn1;
+  const bool vec = (n & 7) == 0;
+  // rows r0 + R: 8 threads cover 64 columns, 8 each (16-byte loads/stores)
+#pragma unroll 1
+  for (int p = 0; p < kPT / 32; ++p) {
+    const int R = p * 32 + threadIdx.x / 8, C = (threadIdx.x % 8) * 8;
+    const int i = r0 + R, j = c0 + C;
+    float gv[8], mv[8], nv[8];
+    const bool full = vec && i < m && j + 8 <= n;
+    if (full) {
+      load8<GT>(g + static_cast<int64_t>(i) * n + j, gv);
+      if (mo) load8<float>(mo + static_cast<int64_t>(i) * n + j, mv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bool in = i < m && j + e < n;
+        gv[e] = in ? to_f(g[static_cast<int64_t>(i) * n + j + e]) : 0.0f;
+        mv[e] = (in && mo) ? mo[static_cast<int64_t>(i) * n + j + e] : 0.0f;
       }
-      if (nh) nh[static_cast<int64_t>(i) * ldn + j] = __float2half_rn(nv * ns);
     }
-    sg[r][tx] = gv * gs;
+    if (!mo) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mv[e] = 0.0f;
+    }
+    __align__(16) __half hg[8], hn[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float m1 = fmaf(b1, mv[e], (1.0f - b1) * gv[e]);
+      nv[e] = kappa * fmaf(b1, m1, (1.0f - b1) * gv[e]);
+      mv[e] = m1;
+      hg[e] = __float2half_rn(gv[e] * gs);
+      hn[e] = __float2half_rn(nv[e] * ns);
+      sg[R][C + e] = gv[e] * gs;
+    }
+    if (full) {
+      if (mo) {
+        float4* dm = reinterpret_cast<float4*>(mo + static_cast<int64_t>(i) * n + j);
+        dm[0] = make_float4(mv[0], mv[1], mv[2], mv[3]);
+        dm[1] = make_float4(mv[4], mv[5], mv[6], mv[7]);
+      }
+      *reinterpret_cast<uint4*>(gh + static_cast<int64_t>(i) * ldn + j) = *reinterpret_cast<const uint4*>(hg);
+      if (nh) *reinterpret_cast<uint4*>(nh + static_cast<int64_t>(i) * ldn + j) = *reinterpret_cast<const uint4*>(hn);
+    } else if (i < m) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (j + e < n) {
+          if (mo) mo[static_cast<int64_t>(i) * n + j + e] = mv[e];
+          gh[static_cast<int64_t>(i) * ldn + j + e] = hg[e];
+          if (nh) nh[static_cast<int64_t>(i) * ldn + j + e] = hn[e];
+        }
+      }
+    }
   }
   __syncthreads();
+  // Ghat^T: row c0 + R holds column R of the tile; 8 threads per 64 entries
   __half* gt = GhT + b * static_cast<int64_t>(n) * ldm;
-  for (int c = threadIdx.y; c < 32; c += 8) {
-    const int j = c0 + c, i = r0 + tx;
-    if (i < m && j < n) gt[static_cast<int64_t>(j) * ldm + i] = __float2half_rn(sg[tx][c]);
+#pragma unroll 1
+  for (int p = 0; p < kPT / 32; ++p) {
+    const int R = p * 32 + threadIdx.x / 8, C = (threadIdx.x % 8) * 8;
+    const int jt = c0 + R, i0 = r0 + C;
+    if (jt >= n) continue;
+    __align__(16) __half ht[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ht[e] = __float2half_rn(sg[C + e][R]);
+    if (i0 + 8 <= m) {
+      *reinterpret_cast<uint4*>(gt + static_cast<int64_t>(jt) * ldm + i0) = *reinterpret_cast<const uint4*>(ht);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (i0 + e < m) gt[static_cast<int64_t>(jt) * ldm + i0 + e] = ht[e];
+    }
   }
 }
 
@@ -202,25 +303,191 @@ __global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* sc
 }
 
 // ---------------------------------------------------------------- normalise
-__global__ void k_normalise(NormaliseArgs A) {
-  __shared__ float t1[32][33];
-  __shared__ float t2[32][33];
+// One block per pair of 64 x 64 tiles (tr, tc), tr <= tc, of one matrix: S is
+// read once per pair (the upper tile, or both tiles when a full input is
+// symmetrised), the outputs of the upper tile are written row by row and
+// those of the mirrored tile (equal by symmetry, recomputed bit for bit from
+// the same fp32 value) from the transposed shared-memory tile, and for
+// upper-only input the lower tile of S is written back as the mirror.
+constexpr int kNT = 64;         // normaliser tile edge
+constexpr int kNTP = kNT + 1;   // padded shared-memory pitch
+
+// the q-th (tr, tc) of the upper triangle of an nt x nt tile grid, row-major
+__device__ __forceinline__ void upper_pair(int q, int nt, int& tr, int& tc) {
+  // reversed index u counts from the last row, whose rows hold 1, 2, ... tiles
+  const int u = nt * (nt + 1) / 2 - 1 - q;
+  int k = static_cast<int>((sqrtf(8.0f * static_cast<float>(u) + 1.0f) - 1.0f) * 0.5f);
+  while (k * (k + 1) / 2 > u) --k;
+  while ((k + 1) * (k + 2) / 2 <= u) ++k;
+  tr = nt - 1 - k;
+  tc = nt - 1 - (u - k * (k + 1) / 2);
+}
+
+struct NormOut {
+  __half y, t, z, yl, tl, zl;
+  bool bad;
+};
+
+__device__ __forceinline__ NormOut norm_value(const NormaliseArgs& A, float s, bool diag, float inv, float rc,
+                                             float a0h, float zsc) {
+  NormOut o;
+  const float y = (s + (diag ? rc : 0.0f)) * inv;
+  o.y = __float2half_rn(y);
+  float yv = __half2float(o.y);
+  o.yl = __float2half_rn(0.0f);
+  if (A.split_y) {
+    o.yl = __float2half_rn(y - yv);
+    yv += __half2float(o.yl);
+  }
+  const float t = fmaf(A.b0, yv, diag ? a0h : 0.0f);
+  o.t = __float2half_rn(t);
+  float tv = __half2float(o.t);
+  o.tl = __float2half_rn(0.0f);
+  if (A.split_t) {
+    o.tl = __float2half_rn(t - tv);
+    tv += __half2float(o.tl);
+  }
+  const float z = tv * zsc;
+  o.z = __float2half_rn(z);
+  o.zl = A.split_z ? __float2half_rn(z - __half2float(o.z)) : __float2half_rn(0.0f);
+  o.bad = !isfinite(y);
+  return o;
+}
+
+// Write the outputs of 8 consecutive columns [j0, j0+8) of row i (binary16
+// rows are 16-byte aligned; ragged ends fall back to single stores).
+__device__ __forceinline__ void norm_store8(const NormaliseArgs& A, int64_t moff, int i, int j0, int d,
+                                           const float* v, float inv, float rc, float a0h, float zsc, bool& bad) {
+  __align__(16) __half hy[8], ht[8], hz[8], ly[8], lt[8], lz[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const NormOut o = norm_value(A, v[e], j0 + e == i, inv, rc, a0h, zsc);
+    hy[e] = o.y;
+    ht[e] = o.t;
+    hz[e] = o.z;
+    ly[e] = o.yl;
+    lt[e] = o.tl;
+    lz[e] = o.zl;
+    bad |= o.bad && (j0 + e < d);
+  }
+  const int64_t e0 = moff + static_cast<int64_t>(i) * A.ld16 + j0;
+  if (j0 + 8 <= d) {
+    *reinterpret_cast<uint4*>(A.Y + e0) = *reinterpret_cast<const uint4*>(hy);
+    *reinterpret_cast<uint4*>(A.T + e0) = *reinterpret_cast<const uint4*>(ht);
+    *reinterpret_cast<uint4*>(A.Z + e0) = *reinterpret_cast<const uint4*>(hz);
+    if (A.split_y) *reinterpret_cast<uint4*>(A.Ylo + e0) = *reinterpret_cast<const uint4*>(ly);
+    if (A.split_t) *reinterpret_cast<uint4*>(A.Tlo + e0) = *reinterpret_cast<const uint4*>(lt);
+    if (A.split_z) *reinterpret_cast<uint4*>(A.Zlo + e0) = *reinterpret_cast<const uint4*>(lz);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (j0 + e < d) {
+        A.Y[e0 + e] = hy[e];
+        A.T[e0 + e] = ht[e];
+        A.Z[e0 + e] = hz[e];
+        if (A.split_y) A.Ylo[e0 + e] = ly[e];
+        if (A.split_t) A.Tlo[e0 + e] = lt[e];
+        if (A.split_z) A.Zlo[e0 + e] = lz[e];
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256, 3) k_normalise(NormaliseArgs A) {
+  __shared__ float sm[kNT][kNTP];
   if (A.status && *reinterpret_cast<const volatile uint32_t*>(A.status) != 0u) return;
-  const int b = blockIdx.z;
+  const int b = blockIdx.y;
   const int d = A.d;
-  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const int nt = (d + kNT - 1) / kNT;
+  int tr, tc;
+  upper_pair(static_cast<int>(blockIdx.x), nt, tr, tc);
+  const int r0 = tr * kNT, c0 = tc * kNT;
+  const bool diag_tile = tr == tc;
   float* S = A.S + static_cast<int64_t>(b) * d * d;
-  const int tx = threadIdx.x;
-  // tile (r0, c0) and the transposed tile (c0, r0); for upper-only input the
-  // value of (i, j) is read from whichever of the two holds it on or above the
-  // diagonal (only those elements are ever read, and only lower ones written)
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int i = r0 + r, j = c0 + tx;
-    t1[r][tx] = (i < d && j < d) ? S[static_cast<int64_t>(i) * d + j] : 0.0f;
-    const int i2 = c0 + r, j2 = r0 + tx;
-    t2[r][tx] = (i2 < d && j2 < d) ? S[static_cast<int64_t>(i2) * d + j2] : 0.0f;
+  const int tid = threadIdx.x;
+  const bool vec = (d & 3) == 0;
+
+  // 1. the upper tile (r0.., c0..) into shared memory; a full input is
+  //    symmetrised with its transposed tile, (S + S^T) / 2
+  for (int q = tid; q < kNT * (kNT / 4); q += 256) {
+    const int r = q / (kNT / 4), c = (q % (kNT / 4)) * 4;
+    const int i = r0 + r, j = c0 + c;
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (i < d) {
+      const float* src = S + static_cast<int64_t>(i) * d + j;
+      if (vec && j + 3 < d) {
+        v = *reinterpret_cast<const float4*>(src);
+      } else {
+        if (j < d) v.x = src[0];
+        if (j + 1 < d) v.y = src[1];
+        if (j + 2 < d) v.z = src[2];
+        if (j + 3 < d) v.w = src[3];
+      }
+    }
+    sm[r][c] = v.x;
+    sm[r][c + 1] = v.y;
+    sm[r][c + 2] = v.z;
+    sm[r][c + 3] = v.w;
   }
   __syncthreads();
+  if (!A.upper_only) {
+    // add the tile (c0.., r0..) transposed; on the diagonal tile that is the
+    // tile itself
+    float part[16];
+    const int r = tid / 4, cb = (tid % 4) * 16;  // this thread's 16 entries of row r of the tile
+    if (diag_tile) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) part[e] = 0.5f * (sm[r][cb + e] + sm[cb + e][r]);
+    } else {
+      // S[c0 + cb + e][r0 + r]: a column of the lower tile, read once per entry
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int i2 = c0 + cb + e, j2 = r0 + r;
+        const float w = (i2 < d && j2 < d) ? S[static_cast<int64_t>(i2) * d + j2] : 0.0f;
+        part[e] = 0.5f * (sm[r][cb + e] + w);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sm[r][cb + e] = part[e];
+    __syncthreads();
+  } else if (diag_tile) {
+    // upper-only diagonal tile: the entries below the diagonal are the mirror
+    float part[16];
+    const int r = tid / 4, cb = (tid % 4) * 16;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) part[e] = (cb + e >= r) ? sm[r][cb + e] : sm[cb + e][r];
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sm[r][cb + e] = part[e];
+    __syncthreads();
+  }
+
+  // 2. the lower triangle of the state for upper-only input: rows c0 + R of
+  //    the lower tile hold sm[.][R]; 16 threads write one 256-byte row
+  if (A.upper_only) {
+#pragma unroll 1
+    for (int p = 0; p < kNT / 16; ++p) {
+      const int R = p * 16 + tid / 16, C = (tid % 16) * 4;
+      const int i = c0 + R, j = r0 + C;
+      if (i >= d) continue;
+      float* dst = S + static_cast<int64_t>(i) * d + j;
+      const float v0 = sm[C][R], v1 = sm[C + 1][R], v2 = sm[C + 2][R], v3 = sm[C + 3][R];
+      if (!diag_tile && vec && j + 3 < d) {
+        *reinterpret_cast<float4*>(dst) = make_float4(v0, v1, v2, v3);
+      } else {
+        // the diagonal tile writes only below the diagonal
+        if (j < d && (!diag_tile || j < i)) dst[0] = v0;
+        if (j + 1 < d && (!diag_tile || j + 1 < i)) dst[1] = v1;
+        if (j + 2 < d && (!diag_tile || j + 2 < i)) dst[2] = v2;
+        if (j + 3 < d && (!diag_tile || j + 3 < i)) dst[3] = v3;
+      }
+    }
+  }
+  if (A.mirror_only) return;
+
+  // 3. Y_0, T_0, Z_1 of the upper tile, then of the mirrored tile; 8 threads
+  //    cover one 128-byte binary16 row of the tile
   const float cp = A.scal[static_cast<int64_t>(A.slot_cprime) * A.scal_ld + b];
   const float c = sqrtf(A.scal[static_cast<int64_t>(A.slot_sumsq) * A.scal_ld + b]);
   const float inv = ldexpf(1.0f, kHeadroom) / cp;
@@ -228,51 +495,30 @@ __global__ void k_normalise(NormaliseArgs A) {
   const float a0h = ldexpf(A.a0, kHeadroom);
   const float zsc = ldexpf(1.0f, -A.z1);
   const int64_t moff = static_cast<int64_t>(b) * A.mat16;
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int i = r0 + r, j = c0 + tx;
-    if (i >= d || j >= d) continue;
-    float s;
-    if (A.upper_only) {
-      s = (i <= j) ? t1[r][tx] : t2[tx][r];
-      if (i > j) S[static_cast<int64_t>(i) * d + j] = s;  // mirror into the state
-    } else {
-      s = 0.5f * (t1[r][tx] + t2[tx][r]);
+  bool bad = false;
+#pragma unroll 1
+  for (int p = 0; p < kNT / 32; ++p) {
+    const int R = p * 32 + tid / 8, C = (tid % 8) * 8;
+    {
+      const int i = r0 + R;
+      if (i < d && c0 + C < d) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = sm[R][C + e];
+        norm_store8(A, moff, i, c0 + C, d, v, inv, rc, a0h, zsc, bad);
+      }
     }
-    if (A.mirror_only) continue;
-    const float y = (s + (i == j ? rc : 0.0f)) * inv;
-    const int64_t e = moff + static_cast<int64_t>(i) * A.ld16 + j;
-    const __half yh = __float2half_rn(y);
-    float yv = __half2float(yh);
-    if (A.split_y) {
-      const __half yl = __float2half_rn(y - yv);
-      A.Ylo[e] = yl;
-      if (A.YTlo) A.YTlo[e] = yl;
-      yv += __half2float(yl);
+    if (!diag_tile) {
+      const int i = c0 + R;
+      if (i < d && r0 + C < d) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = sm[C + e][R];
+        norm_store8(A, moff, i, r0 + C, d, v, inv, rc, a0h, zsc, bad);
+      }
     }
-    A.Y[e] = yh;
-    if (A.YT) A.YT[e] = yh;
-    const float t = fmaf(A.b0, yv, i == j ? a0h : 0.0f);
-    const __half th = __float2half_rn(t);
-    float tv = __half2float(th);
-    if (A.split_t) {
-      const __half tl = __float2half_rn(t - tv);
-      A.Tlo[e] = tl;
-      if (A.TTlo) A.TTlo[e] = tl;
-      tv += __half2float(tl);
-    }
-    A.T[e] = th;
-    if (A.TT) A.TT[e] = th;
-    const float z = tv * zsc;
-    const __half zh = __float2half_rn(z);
-    if (A.split_z) {
-      const __half zl = __float2half_rn(z - __half2float(zh));
-      A.Zlo[e] = zl;
-      if (A.ZTlo) A.ZTlo[e] = zl;
-    }
-    A.Z[e] = zh;
-    if (A.ZT) A.ZT[e] = zh;
-    if (!isfinite(y) && A.status) atomicOr(A.status, kStNonfiniteIter);
   }
+  if (bad && A.status) atomicOr(A.status, kStNonfiniteIter);
 }
 
 // ------------------------------------------------------------- small helpers
@@ -399,12 +645,20 @@ cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int
   const int per_mat = momentum_parts(mn);
   if (per_mat > part_ld) return cudaErrorInvalidValue;
   dim3 grid(per_mat, batch);
-  if (g_bf16)
-    k_momentum_stats<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(G), M, mn,
-                                                          b1, kappa, part, part_ld, batch, status);
-  else
-    k_momentum_stats<float><<<grid, 256, 0, st>>>(static_cast<const float*>(G), M, mn, b1, kappa, part,
-                                                  part_ld, batch, status);
+  const bool vec = (mn % 8) == 0;
+  if (g_bf16) {
+    const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(G);
+    if (vec)
+      k_momentum_stats<__nv_bfloat16, true><<<grid, 256, 0, st>>>(g, M, mn, b1, kappa, part, part_ld, batch, status);
+    else
+      k_momentum_stats<__nv_bfloat16, false><<<grid, 256, 0, st>>>(g, M, mn, b1, kappa, part, part_ld, batch, status);
+  } else {
+    const float* g = static_cast<const float*>(G);
+    if (vec)
+      k_momentum_stats<float, true><<<grid, 256, 0, st>>>(g, M, mn, b1, kappa, part, part_ld, batch, status);
+    else
+      k_momentum_stats<float, false><<<grid, 256, 0, st>>>(g, M, mn, b1, kappa, part, part_ld, batch, status);
+  }
   return cudaGetLastError();
 }
 
@@ -418,13 +672,13 @@ cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, int 
 cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half* GhT, __half* Nh,
                         int batch, int m, int n, int64_t ldm, int64_t ldn, float b1, float kappa,
                         const float* scal, int scal_ld, const uint32_t* status, cudaStream_t st) {
-  dim3 grid((n + 31) / 32, (m + 31) / 32, batch), block(32, 8);
+  dim3 grid((n + kPT - 1) / kPT, (m + kPT - 1) / kPT, batch);
   if (g_bf16)
-    k_pack<__nv_bfloat16><<<grid, block, 0, st>>>(static_cast<const __nv_bfloat16*>(G), M, Gh, GhT, Nh,
-                                                  m, n, ldm, ldn, b1, kappa, scal, scal_ld, status);
+    k_pack<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(G), M, Gh, GhT, Nh, m, n, ldm,
+                                                ldn, b1, kappa, scal, scal_ld, status);
   else
-    k_pack<float><<<grid, block, 0, st>>>(static_cast<const float*>(G), M, Gh, GhT, Nh, m, n, ldm, ldn,
-                                          b1, kappa, scal, scal_ld, status);
+    k_pack<float><<<grid, 256, 0, st>>>(static_cast<const float*>(G), M, Gh, GhT, Nh, m, n, ldm, ldn, b1, kappa,
+                                        scal, scal_ld, status);
   return cudaGetLastError();
 }
 
@@ -437,8 +691,9 @@ cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* s
 }
 
 cudaError_t launch_normalise(const NormaliseArgs& A, int batch, cudaStream_t st) {
-  dim3 grid((A.d + 31) / 32, (A.d + 31) / 32, batch), block(32, 8);
-  k_normalise<<<grid, block, 0, st>>>(A);
+  const int nt = (A.d + kNT - 1) / kNT;
+  dim3 grid(nt * (nt + 1) / 2, batch);
+  k_normalise<<<grid, 256, 0, st>>>(A);
   return cudaGetLastError();
 }
 

@@ -15,10 +15,10 @@ struct NormaliseArgs {
                     //    read it and write the mirrored lower triangle back;
                     // 0: S is a full input, symmetrised as (S + S^T)/2, not written
   int d;
-  int64_t ld16, mat16;
-  __half *Y, *YT, *Ylo, *YTlo;   // Y_0 (both layouts; equal by symmetry)
-  __half *T, *TT, *Tlo, *TTlo;   // T_0
-  __half *Z, *ZT, *Zlo, *ZTlo;   // Z_1 = T_0
+  int64_t ld16, mat16;           // binary16 row pitch (multiple of 8) and matrix stride
+  __half *Y, *Ylo;               // Y_0 (and its low half in the split mode)
+  __half *T, *Tlo;               // T_0
+  __half *Z, *Zlo;               // Z_1 = T_0 2^-z_1
   int split_y, split_t, split_z;
   float a0, b0;
   int z1;
