@@ -124,12 +124,18 @@ __global__ void k_momentum_stats(const GT* __restrict__ G, const float* __restri
   }
 }
 
-// fixed-order double sum of n partials
-__device__ __forceinline__ double sum_parts(const float* p, int64_t n) {
+// Double sum of n partials by one warp in a fixed order: lane l adds
+// p[l], p[l+32], ... in turn, then the lanes' sums are combined by a fixed
+// butterfly and lane 0's value is broadcast, so every run gives the same bits.
+__device__ __forceinline__ double warp_sum_parts(const float* p, int64_t n) {
+  const int lane = threadIdx.x & 31;
   double s = 0.0;
-  for (int64_t i = 0; i < n; ++i) s += static_cast<double>(p[i]);
-  return s;
+  for (int64_t i = lane; i < n; i += 32) s += static_cast<double>(p[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return __shfl_sync(0xffffffffu, s, 0);
 }
+constexpr int kCoeffWarps = 4;  // matrices per block of the coefficient kernels
 
 // power of two 2^e with rms * 2^e in [1, 2); 1 for an all-zero matrix
 __device__ __forceinline__ float pow2_rms_scale(float sumsq, double count) {
@@ -140,13 +146,17 @@ __device__ __forceinline__ float pow2_rms_scale(float sumsq, double count) {
   return ldexpf(1.0f, e);
 }
 
+// one warp per matrix
 __global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, int shampoo, float* scal,
                              int scal_ld, const float* part, int64_t part_ld, int nparts) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  const int b = blockIdx.x * kCoeffWarps + (threadIdx.x >> 5);
   if (b >= batch) return;
+  const double sg = warp_sum_parts(part + static_cast<int64_t>(b) * part_ld, nparts);
+  const double sn = warp_sum_parts(part + (static_cast<int64_t>(batch) + b) * part_ld, nparts);
+  if ((threadIdx.x & 31) != 0) return;
   auto S = [&](int slot) -> float& { return scal[static_cast<int64_t>(slot) * scal_ld + b]; };
-  S(SC_SUMSQ_G) = static_cast<float>(sum_parts(part + static_cast<int64_t>(b) * part_ld, nparts));
-  S(SC_SUMSQ_N) = static_cast<float>(sum_parts(part + (static_cast<int64_t>(batch) + b) * part_ld, nparts));
+  S(SC_SUMSQ_G) = static_cast<float>(sg);
+  S(SC_SUMSQ_N) = static_cast<float>(sn);
   const double cnt = static_cast<double>(m) * static_cast<double>(n);
   const float gs = pow2_rms_scale(S(SC_SUMSQ_G), cnt);
   const float ns = pow2_rms_scale(S(SC_SUMSQ_N), cnt);
@@ -168,10 +178,10 @@ __global__ void k_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, int s
 }
 
 // ------------------------------------------------------------------ pack
-// One block per 64 x 64 tile of one matrix: each thread takes 16 consecutive
-// columns of one row (16-byte loads and stores when n is a multiple of 8),
-// writes M_t, Ghat and Nhat row-major, and Ghat^T goes out through the
-// shared-memory tile, again as 16 consecutive elements per thread.
+// One block per 64 x 64 tile of one matrix: 8 threads cover a 64-column row,
+// 8 consecutive columns each (16-byte loads and stores when n is a multiple
+// of 8); M_t, Ghat and Nhat go out row-major, and Ghat^T through the
+// shared-memory tile, again 8 consecutive entries per thread.
 constexpr int kPT = 64;
 
 template <typename GT>
@@ -272,14 +282,18 @@ __global__ void __launch_bounds__(256) k_pack(const GT* __restrict__ G, float* _
 __global__ void k_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld, int mode,
                               const uint32_t* status, const float* part_a, int64_t part_a_ld, int64_t npart_a,
                               const float* part_b, int64_t part_b_ld, int64_t npart_b) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  // one warp per matrix
+  const int b = blockIdx.x * kCoeffWarps + (threadIdx.x >> 5);
   if (b >= batch) return;
   // a failed stage leaves the previous roots (and their scales) in force
   if (*reinterpret_cast<const volatile uint32_t*>(status) != 0u) return;
-  auto S = [&](int slot) -> float& { return scal[static_cast<int64_t>(slot) * scal_ld + b]; };
   // ||S||_F^2 of both factors from their fixed partial slots
-  if (part_a) S(SC_SUMSQ_SA) = static_cast<float>(sum_parts(part_a + b * part_a_ld, npart_a));
-  if (part_b) S(SC_SUMSQ_SB) = static_cast<float>(sum_parts(part_b + b * part_b_ld, npart_b));
+  const double sa = part_a ? warp_sum_parts(part_a + b * part_a_ld, npart_a) : 0.0;
+  const double sb = part_b ? warp_sum_parts(part_b + b * part_b_ld, npart_b) : 0.0;
+  if ((threadIdx.x & 31) != 0) return;
+  auto S = [&](int slot) -> float& { return scal[static_cast<int64_t>(slot) * scal_ld + b]; };
+  if (part_a) S(SC_SUMSQ_SA) = static_cast<float>(sa);
+  if (part_b) S(SC_SUMSQ_SB) = static_cast<float>(sb);
   const double margin = 1.0 + ldexp(1.0, -8);
   const int h = kHeadroom;
   for (int f = 0; f < 2 && (mode & kPostRoots); ++f) {
@@ -664,7 +678,8 @@ cudaError_t launch_momentum_stats(const void* G, int g_bf16, const float* M, int
 
 cudaError_t launch_coeffs_pre(int batch, int64_t m, int64_t n, float beta2, int shampoo, float* scal,
                               int scal_ld, const float* part, int64_t part_ld, cudaStream_t st) {
-  k_coeffs_pre<<<(batch + 127) / 128, 128, 0, st>>>(batch, m, n, beta2, shampoo, scal, scal_ld, part, part_ld,
+  k_coeffs_pre<<<(batch + kCoeffWarps - 1) / kCoeffWarps, 32 * kCoeffWarps, 0, st>>>(batch, m, n, beta2, shampoo,
+                                                                                     scal, scal_ld, part, part_ld,
                                                     momentum_parts(m * n));
   return cudaGetLastError();
 }
@@ -685,7 +700,8 @@ cudaError_t launch_pack(const void* G, int g_bf16, float* M, __half* Gh, __half*
 cudaError_t launch_coeffs_post(int batch, float ridge, int zK, int zK1, float* scal, int scal_ld, int mode,
                                const uint32_t* status, const float* part_a, int64_t part_a_ld, int64_t npart_a,
                                const float* part_b, int64_t part_b_ld, int64_t npart_b, cudaStream_t st) {
-  k_coeffs_post<<<(batch + 127) / 128, 128, 0, st>>>(batch, ridge, zK, zK1, scal, scal_ld, mode, status, part_a,
+  k_coeffs_post<<<(batch + kCoeffWarps - 1) / kCoeffWarps, 32 * kCoeffWarps, 0, st>>>(batch, ridge, zK, zK1, scal,
+                                                                                      scal_ld, mode, status, part_a,
                                                      part_a_ld, npart_a, part_b, part_b_ld, npart_b);
   return cudaGetLastError();
 }
