@@ -193,7 +193,11 @@ okls_status okls_reset_state(okls_handle h, void *stream);
  * status word and reported by okls_query_status; once the word is non-zero
  * the remaining stages of the step skip their writes, and the W update is
  * skipped whenever an earlier stage flagged (a flag raised by the update
- * itself still lets that step's other tiles land).
+ * itself still lets that step's other tiles land).  Factors with d <= 128
+ * run their whole Newton-Schulz chain in one fused launch, one CTA per
+ * matrix: there a matrix whose chain overflowed keeps its previous root,
+ * while the other matrices of that launch commit their new roots; a root
+ * and its scale are always committed together.
  */
 okls_status okls_step(okls_handle h, void *W_dev, const void *G_dev, float lr,
                       void *stream);

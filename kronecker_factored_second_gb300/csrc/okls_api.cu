@@ -541,14 +541,110 @@ okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, f
                         int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
                         const TraceOut* tr, bool root_only);
 
+// Factors with d <= 128 run the whole chain in one fused on-chip kernel
+// (plain binary16 mode); OKLS_NS_SMALL=0 sends them through the general path.
+constexpr int kSmallMaxD = 128;
+bool small_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("OKLS_NS_SMALL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+okls_status run_ns_small(Factor* const* fs, int nf, const Sched& sc, float ridge, float* scal, int scal_ld,
+                         uint32_t* status, cudaStream_t st, const TraceOut* tr, bool root_only) {
+  SmallNsArgs A;
+  memset(&A, 0, sizeof(A));
+  A.nf = nf;
+  double flops = 0.0;
+  for (int q = 0; q < nf; ++q) {
+    const Factor& f = *fs[q];
+    SmallNsFactor& g = A.f[q];
+    g.S = f.S;
+    g.upper_only = f.S_upper_only ? 1 : 0;
+    g.d = f.d;
+    g.count = f.batch;
+    g.P32 = f.P32;
+    g.Ph = f.Ph[0].p;
+    g.ph_ld = f.Ph[0].ld;
+    g.ph_mat = f.Ph[0].mat();
+    g.root32 = f.root32;
+    g.slot_sumsq = f.slot_sumsq;
+    g.slot_cprime = f.slot_cprime;
+    g.slot_pscale = f.slot_pscale;
+    g.slot_rscale = f.slot_rscale;
+    g.slot_pi = f.slot_pi;
+    // algorithmic work of the chain: 27 (or 28 with the root) d^3 products
+    flops += 2.0 * f.d * static_cast<double>(f.d) * f.d * f.batch * (3.0 * sc.iters - 3.0 + (f.root32 ? 1.0 : 0.0));
+  }
+  A.scal = scal;
+  A.scal_ld = scal_ld;
+  A.ridge = ridge;
+  A.iters = sc.iters;
+  for (int k = 0; k < sc.iters; ++k) {
+    A.a[k] = static_cast<float>(sc.a[k]);
+    A.b[k] = static_cast<float>(sc.b[k]);
+  }
+  for (int k = 0; k <= sc.iters; ++k) A.z[k] = sc.z[k];
+  A.want_p = root_only ? 0 : 1;
+  A.trace = (tr && tr->base) ? tr->base : nullptr;
+  A.trace_count = tr ? tr->count : 0;
+  A.status = status;
+  Prof* pf = g_prof;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  if (pf && pf->timing) {
+    ea = pf->next_event();
+    eb = pf->next_event();
+    if (ea) OKLS_CK(cudaEventRecord(ea, st));
+  }
+  OKLS_CK(launch_ns_small(A, st));
+  if (pf) {
+    if (ea && eb) {
+      OKLS_CK(cudaEventRecord(eb, st));
+      pf->recs.push_back({ea, eb, flops, true, false});
+    }
+    pf->kernels += 1;
+    pf->gemm_launches += 1;
+    pf->gemm_flops += flops;
+    pf->ns_launches += 1;
+    pf->ns_flops += flops;
+  }
+  return OKLS_OK;
+}
+
 okls_status run_ns(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
                    int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
                    const TraceOut* tr, bool root_only = false) {
   for (int q = 0; q < nf && root_only; ++q)
     if (!fs[q]->root32) return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: square-root output");
-  g_in_ns = true;
-  okls_status s = run_ns_body(fs, nf, sc, split, ridge, scal, scal_ld, maps, status, sms, st, tr, root_only);
-  g_in_ns = false;
+  if (sc.iters > kSmallMaxIters) return fail(OKLS_ERR_UNSUPPORTED, "more than %d Newton-Schulz steps", kSmallMaxIters);
+  // the small factors go to the fused kernel, the rest to the GEMM chain;
+  // a trace is taken from factor 0 only, so a traced run keeps factor 0 on
+  // one path
+  Factor* small[2];
+  Factor* big[2];
+  int ns = 0, nb = 0;
+  for (int q = 0; q < nf; ++q) {
+    if (split == 0 && small_enabled() && fs[q]->d <= kSmallMaxD)
+      small[ns++] = fs[q];
+    else
+      big[nb++] = fs[q];
+  }
+  okls_status s = OKLS_OK;
+  if (ns > 0) {
+    const bool tr_small = tr && tr->base && small[0] == fs[0];
+    if ((s = run_ns_small(small, ns, sc, ridge, scal, scal_ld, status, st, tr_small ? tr : nullptr, root_only)) !=
+        OKLS_OK)
+      return s;
+  }
+  if (nb > 0) {
+    const bool tr_big = tr && tr->base && big[0] == fs[0];
+    g_in_ns = true;
+    s = run_ns_body(big, nb, sc, split, ridge, scal, scal_ld, maps, status, sms, st, tr_big ? tr : nullptr,
+                    root_only);
+    g_in_ns = false;
+  }
   return s;
 }
 

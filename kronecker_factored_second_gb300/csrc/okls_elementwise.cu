@@ -21,6 +21,7 @@
 
 #include "okls_internal.h"
 #include "okls_kernels.h"
+#include "okls_norm.cuh"
 
 namespace okls {
 
@@ -337,35 +338,9 @@ __device__ __forceinline__ void upper_pair(int q, int nt, int& tr, int& tc) {
   tc = nt - 1 - (u - k * (k + 1) / 2);
 }
 
-struct NormOut {
-  __half y, t, z, yl, tl, zl;
-  bool bad;
-};
-
 __device__ __forceinline__ NormOut norm_value(const NormaliseArgs& A, float s, bool diag, float inv, float rc,
                                              float a0h, float zsc) {
-  NormOut o;
-  const float y = (s + (diag ? rc : 0.0f)) * inv;
-  o.y = __float2half_rn(y);
-  float yv = __half2float(o.y);
-  o.yl = __float2half_rn(0.0f);
-  if (A.split_y) {
-    o.yl = __float2half_rn(y - yv);
-    yv += __half2float(o.yl);
-  }
-  const float t = fmaf(A.b0, yv, diag ? a0h : 0.0f);
-  o.t = __float2half_rn(t);
-  float tv = __half2float(o.t);
-  o.tl = __float2half_rn(0.0f);
-  if (A.split_t) {
-    o.tl = __float2half_rn(t - tv);
-    tv += __half2float(o.tl);
-  }
-  const float z = tv * zsc;
-  o.z = __float2half_rn(z);
-  o.zl = A.split_z ? __float2half_rn(z - __half2float(o.z)) : __float2half_rn(0.0f);
-  o.bad = !isfinite(y);
-  return o;
+  return norm_value_core(s, diag, inv, rc, a0h, A.b0, zsc, A.split_y != 0, A.split_t != 0, A.split_z != 0);
 }
 
 // Write the outputs of 8 consecutive columns [j0, j0+8) of row i (binary16

@@ -29,6 +29,35 @@ struct NormaliseArgs {
   uint32_t* status;
 };
 
+// Fused Newton-Schulz chain of factors with d <= 128 (okls_ns_small.cu).
+struct SmallNsFactor {
+  float* S;             // count x d x d fp32 factor (its lower triangle is written when upper_only)
+  int upper_only;       // 1: only S's upper triangle is current (factor-product output)
+  int d, count;
+  float* P32;           // count x d x d fp32 output P (want_p)
+  __half* Ph;           // binary16 copy of P, row pitch ph_ld, matrix stride ph_mat (want_p)
+  int64_t ph_ld, ph_mat;
+  float* root32;        // optional count x d x d fp32 square root
+  int slot_sumsq, slot_cprime, slot_pscale, slot_rscale;
+  int slot_pi;          // written with P^ (P = pi P^): a matrix's binary16 root and its scale change together
+};
+constexpr int kSmallMaxIters = 32;
+struct SmallNsArgs {
+  SmallNsFactor f[2];
+  int nf;
+  float* scal;          // per-matrix scalar table [slot][scal_ld]
+  int scal_ld;
+  float ridge;
+  int iters;
+  float a[kSmallMaxIters], b[kSmallMaxIters];
+  int z[kSmallMaxIters + 1];
+  int want_p;           // 0: the last product forms only the square roots
+  uint16_t* trace;      // optional, factor 0 only: (3 iters + 1) x trace_count x d x d binary16
+  int64_t trace_count;
+  uint32_t* status;
+};
+cudaError_t launch_ns_small(const SmallNsArgs& A, cudaStream_t st);
+
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_pair(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 
