@@ -13,6 +13,7 @@ roots.
 from __future__ import annotations
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -396,3 +397,45 @@ def test_bitwise_reproducible():
     P1 = okls.inv_root(S)["P"]
     P2 = okls.inv_root(S)["P"]
     assert torch.equal(P1, P2)
+
+
+_GENERAL_PATH_SCRIPT = r"""
+import os, sys
+import numpy as np
+import torch
+sys.path.insert(0, os.environ["OKLS_ROOT"])
+sys.path.insert(0, os.path.join(os.environ["OKLS_ROOT"], "tests"))
+from gpu_helpers import spd
+from kronecker_factored_second_gb300 import okls
+out = {}
+for d in (48, 100, 128):
+    S = np.stack([spd(d, 300.0, 7 * d + i) for i in range(3)])
+    r = okls.inv_root(torch.tensor(S, dtype=torch.float32, device="cuda"), ridge=1e-3, want_root=True)
+    out[f"P{d}"] = r["P"].cpu().numpy()
+    out[f"R{d}"] = r["root"].cpu().numpy()
+np.savez(sys.argv[1], **out)
+"""
+
+
+def test_fused_small_chain_matches_the_gemm_chain(tmp_path):
+    """Factors with d <= 128 take the fused on-chip chain; the same inputs
+    through the general GEMM chain (OKLS_NS_SMALL=0, a separate process)
+    give bit-identical P and square roots: both round every iterate to
+    binary16 the same way and accumulate the same K16 products in the same
+    order."""
+    import subprocess
+    import sys
+    okls = _okls()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    path = tmp_path / "general.npz"
+    env = dict(os.environ, OKLS_NS_SMALL="0", OKLS_ROOT=root)
+    subprocess.run([sys.executable, "-c", _GENERAL_PATH_SCRIPT, str(path)], env=env, check=True, timeout=600)
+    ref = np.load(path)
+    for d in (48, 100, 128):
+        S = np.stack([spd(d, 300.0, 7 * d + i) for i in range(3)])
+        r = okls.inv_root(torch.tensor(S, dtype=torch.float32, device="cuda"), ridge=1e-3, want_root=True)
+        eP = O.rel_fro(r["P"].cpu().numpy(), ref[f"P{d}"])
+        eR = O.rel_fro(r["root"].cpu().numpy(), ref[f"R{d}"])
+        print(f"d={d}: fused vs GEMM chain P {eP:.2e} root {eR:.2e}")
+        assert np.array_equal(r["P"].cpu().numpy(), ref[f"P{d}"]), (d, eP)
+        assert np.array_equal(r["root"].cpu().numpy(), ref[f"R{d}"]), (d, eR)
