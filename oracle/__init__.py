@@ -1,5 +1,5 @@
-"""Float64 CPU oracle for the Online KL Shampoo (OKLS) preconditioner step
-and the classic Shampoo step it refines.
+"""Float64 CPU oracle for the Online KL Shampoo (OKLS) preconditioner step,
+the classic Shampoo step it refines, and SOAP (Adam in the factors' eigenbasis).
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this package:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
@@ -26,6 +26,10 @@ Parity status per function (the pins live in ``tests/test_oracle_pins.py``):
 * ``quarter_root_exact``, ``quarter_root_chain``  pinned (chained exact chains
   equal the eigendecomposition quarter root, P^4 S = I; the replay's square
   root equals the float64 iteration's).
+* ``soap_step``, ``eigenvectors_aligned``   pinned (no refresh: textbook Adam by
+  entry loops; fixed bases: rotated Adam; eigenvector order and signs;
+  refresh schedule).  The readings of the bias correction, the initial bases
+  and the eigenvector signs follow the pages' listings; no printed values.
 * ``variance_correction``                  pinned by Monte Carlo against its
   definition (variance of the Nesterov combination for iid unit gradients);
   the *choice* of this reading is not printed on the pages.

@@ -45,6 +45,7 @@ __all__ = [
     "ns_replay", "ns_replay_iteration", "factor_ema", "init_state",
     "okls_step", "okls_run", "rel_fro", "NS_HEADROOM", "NS_MARGIN",
     "quarter_root_exact", "quarter_root_chain", "shampoo_init", "shampoo_step",
+    "SoapState", "soap_init", "soap_step", "eigenvectors_aligned",
 ]
 
 # Power-of-two headroom of the stored binary16 operands (reading r9): Y and T
@@ -523,6 +524,77 @@ def shampoo_step(state: OklsState, W: np.ndarray, G: np.ndarray, lr: float,
     decay = adamc_decay(lr, hp.peak, hp.weight_decay)
     W_new = W - decay * W - lr * U
     return OklsState(M=state.M, Sa=L, Sb=R, Pa=Pa, Pb=Pb, t=t), W_new, U
+
+
+# ------------------------------------------------------- SOAP (eigenbasis Adam) ---
+#
+# Page "Clean: Second-order LLM Training at Linear Memory Cost via Nystrom
+# Sketching", Appendix C, Algorithm 4 (SOAP), with the KPOP page's section on
+# running Adam in the Kronecker-factored eigenbasis for the Adam details.
+# Per step: rotate G and the momentum M (kept in the original space) into the
+# eigenbases Q_L, Q_R of the factors L, R; run Adam there with the second
+# moment V kept in the rotated space; rotate the normalised step back; then
+# update L, R, and every f steps refresh Q_L, Q_R.  Readings:
+#   p1  "run Adam on G'": standard Adam, both moments bias-corrected,
+#       N' = (M' / (1 - b1^t)) / (sqrt(V / (1 - b2^t)) + eps) (the KPOP page's
+#       formula; the Clean listing prints the correction on V).
+#   p2  Q_L = I, Q_R = I before the first refresh (L = R = 0).
+#   p3  Eigenvectors(L, Q_L): the eigenvectors of L with eigenvalues in
+#       decreasing order, each column's sign chosen so it has a non-negative
+#       inner product with the same column of the previous basis (the sign
+#       alignment of the Clean page's Algorithm 3).
+#   p4  the refresh happens at the end of steps t with t % f == 0; V is kept
+#       as it is across a refresh.
+#   p5  W <- W - decay - lr N, decay the same decoupled term as OKLS (zero
+#       with weight_decay = 0, the listing's plain step).
+
+@dataclass
+class SoapState:
+    M: np.ndarray    # m x n, original space
+    V: np.ndarray    # m x n, eigenbasis
+    L: np.ndarray    # m x m
+    R: np.ndarray    # n x n
+    QL: np.ndarray   # m x m
+    QR: np.ndarray   # n x n
+    t: int = 0
+
+
+def soap_init(m: int, n: int) -> SoapState:
+    return SoapState(M=np.zeros((m, n)), V=np.zeros((m, n)), L=np.zeros((m, m)), R=np.zeros((n, n)),
+                     QL=np.eye(m), QR=np.eye(n), t=0)
+
+
+def eigenvectors_aligned(S: np.ndarray, Q_prev: np.ndarray) -> np.ndarray:
+    """Reading p3: eigenvectors of the symmetric S, eigenvalues decreasing,
+    column signs aligned with the previous basis."""
+    w, Q = np.linalg.eigh(_sym(S))
+    Q = Q[:, ::-1]
+    s = np.sign(np.sum(Q * Q_prev, axis=0))
+    s[s == 0] = 1.0
+    return Q * s
+
+
+def soap_step(state: SoapState, W: np.ndarray, G: np.ndarray, lr: float, beta1: float, beta2: float,
+              eps: float, f: int, weight_decay: float = 0.0, lr_peak: float | None = None):
+    """One SOAP step for one matrix in float64.  Returns (new_state, W_new, N)."""
+    G = np.asarray(G, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    t = state.t + 1
+    QL, QR = state.QL, state.QR
+    Gr = QL.T @ G @ QR
+    M = beta1 * state.M + (1.0 - beta1) * G
+    Mr = QL.T @ M @ QR
+    V = beta2 * state.V + (1.0 - beta2) * Gr * Gr
+    Nr = (Mr / (1.0 - beta1 ** t)) / (np.sqrt(V / (1.0 - beta2 ** t)) + eps)
+    N = QL @ Nr @ QR.T
+    decay = adamc_decay(lr, lr if lr_peak is None else lr_peak, weight_decay)
+    W_new = W - decay * W - lr * N
+    L = beta2 * state.L + (1.0 - beta2) * (G @ G.T)
+    R = beta2 * state.R + (1.0 - beta2) * (G.T @ G)
+    if t % max(1, f) == 0:
+        QL = eigenvectors_aligned(L, QL)
+        QR = eigenvectors_aligned(R, QR)
+    return SoapState(M=M, V=V, L=L, R=R, QL=QL, QR=QR, t=t), W_new, N
 
 
 def rel_fro(A: np.ndarray, B: np.ndarray) -> float:

@@ -492,3 +492,90 @@ def test_shampoo_stale_roots():
             assert np.array_equal(st.Pa, prev.Pa) and np.array_equal(st.Pb, prev.Pb)
             assert O.rel_fro(U, prev.Pa @ G @ prev.Pb) < 1e-14
         prev = st
+
+
+# ------------------------------------------------------------------- SOAP
+
+def _adam_loops(Gs, lr, b1, b2, eps):
+    """Textbook Adam (both moments bias-corrected), entry by entry."""
+    m, n = Gs[0].shape
+    M = [[0.0] * n for _ in range(m)]
+    V = [[0.0] * n for _ in range(m)]
+    W = [[0.0] * n for _ in range(m)]
+    for t, G in enumerate(Gs, start=1):
+        for i in range(m):
+            for j in range(n):
+                g = float(G[i, j])
+                M[i][j] = b1 * M[i][j] + (1 - b1) * g
+                V[i][j] = b2 * V[i][j] + (1 - b2) * g * g
+                mh = M[i][j] / (1 - b1 ** t)
+                vh = V[i][j] / (1 - b2 ** t)
+                W[i][j] -= lr * mh / (math.sqrt(vh) + eps)
+    return np.array(W)
+
+
+def test_soap_without_refresh_is_adam():
+    """Before any refresh the bases are the identity (reading p2), so SOAP is
+    Adam with both moments bias-corrected (reading p1), entry by entry."""
+    rng = np.random.default_rng(31)
+    Gs = [rng.standard_normal((5, 3)) for _ in range(6)]
+    st = O.soap_init(5, 3)
+    W = np.zeros((5, 3))
+    for G in Gs:
+        st, W, _N = O.soap_step(st, W, G, 0.05, 0.9, 0.99, 1e-8, f=1000)
+    assert np.allclose(W, _adam_loops(Gs, 0.05, 0.9, 0.99, 1e-8), atol=1e-13, rtol=0)
+
+
+def _orth(d, seed):
+    q, _ = np.linalg.qr(np.random.default_rng(seed).standard_normal((d, d)))
+    return q
+
+
+def test_soap_in_a_fixed_basis_is_rotated_adam():
+    """With bases A, B held fixed, the step is Adam on A^T G B rotated back
+    by A (.) B^T: a transposed rotation or a basis on the wrong side fails."""
+    rng = np.random.default_rng(32)
+    m, n = 5, 4
+    A, B = _orth(m, 1), _orth(n, 2)
+    Gs = [rng.standard_normal((m, n)) for _ in range(4)]
+    st = O.soap_init(m, n)
+    st.QL, st.QR = A, B
+    W = np.zeros((m, n))
+    for G in Gs:
+        st, W, _N = O.soap_step(st, W, G, 0.03, 0.8, 0.95, 1e-6, f=1000)
+    W_rot = _adam_loops([A.T @ G @ B for G in Gs], 0.03, 0.8, 0.95, 1e-6)
+    assert O.rel_fro(W, A @ W_rot @ B.T) < 1e-12
+
+
+def test_eigenvectors_are_ordered_and_sign_aligned():
+    """Reading p3: decreasing eigenvalues, each column signed to agree with
+    the previous basis."""
+    d = 6
+    A = _orth(d, 3)
+    lam = np.array([9.0, 7.0, 4.0, 2.5, 1.0, 0.25])
+    S = (A * lam) @ A.T
+    Q = O.eigenvectors_aligned(S, A)
+    assert np.allclose(Q, A, atol=1e-12)
+    flips = np.array([1, -1, 1, -1, -1, 1.0])
+    assert np.allclose(O.eigenvectors_aligned(S, A * flips), A * flips, atol=1e-12)
+    assert np.allclose(np.diag(Q.T @ S @ Q), lam, atol=1e-12)
+
+
+def test_soap_refresh_schedule():
+    """f = 3: the bases change only at the end of steps 3 and 6, to the
+    eigenvectors of the factors of that step; L, R are EMAs of G G^T, G^T G."""
+    rng = np.random.default_rng(33)
+    st = O.soap_init(4, 3)
+    W = np.zeros((4, 3))
+    L = np.zeros((4, 4))
+    for t in range(1, 7):
+        G = rng.standard_normal((4, 3))
+        prev = st
+        st, W, _N = O.soap_step(st, W, G, 0.01, 0.9, 0.95, 1e-8, f=3)
+        L = 0.95 * L + 0.05 * G @ G.T
+        assert np.allclose(st.L, L, atol=1e-14)
+        if t % 3 == 0:
+            QL = st.QL
+            assert np.allclose(QL.T @ L @ QL, np.diag(np.diag(QL.T @ L @ QL)), atol=1e-12)
+        else:
+            assert np.array_equal(st.QL, prev.QL) and np.array_equal(st.QR, prev.QR)
