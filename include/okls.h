@@ -64,18 +64,23 @@ typedef enum okls_dtype { OKLS_F32 = 0, OKLS_BF16 = 1 } okls_dtype;
 /* Preconditioner step computed by okls_step. */
 typedef enum okls_method {
   OKLS_METHOD_OKLS = 0,    /* Online KL Shampoo (the default)              */
-  OKLS_METHOD_SHAMPOO = 1  /* classic Shampoo: summed factors, -1/4 roots */
+  OKLS_METHOD_SHAMPOO = 1, /* classic Shampoo: summed factors, -1/4 roots */
+  OKLS_METHOD_SOAP = 2     /* SOAP: Adam in the factors' eigenbasis       */
 } okls_method;
 
 /* Which piece of state okls_get_state / okls_set_state move.  In Shampoo
  * mode S_a / S_b hold the sums L / R and P_a / P_b their -1/4 roots; M is
- * unused (left at zero). */
+ * unused (left at zero).  In SOAP mode S_a / S_b hold the factor EMAs L / R,
+ * P_a / P_b their eigenbases Q_L / Q_R (eigenvectors in columns), M the
+ * momentum (original space) and V the second moment (eigenbasis). */
 typedef enum okls_state_part {
   OKLS_STATE_M = 0,   /* momentum,                 batch x m x n, fp32 */
   OKLS_STATE_SA = 1,  /* left factor S_a,          batch x m x m, fp32 */
   OKLS_STATE_SB = 2,  /* right factor S_b,         batch x n x n, fp32 */
   OKLS_STATE_PA = 3,  /* left root P_a = S_a^-1/2, batch x m x m, fp32 */
-  OKLS_STATE_PB = 4   /* right root P_b,           batch x n x n, fp32 */
+  OKLS_STATE_PB = 4,  /* right root P_b,           batch x n x n, fp32 */
+  OKLS_STATE_V = 5    /* SOAP only: second moment in the eigenbasis,
+                         batch x m x n, fp32 */
 } okls_state_part;
 
 /* Bits of the device status word (okls_query_status). */
@@ -115,7 +120,19 @@ typedef enum okls_state_part {
  *                   of the last refresh (the practice of recomputing Shampoo
  *                   roots every 20-100 steps; k = 1 is the README's
  *                   zero-staleness method).
- *   method          okls_method.  OKLS_METHOD_SHAMPOO ignores beta1, beta2,
+ *   method          okls_method.  OKLS_METHOD_SOAP (Clean page, Appendix C,
+ *                   Algorithm 4): per step G' = Q_L^T G Q_R, M <- b1 M +
+ *                   (1-b1) G, M' = Q_L^T M Q_R, V <- b2 V + (1-b2) G'^2,
+ *                   N = Q_L [(M'/(1-b1^t)) / (sqrt(V/(1-b2^t)) + eps)] Q_R^T,
+ *                   W <- W - lr wd (lr/lr_peak) W - lr N, L <- b2 L + (1-b2) G G^T,
+ *                   R <- b2 R + (1-b2) G^T G, and after steps t with
+ *                   t % root_every == 0 Q_L, Q_R <- eigenvectors of L, R
+ *                   (decreasing eigenvalues, signs aligned with the previous
+ *                   basis); eps is Adam's.  Q = I before the first refresh.
+ *                   This build runs SOAP for m, n <= 128 only (one CTA per
+ *                   matrix, fp32, Jacobi eigensolver); larger shapes return
+ *                   OKLS_ERR_UNSUPPORTED.
+ *                   OKLS_METHOD_SHAMPOO ignores beta1, beta2,
  *                   variance_correction and eps_every_update (the sums add
  *                   G G^T and G^T G with weight 1, eps enters only at reset,
  *                   no momentum, no shape multiplier) and applies `ridge` to

@@ -28,8 +28,9 @@ OKLS_BF16 = 1
 
 METHOD_OKLS = 0
 METHOD_SHAMPOO = 1
+METHOD_SOAP = 2
 
-STATE_M, STATE_SA, STATE_SB, STATE_PA, STATE_PB = range(5)
+STATE_M, STATE_SA, STATE_SB, STATE_PA, STATE_PB, STATE_V = range(6)
 
 DEV_NONFINITE_INPUT = 0x1
 DEV_NONFINITE_ITER = 0x2

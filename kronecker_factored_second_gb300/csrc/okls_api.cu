@@ -792,6 +792,7 @@ struct okls_handle_s {
   Factor fa, fb;
   Buf Gh, GhT, Nh, Xb, XaT;  // Ghat (m x n), Ghat^T (n x m), Nhat (m x n), X_b / Q (m x n), X_a^T (n x m)
   float *sq_a = nullptr, *sq_b = nullptr;  // Shampoo: fp32 square roots L^1/2, R^1/2 between the chains
+  float* V = nullptr;                      // SOAP: second moment in the eigenbasis
   float* scal = nullptr;
   uint32_t* status = nullptr;
   CUtensorMap* maps = nullptr;
@@ -818,11 +819,30 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
   float* Sb = static_cast<float*>(sp.take(static_cast<size_t>(B * n * n * 4)));
   float* Pa = static_cast<float*>(sp.take(static_cast<size_t>(B * m * m * 4)));
   float* Pb = static_cast<float*>(sp.take(static_cast<size_t>(B * n * n * 4)));
+  const bool soap = c.method == OKLS_METHOD_SOAP;
+  float* V = soap ? static_cast<float*>(sp.take(static_cast<size_t>(B * m * n * 4))) : nullptr;
   Planner wp;
   wp.base = ws;
   CUtensorMap* maps = static_cast<CUtensorMap*>(wp.take(kMapTableBytes, 128));
   float* scal = static_cast<float*>(wp.take(static_cast<size_t>(SC_COUNT * B * 4)));
   uint32_t* status = static_cast<uint32_t*>(wp.take(256));
+  if (soap) {
+    // SOAP keeps everything in the state; the workspace holds the status word
+    out->state_bytes = sp.off;
+    out->ws_bytes = wp.off;
+    if (h) {
+      h->M = M;
+      h->Sa = Sa;
+      h->Sb = Sb;
+      h->Pa = Pa;
+      h->Pb = Pb;
+      h->V = V;
+      h->scal = scal;
+      h->status = status;
+      h->maps = maps;
+    }
+    return OKLS_OK;
+  }
   const int64_t pg_ld = kMaxStatParts, pa_ld = factor_parts(m), pb_ld = factor_parts(n);
   float* part_g = static_cast<float*>(wp.take(static_cast<size_t>(2 * B * pg_ld * 4)));
   float* part_a = static_cast<float*>(wp.take(static_cast<size_t>(B * pa_ld * 4)));
@@ -918,14 +938,70 @@ okls_status validate(const okls_config* c) {
   if (!(c->ns_lo > 0.0f && c->ns_lo < 1.0f)) return fail(OKLS_ERR_INVALID_ARG, "ns_lo must be in (0, 1)");
   if (!finite_nonneg(c->ridge)) return fail(OKLS_ERR_INVALID_ARG, "ridge must be finite and >= 0");
   if (c->root_every < 0) return fail(OKLS_ERR_INVALID_ARG, "root_every must be >= 0 (0 means 1)");
-  if (c->method != OKLS_METHOD_OKLS && c->method != OKLS_METHOD_SHAMPOO)
+  if (c->method != OKLS_METHOD_OKLS && c->method != OKLS_METHOD_SHAMPOO && c->method != OKLS_METHOD_SOAP)
     return fail(OKLS_ERR_INVALID_ARG, "method %d", c->method);
+  if (c->method == OKLS_METHOD_SOAP && (c->m > 128 || c->n > 128))
+    return fail(OKLS_ERR_UNSUPPORTED,
+                "SOAP runs for m, n <= 128 in this build (one-CTA eigensolver); %lld x %lld needs the blocked one",
+                static_cast<long long>(c->m), static_cast<long long>(c->n));
   for (int i = 0; i < 6; ++i)
     if (c->reserved[i] != 0) return fail(OKLS_ERR_INVALID_ARG, "reserved fields must be zero");
   return OKLS_OK;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// SOAP (Clean page, Appendix C, Algorithm 4): the step, then the eigenbasis
+// refresh after steps t with t % root_every == 0.
+okls_status soap_step(okls_handle_s* h, void* W, const void* G, float lr, cudaStream_t st) {
+  const okls_config& c = h->cfg;
+  const int64_t t1 = h->t + 1;
+  ProfScope scope(&h->prof);
+  SoapArgs A;
+  memset(&A, 0, sizeof(A));
+  A.batch = static_cast<int>(c.batch);
+  A.m = static_cast<int>(c.m);
+  A.n = static_cast<int>(c.n);
+  A.G = G;
+  A.W = W;
+  A.g_bf16 = c.grad_dtype == OKLS_BF16;
+  A.w_bf16 = c.param_dtype == OKLS_BF16;
+  A.M = h->M;
+  A.V = h->V;
+  A.L = h->Sa;
+  A.R = h->Sb;
+  A.QL = h->Pa;
+  A.QR = h->Pb;
+  A.beta1 = c.beta1;
+  A.beta2 = c.beta2;
+  A.eps = c.eps;
+  A.lr = lr;
+  A.decay = static_cast<float>(1.0 - static_cast<double>(lr) * c.weight_decay * (static_cast<double>(lr) / c.lr_peak));
+  A.bc1 = static_cast<float>(1.0 / (1.0 - std::pow(static_cast<double>(c.beta1), static_cast<double>(t1))));
+  A.bc2 = static_cast<float>(1.0 / (1.0 - std::pow(static_cast<double>(c.beta2), static_cast<double>(t1))));
+  A.status = h->status;
+  OKLS_CK(launch_soap_step(A, st));
+  note_kernels(1);
+  const int64_t every = c.root_every > 1 ? c.root_every : 1;
+  if (t1 % every == 0) {
+    SoapRefreshArgs R;
+    memset(&R, 0, sizeof(R));
+    R.count = static_cast<int>(c.batch);
+    R.S0 = h->Sa;
+    R.S1 = h->Sb;
+    R.Q0 = h->Pa;
+    R.Q1 = h->Pb;
+    R.d0 = static_cast<int>(c.m);
+    R.d1 = static_cast<int>(c.n);
+    R.max_sweeps = 30;
+    R.tol2 = 1e-14f;
+    R.status = h->status;
+    OKLS_CK(launch_soap_refresh(R, st));
+    note_kernels(1);
+  }
+  h->t = t1;
+  return OKLS_OK;
+}
 
 }  // namespace
 
@@ -1003,6 +1079,13 @@ okls_status okls_reset_state(okls_handle h, void* stream) {
   if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const okls_config& c = h->cfg;
+  if (c.method == OKLS_METHOD_SOAP) {
+    OKLS_CK(cudaMemsetAsync(h->status, 0, 4, st));
+    OKLS_CK(launch_soap_reset(h->M, h->V, h->Sa, h->Sb, h->Pa, h->Pb, static_cast<int>(c.batch), static_cast<int>(c.m),
+                              static_cast<int>(c.n), st));
+    h->t = 0;
+    return OKLS_OK;
+  }
   OKLS_CK(cudaMemsetAsync(h->M, 0, static_cast<size_t>(c.batch * c.m * c.n * 4), st));
   OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(SC_COUNT * c.batch * 4), st));
   OKLS_CK(cudaMemsetAsync(h->status, 0, 4, st));
@@ -1025,6 +1108,7 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
   if (!finite_nonneg(lr)) return fail(OKLS_ERR_INVALID_ARG, "lr must be finite and >= 0");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const okls_config& c = h->cfg;
+  if (c.method == OKLS_METHOD_SOAP) return soap_step(h, W, G, lr, st);
   const bool shampoo = c.method == OKLS_METHOD_SHAMPOO;
   const int B = static_cast<int>(c.batch), m = static_cast<int>(c.m), n = static_cast<int>(c.n);
   const int sld = B;
@@ -1235,6 +1319,11 @@ static okls_status part_ptr(okls_handle h, int32_t part, float** p, size_t* byte
     case OKLS_STATE_SB: *p = h->Sb; *bytes = static_cast<size_t>(c.batch * c.n * c.n * 4); break;
     case OKLS_STATE_PA: *p = h->Pa; *bytes = static_cast<size_t>(c.batch * c.m * c.m * 4); break;
     case OKLS_STATE_PB: *p = h->Pb; *bytes = static_cast<size_t>(c.batch * c.n * c.n * 4); break;
+    case OKLS_STATE_V:
+      if (c.method != OKLS_METHOD_SOAP) return fail(OKLS_ERR_INVALID_ARG, "state part V exists in SOAP mode only");
+      *p = h->V;
+      *bytes = static_cast<size_t>(c.batch * c.m * c.n * 4);
+      break;
     default: return fail(OKLS_ERR_INVALID_ARG, "unknown state part %d", part);
   }
   return OKLS_OK;
@@ -1259,6 +1348,7 @@ okls_status okls_set_state(okls_handle h, int32_t part, const void* src, void* s
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   OKLS_CK(cudaMemcpyAsync(p, src, bytes, cudaMemcpyDeviceToDevice, st));
   const okls_config& c = h->cfg;
+  if (c.method == OKLS_METHOD_SOAP) return OKLS_OK;  // the bases have no binary16 copies
   if (part == OKLS_STATE_PA)
     OKLS_CK(launch_requant(h->Pa, static_cast<int>(c.batch), static_cast<int>(c.m), h->fa.Ph[0].p, nullptr,
                            h->fa.Ph[1].p, nullptr, h->fa.Ph[0].ld, h->fa.Ph[0].mat(), h->scal,

@@ -58,6 +58,32 @@ struct SmallNsArgs {
 };
 cudaError_t launch_ns_small(const SmallNsArgs& A, cudaStream_t st);
 
+// SOAP (okls_soap.cu) for m, n <= 128: one CTA per matrix, fp32.
+struct SoapArgs {
+  int batch, m, n;
+  const void* G;        // batch x m x n, fp32 or bf16 (g_bf16)
+  void* W;              // batch x m x n, fp32 or bf16 (w_bf16), updated in place
+  int g_bf16, w_bf16;
+  float *M, *V, *L, *R; // state: momentum, eigenbasis second moment, factors
+  const float *QL, *QR; // eigenbases
+  float beta1, beta2, eps, lr, decay;
+  float bc1, bc2;       // 1/(1-b1^t), 1/(1-b2^t)
+  uint32_t* status;
+};
+struct SoapRefreshArgs {
+  int count;            // matrices per factor side
+  const float *S0, *S1; // L (count x d0 x d0) and R (count x d1 x d1)
+  float *Q0, *Q1;       // their bases: read as the previous ones, overwritten
+  int d0, d1;
+  int max_sweeps;
+  float tol2;           // stop once off-diagonal^2 <= tol2 * diagonal^2
+  uint32_t* status;
+};
+cudaError_t launch_soap_step(const SoapArgs& A, cudaStream_t st);
+cudaError_t launch_soap_refresh(const SoapRefreshArgs& A, cudaStream_t st);
+cudaError_t launch_soap_reset(float* M, float* V, float* L, float* R, float* QL, float* QR, int batch, int m, int n,
+                              cudaStream_t st);
+
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_pair(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 

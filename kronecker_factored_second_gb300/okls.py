@@ -9,6 +9,8 @@
                    2-D or 3-D parameter.
 `Shampoo`          the classic Shampoo step (summed factors, -1/4 roots)
                    over the same kernels (method="shampoo").
+`SOAP`             Adam in the factors' eigenbasis (method="soap"; matrices up
+                   to 128 x 128 in this build).
 
 All arithmetic happens in libokls.so; nothing here computes on the CPU.
 """
@@ -50,7 +52,7 @@ class OklsBatch:
                  eps_every_update: bool = True, root_every: int = 1, method: str = "okls",
                  device=None):
         lib = L.lib()
-        methods = {"okls": L.METHOD_OKLS, "shampoo": L.METHOD_SHAMPOO}
+        methods = {"okls": L.METHOD_OKLS, "shampoo": L.METHOD_SHAMPOO, "soap": L.METHOD_SOAP}
         if method not in methods:
             raise ValueError(f"okls: method must be one of {sorted(methods)}")
         cfg = L.config_default(batch, m, n)
@@ -123,7 +125,7 @@ class OklsBatch:
     def _part_shape(self, part: int):
         B, m, n = self.batch, self.m, self.n
         return {L.STATE_M: (B, m, n), L.STATE_SA: (B, m, m), L.STATE_SB: (B, n, n),
-                L.STATE_PA: (B, m, m), L.STATE_PB: (B, n, n)}[part]
+                L.STATE_PA: (B, m, m), L.STATE_PB: (B, n, n), L.STATE_V: (B, m, n)}[part]
 
     def get_state(self, part: int, stream=None) -> torch.Tensor:
         out = torch.empty(self._part_shape(part), dtype=torch.float32, device=self.device)
@@ -158,14 +160,15 @@ class OklsBatch:
         L.check(L.lib().okls_profile_read(self._h, ctypes.byref(p)))
         return {k: getattr(p, k) for k, _ in L.okls_profile._fields_}
 
+    def _parts(self):
+        parts = [("M", L.STATE_M), ("Sa", L.STATE_SA), ("Sb", L.STATE_SB), ("Pa", L.STATE_PA), ("Pb", L.STATE_PB)]
+        return parts + [("V", L.STATE_V)] if self.method == "soap" else parts
+
     def state_dict(self) -> dict:
-        return {"t": self.t, **{k: self.get_state(p).cpu() for k, p in
-                                [("M", L.STATE_M), ("Sa", L.STATE_SA), ("Sb", L.STATE_SB),
-                                 ("Pa", L.STATE_PA), ("Pb", L.STATE_PB)]}}
+        return {"t": self.t, **{k: self.get_state(p).cpu() for k, p in self._parts()}}
 
     def load_state_dict(self, sd: dict):
-        for k, p in [("M", L.STATE_M), ("Sa", L.STATE_SA), ("Sb", L.STATE_SB),
-                     ("Pa", L.STATE_PA), ("Pb", L.STATE_PB)]:
+        for k, p in self._parts():
             self.set_state(p, sd[k])
         self.t = int(sd["t"])
 
@@ -272,5 +275,41 @@ class Shampoo(torch.optim.Optimizer):
                                            lr=g["lr_peak"], eps=g["eps"], weight_decay=g["weight_decay"],
                                            ns_split_iters=g["ns_split_iters"], ridge=g["ridge"],
                                            root_every=g["root_every"], method="shampoo", device=p.device)
+                st["okls"].step(p.data, p.grad.contiguous(), g["lr"])
+        return loss
+
+
+class SOAP(torch.optim.Optimizer):
+    """SOAP (Clean page, Appendix C, Algorithm 4) over 2-D and 3-D CUDA
+    parameters with both dimensions <= 128: Adam run in the eigenbases of the
+    factor EMAs L, R, refreshed every `precondition_frequency` steps."""
+
+    def __init__(self, params, lr: float = 3e-3, betas=(0.95, 0.95), eps: float = 1e-8,
+                 weight_decay: float = 0.0, precondition_frequency: int = 10):
+        defaults = dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay,
+                        precondition_frequency=precondition_frequency)
+        super().__init__(params, defaults)
+        for g in self.param_groups:
+            g.setdefault("lr_peak", g["lr"])
+
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = closure() if closure is not None else None
+        for g in self.param_groups:
+            for p in g["params"]:
+                if p.grad is None:
+                    continue
+                if p.dim() not in (2, 3):
+                    raise ValueError("SOAP takes 2-D or 3-D matrix parameters only")
+                st = self.state[p]
+                if "okls" not in st:
+                    B = 1 if p.dim() == 2 else p.shape[0]
+                    m, n = p.shape[-2:]
+                    b1, b2 = g["betas"]
+                    st["okls"] = OklsBatch(B, m, n, param_dtype=p.dtype, grad_dtype=p.grad.dtype,
+                                           lr=g["lr_peak"], beta1=b1, beta2=b2, eps=g["eps"],
+                                           weight_decay=g["weight_decay"],
+                                           root_every=g["precondition_frequency"], method="soap",
+                                           device=p.device)
                 st["okls"].step(p.data, p.grad.contiguous(), g["lr"])
         return loss

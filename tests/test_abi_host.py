@@ -114,7 +114,7 @@ def test_method_is_validated_and_sizes_the_workspace(lib):
     square root per factor (all sizes here are multiples of the 256-byte
     alignment, so the difference is exact)."""
     c = L.config_default(2, 96, 40)
-    c.method = 2
+    c.method = 3
     assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_INVALID_ARG
     c.method = L.METHOD_OKLS
     s0, w0 = L.state_bytes(c)
@@ -123,3 +123,15 @@ def test_method_is_validated_and_sizes_the_workspace(lib):
     B, m, n = 2, 96, 40
     assert s1 == s0
     assert w1 - w0 == 4 * B * (m * m + n * n) - 2 * B * (m * n + n * m)
+
+
+def test_soap_shapes_and_state(lib):
+    """SOAP keeps M, L, R, Q_L, Q_R and V in the state and needs no binary16
+    workspace; this build takes m, n <= 128."""
+    c = L.config_default(3, 128, 64)
+    c.method = L.METHOD_SOAP
+    s, w = L.state_bytes(c)
+    assert s >= 4 * 3 * (2 * 128 * 64 + 2 * 128 * 128 + 2 * 64 * 64)
+    assert w < 1 << 20
+    c.m = 129
+    assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_UNSUPPORTED

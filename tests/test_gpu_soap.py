@@ -1,0 +1,153 @@
+"""GPU parity of the SOAP mode (okls_config.method = SOAP, m, n <= 128)
+against the float64 oracle, through the C ABI.
+
+Teacher-forced: every step starts the oracle from the GPU's own state
+(M, V, L, R, Q_L, Q_R).  Bars: M, V, L, R to 1e-5 (fp32 arithmetic), the step
+N to 1e-4 (2e-2 with bf16 parameters, which round the new W); after a refresh
+the bases must be orthogonal and diagonalise L, R (1e-5), carry decreasing
+eigenvalues and agree in sign with the previous bases (orthogonality to
+1e-5 d in Frobenius norm: fp32 rotations), and every eigenvector
+whose eigenvalue is separated from its neighbours by more than 1e-3 of the
+spectrum must match the oracle's to 1e-3.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from kronecker_factored_second_gb300 import _lib as L
+
+pytestmark = pytest.mark.gpu
+
+PARTS = [("M", L.STATE_M), ("L", L.STATE_SA), ("R", L.STATE_SB), ("QL", L.STATE_PA), ("QR", L.STATE_PB),
+         ("V", L.STATE_V)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    L.lib()  # fail loudly when the library is missing
+    torch.cuda.set_device(0)
+
+
+def _batch(B, m, n, **kw):
+    from kronecker_factored_second_gb300.okls import OklsBatch
+    return OklsBatch(B, m, n, method="soap", **kw)
+
+
+def _snap(ob):
+    torch.cuda.synchronize()
+    return {k: ob.get_state(p).double().cpu().numpy() for k, p in PARTS}
+
+
+def _check_basis(Q, S, Q_prev, Q_ref):
+    d = S.shape[0]
+    out = {}
+    # fp32 rotations: orthogonality holds to ~1e-6 per entry, so the
+    # Frobenius norm of Q^T Q - I is held to 1e-5 d
+    out["orth"] = float(np.linalg.norm(Q.T @ Q - np.eye(d))) / d
+    D = Q.T @ S @ Q
+    out["offdiag"] = float(np.linalg.norm(D - np.diag(np.diag(D))) / max(np.linalg.norm(S), 1e-30))
+    lam = np.diag(D)
+    out["order"] = float(max(0.0, np.max(lam[1:] - lam[:-1]) / max(np.abs(lam).max(), 1e-30))) if d > 1 else 0.0
+    out["sign"] = float(max(0.0, -np.min(np.sum(Q * Q_prev, axis=0))))
+    # eigenvectors with a clear gap must match the oracle's
+    w = np.linalg.eigvalsh(0.5 * (S + S.T))[::-1]
+    scale = max(abs(w).max(), 1e-30)
+    gaps = np.full(d, np.inf)
+    if d > 1:
+        gaps[:-1] = np.minimum(gaps[:-1], w[:-1] - w[1:])
+        gaps[1:] = np.minimum(gaps[1:], w[:-1] - w[1:])
+    sel = gaps > 1e-3 * scale
+    out["vec"] = float(np.max(np.linalg.norm(Q[:, sel] - Q_ref[:, sel], axis=0))) if sel.any() else 0.0
+    return out
+
+
+@pytest.mark.parametrize("B,m,n,dtype", [(1, 128, 64, torch.float32), (3, 40, 24, torch.float32),
+                                         (2, 17, 33, torch.float32), (2, 64, 32, torch.bfloat16)])
+def test_teacher_forced_steps(B, m, n, dtype):
+    lr, b1, b2, eps, f = 0.01, 0.9, 0.95, 1e-8, 2
+    ob = _batch(B, m, n, param_dtype=dtype, lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=0.0, root_every=f)
+    rng = np.random.default_rng(m + n)
+    W = torch.tensor(rng.standard_normal((B, m, n)) * 0.001, dtype=dtype, device="cuda")
+    worst = {}
+    for t in range(1, 6):
+        pre = _snap(ob)
+        Wp = W.double().cpu().numpy()
+        G = torch.tensor(rng.standard_normal((B, m, n)), dtype=dtype, device="cuda")
+        ob.step(W, G, lr)
+        assert ob.query_status() == 0
+        post = _snap(ob)
+        Wn = W.double().cpu().numpy()
+        Gd = G.double().cpu().numpy()
+        for b in range(B):
+            st = O.SoapState(M=pre["M"][b], V=pre["V"][b], L=pre["L"][b], R=pre["R"][b], QL=pre["QL"][b],
+                             QR=pre["QR"][b], t=t - 1)
+            ost, _Wo, No = O.soap_step(st, Wp[b], Gd[b], lr, b1, b2, eps, f)
+            err = {k: O.rel_fro(post[k][b], getattr(ost, k)) for k in ("M", "V", "L", "R")}
+            err["N"] = O.rel_fro((Wp[b] - Wn[b]) / lr, No)
+            if t % f == 0:
+                for side, S in (("QL", post["L"][b]), ("QR", post["R"][b])):
+                    ref = O.eigenvectors_aligned(S, pre[side][b])
+                    for k, v in _check_basis(post[side][b], S, pre[side][b], ref).items():
+                        err[side + "_" + k] = v
+            else:
+                err["Q_same"] = float(not (np.array_equal(post["QL"][b], pre["QL"][b])
+                                           and np.array_equal(post["QR"][b], pre["QR"][b])))
+            for k, v in err.items():
+                worst[k] = max(worst.get(k, 0.0), v)
+    print(f"soap {B}x{m}x{n} {dtype}", {k: f"{v:.1e}" for k, v in worst.items()})
+    for k in ("M", "V", "L", "R"):
+        assert worst[k] < 1e-5, (k, worst)
+    # bf16 parameters round the new W to 8 bits (|W| ~ 5 lr |N| here): ~1% of the step
+    assert worst["N"] < (2e-2 if dtype == torch.bfloat16 else 1e-4), worst
+    assert worst["Q_same"] == 0.0
+    for side in ("QL", "QR"):
+        assert worst[side + "_orth"] < 1e-5 and worst[side + "_offdiag"] < 1e-5, worst
+        assert worst[side + "_order"] < 1e-6 and worst[side + "_sign"] == 0.0, worst
+        assert worst[side + "_vec"] < 1e-3, worst
+    ob.close()
+
+
+def test_without_refresh_the_step_is_adam():
+    """Before any refresh the bases are the identity: SOAP is Adam with both
+    moments bias-corrected."""
+    B, m, n = 2, 24, 16
+    lr, b1, b2, eps = 0.02, 0.9, 0.99, 1e-8
+    ob = _batch(B, m, n, lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=0.0, root_every=1000)
+    rng = np.random.default_rng(3)
+    W = torch.zeros((B, m, n), device="cuda")
+    Mn = np.zeros((B, m, n))
+    Vn = np.zeros((B, m, n))
+    Wn = np.zeros((B, m, n))
+    for t in range(1, 6):
+        G = rng.standard_normal((B, m, n)).astype(np.float32)
+        ob.step(W, torch.tensor(G, device="cuda"), lr)
+        Mn = b1 * Mn + (1 - b1) * G
+        Vn = b2 * Vn + (1 - b2) * G.astype(np.float64) ** 2
+        Wn -= lr * (Mn / (1 - b1 ** t)) / (np.sqrt(Vn / (1 - b2 ** t)) + eps)
+    assert ob.query_status() == 0
+    assert O.rel_fro(W.double().cpu().numpy(), Wn) < 1e-5
+    ob.close()
+
+
+def test_optimizer_class_matches_the_batch_api():
+    from kronecker_factored_second_gb300.okls import SOAP, OklsBatch
+    torch.manual_seed(5)
+    p = torch.nn.Parameter(torch.randn(2, 32, 48, device="cuda") * 0.02)
+    W = p.detach().clone()
+    opt = SOAP([p], lr=0.01, betas=(0.9, 0.95), eps=1e-8, precondition_frequency=2)
+    ob = OklsBatch(2, 32, 48, lr=0.01, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0, root_every=2,
+                   method="soap")
+    for _ in range(4):
+        g = torch.randn(2, 32, 48, device="cuda")
+        p.grad = g.clone()
+        opt.step()
+        ob.step(W, g, 0.01)
+    torch.cuda.synchronize()
+    assert torch.equal(p.detach(), W)
+    ob.close()
