@@ -40,7 +40,11 @@ def dense_flops(m: int, n: int, method: str = "okls") -> float:
     """Dense algorithmic FLOPs of one matrix's step.  OKLS: 27 products of
     each Newton-Schulz chain, the two preconditioned factor inputs and the
     two factor products, the whitening.  Classic Shampoo: two chained chains
-    (54 products) per factor, the two factor products of G, the whitening."""
+    (54 products) per factor, the two factor products of G, the whitening.
+    SOAP: three two-sided rotations and the two factor products (the
+    eigenbasis refresh is not counted)."""
+    if method == "soap":
+        return 3 * 2.0 * m * n * (m + n) + 2.0 * m * n * (m + n)
     if method == "shampoo":
         return 54 * 2.0 * (m ** 3 + n ** 3) + 2.0 * m * n * (m + n) + 2.0 * m * n * (m + n)
     return 27 * 2.0 * (m ** 3 + n ** 3) + 4.0 * m * n * (m + n) + 2.0 * m * n * (m + n)
@@ -268,9 +272,13 @@ def run_okls(args):
     gs = GradientStream(wl, dev)
     n_distinct = max(2, min(wl.steps, args.distinct))
     groups = []
+    extra = {}
+    if args.method == "soap":
+        # SOAP's Adam hyperparameters; the eigenbases are refreshed every 10 steps
+        extra = dict(beta1=0.95, beta2=0.95, eps=1e-8, weight_decay=0.0, root_every=10)
     for gi, g in enumerate(wl.groups):
         ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=args.split, ridge=args.ridge,
-                       method=args.method, device=dev)
+                       method=args.method, device=dev, **extra)
         W = gs.init_weights(gi)
         Gs = [gs.grad(gi, t + 1) for t in range(n_distinct)]
         groups.append((g, ob, W, Gs))
@@ -471,6 +479,35 @@ def run_okls(args):
                         "tflops_dense": sum_over_ranks(fs * args.steps, ws, dev) / (ms3 / 1e3) / 1e12,
                         "gemm_tflops": gt}
 
+    soap_line = None
+    if args.also_soap and args.method == "okls":
+        # SOAP runs matrices up to 128 x 128 in this build: timed on the 128 x 64 workload
+        swl = workload("single128x64")
+        sgs = GradientStream(swl, dev)
+        sg = swl.groups[0]
+        sob = OklsBatch(sg.batch, sg.m, sg.n, param_dtype=sg.dtype, method="soap", beta1=0.95, beta2=0.95,
+                        eps=1e-8, weight_decay=0.0, root_every=10, device=dev)
+        sW = sgs.init_weights(0)
+        sG = [sgs.grad(0, t + 1) for t in range(4)]
+        for k in range(20):
+            sob.step(sW, sG[k % 4], 3e-3)
+        torch.cuda.synchronize()
+        nsteps = 200
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(nsteps):
+            sob.step(sW, sG[k % 4], 3e-3)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if sob.status_nothrow()[1]:
+            raise RuntimeError("device status flagged in the SOAP leg")
+        ms4 = a.elapsed_time(b)
+        soap_line = {"method": "SOAP (Adam in the factors' eigenbasis), fp32, one CTA per matrix, Jacobi refresh "
+                               "every 10 steps; matrices up to 128 x 128 in this build",
+                     "workload": "single128x64: one 128 x 64 fp32 matrix", "steps": nsteps,
+                     "value": sg.batch * nsteps / (ms4 / 1e3), "unit": "matrices/s", "ms_per_step": ms4 / nsteps}
+        sob.close()
+
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(args.cpu_seconds)
@@ -510,6 +547,8 @@ def run_okls(args):
             line["split_mode"] = split_line
         if shampoo_line:
             line["shampoo"] = shampoo_line
+        if soap_line:
+            line["soap"] = soap_line
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -531,7 +570,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--also-split", type=int, default=1)
     ap.add_argument("--also-shampoo", type=int, default=1)
-    ap.add_argument("--method", choices=["okls", "shampoo"], default="okls")
+    ap.add_argument("--also-soap", type=int, default=1)
+    ap.add_argument("--method", choices=["okls", "shampoo", "soap"], default="okls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args()

@@ -23,22 +23,44 @@ namespace okls {
 
 constexpr int kSoapMax = 128;
 constexpr int kSoapThreads = 256;
-constexpr int kSoapStepSmem = 3 * kSoapMax * kSoapMax * 4;                  // G, G', scratch (fp32)
+constexpr int kSoapRefThreads = 512;
+constexpr int kSoapLd = kSoapMax + 4;                           // padded fp32 pitch (16-byte rows)
+constexpr int kSoapBuf = kSoapMax * kSoapLd;                     // floats per staged matrix
+constexpr int kSoapStepSmem = 3 * kSoapBuf * 4;                  // three staged matrices
 constexpr int kSoapRefreshSmem = 2 * kSoapMax * (kSoapMax + 1) * 4 + 4096;  // A, V (+ rotations)
 
-// C (r x c) = op(A) op(B) with all operands in row-major storage:
-// ta: A is stored k x r (use its transpose); tb: B is stored c x k.
-__device__ void soap_mm(float* C, int ldc, const float* A, int lda, bool ta, const float* B, int ldb, bool tb, int r,
-                        int c, int k) {
-  for (int e = threadIdx.x; e < r * c; e += blockDim.x) {
-    const int i = e / c, j = e % c;
-    float acc = 0.0f;
+// Copy a rows x cols fp32 matrix (row-major, pitch cols) into shared memory.
+__device__ __forceinline__ void soap_stage(float* dst, const float* src, int rows, int cols) {
+  for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) dst[(e / cols) * kSoapLd + e % cols] = src[e];
+}
+
+// Product of two staged matrices, r x c = op(A) op(B) with K = k; each thread
+// forms 4 x 4 outputs and hands each of them to `out(i, j, value)`.
+// ta: A is staged k x r (use its transpose); tb: B is staged c x k.
+template <class F>
+__device__ __forceinline__ void soap_mm4(const float* A, bool ta, const float* B, bool tb, int r, int c, int k,
+                                         F&& out) {
+  const int tr = (r + 3) / 4, tcn = (c + 3) / 4;
+  for (int blk = threadIdx.x; blk < tr * tcn; blk += blockDim.x) {
+    const int i0 = (blk / tcn) * 4, j0 = (blk % tcn) * 4;
+    float acc[4][4] = {};
     for (int q = 0; q < k; ++q) {
-      const float a = ta ? A[q * lda + i] : A[i * lda + q];
-      const float b = tb ? B[j * ldb + q] : B[q * ldb + j];
-      acc = fmaf(a, b, acc);
+      float av[4], bv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        av[u] = ta ? A[q * kSoapLd + i0 + u] : A[(i0 + u) * kSoapLd + q];
+        bv[u] = tb ? B[(j0 + u) * kSoapLd + q] : B[q * kSoapLd + j0 + u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
     }
-    C[i * ldc + j] = acc;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        if (i0 + u < r && j0 + v < c) out(i0 + u, j0 + v, acc[u][v]);
   }
 }
 
@@ -51,6 +73,10 @@ __device__ __forceinline__ float w_load<__nv_bfloat16>(const __nv_bfloat16* p) {
 __device__ __forceinline__ void w_store(float* p, float v) { *p = v; }
 __device__ __forceinline__ void w_store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+// One matrix per CTA.  Shared memory holds three staged matrices: G (later
+// N'), a basis (Q_L or Q_R, staged for each product) and one intermediate.
+// Out-of-range rows and columns of the staged tiles are zero, so the 4 x 4
+// tiles never read garbage.
 template <typename WT, typename GT>
 __global__ void __launch_bounds__(kSoapThreads) k_soap_step(SoapArgs A) {
   extern __shared__ float sm[];
@@ -58,9 +84,9 @@ __global__ void __launch_bounds__(kSoapThreads) k_soap_step(SoapArgs A) {
   const int b = blockIdx.x;
   const int m = A.m, n = A.n;
   const int64_t mn = static_cast<int64_t>(m) * n;
-  float* Gs = sm;                       // G, then N' and N
-  float* Gr = sm + kSoapMax * kSoapMax;  // G', then M'
-  float* Tt = Gr + kSoapMax * kSoapMax;  // products' left halves
+  float* Gs = sm;                 // G, then N'
+  float* Qs = sm + kSoapBuf;      // Q_L or Q_R
+  float* Ts = sm + 2 * kSoapBuf;  // left halves of the two-sided products
   const GT* G = static_cast<const GT*>(A.G) + b * mn;
   WT* W = static_cast<WT*>(A.W) + b * mn;
   float* M = A.M + b * mn;
@@ -71,59 +97,65 @@ __global__ void __launch_bounds__(kSoapThreads) k_soap_step(SoapArgs A) {
   const float* QR = A.QR + static_cast<int64_t>(b) * n * n;
   bool bad = false;
 
+  for (int e = threadIdx.x; e < 3 * kSoapBuf; e += blockDim.x) sm[e] = 0.0f;
+  __syncthreads();
   for (int e = threadIdx.x; e < mn; e += blockDim.x) {
     const float g = w_load<GT>(G + e);
     bad |= !isfinite(g);
-    Gs[e] = g;
+    Gs[(e / n) * kSoapLd + e % n] = g;
   }
+  soap_stage(Qs, QL, m, m);
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0) atomicOr(A.status, kStNonfiniteInput);
     return;
   }
-  // G' = Q_L^T G Q_R
-  soap_mm(Tt, n, QL, m, true, Gs, n, false, m, n, m);
+  // G' = Q_L^T G Q_R, straight into V <- b2 V + (1-b2) G'^2
+  soap_mm4(Qs, true, Gs, false, m, n, m, [&](int i, int j, float v) { Ts[i * kSoapLd + j] = v; });
   __syncthreads();
-  soap_mm(Gr, n, Tt, n, false, QR, n, false, m, n, n);
+  soap_stage(Qs, QR, n, n);
   __syncthreads();
-  // V <- b2 V + (1-b2) G'^2; M <- b1 M + (1-b1) G (into the state); G' is done
-  for (int e = threadIdx.x; e < mn; e += blockDim.x) {
-    V[e] = fmaf(A.beta2, V[e], (1.0f - A.beta2) * Gr[e] * Gr[e]);
-    M[e] = fmaf(A.beta1, M[e], (1.0f - A.beta1) * Gs[e]);
-  }
-  __syncthreads();
-  // L <- b2 L + (1-b2) G G^T, R <- b2 R + (1-b2) G^T G (G still in Gs)
-  for (int e = threadIdx.x; e < m * m; e += blockDim.x) {
-    const int i = e / m, j = e % m;
-    float acc = 0.0f;
-    for (int q = 0; q < n; ++q) acc = fmaf(Gs[i * n + q], Gs[j * n + q], acc);
-    L[e] = fmaf(A.beta2, L[e], (1.0f - A.beta2) * acc);
-  }
-  for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
-    const int i = e / n, j = e % n;
-    float acc = 0.0f;
-    for (int q = 0; q < m; ++q) acc = fmaf(Gs[q * n + i], Gs[q * n + j], acc);
-    R[e] = fmaf(A.beta2, R[e], (1.0f - A.beta2) * acc);
-  }
-  // M' = Q_L^T M Q_R (M read back from the state this block just wrote)
-  __syncthreads();
-  soap_mm(Tt, n, QL, m, true, M, n, false, m, n, m);
-  __syncthreads();
-  soap_mm(Gr, n, Tt, n, false, QR, n, false, m, n, n);
-  __syncthreads();
-  // N' = (M' / (1 - b1^t)) / (sqrt(V / (1 - b2^t)) + eps)
+  soap_mm4(Ts, false, Qs, false, m, n, n, [&](int i, int j, float v) {
+    float& x = V[static_cast<int64_t>(i) * n + j];
+    x = fmaf(A.beta2, x, (1.0f - A.beta2) * v * v);
+  });
+  // M <- b1 M + (1-b1) G; L <- b2 L + (1-b2) G G^T; R <- b2 R + (1-b2) G^T G
   for (int e = threadIdx.x; e < mn; e += blockDim.x)
-    Gs[e] = (Gr[e] * A.bc1) / (sqrtf(V[e] * A.bc2) + A.eps);
+    M[e] = fmaf(A.beta1, M[e], (1.0f - A.beta1) * Gs[(e / n) * kSoapLd + e % n]);
+  soap_mm4(Gs, false, Gs, true, m, m, n, [&](int i, int j, float v) {
+    float& x = L[static_cast<int64_t>(i) * m + j];
+    x = fmaf(A.beta2, x, (1.0f - A.beta2) * v);
+  });
+  soap_mm4(Gs, true, Gs, false, n, n, m, [&](int i, int j, float v) {
+    float& x = R[static_cast<int64_t>(i) * n + j];
+    x = fmaf(A.beta2, x, (1.0f - A.beta2) * v);
+  });
   __syncthreads();
-  // N = Q_L N' Q_R^T
-  soap_mm(Tt, n, QL, m, false, Gs, n, false, m, n, m);
+  // M' = Q_L^T M Q_R, then N' = (M'/(1-b1^t)) / (sqrt(V/(1-b2^t)) + eps) into Gs
+  for (int e = threadIdx.x; e < mn; e += blockDim.x) Gs[(e / n) * kSoapLd + e % n] = M[e];
+  soap_stage(Qs, QL, m, m);
   __syncthreads();
-  soap_mm(Gs, n, Tt, n, false, QR, n, true, m, n, n);
+  soap_mm4(Qs, true, Gs, false, m, n, m, [&](int i, int j, float v) { Ts[i * kSoapLd + j] = v; });
   __syncthreads();
-  for (int e = threadIdx.x; e < mn; e += blockDim.x) {
-    const float w = fmaf(-A.lr, Gs[e], A.decay * w_load<WT>(W + e));
-    bad |= !isfinite(w);
-    w_store(W + e, w);
-  }
+  soap_stage(Qs, QR, n, n);
+  __syncthreads();
+  soap_mm4(Ts, false, Qs, false, m, n, n, [&](int i, int j, float v) {
+    const float vv = V[static_cast<int64_t>(i) * n + j];
+    Gs[i * kSoapLd + j] = (v * A.bc1) / (sqrtf(vv * A.bc2) + A.eps);
+  });
+  __syncthreads();
+  // N = Q_L N' Q_R^T and the update
+  soap_stage(Qs, QL, m, m);
+  __syncthreads();
+  soap_mm4(Qs, false, Gs, false, m, n, m, [&](int i, int j, float v) { Ts[i * kSoapLd + j] = v; });
+  __syncthreads();
+  soap_stage(Qs, QR, n, n);
+  __syncthreads();
+  soap_mm4(Ts, false, Qs, true, m, n, n, [&](int i, int j, float v) {
+    WT* w = W + static_cast<int64_t>(i) * n + j;
+    const float nw = fmaf(-A.lr, v, A.decay * w_load<WT>(w));
+    bad |= !isfinite(nw);
+    w_store(w, nw);
+  });
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(A.status, kStNonfiniteUpdate);
 }
 
@@ -135,7 +167,7 @@ __device__ __forceinline__ int rr_index(int pos, int r, int dp) {
   return 1 + (pos - 1 + r) % (dp - 1);
 }
 
-__global__ void __launch_bounds__(kSoapThreads) k_soap_refresh(SoapRefreshArgs A) {
+__global__ void __launch_bounds__(kSoapRefThreads) k_soap_refresh(SoapRefreshArgs A) {
   extern __shared__ float sm[];
   if (*reinterpret_cast<const volatile uint32_t*>(A.status) != 0u) return;
   const int fi = blockIdx.x < A.count ? 0 : 1;
@@ -148,7 +180,7 @@ __global__ void __launch_bounds__(kSoapThreads) k_soap_refresh(SoapRefreshArgs A
   float* Vs = sm + kSoapMax * ld;    // accumulated rotations (eigenvectors in columns)
   float* cs = Vs + kSoapMax * ld;    // per pair: c, s
   int* pr = reinterpret_cast<int*>(cs + kSoapMax);  // per pair: p, q
-  __shared__ float red[kSoapThreads / 32];
+  __shared__ float red[kSoapRefThreads / 32];
   __shared__ float off_sum, diag_sum;
   const int dp = d + (d & 1);
   const int np = dp / 2;
@@ -178,7 +210,7 @@ __global__ void __launch_bounds__(kSoapThreads) k_soap_refresh(SoapRefreshArgs A
     __syncthreads();
     if (threadIdx.x == 0) {
       float t = 0.0f;
-      for (int w = 0; w < kSoapThreads / 32; ++w) t += red[w];
+      for (int w = 0; w < kSoapRefThreads / 32; ++w) t += red[w];
       off_sum = t;
     }
     __syncthreads();
@@ -186,7 +218,7 @@ __global__ void __launch_bounds__(kSoapThreads) k_soap_refresh(SoapRefreshArgs A
     __syncthreads();
     if (threadIdx.x == 0) {
       float t = 0.0f;
-      for (int w = 0; w < kSoapThreads / 32; ++w) t += red[w];
+      for (int w = 0; w < kSoapRefThreads / 32; ++w) t += red[w];
       diag_sum = t;
     }
     __syncthreads();
@@ -214,27 +246,34 @@ __global__ void __launch_bounds__(kSoapThreads) k_soap_refresh(SoapRefreshArgs A
         pr[2 * k + 1] = q;
       }
       __syncthreads();
+      // threads: lane j = tid % 128 walks a row or column, group tid / 128 a
+      // quarter of the pairs
+      const int j = threadIdx.x & (kSoapMax - 1);
+      const int g0 = threadIdx.x >> 7;
+      constexpr int kGroups = kSoapRefThreads / kSoapMax;
       // 2. rows p, q of A (A <- J^T A)
-      for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
-        const int k = e / dp, j = e % dp;
-        const int p = pr[2 * k], q = pr[2 * k + 1];
-        const float c = cs[2 * k], s = cs[2 * k + 1];
-        const float ap = As[p * ld + j], aq = As[q * ld + j];
-        As[p * ld + j] = c * ap - s * aq;
-        As[q * ld + j] = s * ap + c * aq;
+      if (j < dp) {
+        for (int k = g0; k < np; k += kGroups) {
+          const int p = pr[2 * k], q = pr[2 * k + 1];
+          const float c = cs[2 * k], s = cs[2 * k + 1];
+          const float ap = As[p * ld + j], aq = As[q * ld + j];
+          As[p * ld + j] = c * ap - s * aq;
+          As[q * ld + j] = s * ap + c * aq;
+        }
       }
       __syncthreads();
-      // 3. columns p, q of A (A <- A J) and of V (V <- V J)
-      for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
-        const int k = e / dp, i = e % dp;
-        const int p = pr[2 * k], q = pr[2 * k + 1];
-        const float c = cs[2 * k], s = cs[2 * k + 1];
-        const float ap = As[i * ld + p], aq = As[i * ld + q];
-        As[i * ld + p] = c * ap - s * aq;
-        As[i * ld + q] = s * ap + c * aq;
-        const float vp = Vs[i * ld + p], vq = Vs[i * ld + q];
-        Vs[i * ld + p] = c * vp - s * vq;
-        Vs[i * ld + q] = s * vp + c * vq;
+      // 3. columns p, q of A (A <- A J) and of V (V <- V J); j is the row here
+      if (j < dp) {
+        for (int k = g0; k < np; k += kGroups) {
+          const int p = pr[2 * k], q = pr[2 * k + 1];
+          const float c = cs[2 * k], s = cs[2 * k + 1];
+          const float ap = As[j * ld + p], aq = As[j * ld + q];
+          As[j * ld + p] = c * ap - s * aq;
+          As[j * ld + q] = s * ap + c * aq;
+          const float vp = Vs[j * ld + p], vq = Vs[j * ld + q];
+          Vs[j * ld + p] = c * vp - s * vq;
+          Vs[j * ld + q] = s * vp + c * vq;
+        }
       }
       __syncthreads();
     }
@@ -327,7 +366,7 @@ cudaError_t launch_soap_step(const SoapArgs& A, cudaStream_t st) {
 cudaError_t launch_soap_refresh(const SoapRefreshArgs& A, cudaStream_t st) {
   cudaError_t e = soap_attributes();
   if (e != cudaSuccess) return e;
-  k_soap_refresh<<<2 * A.count, kSoapThreads, kSoapRefreshSmem, st>>>(A);
+  k_soap_refresh<<<2 * A.count, kSoapRefThreads, kSoapRefreshSmem, st>>>(A);
   return cudaGetLastError();
 }
 
