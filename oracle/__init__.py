@@ -1,5 +1,6 @@
 """Float64 CPU oracle for the Online KL Shampoo (OKLS) preconditioner step,
-the classic Shampoo step it refines, and SOAP (Adam in the factors' eigenbasis).
+the classic Shampoo step it refines, SOAP (Adam in the factors' eigenbasis)
+and Clean (Nyström low-rank factors with block-wise Adam).
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this package:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
@@ -30,6 +31,11 @@ Parity status per function (the pins live in ``tests/test_oracle_pins.py``):
   entry loops; fixed bases: rotated Adam; eigenvector order and signs;
   refresh schedule).  The readings of the bias correction, the initial bases
   and the eigenvector signs follow the pages' listings; no printed values.
+* ``nystrom_warm``, ``clean_step``          pinned (exactly low-rank operators
+  recovered, with and without warm start; power iterations track the top
+  eigenpairs; the four blocks partition G; pooled moments by entry loops;
+  full-rank bases reduce to rotated Adam; unchanged bases leave the moments
+  in place).  Readings c1-c7 in the module; no printed values.
 * ``variance_correction``                  pinned by Monte Carlo against its
   definition (variance of the Nesterov combination for iid unit gradients);
   the *choice* of this reading is not printed on the pages.

@@ -46,6 +46,7 @@ __all__ = [
     "okls_step", "okls_run", "rel_fro", "NS_HEADROOM", "NS_MARGIN",
     "quarter_root_exact", "quarter_root_chain", "shampoo_init", "shampoo_step",
     "SoapState", "soap_init", "soap_step", "eigenvectors_aligned",
+    "nystrom_warm", "CleanState", "clean_init", "clean_step",
 ]
 
 # Power-of-two headroom of the stored binary16 operands (reading r9): Y and T
@@ -595,6 +596,140 @@ def soap_step(state: SoapState, W: np.ndarray, G: np.ndarray, lr: float, beta1: 
         QL = eigenvectors_aligned(L, QL)
         QR = eigenvectors_aligned(R, QR)
     return SoapState(M=M, V=V, L=L, R=R, QL=QL, QR=QR, t=t), W_new, N
+
+
+# ------------------------------------------------------------- Clean (Nystrom) ---
+#
+# Page "Clean: Second-order LLM Training at Linear Memory Cost via Nystrom
+# Sketching": Algorithm 1 (the step), Eqn. (8) (the sketch of the factor
+# without forming it), Eqns. (10)-(13) and Table 1 (the four blocks and their
+# moments), Eqns. (14)-(15) (moving the moments to refreshed bases), Eqn. (16)
+# (the update), Appendix A Algorithm 3 (warm-started Nystrom with subspace
+# iteration).  Readings:
+#   c1  Algorithm 3 orthonormalises the starting sketch in both branches
+#       (warm start [U_prev, Psi] and cold start): the listing's line 5 QR.
+#   c2  eps(x) is the spacing of binary64 numbers at x: 2^(floor(log2 x) - 52);
+#       norm(Y, 2) is the spectral norm.
+#   c3  Y_nu / C is right division, Y_nu C^-1, with C the upper Cholesky
+#       factor (C^T C = (B + B^T)/2).
+#   c4  the Gaussian draws Psi are inputs (m x p with a warm start, m x (r+p)
+#       at the first refresh); thin QR takes R with a non-negative diagonal.
+#   c5  the factor sketched at a refresh is b2 U Lambda U^T + (1-b2) G G^T
+#       with the previous refresh's factors, (1-b2) G G^T at the first one.
+#   c6  the moments use the step count t of the whole run for their bias
+#       corrections; the pooled second moments are sums (1^T (G_A)^2,
+#       (G_B)^2 1, ||C||_F^2) as printed, bias-corrected like V.
+#   c7  W <- W - alpha lr G~ (no weight decay in the listing); alpha = 1.
+
+def _qr_pos(X: np.ndarray) -> np.ndarray:
+    """Thin QR with a non-negative diagonal of R (reading c4)."""
+    Q, R = np.linalg.qr(X)
+    s = np.sign(np.diag(R))
+    s[s == 0] = 1.0
+    return Q * s
+
+
+def _eps64(x: float) -> float:
+    """Spacing of binary64 numbers at x (reading c2)."""
+    return 0.0 if x == 0.0 else 2.0 ** (math.floor(math.log2(abs(x))) - 52)
+
+
+def nystrom_warm(apply_A, r: int, p: int, q: int, U_prev, Psi: np.ndarray):
+    """Algorithm 3: rank-r Nystrom approximation [U, Lambda] of the PSD
+    operator apply_A (X -> A X), warm-started at U_prev (or None)."""
+    Omega = np.hstack([U_prev, Psi]) if U_prev is not None else Psi
+    Omega = _qr_pos(Omega)
+    for _ in range(q):
+        Omega = _qr_pos(apply_A(Omega))
+    Y = apply_A(Omega)
+    nu = _eps64(float(np.linalg.norm(Y, 2)))
+    Yn = Y + nu * Omega
+    B = Omega.T @ Yn
+    C = np.linalg.cholesky(0.5 * (B + B.T)).T          # upper: C^T C = (B + B^T)/2
+    U, sig, _vt = np.linalg.svd(np.linalg.solve(C.T, Yn.T).T, full_matrices=False)
+    lam = np.maximum(0.0, sig ** 2 - nu)
+    U, lam = U[:, :r], lam[:r]
+    if U_prev is not None:
+        s = np.sign(np.sum(U * U_prev, axis=0))
+        s[s == 0] = 1.0
+        U = U * s
+    return U, lam
+
+
+@dataclass
+class CleanState:
+    UL: np.ndarray | None = None   # m x r
+    lamL: np.ndarray | None = None
+    UR: np.ndarray | None = None   # n x r
+    lamR: np.ndarray | None = None
+    M: np.ndarray | None = None    # r x r (Main)
+    V: np.ndarray | None = None
+    MA: np.ndarray | None = None   # m x r (block A)
+    vA: np.ndarray | None = None   # r
+    MB: np.ndarray | None = None   # r x n (block B)
+    vB: np.ndarray | None = None   # r
+    vC: float = 0.0                # block C
+    t: int = 0
+
+
+def clean_init(m: int, n: int, r: int) -> CleanState:
+    return CleanState(M=np.zeros((r, r)), V=np.zeros((r, r)), MA=np.zeros((m, r)), vA=np.zeros(r),
+                      MB=np.zeros((r, n)), vB=np.zeros(r), vC=0.0, t=0)
+
+
+def clean_step(state: CleanState, W: np.ndarray, G: np.ndarray, lr: float, beta1: float, beta2: float,
+               eps: float, r: int, p: int, q: int, T: int, psiL=None, psiR=None, alpha: float = 1.0):
+    """One Clean step for one matrix in float64 (Algorithm 1).  psiL, psiR
+    are the Gaussian draws of a refresh step.  Returns (state, W_new, G~)."""
+    G = np.asarray(G, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    m, n = G.shape
+    t = state.t + 1
+    st = CleanState(**{k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in state.__dict__.items()})
+    st.t = t
+    if (t - 1) % T == 0:
+        def aL(X, U=st.UL, lam=st.lamL):
+            out = (1.0 - beta2) * (G @ (G.T @ X))
+            return out + beta2 * (U @ (lam[:, None] * (U.T @ X))) if U is not None else out
+
+        def aR(X, U=st.UR, lam=st.lamR):
+            out = (1.0 - beta2) * (G.T @ (G @ X))
+            return out + beta2 * (U @ (lam[:, None] * (U.T @ X))) if U is not None else out
+        ULn, lamLn = nystrom_warm(aL, r, p, q, st.UL, psiL)
+        URn, lamRn = nystrom_warm(aR, r, p, q, st.UR, psiR)
+        if st.UL is not None:
+            # Eqns. (14)-(15): moments into the new bases
+            OL = ULn.T @ st.UL            # r x r: new^T old
+            OR = st.UR.T @ URn            # r x r: old^T new
+            PLn = np.eye(m) - ULn @ ULn.T
+            PRn = np.eye(n) - URn @ URn.T
+            st.M = OL @ st.M @ OR
+            st.MA = PLn @ st.MA @ OR
+            st.MB = OL @ st.MB @ PRn
+            st.vA = st.vA @ (OR * OR)
+            st.vB = (OL * OL) @ st.vB
+        st.UL, st.lamL, st.UR, st.lamR = ULn, lamLn, URn, lamRn
+    UL, UR = st.UL, st.UR
+    PL = np.eye(m) - UL @ UL.T
+    PR = np.eye(n) - UR @ UR.T
+    S = UL.T @ G @ UR
+    GA = PL @ G @ UR
+    GB = UL.T @ G @ PR
+    C = PL @ G @ PR
+    st.M = beta1 * st.M + (1.0 - beta1) * S
+    st.V = beta2 * st.V + (1.0 - beta2) * S * S
+    st.MA = beta1 * st.MA + (1.0 - beta1) * GA
+    st.vA = beta2 * st.vA + (1.0 - beta2) * np.sum(GA * GA, axis=0)
+    st.MB = beta1 * st.MB + (1.0 - beta1) * GB
+    st.vB = beta2 * st.vB + (1.0 - beta2) * np.sum(GB * GB, axis=1)
+    st.vC = beta2 * st.vC + (1.0 - beta2) * float(np.sum(C * C))
+    c1, c2 = 1.0 - beta1 ** t, 1.0 - beta2 ** t
+    main = (st.M / c1) / (np.sqrt(st.V / c2) + eps)
+    blkA = (st.MA / c1) / (np.sqrt(st.vA / c2)[None, :] + eps)
+    blkB = (st.MB / c1) / (np.sqrt(st.vB / c2)[:, None] + eps)
+    blkC = C / (math.sqrt(st.vC / c2) + eps)
+    Gt = UL @ main @ UR.T + blkA @ UR.T + UL @ blkB + blkC
+    return st, W - alpha * lr * Gt, Gt
 
 
 def rel_fro(A: np.ndarray, B: np.ndarray) -> float:

@@ -579,3 +579,125 @@ def test_soap_refresh_schedule():
             assert np.allclose(QL.T @ L @ QL, np.diag(np.diag(QL.T @ L @ QL)), atol=1e-12)
         else:
             assert np.array_equal(st.QL, prev.QL) and np.array_equal(st.QR, prev.QR)
+
+
+# ------------------------------------------------------------------ Clean
+
+def test_eps64_is_the_binary64_spacing():
+    """Reading c2: eps(x) = 2^(floor(log2 x) - 52)."""
+    from oracle import okls_oracle as OO
+    assert OO._eps64(1.0) == 2.0 ** -52 and OO._eps64(3.0) == 2.0 ** -51
+    assert OO._eps64(0.75) == 2.0 ** -53 and np.nextafter(8.0, 9.0) - 8.0 == OO._eps64(8.0)
+
+
+@pytest.mark.parametrize("warm", [False, True])
+def test_nystrom_recovers_an_exactly_low_rank_operator(warm):
+    """Algorithm 3 on a rank-r PSD matrix returns its eigenpairs (decreasing;
+    with a warm start, signs aligned to it) to rounding."""
+    rng = np.random.default_rng(41)
+    d, r, p = 30, 5, 4
+    U0 = _orth(d, 9)[:, :r]
+    lam0 = np.array([9.0, 6.0, 4.0, 2.0, 1.0])
+    A = (U0 * lam0) @ U0.T
+    prev = U0 * np.array([1, -1, 1, 1, -1.0]) if warm else None
+    psi = rng.standard_normal((d, p if warm else r + p))
+    U, lam = O.nystrom_warm(lambda X: A @ X, r, p, 1, prev, psi)
+    assert np.allclose(lam, lam0, rtol=1e-10)
+    if warm:
+        assert np.allclose(U, prev, atol=1e-10)
+    else:
+        assert np.allclose(np.abs(U.T @ U0), np.eye(r), atol=1e-10)
+
+
+def test_nystrom_with_power_iterations_tracks_the_top_eigenpairs():
+    rng = np.random.default_rng(42)
+    d, r, p = 40, 4, 6
+    Q = _orth(d, 10)
+    lam_all = 0.5 ** np.arange(d)
+    A = (Q * lam_all) @ Q.T
+    U, lam = O.nystrom_warm(lambda X: A @ X, r, p, 3, None, rng.standard_normal((d, r + p)))
+    assert np.allclose(lam, lam_all[:r], rtol=1e-6)
+    assert np.allclose(np.abs(U.T @ Q[:, :r]), np.eye(r), atol=1e-6)
+
+
+def test_clean_blocks_partition_the_gradient():
+    """Eqn. (10) with the scalings dropped: U_L S U_R^T + G_A U_R^T + U_L G_B
+    + C = G for orthonormal U_L, U_R (a projector on the wrong side breaks it)."""
+    rng = np.random.default_rng(43)
+    m, n, r = 9, 7, 3
+    UL, UR = _orth(m, 11)[:, :r], _orth(n, 12)[:, :r]
+    G = rng.standard_normal((m, n))
+    PL, PR = np.eye(m) - UL @ UL.T, np.eye(n) - UR @ UR.T
+    S, GA, GB, C = UL.T @ G @ UR, PL @ G @ UR, UL.T @ G @ PR, PL @ G @ PR
+    assert O.rel_fro(UL @ S @ UR.T + GA @ UR.T + UL @ GB + C, G) < 1e-14
+
+
+def test_clean_moments_by_entry_loops():
+    """Table 1 / Eqns. (12)-(13): first moments EMAs of S, G_A, G_B; second
+    moments V entry-wise, v_A summed over rows, v_B over columns, v_C the
+    squared Frobenius norm of C (sums as printed, reading c6)."""
+    rng = np.random.default_rng(44)
+    m, n, r, p = 8, 6, 2, 2
+    b1, b2 = 0.8, 0.9
+    st = O.clean_init(m, n, r)
+    G1 = rng.standard_normal((m, n))
+    st, _W, _Gt = O.clean_step(st, np.zeros((m, n)), G1, 0.1, b1, b2, 1e-8, r, p, 1, 100,
+                               rng.standard_normal((m, r + p)), rng.standard_normal((n, r + p)))
+    UL, UR = st.UL, st.UR
+    G2 = rng.standard_normal((m, n))
+    prev = st
+    st, _W, _Gt = O.clean_step(prev, np.zeros((m, n)), G2, 0.1, b1, b2, 1e-8, r, p, 1, 100)
+    PL, PR = np.eye(m) - UL @ UL.T, np.eye(n) - UR @ UR.T
+    GA, GB, C = PL @ G2 @ UR, UL.T @ G2 @ PR, PL @ G2 @ PR
+    for j in range(r):
+        s = sum(GA[i, j] ** 2 for i in range(m))
+        assert abs(st.vA[j] - (b2 * prev.vA[j] + (1 - b2) * s)) < 1e-12
+    for i in range(r):
+        s = sum(GB[i, j] ** 2 for j in range(n))
+        assert abs(st.vB[i] - (b2 * prev.vB[i] + (1 - b2) * s)) < 1e-12
+    s = sum(C[i, j] ** 2 for i in range(m) for j in range(n))
+    assert abs(st.vC - (b2 * prev.vC + (1 - b2) * s)) < 1e-12
+    assert np.allclose(st.MA, b1 * prev.MA + (1 - b1) * GA, atol=1e-14)
+
+
+def test_clean_full_rank_bases_are_rotated_adam():
+    """r = m = n: the complements vanish, blocks A, B, C are zero, and with
+    the bases of the first refresh kept the whole run is Adam on
+    S_t = U_L^T G_t U_R rotated back by U_L (.) U_R^T."""
+    rng = np.random.default_rng(45)
+    d, r, p, lr, b1, b2, eps = 5, 5, 0, 0.05, 0.9, 0.95, 1e-8
+    st = O.clean_init(d, d, r)
+    W = np.zeros((d, d))
+    Gs = [rng.standard_normal((d, d)) for _ in range(4)]
+    for t, G in enumerate(Gs, start=1):
+        psi = (rng.standard_normal((d, r)), rng.standard_normal((d, r))) if t == 1 else (None, None)
+        st, W, _ = O.clean_step(st, W, G, lr, b1, b2, eps, r, p, 1, 1000, *psi)
+    assert np.abs(st.MA).max() < 1e-12 and np.abs(st.MB).max() < 1e-12 and st.vC < 1e-20
+    W_rot = _adam_loops([st.UL.T @ G @ st.UR for G in Gs], lr, b1, b2, eps)
+    # the complement blocks are rounding-level (~1e-16) but block C divides by
+    # sqrt(v_C) + eps, lifting them to ~1e-16 / eps = 1e-8
+    assert O.rel_fro(W, st.UL @ W_rot @ st.UR.T) < 1e-6
+
+
+def test_clean_moment_transport_is_identity_for_an_unchanged_basis():
+    """Eqns. (14)-(15): a refresh that returns the same bases leaves every
+    moment as it was."""
+    rng = np.random.default_rng(46)
+    m, n, r, p = 10, 8, 3, 2
+    UL0, UR0 = _orth(m, 13)[:, :r], _orth(n, 14)[:, :r]
+    st = O.clean_init(m, n, r)
+    st.UL, st.lamL, st.UR, st.lamR = UL0, np.array([3.0, 2.0, 1.0]), UR0, np.array([3.0, 2.0, 1.0])
+    st.M = rng.standard_normal((r, r))
+    st.MA = (np.eye(m) - UL0 @ UL0.T) @ rng.standard_normal((m, r))
+    st.MB = rng.standard_normal((r, n)) @ (np.eye(n) - UR0 @ UR0.T)
+    st.vA, st.vB = rng.random(r), rng.random(r)
+    st.t = 3   # the next step (t = 4) refreshes with T = 3
+    # a gradient that keeps the factors' eigenvectors: G = U_L diag U_R^T
+    G = UL0 @ np.diag([1.0, 0.8, 0.6]) @ UR0.T
+    new, _W, _ = O.clean_step(st, np.zeros((m, n)), G, 0.0, 0.0, 0.5, 1e-8, r, p, 2, 3,
+                              rng.standard_normal((m, p)), rng.standard_normal((n, p)))
+    assert np.allclose(new.UL, UL0, atol=1e-10) and np.allclose(new.UR, UR0, atol=1e-10)
+    # with beta1 = 0 the first moments are this step's blocks; v_A, v_B decay with beta2 only
+    assert np.allclose(new.vA, 0.5 * st.vA + 0.5 * np.sum(((np.eye(m) - UL0 @ UL0.T) @ G @ UR0) ** 2, axis=0),
+                       atol=1e-10)
+    assert np.allclose(new.vB, 0.5 * st.vB, atol=1e-10)
