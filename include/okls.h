@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define OKLS_ABI_VERSION 2
+#define OKLS_ABI_VERSION 3
 
 typedef enum okls_status {
   OKLS_OK = 0,
@@ -65,22 +65,33 @@ typedef enum okls_dtype { OKLS_F32 = 0, OKLS_BF16 = 1 } okls_dtype;
 typedef enum okls_method {
   OKLS_METHOD_OKLS = 0,    /* Online KL Shampoo (the default)              */
   OKLS_METHOD_SHAMPOO = 1, /* classic Shampoo: summed factors, -1/4 roots */
-  OKLS_METHOD_SOAP = 2     /* SOAP: Adam in the factors' eigenbasis       */
+  OKLS_METHOD_SOAP = 2,    /* SOAP: Adam in the factors' eigenbasis       */
+  OKLS_METHOD_CLEAN = 3    /* Clean: Nystrom low-rank bases, block Adam   */
 } okls_method;
 
 /* Which piece of state okls_get_state / okls_set_state move.  In Shampoo
  * mode S_a / S_b hold the sums L / R and P_a / P_b their -1/4 roots; M is
  * unused (left at zero).  In SOAP mode S_a / S_b hold the factor EMAs L / R,
  * P_a / P_b their eigenbases Q_L / Q_R (eigenvectors in columns), M the
- * momentum (original space) and V the second moment (eigenbasis). */
+ * momentum (original space) and V the second moment (eigenbasis).  In Clean
+ * mode (rank r) the sizes differ: P_a / P_b are the bases U_L (batch x m x r)
+ * and U_R (batch x n x r, orthonormal columns), S_a / S_b their eigenvalues
+ * Lambda_L, Lambda_R (batch x r, decreasing), M / V the Main block's moments
+ * (batch x r x r), and parts 6-10 the A and B blocks' first moments and the
+ * pooled second moments of blocks A, B and C. */
 typedef enum okls_state_part {
   OKLS_STATE_M = 0,   /* momentum,                 batch x m x n, fp32 */
   OKLS_STATE_SA = 1,  /* left factor S_a,          batch x m x m, fp32 */
   OKLS_STATE_SB = 2,  /* right factor S_b,         batch x n x n, fp32 */
   OKLS_STATE_PA = 3,  /* left root P_a = S_a^-1/2, batch x m x m, fp32 */
   OKLS_STATE_PB = 4,  /* right root P_b,           batch x n x n, fp32 */
-  OKLS_STATE_V = 5    /* SOAP only: second moment in the eigenbasis,
-                         batch x m x n, fp32 */
+  OKLS_STATE_V = 5,   /* SOAP only: second moment in the eigenbasis,
+                         batch x m x n, fp32 (Clean: batch x r x r) */
+  OKLS_STATE_MA = 6,  /* Clean only: M_A, batch x m x r, fp32 */
+  OKLS_STATE_MB = 7,  /* Clean only: M_B, batch x r x n, fp32 */
+  OKLS_STATE_VA = 8,  /* Clean only: v_A, batch x r, fp32 */
+  OKLS_STATE_VB = 9,  /* Clean only: v_B, batch x r, fp32 */
+  OKLS_STATE_VC = 10  /* Clean only: v_C, batch, fp32 */
 } okls_state_part;
 
 /* Bits of the device status word (okls_query_status). */
@@ -132,6 +143,28 @@ typedef enum okls_state_part {
  *                   This build runs SOAP for m, n <= 128 only (one CTA per
  *                   matrix, fp32, Jacobi eigensolver); larger shapes return
  *                   OKLS_ERR_UNSUPPORTED.
+ *                   OKLS_METHOD_CLEAN (Clean page, Algorithm 1 with the
+ *                   sketch of Eqn. (8) and Appendix A, Algorithm 3): at
+ *                   steps t = 1, 1+T, 1+2T, ... (T = root_every) U_L,
+ *                   Lambda_L <- rank-`rank` Nystrom approximation of
+ *                   b2 U_L Lambda_L U_L^T + (1-b2) G G^T (only the second
+ *                   term at t = 1), sketched with rank + oversample columns
+ *                   and `power_iters` subspace iterations, likewise U_R from
+ *                   G^T G, and the moments move to the new bases (Eqns. (14),
+ *                   (15)).  Then, with P_L = I - U_L U_L^T, P_R = I - U_R U_R^T:
+ *                   S = U_L^T G U_R, G_A = P_L G U_R, G_B = U_L^T G P_R,
+ *                   C = P_L G P_R; M, V (entry-wise on S), M_A, v_A (column
+ *                   sums of G_A^2), M_B, v_B (row sums of G_B^2), v_C
+ *                   (||C||_F^2) are Adam moments with both bias corrections;
+ *                   G~ = U_L N(M, V) U_R^T + N(M_A, v_A) U_R^T + U_L N(M_B, v_B)
+ *                   + C / (sqrt(v_C / (1-b2^t)) + eps), N(m, v) = (m/(1-b1^t)) /
+ *                   (sqrt(v/(1-b2^t)) + eps); W <- W - lr wd (lr/lr_peak) W
+ *                   - lr G~.  The sketch's Gaussian draws are an input (see
+ *                   okls_step_noise).  This build runs Clean for m, n <= 128
+ *                   and rank + oversample <= 64 (one CTA per factor, fp32);
+ *                   larger shapes return OKLS_ERR_UNSUPPORTED.
+ *   rank, oversample, power_iters  Clean's r >= 1, p >= 0 (r + p <=
+ *                   min(m, n)) and q in [0, 16]; zero for the other methods.
  *                   OKLS_METHOD_SHAMPOO ignores beta1, beta2,
  *                   variance_correction and eps_every_update (the sums add
  *                   G G^T and G^T G with weight 1, eps enters only at reset,
@@ -160,7 +193,10 @@ typedef struct okls_config {
   int32_t eps_every_update;
   int32_t root_every;
   int32_t method;      /* an okls_method value; 0 = OKLS */
-  int32_t reserved[6]; /* must be zero */
+  int32_t rank;        /* Clean only */
+  int32_t oversample;  /* Clean only */
+  int32_t power_iters; /* Clean only */
+  int32_t reserved[3]; /* must be zero */
 } okls_config;
 
 typedef struct okls_handle_s *okls_handle;
@@ -218,6 +254,24 @@ okls_status okls_reset_state(okls_handle h, void *stream);
  */
 okls_status okls_step(okls_handle h, void *W_dev, const void *G_dev, float lr,
                       void *stream);
+
+/*
+ * okls_step with the Gaussian draws of Clean's sketch (Clean page, Appendix A,
+ * Algorithm 3: Psi ~ N(0, I)) as an input.
+ *   noise_dev  device, fp32, batch x (m + n) x (rank + oversample), 16-byte
+ *              aligned, read only: per matrix Psi_L (m rows) then Psi_R
+ *              (n rows), row-major.  The first refresh (a state without
+ *              bases) takes all rank + oversample columns as the sketch;
+ *              later refreshes take the first `oversample` columns of each
+ *              row beside the previous basis.  Read only on refresh steps
+ *              (t = 1, 1+T, ...), where NULL returns OKLS_ERR_INVALID_ARG;
+ *              may be NULL on the others.  The other methods ignore it.
+ * okls_step(h, ...) is okls_step_noise(h, ..., NULL, stream).  A refresh
+ * whose Cholesky factor breaks down raises OKLS_DEV_NONFINITE_ITER; that step
+ * then changes neither W nor the state (the step counter still advances).
+ */
+okls_status okls_step_noise(okls_handle h, void *W_dev, const void *G_dev,
+                            float lr, const float *noise_dev, void *stream);
 
 /* Synchronise `stream`, read the device status word into *dev_status (may be
  * NULL) and clear it.  Returns OKLS_ERR_NONFINITE / OKLS_ERR_TIMEOUT when the

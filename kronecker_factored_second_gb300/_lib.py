@@ -29,8 +29,10 @@ OKLS_BF16 = 1
 METHOD_OKLS = 0
 METHOD_SHAMPOO = 1
 METHOD_SOAP = 2
+METHOD_CLEAN = 3
 
 STATE_M, STATE_SA, STATE_SB, STATE_PA, STATE_PB, STATE_V = range(6)
+STATE_MA, STATE_MB, STATE_VA, STATE_VB, STATE_VC = range(6, 11)
 
 DEV_NONFINITE_INPUT = 0x1
 DEV_NONFINITE_ITER = 0x2
@@ -58,7 +60,10 @@ class okls_config(ctypes.Structure):
         ("eps_every_update", ctypes.c_int32),
         ("root_every", ctypes.c_int32),
         ("method", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 6),
+        ("rank", ctypes.c_int32),
+        ("oversample", ctypes.c_int32),
+        ("power_iters", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 
@@ -101,6 +106,7 @@ _SIGS = {
     "okls_create": (_I32, [ctypes.POINTER(okls_config), _P, _SZ, _P, _SZ, ctypes.POINTER(_P)]),
     "okls_reset_state": (_I32, [_P, _P]),
     "okls_step": (_I32, [_P, _P, _P, _F, _P]),
+    "okls_step_noise": (_I32, [_P, _P, _P, _F, _P, _P]),
     "okls_query_status": (_I32, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "okls_get_state": (_I32, [_P, _I32, _P, _P]),
     "okls_set_state": (_I32, [_P, _I32, _P, _P]),

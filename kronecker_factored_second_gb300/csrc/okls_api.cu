@@ -792,7 +792,11 @@ struct okls_handle_s {
   Factor fa, fb;
   Buf Gh, GhT, Nh, Xb, XaT;  // Ghat (m x n), Ghat^T (n x m), Nhat (m x n), X_b / Q (m x n), X_a^T (n x m)
   float *sq_a = nullptr, *sq_b = nullptr;  // Shampoo: fp32 square roots L^1/2, R^1/2 between the chains
-  float* V = nullptr;                      // SOAP: second moment in the eigenbasis
+  float* V = nullptr;                      // SOAP: second moment in the eigenbasis; Clean: Main block's
+  // Clean: block moments of A (m x r), B (r x n), pooled second moments, and
+  // the refreshed bases of a refresh step (workspace)
+  float *MA = nullptr, *MB = nullptr, *vA = nullptr, *vB = nullptr, *vC = nullptr;
+  float *ULn = nullptr, *URn = nullptr, *lamLn = nullptr, *lamRn = nullptr;
   float* scal = nullptr;
   uint32_t* status = nullptr;
   CUtensorMap* maps = nullptr;
@@ -809,9 +813,59 @@ struct Layout {
   size_t state_bytes = 0, ws_bytes = 0;
 };
 
+// Clean: bases U_L (m x r), U_R (n x r) and eigenvalues in P_a / P_b and
+// S_a / S_b, Main moments in M / V, the A and B block moments and the pooled
+// second moments; the workspace holds the status word and a refresh's output.
+okls_status plan_clean(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_s* h, Layout* out) {
+  const int64_t B = c.batch, m = c.m, n = c.n, r = c.rank;
+  Planner sp;
+  sp.base = state;
+  auto f32 = [](Planner& pl, int64_t elems) { return static_cast<float*>(pl.take(static_cast<size_t>(elems * 4))); };
+  float* UL = f32(sp, B * m * r);
+  float* UR = f32(sp, B * n * r);
+  float* lamL = f32(sp, B * r);
+  float* lamR = f32(sp, B * r);
+  float* M = f32(sp, B * r * r);
+  float* V = f32(sp, B * r * r);
+  float* MA = f32(sp, B * m * r);
+  float* MB = f32(sp, B * r * n);
+  float* vA = f32(sp, B * r);
+  float* vB = f32(sp, B * r);
+  float* vC = f32(sp, B);
+  Planner wp;
+  wp.base = ws;
+  uint32_t* status = static_cast<uint32_t*>(wp.take(256));
+  float* ULn = f32(wp, B * m * r);
+  float* URn = f32(wp, B * n * r);
+  float* lamLn = f32(wp, B * r);
+  float* lamRn = f32(wp, B * r);
+  out->state_bytes = sp.off;
+  out->ws_bytes = wp.off;
+  if (h) {
+    h->Pa = UL;
+    h->Pb = UR;
+    h->Sa = lamL;
+    h->Sb = lamR;
+    h->M = M;
+    h->V = V;
+    h->MA = MA;
+    h->MB = MB;
+    h->vA = vA;
+    h->vB = vB;
+    h->vC = vC;
+    h->ULn = ULn;
+    h->URn = URn;
+    h->lamLn = lamLn;
+    h->lamRn = lamRn;
+    h->status = status;
+  }
+  return OKLS_OK;
+}
+
 // Lays out state and workspace; with bases set, fills the handle too.
 okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_s* h, Layout* out) {
   const int64_t B = c.batch, m = c.m, n = c.n;
+  if (c.method == OKLS_METHOD_CLEAN) return plan_clean(c, state, ws, h, out);
   Planner sp;
   sp.base = state;
   float* M = static_cast<float*>(sp.take(static_cast<size_t>(B * m * n * 4)));
@@ -938,13 +992,26 @@ okls_status validate(const okls_config* c) {
   if (!(c->ns_lo > 0.0f && c->ns_lo < 1.0f)) return fail(OKLS_ERR_INVALID_ARG, "ns_lo must be in (0, 1)");
   if (!finite_nonneg(c->ridge)) return fail(OKLS_ERR_INVALID_ARG, "ridge must be finite and >= 0");
   if (c->root_every < 0) return fail(OKLS_ERR_INVALID_ARG, "root_every must be >= 0 (0 means 1)");
-  if (c->method != OKLS_METHOD_OKLS && c->method != OKLS_METHOD_SHAMPOO && c->method != OKLS_METHOD_SOAP)
+  if (c->method != OKLS_METHOD_OKLS && c->method != OKLS_METHOD_SHAMPOO && c->method != OKLS_METHOD_SOAP &&
+      c->method != OKLS_METHOD_CLEAN)
     return fail(OKLS_ERR_INVALID_ARG, "method %d", c->method);
+  if (c->method == OKLS_METHOD_CLEAN) {
+    if (c->rank < 1 || c->oversample < 0 || c->power_iters < 0 || c->power_iters > 16)
+      return fail(OKLS_ERR_INVALID_ARG, "Clean needs rank >= 1, oversample >= 0, power_iters in [0, 16]");
+    const int64_t k = static_cast<int64_t>(c->rank) + c->oversample;
+    if (k > c->m || k > c->n)
+      return fail(OKLS_ERR_INVALID_ARG, "rank + oversample (%lld) exceeds min(m, n)", static_cast<long long>(k));
+    if (c->m > 128 || c->n > 128 || k > 64)
+      return fail(OKLS_ERR_UNSUPPORTED,
+                  "Clean runs for m, n <= 128 and rank + oversample <= 64 in this build (one CTA per factor)");
+  } else if (c->rank != 0 || c->oversample != 0 || c->power_iters != 0) {
+    return fail(OKLS_ERR_INVALID_ARG, "rank, oversample and power_iters are Clean's; leave them zero");
+  }
   if (c->method == OKLS_METHOD_SOAP && (c->m > 128 || c->n > 128))
     return fail(OKLS_ERR_UNSUPPORTED,
                 "SOAP runs for m, n <= 128 in this build (one-CTA eigensolver); %lld x %lld needs the blocked one",
                 static_cast<long long>(c->m), static_cast<long long>(c->n));
-  for (int i = 0; i < 6; ++i)
+  for (int i = 0; i < 3; ++i)
     if (c->reserved[i] != 0) return fail(OKLS_ERR_INVALID_ARG, "reserved fields must be zero");
   return OKLS_OK;
 }
@@ -1004,6 +1071,77 @@ okls_status soap_step(okls_handle_s* h, void* W, const void* G, float lr, cudaSt
   h->t = t1;
   return OKLS_OK;
 }
+
+CleanArgs clean_args(okls_handle_s* h) {
+  const okls_config& c = h->cfg;
+  CleanArgs A;
+  memset(&A, 0, sizeof(A));
+  A.batch = static_cast<int>(c.batch);
+  A.m = static_cast<int>(c.m);
+  A.n = static_cast<int>(c.n);
+  A.r = c.rank;
+  A.p = c.oversample;
+  A.q = c.power_iters;
+  A.UL = h->Pa;
+  A.UR = h->Pb;
+  A.lamL = h->Sa;
+  A.lamR = h->Sb;
+  A.ULn = h->ULn;
+  A.URn = h->URn;
+  A.lamLn = h->lamLn;
+  A.lamRn = h->lamRn;
+  A.Mm = h->M;
+  A.Vm = h->V;
+  A.MA = h->MA;
+  A.MB = h->MB;
+  A.vA = h->vA;
+  A.vB = h->vB;
+  A.vC = h->vC;
+  A.status = h->status;
+  return A;
+}
+
+// Clean (Algorithm 1 of the Clean page): at steps t with (t - 1) % T == 0
+// (T = root_every) both factors are re-sketched (Algorithm 3) and the moments
+// moved to the new bases (Eqns. (14)-(15)); then the block step of
+// Eqns. (10)-(13) and (16) with alpha = 1.
+okls_status clean_step(okls_handle_s* h, void* W, const void* G, float lr, const float* noise, cudaStream_t st) {
+  const okls_config& c = h->cfg;
+  const int64_t t1 = h->t + 1;
+  const int64_t every = c.root_every > 1 ? c.root_every : 1;
+  const bool refresh = (t1 - 1) % every == 0;
+  if (refresh && !noise) return fail(OKLS_ERR_INVALID_ARG, "step %lld refreshes the sketch: noise is required",
+                                     static_cast<long long>(t1));
+  if (noise && !aligned(noise, 16)) return fail(OKLS_ERR_UNSUPPORTED, "noise must be 16-byte aligned");
+  ProfScope scope(&h->prof);
+  CleanArgs A = clean_args(h);
+  A.G = G;
+  A.W = W;
+  A.g_bf16 = c.grad_dtype == OKLS_BF16;
+  A.w_bf16 = c.param_dtype == OKLS_BF16;
+  A.noise = noise;
+  A.warm = h->t > 0;
+  A.beta1 = c.beta1;
+  A.beta2 = c.beta2;
+  A.eps = c.eps;
+  A.alr = lr;
+  A.decay = static_cast<float>(1.0 - static_cast<double>(lr) * c.weight_decay * (static_cast<double>(lr) / c.lr_peak));
+  A.bc1 = static_cast<float>(1.0 / (1.0 - std::pow(static_cast<double>(c.beta1), static_cast<double>(t1))));
+  A.bc2 = static_cast<float>(1.0 / (1.0 - std::pow(static_cast<double>(c.beta2), static_cast<double>(t1))));
+  // Jacobi converges quadratically; 1e-6 relative off-diagonal is the fp32 floor
+  A.max_sweeps = 15;
+  A.tol2 = 1e-12f;
+  if (refresh) {
+    OKLS_CK(launch_clean_refresh(A, st));
+    note_kernels(2);
+  }
+  OKLS_CK(launch_clean_step(A, st));
+  note_kernels(1);
+  h->t = t1;
+  return OKLS_OK;
+}
+
+okls_status step_impl(okls_handle h, void* W, const void* G, float lr, const float* noise, void* stream);
 
 }  // namespace
 
@@ -1081,6 +1219,12 @@ okls_status okls_reset_state(okls_handle h, void* stream) {
   if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const okls_config& c = h->cfg;
+  if (c.method == OKLS_METHOD_CLEAN) {
+    OKLS_CK(cudaMemsetAsync(h->status, 0, 4, st));
+    OKLS_CK(launch_clean_reset(clean_args(h), st));
+    h->t = 0;
+    return OKLS_OK;
+  }
   if (c.method == OKLS_METHOD_SOAP) {
     OKLS_CK(cudaMemsetAsync(h->status, 0, 4, st));
     OKLS_CK(launch_soap_reset(h->M, h->V, h->Sa, h->Sb, h->Pa, h->Pb, static_cast<int>(c.batch), static_cast<int>(c.m),
@@ -1104,12 +1248,25 @@ okls_status okls_reset_state(okls_handle h, void* stream) {
 }
 
 okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* stream) {
+  return step_impl(h, W, G, lr, nullptr, stream);
+}
+
+okls_status okls_step_noise(okls_handle h, void* W, const void* G, float lr, const float* noise, void* stream) {
+  return step_impl(h, W, G, lr, noise, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+okls_status step_impl(okls_handle h, void* W, const void* G, float lr, const float* noise, void* stream) {
   if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
   if (!W || !G) return fail(OKLS_ERR_INVALID_ARG, "W or G is NULL");
   if (!aligned(W, 16) || !aligned(G, 16)) return fail(OKLS_ERR_UNSUPPORTED, "W and G must be 16-byte aligned");
   if (!finite_nonneg(lr)) return fail(OKLS_ERR_INVALID_ARG, "lr must be finite and >= 0");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const okls_config& c = h->cfg;
+  if (c.method == OKLS_METHOD_CLEAN) return clean_step(h, W, G, lr, noise, st);
   if (c.method == OKLS_METHOD_SOAP) return soap_step(h, W, G, lr, st);
   const bool shampoo = c.method == OKLS_METHOD_SHAMPOO;
   const int B = static_cast<int>(c.batch), m = static_cast<int>(c.m), n = static_cast<int>(c.n);
@@ -1300,6 +1457,10 @@ okls_status okls_step(okls_handle h, void* W, const void* G, float lr, void* str
   return OKLS_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
 okls_status okls_query_status(okls_handle h, void* stream, uint32_t* dev_status) {
   if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1315,6 +1476,26 @@ okls_status okls_query_status(okls_handle h, void* stream, uint32_t* dev_status)
 
 static okls_status part_ptr(okls_handle h, int32_t part, float** p, size_t* bytes) {
   const okls_config& c = h->cfg;
+  if (c.method == OKLS_METHOD_CLEAN) {
+    const int64_t B = c.batch, m = c.m, n = c.n, r = c.rank;
+    int64_t elems = 0;
+    switch (part) {
+      case OKLS_STATE_M: *p = h->M; elems = B * r * r; break;
+      case OKLS_STATE_V: *p = h->V; elems = B * r * r; break;
+      case OKLS_STATE_PA: *p = h->Pa; elems = B * m * r; break;
+      case OKLS_STATE_PB: *p = h->Pb; elems = B * n * r; break;
+      case OKLS_STATE_SA: *p = h->Sa; elems = B * r; break;
+      case OKLS_STATE_SB: *p = h->Sb; elems = B * r; break;
+      case OKLS_STATE_MA: *p = h->MA; elems = B * m * r; break;
+      case OKLS_STATE_MB: *p = h->MB; elems = B * r * n; break;
+      case OKLS_STATE_VA: *p = h->vA; elems = B * r; break;
+      case OKLS_STATE_VB: *p = h->vB; elems = B * r; break;
+      case OKLS_STATE_VC: *p = h->vC; elems = B; break;
+      default: return fail(OKLS_ERR_INVALID_ARG, "unknown state part %d", part);
+    }
+    *bytes = static_cast<size_t>(elems * 4);
+    return OKLS_OK;
+  }
   switch (part) {
     case OKLS_STATE_M: *p = h->M; *bytes = static_cast<size_t>(c.batch * c.m * c.n * 4); break;
     case OKLS_STATE_SA: *p = h->Sa; *bytes = static_cast<size_t>(c.batch * c.m * c.m * 4); break;
@@ -1322,7 +1503,8 @@ static okls_status part_ptr(okls_handle h, int32_t part, float** p, size_t* byte
     case OKLS_STATE_PA: *p = h->Pa; *bytes = static_cast<size_t>(c.batch * c.m * c.m * 4); break;
     case OKLS_STATE_PB: *p = h->Pb; *bytes = static_cast<size_t>(c.batch * c.n * c.n * 4); break;
     case OKLS_STATE_V:
-      if (c.method != OKLS_METHOD_SOAP) return fail(OKLS_ERR_INVALID_ARG, "state part V exists in SOAP mode only");
+      if (c.method != OKLS_METHOD_SOAP)
+        return fail(OKLS_ERR_INVALID_ARG, "state part V exists in SOAP and Clean modes only");
       *p = h->V;
       *bytes = static_cast<size_t>(c.batch * c.m * c.n * 4);
       break;
@@ -1350,7 +1532,8 @@ okls_status okls_set_state(okls_handle h, int32_t part, const void* src, void* s
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   OKLS_CK(cudaMemcpyAsync(p, src, bytes, cudaMemcpyDeviceToDevice, st));
   const okls_config& c = h->cfg;
-  if (c.method == OKLS_METHOD_SOAP) return OKLS_OK;  // the bases have no binary16 copies
+  // SOAP's and Clean's bases have no binary16 copies
+  if (c.method == OKLS_METHOD_SOAP || c.method == OKLS_METHOD_CLEAN) return OKLS_OK;
   if (part == OKLS_STATE_PA)
     OKLS_CK(launch_requant(h->Pa, static_cast<int>(c.batch), static_cast<int>(c.m), h->fa.Ph[0].p, nullptr,
                            h->fa.Ph[1].p, nullptr, h->fa.Ph[0].ld, h->fa.Ph[0].mat(), h->scal,

@@ -1,0 +1,626 @@
+// Clean (Nystrom low-rank factors with block-wise Adam) for m, n <= 128 and
+// r + p <= 64 (sm_103a).
+//
+// Page "Clean: Second-order LLM Training at Linear Memory Cost via Nystrom
+// Sketching": Algorithm 1 (the step), Eqn. (8) (the sketch A Omega of
+// b2 U Lambda U^T + (1-b2) G G^T without forming it), Appendix A Algorithm 3
+// (warm-started Nystrom with subspace iteration), Eqns. (10)-(13) and
+// Table 1 (blocks Main, A, B, C and their moments), Eqns. (14)-(15) (moments
+// moved to refreshed bases) and Eqn. (16) (the update).
+//
+// One CTA per (matrix, side) for the refresh and one per matrix for the
+// moment transport and the step; fp32 in shared memory on the CUDA cores.
+// The thin QRs are classical Gram-Schmidt applied twice (robust on the
+// ill-conditioned power-iterated sketch), the k x k Cholesky is right-looking,
+// the thin SVD of Y_nu C^-1 comes from a cyclic Jacobi eigensolve of its
+// Gram matrix, and nu is the binary32 spacing at the spectral norm of Y (the
+// working precision's eps).
+#include <cuda_bf16.h>
+
+#include "okls_internal.h"
+#include "okls_kernels.h"
+
+namespace okls {
+
+constexpr int kCMax = 128;   // m, n
+constexpr int kCK = 64;      // r + p
+constexpr int kCThreads = 256;
+constexpr int kCKld = kCK + 1;
+
+// ------------------------------------------------------------- block helpers
+__device__ __forceinline__ float c_block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float s = 0.0f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) s += red[i];
+  return s;  // every thread
+}
+
+// C (r x c, pitch ldc) = sum_k op(A)[i][k] op(B)[k][j]; ta: A stored k x r; tb: B stored c x k
+__device__ void c_mm(float* C, int ldc, const float* A, int lda, bool ta, const float* B, int ldb, bool tb, int r,
+                     int c, int k, float alpha = 1.0f, float beta = 0.0f) {
+  for (int e = threadIdx.x; e < r * c; e += blockDim.x) {
+    const int i = e / c, j = e % c;
+    float acc = 0.0f;
+    for (int q = 0; q < k; ++q) {
+      const float a = ta ? A[q * lda + i] : A[i * lda + q];
+      const float b = tb ? B[j * ldb + q] : B[q * ldb + j];
+      acc = fmaf(a, b, acc);
+    }
+    C[i * ldc + j] = beta == 0.0f ? alpha * acc : fmaf(alpha, acc, beta * C[i * ldc + j]);
+  }
+}
+
+// Orthonormalise the k columns of X (d x k, pitch ld) in place: classical
+// Gram-Schmidt twice per column; R's diagonal comes out non-negative.
+__device__ void c_qr(float* X, int ld, int d, int k, float* coef, float* red) {
+  for (int j = 0; j < k; ++j) {
+    for (int pass = 0; pass < 2; ++pass) {
+      // coef[i] = <x_i, x_j>, i < j
+      for (int i = threadIdx.x >> 5; i < j; i += blockDim.x >> 5) {
+        float s = 0.0f;
+        for (int row = threadIdx.x & 31; row < d; row += 32) s = fmaf(X[row * ld + i], X[row * ld + j], s);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if ((threadIdx.x & 31) == 0) coef[i] = s;
+      }
+      __syncthreads();
+      for (int row = threadIdx.x; row < d; row += blockDim.x) {
+        float v = X[row * ld + j];
+        for (int i = 0; i < j; ++i) v = fmaf(-coef[i], X[row * ld + i], v);
+        X[row * ld + j] = v;
+      }
+      __syncthreads();
+    }
+    float s = 0.0f;
+    for (int row = threadIdx.x; row < d; row += blockDim.x) s = fmaf(X[row * ld + j], X[row * ld + j], s);
+    const float nrm = sqrtf(c_block_sum(s, red));
+    const float inv = nrm > 0.0f ? 1.0f / nrm : 0.0f;
+    for (int row = threadIdx.x; row < d; row += blockDim.x) X[row * ld + j] *= inv;
+    __syncthreads();
+  }
+}
+
+// Eigen-decomposition of the symmetric k x k matrix A (pitch kCKld) by
+// cyclic Jacobi: A ends diagonal, V holds the eigenvectors in columns.
+__device__ void c_jacobi(float* A, float* V, int k, float* cs, int* pr, float* red, int max_sweeps, float tol2) {
+  const int dp = k + (k & 1), np = dp / 2;
+  for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
+    const int i = e / dp, j = e % dp;
+    if (i >= k || j >= k) A[i * kCKld + j] = 0.0f;
+    V[i * kCKld + j] = i == j ? 1.0f : 0.0f;
+  }
+  __syncthreads();
+  for (int sweep = 0; sweep < max_sweeps; ++sweep) {
+    float off = 0.0f, dg = 0.0f;
+    for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
+      const int i = e / dp, j = e % dp;
+      const float v = A[i * kCKld + j];
+      if (i == j)
+        dg = fmaf(v, v, dg);
+      else
+        off = fmaf(v, v, off);
+    }
+    const float offs = c_block_sum(off, red);
+    const float dgs = c_block_sum(dg, red);
+    if (!(offs > tol2 * dgs)) break;
+    for (int rd = 0; rd < dp - 1; ++rd) {
+      for (int q = threadIdx.x; q < np; q += blockDim.x) {
+        auto idx = [&](int pos) { return pos == 0 ? 0 : 1 + (pos - 1 + rd) % (dp - 1); };
+        int p = idx(q), r = idx(dp - 1 - q);
+        if (p > r) {
+          const int x = p;
+          p = r;
+          r = x;
+        }
+        const float apq = A[p * kCKld + r];
+        float c = 1.0f, s = 0.0f;
+        if (apq != 0.0f) {
+          const float th = (A[r * kCKld + r] - A[p * kCKld + p]) / (2.0f * apq);
+          const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
+          c = rsqrtf(fmaf(t, t, 1.0f));
+          s = t * c;
+        }
+        cs[2 * q] = c;
+        cs[2 * q + 1] = s;
+        pr[2 * q] = p;
+        pr[2 * q + 1] = r;
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
+        const int q = e / dp, j = e % dp;
+        const int p = pr[2 * q], r = pr[2 * q + 1];
+        const float c = cs[2 * q], s = cs[2 * q + 1];
+        const float ap = A[p * kCKld + j], ar = A[r * kCKld + j];
+        A[p * kCKld + j] = c * ap - s * ar;
+        A[r * kCKld + j] = s * ap + c * ar;
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
+        const int q = e / dp, i = e % dp;
+        const int p = pr[2 * q], r = pr[2 * q + 1];
+        const float c = cs[2 * q], s = cs[2 * q + 1];
+        const float ap = A[i * kCKld + p], ar = A[i * kCKld + r];
+        A[i * kCKld + p] = c * ap - s * ar;
+        A[i * kCKld + r] = s * ap + c * ar;
+        const float vp = V[i * kCKld + p], vr = V[i * kCKld + r];
+        V[i * kCKld + p] = c * vp - s * vr;
+        V[i * kCKld + r] = s * vp + c * vr;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// An earlier stage flagged the status word: one read per block, so that every
+// thread of the block takes the same branch.
+__device__ __forceinline__ bool c_flagged(const uint32_t* status) {
+  return __syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(status) != 0u);
+}
+
+// spacing of binary32 numbers at x > 0
+__device__ __forceinline__ float c_eps32(float x) { return x > 0.0f ? ldexpf(1.0f, ilogbf(x) - 23) : 0.0f; }
+
+template <typename GT>
+__device__ __forceinline__ float c_gload(const GT* p);
+template <>
+__device__ __forceinline__ float c_gload<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float c_gload<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// ------------------------------------------------------------------ refresh
+// Block (matrix b, side s): s = 0 sketches L (d = m), s = 1 sketches R (d = n).
+template <typename GT>
+__global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
+  extern __shared__ float sm[];
+  if (c_flagged(A.status)) return;
+  const int side = blockIdx.x < A.batch ? 0 : 1;
+  const int b = side == 0 ? blockIdx.x : blockIdx.x - A.batch;
+  const int m = A.m, n = A.n, r = A.r, k = A.r + A.p;
+  const int d = side == 0 ? m : n, o = side == 0 ? n : m;  // sketched and other dimension
+  float* Gs = sm;                         // m x n
+  float* Om = Gs + kCMax * kCMax;         // d x k (pitch kCK)
+  float* Yb = Om + kCMax * kCK;           // d x k
+  float* Tb = Yb + kCMax * kCK;           // o x k, later r x k
+  float* K1 = Tb + kCMax * kCK;           // k x k
+  float* K2 = K1 + kCK * kCKld;           // k x k
+  float* K3 = K2 + kCK * kCKld;           // k x k
+  float* vec = K3 + kCK * kCKld;          // 4 * kCK
+  float* cs = vec + 4 * kCK;              // 2 * kCK
+  int* pr = reinterpret_cast<int*>(cs + 2 * kCK);  // 2 * kCK
+  __shared__ float red[kCThreads / 32];
+  __shared__ float scal[2];
+  const GT* G = static_cast<const GT*>(A.G) + static_cast<int64_t>(b) * m * n;
+  const float* Uold = (side == 0 ? A.UL : A.UR) + static_cast<int64_t>(b) * d * r;
+  const float* lold = (side == 0 ? A.lamL : A.lamR) + static_cast<int64_t>(b) * r;
+  float* Unew = (side == 0 ? A.ULn : A.URn) + static_cast<int64_t>(b) * d * r;
+  float* lnew = (side == 0 ? A.lamLn : A.lamRn) + static_cast<int64_t>(b) * r;
+  const float* noise = A.noise + static_cast<int64_t>(b) * (m + n) * k + (side == 0 ? 0 : static_cast<int64_t>(m) * k);
+
+  for (int e = threadIdx.x; e < m * n; e += blockDim.x) Gs[e] = c_gload<GT>(G + e);
+  // Omega = [U_prev, Psi] (warm) or Psi (cold), then orthonormalised (reading c1)
+  for (int e = threadIdx.x; e < d * k; e += blockDim.x) {
+    const int i = e / k, j = e % k;
+    float v;
+    if (A.warm)
+      v = j < r ? Uold[i * r + j] : noise[i * k + (j - r)];
+    else
+      v = noise[i * k + j];
+    Om[i * kCK + j] = v;
+  }
+  __syncthreads();
+  c_qr(Om, kCK, d, k, vec, red);
+  // Y = A Omega with A = b2 U Lambda U^T + (1-b2) G G^T (L side) or G^T G (R side)
+  auto apply = [&](const float* X, float* Y) {
+    // Tb (o x k) = G^T X (L side) or G X (R side)
+    if (side == 0)
+      c_mm(Tb, kCK, Gs, n, true, X, kCK, false, o, k, d);
+    else
+      c_mm(Tb, kCK, Gs, n, false, X, kCK, false, o, k, d);
+    __syncthreads();
+    if (side == 0)
+      c_mm(Y, kCK, Gs, n, false, Tb, kCK, false, d, k, o, 1.0f - A.beta2);
+    else
+      c_mm(Y, kCK, Gs, n, true, Tb, kCK, false, d, k, o, 1.0f - A.beta2);
+    __syncthreads();
+    if (A.warm) {
+      // + b2 U (Lambda (U^T X)); Tb (r x k) = U^T X, scaled by Lambda
+      c_mm(Tb, kCK, Uold, r, true, X, kCK, false, r, k, d);
+      __syncthreads();
+      for (int e = threadIdx.x; e < r * k; e += blockDim.x) Tb[(e / k) * kCK + e % k] *= lold[e / k];
+      __syncthreads();
+      c_mm(Y, kCK, Uold, r, false, Tb, kCK, false, d, k, r, A.beta2, 1.0f);
+      __syncthreads();
+    }
+  };
+  for (int it = 0; it < A.q; ++it) {
+    apply(Om, Yb);
+    for (int e = threadIdx.x; e < d * k; e += blockDim.x) Om[(e / k) * kCK + e % k] = Yb[(e / k) * kCK + e % k];
+    __syncthreads();
+    c_qr(Om, kCK, d, k, vec, red);
+  }
+  apply(Om, Yb);
+  // nu = eps(||Y||_2): ||Y||_2^2 = largest eigenvalue of Y^T Y (power iteration)
+  c_mm(K1, kCKld, Yb, kCK, true, Yb, kCK, false, k, k, d);
+  __syncthreads();
+  for (int j = threadIdx.x; j < k; j += blockDim.x) vec[j] = 1.0f;
+  __syncthreads();
+  for (int it = 0; it < 60; ++it) {
+    for (int i = threadIdx.x; i < k; i += blockDim.x) {
+      float s = 0.0f;
+      for (int j = 0; j < k; ++j) s = fmaf(K1[i * kCKld + j], vec[j], s);
+      vec[kCK + i] = s;
+    }
+    __syncthreads();
+    float s = 0.0f;
+    for (int i = threadIdx.x; i < k; i += blockDim.x) s = fmaf(vec[kCK + i], vec[kCK + i], s);
+    const float nrm = sqrtf(c_block_sum(s, red));
+    for (int i = threadIdx.x; i < k; i += blockDim.x) vec[i] = nrm > 0.0f ? vec[kCK + i] / nrm : 0.0f;
+    if (threadIdx.x == 0) scal[0] = nrm;  // -> lambda_max of Y^T Y
+    __syncthreads();
+  }
+  const float nu = c_eps32(sqrtf(scal[0]));
+  // Y_nu = Y + nu Omega;  B = Omega^T Y_nu;  C = chol((B + B^T)/2), upper
+  for (int e = threadIdx.x; e < d * k; e += blockDim.x) {
+    const int i = e / k, j = e % k;
+    Yb[i * kCK + j] = fmaf(nu, Om[i * kCK + j], Yb[i * kCK + j]);
+  }
+  __syncthreads();
+  c_mm(K1, kCKld, Om, kCK, true, Yb, kCK, false, k, k, d);
+  __syncthreads();
+  for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
+    const int i = e / k, j = e % k;
+    K2[i * kCKld + j] = 0.5f * (K1[i * kCKld + j] + K1[j * kCKld + i]);
+  }
+  __syncthreads();
+  // right-looking Cholesky of K2 into its lower triangle: K2 = Lc Lc^T, C = Lc^T
+  bool bad = false;
+  for (int j = 0; j < k; ++j) {
+    if (threadIdx.x == 0) {
+      const float djj = K2[j * kCKld + j];
+      scal[1] = djj > 0.0f ? sqrtf(djj) : 0.0f;
+    }
+    __syncthreads();
+    const float cj = scal[1];
+    if (!(cj > 0.0f)) bad = true;
+    for (int i = j + threadIdx.x; i < k; i += blockDim.x) K2[i * kCKld + j] = i == j ? cj : (cj > 0.0f ? K2[i * kCKld + j] / cj : 0.0f);
+    __syncthreads();
+    for (int e = threadIdx.x; e < (k - j - 1) * (k - j - 1); e += blockDim.x) {
+      const int i = j + 1 + e / (k - j - 1), l = j + 1 + e % (k - j - 1);
+      if (l <= i) K2[i * kCKld + l] = fmaf(-K2[i * kCKld + j], K2[l * kCKld + j], K2[i * kCKld + l]);
+    }
+    __syncthreads();
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) atomicOr(A.status, kStNonfiniteIter);
+    return;
+  }
+  // Z = Y_nu C^-1 = Y_nu Lc^-T: row by row, z Lc^T = y (forward substitution)
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    for (int j = 0; j < k; ++j) {
+      float v = Yb[i * kCK + j];
+      for (int l = 0; l < j; ++l) v = fmaf(-Yb[i * kCK + l], K2[j * kCKld + l], v);
+      Yb[i * kCK + j] = v / K2[j * kCKld + j];
+    }
+  }
+  __syncthreads();
+  // thin SVD of Z: eigen-decomposition of Z^T Z = V Sigma^2 V^T
+  c_mm(K1, kCKld, Yb, kCK, true, Yb, kCK, false, k, k, d);
+  __syncthreads();
+  c_jacobi(K1, K3, k, cs, pr, red, A.max_sweeps, A.tol2);
+  // order by decreasing Sigma^2: rank of each eigenvalue
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const float lj = K1[j * kCKld + j];
+    int rank = 0;
+    for (int i = 0; i < k; ++i) {
+      const float li = K1[i * kCKld + i];
+      rank += (li > lj) || (li == lj && i < j);
+    }
+    pr[j] = rank;
+    vec[2 * kCK + rank] = lj;
+  }
+  __syncthreads();
+  // U[:, rank] = Z v_j / sigma_j for the r leading ranks; Lambda = max(0, Sigma^2 - nu)
+  for (int e = threadIdx.x; e < d * k; e += blockDim.x) {
+    const int i = e / k, j = e % k;
+    const int rank = pr[j];
+    if (rank >= r) continue;
+    const float s2 = K1[j * kCKld + j];
+    float v = 0.0f;
+    for (int l = 0; l < k; ++l) v = fmaf(Yb[i * kCK + l], K3[l * kCKld + j], v);
+    Tb[i * kCK + rank] = s2 > 0.0f ? v * rsqrtf(s2) : 0.0f;
+  }
+  __syncthreads();
+  // sign alignment with the previous basis (warm start)
+  for (int j = threadIdx.x; j < r; j += blockDim.x) {
+    float s = 1.0f;
+    if (A.warm) {
+      float dot = 0.0f;
+      for (int i = 0; i < d; ++i) dot = fmaf(Tb[i * kCK + j], Uold[i * r + j], dot);
+      s = dot < 0.0f ? -1.0f : 1.0f;
+    }
+    cs[j] = s;
+    lnew[j] = fmaxf(0.0f, vec[2 * kCK + j] - nu);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < d * r; e += blockDim.x) {
+    const int i = e / r, j = e % r;
+    Unew[e] = cs[j] * Tb[i * kCK + j];
+  }
+}
+
+// ------------------------------------------------------------ moment transport
+// Eqns. (14)-(15) with O_L = U_L,new^T U_L,old and O_R = U_R,old^T U_R,new;
+// then the new bases become the current ones.
+__global__ void __launch_bounds__(kCThreads) k_clean_rotate(CleanArgs A) {
+  extern __shared__ float sm[];
+  if (c_flagged(A.status)) return;
+  const int b = blockIdx.x;
+  const int m = A.m, n = A.n, r = A.r;
+  float* UL = A.UL + static_cast<int64_t>(b) * m * r;
+  float* UR = A.UR + static_cast<int64_t>(b) * n * r;
+  const float* ULn = A.ULn + static_cast<int64_t>(b) * m * r;
+  const float* URn = A.URn + static_cast<int64_t>(b) * n * r;
+  float* M = A.Mm + static_cast<int64_t>(b) * r * r;
+  float* MA = A.MA + static_cast<int64_t>(b) * m * r;
+  float* MB = A.MB + static_cast<int64_t>(b) * r * n;
+  float* vA = A.vA + static_cast<int64_t>(b) * r;
+  float* vB = A.vB + static_cast<int64_t>(b) * r;
+  float* OL = sm;                    // r x r (pitch kCKld)
+  float* OR = OL + kCK * kCKld;      // r x r
+  float* T1 = OR + kCK * kCKld;      // up to kCMax x kCK
+  float* T2 = T1 + kCMax * kCK;      // up to kCMax x kCK
+  if (A.warm) {
+    c_mm(OL, kCKld, ULn, r, true, UL, r, false, r, r, m);
+    c_mm(OR, kCKld, UR, r, true, URn, r, false, r, r, n);
+    __syncthreads();
+    // M <- O_L M O_R
+    c_mm(T1, kCK, OL, kCKld, false, M, r, false, r, r, r);
+    __syncthreads();
+    c_mm(M, r, T1, kCK, false, OR, kCKld, false, r, r, r);
+    // M_A <- (I - U_Ln U_Ln^T) M_A O_R
+    c_mm(T2, kCK, MA, r, false, OR, kCKld, false, m, r, r);
+    __syncthreads();
+    c_mm(T1, kCK, ULn, r, true, T2, kCK, false, r, r, m);  // U_Ln^T (M_A O_R)
+    __syncthreads();
+    for (int e = threadIdx.x; e < m * r; e += blockDim.x) {
+      const int i = e / r, j = e % r;
+      float v = T2[i * kCK + j];
+      for (int l = 0; l < r; ++l) v = fmaf(-ULn[i * r + l], T1[l * kCK + j], v);
+      MA[e] = v;
+    }
+    __syncthreads();
+    // M_B <- O_L M_B (I - U_Rn U_Rn^T)
+    c_mm(T2, kCMax, OL, kCKld, false, MB, n, false, r, n, r);
+    __syncthreads();
+    c_mm(T1, kCK, T2, kCMax, false, URn, r, false, r, r, n);  // (O_L M_B) U_Rn
+    __syncthreads();
+    for (int e = threadIdx.x; e < r * n; e += blockDim.x) {
+      const int i = e / n, j = e % n;
+      float v = T2[i * kCMax + j];
+      for (int l = 0; l < r; ++l) v = fmaf(-T1[i * kCK + l], URn[j * r + l], v);
+      MB[e] = v;
+    }
+    __syncthreads();
+    // v_A^T <- v_A^T (O_R)^2, v_B <- (O_L)^2 v_B
+    for (int j = threadIdx.x; j < r; j += blockDim.x) {
+      float sa = 0.0f, sb = 0.0f;
+      for (int l = 0; l < r; ++l) {
+        sa = fmaf(vA[l], OR[l * kCKld + j] * OR[l * kCKld + j], sa);
+        sb = fmaf(OL[j * kCKld + l] * OL[j * kCKld + l], vB[l], sb);
+      }
+      T1[j] = sa;
+      T1[kCK + j] = sb;
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < r; j += blockDim.x) {
+      vA[j] = T1[j];
+      vB[j] = T1[kCK + j];
+    }
+    __syncthreads();
+  }
+  // the new bases (and their eigenvalues) become current
+  for (int e = threadIdx.x; e < m * r; e += blockDim.x) UL[e] = ULn[e];
+  for (int e = threadIdx.x; e < n * r; e += blockDim.x) UR[e] = URn[e];
+  for (int j = threadIdx.x; j < r; j += blockDim.x) {
+    A.lamL[static_cast<int64_t>(b) * r + j] = A.lamLn[static_cast<int64_t>(b) * r + j];
+    A.lamR[static_cast<int64_t>(b) * r + j] = A.lamRn[static_cast<int64_t>(b) * r + j];
+  }
+}
+
+// ----------------------------------------------------------------- the step
+template <typename WT>
+__device__ __forceinline__ float c_wload(const WT* p);
+template <>
+__device__ __forceinline__ float c_wload<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float c_wload<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void c_wstore(float* p, float v) { *p = v; }
+__device__ __forceinline__ void c_wstore(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+template <typename WT, typename GT>
+__global__ void __launch_bounds__(kCThreads) k_clean_step(CleanArgs A) {
+  extern __shared__ float sm[];
+  if (c_flagged(A.status)) return;
+  const int b = blockIdx.x;
+  const int m = A.m, n = A.n, r = A.r;
+  const int64_t mn = static_cast<int64_t>(m) * n;
+  const GT* G = static_cast<const GT*>(A.G) + b * mn;
+  WT* W = static_cast<WT*>(A.W) + b * mn;
+  const float* UL = A.UL + static_cast<int64_t>(b) * m * r;
+  const float* UR = A.UR + static_cast<int64_t>(b) * n * r;
+  float* M = A.Mm + static_cast<int64_t>(b) * r * r;
+  float* V = A.Vm + static_cast<int64_t>(b) * r * r;
+  float* MA = A.MA + static_cast<int64_t>(b) * m * r;
+  float* MB = A.MB + static_cast<int64_t>(b) * r * n;
+  float* vA = A.vA + static_cast<int64_t>(b) * r;
+  float* vB = A.vB + static_cast<int64_t>(b) * r;
+  float* vC = A.vC + b;
+  float* Gs = sm;                      // G, then C
+  float* GU = Gs + kCMax * kCMax;      // G U_R (m x r), then the A block's step
+  float* UG = GU + kCMax * kCK;        // U_L^T G (r x n), then the B block's step
+  float* Ss = UG + kCK * kCMax;        // S (r x r), then the Main block's step
+  float* T1 = Ss + kCK * kCKld;        // m x r scratch
+  __shared__ float red[kCThreads / 32];
+  bool bad = false;
+  for (int e = threadIdx.x; e < mn; e += blockDim.x) {
+    const float g = c_gload<GT>(G + e);
+    bad |= !isfinite(g);
+    Gs[e] = g;
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) atomicOr(A.status, kStNonfiniteInput);
+    return;
+  }
+  c_mm(GU, kCK, Gs, n, false, UR, r, false, m, r, n);       // G U_R
+  c_mm(UG, kCMax, UL, r, true, Gs, n, false, r, n, m);      // U_L^T G
+  __syncthreads();
+  c_mm(Ss, kCKld, UL, r, true, GU, kCK, false, r, r, m);    // S = U_L^T G U_R
+  __syncthreads();
+  // G_A = G U_R - U_L S (into T1), G_B = U_L^T G - S U_R^T (in place of U_L^T G)
+  for (int e = threadIdx.x; e < m * r; e += blockDim.x) {
+    const int i = e / r, j = e % r;
+    float v = GU[i * kCK + j];
+    for (int l = 0; l < r; ++l) v = fmaf(-UL[i * r + l], Ss[l * kCKld + j], v);
+    T1[i * kCK + j] = v;
+  }
+  for (int e = threadIdx.x; e < r * n; e += blockDim.x) {
+    const int i = e / n, j = e % n;
+    float v = UG[i * kCMax + j];
+    for (int l = 0; l < r; ++l) v = fmaf(-Ss[i * kCKld + l], UR[j * r + l], v);
+    UG[i * kCMax + j] = v;
+  }
+  __syncthreads();
+  // C = (I - U_L U_L^T) G (I - U_R U_R^T) = G - U_L G_B - (G U_R) U_R^T (in place of G)
+  for (int e = threadIdx.x; e < m * n; e += blockDim.x) {
+    const int i = e / n, j = e % n;
+    float v = Gs[e];
+    for (int l = 0; l < r; ++l) {
+      v = fmaf(-UL[i * r + l], UG[l * kCMax + j], v);
+      v = fmaf(-GU[i * kCK + l], UR[j * r + l], v);
+    }
+    Gs[e] = v;
+  }
+  __syncthreads();
+  // moments (Table 1)
+  const float b1 = A.beta1, b2 = A.beta2;
+  for (int e = threadIdx.x; e < r * r; e += blockDim.x) {
+    const float s = Ss[(e / r) * kCKld + e % r];
+    M[e] = fmaf(b1, M[e], (1.0f - b1) * s);
+    V[e] = fmaf(b2, V[e], (1.0f - b2) * s * s);
+  }
+  for (int e = threadIdx.x; e < m * r; e += blockDim.x) MA[e] = fmaf(b1, MA[e], (1.0f - b1) * T1[(e / r) * kCK + e % r]);
+  for (int e = threadIdx.x; e < r * n; e += blockDim.x) MB[e] = fmaf(b1, MB[e], (1.0f - b1) * UG[(e / n) * kCMax + e % n]);
+  for (int j = threadIdx.x; j < r; j += blockDim.x) {
+    float sa = 0.0f, sb = 0.0f;
+    for (int i = 0; i < m; ++i) sa = fmaf(T1[i * kCK + j], T1[i * kCK + j], sa);
+    for (int q = 0; q < n; ++q) sb = fmaf(UG[j * kCMax + q], UG[j * kCMax + q], sb);
+    vA[j] = fmaf(b2, vA[j], (1.0f - b2) * sa);
+    vB[j] = fmaf(b2, vB[j], (1.0f - b2) * sb);
+  }
+  float sc = 0.0f;
+  for (int e = threadIdx.x; e < m * n; e += blockDim.x) sc = fmaf(Gs[e], Gs[e], sc);
+  const float cnorm2 = c_block_sum(sc, red);
+  if (threadIdx.x == 0) *vC = fmaf(b2, *vC, (1.0f - b2) * cnorm2);
+  __syncthreads();
+  // normalised blocks (bias-corrected moments)
+  const float bc1 = A.bc1, bc2 = A.bc2, eps = A.eps;
+  for (int e = threadIdx.x; e < r * r; e += blockDim.x)
+    Ss[(e / r) * kCKld + e % r] = (M[e] * bc1) / (sqrtf(V[e] * bc2) + eps);
+  for (int e = threadIdx.x; e < m * r; e += blockDim.x)
+    GU[(e / r) * kCK + e % r] = (MA[e] * bc1) / (sqrtf(vA[e % r] * bc2) + eps);
+  for (int e = threadIdx.x; e < r * n; e += blockDim.x)
+    UG[(e / n) * kCMax + e % n] = (MB[e] * bc1) / (sqrtf(vB[e / n] * bc2) + eps);
+  const float cden = 1.0f / (sqrtf(*vC * bc2) + eps);
+  __syncthreads();
+  // G~ = U_L Nm U_R^T + NA U_R^T + U_L NB + C cden;  T1 (m x r) = U_L Nm
+  c_mm(T1, kCK, UL, r, false, Ss, kCKld, false, m, r, r);
+  __syncthreads();
+  for (int e = threadIdx.x; e < mn; e += blockDim.x) {
+    const int i = e / n, j = e % n;
+    float g = Gs[e] * cden;
+    for (int l = 0; l < r; ++l) {
+      g = fmaf(T1[i * kCK + l] + GU[i * kCK + l], UR[j * r + l], g);
+      g = fmaf(UL[i * r + l], UG[l * kCMax + j], g);
+    }
+    const float w = fmaf(-A.alr, g, A.decay * c_wload<WT>(W + e));
+    bad |= !isfinite(w);
+    c_wstore(W + e, w);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(A.status, kStNonfiniteUpdate);
+}
+
+// reset: every moment zero (the bases are written by the first refresh)
+__global__ void k_clean_reset(CleanArgs A) {
+  const int b = blockIdx.x;
+  const int m = A.m, n = A.n, r = A.r;
+  for (int e = threadIdx.x; e < r * r; e += blockDim.x) {
+    A.Mm[static_cast<int64_t>(b) * r * r + e] = 0.0f;
+    A.Vm[static_cast<int64_t>(b) * r * r + e] = 0.0f;
+  }
+  for (int e = threadIdx.x; e < m * r; e += blockDim.x) A.MA[static_cast<int64_t>(b) * m * r + e] = 0.0f;
+  for (int e = threadIdx.x; e < r * n; e += blockDim.x) A.MB[static_cast<int64_t>(b) * r * n + e] = 0.0f;
+  for (int j = threadIdx.x; j < r; j += blockDim.x) {
+    A.vA[static_cast<int64_t>(b) * r + j] = 0.0f;
+    A.vB[static_cast<int64_t>(b) * r + j] = 0.0f;
+  }
+  if (threadIdx.x == 0) A.vC[b] = 0.0f;
+}
+
+constexpr int kCRefreshSmem = (kCMax * kCMax + 3 * kCMax * kCK + 3 * kCK * kCKld + 8 * kCK) * 4;
+constexpr int kCRotateSmem = (2 * kCK * kCKld + 2 * kCMax * kCK) * 4;
+constexpr int kCStepSmem = (kCMax * kCMax + 2 * kCMax * kCK + kCK * kCKld + kCMax * kCK) * 4;
+
+static cudaError_t clean_attributes() {
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || attr_dev == dev) return e;
+  const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  e = cudaFuncSetAttribute(k_clean_refresh<float>, at, kCRefreshSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_refresh<__nv_bfloat16>, at, kCRefreshSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_rotate, at, kCRotateSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<float, float>, at, kCStepSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<float, __nv_bfloat16>, at, kCStepSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<__nv_bfloat16, float>, at, kCStepSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<__nv_bfloat16, __nv_bfloat16>, at, kCStepSmem);
+  if (e == cudaSuccess) attr_dev = dev;
+  return e;
+}
+
+cudaError_t launch_clean_refresh(const CleanArgs& A, cudaStream_t st) {
+  cudaError_t e = clean_attributes();
+  if (e != cudaSuccess) return e;
+  if (A.g_bf16)
+    k_clean_refresh<__nv_bfloat16><<<2 * A.batch, kCThreads, kCRefreshSmem, st>>>(A);
+  else
+    k_clean_refresh<float><<<2 * A.batch, kCThreads, kCRefreshSmem, st>>>(A);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_clean_rotate<<<A.batch, kCThreads, kCRotateSmem, st>>>(A);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clean_step(const CleanArgs& A, cudaStream_t st) {
+  cudaError_t e = clean_attributes();
+  if (e != cudaSuccess) return e;
+  if (A.w_bf16 && A.g_bf16)
+    k_clean_step<__nv_bfloat16, __nv_bfloat16><<<A.batch, kCThreads, kCStepSmem, st>>>(A);
+  else if (A.w_bf16)
+    k_clean_step<__nv_bfloat16, float><<<A.batch, kCThreads, kCStepSmem, st>>>(A);
+  else if (A.g_bf16)
+    k_clean_step<float, __nv_bfloat16><<<A.batch, kCThreads, kCStepSmem, st>>>(A);
+  else
+    k_clean_step<float, float><<<A.batch, kCThreads, kCStepSmem, st>>>(A);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clean_reset(const CleanArgs& A, cudaStream_t st) {
+  k_clean_reset<<<A.batch, 256, 0, st>>>(A);
+  return cudaGetLastError();
+}
+
+}  // namespace okls

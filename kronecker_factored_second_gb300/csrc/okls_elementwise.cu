@@ -384,7 +384,10 @@ __device__ __forceinline__ void norm_store8(const NormaliseArgs& A, int64_t moff
 
 __global__ void __launch_bounds__(256, 3) k_normalise(NormaliseArgs A) {
   __shared__ float sm[kNT][kNTP];
-  if (A.status && *reinterpret_cast<const volatile uint32_t*>(A.status) != 0u) return;
+  // this grid raises the status word itself: one read per block keeps the
+  // early exit uniform across the block's threads
+  if (A.status && __syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(A.status) != 0u))
+    return;
   const int b = blockIdx.y;
   const int d = A.d;
   const int nt = (d + kNT - 1) / kNT;

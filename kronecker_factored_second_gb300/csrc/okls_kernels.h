@@ -84,6 +84,31 @@ cudaError_t launch_soap_refresh(const SoapRefreshArgs& A, cudaStream_t st);
 cudaError_t launch_soap_reset(float* M, float* V, float* L, float* R, float* QL, float* QR, int batch, int m, int n,
                               cudaStream_t st);
 
+// Clean (m, n <= 128, r + p <= 64): refresh (Nystrom sketches of both
+// factors, then the moments moved to the new bases), the block step, reset.
+struct CleanArgs {
+  int batch, m, n, r, p, q;
+  int warm;                          // the state holds bases from an earlier refresh
+  const void* G;                     // batch x m x n, fp32 or bf16 (g_bf16)
+  void* W;                           // batch x m x n, fp32 or bf16 (w_bf16), updated in place
+  int g_bf16, w_bf16;
+  const float* noise;                // batch x (m + n) x (r + p): Psi_L rows, then Psi_R rows
+  float *UL, *UR, *lamL, *lamR;      // state: bases (m x r, n x r) and their eigenvalues
+  float *ULn, *URn, *lamLn, *lamRn;  // workspace: the refreshed ones
+  float *Mm, *Vm;                    // Main block moments, r x r
+  float *MA, *MB;                    // A block (m x r) and B block (r x n) first moments
+  float *vA, *vB, *vC;               // pooled second moments: r, r, 1
+  float beta1, beta2, eps;
+  float alr, decay;                  // alpha lr; W <- decay W - alpha lr G~
+  float bc1, bc2;                    // 1/(1-b1^t), 1/(1-b2^t)
+  int max_sweeps;                    // Jacobi sweeps of the thin SVD
+  float tol2;
+  uint32_t* status;
+};
+cudaError_t launch_clean_refresh(const CleanArgs& A, cudaStream_t st);
+cudaError_t launch_clean_step(const CleanArgs& A, cudaStream_t st);
+cudaError_t launch_clean_reset(const CleanArgs& A, cudaStream_t st);
+
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_pair(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 

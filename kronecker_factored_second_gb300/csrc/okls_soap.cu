@@ -80,7 +80,9 @@ __device__ __forceinline__ void w_store(__nv_bfloat16* p, float v) { *p = __floa
 template <typename WT, typename GT>
 __global__ void __launch_bounds__(kSoapThreads) k_soap_step(SoapArgs A) {
   extern __shared__ float sm[];
-  if (*reinterpret_cast<const volatile uint32_t*>(A.status) != 0u) return;
+  // this grid raises the status word itself: one read per block keeps the
+  // early exit uniform across the block's threads
+  if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(A.status) != 0u)) return;
   const int b = blockIdx.x;
   const int m = A.m, n = A.n;
   const int64_t mn = static_cast<int64_t>(m) * n;

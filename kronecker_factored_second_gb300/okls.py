@@ -11,6 +11,10 @@
                    over the same kernels (method="shampoo").
 `SOAP`             Adam in the factors' eigenbasis (method="soap"; matrices up
                    to 128 x 128 in this build).
+`Clean`            block-wise Adam in Nystrom low-rank bases (method="clean";
+                   matrices up to 128 x 128 and rank + oversample <= 64 in
+                   this build); the sketch's Gaussian draws come from a
+                   torch.Generator and are passed to the library as an input.
 
 All arithmetic happens in libokls.so; nothing here computes on the CPU.
 """
@@ -50,9 +54,10 @@ class OklsBatch:
                  ns_iters: int = 10, ns_split_iters: int = 0, ns_lo: float = 1e-3,
                  ridge: float = 1e-3, variance_correction: bool = True,
                  eps_every_update: bool = True, root_every: int = 1, method: str = "okls",
-                 device=None):
+                 rank: int = 0, oversample: int = 0, power_iters: int = 0, device=None):
         lib = L.lib()
-        methods = {"okls": L.METHOD_OKLS, "shampoo": L.METHOD_SHAMPOO, "soap": L.METHOD_SOAP}
+        methods = {"okls": L.METHOD_OKLS, "shampoo": L.METHOD_SHAMPOO, "soap": L.METHOD_SOAP,
+                   "clean": L.METHOD_CLEAN}
         if method not in methods:
             raise ValueError(f"okls: method must be one of {sorted(methods)}")
         cfg = L.config_default(batch, m, n)
@@ -65,7 +70,10 @@ class OklsBatch:
         cfg.eps_every_update = int(eps_every_update)
         cfg.root_every = int(root_every)
         cfg.method = methods[method]
+        cfg.rank, cfg.oversample, cfg.power_iters = int(rank), int(oversample), int(power_iters)
         self.method = method
+        self.rank, self.oversample = int(rank), int(oversample)
+        self.root_every = max(1, int(root_every))
         self.cfg = cfg
         self.batch, self.m, self.n = batch, m, n
         self.param_dtype = param_dtype
@@ -98,14 +106,31 @@ class OklsBatch:
         L.check(L.lib().okls_reset_state(self._h, _stream(stream)))
 
     # -- the step
-    def step(self, W: torch.Tensor, G: torch.Tensor, lr: float, stream=None):
-        _require_cuda(W, G)
+    def step(self, W: torch.Tensor, G: torch.Tensor, lr: float, stream=None, noise: torch.Tensor | None = None):
+        """One step; `noise` (Clean only, fp32, `noise_shape`) holds the
+        sketch's Gaussian draws and is required when `refresh_due`."""
+        _require_cuda(W, G, noise)
         shape = (self.batch, self.m, self.n)
         if tuple(W.shape[-2:]) != shape[1:] or W.numel() != G.numel() or W.numel() != self.batch * self.m * self.n:
             raise ValueError(f"okls: expected W, G of shape {shape}")
         if W.dtype != self.param_dtype or G.dtype != self.grad_dtype:
             raise ValueError("okls: dtype mismatch")
-        L.check(L.lib().okls_step(self._h, _ptr(W), _ptr(G), float(lr), _stream(stream)))
+        if noise is None:
+            L.check(L.lib().okls_step(self._h, _ptr(W), _ptr(G), float(lr), _stream(stream)))
+            return
+        if noise.dtype != torch.float32 or tuple(noise.shape) != self.noise_shape:
+            raise ValueError(f"okls: noise must be fp32 of shape {self.noise_shape}")
+        L.check(L.lib().okls_step_noise(self._h, _ptr(W), _ptr(G), float(lr), _ptr(noise), _stream(stream)))
+
+    @property
+    def noise_shape(self) -> tuple[int, int, int]:
+        """Clean: per matrix Psi_L (m rows) then Psi_R (n rows), rank + oversample columns."""
+        return (self.batch, self.m + self.n, self.rank + self.oversample)
+
+    @property
+    def refresh_due(self) -> bool:
+        """Clean: the next step re-sketches the bases (t = 1, 1+T, ...)."""
+        return self.method == "clean" and self.t % self.root_every == 0
 
     def query_status(self, stream=None) -> int:
         """Synchronise and return (and clear) the device status word; raises
@@ -124,6 +149,11 @@ class OklsBatch:
     # -- state
     def _part_shape(self, part: int):
         B, m, n = self.batch, self.m, self.n
+        if self.method == "clean":
+            r = self.rank
+            return {L.STATE_M: (B, r, r), L.STATE_V: (B, r, r), L.STATE_PA: (B, m, r), L.STATE_PB: (B, n, r),
+                    L.STATE_SA: (B, r), L.STATE_SB: (B, r), L.STATE_MA: (B, m, r), L.STATE_MB: (B, r, n),
+                    L.STATE_VA: (B, r), L.STATE_VB: (B, r), L.STATE_VC: (B,)}[part]
         return {L.STATE_M: (B, m, n), L.STATE_SA: (B, m, m), L.STATE_SB: (B, n, n),
                 L.STATE_PA: (B, m, m), L.STATE_PB: (B, n, n), L.STATE_V: (B, m, n)}[part]
 
@@ -162,6 +192,9 @@ class OklsBatch:
 
     def _parts(self):
         parts = [("M", L.STATE_M), ("Sa", L.STATE_SA), ("Sb", L.STATE_SB), ("Pa", L.STATE_PA), ("Pb", L.STATE_PB)]
+        if self.method == "clean":
+            return parts + [("V", L.STATE_V), ("MA", L.STATE_MA), ("MB", L.STATE_MB), ("vA", L.STATE_VA),
+                            ("vB", L.STATE_VB), ("vC", L.STATE_VC)]
         return parts + [("V", L.STATE_V)] if self.method == "soap" else parts
 
     def state_dict(self) -> dict:
@@ -312,4 +345,59 @@ class SOAP(torch.optim.Optimizer):
                                            root_every=g["precondition_frequency"], method="soap",
                                            device=p.device)
                 st["okls"].step(p.data, p.grad.contiguous(), g["lr"])
+        return loss
+
+
+class Clean(torch.optim.Optimizer):
+    """Clean (Clean page, Algorithm 1) over 2-D and 3-D CUDA parameters with
+    both dimensions <= 128: block-wise Adam in rank-`rank` Nystrom bases of
+    the two Kronecker factors, re-sketched every `precondition_frequency`
+    steps with `oversample` extra Gaussian columns and `power_iters`
+    subspace iterations.  The Gaussian draws come from `generator` (a CUDA
+    torch.Generator; seeded from `seed` when not given)."""
+
+    def __init__(self, params, lr: float = 3e-3, betas=(0.95, 0.95), eps: float = 1e-8,
+                 weight_decay: float = 0.0, rank: int = 16, oversample: int = 8, power_iters: int = 1,
+                 precondition_frequency: int = 10, generator: torch.Generator | None = None, seed: int = 0):
+        defaults = dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay, rank=rank,
+                        oversample=oversample, power_iters=power_iters,
+                        precondition_frequency=precondition_frequency)
+        super().__init__(params, defaults)
+        for g in self.param_groups:
+            g.setdefault("lr_peak", g["lr"])
+        self._gen = generator
+        self._seed = seed
+
+    def _generator(self, device) -> torch.Generator:
+        if self._gen is None:
+            self._gen = torch.Generator(device=device)
+            self._gen.manual_seed(self._seed)
+        return self._gen
+
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = closure() if closure is not None else None
+        for g in self.param_groups:
+            for p in g["params"]:
+                if p.grad is None:
+                    continue
+                if p.dim() not in (2, 3):
+                    raise ValueError("Clean takes 2-D or 3-D matrix parameters only")
+                st = self.state[p]
+                if "okls" not in st:
+                    B = 1 if p.dim() == 2 else p.shape[0]
+                    m, n = p.shape[-2:]
+                    b1, b2 = g["betas"]
+                    st["okls"] = OklsBatch(B, m, n, param_dtype=p.dtype, grad_dtype=p.grad.dtype,
+                                           lr=g["lr_peak"], beta1=b1, beta2=b2, eps=g["eps"],
+                                           weight_decay=g["weight_decay"],
+                                           root_every=g["precondition_frequency"], method="clean",
+                                           rank=g["rank"], oversample=g["oversample"],
+                                           power_iters=g["power_iters"], device=p.device)
+                ob = st["okls"]
+                noise = None
+                if ob.refresh_due:
+                    noise = torch.randn(ob.noise_shape, generator=self._generator(p.device), device=p.device,
+                                        dtype=torch.float32)
+                ob.step(p.data, p.grad.contiguous(), g["lr"], noise=noise)
         return loss

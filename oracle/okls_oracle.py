@@ -678,9 +678,13 @@ def clean_init(m: int, n: int, r: int) -> CleanState:
 
 
 def clean_step(state: CleanState, W: np.ndarray, G: np.ndarray, lr: float, beta1: float, beta2: float,
-               eps: float, r: int, p: int, q: int, T: int, psiL=None, psiR=None, alpha: float = 1.0):
+               eps: float, r: int, p: int, q: int, T: int, psiL=None, psiR=None, alpha: float = 1.0,
+               bases=None):
     """One Clean step for one matrix in float64 (Algorithm 1).  psiL, psiR
-    are the Gaussian draws of a refresh step.  Returns (state, W_new, G~)."""
+    are the Gaussian draws of a refresh step.  `bases` = (U_L, Lambda_L,
+    U_R, Lambda_R), when given, stands in for Algorithm 3's output at a
+    refresh (teacher forcing: the rest of the step then runs on those
+    bases).  Returns (state, W_new, G~)."""
     G = np.asarray(G, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
     m, n = G.shape
@@ -695,8 +699,11 @@ def clean_step(state: CleanState, W: np.ndarray, G: np.ndarray, lr: float, beta1
         def aR(X, U=st.UR, lam=st.lamR):
             out = (1.0 - beta2) * (G.T @ (G @ X))
             return out + beta2 * (U @ (lam[:, None] * (U.T @ X))) if U is not None else out
-        ULn, lamLn = nystrom_warm(aL, r, p, q, st.UL, psiL)
-        URn, lamRn = nystrom_warm(aR, r, p, q, st.UR, psiR)
+        if bases is None:
+            ULn, lamLn = nystrom_warm(aL, r, p, q, st.UL, psiL)
+            URn, lamRn = nystrom_warm(aR, r, p, q, st.UR, psiR)
+        else:
+            ULn, lamLn, URn, lamRn = (np.asarray(x, dtype=np.float64) for x in bases)
         if st.UL is not None:
             # Eqns. (14)-(15): moments into the new bases
             OL = ULn.T @ st.UL            # r x r: new^T old

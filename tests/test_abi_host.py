@@ -24,7 +24,7 @@ def test_library_exports_every_header_function(lib):
     assert len(names) >= 15
     for name in names:
         assert hasattr(lib, name), name
-    assert lib.okls_abi_version() == 2
+    assert lib.okls_abi_version() == 3
 
 
 def test_header_names_match_binding():
@@ -67,7 +67,7 @@ def test_invalid_configs_rejected(lib, field, value):
 
 def test_reserved_fields_must_be_zero(lib):
     c = L.config_default(1, 64, 32)
-    c.reserved[3] = 1
+    c.reserved[2] = 1
     assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_INVALID_ARG
 
 
@@ -114,7 +114,7 @@ def test_method_is_validated_and_sizes_the_workspace(lib):
     square root per factor (all sizes here are multiples of the 256-byte
     alignment, so the difference is exact)."""
     c = L.config_default(2, 96, 40)
-    c.method = 3
+    c.method = 4
     assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_INVALID_ARG
     c.method = L.METHOD_OKLS
     s0, w0 = L.state_bytes(c)
@@ -135,3 +135,29 @@ def test_soap_shapes_and_state(lib):
     assert w < 1 << 20
     c.m = 129
     assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_UNSUPPORTED
+
+
+def test_clean_shapes_and_validation(lib):
+    """Clean keeps rank-r bases, their eigenvalues and the four blocks'
+    moments (linear in m and n); this build takes m, n <= 128 and
+    rank + oversample <= 64, and the rank fields belong to Clean alone."""
+    B, m, n, r = 3, 128, 96, 16
+    c = L.config_default(B, m, n)
+    c.method = L.METHOD_CLEAN
+    assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_INVALID_ARG  # rank 0
+    c.rank, c.oversample, c.power_iters = r, 8, 1
+    s, w = L.state_bytes(c)
+    floats = B * (m * r + n * r + 2 * r + 2 * r * r + m * r + r * n + 2 * r + 1)
+    assert 4 * floats <= s <= 4 * floats + 11 * 256
+    assert w <= 256 + 4 * B * (m * r + n * r + 2 * r) + 5 * 256
+    for field, value, code in [("rank", 0, L.OKLS_ERR_INVALID_ARG), ("oversample", -1, L.OKLS_ERR_INVALID_ARG),
+                               ("power_iters", 17, L.OKLS_ERR_INVALID_ARG),
+                               ("rank", 89, L.OKLS_ERR_INVALID_ARG),       # r + p > min(m, n)
+                               ("rank", 57, L.OKLS_ERR_UNSUPPORTED),       # r + p > 64
+                               ("m", 129, L.OKLS_ERR_UNSUPPORTED)]:
+        c2 = L.okls_config.from_buffer_copy(c)
+        setattr(c2, field, value)
+        assert lib.okls_state_bytes(ctypes.byref(c2), None, None) == code, (field, value)
+    c3 = L.config_default(B, m, n)
+    c3.rank = 4
+    assert lib.okls_state_bytes(ctypes.byref(c3), None, None) == L.OKLS_ERR_INVALID_ARG
