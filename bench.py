@@ -479,34 +479,50 @@ def run_okls(args):
                         "tflops_dense": sum_over_ranks(fs * args.steps, ws, dev) / (ms3 / 1e3) / 1e12,
                         "gemm_tflops": gt}
 
-    soap_line = None
-    if args.also_soap and args.method == "okls":
-        # SOAP runs matrices up to 128 x 128 in this build: timed on the 128 x 64 workload
+    def small_leg(method, **kw):
+        """One 128 x 64 matrix (the one-CTA methods take m, n <= 128 in this
+        build), 200 timed steps after 20 warm-up steps; Clean's Gaussian
+        draws are drawn up front and stay resident like the gradients."""
         swl = workload("single128x64")
         sgs = GradientStream(swl, dev)
         sg = swl.groups[0]
-        sob = OklsBatch(sg.batch, sg.m, sg.n, param_dtype=sg.dtype, method="soap", beta1=0.95, beta2=0.95,
-                        eps=1e-8, weight_decay=0.0, root_every=10, device=dev)
+        sob = OklsBatch(sg.batch, sg.m, sg.n, param_dtype=sg.dtype, method=method, beta1=0.95, beta2=0.95,
+                        eps=1e-8, weight_decay=0.0, root_every=10, device=dev, **kw)
         sW = sgs.init_weights(0)
         sG = [sgs.grad(0, t + 1) for t in range(4)]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(swl.seed + 17)
+        noise = [torch.randn(sob.noise_shape, generator=gen, device=dev) for _ in range(4)] \
+            if method == "clean" else None
+
+        def st(k):
+            sob.step(sW, sG[k % 4], 3e-3, noise=noise[k % 4] if noise and sob.refresh_due else None)
         for k in range(20):
-            sob.step(sW, sG[k % 4], 3e-3)
+            st(k)
         torch.cuda.synchronize()
         nsteps = 200
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for k in range(nsteps):
-            sob.step(sW, sG[k % 4], 3e-3)
+            st(k)
         b.record(stream)
         torch.cuda.synchronize()
         if sob.status_nothrow()[1]:
-            raise RuntimeError("device status flagged in the SOAP leg")
+            raise RuntimeError(f"device status flagged in the {method} leg")
         ms4 = a.elapsed_time(b)
-        soap_line = {"method": "SOAP (Adam in the factors' eigenbasis), fp32, one CTA per matrix, Jacobi refresh "
-                               "every 10 steps; matrices up to 128 x 128 in this build",
-                     "workload": "single128x64: one 128 x 64 fp32 matrix", "steps": nsteps,
-                     "value": sg.batch * nsteps / (ms4 / 1e3), "unit": "matrices/s", "ms_per_step": ms4 / nsteps}
         sob.close()
+        return {"workload": "single128x64: one 128 x 64 fp32 matrix", "steps": nsteps,
+                "value": sg.batch * nsteps / (ms4 / 1e3), "unit": "matrices/s", "ms_per_step": ms4 / nsteps}
+
+    soap_line = clean_line = None
+    if args.also_soap and args.method == "okls":
+        soap_line = {"method": "SOAP (Adam in the factors' eigenbasis), fp32, one CTA per matrix, Jacobi refresh "
+                               "every 10 steps; matrices up to 128 x 128 in this build", **small_leg("soap")}
+    if args.also_clean and args.method == "okls":
+        clean_line = {"method": "Clean (block Adam in rank-16 Nystrom bases, oversampling 8, one power iteration), "
+                                "fp32, one CTA per factor, refresh every 10 steps; matrices up to 128 x 128 and "
+                                "rank + oversampling <= 64 in this build",
+                      **small_leg("clean", rank=16, oversample=8, power_iters=1)}
 
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline:
@@ -549,6 +565,8 @@ def run_okls(args):
             line["shampoo"] = shampoo_line
         if soap_line:
             line["soap"] = soap_line
+        if clean_line:
+            line["clean"] = clean_line
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -571,6 +589,7 @@ def main():
     ap.add_argument("--also-split", type=int, default=1)
     ap.add_argument("--also-shampoo", type=int, default=1)
     ap.add_argument("--also-soap", type=int, default=1)
+    ap.add_argument("--also-clean", type=int, default=1)
     ap.add_argument("--method", choices=["okls", "shampoo", "soap"], default="okls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -5,14 +5,15 @@ Teacher-forced: every step starts the oracle from the GPU's own state.
 A refresh step is checked in two parts:
   * the sketch: the oracle's Algorithm 3 on the same Gaussian draws gives
     the reference bases and eigenvalues; the GPU's eigenvalues must match to
-    1e-4 of the largest, its bases must be orthonormal (1e-4 in Frobenius
+    1e-4 of the largest, its bases must be orthonormal (1e-5 in Frobenius
     norm over r) and every basis vector whose eigenvalue is separated from
     its neighbours by more than 1e-2 of the largest must match the oracle's
-    to 2e-3 (up to sign at the first refresh, where no previous basis fixes
-    it);
+    to 5e-4 (up to sign at the first refresh, where no previous basis fixes
+    it): fp32 Gram-Schmidt, Cholesky and Jacobi rotations, whose errors the
+    gap divides;
   * the step: the oracle's Algorithm 1 runs on the GPU's new bases (the
     `bases` hook), so the moment transport of Eqns. (14)-(15) and the four
-    blocks' moments are compared to 1e-4 (fp32 sums of up to m n terms,
+    blocks' moments are compared to 5e-5 (fp32 sums of up to m n terms,
     amplified by the cancellation in the projected blocks) of their norm
     plus an absolute floor at the blocks' rounding scale, e = 4 2^-24
     ||G||_F for a first moment and 2 ||G||_F e for a second one: where the
@@ -21,7 +22,7 @@ A refresh step is checked in two parts:
     noise on both sides.
 G~ is checked twice.  Assembly: G~ rebuilt in float64 from the GPU's own
 new state (bases, moments, and C = P_L G P_R) must match the applied update
-to 1e-4 (2e-2 with bf16 parameters: the new W rounds to 8 bits).  Against the
+to 1e-5 (2e-2 with bf16 parameters: the new W rounds to 8 bits).  Against the
 oracle: G~ is a sum of normalised units (each entry of the Main block, each
 column of N(M_A, v_A), each row of N(M_B, v_B), and C), and a unit whose
 moment m_u is small against the rounding of the G-linear terms (the e above,
@@ -49,6 +50,7 @@ PARTS = [("UL", L.STATE_PA), ("UR", L.STATE_PB), ("lamL", L.STATE_SA), ("lamR", 
          ("V", L.STATE_V), ("MA", L.STATE_MA), ("MB", L.STATE_MB), ("vA", L.STATE_VA), ("vB", L.STATE_VB),
          ("vC", L.STATE_VC)]
 MOMENTS = ("M", "V", "MA", "MB", "vA", "vB", "vC")
+MOMENT_BAR = 5e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -215,7 +217,7 @@ def test_teacher_forced_steps(B, m, n, r, p, q, T, dtype, wd, spectrum):
             for k in MOMENTS:
                 ref = np.asarray(getattr(ost, k), dtype=np.float64)
                 floor = e if k in ("M", "MA", "MB") else 2.0 * np.linalg.norm(Gd[b]) * e
-                err[k] = float(np.linalg.norm(post[k][b] - ref)) / (float(np.linalg.norm(ref)) + 1e4 * floor)
+                err[k] = float(np.linalg.norm(post[k][b] - ref)) / (float(np.linalg.norm(ref)) + floor / MOMENT_BAR)
             Ng = (decay * Wp[b] - Wn[b]) / lr
             bc1, bc2 = 1.0 / (1.0 - b1 ** t), 1.0 / (1.0 - b2 ** t)
             err["N"] = O.rel_fro(Ng, Gto)  # reported only: see the module docstring
@@ -223,19 +225,18 @@ def test_teacher_forced_steps(B, m, n, r, p, q, T, dtype, wd, spectrum):
             bound = _unit_bound(ost, post["UL"][b], post["UR"][b], Gd[b], b1, bc1, bc2, eps,
                                 2e-2 if dtype == torch.bfloat16 else 1e-4)
             err["N_units"] = float(np.linalg.norm(Ng - Gto)) / bound
-            print(f"  t={t} b={b}", {k: f"{v:.1e}" for k, v in err.items()})
             for k, v in err.items():
                 worst[k] = max(worst.get(k, 0.0), v)
     print(f"clean {B}x{m}x{n} r{r} p{p} q{q} T{T} {dtype} {spectrum}", {k: f"{v:.1e}" for k, v in worst.items()})
     for k in MOMENTS:
-        assert worst[k] < 1e-4, (k, worst)
-    assert worst["N_asm"] < (2e-2 if dtype == torch.bfloat16 else 1e-4), worst
+        assert worst[k] < MOMENT_BAR, (k, worst)
+    assert worst["N_asm"] < (2e-2 if dtype == torch.bfloat16 else 1e-5), worst
     assert worst["N_units"] <= 1.0, worst
     assert worst.get("U_same", 0.0) == 0.0
     for side in ("L", "R"):
-        assert worst[side + "_lam"] < 1e-4 and worst[side + "_orth"] < 1e-4, worst
+        assert worst[side + "_lam"] < 1e-4 and worst[side + "_orth"] < 1e-5, worst
         assert worst[side + "_order"] == 0.0, worst
-        assert worst[side + "_vec"] < 2e-3, worst
+        assert worst[side + "_vec"] < 5e-4, worst
     ob.close()
 
 
