@@ -172,7 +172,54 @@ __device__ __forceinline__ float c_gload<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float c_gload<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
+// Staged-operand pitches: odd, so that the rows a warp's 4 x 4 tiles read at
+// one k fall into distinct banks.
+constexpr int kPG = kCMax + 1;  // m x n and r x n operands
+constexpr int kPU = kCK + 1;    // m x r, n x r and r x r operands
+
+// r x c = op(A) op(B) over K = k from shared memory; each thread forms 4 x 4
+// outputs and hands each one to out(i, j, value).  Rows and columns past r,
+// c read whatever the padded buffers hold and are discarded.
+// ta: A is staged k x r; tb: B is staged c x k.
+template <class F>
+__device__ __forceinline__ void c_mm4(const float* A, int lda, bool ta, const float* B, int ldb, bool tb, int r,
+                                      int c, int k, F&& out) {
+  const int tr = (r + 3) >> 2, tcn = (c + 3) >> 2;
+  for (int blk = threadIdx.x; blk < tr * tcn; blk += blockDim.x) {
+    const int i0 = (blk / tcn) << 2, j0 = (blk % tcn) << 2;
+    float acc[4][4] = {};
+    for (int q = 0; q < k; ++q) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        av[u] = ta ? A[q * lda + i0 + u] : A[(i0 + u) * lda + q];
+        bv[u] = tb ? B[(j0 + u) * ldb + q] : B[q * ldb + j0 + u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        if (i0 + u < r && j0 + v < c) out(i0 + u, j0 + v, acc[u][v]);
+  }
+}
+
 // ------------------------------------------------------------------ refresh
+// Shared-memory plan of the refresh (floats).  The k x k region holds the
+// previous basis while the sketch is applied, then Omega^T Y_nu (Cholesky),
+// Z^T Z (Jacobi) and the eigenvectors.
+constexpr int kRG = 0;                          // G                    (m x n, pitch kPG)
+constexpr int kROm = kRG + kCMax * kPG;         // Omega                (d x k, pitch kPU)
+constexpr int kRY = kROm + kCMax * kPU;         // Y, Y_nu, Z           (d x k)
+constexpr int kRT = kRY + kCMax * kPU;          // G^T X / G X / U^T X; the new basis (d x k)
+constexpr int kRK = kRT + kCMax * kPU;          // U_prev (d x r), then K1, K2, K3 (k x k each)
+constexpr int kRVec = kRK + 3 * kCK * kPU;      // 4 kCK floats, 2 kCK floats, 2 kCK ints
+constexpr int kRefreshFloats = kRVec + 8 * kCK;
+
 // Block (matrix b, side s): s = 0 sketches L (d = m), s = 1 sketches R (d = n).
 template <typename GT>
 __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
@@ -182,15 +229,16 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   const int b = side == 0 ? blockIdx.x : blockIdx.x - A.batch;
   const int m = A.m, n = A.n, r = A.r, k = A.r + A.p;
   const int d = side == 0 ? m : n, o = side == 0 ? n : m;  // sketched and other dimension
-  float* Gs = sm;                         // m x n
-  float* Om = Gs + kCMax * kCMax;         // d x k (pitch kCK)
-  float* Yb = Om + kCMax * kCK;           // d x k
-  float* Tb = Yb + kCMax * kCK;           // o x k, later r x k
-  float* K1 = Tb + kCMax * kCK;           // k x k
-  float* K2 = K1 + kCK * kCKld;           // k x k
-  float* K3 = K2 + kCK * kCKld;           // k x k
-  float* vec = K3 + kCK * kCKld;          // 4 * kCK
-  float* cs = vec + 4 * kCK;              // 2 * kCK
+  float* Gs = sm + kRG;
+  float* Om = sm + kROm;
+  float* Yb = sm + kRY;
+  float* Tb = sm + kRT;
+  float* Us = sm + kRK;                  // U_prev while the sketch is applied
+  float* K1 = sm + kRK;
+  float* K2 = K1 + kCK * kPU;
+  float* K3 = K2 + kCK * kPU;
+  float* vec = sm + kRVec;               // 4 * kCK
+  float* cs = vec + 4 * kCK;             // 2 * kCK
   int* pr = reinterpret_cast<int*>(cs + 2 * kCK);  // 2 * kCK
   __shared__ float red[kCThreads / 32];
   __shared__ float scal[2];
@@ -201,7 +249,7 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   float* lnew = (side == 0 ? A.lamLn : A.lamRn) + static_cast<int64_t>(b) * r;
   const float* noise = A.noise + static_cast<int64_t>(b) * (m + n) * k + (side == 0 ? 0 : static_cast<int64_t>(m) * k);
 
-  for (int e = threadIdx.x; e < m * n; e += blockDim.x) Gs[e] = c_gload<GT>(G + e);
+  for (int e = threadIdx.x; e < m * n; e += blockDim.x) Gs[(e / n) * kPG + e % n] = c_gload<GT>(G + e);
   // Omega = [U_prev, Psi] (warm) or Psi (cold), then orthonormalised (reading c1)
   for (int e = threadIdx.x; e < d * k; e += blockDim.x) {
     const int i = e / k, j = e % k;
@@ -210,88 +258,98 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
       v = j < r ? Uold[i * r + j] : noise[i * k + (j - r)];
     else
       v = noise[i * k + j];
-    Om[i * kCK + j] = v;
+    Om[i * kPU + j] = v;
   }
+  if (A.warm)
+    for (int e = threadIdx.x; e < d * r; e += blockDim.x) Us[(e / r) * kPU + e % r] = Uold[e];
   __syncthreads();
-  c_qr(Om, kCK, d, k, vec, red);
-  // Y = A Omega with A = b2 U Lambda U^T + (1-b2) G G^T (L side) or G^T G (R side)
+  c_qr(Om, kPU, d, k, vec, red);
+  // Y = A X with A = b2 U Lambda U^T + (1-b2) G G^T (L side) or G^T G (R side)
+  const float w2 = 1.0f - A.beta2;
   auto apply = [&](const float* X, float* Y) {
-    // Tb (o x k) = G^T X (L side) or G X (R side)
-    if (side == 0)
-      c_mm(Tb, kCK, Gs, n, true, X, kCK, false, o, k, d);
-    else
-      c_mm(Tb, kCK, Gs, n, false, X, kCK, false, o, k, d);
-    __syncthreads();
-    if (side == 0)
-      c_mm(Y, kCK, Gs, n, false, Tb, kCK, false, d, k, o, 1.0f - A.beta2);
-    else
-      c_mm(Y, kCK, Gs, n, true, Tb, kCK, false, d, k, o, 1.0f - A.beta2);
+    if (side == 0) {
+      c_mm4(Gs, kPG, true, X, kPU, false, o, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = v; });
+      __syncthreads();
+      c_mm4(Gs, kPG, false, Tb, kPU, false, d, k, o, [&](int i, int j, float v) { Y[i * kPU + j] = w2 * v; });
+    } else {
+      c_mm4(Gs, kPG, false, X, kPU, false, o, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = v; });
+      __syncthreads();
+      c_mm4(Gs, kPG, true, Tb, kPU, false, d, k, o, [&](int i, int j, float v) { Y[i * kPU + j] = w2 * v; });
+    }
     __syncthreads();
     if (A.warm) {
-      // + b2 U (Lambda (U^T X)); Tb (r x k) = U^T X, scaled by Lambda
-      c_mm(Tb, kCK, Uold, r, true, X, kCK, false, r, k, d);
+      // + b2 U (Lambda (U^T X))
+      c_mm4(Us, kPU, true, X, kPU, false, r, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = lold[i] * v; });
       __syncthreads();
-      for (int e = threadIdx.x; e < r * k; e += blockDim.x) Tb[(e / k) * kCK + e % k] *= lold[e / k];
-      __syncthreads();
-      c_mm(Y, kCK, Uold, r, false, Tb, kCK, false, d, k, r, A.beta2, 1.0f);
+      c_mm4(Us, kPU, false, Tb, kPU, false, d, k, r,
+            [&](int i, int j, float v) { Y[i * kPU + j] = fmaf(A.beta2, v, Y[i * kPU + j]); });
       __syncthreads();
     }
   };
   for (int it = 0; it < A.q; ++it) {
     apply(Om, Yb);
-    for (int e = threadIdx.x; e < d * k; e += blockDim.x) Om[(e / k) * kCK + e % k] = Yb[(e / k) * kCK + e % k];
+    for (int e = threadIdx.x; e < d * k; e += blockDim.x) Om[(e / k) * kPU + e % k] = Yb[(e / k) * kPU + e % k];
     __syncthreads();
-    c_qr(Om, kCK, d, k, vec, red);
+    c_qr(Om, kPU, d, k, vec, red);
   }
   apply(Om, Yb);
-  // nu = eps(||Y||_2): ||Y||_2^2 = largest eigenvalue of Y^T Y (power iteration)
-  c_mm(K1, kCKld, Yb, kCK, true, Yb, kCK, false, k, k, d);
+  // nu = eps(||Y||_2): ||Y||_2^2 = largest eigenvalue of Y^T Y, by 60 power
+  // steps in one warp (k <= 64: two entries per lane, no block barriers)
+  c_mm4(Yb, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
   __syncthreads();
-  for (int j = threadIdx.x; j < k; j += blockDim.x) vec[j] = 1.0f;
-  __syncthreads();
-  for (int it = 0; it < 60; ++it) {
-    for (int i = threadIdx.x; i < k; i += blockDim.x) {
-      float s = 0.0f;
-      for (int j = 0; j < k; ++j) s = fmaf(K1[i * kCKld + j], vec[j], s);
-      vec[kCK + i] = s;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    for (int j = lane; j < k; j += 32) vec[j] = 1.0f;
+    __syncwarp();
+    float nrm = 0.0f;
+    for (int it = 0; it < 60; ++it) {
+      float s2 = 0.0f;
+      for (int i = lane; i < k; i += 32) {
+        float s = 0.0f;
+        for (int j = 0; j < k; ++j) s = fmaf(K1[i * kPU + j], vec[j], s);
+        vec[kCK + i] = s;
+        s2 = fmaf(s, s, s2);
+      }
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o2);
+      nrm = sqrtf(s2);  // -> lambda_max of Y^T Y
+      __syncwarp();
+      for (int i = lane; i < k; i += 32) vec[i] = nrm > 0.0f ? vec[kCK + i] / nrm : 0.0f;
+      __syncwarp();
     }
-    __syncthreads();
-    float s = 0.0f;
-    for (int i = threadIdx.x; i < k; i += blockDim.x) s = fmaf(vec[kCK + i], vec[kCK + i], s);
-    const float nrm = sqrtf(c_block_sum(s, red));
-    for (int i = threadIdx.x; i < k; i += blockDim.x) vec[i] = nrm > 0.0f ? vec[kCK + i] / nrm : 0.0f;
-    if (threadIdx.x == 0) scal[0] = nrm;  // -> lambda_max of Y^T Y
-    __syncthreads();
+    if (lane == 0) scal[0] = nrm;
   }
+  __syncthreads();
   const float nu = c_eps32(sqrtf(scal[0]));
   // Y_nu = Y + nu Omega;  B = Omega^T Y_nu;  C = chol((B + B^T)/2), upper
   for (int e = threadIdx.x; e < d * k; e += blockDim.x) {
     const int i = e / k, j = e % k;
-    Yb[i * kCK + j] = fmaf(nu, Om[i * kCK + j], Yb[i * kCK + j]);
+    Yb[i * kPU + j] = fmaf(nu, Om[i * kPU + j], Yb[i * kPU + j]);
   }
   __syncthreads();
-  c_mm(K1, kCKld, Om, kCK, true, Yb, kCK, false, k, k, d);
+  c_mm4(Om, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
   __syncthreads();
   for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
     const int i = e / k, j = e % k;
-    K2[i * kCKld + j] = 0.5f * (K1[i * kCKld + j] + K1[j * kCKld + i]);
+    K2[i * kPU + j] = 0.5f * (K1[i * kPU + j] + K1[j * kPU + i]);
   }
   __syncthreads();
   // right-looking Cholesky of K2 into its lower triangle: K2 = Lc Lc^T, C = Lc^T
   bool bad = false;
   for (int j = 0; j < k; ++j) {
     if (threadIdx.x == 0) {
-      const float djj = K2[j * kCKld + j];
+      const float djj = K2[j * kPU + j];
       scal[1] = djj > 0.0f ? sqrtf(djj) : 0.0f;
     }
     __syncthreads();
     const float cj = scal[1];
     if (!(cj > 0.0f)) bad = true;
-    for (int i = j + threadIdx.x; i < k; i += blockDim.x) K2[i * kCKld + j] = i == j ? cj : (cj > 0.0f ? K2[i * kCKld + j] / cj : 0.0f);
+    for (int i = j + threadIdx.x; i < k; i += blockDim.x)
+      K2[i * kPU + j] = i == j ? cj : (cj > 0.0f ? K2[i * kPU + j] / cj : 0.0f);
     __syncthreads();
     for (int e = threadIdx.x; e < (k - j - 1) * (k - j - 1); e += blockDim.x) {
       const int i = j + 1 + e / (k - j - 1), l = j + 1 + e % (k - j - 1);
-      if (l <= i) K2[i * kCKld + l] = fmaf(-K2[i * kCKld + j], K2[l * kCKld + j], K2[i * kCKld + l]);
+      if (l <= i) K2[i * kPU + l] = fmaf(-K2[i * kPU + j], K2[l * kPU + j], K2[i * kPU + l]);
     }
     __syncthreads();
   }
@@ -302,22 +360,22 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   // Z = Y_nu C^-1 = Y_nu Lc^-T: row by row, z Lc^T = y (forward substitution)
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     for (int j = 0; j < k; ++j) {
-      float v = Yb[i * kCK + j];
-      for (int l = 0; l < j; ++l) v = fmaf(-Yb[i * kCK + l], K2[j * kCKld + l], v);
-      Yb[i * kCK + j] = v / K2[j * kCKld + j];
+      float v = Yb[i * kPU + j];
+      for (int l = 0; l < j; ++l) v = fmaf(-Yb[i * kPU + l], K2[j * kPU + l], v);
+      Yb[i * kPU + j] = v / K2[j * kPU + j];
     }
   }
   __syncthreads();
   // thin SVD of Z: eigen-decomposition of Z^T Z = V Sigma^2 V^T
-  c_mm(K1, kCKld, Yb, kCK, true, Yb, kCK, false, k, k, d);
+  c_mm4(Yb, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
   __syncthreads();
   c_jacobi(K1, K3, k, cs, pr, red, A.max_sweeps, A.tol2);
   // order by decreasing Sigma^2: rank of each eigenvalue
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
-    const float lj = K1[j * kCKld + j];
+    const float lj = K1[j * kPU + j];
     int rank = 0;
     for (int i = 0; i < k; ++i) {
-      const float li = K1[i * kCKld + i];
+      const float li = K1[i * kPU + i];
       rank += (li > lj) || (li == lj && i < j);
     }
     pr[j] = rank;
@@ -325,22 +383,20 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   }
   __syncthreads();
   // U[:, rank] = Z v_j / sigma_j for the r leading ranks; Lambda = max(0, Sigma^2 - nu)
-  for (int e = threadIdx.x; e < d * k; e += blockDim.x) {
-    const int i = e / k, j = e % k;
+  c_mm4(Yb, kPU, false, K3, kPU, false, d, k, k, [&](int i, int j, float v) {
     const int rank = pr[j];
-    if (rank >= r) continue;
-    const float s2 = K1[j * kCKld + j];
-    float v = 0.0f;
-    for (int l = 0; l < k; ++l) v = fmaf(Yb[i * kCK + l], K3[l * kCKld + j], v);
-    Tb[i * kCK + rank] = s2 > 0.0f ? v * rsqrtf(s2) : 0.0f;
-  }
+    if (rank < r) {
+      const float s2 = K1[j * kPU + j];
+      Tb[i * kPU + rank] = s2 > 0.0f ? v * rsqrtf(s2) : 0.0f;
+    }
+  });
   __syncthreads();
   // sign alignment with the previous basis (warm start)
   for (int j = threadIdx.x; j < r; j += blockDim.x) {
     float s = 1.0f;
     if (A.warm) {
       float dot = 0.0f;
-      for (int i = 0; i < d; ++i) dot = fmaf(Tb[i * kCK + j], Uold[i * r + j], dot);
+      for (int i = 0; i < d; ++i) dot = fmaf(Tb[i * kPU + j], Uold[i * r + j], dot);
       s = dot < 0.0f ? -1.0f : 1.0f;
     }
     cs[j] = s;
@@ -349,7 +405,7 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   __syncthreads();
   for (int e = threadIdx.x; e < d * r; e += blockDim.x) {
     const int i = e / r, j = e % r;
-    Unew[e] = cs[j] * Tb[i * kCK + j];
+    Unew[e] = cs[j] * Tb[i * kPU + j];
   }
 }
 
@@ -442,6 +498,16 @@ __device__ __forceinline__ float c_wload<__nv_bfloat16>(const __nv_bfloat16* p) 
 __device__ __forceinline__ void c_wstore(float* p, float v) { *p = v; }
 __device__ __forceinline__ void c_wstore(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+// Shared-memory plan of the step (floats): every buffer has 4-row slack so
+// the tiles' discarded rows stay inside it.
+constexpr int kSG = 0;                         // G, then C          (m x n, pitch kPG)
+constexpr int kSUL = kSG + kCMax * kPG;        // U_L                (m x r, pitch kPU)
+constexpr int kSUR = kSUL + kCMax * kPU;       // U_R                (n x r)
+constexpr int kSGU = kSUR + kCMax * kPU;       // G U_R -> G_A -> N(M_A, v_A) -> U_L N(M, V) + N(M_A, v_A)
+constexpr int kSUG = kSGU + kCMax * kPU;       // U_L^T G -> G_B -> N(M_B, v_B)  (r x n, pitch kPG)
+constexpr int kSS = kSUG + kCK * kPG;          // S -> N(M, V)       (r x r, pitch kPU)
+constexpr int kStepFloats = kSS + kCK * kPU;
+
 template <typename WT, typename GT>
 __global__ void __launch_bounds__(kCThreads) k_clean_step(CleanArgs A) {
   extern __shared__ float sm[];
@@ -460,97 +526,94 @@ __global__ void __launch_bounds__(kCThreads) k_clean_step(CleanArgs A) {
   float* vA = A.vA + static_cast<int64_t>(b) * r;
   float* vB = A.vB + static_cast<int64_t>(b) * r;
   float* vC = A.vC + b;
-  float* Gs = sm;                      // G, then C
-  float* GU = Gs + kCMax * kCMax;      // G U_R (m x r), then the A block's step
-  float* UG = GU + kCMax * kCK;        // U_L^T G (r x n), then the B block's step
-  float* Ss = UG + kCK * kCMax;        // S (r x r), then the Main block's step
-  float* T1 = Ss + kCK * kCKld;        // m x r scratch
+  float* Gs = sm + kSG;
+  float* ULs = sm + kSUL;
+  float* URs = sm + kSUR;
+  float* GU = sm + kSGU;
+  float* UG = sm + kSUG;
+  float* Ss = sm + kSS;
   __shared__ float red[kCThreads / 32];
   bool bad = false;
   for (int e = threadIdx.x; e < mn; e += blockDim.x) {
     const float g = c_gload<GT>(G + e);
     bad |= !isfinite(g);
-    Gs[e] = g;
+    Gs[(e / n) * kPG + e % n] = g;
   }
+  for (int e = threadIdx.x; e < m * r; e += blockDim.x) ULs[(e / r) * kPU + e % r] = UL[e];
+  for (int e = threadIdx.x; e < n * r; e += blockDim.x) URs[(e / r) * kPU + e % r] = UR[e];
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0) atomicOr(A.status, kStNonfiniteInput);
     return;
   }
-  c_mm(GU, kCK, Gs, n, false, UR, r, false, m, r, n);       // G U_R
-  c_mm(UG, kCMax, UL, r, true, Gs, n, false, r, n, m);      // U_L^T G
+  // G U_R (m x r) and U_L^T G (r x n)
+  c_mm4(Gs, kPG, false, URs, kPU, false, m, r, n, [&](int i, int j, float v) { GU[i * kPU + j] = v; });
+  c_mm4(ULs, kPU, true, Gs, kPG, false, r, n, m, [&](int i, int j, float v) { UG[i * kPG + j] = v; });
   __syncthreads();
-  c_mm(Ss, kCKld, UL, r, true, GU, kCK, false, r, r, m);    // S = U_L^T G U_R
+  // S = U_L^T (G U_R)
+  c_mm4(ULs, kPU, true, GU, kPU, false, r, r, m, [&](int i, int j, float v) { Ss[i * kPU + j] = v; });
   __syncthreads();
-  // G_A = G U_R - U_L S (into T1), G_B = U_L^T G - S U_R^T (in place of U_L^T G)
-  for (int e = threadIdx.x; e < m * r; e += blockDim.x) {
-    const int i = e / r, j = e % r;
-    float v = GU[i * kCK + j];
-    for (int l = 0; l < r; ++l) v = fmaf(-UL[i * r + l], Ss[l * kCKld + j], v);
-    T1[i * kCK + j] = v;
-  }
-  for (int e = threadIdx.x; e < r * n; e += blockDim.x) {
-    const int i = e / n, j = e % n;
-    float v = UG[i * kCMax + j];
-    for (int l = 0; l < r; ++l) v = fmaf(-Ss[i * kCKld + l], UR[j * r + l], v);
-    UG[i * kCMax + j] = v;
-  }
+  // G_B = U_L^T G - S U_R^T (in place)
+  c_mm4(Ss, kPU, false, URs, kPU, true, r, n, r, [&](int i, int j, float v) { UG[i * kPG + j] -= v; });
   __syncthreads();
-  // C = (I - U_L U_L^T) G (I - U_R U_R^T) = G - U_L G_B - (G U_R) U_R^T (in place of G)
-  for (int e = threadIdx.x; e < m * n; e += blockDim.x) {
-    const int i = e / n, j = e % n;
-    float v = Gs[e];
-    for (int l = 0; l < r; ++l) {
-      v = fmaf(-UL[i * r + l], UG[l * kCMax + j], v);
-      v = fmaf(-GU[i * kCK + l], UR[j * r + l], v);
-    }
-    Gs[e] = v;
-  }
+  // C = (I - U_L U_L^T) G (I - U_R U_R^T) = G - U_L G_B - (G U_R) U_R^T, in place;
+  // both products hand each element to the same thread, which also sums ||C||^2
+  c_mm4(ULs, kPU, false, UG, kPG, false, m, n, r, [&](int i, int j, float v) { Gs[i * kPG + j] -= v; });
+  float sc = 0.0f;
+  c_mm4(GU, kPU, false, URs, kPU, true, m, n, r, [&](int i, int j, float v) {
+    const float c = Gs[i * kPG + j] - v;
+    Gs[i * kPG + j] = c;
+    sc = fmaf(c, c, sc);
+  });
+  __syncthreads();
+  // G_A = G U_R - U_L S (in place)
+  c_mm4(ULs, kPU, false, Ss, kPU, false, m, r, r, [&](int i, int j, float v) { GU[i * kPU + j] -= v; });
   __syncthreads();
   // moments (Table 1)
   const float b1 = A.beta1, b2 = A.beta2;
   for (int e = threadIdx.x; e < r * r; e += blockDim.x) {
-    const float s = Ss[(e / r) * kCKld + e % r];
+    const float s = Ss[(e / r) * kPU + e % r];
     M[e] = fmaf(b1, M[e], (1.0f - b1) * s);
     V[e] = fmaf(b2, V[e], (1.0f - b2) * s * s);
   }
-  for (int e = threadIdx.x; e < m * r; e += blockDim.x) MA[e] = fmaf(b1, MA[e], (1.0f - b1) * T1[(e / r) * kCK + e % r]);
-  for (int e = threadIdx.x; e < r * n; e += blockDim.x) MB[e] = fmaf(b1, MB[e], (1.0f - b1) * UG[(e / n) * kCMax + e % n]);
+  for (int e = threadIdx.x; e < m * r; e += blockDim.x)
+    MA[e] = fmaf(b1, MA[e], (1.0f - b1) * GU[(e / r) * kPU + e % r]);
+  for (int e = threadIdx.x; e < r * n; e += blockDim.x)
+    MB[e] = fmaf(b1, MB[e], (1.0f - b1) * UG[(e / n) * kPG + e % n]);
   for (int j = threadIdx.x; j < r; j += blockDim.x) {
     float sa = 0.0f, sb = 0.0f;
-    for (int i = 0; i < m; ++i) sa = fmaf(T1[i * kCK + j], T1[i * kCK + j], sa);
-    for (int q = 0; q < n; ++q) sb = fmaf(UG[j * kCMax + q], UG[j * kCMax + q], sb);
+    for (int i = 0; i < m; ++i) sa = fmaf(GU[i * kPU + j], GU[i * kPU + j], sa);
+    for (int q = 0; q < n; ++q) sb = fmaf(UG[j * kPG + q], UG[j * kPG + q], sb);
     vA[j] = fmaf(b2, vA[j], (1.0f - b2) * sa);
     vB[j] = fmaf(b2, vB[j], (1.0f - b2) * sb);
   }
-  float sc = 0.0f;
-  for (int e = threadIdx.x; e < m * n; e += blockDim.x) sc = fmaf(Gs[e], Gs[e], sc);
   const float cnorm2 = c_block_sum(sc, red);
   if (threadIdx.x == 0) *vC = fmaf(b2, *vC, (1.0f - b2) * cnorm2);
   __syncthreads();
-  // normalised blocks (bias-corrected moments)
+  // normalised blocks with both bias corrections, in place
   const float bc1 = A.bc1, bc2 = A.bc2, eps = A.eps;
   for (int e = threadIdx.x; e < r * r; e += blockDim.x)
-    Ss[(e / r) * kCKld + e % r] = (M[e] * bc1) / (sqrtf(V[e] * bc2) + eps);
+    Ss[(e / r) * kPU + e % r] = (M[e] * bc1) / (sqrtf(V[e] * bc2) + eps);
   for (int e = threadIdx.x; e < m * r; e += blockDim.x)
-    GU[(e / r) * kCK + e % r] = (MA[e] * bc1) / (sqrtf(vA[e % r] * bc2) + eps);
+    GU[(e / r) * kPU + e % r] = (MA[e] * bc1) / (sqrtf(vA[e % r] * bc2) + eps);
   for (int e = threadIdx.x; e < r * n; e += blockDim.x)
-    UG[(e / n) * kCMax + e % n] = (MB[e] * bc1) / (sqrtf(vB[e / n] * bc2) + eps);
+    UG[(e / n) * kPG + e % n] = (MB[e] * bc1) / (sqrtf(vB[e / n] * bc2) + eps);
   const float cden = 1.0f / (sqrtf(*vC * bc2) + eps);
   __syncthreads();
-  // G~ = U_L Nm U_R^T + NA U_R^T + U_L NB + C cden;  T1 (m x r) = U_L Nm
-  c_mm(T1, kCK, UL, r, false, Ss, kCKld, false, m, r, r);
+  // U_L N(M, V) + N(M_A, v_A), in place
+  c_mm4(ULs, kPU, false, Ss, kPU, false, m, r, r, [&](int i, int j, float v) { GU[i * kPU + j] += v; });
   __syncthreads();
-  for (int e = threadIdx.x; e < mn; e += blockDim.x) {
-    const int i = e / n, j = e % n;
-    float g = Gs[e] * cden;
-    for (int l = 0; l < r; ++l) {
-      g = fmaf(T1[i * kCK + l] + GU[i * kCK + l], UR[j * r + l], g);
-      g = fmaf(UL[i * r + l], UG[l * kCMax + j], g);
-    }
+  // G~ = C cden + (U_L N(M, V) + N(M_A, v_A)) U_R^T + U_L N(M_B, v_B), folded
+  // into W; both products hand each element to the same thread
+  c_mm4(GU, kPU, false, URs, kPU, true, m, n, r, [&](int i, int j, float v) {
+    Gs[i * kPG + j] = fmaf(Gs[i * kPG + j], cden, v);
+  });
+  c_mm4(ULs, kPU, false, UG, kPG, false, m, n, r, [&](int i, int j, float v) {
+    const float g = Gs[i * kPG + j] + v;
+    const int64_t e = static_cast<int64_t>(i) * n + j;
     const float w = fmaf(-A.alr, g, A.decay * c_wload<WT>(W + e));
     bad |= !isfinite(w);
     c_wstore(W + e, w);
-  }
+  });
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(A.status, kStNonfiniteUpdate);
 }
 
@@ -571,9 +634,9 @@ __global__ void k_clean_reset(CleanArgs A) {
   if (threadIdx.x == 0) A.vC[b] = 0.0f;
 }
 
-constexpr int kCRefreshSmem = (kCMax * kCMax + 3 * kCMax * kCK + 3 * kCK * kCKld + 8 * kCK) * 4;
+constexpr int kCRefreshSmem = kRefreshFloats * 4;
 constexpr int kCRotateSmem = (2 * kCK * kCKld + 2 * kCMax * kCK) * 4;
-constexpr int kCStepSmem = (kCMax * kCMax + 2 * kCMax * kCK + kCK * kCKld + kCMax * kCK) * 4;
+constexpr int kCStepSmem = kStepFloats * 4;
 
 static cudaError_t clean_attributes() {
   static int attr_dev = -1;
