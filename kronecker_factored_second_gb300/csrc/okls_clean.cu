@@ -19,6 +19,7 @@
 
 #include "okls_internal.h"
 #include "okls_kernels.h"
+#include "okls_tile.cuh"
 
 namespace okls {
 
@@ -177,37 +178,6 @@ __device__ __forceinline__ float c_gload<__nv_bfloat16>(const __nv_bfloat16* p) 
 constexpr int kPG = kCMax + 1;  // m x n and r x n operands
 constexpr int kPU = kCK + 1;    // m x r, n x r and r x r operands
 
-// r x c = op(A) op(B) over K = k from shared memory; each thread forms 4 x 4
-// outputs and hands each one to out(i, j, value).  Rows and columns past r,
-// c read whatever the padded buffers hold and are discarded.
-// ta: A is staged k x r; tb: B is staged c x k.
-template <class F>
-__device__ __forceinline__ void c_mm4(const float* A, int lda, bool ta, const float* B, int ldb, bool tb, int r,
-                                      int c, int k, F&& out) {
-  const int tr = (r + 3) >> 2, tcn = (c + 3) >> 2;
-  for (int blk = threadIdx.x; blk < tr * tcn; blk += blockDim.x) {
-    const int i0 = (blk / tcn) << 2, j0 = (blk % tcn) << 2;
-    float acc[4][4] = {};
-    for (int q = 0; q < k; ++q) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        av[u] = ta ? A[q * lda + i0 + u] : A[(i0 + u) * lda + q];
-        bv[u] = tb ? B[(j0 + u) * ldb + q] : B[q * ldb + j0 + u];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int v = 0; v < 4; ++v)
-        if (i0 + u < r && j0 + v < c) out(i0 + u, j0 + v, acc[u][v]);
-  }
-}
-
 // ------------------------------------------------------------------ refresh
 // Shared-memory plan of the refresh (floats).  The k x k region holds the
 // previous basis while the sketch is applied, then Omega^T Y_nu (Cholesky),
@@ -268,20 +238,20 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   const float w2 = 1.0f - A.beta2;
   auto apply = [&](const float* X, float* Y) {
     if (side == 0) {
-      c_mm4(Gs, kPG, true, X, kPU, false, o, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = v; });
+      tile_mm4(Gs, kPG, true, X, kPU, false, o, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = v; });
       __syncthreads();
-      c_mm4(Gs, kPG, false, Tb, kPU, false, d, k, o, [&](int i, int j, float v) { Y[i * kPU + j] = w2 * v; });
+      tile_mm4(Gs, kPG, false, Tb, kPU, false, d, k, o, [&](int i, int j, float v) { Y[i * kPU + j] = w2 * v; });
     } else {
-      c_mm4(Gs, kPG, false, X, kPU, false, o, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = v; });
+      tile_mm4(Gs, kPG, false, X, kPU, false, o, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = v; });
       __syncthreads();
-      c_mm4(Gs, kPG, true, Tb, kPU, false, d, k, o, [&](int i, int j, float v) { Y[i * kPU + j] = w2 * v; });
+      tile_mm4(Gs, kPG, true, Tb, kPU, false, d, k, o, [&](int i, int j, float v) { Y[i * kPU + j] = w2 * v; });
     }
     __syncthreads();
     if (A.warm) {
       // + b2 U (Lambda (U^T X))
-      c_mm4(Us, kPU, true, X, kPU, false, r, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = lold[i] * v; });
+      tile_mm4(Us, kPU, true, X, kPU, false, r, k, d, [&](int i, int j, float v) { Tb[i * kPU + j] = lold[i] * v; });
       __syncthreads();
-      c_mm4(Us, kPU, false, Tb, kPU, false, d, k, r,
+      tile_mm4(Us, kPU, false, Tb, kPU, false, d, k, r,
             [&](int i, int j, float v) { Y[i * kPU + j] = fmaf(A.beta2, v, Y[i * kPU + j]); });
       __syncthreads();
     }
@@ -295,7 +265,7 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   apply(Om, Yb);
   // nu = eps(||Y||_2): ||Y||_2^2 = largest eigenvalue of Y^T Y, by 60 power
   // steps in one warp (k <= 64: two entries per lane, no block barriers)
-  c_mm4(Yb, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
+  tile_mm4(Yb, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
   __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -327,7 +297,7 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
     Yb[i * kPU + j] = fmaf(nu, Om[i * kPU + j], Yb[i * kPU + j]);
   }
   __syncthreads();
-  c_mm4(Om, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
+  tile_mm4(Om, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
   __syncthreads();
   for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
     const int i = e / k, j = e % k;
@@ -367,7 +337,7 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   }
   __syncthreads();
   // thin SVD of Z: eigen-decomposition of Z^T Z = V Sigma^2 V^T
-  c_mm4(Yb, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
+  tile_mm4(Yb, kPU, true, Yb, kPU, false, k, k, d, [&](int i, int j, float v) { K1[i * kPU + j] = v; });
   __syncthreads();
   c_jacobi(K1, K3, k, cs, pr, red, A.max_sweeps, A.tol2);
   // order by decreasing Sigma^2: rank of each eigenvalue
@@ -383,7 +353,7 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
   }
   __syncthreads();
   // U[:, rank] = Z v_j / sigma_j for the r leading ranks; Lambda = max(0, Sigma^2 - nu)
-  c_mm4(Yb, kPU, false, K3, kPU, false, d, k, k, [&](int i, int j, float v) {
+  tile_mm4(Yb, kPU, false, K3, kPU, false, d, k, k, [&](int i, int j, float v) {
     const int rank = pr[j];
     if (rank < r) {
       const float s2 = K1[j * kPU + j];
@@ -546,27 +516,27 @@ __global__ void __launch_bounds__(kCThreads) k_clean_step(CleanArgs A) {
     return;
   }
   // G U_R (m x r) and U_L^T G (r x n)
-  c_mm4(Gs, kPG, false, URs, kPU, false, m, r, n, [&](int i, int j, float v) { GU[i * kPU + j] = v; });
-  c_mm4(ULs, kPU, true, Gs, kPG, false, r, n, m, [&](int i, int j, float v) { UG[i * kPG + j] = v; });
+  tile_mm4(Gs, kPG, false, URs, kPU, false, m, r, n, [&](int i, int j, float v) { GU[i * kPU + j] = v; });
+  tile_mm4(ULs, kPU, true, Gs, kPG, false, r, n, m, [&](int i, int j, float v) { UG[i * kPG + j] = v; });
   __syncthreads();
   // S = U_L^T (G U_R)
-  c_mm4(ULs, kPU, true, GU, kPU, false, r, r, m, [&](int i, int j, float v) { Ss[i * kPU + j] = v; });
+  tile_mm4(ULs, kPU, true, GU, kPU, false, r, r, m, [&](int i, int j, float v) { Ss[i * kPU + j] = v; });
   __syncthreads();
   // G_B = U_L^T G - S U_R^T (in place)
-  c_mm4(Ss, kPU, false, URs, kPU, true, r, n, r, [&](int i, int j, float v) { UG[i * kPG + j] -= v; });
+  tile_mm4(Ss, kPU, false, URs, kPU, true, r, n, r, [&](int i, int j, float v) { UG[i * kPG + j] -= v; });
   __syncthreads();
   // C = (I - U_L U_L^T) G (I - U_R U_R^T) = G - U_L G_B - (G U_R) U_R^T, in place;
   // both products hand each element to the same thread, which also sums ||C||^2
-  c_mm4(ULs, kPU, false, UG, kPG, false, m, n, r, [&](int i, int j, float v) { Gs[i * kPG + j] -= v; });
+  tile_mm4(ULs, kPU, false, UG, kPG, false, m, n, r, [&](int i, int j, float v) { Gs[i * kPG + j] -= v; });
   float sc = 0.0f;
-  c_mm4(GU, kPU, false, URs, kPU, true, m, n, r, [&](int i, int j, float v) {
+  tile_mm4(GU, kPU, false, URs, kPU, true, m, n, r, [&](int i, int j, float v) {
     const float c = Gs[i * kPG + j] - v;
     Gs[i * kPG + j] = c;
     sc = fmaf(c, c, sc);
   });
   __syncthreads();
   // G_A = G U_R - U_L S (in place)
-  c_mm4(ULs, kPU, false, Ss, kPU, false, m, r, r, [&](int i, int j, float v) { GU[i * kPU + j] -= v; });
+  tile_mm4(ULs, kPU, false, Ss, kPU, false, m, r, r, [&](int i, int j, float v) { GU[i * kPU + j] -= v; });
   __syncthreads();
   // moments (Table 1)
   const float b1 = A.beta1, b2 = A.beta2;
@@ -600,14 +570,14 @@ __global__ void __launch_bounds__(kCThreads) k_clean_step(CleanArgs A) {
   const float cden = 1.0f / (sqrtf(*vC * bc2) + eps);
   __syncthreads();
   // U_L N(M, V) + N(M_A, v_A), in place
-  c_mm4(ULs, kPU, false, Ss, kPU, false, m, r, r, [&](int i, int j, float v) { GU[i * kPU + j] += v; });
+  tile_mm4(ULs, kPU, false, Ss, kPU, false, m, r, r, [&](int i, int j, float v) { GU[i * kPU + j] += v; });
   __syncthreads();
   // G~ = C cden + (U_L N(M, V) + N(M_A, v_A)) U_R^T + U_L N(M_B, v_B), folded
   // into W; both products hand each element to the same thread
-  c_mm4(GU, kPU, false, URs, kPU, true, m, n, r, [&](int i, int j, float v) {
+  tile_mm4(GU, kPU, false, URs, kPU, true, m, n, r, [&](int i, int j, float v) {
     Gs[i * kPG + j] = fmaf(Gs[i * kPG + j], cden, v);
   });
-  c_mm4(ULs, kPU, false, UG, kPG, false, m, n, r, [&](int i, int j, float v) {
+  tile_mm4(ULs, kPU, false, UG, kPG, false, m, n, r, [&](int i, int j, float v) {
     const float g = Gs[i * kPG + j] + v;
     const int64_t e = static_cast<int64_t>(i) * n + j;
     const float w = fmaf(-A.alr, g, A.decay * c_wload<WT>(W + e));

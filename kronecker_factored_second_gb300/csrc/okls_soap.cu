@@ -18,6 +18,7 @@
 
 #include "okls_internal.h"
 #include "okls_kernels.h"
+#include "okls_tile.cuh"
 
 namespace okls {
 
@@ -27,7 +28,7 @@ constexpr int kSoapRefThreads = 512;
 constexpr int kSoapLd = kSoapMax + 4;                           // padded fp32 pitch (16-byte rows)
 constexpr int kSoapBuf = kSoapMax * kSoapLd;                     // floats per staged matrix
 constexpr int kSoapStepSmem = 3 * kSoapBuf * 4;                  // three staged matrices
-constexpr int kSoapRefreshSmem = 2 * kSoapMax * (kSoapMax + 1) * 4 + 4096;  // A, V (+ rotations)
+constexpr int kSoapRefreshSmem = 3 * kSoapMax * (kSoapMax + 1) * 4 + 4096;  // A, V, T (+ rotations)
 
 // Copy a rows x cols fp32 matrix (row-major, pitch cols) into shared memory.
 __device__ __forceinline__ void soap_stage(float* dst, const float* src, int rows, int cols) {
@@ -171,7 +172,7 @@ __device__ __forceinline__ int rr_index(int pos, int r, int dp) {
 
 __global__ void __launch_bounds__(kSoapRefThreads) k_soap_refresh(SoapRefreshArgs A) {
   extern __shared__ float sm[];
-  if (*reinterpret_cast<const volatile uint32_t*>(A.status) != 0u) return;
+  if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(A.status) != 0u)) return;
   const int fi = blockIdx.x < A.count ? 0 : 1;
   const int b = fi == 0 ? blockIdx.x : blockIdx.x - A.count;
   const int d = fi == 0 ? A.d0 : A.d1;
@@ -180,16 +181,47 @@ __global__ void __launch_bounds__(kSoapRefThreads) k_soap_refresh(SoapRefreshArg
   const int ld = kSoapMax + 1;
   float* As = sm;                    // the matrix being diagonalised
   float* Vs = sm + kSoapMax * ld;    // accumulated rotations (eigenvectors in columns)
-  float* cs = Vs + kSoapMax * ld;    // per pair: c, s
+  float* Ts = Vs + kSoapMax * ld;    // the polished previous basis
+  float* cs = Ts + kSoapMax * ld;    // per pair: c, s
   int* pr = reinterpret_cast<int*>(cs + kSoapMax);  // per pair: p, q
   __shared__ float red[kSoapRefThreads / 32];
   __shared__ float off_sum, diag_sum;
   const int dp = d + (d & 1);
   const int np = dp / 2;
+  // Warm start from the previous basis Q (the argument of Eigenvectors(L, Q_L)):
+  // Q^ = Q (3 I - Q^T Q) / 2 (one polar step: keeps the basis orthogonal to
+  // the fp32 floor however many refreshes it has been through), then the
+  // iteration starts from A = Q^^T S Q^ and V = Q^.  With Q = I (the first
+  // refresh) every step is exact and this is the plain Jacobi start.
+  for (int e = threadIdx.x; e < d * d; e += blockDim.x) Vs[(e / d) * ld + e % d] = Q[e];
+  __syncthreads();
+  tile_mm4(Vs, ld, true, Vs, ld, false, d, d, d,
+           [&](int i, int j, float v) { As[i * ld + j] = (i == j ? 1.5f : 0.0f) - 0.5f * v; });
+  __syncthreads();
+  tile_mm4(Vs, ld, false, As, ld, false, d, d, d, [&](int i, int j, float v) { Ts[i * ld + j] = v; });
+  __syncthreads();
+  for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
+    const int i = e / d, j = e % d;
+    As[i * ld + j] = 0.5f * (S[i * d + j] + S[j * d + i]);
+  }
+  __syncthreads();
+  tile_mm4(As, ld, false, Ts, ld, false, d, d, d, [&](int i, int j, float v) { Vs[i * ld + j] = v; });  // S Q^
+  __syncthreads();
+  tile_mm4(Ts, ld, true, Vs, ld, false, d, d, d, [&](int i, int j, float v) { As[i * ld + j] = v; });  // Q^T S Q^
+  __syncthreads();
   for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
     const int i = e / dp, j = e % dp;
-    As[i * ld + j] = (i < d && j < d) ? 0.5f * (S[i * d + j] + S[j * d + i]) : 0.0f;
-    Vs[i * ld + j] = i == j ? 1.0f : 0.0f;
+    if (i < d && j < d) {
+      if (i < j) {
+        const float v = 0.5f * (As[i * ld + j] + As[j * ld + i]);
+        As[i * ld + j] = v;
+        As[j * ld + i] = v;
+      }
+      Vs[i * ld + j] = Ts[i * ld + j];
+    } else {
+      As[i * ld + j] = 0.0f;  // the padding index of an odd d
+      Vs[i * ld + j] = i == j ? 1.0f : 0.0f;
+    }
   }
   __syncthreads();
   for (int sweep = 0; sweep < A.max_sweeps; ++sweep) {
