@@ -41,21 +41,6 @@ __device__ __forceinline__ float c_block_sum(float v, float* red) {
   return s;  // every thread
 }
 
-// C (r x c, pitch ldc) = sum_k op(A)[i][k] op(B)[k][j]; ta: A stored k x r; tb: B stored c x k
-__device__ void c_mm(float* C, int ldc, const float* A, int lda, bool ta, const float* B, int ldb, bool tb, int r,
-                     int c, int k, float alpha = 1.0f, float beta = 0.0f) {
-  for (int e = threadIdx.x; e < r * c; e += blockDim.x) {
-    const int i = e / c, j = e % c;
-    float acc = 0.0f;
-    for (int q = 0; q < k; ++q) {
-      const float a = ta ? A[q * lda + i] : A[i * lda + q];
-      const float b = tb ? B[j * ldb + q] : B[q * ldb + j];
-      acc = fmaf(a, b, acc);
-    }
-    C[i * ldc + j] = beta == 0.0f ? alpha * acc : fmaf(alpha, acc, beta * C[i * ldc + j]);
-  }
-}
-
 // Orthonormalise the k columns of X (d x k, pitch ld) in place: classical
 // Gram-Schmidt twice per column; R's diagonal comes out non-negative.
 __device__ void c_qr(float* X, int ld, int d, int k, float* coef, float* red) {
@@ -381,7 +366,16 @@ __global__ void __launch_bounds__(kCThreads) k_clean_refresh(CleanArgs A) {
 
 // ------------------------------------------------------------ moment transport
 // Eqns. (14)-(15) with O_L = U_L,new^T U_L,old and O_R = U_R,old^T U_R,new;
-// then the new bases become the current ones.
+// then the new bases become the current ones.  Shared-memory plan (floats):
+constexpr int kXBuf = kCMax * kPU;             // >= m x r (pitch kPU) and r x n (pitch kPG)
+constexpr int kXULn = 0;                       // U_L,new       (m x r, pitch kPU)
+constexpr int kXURn = kXULn + kXBuf;           // U_R,new       (n x r)
+constexpr int kXS1 = kXURn + kXBuf;            // scratch
+constexpr int kXS2 = kXS1 + kXBuf;             // scratch
+constexpr int kXOL = kXS2 + kXBuf;             // O_L           (r x r, pitch kPU)
+constexpr int kXOR = kXOL + kCK * kPU;         // O_R
+constexpr int kRotateFloats = kXOR + kCK * kPU;
+
 __global__ void __launch_bounds__(kCThreads) k_clean_rotate(CleanArgs A) {
   extern __shared__ float sm[];
   if (c_flagged(A.status)) return;
@@ -391,63 +385,70 @@ __global__ void __launch_bounds__(kCThreads) k_clean_rotate(CleanArgs A) {
   float* UR = A.UR + static_cast<int64_t>(b) * n * r;
   const float* ULn = A.ULn + static_cast<int64_t>(b) * m * r;
   const float* URn = A.URn + static_cast<int64_t>(b) * n * r;
-  float* M = A.Mm + static_cast<int64_t>(b) * r * r;
-  float* MA = A.MA + static_cast<int64_t>(b) * m * r;
-  float* MB = A.MB + static_cast<int64_t>(b) * r * n;
-  float* vA = A.vA + static_cast<int64_t>(b) * r;
-  float* vB = A.vB + static_cast<int64_t>(b) * r;
-  float* OL = sm;                    // r x r (pitch kCKld)
-  float* OR = OL + kCK * kCKld;      // r x r
-  float* T1 = OR + kCK * kCKld;      // up to kCMax x kCK
-  float* T2 = T1 + kCMax * kCK;      // up to kCMax x kCK
   if (A.warm) {
-    c_mm(OL, kCKld, ULn, r, true, UL, r, false, r, r, m);
-    c_mm(OR, kCKld, UR, r, true, URn, r, false, r, r, n);
+    float* M = A.Mm + static_cast<int64_t>(b) * r * r;
+    float* MA = A.MA + static_cast<int64_t>(b) * m * r;
+    float* MB = A.MB + static_cast<int64_t>(b) * r * n;
+    float* vA = A.vA + static_cast<int64_t>(b) * r;
+    float* vB = A.vB + static_cast<int64_t>(b) * r;
+    float* Ln = sm + kXULn;
+    float* Rn = sm + kXURn;
+    float* S1 = sm + kXS1;
+    float* S2 = sm + kXS2;
+    float* OL = sm + kXOL;
+    float* OR = sm + kXOR;
+    for (int e = threadIdx.x; e < m * r; e += blockDim.x) {
+      Ln[(e / r) * kPU + e % r] = ULn[e];
+      S1[(e / r) * kPU + e % r] = UL[e];
+    }
+    for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
+      Rn[(e / r) * kPU + e % r] = URn[e];
+      S2[(e / r) * kPU + e % r] = UR[e];
+    }
+    __syncthreads();
+    tile_mm4(Ln, kPU, true, S1, kPU, false, r, r, m, [&](int i, int j, float v) { OL[i * kPU + j] = v; });
+    tile_mm4(S2, kPU, true, Rn, kPU, false, r, r, n, [&](int i, int j, float v) { OR[i * kPU + j] = v; });
     __syncthreads();
     // M <- O_L M O_R
-    c_mm(T1, kCK, OL, kCKld, false, M, r, false, r, r, r);
+    for (int e = threadIdx.x; e < r * r; e += blockDim.x) S1[(e / r) * kPU + e % r] = M[e];
     __syncthreads();
-    c_mm(M, r, T1, kCK, false, OR, kCKld, false, r, r, r);
-    // M_A <- (I - U_Ln U_Ln^T) M_A O_R
-    c_mm(T2, kCK, MA, r, false, OR, kCKld, false, m, r, r);
+    tile_mm4(OL, kPU, false, S1, kPU, false, r, r, r, [&](int i, int j, float v) { S2[i * kPU + j] = v; });
     __syncthreads();
-    c_mm(T1, kCK, ULn, r, true, T2, kCK, false, r, r, m);  // U_Ln^T (M_A O_R)
+    tile_mm4(S2, kPU, false, OR, kPU, false, r, r, r, [&](int i, int j, float v) { M[i * r + j] = v; });
     __syncthreads();
-    for (int e = threadIdx.x; e < m * r; e += blockDim.x) {
-      const int i = e / r, j = e % r;
-      float v = T2[i * kCK + j];
-      for (int l = 0; l < r; ++l) v = fmaf(-ULn[i * r + l], T1[l * kCK + j], v);
-      MA[e] = v;
-    }
+    // M_A <- (I - U_Ln U_Ln^T) M_A O_R:  T = M_A O_R, X = U_Ln^T T, M_A = T - U_Ln X
+    for (int e = threadIdx.x; e < m * r; e += blockDim.x) S1[(e / r) * kPU + e % r] = MA[e];
     __syncthreads();
-    // M_B <- O_L M_B (I - U_Rn U_Rn^T)
-    c_mm(T2, kCMax, OL, kCKld, false, MB, n, false, r, n, r);
+    tile_mm4(S1, kPU, false, OR, kPU, false, m, r, r, [&](int i, int j, float v) { S2[i * kPU + j] = v; });
     __syncthreads();
-    c_mm(T1, kCK, T2, kCMax, false, URn, r, false, r, r, n);  // (O_L M_B) U_Rn
+    tile_mm4(Ln, kPU, true, S2, kPU, false, r, r, m, [&](int i, int j, float v) { S1[i * kPU + j] = v; });
     __syncthreads();
-    for (int e = threadIdx.x; e < r * n; e += blockDim.x) {
-      const int i = e / n, j = e % n;
-      float v = T2[i * kCMax + j];
-      for (int l = 0; l < r; ++l) v = fmaf(-T1[i * kCK + l], URn[j * r + l], v);
-      MB[e] = v;
-    }
+    tile_mm4(Ln, kPU, false, S1, kPU, false, m, r, r,
+             [&](int i, int j, float v) { MA[i * r + j] = S2[i * kPU + j] - v; });
     __syncthreads();
-    // v_A^T <- v_A^T (O_R)^2, v_B <- (O_L)^2 v_B
-    for (int j = threadIdx.x; j < r; j += blockDim.x) {
-      float sa = 0.0f, sb = 0.0f;
+    // M_B <- O_L M_B (I - U_Rn U_Rn^T):  T = O_L M_B, Y = T U_Rn, M_B = T - Y U_Rn^T
+    for (int e = threadIdx.x; e < r * n; e += blockDim.x) S1[(e / n) * kPG + e % n] = MB[e];
+    __syncthreads();
+    tile_mm4(OL, kPU, false, S1, kPG, false, r, n, r, [&](int i, int j, float v) { S2[i * kPG + j] = v; });
+    __syncthreads();
+    tile_mm4(S2, kPG, false, Rn, kPU, false, r, r, n, [&](int i, int j, float v) { S1[i * kPU + j] = v; });
+    __syncthreads();
+    tile_mm4(S1, kPU, false, Rn, kPU, true, r, n, r,
+             [&](int i, int j, float v) { MB[i * n + j] = S2[i * kPG + j] - v; });
+    // v_A^T <- v_A^T (O_R)^2, v_B <- (O_L)^2 v_B (entry-wise squares)
+    float sa = 0.0f, sb = 0.0f;
+    const int j = threadIdx.x;
+    if (j < r) {
       for (int l = 0; l < r; ++l) {
-        sa = fmaf(vA[l], OR[l * kCKld + j] * OR[l * kCKld + j], sa);
-        sb = fmaf(OL[j * kCKld + l] * OL[j * kCKld + l], vB[l], sb);
+        sa = fmaf(vA[l], OR[l * kPU + j] * OR[l * kPU + j], sa);
+        sb = fmaf(OL[j * kPU + l] * OL[j * kPU + l], vB[l], sb);
       }
-      T1[j] = sa;
-      T1[kCK + j] = sb;
     }
     __syncthreads();
-    for (int j = threadIdx.x; j < r; j += blockDim.x) {
-      vA[j] = T1[j];
-      vB[j] = T1[kCK + j];
+    if (j < r) {
+      vA[j] = sa;
+      vB[j] = sb;
     }
-    __syncthreads();
   }
   // the new bases (and their eigenvalues) become current
   for (int e = threadIdx.x; e < m * r; e += blockDim.x) UL[e] = ULn[e];
@@ -605,7 +606,7 @@ __global__ void k_clean_reset(CleanArgs A) {
 }
 
 constexpr int kCRefreshSmem = kRefreshFloats * 4;
-constexpr int kCRotateSmem = (2 * kCK * kCKld + 2 * kCMax * kCK) * 4;
+constexpr int kCRotateSmem = kRotateFloats * 4;
 constexpr int kCStepSmem = kStepFloats * 4;
 
 static cudaError_t clean_attributes() {
