@@ -22,7 +22,8 @@ A refresh step is checked in two parts:
     noise on both sides.
 G~ is checked twice.  Assembly: G~ rebuilt in float64 from the GPU's own
 new state (bases, moments, and C = P_L G P_R) must match the applied update
-to 1e-5 (2e-2 with bf16 parameters: the new W rounds to 8 bits).  Against the
+to 1e-5 (2e-2 with bf16 parameters: the new W rounds to 8 bits), plus the
+rounding floor of the C term where C itself sits at that floor.  Against the
 oracle: G~ is a sum of normalised units (each entry of the Main block, each
 column of N(M_A, v_A), each row of N(M_B, v_B), and C), and a unit whose
 moment m_u is small against the rounding of the G-linear terms (the e above,
@@ -101,7 +102,11 @@ def _check_sketch(U, lam, Uo, lamo, aligned):
 
 
 def _assemble(post, b, G, bc1, bc2, eps):
-    """G~ of Eqn. (16) from the GPU's state after the step, in float64."""
+    """G~ of Eqn. (16) from the GPU's state after the step, in float64, and
+    the allowance for its C term: C is recomputed here from G and the GPU's
+    bases, so the two differ by the rounding floor e = 4 2^-24 ||G||_F,
+    scaled by the GPU's normaliser: negligible unless C itself sits at that
+    floor (a basis spanning all of R^n), where the normalised C is noise."""
     UL, UR = post["UL"][b], post["UR"][b]
     PL = np.eye(UL.shape[0]) - UL @ UL.T
     PR = np.eye(UR.shape[0]) - UR @ UR.T
@@ -109,7 +114,10 @@ def _assemble(post, b, G, bc1, bc2, eps):
     main = (post["M"][b] * bc1) / (np.sqrt(post["V"][b] * bc2) + eps)
     bA = (post["MA"][b] * bc1) / (np.sqrt(post["vA"][b] * bc2)[None, :] + eps)
     bB = (post["MB"][b] * bc1) / (np.sqrt(post["vB"][b] * bc2)[:, None] + eps)
-    return UL @ main @ UR.T + bA @ UR.T + UL @ bB + C / (np.sqrt(post["vC"][b] * bc2) + eps)
+    cden = 1.0 / (np.sqrt(post["vC"][b] * bc2) + eps)
+    e = 4.0 * 2.0 ** -24 * np.linalg.norm(G)
+    allowance = e * cden
+    return UL @ main @ UR.T + bA @ UR.T + UL @ bB + C * cden, allowance
 
 
 def _unit_bound(ost, UL, UR, G, b1, bc1, bc2, eps, base):
@@ -151,6 +159,9 @@ CASES = [
     (2, 17, 33, 4, 3, 2, 3, torch.float32, 0.0, "iid"),
     (2, 48, 16, 12, 4, 1, 2, torch.float32, 0.0, "iid"),   # r + p = n: the right sketch spans R^n
     (2, 64, 32, 8, 8, 1, 2, torch.bfloat16, 0.0, "iid"),
+    (2, 20, 12, 1, 0, 1, 2, torch.float32, 0.0, "iid"),      # the smallest basis: r = 1, no oversampling
+    (1, 128, 128, 48, 16, 2, 2, torch.float32, 0.0, "iid"),  # the largest sketch: r + p = 64
+    (2, 9, 1, 1, 0, 1, 1, torch.float32, 0.0, "iid"),        # n = 1: U_R spans R^1, G_B and C vanish
 ]
 
 
@@ -221,7 +232,10 @@ def test_teacher_forced_steps(B, m, n, r, p, q, T, dtype, wd, spectrum):
             Ng = (decay * Wp[b] - Wn[b]) / lr
             bc1, bc2 = 1.0 / (1.0 - b1 ** t), 1.0 / (1.0 - b2 ** t)
             err["N"] = O.rel_fro(Ng, Gto)  # reported only: see the module docstring
-            err["N_asm"] = O.rel_fro(Ng, _assemble(post, b, Gd[b], bc1, bc2, eps))
+            Gasm, allow = _assemble(post, b, Gd[b], bc1, bc2, eps)
+            asm_bar = 2e-2 if dtype == torch.bfloat16 else 1e-5
+            # as a fraction of the bar: <= 1 passes
+            err["N_asm"] = float(np.linalg.norm(Ng - Gasm)) / (asm_bar * float(np.linalg.norm(Gasm)) + allow)
             bound = _unit_bound(ost, post["UL"][b], post["UR"][b], Gd[b], b1, bc1, bc2, eps,
                                 2e-2 if dtype == torch.bfloat16 else 1e-4)
             err["N_units"] = float(np.linalg.norm(Ng - Gto)) / bound
@@ -230,7 +244,7 @@ def test_teacher_forced_steps(B, m, n, r, p, q, T, dtype, wd, spectrum):
     print(f"clean {B}x{m}x{n} r{r} p{p} q{q} T{T} {dtype} {spectrum}", {k: f"{v:.1e}" for k, v in worst.items()})
     for k in MOMENTS:
         assert worst[k] < MOMENT_BAR, (k, worst)
-    assert worst["N_asm"] < (2e-2 if dtype == torch.bfloat16 else 1e-5), worst
+    assert worst["N_asm"] <= 1.0, worst
     assert worst["N_units"] <= 1.0, worst
     assert worst.get("U_same", 0.0) == 0.0
     for side in ("L", "R"):
@@ -292,4 +306,22 @@ def test_optimizer_class_matches_the_batch_api():
         ob.step(W, g, 0.01, noise=noise)
     torch.cuda.synchronize()
     assert torch.equal(p.detach(), W)
+    ob.close()
+
+
+def test_cholesky_breakdown_flags_and_leaves_w_and_state():
+    """All-zero Gaussian draws at the first refresh make the sketch, and so
+    Omega^T Y_nu, zero: the Cholesky factorisation breaks down, the status
+    word carries the iteration bit, and neither W nor the state moves."""
+    ob = _batch(2, 32, 24, rank=4, oversample=2, power_iters=1, root_every=3)
+    W = torch.randn((2, 32, 24), device="cuda") * 0.01
+    W0 = W.clone()
+    pre = _snap(ob)
+    ob.step(W, torch.randn((2, 32, 24), device="cuda"), 0.01, noise=torch.zeros(ob.noise_shape, device="cuda"))
+    code, word = ob.status_nothrow()
+    assert code == L.OKLS_ERR_NONFINITE and word & L.DEV_NONFINITE_ITER
+    assert torch.equal(W, W0)
+    post = _snap(ob)
+    for k in pre:
+        assert np.array_equal(pre[k], post[k]), k
     ob.close()
