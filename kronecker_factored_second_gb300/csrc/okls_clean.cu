@@ -9,7 +9,10 @@
 // moved to refreshed bases) and Eqn. (16) (the update).
 //
 // One CTA per (matrix, side) for the refresh and one per matrix for the
-// moment transport and the step; fp32 in shared memory on the CUDA cores.
+// moment transport and the step; fp32 in shared memory on the CUDA cores,
+// every product on staged operands with 4 x 4 register tiles (at these
+// sizes a product is at most ~1 M FMAs and the bases must be fp32-accurate,
+// so neither the tensor cores nor binary16 operands are used).
 // The thin QRs are classical Gram-Schmidt applied twice (robust on the
 // ill-conditioned power-iterated sketch), the k x k Cholesky is right-looking,
 // the thin SVD of Y_nu C^-1 comes from a cyclic Jacobi eigensolve of its
@@ -26,7 +29,10 @@ namespace okls {
 constexpr int kCMax = 128;   // m, n
 constexpr int kCK = 64;      // r + p
 constexpr int kCThreads = 256;
-constexpr int kCKld = kCK + 1;
+// Staged-operand pitches: odd, so that the rows a warp's 4 x 4 tiles read at
+// one k fall into distinct banks.
+constexpr int kPG = kCMax + 1;  // m x n and r x n operands
+constexpr int kPU = kCK + 1;    // m x r, n x r and r x r operands
 
 // ------------------------------------------------------------- block helpers
 __device__ __forceinline__ float c_block_sum(float v, float* red) {
@@ -71,21 +77,21 @@ __device__ void c_qr(float* X, int ld, int d, int k, float* coef, float* red) {
   }
 }
 
-// Eigen-decomposition of the symmetric k x k matrix A (pitch kCKld) by
+// Eigen-decomposition of the symmetric k x k matrix A (pitch kPU) by
 // cyclic Jacobi: A ends diagonal, V holds the eigenvectors in columns.
 __device__ void c_jacobi(float* A, float* V, int k, float* cs, int* pr, float* red, int max_sweeps, float tol2) {
   const int dp = k + (k & 1), np = dp / 2;
   for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
     const int i = e / dp, j = e % dp;
-    if (i >= k || j >= k) A[i * kCKld + j] = 0.0f;
-    V[i * kCKld + j] = i == j ? 1.0f : 0.0f;
+    if (i >= k || j >= k) A[i * kPU + j] = 0.0f;
+    V[i * kPU + j] = i == j ? 1.0f : 0.0f;
   }
   __syncthreads();
   for (int sweep = 0; sweep < max_sweeps; ++sweep) {
     float off = 0.0f, dg = 0.0f;
     for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
       const int i = e / dp, j = e % dp;
-      const float v = A[i * kCKld + j];
+      const float v = A[i * kPU + j];
       if (i == j)
         dg = fmaf(v, v, dg);
       else
@@ -103,10 +109,10 @@ __device__ void c_jacobi(float* A, float* V, int k, float* cs, int* pr, float* r
           p = r;
           r = x;
         }
-        const float apq = A[p * kCKld + r];
+        const float apq = A[p * kPU + r];
         float c = 1.0f, s = 0.0f;
         if (apq != 0.0f) {
-          const float th = (A[r * kCKld + r] - A[p * kCKld + p]) / (2.0f * apq);
+          const float th = (A[r * kPU + r] - A[p * kPU + p]) / (2.0f * apq);
           const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
           c = rsqrtf(fmaf(t, t, 1.0f));
           s = t * c;
@@ -121,21 +127,21 @@ __device__ void c_jacobi(float* A, float* V, int k, float* cs, int* pr, float* r
         const int q = e / dp, j = e % dp;
         const int p = pr[2 * q], r = pr[2 * q + 1];
         const float c = cs[2 * q], s = cs[2 * q + 1];
-        const float ap = A[p * kCKld + j], ar = A[r * kCKld + j];
-        A[p * kCKld + j] = c * ap - s * ar;
-        A[r * kCKld + j] = s * ap + c * ar;
+        const float ap = A[p * kPU + j], ar = A[r * kPU + j];
+        A[p * kPU + j] = c * ap - s * ar;
+        A[r * kPU + j] = s * ap + c * ar;
       }
       __syncthreads();
       for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
         const int q = e / dp, i = e % dp;
         const int p = pr[2 * q], r = pr[2 * q + 1];
         const float c = cs[2 * q], s = cs[2 * q + 1];
-        const float ap = A[i * kCKld + p], ar = A[i * kCKld + r];
-        A[i * kCKld + p] = c * ap - s * ar;
-        A[i * kCKld + r] = s * ap + c * ar;
-        const float vp = V[i * kCKld + p], vr = V[i * kCKld + r];
-        V[i * kCKld + p] = c * vp - s * vr;
-        V[i * kCKld + r] = s * vp + c * vr;
+        const float ap = A[i * kPU + p], ar = A[i * kPU + r];
+        A[i * kPU + p] = c * ap - s * ar;
+        A[i * kPU + r] = s * ap + c * ar;
+        const float vp = V[i * kPU + p], vr = V[i * kPU + r];
+        V[i * kPU + p] = c * vp - s * vr;
+        V[i * kPU + r] = s * vp + c * vr;
       }
       __syncthreads();
     }
@@ -157,11 +163,6 @@ template <>
 __device__ __forceinline__ float c_gload<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float c_gload<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-
-// Staged-operand pitches: odd, so that the rows a warp's 4 x 4 tiles read at
-// one k fall into distinct banks.
-constexpr int kPG = kCMax + 1;  // m x n and r x n operands
-constexpr int kPU = kCK + 1;    // m x r, n x r and r x r operands
 
 // ------------------------------------------------------------------ refresh
 // Shared-memory plan of the refresh (floats).  The k x k region holds the
