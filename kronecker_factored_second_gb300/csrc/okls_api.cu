@@ -797,6 +797,8 @@ struct okls_handle_s {
   // the refreshed bases of a refresh step (workspace)
   float *MA = nullptr, *MB = nullptr, *vA = nullptr, *vB = nullptr, *vC = nullptr;
   float *ULn = nullptr, *URn = nullptr, *lamLn = nullptr, *lamRn = nullptr;
+  bool clean_large = false;  // Clean past one CTA's shared memory (batched fp32 GEMMs)
+  ClLarge cl;                // its buffers (the state pointers above, plus workspace)
   float* scal = nullptr;
   uint32_t* status = nullptr;
   CUtensorMap* maps = nullptr;
@@ -812,6 +814,15 @@ namespace {
 struct Layout {
   size_t state_bytes = 0, ws_bytes = 0;
 };
+
+// Clean runs one CTA per factor while a factor's panels fit its shared
+// memory (m, n <= 128, r + p <= 64); past that, or with OKLS_CLEAN_LARGE=1,
+// the batched-GEMM path.
+bool clean_large_path(const okls_config& c) {
+  const char* e = getenv("OKLS_CLEAN_LARGE");
+  if (e && e[0] == '1') return true;
+  return c.m > 128 || c.n > 128 || c.rank + c.oversample > 64;
+}
 
 // Clean: bases U_L (m x r), U_R (n x r) and eigenvalues in P_a / P_b and
 // S_a / S_b, Main moments in M / V, the A and B block moments and the pooled
@@ -839,6 +850,34 @@ okls_status plan_clean(const okls_config& c, uint8_t* state, uint8_t* ws, okls_h
   float* URn = f32(wp, B * n * r);
   float* lamLn = f32(wp, B * r);
   float* lamRn = f32(wp, B * r);
+  const bool large = clean_large_path(c);
+  ClLarge cl;
+  memset(&cl, 0, sizeof(cl));
+  if (large) {
+    const int64_t k = static_cast<int64_t>(c.rank) + c.oversample, dmax = m > n ? m : n;
+    cl.Om = f32(wp, B * dmax * k);
+    cl.Y = f32(wp, B * dmax * k);
+    cl.X = f32(wp, B * dmax * k);
+    cl.T1 = f32(wp, B * dmax * k);
+    cl.Gram = f32(wp, B * k * k);
+    cl.Rinv = f32(wp, B * k * k);
+    cl.WU = f32(wp, B * k * r);
+    cl.P = f32(wp, B * k * r);
+    cl.nu = f32(wp, B);
+    cl.Mn = f32(wp, B * r * r);
+    cl.Sm = f32(wp, B * r * r);
+    cl.MAn = f32(wp, B * m * r);
+    cl.MBn = f32(wp, B * r * n);
+    cl.vAn = f32(wp, B * r);
+    cl.vBn = f32(wp, B * r);
+    cl.GU = f32(wp, B * m * r);
+    cl.UG = f32(wp, B * r * n);
+    cl.S = f32(wp, B * r * r);
+    cl.Nm = f32(wp, B * r * r);
+    cl.Cb = f32(wp, B * m * n);
+    cl.part = f32(wp, B * kClParts);
+    cl.cden = f32(wp, B);
+  }
   out->state_bytes = sp.off;
   out->ws_bytes = wp.off;
   if (h) {
@@ -858,6 +897,33 @@ okls_status plan_clean(const okls_config& c, uint8_t* state, uint8_t* ws, okls_h
     h->lamLn = lamLn;
     h->lamRn = lamRn;
     h->status = status;
+    h->clean_large = large;
+    if (large) {
+      cl.batch = static_cast<int>(B);
+      cl.m = static_cast<int>(m);
+      cl.n = static_cast<int>(n);
+      cl.r = c.rank;
+      cl.p = c.oversample;
+      cl.q = c.power_iters;
+      cl.k = c.rank + c.oversample;
+      cl.status = status;
+      cl.UL = UL;
+      cl.UR = UR;
+      cl.lamL = lamL;
+      cl.lamR = lamR;
+      cl.M = M;
+      cl.V = V;
+      cl.MA = MA;
+      cl.MB = MB;
+      cl.vA = vA;
+      cl.vB = vB;
+      cl.vC = vC;
+      cl.ULn = ULn;
+      cl.URn = URn;
+      cl.lamLn = lamLn;
+      cl.lamRn = lamRn;
+      h->cl = cl;
+    }
   }
   return OKLS_OK;
 }
@@ -1001,9 +1067,9 @@ okls_status validate(const okls_config* c) {
     const int64_t k = static_cast<int64_t>(c->rank) + c->oversample;
     if (k > c->m || k > c->n)
       return fail(OKLS_ERR_INVALID_ARG, "rank + oversample (%lld) exceeds min(m, n)", static_cast<long long>(k));
-    if (c->m > 128 || c->n > 128 || k > 64)
+    if (c->m > 16384 || c->n > 16384 || k > 128)
       return fail(OKLS_ERR_UNSUPPORTED,
-                  "Clean runs for m, n <= 128 and rank + oversample <= 64 in this build (one CTA per factor)");
+                  "Clean runs for m, n <= 16384 and rank + oversample <= 128 in this build (k x k work in one CTA)");
   } else if (c->rank != 0 || c->oversample != 0 || c->power_iters != 0) {
     return fail(OKLS_ERR_INVALID_ARG, "rank, oversample and power_iters are Clean's; leave them zero");
   }
@@ -1131,6 +1197,30 @@ okls_status clean_step(okls_handle_s* h, void* W, const void* G, float lr, const
   // Jacobi converges quadratically; 1e-6 relative off-diagonal is the fp32 floor
   A.max_sweeps = 15;
   A.tol2 = 1e-12f;
+  if (h->clean_large) {
+    ClLarge L = h->cl;
+    L.warm = A.warm;
+    L.beta1 = A.beta1;
+    L.beta2 = A.beta2;
+    L.eps = A.eps;
+    L.alr = A.alr;
+    L.decay = A.decay;
+    L.bc1 = A.bc1;
+    L.bc2 = A.bc2;
+    L.max_sweeps = A.max_sweeps;
+    L.tol2 = A.tol2;
+    L.G = G;
+    L.W = W;
+    L.g_bf16 = A.g_bf16;
+    L.w_bf16 = A.w_bf16;
+    L.noise = noise;
+    int launches = 0;
+    if (refresh) OKLS_CK(clean_large_refresh(L, st, &launches));
+    OKLS_CK(clean_large_step(L, st, &launches));
+    note_kernels(launches);
+    h->t = t1;
+    return OKLS_OK;
+  }
   if (refresh) {
     OKLS_CK(launch_clean_refresh(A, st));
     note_kernels(2);

@@ -1,0 +1,802 @@
+// Clean for shapes past one CTA's shared memory: m, n up to 16384 and
+// r + p <= 128 (sm_103a).
+//
+// Page "Clean: Second-order LLM Training at Linear Memory Cost via Nystrom
+// Sketching": Algorithm 1, Eqn. (8), Appendix A Algorithm 3, Eqns. (10)-(16),
+// Table 1 -- the same method as the one-CTA kernels, restated for tall
+// operands.  Every product with a dimension that grows with m or n is a
+// batched fp32 GEMM (`cl_gemm`: 64 x 64 tiles, 4 x 4 per thread, both
+// operands staged in shared memory); only k x k work (k = r + p) stays in
+// one CTA per matrix: the Cholesky factors and inverses of the thin QRs and
+// of Omega^T Y_nu, the norm estimate for nu, and the Jacobi eigensolve of
+// Z^T Z that yields the thin SVD.  The thin QRs are Cholesky-QR applied four
+// times, a pass shifted where its factorisation breaks down (the
+// power-iterated sketch is ill-conditioned), so they reduce to Gram
+// products, k x k factorisations and products again.
+#include <cuda_bf16.h>
+
+#include "okls_internal.h"
+#include "okls_kernels.h"
+
+namespace okls {
+
+// ---------------------------------------------------------------- the GEMM
+constexpr int kGT = 64;       // output tile edge
+constexpr int kGK = 16;       // K per stage
+constexpr int kGP = kGT + 4;  // staged pitch (16-byte rows)
+
+template <typename T>
+__device__ __forceinline__ float cl_ld(const T* p);
+template <>
+__device__ __forceinline__ float cl_ld<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float cl_ld<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// C[b] = alpha op(A[b]) op(B[b]) + beta_b C[b], beta_b = beta_dev ? beta_dev[b] : beta.
+// A is M x K (lda), or K x M when ta; B is K x N (ldb), or N x K when tb.
+template <typename TA, typename TB>
+__global__ void __launch_bounds__(256) k_cl_gemm(ClGemm g) {
+  __shared__ __align__(16) float As[kGK][kGP];
+  __shared__ __align__(16) float Bs[kGK][kGP];
+  const int b = blockIdx.z;
+  const TA* A = static_cast<const TA*>(g.A) + static_cast<int64_t>(b) * g.sA;
+  const TB* B = static_cast<const TB*>(g.B) + static_cast<int64_t>(b) * g.sB;
+  float* C = g.C + static_cast<int64_t>(b) * g.sC;
+  const int m0 = blockIdx.y * kGT, n0 = blockIdx.x * kGT;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < g.K; k0 += kGK) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int e = threadIdx.x + 256 * s;
+      // A tile (kGT rows of M, kGK of K) into As[k][m]
+      int i, kk;
+      if (g.ta) {
+        kk = e >> 6;
+        i = e & 63;
+      } else {
+        i = e >> 4;
+        kk = e & 15;
+      }
+      const int gm = m0 + i, gk = k0 + kk;
+      float va = 0.0f;
+      if (gm < g.M && gk < g.K)
+        va = cl_ld<TA>(g.ta ? A + static_cast<int64_t>(gk) * g.lda + gm : A + static_cast<int64_t>(gm) * g.lda + gk);
+      As[kk][i] = va;
+      // B tile (kGK of K, kGT columns of N) into Bs[k][n]
+      int j, kb;
+      if (g.tb) {
+        j = e >> 4;
+        kb = e & 15;
+      } else {
+        kb = e >> 6;
+        j = e & 63;
+      }
+      const int gn = n0 + j, gkb = k0 + kb;
+      float vb = 0.0f;
+      if (gn < g.N && gkb < g.K)
+        vb = cl_ld<TB>(g.tb ? B + static_cast<int64_t>(gn) * g.ldb + gkb : B + static_cast<int64_t>(gkb) * g.ldb + gn);
+      Bs[kb][j] = vb;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kGK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 bq = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+    }
+    __syncthreads();
+  }
+  const float beta = g.beta_dev ? g.beta_dev[b] : g.beta;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int gm = m0 + ty * 4 + u;
+    if (gm >= g.M) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int gn = n0 + tx * 4 + v;
+      if (gn >= g.N) continue;
+      float* c = C + static_cast<int64_t>(gm) * g.ldc + gn;
+      *c = beta == 0.0f ? g.alpha * acc[u][v] : fmaf(g.alpha, acc[u][v], beta * *c);
+    }
+  }
+}
+
+
+// ------------------------------------------------------------- k x k kernels
+constexpr int kLK = 128;           // largest k = r + p
+constexpr int kLP = kLK + 1;       // odd pitch of the staged k x k matrices
+constexpr int kLThreads = 256;
+constexpr int kLSmallSmem = 2 * kLK * kLP * 4 + 4 * kLK * 4;
+
+__device__ __forceinline__ bool cl_flagged(const uint32_t* status) {
+  return __syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(status) != 0u);
+}
+
+__device__ __forceinline__ float cl_block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float s = 0.0f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) s += red[i];
+  return s;
+}
+
+// Cholesky factor of the symmetric part of a k x k Gram matrix and the
+// inverse of its upper factor R = L^T: Rinv = L^-T, so that X Rinv has
+// orthonormal columns when Gram = X^T X.  With `adaptive` a breakdown (a
+// pivot that is not positive: the panel's condition number squared has
+// passed 2^24) restarts the factorisation with the diagonal shifted by
+// 11 (k + sqrt(d)) 2^-24 trace(Gram), above the rounding error of the Gram
+// product -- shifted Cholesky-QR, which trades a well-conditioned factor for
+// a partial orthogonalisation that the next pass completes.  A breakdown
+// that remains raises kStNonfiniteIter.
+__global__ void __launch_bounds__(kLThreads) k_cl_chol_inv(const float* Gram, float* Rinv, int k, int d, int adaptive,
+                                                           uint32_t* status) {
+  extern __shared__ float sm[];
+  __shared__ float red[kLThreads / 32];
+  __shared__ float piv;
+  const int b = blockIdx.x;
+  const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
+  float* Rb = Rinv + static_cast<int64_t>(b) * k * k;
+  float* Ls = sm;              // k x k, lower triangle used
+  float* Xs = sm + kLK * kLP;  // L^-1, column by column
+  float tr = 0.0f;
+  for (int e = threadIdx.x; e < k * k; e += blockDim.x)
+    if (e / k == e % k) tr += Gb[e];
+  tr = cl_block_sum(tr, red);
+  bool bad = false;
+  for (int attempt = 0; attempt < (adaptive ? 2 : 1); ++attempt) {
+    const float sh = attempt == 0 ? 0.0f : 11.0f * (k + sqrtf(static_cast<float>(d))) * 5.9604645e-8f * tr;
+    for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
+      const int i = e / k, j = e % k;
+      Ls[i * kLP + j] = 0.5f * (Gb[i * k + j] + Gb[j * k + i]) + (i == j ? sh : 0.0f);
+    }
+    __syncthreads();
+    bad = false;
+    for (int j = 0; j < k; ++j) {
+      if (threadIdx.x == 0) {
+        const float djj = Ls[j * kLP + j];
+        piv = djj > 0.0f ? sqrtf(djj) : 0.0f;
+      }
+      __syncthreads();
+      const float cj = piv;
+      if (!(cj > 0.0f)) bad = true;
+      for (int i = j + threadIdx.x; i < k; i += blockDim.x)
+        Ls[i * kLP + j] = i == j ? cj : (cj > 0.0f ? Ls[i * kLP + j] / cj : 0.0f);
+      __syncthreads();
+      const int w = k - j - 1;
+      for (int e = threadIdx.x; e < w * w; e += blockDim.x) {
+        const int i = j + 1 + e / w, l = j + 1 + e % w;
+        if (l <= i) Ls[i * kLP + l] = fmaf(-Ls[i * kLP + j], Ls[l * kLP + j], Ls[i * kLP + l]);
+      }
+      __syncthreads();
+    }
+    if (!__syncthreads_or(bad)) break;
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) atomicOr(status, kStNonfiniteIter);
+    return;
+  }
+  // column c of L^-1 by forward substitution (one thread per column)
+  for (int c = threadIdx.x; c < k; c += blockDim.x) {
+    for (int i = 0; i < c; ++i) Xs[i * kLP + c] = 0.0f;
+    Xs[c * kLP + c] = 1.0f / Ls[c * kLP + c];
+    for (int i = c + 1; i < k; ++i) {
+      float v = 0.0f;
+      for (int l = c; l < i; ++l) v = fmaf(Ls[i * kLP + l], Xs[l * kLP + c], v);
+      Xs[i * kLP + c] = -v / Ls[i * kLP + i];
+    }
+  }
+  __syncthreads();
+  // Rinv = (L^-1)^T
+  for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
+    const int i = e / k, j = e % k;
+    Rb[e] = Xs[j * kLP + i];
+  }
+}
+
+// nu = spacing of binary32 numbers at ||Y||_2, ||Y||_2^2 the largest
+// eigenvalue of the Gram matrix Y^T Y (60 power steps in one warp).
+__global__ void __launch_bounds__(kLThreads) k_cl_norm(const float* Gram, float* nu, int k) {
+  extern __shared__ float sm[];
+  const int b = blockIdx.x;
+  const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
+  float* As = sm;
+  float* v = sm + kLK * kLP;  // 2 k
+  for (int e = threadIdx.x; e < k * k; e += blockDim.x) As[(e / k) * kLP + e % k] = Gb[e];
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  for (int j = lane; j < k; j += 32) v[j] = 1.0f;
+  __syncwarp();
+  float nrm = 0.0f;
+  for (int it = 0; it < 60; ++it) {
+    float s2 = 0.0f;
+    for (int i = lane; i < k; i += 32) {
+      float s = 0.0f;
+      for (int j = 0; j < k; ++j) s = fmaf(As[i * kLP + j], v[j], s);
+      v[kLK + i] = s;
+      s2 = fmaf(s, s, s2);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    nrm = sqrtf(s2);
+    __syncwarp();
+    for (int i = lane; i < k; i += 32) v[i] = nrm > 0.0f ? v[kLK + i] / nrm : 0.0f;
+    __syncwarp();
+  }
+  if (lane == 0) {
+    const float yn = sqrtf(nrm);
+    nu[b] = yn > 0.0f ? ldexpf(1.0f, ilogbf(yn) - 23) : 0.0f;
+  }
+}
+
+// Thin SVD of Z from the eigen-decomposition of Z^T Z = V Sigma^2 V^T (cyclic
+// Jacobi in shared memory).  Writes WU (k x r) with U = Z WU: column c of WU
+// is s_c v_j / sigma_j for the eigenpair j of rank c (decreasing Sigma^2),
+// s_c = +-1 aligning U's column with the previous basis (P = Z^T U_prev,
+// k x r; null at the first refresh); and Lambda_c = max(0, sigma_j^2 - nu).
+__global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const float* P, const float* nu, float* WU,
+                                                      float* lam, int k, int r, int max_sweeps, float tol2,
+                                                      const uint32_t* status) {
+  extern __shared__ float sm[];
+  __shared__ float red[kLThreads / 32];
+  if (cl_flagged(status)) return;
+  const int b = blockIdx.x;
+  const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
+  float* As = sm;
+  float* Vs = sm + kLK * kLP;
+  float* cs = Vs + kLK * kLP;            // 2 per pair
+  int* pr = reinterpret_cast<int*>(cs + kLK);  // 2 per pair, then ranks
+  const int dp = k + (k & 1), np = dp / 2;
+  for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
+    const int i = e / dp, j = e % dp;
+    As[i * kLP + j] = (i < k && j < k) ? 0.5f * (Gb[i * k + j] + Gb[j * k + i]) : 0.0f;
+    Vs[i * kLP + j] = i == j ? 1.0f : 0.0f;
+  }
+  __syncthreads();
+  for (int sweep = 0; sweep < max_sweeps; ++sweep) {
+    float off = 0.0f, dg = 0.0f;
+    for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
+      const int i = e / dp, j = e % dp;
+      const float v = As[i * kLP + j];
+      if (i == j)
+        dg = fmaf(v, v, dg);
+      else
+        off = fmaf(v, v, off);
+    }
+    const float offs = cl_block_sum(off, red);
+    const float dgs = cl_block_sum(dg, red);
+    if (!(offs > tol2 * dgs)) break;
+    for (int rd = 0; rd < dp - 1; ++rd) {
+      for (int q = threadIdx.x; q < np; q += blockDim.x) {
+        auto idx = [&](int pos) { return pos == 0 ? 0 : 1 + (pos - 1 + rd) % (dp - 1); };
+        int pp = idx(q), qq = idx(dp - 1 - q);
+        if (pp > qq) {
+          const int x = pp;
+          pp = qq;
+          qq = x;
+        }
+        const float apq = As[pp * kLP + qq];
+        float c = 1.0f, sn = 0.0f;
+        if (apq != 0.0f) {
+          const float th = (As[qq * kLP + qq] - As[pp * kLP + pp]) / (2.0f * apq);
+          const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
+          c = rsqrtf(fmaf(t, t, 1.0f));
+          sn = t * c;
+        }
+        cs[2 * q] = c;
+        cs[2 * q + 1] = sn;
+        pr[2 * q] = pp;
+        pr[2 * q + 1] = qq;
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
+        const int q = e / dp, j = e % dp;
+        const int pp = pr[2 * q], qq = pr[2 * q + 1];
+        const float c = cs[2 * q], sn = cs[2 * q + 1];
+        const float ap = As[pp * kLP + j], aq = As[qq * kLP + j];
+        As[pp * kLP + j] = c * ap - sn * aq;
+        As[qq * kLP + j] = sn * ap + c * aq;
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
+        const int q = e / dp, i = e % dp;
+        const int pp = pr[2 * q], qq = pr[2 * q + 1];
+        const float c = cs[2 * q], sn = cs[2 * q + 1];
+        const float ap = As[i * kLP + pp], aq = As[i * kLP + qq];
+        As[i * kLP + pp] = c * ap - sn * aq;
+        As[i * kLP + qq] = sn * ap + c * aq;
+        const float vp = Vs[i * kLP + pp], vq = Vs[i * kLP + qq];
+        Vs[i * kLP + pp] = c * vp - sn * vq;
+        Vs[i * kLP + qq] = sn * vp + c * vq;
+      }
+      __syncthreads();
+    }
+  }
+  // ranks by decreasing Sigma^2 (ties by index)
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const float lj = As[j * kLP + j];
+    int rank = 0;
+    for (int i = 0; i < k; ++i) {
+      const float li = As[i * kLP + i];
+      rank += (li > lj) || (li == lj && i < j);
+    }
+    pr[j] = rank;
+  }
+  __syncthreads();
+  const float nub = nu[b];
+  float* W = WU + static_cast<int64_t>(b) * k * r;
+  const float* Pb = P ? P + static_cast<int64_t>(b) * k * r : nullptr;
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const int c = pr[j];
+    if (c >= r) continue;
+    const float s2 = As[j * kLP + j];
+    const float inv = s2 > 0.0f ? rsqrtf(s2) : 0.0f;
+    float sg = 1.0f;
+    if (Pb) {
+      float dot = 0.0f;
+      for (int l = 0; l < k; ++l) dot = fmaf(Vs[l * kLP + j], Pb[l * r + c], dot);
+      sg = dot < 0.0f ? -1.0f : 1.0f;
+    }
+    for (int l = 0; l < k; ++l) W[l * r + c] = sg * inv * Vs[l * kLP + j];
+    lam[static_cast<int64_t>(b) * r + c] = fmaxf(0.0f, s2 - nub);
+  }
+}
+
+// ------------------------------------------------------- element-wise kernels
+// Omega = [U_prev, Psi] (warm) or Psi (cold) for one side: rows row0.. of the
+// noise block, d rows, k columns.
+__global__ void k_cl_omega(const float* Uprev, const float* noise, float* Om, int d, int k, int r, int mn, int row0,
+                           int warm, int64_t om_stride) {
+  const int b = blockIdx.y;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < static_cast<int64_t>(d) * k;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(e / k), j = static_cast<int>(e % k);
+    const float* nz = noise + (static_cast<int64_t>(b) * mn + row0 + i) * k;
+    float v;
+    if (warm)
+      v = j < r ? Uprev[(static_cast<int64_t>(b) * d + i) * r + j] : nz[j - r];
+    else
+      v = nz[j];
+    Om[b * om_stride + e] = v;
+  }
+}
+
+// X (rows x cols, batch-strided) += coef[b] * Y; or X[i][j] *= rowscale[b][i]
+__global__ void k_cl_axpy(float* X, const float* Y, const float* coef, int64_t elems, int64_t stride) {
+  const int b = blockIdx.y;
+  const float c = coef[b];
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < elems;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    X[b * stride + e] = fmaf(c, Y[b * stride + e], X[b * stride + e]);
+}
+
+__global__ void k_cl_rowscale(float* X, const float* scale, int rows, int cols, int64_t stride, int scale_stride) {
+  const int b = blockIdx.y;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < static_cast<int64_t>(rows) * cols;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    X[b * stride + e] *= scale[static_cast<int64_t>(b) * scale_stride + e / cols];
+}
+
+template <typename GT>
+__global__ void k_cl_prep(const GT* G, float* Cb, int64_t mn, uint32_t* status) {
+  const int b = blockIdx.y;
+  bool bad = false;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < mn;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float g = cl_ld<GT>(G + b * mn + e);
+    bad |= !isfinite(g);
+    Cb[b * mn + e] = g;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, kStNonfiniteInput);
+}
+
+// fixed-slot partial sums of squares (kClParts blocks per matrix, summed in
+// order by k_cl_moments)
+__global__ void __launch_bounds__(256) k_cl_sumsq(const float* X, int64_t elems, float* part) {
+  __shared__ float red[8];
+  const int b = blockIdx.y;
+  float s = 0.0f;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < elems;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float v = X[b * elems + e];
+    s = fmaf(v, v, s);
+  }
+  s = cl_block_sum(s, red);
+  if (threadIdx.x == 0) part[static_cast<int64_t>(b) * kClParts + blockIdx.x] = s;
+}
+
+// One CTA per matrix: Main moments and N(M, V); the pooled second moments of
+// blocks A, B and C; the C normaliser.
+__global__ void __launch_bounds__(256) k_cl_moments(ClLarge L) {
+  if (cl_flagged(L.status)) return;
+  const int b = blockIdx.x;
+  const int m = L.m, n = L.n, r = L.r;
+  float* M = L.M + static_cast<int64_t>(b) * r * r;
+  float* V = L.V + static_cast<int64_t>(b) * r * r;
+  const float* S = L.S + static_cast<int64_t>(b) * r * r;
+  float* Nm = L.Nm + static_cast<int64_t>(b) * r * r;
+  const float* GA = L.GU + static_cast<int64_t>(b) * m * r;
+  const float* GB = L.UG + static_cast<int64_t>(b) * r * n;
+  const float b1 = L.beta1, b2 = L.beta2;
+  for (int e = threadIdx.x; e < r * r; e += blockDim.x) {
+    const float s = S[e];
+    const float mm = fmaf(b1, M[e], (1.0f - b1) * s);
+    const float vv = fmaf(b2, V[e], (1.0f - b2) * s * s);
+    M[e] = mm;
+    V[e] = vv;
+    Nm[e] = (mm * L.bc1) / (sqrtf(vv * L.bc2) + L.eps);
+  }
+  // v_A: column sums of G_A^2; v_B: row sums of G_B^2 (a warp per column / row)
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = w; j < r; j += blockDim.x >> 5) {
+    float sa = 0.0f, sb = 0.0f;
+    for (int i = lane; i < m; i += 32) sa = fmaf(GA[static_cast<int64_t>(i) * r + j], GA[static_cast<int64_t>(i) * r + j], sa);
+    for (int i = lane; i < n; i += 32) sb = fmaf(GB[static_cast<int64_t>(j) * n + i], GB[static_cast<int64_t>(j) * n + i], sb);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sa += __shfl_xor_sync(0xffffffffu, sa, o);
+      sb += __shfl_xor_sync(0xffffffffu, sb, o);
+    }
+    if (lane == 0) {
+      L.vA[static_cast<int64_t>(b) * r + j] = fmaf(b2, L.vA[static_cast<int64_t>(b) * r + j], (1.0f - b2) * sa);
+      L.vB[static_cast<int64_t>(b) * r + j] = fmaf(b2, L.vB[static_cast<int64_t>(b) * r + j], (1.0f - b2) * sb);
+    }
+  }
+  if (threadIdx.x == 0) {
+    float c2 = 0.0f;
+    for (int i = 0; i < kClParts; ++i) c2 += L.part[static_cast<int64_t>(b) * kClParts + i];
+    const float vc = fmaf(b2, L.vC[b], (1.0f - b2) * c2);
+    L.vC[b] = vc;
+    L.cden[b] = 1.0f / (sqrtf(vc * L.bc2) + L.eps);
+  }
+}
+
+// Block A and B first moments, then their normalised forms in place of G_A,
+// G_B (one index space: m r entries of A, then r n of B).
+__global__ void __launch_bounds__(256) k_cl_blocks(ClLarge L) {
+  if (cl_flagged(L.status)) return;
+  const int b = blockIdx.y;
+  const int m = L.m, n = L.n, r = L.r;
+  const int64_t na = static_cast<int64_t>(m) * r, nb = static_cast<int64_t>(r) * n;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < na + nb;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (e < na) {
+      const int64_t o = b * na + e;
+      const float mv = fmaf(L.beta1, L.MA[o], (1.0f - L.beta1) * L.GU[o]);
+      L.MA[o] = mv;
+      L.GU[o] = (mv * L.bc1) / (sqrtf(L.vA[static_cast<int64_t>(b) * r + e % r] * L.bc2) + L.eps);
+    } else {
+      const int64_t f = e - na, o = b * nb + f;
+      const float mv = fmaf(L.beta1, L.MB[o], (1.0f - L.beta1) * L.UG[o]);
+      L.MB[o] = mv;
+      L.UG[o] = (mv * L.bc1) / (sqrtf(L.vB[static_cast<int64_t>(b) * r + f / n] * L.bc2) + L.eps);
+    }
+  }
+}
+
+template <typename WT>
+__device__ __forceinline__ void cl_st(WT* p, float v);
+template <>
+__device__ __forceinline__ void cl_st<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void cl_st<__nv_bfloat16>(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+template <typename WT>
+__global__ void __launch_bounds__(256) k_cl_update(WT* W, const float* Gt, int64_t mn, float decay, float alr,
+                                                   uint32_t* status) {
+  if (cl_flagged(status)) return;
+  const int b = blockIdx.y;
+  bool bad = false;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < mn;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t o = b * mn + e;
+    const float w = fmaf(-alr, Gt[o], decay * cl_ld<WT>(W + o));
+    bad |= !isfinite(w);
+    cl_st<WT>(W + o, w);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, kStNonfiniteUpdate);
+}
+
+// v_A^T <- v_A^T (O_R)^2, v_B <- (O_L)^2 v_B (entry-wise squares); one CTA per matrix
+__global__ void k_cl_vrot(const float* vA, const float* vB, const float* OL, const float* OR, float* vAn, float* vBn,
+                          int r) {
+  const int b = blockIdx.x;
+  const float* ol = OL + static_cast<int64_t>(b) * r * r;
+  const float* orr = OR + static_cast<int64_t>(b) * r * r;
+  for (int j = threadIdx.x; j < r; j += blockDim.x) {
+    float sa = 0.0f, sb = 0.0f;
+    for (int l = 0; l < r; ++l) {
+      sa = fmaf(vA[static_cast<int64_t>(b) * r + l], orr[l * r + j] * orr[l * r + j], sa);
+      sb = fmaf(ol[j * r + l] * ol[j * r + l], vB[static_cast<int64_t>(b) * r + l], sb);
+    }
+    vAn[static_cast<int64_t>(b) * r + j] = sa;
+    vBn[static_cast<int64_t>(b) * r + j] = sb;
+  }
+}
+
+// The refreshed bases (and, after a warm refresh, the transported moments)
+// become the state -- unless an earlier stage flagged the status word.
+__global__ void k_cl_install(ClLarge L) {
+  if (cl_flagged(L.status)) return;
+  const int b = blockIdx.y;
+  const int64_t m = L.m, n = L.n, r = L.r;
+  auto copy = [&](float* dst, const float* src, int64_t elems) {
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < elems;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      dst[b * elems + e] = src[b * elems + e];
+  };
+  copy(L.UL, L.ULn, m * r);
+  copy(L.UR, L.URn, n * r);
+  copy(L.lamL, L.lamLn, r);
+  copy(L.lamR, L.lamRn, r);
+  if (L.warm) {
+    copy(L.M, L.Mn, r * r);
+    copy(L.MA, L.MAn, m * r);
+    copy(L.MB, L.MBn, r * n);
+    copy(L.vA, L.vAn, r);
+    copy(L.vB, L.vBn, r);
+  }
+}
+
+cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return cudaSuccess;
+  const dim3 grid((g.N + kGT - 1) / kGT, (g.M + kGT - 1) / kGT, g.batch);
+  if (g.a_bf16 && g.b_bf16)
+    k_cl_gemm<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(g);
+  else if (g.a_bf16)
+    k_cl_gemm<__nv_bfloat16, float><<<grid, 256, 0, st>>>(g);
+  else if (g.b_bf16)
+    k_cl_gemm<float, __nv_bfloat16><<<grid, 256, 0, st>>>(g);
+  else
+    k_cl_gemm<float, float><<<grid, 256, 0, st>>>(g);
+  return cudaGetLastError();
+}
+
+
+// ------------------------------------------------------------- orchestration
+namespace {
+
+struct ClRun {
+  const ClLarge& L;
+  cudaStream_t st;
+  int* launches;
+  cudaError_t err = cudaSuccess;
+
+  // C = alpha op(A) op(B) + beta C over the batch
+  void gemm(const void* A, int abf, int ta, int64_t lda, int64_t sA, const void* B, int bbf, int tb, int64_t ldb,
+            int64_t sB, float* C, int64_t ldc, int64_t sC, int M, int N, int K, float alpha = 1.0f, float beta = 0.0f,
+            const float* beta_dev = nullptr) {
+    if (err != cudaSuccess) return;
+    ClGemm g;
+    g.A = A;
+    g.B = B;
+    g.C = C;
+    g.a_bf16 = abf;
+    g.b_bf16 = bbf;
+    g.ta = ta;
+    g.tb = tb;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.lda = lda;
+    g.ldb = ldb;
+    g.ldc = ldc;
+    g.sA = sA;
+    g.sB = sB;
+    g.sC = sC;
+    g.batch = L.batch;
+    g.alpha = alpha;
+    g.beta = beta;
+    g.beta_dev = beta_dev;
+    err = launch_cl_gemm(g, st);
+    ++*launches;
+  }
+  template <class F>
+  void launch(F&& f) {
+    if (err != cudaSuccess) return;
+    f();
+    err = cudaGetLastError();
+    ++*launches;
+  }
+  dim3 grid_for(int64_t elems) const {
+    const int64_t g = (elems + 255) / 256;
+    return dim3(static_cast<unsigned>(g < 256 ? (g > 0 ? g : 1) : 256), static_cast<unsigned>(L.batch));
+  }
+};
+
+cudaError_t cl_attributes() {
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || attr_dev == dev) return e;
+  const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  e = cudaFuncSetAttribute(k_cl_chol_inv, at, kLSmallSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_norm, at, kLSmallSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_svd, at, kLSmallSmem);
+  if (e == cudaSuccess) attr_dev = dev;
+  return e;
+}
+
+// Thin QR of the batch of d x k panels in `cur`: four Cholesky-QR passes,
+// each shifted only where its factorisation breaks down (panels with
+// condition numbers up to ~1e6 come out orthonormal); `spare` is a second
+// panel buffer.  An even number of passes leaves Q in `cur`.
+float* cl_qr(ClRun& R, float* cur, float* spare, int d) {
+  const ClLarge& L = R.L;
+  const int k = L.k;
+  const int64_t sP = static_cast<int64_t>(L.m > L.n ? L.m : L.n) * k, sK = static_cast<int64_t>(k) * k;
+  for (int pass = 0; pass < 4; ++pass) {
+    R.gemm(cur, 0, 1, k, sP, cur, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
+    R.launch([&] { k_cl_chol_inv<<<L.batch, kLThreads, kLSmallSmem, R.st>>>(L.Gram, L.Rinv, k, d, 1, L.status); });
+    R.gemm(cur, 0, 0, k, sP, L.Rinv, 0, 0, k, sK, spare, k, sP, d, k, k);
+    float* t = cur;
+    cur = spare;
+    spare = t;
+  }
+  return cur;
+}
+
+// Y = (b2 U Lambda U^T + (1 - b2) G G^T) X on the left side (side 0), or
+// with G^T G on the right side; the factor is never formed.
+void cl_apply(ClRun& R, int side, const float* X, float* Y) {
+  const ClLarge& L = R.L;
+  const int m = L.m, n = L.n, r = L.r, k = L.k;
+  const int64_t sP = static_cast<int64_t>(m > n ? m : n) * k, mn = static_cast<int64_t>(m) * n;
+  const int d = side == 0 ? m : n;
+  if (side == 0) {
+    R.gemm(L.G, L.g_bf16, 1, n, mn, X, 0, 0, k, sP, L.T1, k, sP, n, k, m);
+    R.gemm(L.G, L.g_bf16, 0, n, mn, L.T1, 0, 0, k, sP, Y, k, sP, m, k, n, 1.0f - L.beta2);
+  } else {
+    R.gemm(L.G, L.g_bf16, 0, n, mn, X, 0, 0, k, sP, L.T1, k, sP, m, k, n);
+    R.gemm(L.G, L.g_bf16, 1, n, mn, L.T1, 0, 0, k, sP, Y, k, sP, n, k, m, 1.0f - L.beta2);
+  }
+  if (L.warm) {
+    const float* U = side == 0 ? L.UL : L.UR;
+    const float* lam = side == 0 ? L.lamL : L.lamR;
+    const int64_t sU = static_cast<int64_t>(d) * r;
+    R.gemm(U, 0, 1, r, sU, X, 0, 0, k, sP, L.T1, k, sP, r, k, d);
+    R.launch([&] {
+      k_cl_rowscale<<<R.grid_for(static_cast<int64_t>(r) * k), 256, 0, R.st>>>(L.T1, lam, r, k, sP, r);
+    });
+    R.gemm(U, 0, 0, r, sU, L.T1, 0, 0, k, sP, Y, k, sP, d, k, r, L.beta2, 1.0f);
+  }
+}
+
+// Algorithm 3 for one side: the new basis (d x r) and eigenvalues.
+void cl_nystrom(ClRun& R, int side) {
+  const ClLarge& L = R.L;
+  const int m = L.m, n = L.n, r = L.r, k = L.k;
+  const int d = side == 0 ? m : n;
+  const int64_t sP = static_cast<int64_t>(m > n ? m : n) * k, sK = static_cast<int64_t>(k) * k;
+  const int64_t sU = static_cast<int64_t>(d) * r;
+  const float* Uprev = side == 0 ? L.UL : L.UR;
+  float* Uout = side == 0 ? L.ULn : L.URn;
+  float* lamOut = side == 0 ? L.lamLn : L.lamRn;
+  R.launch([&] {
+    k_cl_omega<<<R.grid_for(static_cast<int64_t>(d) * k), 256, 0, R.st>>>(Uprev, L.noise, L.Om, d, k, r, m + n,
+                                                                          side == 0 ? 0 : m, L.warm, sP);
+  });
+  // panels: Om, X (QR ping-pong), Y, T1 (apply's temporary)
+  float* om = cl_qr(R, L.Om, L.X, d);  // Q in Om
+  for (int it = 0; it < L.q; ++it) {
+    cl_apply(R, side, om, L.Y);
+    om = cl_qr(R, L.Y, L.X, d);  // Q in Y; Om is spent
+    float* t = om == L.Y ? L.Om : om;
+    if (om == L.Y) {
+      // keep the basis out of the Y panel, which the next apply writes
+      if (R.err == cudaSuccess)
+        R.err = cudaMemcpyAsync(t, L.Y, static_cast<size_t>(L.batch) * sP * 4, cudaMemcpyDeviceToDevice, R.st);
+      om = t;
+    }
+  }
+  float* free_panel = om == L.Om ? L.X : L.Om;
+  cl_apply(R, side, om, L.Y);
+  // nu = eps(||Y||_2); Y_nu = Y + nu Omega
+  R.gemm(L.Y, 0, 1, k, sP, L.Y, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
+  R.launch([&] { k_cl_norm<<<L.batch, kLThreads, kLSmallSmem, R.st>>>(L.Gram, L.nu, k); });
+  R.launch([&] { k_cl_axpy<<<R.grid_for(static_cast<int64_t>(d) * k), 256, 0, R.st>>>(L.Y, om, L.nu, static_cast<int64_t>(d) * k, sP); });
+  // C^T C = (B + B^T)/2, B = Omega^T Y_nu;  Z = Y_nu C^-1
+  R.gemm(om, 0, 1, k, sP, L.Y, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
+  R.launch([&] { k_cl_chol_inv<<<L.batch, kLThreads, kLSmallSmem, R.st>>>(L.Gram, L.Rinv, k, d, 0, L.status); });
+  float* Z = free_panel;
+  R.gemm(L.Y, 0, 0, k, sP, L.Rinv, 0, 0, k, sK, Z, k, sP, d, k, k);
+  // thin SVD of Z from Z^T Z; signs against the previous basis
+  R.gemm(Z, 0, 1, k, sP, Z, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
+  if (L.warm) R.gemm(Z, 0, 1, k, sP, Uprev, 0, 0, r, sU, L.P, r, static_cast<int64_t>(k) * r, k, r, d);
+  R.launch([&] {
+    k_cl_svd<<<L.batch, kLThreads, kLSmallSmem, R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU, lamOut, k, r,
+                                                          L.max_sweeps, L.tol2, L.status);
+  });
+  R.gemm(Z, 0, 0, k, sP, L.WU, 0, 0, r, static_cast<int64_t>(k) * r, Uout, r, sU, d, r, k);
+}
+
+}  // namespace
+
+cudaError_t clean_large_refresh(const ClLarge& L, cudaStream_t st, int* launches) {
+  cudaError_t e = cl_attributes();
+  if (e != cudaSuccess) return e;
+  ClRun R{L, st, launches};
+  cl_nystrom(R, 0);
+  cl_nystrom(R, 1);
+  if (L.warm) {
+    // Eqns. (14)-(15): O_L = U_Ln^T U_L, O_R = U_R^T U_Rn
+    const int m = L.m, n = L.n, r = L.r, k = L.k;
+    const int64_t sR = static_cast<int64_t>(r) * r, sK = static_cast<int64_t>(k) * k;
+    const int64_t sMA = static_cast<int64_t>(m) * r, sMB = static_cast<int64_t>(r) * n, sUR = static_cast<int64_t>(n) * r;
+    float* OL = L.Sm;
+    float* OR = L.S;
+    R.gemm(L.ULn, 0, 1, r, sMA, L.UL, 0, 0, r, sMA, OL, r, sR, r, r, m);
+    R.gemm(L.UR, 0, 1, r, sUR, L.URn, 0, 0, r, sUR, OR, r, sR, r, r, n);
+    // M <- O_L M O_R
+    R.gemm(OL, 0, 0, r, sR, L.M, 0, 0, r, sR, L.Nm, r, sR, r, r, r);
+    R.gemm(L.Nm, 0, 0, r, sR, OR, 0, 0, r, sR, L.Mn, r, sR, r, r, r);
+    // M_A <- (I - U_Ln U_Ln^T) M_A O_R
+    R.gemm(L.MA, 0, 0, r, sMA, OR, 0, 0, r, sR, L.MAn, r, sMA, m, r, r);
+    R.gemm(L.ULn, 0, 1, r, sMA, L.MAn, 0, 0, r, sMA, L.Gram, r, sK, r, r, m);
+    R.gemm(L.ULn, 0, 0, r, sMA, L.Gram, 0, 0, r, sK, L.MAn, r, sMA, m, r, r, -1.0f, 1.0f);
+    // M_B <- O_L M_B (I - U_Rn U_Rn^T)
+    R.gemm(OL, 0, 0, r, sR, L.MB, 0, 0, n, sMB, L.MBn, n, sMB, r, n, r);
+    R.gemm(L.MBn, 0, 0, n, sMB, L.URn, 0, 0, r, sUR, L.Rinv, r, sK, r, r, n);
+    R.gemm(L.Rinv, 0, 0, r, sK, L.URn, 0, 1, r, sUR, L.MBn, n, sMB, r, n, r, -1.0f, 1.0f);
+    R.launch([&] { k_cl_vrot<<<L.batch, 128, 0, st>>>(L.vA, L.vB, OL, OR, L.vAn, L.vBn, r); });
+  }
+  R.launch([&] {
+    const int64_t big = static_cast<int64_t>(L.m > L.n ? L.m : L.n) * L.r;
+    k_cl_install<<<R.grid_for(big > static_cast<int64_t>(L.r) * L.n ? big : static_cast<int64_t>(L.r) * L.n), 256, 0,
+                   st>>>(L);
+  });
+  return R.err;
+}
+
+cudaError_t clean_large_step(const ClLarge& L, cudaStream_t st, int* launches) {
+  ClRun R{L, st, launches};
+  const int m = L.m, n = L.n, r = L.r;
+  const int64_t mn = static_cast<int64_t>(m) * n, sMA = static_cast<int64_t>(m) * r;
+  const int64_t sMB = static_cast<int64_t>(r) * n, sUR = static_cast<int64_t>(n) * r, sR = static_cast<int64_t>(r) * r;
+  const int gb = L.g_bf16;
+  R.launch([&] {
+    if (gb)
+      k_cl_prep<__nv_bfloat16><<<R.grid_for(mn), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(L.G), L.Cb, mn,
+                                                                L.status);
+    else
+      k_cl_prep<float><<<R.grid_for(mn), 256, 0, st>>>(static_cast<const float*>(L.G), L.Cb, mn, L.status);
+  });
+  // G U_R, U_L^T G, S = U_L^T G U_R
+  R.gemm(L.G, gb, 0, n, mn, L.UR, 0, 0, r, sUR, L.GU, r, sMA, m, r, n);
+  R.gemm(L.UL, 0, 1, r, sMA, L.G, gb, 0, n, mn, L.UG, n, sMB, r, n, m);
+  R.gemm(L.UL, 0, 1, r, sMA, L.GU, 0, 0, r, sMA, L.S, r, sR, r, r, m);
+  // G_B = U_L^T G - S U_R^T;  C = G - U_L G_B - (G U_R) U_R^T;  G_A = G U_R - U_L S
+  R.gemm(L.S, 0, 0, r, sR, L.UR, 0, 1, r, sUR, L.UG, n, sMB, r, n, r, -1.0f, 1.0f);
+  R.gemm(L.UL, 0, 0, r, sMA, L.UG, 0, 0, n, sMB, L.Cb, n, mn, m, n, r, -1.0f, 1.0f);
+  R.gemm(L.GU, 0, 0, r, sMA, L.UR, 0, 1, r, sUR, L.Cb, n, mn, m, n, r, -1.0f, 1.0f);
+  R.gemm(L.UL, 0, 0, r, sMA, L.S, 0, 0, r, sR, L.GU, r, sMA, m, r, r, -1.0f, 1.0f);
+  // moments (Table 1) and the normalised blocks
+  R.launch([&] { k_cl_sumsq<<<dim3(kClParts, L.batch), 256, 0, st>>>(L.Cb, mn, L.part); });
+  R.launch([&] { k_cl_moments<<<L.batch, 256, 0, st>>>(L); });
+  R.launch([&] { k_cl_blocks<<<R.grid_for(sMA + sMB), 256, 0, st>>>(L); });
+  // G~ = C cden + (U_L N(M, V) + N(M_A, v_A)) U_R^T + U_L N(M_B, v_B)
+  R.gemm(L.UL, 0, 0, r, sMA, L.Nm, 0, 0, r, sR, L.GU, r, sMA, m, r, r, 1.0f, 1.0f);
+  R.gemm(L.GU, 0, 0, r, sMA, L.UR, 0, 1, r, sUR, L.Cb, n, mn, m, n, r, 1.0f, 0.0f, L.cden);
+  R.gemm(L.UL, 0, 0, r, sMA, L.UG, 0, 0, n, sMB, L.Cb, n, mn, m, n, r, 1.0f, 1.0f);
+  R.launch([&] {
+    if (L.w_bf16)
+      k_cl_update<__nv_bfloat16><<<R.grid_for(mn), 256, 0, st>>>(static_cast<__nv_bfloat16*>(L.W), L.Cb, mn, L.decay,
+                                                                  L.alr, L.status);
+    else
+      k_cl_update<float><<<R.grid_for(mn), 256, 0, st>>>(static_cast<float*>(L.W), L.Cb, mn, L.decay, L.alr,
+                                                          L.status);
+  });
+  return R.err;
+}
+
+}  // namespace okls

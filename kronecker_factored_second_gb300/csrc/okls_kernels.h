@@ -109,6 +109,50 @@ cudaError_t launch_clean_refresh(const CleanArgs& A, cudaStream_t st);
 cudaError_t launch_clean_step(const CleanArgs& A, cudaStream_t st);
 cudaError_t launch_clean_reset(const CleanArgs& A, cudaStream_t st);
 
+// Clean for large shapes (m, n <= 16384, r + p <= 128): a batched fp32 GEMM
+// and the k x k kernels around it, orchestrated by clean_large_refresh /
+// clean_large_step.
+struct ClGemm {
+  const void* A;      // fp32, or bf16 when a_bf16
+  const void* B;      // fp32, or bf16 when b_bf16
+  float* C;
+  int a_bf16, b_bf16;
+  int ta, tb;         // A stored K x M / B stored N x K
+  int M, N, K;
+  int64_t lda, ldb, ldc;
+  int64_t sA, sB, sC; // batch strides (elements)
+  int batch;
+  float alpha, beta;
+  const float* beta_dev;  // per-batch beta when not null
+};
+cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st);
+
+// Device buffers of the large Clean path; every array is batch-strided.
+struct ClLarge {
+  int batch, m, n, r, p, q, k;
+  int warm;
+  float beta1, beta2, eps, alr, decay, bc1, bc2;
+  int max_sweeps;
+  float tol2;
+  uint32_t* status;
+  const void* G;
+  void* W;
+  int g_bf16, w_bf16;
+  const float* noise;                 // batch x (m + n) x k
+  // state
+  float *UL, *UR, *lamL, *lamR, *M, *V, *MA, *MB, *vA, *vB, *vC;
+  // workspace
+  float *ULn, *URn, *lamLn, *lamRn;   // refreshed bases
+  float *Om, *Y, *X, *T1;             // d x k panels (d = max(m, n))
+  float *Gram, *Rinv, *WU, *P, *nu;   // k x k, k x k, k x r, k x r, 1
+  float *Mn, *Sm, *MAn, *MBn, *vAn, *vBn;  // transported moments (r x r, r x r, m x r, r x n, r, r)
+  float *GU, *UG, *S, *Nm, *Cb;       // step: m x r, r x n, r x r, r x r, m x n
+  float *part, *cden;                 // sum-of-squares partials (batch x kClParts), 1
+};
+constexpr int kClParts = 64;
+cudaError_t clean_large_refresh(const ClLarge& L, cudaStream_t st, int* launches);
+cudaError_t clean_large_step(const ClLarge& L, cudaStream_t st, int* launches);
+
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_pair(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 

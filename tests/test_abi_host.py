@@ -139,8 +139,8 @@ def test_soap_shapes_and_state(lib):
 
 def test_clean_shapes_and_validation(lib):
     """Clean keeps rank-r bases, their eigenvalues and the four blocks'
-    moments (linear in m and n); this build takes m, n <= 128 and
-    rank + oversample <= 64, and the rank fields belong to Clean alone."""
+    moments (linear in m and n); this build takes m, n <= 16384 and
+    rank + oversample <= 128, and the rank fields belong to Clean alone."""
     B, m, n, r = 3, 128, 96, 16
     c = L.config_default(B, m, n)
     c.method = L.METHOD_CLEAN
@@ -153,11 +153,22 @@ def test_clean_shapes_and_validation(lib):
     for field, value, code in [("rank", 0, L.OKLS_ERR_INVALID_ARG), ("oversample", -1, L.OKLS_ERR_INVALID_ARG),
                                ("power_iters", 17, L.OKLS_ERR_INVALID_ARG),
                                ("rank", 89, L.OKLS_ERR_INVALID_ARG),       # r + p > min(m, n)
-                               ("rank", 57, L.OKLS_ERR_UNSUPPORTED),       # r + p > 64
-                               ("m", 129, L.OKLS_ERR_UNSUPPORTED)]:
+                               ("m", 16385, L.OKLS_ERR_UNSUPPORTED)]:
         c2 = L.okls_config.from_buffer_copy(c)
         setattr(c2, field, value)
         assert lib.okls_state_bytes(ctypes.byref(c2), None, None) == code, (field, value)
+    # past one CTA's shared memory (m > 128 or r + p > 64) the batched-GEMM
+    # path takes over: the same state, a workspace of d x (r + p) panels and
+    # one m x n fp32 buffer per matrix; r + p above 128 is not supported
+    cl = L.config_default(2, 300, 200)
+    cl.method, cl.rank, cl.oversample, cl.power_iters = L.METHOD_CLEAN, 32, 16, 1
+    s2, w2 = L.state_bytes(cl)
+    B2, m2, n2, r2, k2 = 2, 300, 200, 32, 48
+    assert 4 * B2 * (m2 * r2 + n2 * r2 + 2 * r2 + 2 * r2 * r2 + m2 * r2 + r2 * n2 + 2 * r2 + 1) <= s2
+    assert w2 >= 4 * B2 * (4 * m2 * k2 + m2 * n2)
+    cl.n = 300
+    cl.rank, cl.oversample = 121, 8
+    assert lib.okls_state_bytes(ctypes.byref(cl), None, None) == L.OKLS_ERR_UNSUPPORTED
     c3 = L.config_default(B, m, n)
     c3.rank = 4
     assert lib.okls_state_bytes(ctypes.byref(c3), None, None) == L.OKLS_ERR_INVALID_ARG

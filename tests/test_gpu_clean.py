@@ -164,12 +164,31 @@ CASES = [
     (2, 9, 1, 1, 0, 1, 1, torch.float32, 0.0, "iid"),        # n = 1: U_R spans R^1, G_B and C vanish
 ]
 
+# the batched-GEMM path: m or n past 128, or r + p past 64 (or forced)
+LARGE_CASES = [
+    (2, 200, 144, 16, 8, 1, 2, torch.float32, 0.0, "iid"),
+    (1, 300, 520, 56, 16, 1, 2, torch.float32, 0.1, "iid"),
+    (1, 260, 200, 112, 16, 2, 3, torch.float32, 0.0, "decay"),  # the largest sketch: r + p = 128
+    (2, 160, 96, 12, 4, 1, 2, torch.bfloat16, 0.0, "iid"),
+    (2, 96, 64, 8, 4, 1, 2, torch.float32, 0.0, "iid"),       # a one-CTA shape, forced onto this path
+]
+
 
 @pytest.mark.parametrize("B,m,n,r,p,q,T,dtype,wd,spectrum", CASES)
 def test_teacher_forced_steps(B, m, n, r, p, q, T, dtype, wd, spectrum):
     """spectrum "iid": G with iid N(0, 1) factors; "decay": singular values
     1/(1+k), as in a layer's gradient, where the first (cold) sketch is
     nearly exact and its residual blocks are rounding-dominated."""
+    _teacher_forced(B, m, n, r, p, q, T, dtype, wd, spectrum)
+
+
+@pytest.mark.parametrize("B,m,n,r,p,q,T,dtype,wd,spectrum", LARGE_CASES)
+def test_teacher_forced_steps_large_path(B, m, n, r, p, q, T, dtype, wd, spectrum, monkeypatch):
+    monkeypatch.setenv("OKLS_CLEAN_LARGE", "1")
+    _teacher_forced(B, m, n, r, p, q, T, dtype, wd, spectrum)
+
+
+def _teacher_forced(B, m, n, r, p, q, T, dtype, wd, spectrum):
     lr, b1, b2, eps = 0.01, 0.95, 0.95, 1e-8
     ob = _batch(B, m, n, param_dtype=dtype, lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=wd, root_every=T,
                 rank=r, oversample=p, power_iters=q)
