@@ -5,8 +5,8 @@
 // Sketching": Algorithm 1, Eqn. (8), Appendix A Algorithm 3, Eqns. (10)-(16),
 // Table 1 -- the same method as the one-CTA kernels, restated for tall
 // operands.  Every product with a dimension that grows with m or n is a
-// batched fp32 GEMM (`cl_gemm`: 64 x 64 tiles, 4 x 4 per thread, both
-// operands staged in shared memory); only k x k work (k = r + p) stays in
+// batched fp32 GEMM (`k_cl_gemm`: 128 x 128 tiles, 8 x 8 per thread,
+// double-buffered slices in shared memory); only k x k work (k = r + p) stays in
 // one CTA per matrix: the Cholesky factors and inverses of the thin QRs and
 // of Omega^T Y_nu, the norm estimate for nu, and the Jacobi eigensolve of
 // Z^T Z that yields the thin SVD.  The thin QRs are Cholesky-QR applied four
@@ -21,9 +21,13 @@
 namespace okls {
 
 // ---------------------------------------------------------------- the GEMM
-constexpr int kGT = 64;       // output tile edge
-constexpr int kGK = 16;       // K per stage
-constexpr int kGP = kGT + 4;  // staged pitch (16-byte rows)
+// 128 x 128 output tile per CTA, K in slices of 8, 256 threads with 8 x 8
+// outputs each (two 4-row by two 4-column groups, so that a warp's float4
+// reads of the staged slices are conflict-free); the next slice is fetched
+// into registers while the current one is multiplied (double-buffered shared
+// memory, one barrier per slice).
+constexpr int kGM = 128;  // output tile edge
+constexpr int kGK = 8;    // K per slice
 
 template <typename T>
 __device__ __forceinline__ float cl_ld(const T* p);
@@ -32,74 +36,101 @@ __device__ __forceinline__ float cl_ld<float>(const float* p) { return __ldg(p);
 template <>
 __device__ __forceinline__ float cl_ld<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
+// Four elements of a slice of an operand staged as [k][128]: `trans` says
+// whether the operand's rows are k (stored K x rows, ld) or the tile's
+// rows (stored rows x K, ld).  Out-of-range elements read as 0.
+template <typename T>
+__device__ __forceinline__ void cl_fetch(const T* X, bool kmajor, int64_t ld, int row0, int rows, int k0, int K,
+                                         float v[4], int& kk, int& i0) {
+  const int t = threadIdx.x;
+  if (kmajor) {  // element (k, i) at X[k ld + i]: a slice row is 128 contiguous entries
+    kk = t >> 5;
+    i0 = (t & 31) * 4;
+    const int gk = k0 + kk;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gi = row0 + i0 + u;
+      v[u] = (gk < K && gi < rows) ? cl_ld<T>(X + static_cast<int64_t>(gk) * ld + gi) : 0.0f;
+    }
+  } else {  // element (k, i) at X[i ld + k]: 8 contiguous k per row
+    i0 = t >> 1;
+    kk = (t & 1) * 4;
+    const int gi = row0 + i0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gk = k0 + kk + u;
+      v[u] = (gk < K && gi < rows) ? cl_ld<T>(X + static_cast<int64_t>(gi) * ld + gk) : 0.0f;
+    }
+  }
+}
+
+__device__ __forceinline__ void cl_stage(float (*S)[kGM], bool kmajor, const float v[4], int kk, int i0) {
+  if (kmajor) {
+    *reinterpret_cast<float4*>(&S[kk][i0]) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) S[kk + u][i0] = v[u];
+  }
+}
+
 // C[b] = alpha op(A[b]) op(B[b]) + beta_b C[b], beta_b = beta_dev ? beta_dev[b] : beta.
 // A is M x K (lda), or K x M when ta; B is K x N (ldb), or N x K when tb.
 template <typename TA, typename TB>
 __global__ void __launch_bounds__(256) k_cl_gemm(ClGemm g) {
-  __shared__ __align__(16) float As[kGK][kGP];
-  __shared__ __align__(16) float Bs[kGK][kGP];
+  __shared__ __align__(16) float As[2][kGK][kGM];
+  __shared__ __align__(16) float Bs[2][kGK][kGM];
   const int b = blockIdx.z;
   const TA* A = static_cast<const TA*>(g.A) + static_cast<int64_t>(b) * g.sA;
   const TB* B = static_cast<const TB*>(g.B) + static_cast<int64_t>(b) * g.sB;
   float* C = g.C + static_cast<int64_t>(b) * g.sC;
-  const int m0 = blockIdx.y * kGT, n0 = blockIdx.x * kGT;
+  const int m0 = blockIdx.y * kGM, n0 = blockIdx.x * kGM;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
+  // A is staged [k][m]: k-major when stored K x M (ta); B is staged [k][n]:
+  // k-major when stored K x N (not tb)
+  const bool a_kmaj = g.ta != 0, b_kmaj = g.tb == 0;
+  float acc[8][8] = {};
+  float va[4], vb[4];
+  int akk, ai0, bkk, bi0;
+  cl_fetch<TA>(A, a_kmaj, g.lda, m0, g.M, 0, g.K, va, akk, ai0);
+  cl_fetch<TB>(B, b_kmaj, g.ldb, n0, g.N, 0, g.K, vb, bkk, bi0);
+  cl_stage(As[0], a_kmaj, va, akk, ai0);
+  cl_stage(Bs[0], b_kmaj, vb, bkk, bi0);
+  __syncthreads();
+  int buf = 0;
   for (int k0 = 0; k0 < g.K; k0 += kGK) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int e = threadIdx.x + 256 * s;
-      // A tile (kGT rows of M, kGK of K) into As[k][m]
-      int i, kk;
-      if (g.ta) {
-        kk = e >> 6;
-        i = e & 63;
-      } else {
-        i = e >> 4;
-        kk = e & 15;
-      }
-      const int gm = m0 + i, gk = k0 + kk;
-      float va = 0.0f;
-      if (gm < g.M && gk < g.K)
-        va = cl_ld<TA>(g.ta ? A + static_cast<int64_t>(gk) * g.lda + gm : A + static_cast<int64_t>(gm) * g.lda + gk);
-      As[kk][i] = va;
-      // B tile (kGK of K, kGT columns of N) into Bs[k][n]
-      int j, kb;
-      if (g.tb) {
-        j = e >> 4;
-        kb = e & 15;
-      } else {
-        kb = e >> 6;
-        j = e & 63;
-      }
-      const int gn = n0 + j, gkb = k0 + kb;
-      float vb = 0.0f;
-      if (gn < g.N && gkb < g.K)
-        vb = cl_ld<TB>(g.tb ? B + static_cast<int64_t>(gn) * g.ldb + gkb : B + static_cast<int64_t>(gkb) * g.ldb + gn);
-      Bs[kb][j] = vb;
+    const bool more = k0 + kGK < g.K;
+    if (more) {
+      cl_fetch<TA>(A, a_kmaj, g.lda, m0, g.M, k0 + kGK, g.K, va, akk, ai0);
+      cl_fetch<TB>(B, b_kmaj, g.ldb, n0, g.N, k0 + kGK, g.K, vb, bkk, bi0);
     }
-    __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < kGK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
-      const float4 bq = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 8; ++u)
 #pragma unroll
-        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+        for (int v = 0; v < 8; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+    }
+    if (more) {
+      cl_stage(As[buf ^ 1], a_kmaj, va, akk, ai0);
+      cl_stage(Bs[buf ^ 1], b_kmaj, vb, bkk, bi0);
     }
     __syncthreads();
+    buf ^= 1;
   }
   const float beta = g.beta_dev ? g.beta_dev[b] : g.beta;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int gm = m0 + ty * 4 + u;
+  for (int u = 0; u < 8; ++u) {
+    const int gm = m0 + (u < 4 ? ty * 4 + u : 64 + ty * 4 + u - 4);
     if (gm >= g.M) continue;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int gn = n0 + tx * 4 + v;
+    for (int v = 0; v < 8; ++v) {
+      const int gn = n0 + (v < 4 ? tx * 4 + v : 64 + tx * 4 + v - 4);
       if (gn >= g.N) continue;
       float* c = C + static_cast<int64_t>(gm) * g.ldc + gn;
       *c = beta == 0.0f ? g.alpha * acc[u][v] : fmaf(g.alpha, acc[u][v], beta * *c);
@@ -107,6 +138,19 @@ __global__ void __launch_bounds__(256) k_cl_gemm(ClGemm g) {
   }
 }
 
+cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return cudaSuccess;
+  const dim3 grid((g.N + kGM - 1) / kGM, (g.M + kGM - 1) / kGM, g.batch);
+  if (g.a_bf16 && g.b_bf16)
+    k_cl_gemm<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(g);
+  else if (g.a_bf16)
+    k_cl_gemm<__nv_bfloat16, float><<<grid, 256, 0, st>>>(g);
+  else if (g.b_bf16)
+    k_cl_gemm<float, __nv_bfloat16><<<grid, 256, 0, st>>>(g);
+  else
+    k_cl_gemm<float, float><<<grid, 256, 0, st>>>(g);
+  return cudaGetLastError();
+}
 
 // ------------------------------------------------------------- k x k kernels
 constexpr int kLK = 128;           // largest k = r + p
@@ -548,19 +592,6 @@ __global__ void k_cl_install(ClLarge L) {
   }
 }
 
-cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st) {
-  if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return cudaSuccess;
-  const dim3 grid((g.N + kGT - 1) / kGT, (g.M + kGT - 1) / kGT, g.batch);
-  if (g.a_bf16 && g.b_bf16)
-    k_cl_gemm<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(g);
-  else if (g.a_bf16)
-    k_cl_gemm<__nv_bfloat16, float><<<grid, 256, 0, st>>>(g);
-  else if (g.b_bf16)
-    k_cl_gemm<float, __nv_bfloat16><<<grid, 256, 0, st>>>(g);
-  else
-    k_cl_gemm<float, float><<<grid, 256, 0, st>>>(g);
-  return cudaGetLastError();
-}
 
 
 // ------------------------------------------------------------- orchestration
