@@ -479,6 +479,43 @@ def run_okls(args):
                         "tflops_dense": sum_over_ranks(fs * args.steps, ws, dev) / (ms3 / 1e3) / 1e12,
                         "gemm_tflops": gt}
 
+    clean_large_line = None
+    if args.also_clean_large and args.method == "okls" and args.workload == "llama1.2b":
+        # Clean over the same layer set: rank 120 + oversampling 8 (the pages'
+        # 1.3B runs use rank 256; this build's k x k kernels take r + p <= 128),
+        # one power iteration, a refresh every 10 steps, the pages' betas
+        rebuild(method="clean", rank=120, oversample=8, power_iters=1, root_every=10, beta1=0.95, beta2=0.95,
+                eps=1e-8, weight_decay=0.0, lr=args.lr)
+        cgen = torch.Generator(device=dev)
+        cgen.manual_seed(wl.seed + 29)
+        cnoise = [torch.randn(ob.noise_shape, generator=cgen, device=dev) for (_g, ob, _W, _G) in groups]
+
+        def clean_step(k):
+            for i, (_g, ob, W, Gs) in enumerate(groups):
+                ob.step(W, Gs[k % len(Gs)], args.lr, noise=cnoise[i] if ob.refresh_due else None)
+        for k in range(3):
+            clean_step(k)
+        torch.cuda.synchronize()
+        csteps = 20
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(csteps):
+            clean_step(k)
+        b.record(stream)
+        torch.cuda.synchronize()
+        for (_g, ob, _W, _G) in groups:
+            if ob.status_nothrow()[1]:
+                raise RuntimeError("device status flagged in the Clean leg")
+        ms5 = max_over_ranks(a.elapsed_time(b), ws, dev)
+        clean_large_line = {
+            "method": "Clean (block Adam in rank-120 Nystrom bases, oversampling 8, one power iteration, refresh "
+                      "every 10 steps); batched fp32 GEMMs, k x k work in one CTA per matrix",
+            "workload": "the same 168-matrix layer set, bf16 W and G", "steps": csteps,
+            "value": sum_over_ranks(matrices * csteps, ws, dev) / (ms5 / 1e3), "unit": "matrices/s",
+            "ms_per_step": ms5 / csteps,
+            "state_gb": sum(ob.state.numel() for (_g, ob, _W, _G) in groups) / 1e9}
+        del cnoise
+
     def small_leg(method, **kw):
         """One 128 x 64 matrix (the one-CTA methods take m, n <= 128 in this
         build), 200 timed steps after 20 warm-up steps; Clean's Gaussian
@@ -567,6 +604,8 @@ def run_okls(args):
             line["soap"] = soap_line
         if clean_line:
             line["clean"] = clean_line
+        if clean_large_line:
+            line["clean_large"] = clean_large_line
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -590,6 +629,7 @@ def main():
     ap.add_argument("--also-shampoo", type=int, default=1)
     ap.add_argument("--also-soap", type=int, default=1)
     ap.add_argument("--also-clean", type=int, default=1)
+    ap.add_argument("--also-clean-large", type=int, default=1)
     ap.add_argument("--method", choices=["okls", "shampoo", "soap"], default="okls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
