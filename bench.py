@@ -481,10 +481,9 @@ def run_okls(args):
 
     clean_large_line = None
     if args.also_clean_large and args.method == "okls" and args.workload == "llama1.2b":
-        # Clean over the same layer set: rank 120 + oversampling 8 (the pages'
-        # 1.3B runs use rank 256; this build's k x k kernels take r + p <= 128),
-        # one power iteration, a refresh every 10 steps, the pages' betas
-        rebuild(method="clean", rank=120, oversample=8, power_iters=1, root_every=10, beta1=0.95, beta2=0.95,
+        # Clean over the same layer set with the pages' 1.3B settings: rank 256,
+        # oversampling 8, one power iteration, a refresh every 10 steps, betas 0.95
+        rebuild(method="clean", rank=256, oversample=8, power_iters=1, root_every=10, beta1=0.95, beta2=0.95,
                 eps=1e-8, weight_decay=0.0, lr=args.lr)
         cgen = torch.Generator(device=dev)
         cgen.manual_seed(wl.seed + 29)
@@ -508,8 +507,8 @@ def run_okls(args):
                 raise RuntimeError("device status flagged in the Clean leg")
         ms5 = max_over_ranks(a.elapsed_time(b), ws, dev)
         clean_large_line = {
-            "method": "Clean (block Adam in rank-120 Nystrom bases, oversampling 8, one power iteration, refresh "
-                      "every 10 steps); batched fp32 GEMMs, k x k work in one CTA per matrix",
+            "method": "Clean (block Adam in rank-256 Nystrom bases, oversampling 8, one power iteration, refresh "
+                      "every 10 steps, betas 0.95); batched fp32 GEMMs, k x k work in one CTA per matrix",
             "workload": "the same 168-matrix layer set, bf16 W and G", "steps": csteps,
             "value": sum_over_ranks(matrices * csteps, ws, dev) / (ms5 / 1e3), "unit": "matrices/s",
             "ms_per_step": ms5 / csteps,

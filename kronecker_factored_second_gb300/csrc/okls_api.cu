@@ -877,6 +877,7 @@ okls_status plan_clean(const okls_config& c, uint8_t* state, uint8_t* ws, okls_h
     cl.Cb = f32(wp, B * m * n);
     cl.part = f32(wp, B * kClParts);
     cl.cden = f32(wp, B);
+    cl.KK = k > 128 ? f32(wp, B * 2 * (k + 1) * (k + 1)) : nullptr;
   }
   out->state_bytes = sp.off;
   out->ws_bytes = wp.off;
@@ -1067,9 +1068,9 @@ okls_status validate(const okls_config* c) {
     const int64_t k = static_cast<int64_t>(c->rank) + c->oversample;
     if (k > c->m || k > c->n)
       return fail(OKLS_ERR_INVALID_ARG, "rank + oversample (%lld) exceeds min(m, n)", static_cast<long long>(k));
-    if (c->m > 16384 || c->n > 16384 || k > 128)
-      return fail(OKLS_ERR_UNSUPPORTED,
-                  "Clean runs for m, n <= 16384 and rank + oversample <= 128 in this build (k x k work in one CTA)");
+    if (c->m > 16384 || c->n > 16384 || k > kClMaxK)
+      return fail(OKLS_ERR_UNSUPPORTED, "Clean runs for m, n <= 16384 and rank + oversample <= %d in this build",
+                  kClMaxK);
   } else if (c->rank != 0 || c->oversample != 0 || c->power_iters != 0) {
     return fail(OKLS_ERR_INVALID_ARG, "rank, oversample and power_iters are Clean's; leave them zero");
   }

@@ -1,5 +1,5 @@
 // Clean for shapes past one CTA's shared memory: m, n up to 16384 and
-// r + p <= 128 (sm_103a).
+// r + p <= 544 (sm_103a).
 //
 // Page "Clean: Second-order LLM Training at Linear Memory Cost via Nystrom
 // Sketching": Algorithm 1, Eqn. (8), Appendix A Algorithm 3, Eqns. (10)-(16),
@@ -153,10 +153,34 @@ cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------- k x k kernels
-constexpr int kLK = 128;           // largest k = r + p
-constexpr int kLP = kLK + 1;       // odd pitch of the staged k x k matrices
+// Up to k = kLK the two k x k matrices of these kernels live in shared
+// memory; past it (k <= kClMaxK) in a per-matrix workspace slice of
+// 2 (k + 1)^2 floats, which stays in L2 -- the same code, a slower access.
+constexpr int kLK = 128;
+constexpr int kLP = kLK + 1;        // odd pitch of the staged k x k matrices
 constexpr int kLThreads = 256;
-constexpr int kLSmallSmem = 2 * kLK * kLP * 4 + 4 * kLK * 4;
+constexpr int kLVec = 2 * kClMaxK;  // floats: vectors / rotation parameters
+constexpr int kLInts = 2 * kClMaxK; // ints: pairs, then ranks
+constexpr int kLHead = kLVec + kLInts;
+constexpr int kLSmallSmem = (kLHead + 2 * kLK * kLP) * 4;
+// up to here the k x k matrix of the Cholesky and eigensolve kernels fits
+// shared memory as a packed triangle
+constexpr int kPackMaxK = 330;
+
+struct KkStore {
+  float* a;
+  float* b;
+  int ld;
+};
+
+__device__ __forceinline__ KkStore kk_store(float* sm, float* scratch, int k) {
+  if (k <= kLK) return {sm + kLHead, sm + kLHead + kLK * kLP, kLP};
+  // (k + 1) rows of pitch k + 1: the Jacobi iteration pads an odd k by one
+  float* g = scratch + static_cast<int64_t>(blockIdx.x) * 2 * (k + 1) * (k + 1);
+  return {g, g + static_cast<int64_t>(k + 1) * (k + 1), k + 1};
+}
+
+inline int kk_smem(int k) { return k <= kLK ? kLSmallSmem : kLHead * 4; }
 
 __device__ __forceinline__ bool cl_flagged(const uint32_t* status) {
   return __syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(status) != 0u);
@@ -183,15 +207,17 @@ __device__ __forceinline__ float cl_block_sum(float v, float* red) {
 // a partial orthogonalisation that the next pass completes.  A breakdown
 // that remains raises kStNonfiniteIter.
 __global__ void __launch_bounds__(kLThreads) k_cl_chol_inv(const float* Gram, float* Rinv, int k, int d, int adaptive,
-                                                           uint32_t* status) {
+                                                           float* scratch, uint32_t* status) {
   extern __shared__ float sm[];
   __shared__ float red[kLThreads / 32];
   __shared__ float piv;
   const int b = blockIdx.x;
   const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
   float* Rb = Rinv + static_cast<int64_t>(b) * k * k;
-  float* Ls = sm;              // k x k, lower triangle used
-  float* Xs = sm + kLK * kLP;  // L^-1, column by column
+  const KkStore ks = kk_store(sm, scratch, k);
+  const int ld = ks.ld;
+  float* Ls = ks.a;  // k x k, lower triangle used
+  float* Xs = ks.b;  // L^-1, column by column
   float tr = 0.0f;
   for (int e = threadIdx.x; e < k * k; e += blockDim.x)
     if (e / k == e % k) tr += Gb[e];
@@ -201,25 +227,25 @@ __global__ void __launch_bounds__(kLThreads) k_cl_chol_inv(const float* Gram, fl
     const float sh = attempt == 0 ? 0.0f : 11.0f * (k + sqrtf(static_cast<float>(d))) * 5.9604645e-8f * tr;
     for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
       const int i = e / k, j = e % k;
-      Ls[i * kLP + j] = 0.5f * (Gb[i * k + j] + Gb[j * k + i]) + (i == j ? sh : 0.0f);
+      Ls[i * ld + j] = 0.5f * (Gb[i * k + j] + Gb[j * k + i]) + (i == j ? sh : 0.0f);
     }
     __syncthreads();
     bad = false;
     for (int j = 0; j < k; ++j) {
       if (threadIdx.x == 0) {
-        const float djj = Ls[j * kLP + j];
+        const float djj = Ls[j * ld + j];
         piv = djj > 0.0f ? sqrtf(djj) : 0.0f;
       }
       __syncthreads();
       const float cj = piv;
       if (!(cj > 0.0f)) bad = true;
       for (int i = j + threadIdx.x; i < k; i += blockDim.x)
-        Ls[i * kLP + j] = i == j ? cj : (cj > 0.0f ? Ls[i * kLP + j] / cj : 0.0f);
+        Ls[i * ld + j] = i == j ? cj : (cj > 0.0f ? Ls[i * ld + j] / cj : 0.0f);
       __syncthreads();
       const int w = k - j - 1;
       for (int e = threadIdx.x; e < w * w; e += blockDim.x) {
         const int i = j + 1 + e / w, l = j + 1 + e % w;
-        if (l <= i) Ls[i * kLP + l] = fmaf(-Ls[i * kLP + j], Ls[l * kLP + j], Ls[i * kLP + l]);
+        if (l <= i) Ls[i * ld + l] = fmaf(-Ls[i * ld + j], Ls[l * ld + j], Ls[i * ld + l]);
       }
       __syncthreads();
     }
@@ -231,53 +257,117 @@ __global__ void __launch_bounds__(kLThreads) k_cl_chol_inv(const float* Gram, fl
   }
   // column c of L^-1 by forward substitution (one thread per column)
   for (int c = threadIdx.x; c < k; c += blockDim.x) {
-    for (int i = 0; i < c; ++i) Xs[i * kLP + c] = 0.0f;
-    Xs[c * kLP + c] = 1.0f / Ls[c * kLP + c];
+    for (int i = 0; i < c; ++i) Xs[i * ld + c] = 0.0f;
+    Xs[c * ld + c] = 1.0f / Ls[c * ld + c];
     for (int i = c + 1; i < k; ++i) {
       float v = 0.0f;
-      for (int l = c; l < i; ++l) v = fmaf(Ls[i * kLP + l], Xs[l * kLP + c], v);
-      Xs[i * kLP + c] = -v / Ls[i * kLP + i];
+      for (int l = c; l < i; ++l) v = fmaf(Ls[i * ld + l], Xs[l * ld + c], v);
+      Xs[i * ld + c] = -v / Ls[i * ld + i];
     }
   }
   __syncthreads();
   // Rinv = (L^-1)^T
   for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
     const int i = e / k, j = e % k;
-    Rb[e] = Xs[j * kLP + i];
+    Rb[e] = Xs[j * ld + i];
   }
 }
 
-// nu = spacing of binary32 numbers at ||Y||_2, ||Y||_2^2 the largest
-// eigenvalue of the Gram matrix Y^T Y (60 power steps in one warp).
-__global__ void __launch_bounds__(kLThreads) k_cl_norm(const float* Gram, float* nu, int k) {
+// The same factorisation for 128 < k <= kPackMaxK with L as a packed lower
+// triangle in shared memory; each thread forward-substitutes a column of
+// L^-1 straight into the matching row of Rinv = L^-T.
+__device__ __forceinline__ int pl_idx(int i, int j) { return i * (i + 1) / 2 + j; }  // i >= j
+
+__global__ void __launch_bounds__(kLThreads) k_cl_chol_inv_packed(const float* Gram, float* Rinv, int k, int d,
+                                                                  int adaptive, uint32_t* status) {
   extern __shared__ float sm[];
+  __shared__ float red[kLThreads / 32];
+  __shared__ float piv;
   const int b = blockIdx.x;
   const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
-  float* As = sm;
-  float* v = sm + kLK * kLP;  // 2 k
-  for (int e = threadIdx.x; e < k * k; e += blockDim.x) As[(e / k) * kLP + e % k] = Gb[e];
+  float* Rb = Rinv + static_cast<int64_t>(b) * k * k;
+  float* Ls = sm + kLHead;
+  float tr = 0.0f;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) tr += Gb[i * k + i];
+  tr = cl_block_sum(tr, red);
+  bool bad = false;
+  for (int attempt = 0; attempt < (adaptive ? 2 : 1); ++attempt) {
+    const float sh = attempt == 0 ? 0.0f : 11.0f * (k + sqrtf(static_cast<float>(d))) * 5.9604645e-8f * tr;
+    for (int i = threadIdx.x; i < k; i += blockDim.x)
+      for (int j = 0; j <= i; ++j) Ls[pl_idx(i, j)] = 0.5f * (Gb[i * k + j] + Gb[j * k + i]) + (i == j ? sh : 0.0f);
+    __syncthreads();
+    bad = false;
+    for (int j = 0; j < k; ++j) {
+      if (threadIdx.x == 0) {
+        const float djj = Ls[pl_idx(j, j)];
+        piv = djj > 0.0f ? sqrtf(djj) : 0.0f;
+      }
+      __syncthreads();
+      const float cj = piv;
+      if (!(cj > 0.0f)) bad = true;
+      for (int i = j + threadIdx.x; i < k; i += blockDim.x)
+        Ls[pl_idx(i, j)] = i == j ? cj : (cj > 0.0f ? Ls[pl_idx(i, j)] / cj : 0.0f);
+      __syncthreads();
+      const int w = k - j - 1;
+      for (int e = threadIdx.x; e < w * w; e += blockDim.x) {
+        const int i = j + 1 + e / w, l = j + 1 + e % w;
+        if (l <= i) Ls[pl_idx(i, l)] = fmaf(-Ls[pl_idx(i, j)], Ls[pl_idx(l, j)], Ls[pl_idx(i, l)]);
+      }
+      __syncthreads();
+    }
+    if (!__syncthreads_or(bad)) break;
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) atomicOr(status, kStNonfiniteIter);
+    return;
+  }
+  for (int c = threadIdx.x; c < k; c += blockDim.x) {
+    float* x = Rb + static_cast<int64_t>(c) * k;  // row c of Rinv = column c of L^-1
+    for (int i = 0; i < c; ++i) x[i] = 0.0f;
+    x[c] = 1.0f / Ls[pl_idx(c, c)];
+    for (int i = c + 1; i < k; ++i) {
+      float v = 0.0f;
+      for (int l = c; l < i; ++l) v = fmaf(Ls[pl_idx(i, l)], x[l], v);
+      x[i] = -v / Ls[pl_idx(i, i)];
+    }
+  }
+}
+
+inline int packed_chol_smem(int k) { return (kLHead + k * (k + 1) / 2) * 4; }
+
+// nu = spacing of binary32 numbers at ||Y||_2, ||Y||_2^2 the largest
+// eigenvalue of the Gram matrix Y^T Y (60 power steps; every warp takes
+// rows of the product).
+__global__ void __launch_bounds__(kLThreads) k_cl_norm(const float* Gram, float* nu, int k, float* scratch) {
+  extern __shared__ float sm[];
+  __shared__ float red[kLThreads / 32];
+  const int b = blockIdx.x;
+  const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
+  const KkStore ks = kk_store(sm, scratch, k);
+  const int ld = ks.ld;
+  float* As = ks.a;
+  float* v = sm;  // 2 k: the iterate and its image
+  for (int e = threadIdx.x; e < k * k; e += blockDim.x) As[(e / k) * ld + e % k] = Gb[e];
+  for (int j = threadIdx.x; j < k; j += blockDim.x) v[j] = 1.0f;
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  for (int j = lane; j < k; j += 32) v[j] = 1.0f;
-  __syncwarp();
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   float nrm = 0.0f;
   for (int it = 0; it < 60; ++it) {
     float s2 = 0.0f;
-    for (int i = lane; i < k; i += 32) {
+    for (int i = w; i < k; i += nw) {
       float s = 0.0f;
-      for (int j = 0; j < k; ++j) s = fmaf(As[i * kLP + j], v[j], s);
-      v[kLK + i] = s;
+      for (int j = lane; j < k; j += 32) s = fmaf(As[static_cast<int64_t>(i) * ld + j], v[j], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) v[kClMaxK + i] = s;
       s2 = fmaf(s, s, s2);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-    nrm = sqrtf(s2);
-    __syncwarp();
-    for (int i = lane; i < k; i += 32) v[i] = nrm > 0.0f ? v[kLK + i] / nrm : 0.0f;
-    __syncwarp();
+    // s2 is the same on every lane of a warp: count it once per warp
+    nrm = sqrtf(cl_block_sum(lane == 0 ? s2 : 0.0f, red));
+    for (int i = threadIdx.x; i < k; i += blockDim.x) v[i] = nrm > 0.0f ? v[kClMaxK + i] / nrm : 0.0f;
+    __syncthreads();
   }
-  if (lane == 0) {
+  if (threadIdx.x == 0) {
     const float yn = sqrtf(nrm);
     nu[b] = yn > 0.0f ? ldexpf(1.0f, ilogbf(yn) - 23) : 0.0f;
   }
@@ -290,28 +380,30 @@ __global__ void __launch_bounds__(kLThreads) k_cl_norm(const float* Gram, float*
 // k x r; null at the first refresh); and Lambda_c = max(0, sigma_j^2 - nu).
 __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const float* P, const float* nu, float* WU,
                                                       float* lam, int k, int r, int max_sweeps, float tol2,
-                                                      const uint32_t* status) {
+                                                      float* scratch, const uint32_t* status) {
   extern __shared__ float sm[];
   __shared__ float red[kLThreads / 32];
   if (cl_flagged(status)) return;
   const int b = blockIdx.x;
   const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
-  float* As = sm;
-  float* Vs = sm + kLK * kLP;
-  float* cs = Vs + kLK * kLP;            // 2 per pair
-  int* pr = reinterpret_cast<int*>(cs + kLK);  // 2 per pair, then ranks
+  const KkStore ks = kk_store(sm, scratch, k);
+  const int ld = ks.ld;
+  float* As = ks.a;
+  float* Vs = ks.b;
+  float* cs = sm;                                  // 2 per pair
+  int* pr = reinterpret_cast<int*>(sm + kLVec);    // 2 per pair, then ranks
   const int dp = k + (k & 1), np = dp / 2;
   for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
     const int i = e / dp, j = e % dp;
-    As[i * kLP + j] = (i < k && j < k) ? 0.5f * (Gb[i * k + j] + Gb[j * k + i]) : 0.0f;
-    Vs[i * kLP + j] = i == j ? 1.0f : 0.0f;
+    As[i * ld + j] = (i < k && j < k) ? 0.5f * (Gb[i * k + j] + Gb[j * k + i]) : 0.0f;
+    Vs[i * ld + j] = i == j ? 1.0f : 0.0f;
   }
   __syncthreads();
   for (int sweep = 0; sweep < max_sweeps; ++sweep) {
     float off = 0.0f, dg = 0.0f;
     for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) {
       const int i = e / dp, j = e % dp;
-      const float v = As[i * kLP + j];
+      const float v = As[i * ld + j];
       if (i == j)
         dg = fmaf(v, v, dg);
       else
@@ -329,10 +421,10 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
           pp = qq;
           qq = x;
         }
-        const float apq = As[pp * kLP + qq];
+        const float apq = As[pp * ld + qq];
         float c = 1.0f, sn = 0.0f;
         if (apq != 0.0f) {
-          const float th = (As[qq * kLP + qq] - As[pp * kLP + pp]) / (2.0f * apq);
+          const float th = (As[qq * ld + qq] - As[pp * ld + pp]) / (2.0f * apq);
           const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
           c = rsqrtf(fmaf(t, t, 1.0f));
           sn = t * c;
@@ -347,31 +439,31 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
         const int q = e / dp, j = e % dp;
         const int pp = pr[2 * q], qq = pr[2 * q + 1];
         const float c = cs[2 * q], sn = cs[2 * q + 1];
-        const float ap = As[pp * kLP + j], aq = As[qq * kLP + j];
-        As[pp * kLP + j] = c * ap - sn * aq;
-        As[qq * kLP + j] = sn * ap + c * aq;
+        const float ap = As[pp * ld + j], aq = As[qq * ld + j];
+        As[pp * ld + j] = c * ap - sn * aq;
+        As[qq * ld + j] = sn * ap + c * aq;
       }
       __syncthreads();
       for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
         const int q = e / dp, i = e % dp;
         const int pp = pr[2 * q], qq = pr[2 * q + 1];
         const float c = cs[2 * q], sn = cs[2 * q + 1];
-        const float ap = As[i * kLP + pp], aq = As[i * kLP + qq];
-        As[i * kLP + pp] = c * ap - sn * aq;
-        As[i * kLP + qq] = sn * ap + c * aq;
-        const float vp = Vs[i * kLP + pp], vq = Vs[i * kLP + qq];
-        Vs[i * kLP + pp] = c * vp - sn * vq;
-        Vs[i * kLP + qq] = sn * vp + c * vq;
+        const float ap = As[i * ld + pp], aq = As[i * ld + qq];
+        As[i * ld + pp] = c * ap - sn * aq;
+        As[i * ld + qq] = sn * ap + c * aq;
+        const float vp = Vs[i * ld + pp], vq = Vs[i * ld + qq];
+        Vs[i * ld + pp] = c * vp - sn * vq;
+        Vs[i * ld + qq] = sn * vp + c * vq;
       }
       __syncthreads();
     }
   }
   // ranks by decreasing Sigma^2 (ties by index)
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
-    const float lj = As[j * kLP + j];
+    const float lj = As[j * ld + j];
     int rank = 0;
     for (int i = 0; i < k; ++i) {
-      const float li = As[i * kLP + i];
+      const float li = As[i * ld + i];
       rank += (li > lj) || (li == lj && i < j);
     }
     pr[j] = rank;
@@ -383,17 +475,163 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
     const int c = pr[j];
     if (c >= r) continue;
-    const float s2 = As[j * kLP + j];
+    const float s2 = As[j * ld + j];
     const float inv = s2 > 0.0f ? rsqrtf(s2) : 0.0f;
     float sg = 1.0f;
     if (Pb) {
       float dot = 0.0f;
-      for (int l = 0; l < k; ++l) dot = fmaf(Vs[l * kLP + j], Pb[l * r + c], dot);
+      for (int l = 0; l < k; ++l) dot = fmaf(Vs[l * ld + j], Pb[l * r + c], dot);
       sg = dot < 0.0f ? -1.0f : 1.0f;
     }
-    for (int l = 0; l < k; ++l) W[l * r + c] = sg * inv * Vs[l * kLP + j];
+    for (int l = 0; l < k; ++l) W[l * r + c] = sg * inv * Vs[l * ld + j];
     lam[static_cast<int64_t>(b) * r + c] = fmaxf(0.0f, s2 - nub);
   }
+}
+
+// The same thin SVD for 128 < k <= kPackMaxK: Z^T Z kept in shared memory as
+// a packed upper triangle (padded to an even size dp), the eigenvectors as
+// V^T rows in the L2-resident scratch.  A round's d'/2 disjoint rotations
+// (J_pq acting on rows and columns p, q) are applied as one pass over the
+// 2 x 2 blocks A[{p1, q1}, {p2, q2}] of every two pairs of the round
+// (block <- J1^T block J2; each unordered index pair lies in exactly one
+// block) and over the V^T rows p, q: two barriers per round.
+__device__ __forceinline__ int pk_idx(int i, int j, int dp) {  // i <= j
+  return i * dp - (i * (i - 1)) / 2 + (j - i);
+}
+__device__ __forceinline__ float pk_get(const float* A, int i, int j, int dp) {
+  return i <= j ? A[pk_idx(i, j, dp)] : A[pk_idx(j, i, dp)];
+}
+__device__ __forceinline__ void pk_set(float* A, int i, int j, int dp, float v) {
+  if (i <= j)
+    A[pk_idx(i, j, dp)] = v;
+  else
+    A[pk_idx(j, i, dp)] = v;
+}
+
+__global__ void __launch_bounds__(kLThreads) k_cl_svd_packed(const float* Gram, const float* P, const float* nu,
+                                                             float* WU, float* lam, int k, int r, int max_sweeps,
+                                                             float tol2, float* scratch, const uint32_t* status) {
+  extern __shared__ float sm[];
+  __shared__ float red[kLThreads / 32];
+  if (cl_flagged(status)) return;
+  const int b = blockIdx.x;
+  const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
+  const int dp = k + (k & 1), np = dp / 2;
+  float* cs = sm;                                // 2 per pair
+  int* pr = reinterpret_cast<int*>(sm + kLVec);  // 2 per pair, then ranks
+  float* A = sm + kLHead;                        // packed upper triangle, dp (dp + 1) / 2
+  float* Vt = scratch + static_cast<int64_t>(b) * 2 * (k + 1) * (k + 1);  // dp x dp, row c = column c of V
+  for (int j = threadIdx.x; j < dp; j += blockDim.x)
+    for (int i = 0; i <= j; ++i)
+      A[pk_idx(i, j, dp)] = (i < k && j < k) ? 0.5f * (Gb[i * k + j] + Gb[j * k + i]) : 0.0f;
+  for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) Vt[e] = (e / dp == e % dp) ? 1.0f : 0.0f;
+  __syncthreads();
+  for (int sweep = 0; sweep < max_sweeps; ++sweep) {
+    float off = 0.0f, dg = 0.0f;
+    for (int j = threadIdx.x; j < dp; j += blockDim.x)
+      for (int i = 0; i <= j; ++i) {
+        const float v = A[pk_idx(i, j, dp)];
+        if (i == j)
+          dg = fmaf(v, v, dg);
+        else
+          off = fmaf(2.0f * v, v, off);
+      }
+    const float offs = cl_block_sum(off, red);
+    const float dgs = cl_block_sum(dg, red);
+    if (!(offs > tol2 * dgs)) break;
+    for (int rd = 0; rd < dp - 1; ++rd) {
+      for (int q = threadIdx.x; q < np; q += blockDim.x) {
+        auto idx = [&](int pos) { return pos == 0 ? 0 : 1 + (pos - 1 + rd) % (dp - 1); };
+        int pp = idx(q), qq = idx(dp - 1 - q);
+        if (pp > qq) {
+          const int x = pp;
+          pp = qq;
+          qq = x;
+        }
+        const float apq = A[pk_idx(pp, qq, dp)];
+        float c = 1.0f, sn = 0.0f;
+        if (apq != 0.0f) {
+          const float th = (A[pk_idx(qq, qq, dp)] - A[pk_idx(pp, pp, dp)]) / (2.0f * apq);
+          const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
+          c = rsqrtf(fmaf(t, t, 1.0f));
+          sn = t * c;
+        }
+        cs[2 * q] = c;
+        cs[2 * q + 1] = sn;
+        pr[2 * q] = pp;
+        pr[2 * q + 1] = qq;
+      }
+      __syncthreads();
+      // A <- J^T A J on the 2 x 2 blocks of pairs (u, v), u <= v
+      for (int e = threadIdx.x; e < np * np; e += blockDim.x) {
+        const int u = e / np, v = e % np;
+        if (u > v) continue;
+        const int p1 = pr[2 * u], q1 = pr[2 * u + 1], p2 = pr[2 * v], q2 = pr[2 * v + 1];
+        const float c1 = cs[2 * u], s1 = cs[2 * u + 1], c2 = cs[2 * v], s2 = cs[2 * v + 1];
+        const float a11 = pk_get(A, p1, p2, dp), a12 = pk_get(A, p1, q2, dp);
+        const float a21 = pk_get(A, q1, p2, dp), a22 = pk_get(A, q1, q2, dp);
+        // rows: J1^T = [[c1, -s1], [s1, c1]]
+        const float r11 = c1 * a11 - s1 * a21, r12 = c1 * a12 - s1 * a22;
+        const float r21 = s1 * a11 + c1 * a21, r22 = s1 * a12 + c1 * a22;
+        // columns: J2 = [[c2, s2], [-s2, c2]]
+        const float n11 = c2 * r11 - s2 * r12, n12 = s2 * r11 + c2 * r12;
+        const float n21 = c2 * r21 - s2 * r22, n22 = s2 * r21 + c2 * r22;
+        if (u == v) {
+          pk_set(A, p1, p1, dp, n11);
+          pk_set(A, p1, q1, dp, n12);
+          pk_set(A, q1, q1, dp, n22);
+        } else {
+          pk_set(A, p1, p2, dp, n11);
+          pk_set(A, p1, q2, dp, n12);
+          pk_set(A, q1, p2, dp, n21);
+          pk_set(A, q1, q2, dp, n22);
+        }
+      }
+      // V <- V J: rows p, q of V^T
+      for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
+        const int u = e / dp, l = e % dp;
+        const int pp = pr[2 * u], qq = pr[2 * u + 1];
+        const float c = cs[2 * u], sn = cs[2 * u + 1];
+        const float vp = Vt[static_cast<int64_t>(pp) * dp + l], vq = Vt[static_cast<int64_t>(qq) * dp + l];
+        Vt[static_cast<int64_t>(pp) * dp + l] = c * vp - sn * vq;
+        Vt[static_cast<int64_t>(qq) * dp + l] = sn * vp + c * vq;
+      }
+      __syncthreads();
+    }
+  }
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const float lj = A[pk_idx(j, j, dp)];
+    int rank = 0;
+    for (int i = 0; i < k; ++i) {
+      const float li = A[pk_idx(i, i, dp)];
+      rank += (li > lj) || (li == lj && i < j);
+    }
+    pr[j] = rank;
+  }
+  __syncthreads();
+  const float nub = nu[b];
+  float* W = WU + static_cast<int64_t>(b) * k * r;
+  const float* Pb = P ? P + static_cast<int64_t>(b) * k * r : nullptr;
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const int c = pr[j];
+    if (c >= r) continue;
+    const float s2 = A[pk_idx(j, j, dp)];
+    const float inv = s2 > 0.0f ? rsqrtf(s2) : 0.0f;
+    const float* vj = Vt + static_cast<int64_t>(j) * dp;
+    float sg = 1.0f;
+    if (Pb) {
+      float dot = 0.0f;
+      for (int l = 0; l < k; ++l) dot = fmaf(vj[l], Pb[l * r + c], dot);
+      sg = dot < 0.0f ? -1.0f : 1.0f;
+    }
+    for (int l = 0; l < k; ++l) W[l * r + c] = sg * inv * vj[l];
+    lam[static_cast<int64_t>(b) * r + c] = fmaxf(0.0f, s2 - nub);
+  }
+}
+
+inline int packed_smem(int k) {
+  const int dp = k + (k & 1);
+  return (kLHead + dp * (dp + 1) / 2) * 4;
 }
 
 // ------------------------------------------------------- element-wise kernels
@@ -645,6 +883,13 @@ struct ClRun {
   }
 };
 
+void cl_chol(const ClLarge& L, int k, int d, int adaptive, cudaStream_t st) {
+  if (k > kLK && k <= kPackMaxK)
+    k_cl_chol_inv_packed<<<L.batch, kLThreads, packed_chol_smem(k), st>>>(L.Gram, L.Rinv, k, d, adaptive, L.status);
+  else
+    k_cl_chol_inv<<<L.batch, kLThreads, kk_smem(k), st>>>(L.Gram, L.Rinv, k, d, adaptive, L.KK, L.status);
+}
+
 cudaError_t cl_attributes() {
   static int attr_dev = -1;
   int dev = 0;
@@ -654,6 +899,8 @@ cudaError_t cl_attributes() {
   e = cudaFuncSetAttribute(k_cl_chol_inv, at, kLSmallSmem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_norm, at, kLSmallSmem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_svd, at, kLSmallSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_svd_packed, at, packed_smem(kPackMaxK));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_chol_inv_packed, at, packed_chol_smem(kPackMaxK));
   if (e == cudaSuccess) attr_dev = dev;
   return e;
 }
@@ -668,7 +915,7 @@ float* cl_qr(ClRun& R, float* cur, float* spare, int d) {
   const int64_t sP = static_cast<int64_t>(L.m > L.n ? L.m : L.n) * k, sK = static_cast<int64_t>(k) * k;
   for (int pass = 0; pass < 4; ++pass) {
     R.gemm(cur, 0, 1, k, sP, cur, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
-    R.launch([&] { k_cl_chol_inv<<<L.batch, kLThreads, kLSmallSmem, R.st>>>(L.Gram, L.Rinv, k, d, 1, L.status); });
+    R.launch([&] { cl_chol(L, k, d, 1, R.st); });
     R.gemm(cur, 0, 0, k, sP, L.Rinv, 0, 0, k, sK, spare, k, sP, d, k, k);
     float* t = cur;
     cur = spare;
@@ -734,19 +981,24 @@ void cl_nystrom(ClRun& R, int side) {
   cl_apply(R, side, om, L.Y);
   // nu = eps(||Y||_2); Y_nu = Y + nu Omega
   R.gemm(L.Y, 0, 1, k, sP, L.Y, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
-  R.launch([&] { k_cl_norm<<<L.batch, kLThreads, kLSmallSmem, R.st>>>(L.Gram, L.nu, k); });
+  R.launch([&] { k_cl_norm<<<L.batch, kLThreads, kk_smem(k), R.st>>>(L.Gram, L.nu, k, L.KK); });
   R.launch([&] { k_cl_axpy<<<R.grid_for(static_cast<int64_t>(d) * k), 256, 0, R.st>>>(L.Y, om, L.nu, static_cast<int64_t>(d) * k, sP); });
   // C^T C = (B + B^T)/2, B = Omega^T Y_nu;  Z = Y_nu C^-1
   R.gemm(om, 0, 1, k, sP, L.Y, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
-  R.launch([&] { k_cl_chol_inv<<<L.batch, kLThreads, kLSmallSmem, R.st>>>(L.Gram, L.Rinv, k, d, 0, L.status); });
+  R.launch([&] { cl_chol(L, k, d, 0, R.st); });
   float* Z = free_panel;
   R.gemm(L.Y, 0, 0, k, sP, L.Rinv, 0, 0, k, sK, Z, k, sP, d, k, k);
   // thin SVD of Z from Z^T Z; signs against the previous basis
   R.gemm(Z, 0, 1, k, sP, Z, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
   if (L.warm) R.gemm(Z, 0, 1, k, sP, Uprev, 0, 0, r, sU, L.P, r, static_cast<int64_t>(k) * r, k, r, d);
   R.launch([&] {
-    k_cl_svd<<<L.batch, kLThreads, kLSmallSmem, R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU, lamOut, k, r,
-                                                          L.max_sweeps, L.tol2, L.status);
+    if (k > kLK && k <= kPackMaxK)
+      k_cl_svd_packed<<<L.batch, kLThreads, packed_smem(k), R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU,
+                                                                     lamOut, k, r, L.max_sweeps, L.tol2, L.KK,
+                                                                     L.status);
+    else
+      k_cl_svd<<<L.batch, kLThreads, kk_smem(k), R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU, lamOut, k, r,
+                                                           L.max_sweeps, L.tol2, L.KK, L.status);
   });
   R.gemm(Z, 0, 0, k, sP, L.WU, 0, 0, r, static_cast<int64_t>(k) * r, Uout, r, sU, d, r, k);
 }

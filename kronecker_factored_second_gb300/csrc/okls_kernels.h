@@ -109,7 +109,7 @@ cudaError_t launch_clean_refresh(const CleanArgs& A, cudaStream_t st);
 cudaError_t launch_clean_step(const CleanArgs& A, cudaStream_t st);
 cudaError_t launch_clean_reset(const CleanArgs& A, cudaStream_t st);
 
-// Clean for large shapes (m, n <= 16384, r + p <= 128): a batched fp32 GEMM
+// Clean for large shapes (m, n <= 16384, r + p <= 544): a batched fp32 GEMM
 // and the k x k kernels around it, orchestrated by clean_large_refresh /
 // clean_large_step.
 struct ClGemm {
@@ -148,8 +148,10 @@ struct ClLarge {
   float *Mn, *Sm, *MAn, *MBn, *vAn, *vBn;  // transported moments (r x r, r x r, m x r, r x n, r, r)
   float *GU, *UG, *S, *Nm, *Cb;       // step: m x r, r x n, r x r, r x r, m x n
   float *part, *cden;                 // sum-of-squares partials (batch x kClParts), 1
+  float* KK;                          // k x k scratch past k = 128: batch x 2 (k + 1)^2
 };
 constexpr int kClParts = 64;
+constexpr int kClMaxK = 544;  // largest r + p of the batched-GEMM path
 cudaError_t clean_large_refresh(const ClLarge& L, cudaStream_t st, int* launches);
 cudaError_t clean_large_step(const ClLarge& L, cudaStream_t st, int* launches);
 

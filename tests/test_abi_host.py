@@ -140,7 +140,7 @@ def test_soap_shapes_and_state(lib):
 def test_clean_shapes_and_validation(lib):
     """Clean keeps rank-r bases, their eigenvalues and the four blocks'
     moments (linear in m and n); this build takes m, n <= 16384 and
-    rank + oversample <= 128, and the rank fields belong to Clean alone."""
+    rank + oversample <= 544, and the rank fields belong to Clean alone."""
     B, m, n, r = 3, 128, 96, 16
     c = L.config_default(B, m, n)
     c.method = L.METHOD_CLEAN
@@ -159,16 +159,18 @@ def test_clean_shapes_and_validation(lib):
         assert lib.okls_state_bytes(ctypes.byref(c2), None, None) == code, (field, value)
     # past one CTA's shared memory (m > 128 or r + p > 64) the batched-GEMM
     # path takes over: the same state, a workspace of d x (r + p) panels and
-    # one m x n fp32 buffer per matrix; r + p above 128 is not supported
+    # one m x n fp32 buffer per matrix; r + p above 544 is not supported
     cl = L.config_default(2, 300, 200)
     cl.method, cl.rank, cl.oversample, cl.power_iters = L.METHOD_CLEAN, 32, 16, 1
     s2, w2 = L.state_bytes(cl)
     B2, m2, n2, r2, k2 = 2, 300, 200, 32, 48
     assert 4 * B2 * (m2 * r2 + n2 * r2 + 2 * r2 + 2 * r2 * r2 + m2 * r2 + r2 * n2 + 2 * r2 + 1) <= s2
     assert w2 >= 4 * B2 * (4 * m2 * k2 + m2 * n2)
-    cl.n = 300
-    cl.rank, cl.oversample = 121, 8
+    cl.m = cl.n = 600
+    cl.rank, cl.oversample = 537, 8
     assert lib.okls_state_bytes(ctypes.byref(cl), None, None) == L.OKLS_ERR_UNSUPPORTED
+    cl.rank = 536
+    L.state_bytes(cl)
     c3 = L.config_default(B, m, n)
     c3.rank = 4
     assert lib.okls_state_bytes(ctypes.byref(c3), None, None) == L.OKLS_ERR_INVALID_ARG

@@ -5,7 +5,8 @@ Teacher-forced: every step starts the oracle from the GPU's own state.
 A refresh step is checked in two parts:
   * the sketch: the oracle's Algorithm 3 on the same Gaussian draws gives
     the reference bases and eigenvalues; the GPU's eigenvalues must match to
-    1e-4 of the largest, its bases must be orthonormal (1e-5 in Frobenius
+    1e-4 max(1, (r + p)/128) of the largest (Jacobi's stopping rule and the
+    Gram sums grow with the sketch width), its bases must be orthonormal (1e-5 in Frobenius
     norm over r) and every basis vector whose eigenvalue is separated from
     its neighbours by more than 1e-2 of the largest must match the oracle's
     to 5e-4 (up to sign at the first refresh, where no previous basis fixes
@@ -171,6 +172,9 @@ LARGE_CASES = [
     (1, 260, 200, 112, 16, 2, 3, torch.float32, 0.0, "decay"),  # the largest sketch: r + p = 128
     (2, 160, 96, 12, 4, 1, 2, torch.bfloat16, 0.0, "iid"),
     (2, 96, 64, 8, 4, 1, 2, torch.float32, 0.0, "iid"),       # a one-CTA shape, forced onto this path
+    (2, 260, 180, 131, 6, 1, 2, torch.float32, 0.0, "iid"),   # r + p = 137: packed eigensolve, odd k
+    (1, 400, 300, 256, 8, 1, 2, torch.float32, 0.0, "iid"),   # the pages' rank 256 with oversampling 8
+    (1, 420, 360, 332, 8, 0, 2, torch.float32, 0.0, "iid"),   # r + p = 340: the eigensolve's matrices in L2
 ]
 
 
@@ -267,7 +271,8 @@ def _teacher_forced(B, m, n, r, p, q, T, dtype, wd, spectrum):
     assert worst["N_units"] <= 1.0, worst
     assert worst.get("U_same", 0.0) == 0.0
     for side in ("L", "R"):
-        assert worst[side + "_lam"] < 1e-4 and worst[side + "_orth"] < 1e-5, worst
+        # past k = 128 the k x k stopping rule and Gram sums add error that grows with k
+        assert worst[side + "_lam"] < 1e-4 * max(1.0, (r + p) / 128) and worst[side + "_orth"] < 1e-5, worst
         assert worst[side + "_order"] == 0.0, worst
         assert worst[side + "_vec"] < 5e-4, worst
     ob.close()
