@@ -160,9 +160,14 @@ typedef enum okls_state_part {
  *                   + C / (sqrt(v_C / (1-b2^t)) + eps), N(m, v) = (m/(1-b1^t)) /
  *                   (sqrt(v/(1-b2^t)) + eps); W <- W - lr wd (lr/lr_peak) W
  *                   - lr G~.  The sketch's Gaussian draws are an input (see
- *                   okls_step_noise).  This build runs Clean for m, n <= 128
- *                   and rank + oversample <= 64 (one CTA per factor, fp32);
- *                   larger shapes return OKLS_ERR_UNSUPPORTED.
+ *                   okls_step_noise).  This build runs Clean for m, n <=
+ *                   16384 and rank + oversample <= 544, in fp32: one CTA per
+ *                   factor up to 128 x 128 with rank + oversample <= 64,
+ *                   batched GEMMs past that (the workspace then holds four
+ *                   max(m, n) x (rank + oversample) panels and one m x n
+ *                   buffer per matrix; OKLS_CLEAN_LARGE=1 selects that path
+ *                   for every shape).  Larger shapes return
+ *                   OKLS_ERR_UNSUPPORTED.
  *   rank, oversample, power_iters  Clean's r >= 1, p >= 0 (r + p <=
  *                   min(m, n)) and q in [0, 16]; zero for the other methods.
  *                   OKLS_METHOD_SHAMPOO ignores beta1, beta2,

@@ -12,8 +12,8 @@
 `SOAP`             Adam in the factors' eigenbasis (method="soap"; matrices up
                    to 128 x 128 in this build).
 `Clean`            block-wise Adam in Nystrom low-rank bases (method="clean";
-                   matrices up to 128 x 128 and rank + oversample <= 64 in
-                   this build); the sketch's Gaussian draws come from a
+                   matrices up to 16384 x 16384 and rank + oversample <= 544
+                   in this build); the sketch's Gaussian draws come from a
                    torch.Generator and are passed to the library as an input.
 
 All arithmetic happens in libokls.so; nothing here computes on the CPU.
@@ -349,8 +349,9 @@ class SOAP(torch.optim.Optimizer):
 
 
 class Clean(torch.optim.Optimizer):
-    """Clean (Clean page, Algorithm 1) over 2-D and 3-D CUDA parameters with
-    both dimensions <= 128: block-wise Adam in rank-`rank` Nystrom bases of
+    """Clean (Clean page, Algorithm 1) over 2-D and 3-D CUDA parameters (both
+    dimensions <= 16384, rank + oversample <= 544 and <= both dimensions):
+    block-wise Adam in rank-`rank` Nystrom bases of
     the two Kronecker factors, re-sketched every `precondition_frequency`
     steps with `oversample` extra Gaussian columns and `power_iters`
     subspace iterations.  The Gaussian draws come from `generator` (a CUDA
