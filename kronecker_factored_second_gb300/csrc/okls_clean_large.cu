@@ -422,9 +422,11 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
           qq = x;
         }
         const float apq = As[pp * ld + qq];
+        const float app = As[pp * ld + pp], aqq = As[qq * ld + qq];
         float c = 1.0f, sn = 0.0f;
-        if (apq != 0.0f) {
-          const float th = (As[qq * ld + qq] - As[pp * ld + pp]) / (2.0f * apq);
+        // threshold Jacobi (see k_cl_svd_packed)
+        if (apq * apq > tol2 / static_cast<float>(k) * fabsf(app * aqq)) {
+          const float th = (aqq - app) / (2.0f * apq);
           const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
           c = rsqrtf(fmaf(t, t, 1.0f));
           sn = t * c;
@@ -437,8 +439,9 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
       __syncthreads();
       for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
         const int q = e / dp, j = e % dp;
-        const int pp = pr[2 * q], qq = pr[2 * q + 1];
         const float c = cs[2 * q], sn = cs[2 * q + 1];
+        if (sn == 0.0f) continue;
+        const int pp = pr[2 * q], qq = pr[2 * q + 1];
         const float ap = As[pp * ld + j], aq = As[qq * ld + j];
         As[pp * ld + j] = c * ap - sn * aq;
         As[qq * ld + j] = sn * ap + c * aq;
@@ -446,8 +449,9 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
       __syncthreads();
       for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
         const int q = e / dp, i = e % dp;
-        const int pp = pr[2 * q], qq = pr[2 * q + 1];
         const float c = cs[2 * q], sn = cs[2 * q + 1];
+        if (sn == 0.0f) continue;
+        const int pp = pr[2 * q], qq = pr[2 * q + 1];
         const float ap = As[i * ld + pp], aq = As[i * ld + qq];
         As[i * ld + pp] = c * ap - sn * aq;
         As[i * ld + qq] = sn * ap + c * aq;
@@ -517,6 +521,7 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd_packed(const float* Gram, 
   const int b = blockIdx.x;
   const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
   const int dp = k + (k & 1), np = dp / 2;
+  const float skip2 = tol2 / static_cast<float>(k);
   float* cs = sm;                                // 2 per pair
   int* pr = reinterpret_cast<int*>(sm + kLVec);  // 2 per pair, then ranks
   float* A = sm + kLHead;                        // packed upper triangle, dp (dp + 1) / 2
@@ -549,9 +554,12 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd_packed(const float* Gram, 
           qq = x;
         }
         const float apq = A[pk_idx(pp, qq, dp)];
+        const float app = A[pk_idx(pp, pp, dp)], aqq = A[pk_idx(qq, qq, dp)];
         float c = 1.0f, sn = 0.0f;
-        if (apq != 0.0f) {
-          const float th = (A[pk_idx(qq, qq, dp)] - A[pk_idx(pp, pp, dp)]) / (2.0f * apq);
+        // threshold Jacobi: a pair already below tol2 / k of its diagonal is
+        // left alone (when every pair is, the sweep's stopping rule holds)
+        if (apq * apq > skip2 * fabsf(app * aqq)) {
+          const float th = (aqq - app) / (2.0f * apq);
           const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
           c = rsqrtf(fmaf(t, t, 1.0f));
           sn = t * c;
@@ -566,8 +574,9 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd_packed(const float* Gram, 
       for (int e = threadIdx.x; e < np * np; e += blockDim.x) {
         const int u = e / np, v = e % np;
         if (u > v) continue;
-        const int p1 = pr[2 * u], q1 = pr[2 * u + 1], p2 = pr[2 * v], q2 = pr[2 * v + 1];
         const float c1 = cs[2 * u], s1 = cs[2 * u + 1], c2 = cs[2 * v], s2 = cs[2 * v + 1];
+        if (s1 == 0.0f && s2 == 0.0f) continue;  // both rotations are the identity
+        const int p1 = pr[2 * u], q1 = pr[2 * u + 1], p2 = pr[2 * v], q2 = pr[2 * v + 1];
         const float a11 = pk_get(A, p1, p2, dp), a12 = pk_get(A, p1, q2, dp);
         const float a21 = pk_get(A, q1, p2, dp), a22 = pk_get(A, q1, q2, dp);
         // rows: J1^T = [[c1, -s1], [s1, c1]]
@@ -590,8 +599,9 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd_packed(const float* Gram, 
       // V <- V J: rows p, q of V^T
       for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
         const int u = e / dp, l = e % dp;
-        const int pp = pr[2 * u], qq = pr[2 * u + 1];
         const float c = cs[2 * u], sn = cs[2 * u + 1];
+        if (sn == 0.0f) continue;
+        const int pp = pr[2 * u], qq = pr[2 * u + 1];
         const float vp = Vt[static_cast<int64_t>(pp) * dp + l], vq = Vt[static_cast<int64_t>(qq) * dp + l];
         Vt[static_cast<int64_t>(pp) * dp + l] = c * vp - sn * vq;
         Vt[static_cast<int64_t>(qq) * dp + l] = sn * vp + c * vq;
