@@ -159,6 +159,7 @@ cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st) {
 constexpr int kLK = 128;
 constexpr int kLP = kLK + 1;        // odd pitch of the staged k x k matrices
 constexpr int kLThreads = 256;
+constexpr int kLWide = 1024;  // the packed kernels: more of a round's work in flight
 constexpr int kLVec = 2 * kClMaxK;  // floats: vectors / rotation parameters
 constexpr int kLInts = 2 * kClMaxK; // ints: pairs, then ranks
 constexpr int kLHead = kLVec + kLInts;
@@ -278,10 +279,10 @@ __global__ void __launch_bounds__(kLThreads) k_cl_chol_inv(const float* Gram, fl
 // L^-1 straight into the matching row of Rinv = L^-T.
 __device__ __forceinline__ int pl_idx(int i, int j) { return i * (i + 1) / 2 + j; }  // i >= j
 
-__global__ void __launch_bounds__(kLThreads) k_cl_chol_inv_packed(const float* Gram, float* Rinv, int k, int d,
+__global__ void __launch_bounds__(kLWide) k_cl_chol_inv_packed(const float* Gram, float* Rinv, int k, int d,
                                                                   int adaptive, uint32_t* status) {
   extern __shared__ float sm[];
-  __shared__ float red[kLThreads / 32];
+  __shared__ float red[kLWide / 32];
   __shared__ float piv;
   const int b = blockIdx.x;
   const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
@@ -512,11 +513,11 @@ __device__ __forceinline__ void pk_set(float* A, int i, int j, int dp, float v) 
     A[pk_idx(j, i, dp)] = v;
 }
 
-__global__ void __launch_bounds__(kLThreads) k_cl_svd_packed(const float* Gram, const float* P, const float* nu,
+__global__ void __launch_bounds__(kLWide) k_cl_svd_packed(const float* Gram, const float* P, const float* nu,
                                                              float* WU, float* lam, int k, int r, int max_sweeps,
                                                              float tol2, float* scratch, const uint32_t* status) {
   extern __shared__ float sm[];
-  __shared__ float red[kLThreads / 32];
+  __shared__ float red[kLWide / 32];
   if (cl_flagged(status)) return;
   const int b = blockIdx.x;
   const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
@@ -895,7 +896,7 @@ struct ClRun {
 
 void cl_chol(const ClLarge& L, int k, int d, int adaptive, cudaStream_t st) {
   if (k > kLK && k <= kPackMaxK)
-    k_cl_chol_inv_packed<<<L.batch, kLThreads, packed_chol_smem(k), st>>>(L.Gram, L.Rinv, k, d, adaptive, L.status);
+    k_cl_chol_inv_packed<<<L.batch, kLWide, packed_chol_smem(k), st>>>(L.Gram, L.Rinv, k, d, adaptive, L.status);
   else
     k_cl_chol_inv<<<L.batch, kLThreads, kk_smem(k), st>>>(L.Gram, L.Rinv, k, d, adaptive, L.KK, L.status);
 }
@@ -1003,7 +1004,7 @@ void cl_nystrom(ClRun& R, int side) {
   if (L.warm) R.gemm(Z, 0, 1, k, sP, Uprev, 0, 0, r, sU, L.P, r, static_cast<int64_t>(k) * r, k, r, d);
   R.launch([&] {
     if (k > kLK && k <= kPackMaxK)
-      k_cl_svd_packed<<<L.batch, kLThreads, packed_smem(k), R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU,
+      k_cl_svd_packed<<<L.batch, kLWide, packed_smem(k), R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU,
                                                                      lamOut, k, r, L.max_sweeps, L.tol2, L.KK,
                                                                      L.status);
     else
