@@ -21,13 +21,14 @@
 namespace okls {
 
 // ---------------------------------------------------------------- the GEMM
-// 128 x 128 output tile per CTA, K in slices of 8, 256 threads with 8 x 8
+// 128 x 128 output tile per CTA, K in slices of 16, 256 threads with 8 x 8
 // outputs each (two 4-row by two 4-column groups, so that a warp's float4
 // reads of the staged slices are conflict-free); the next slice is fetched
 // into registers while the current one is multiplied (double-buffered shared
-// memory, one barrier per slice).
+// memory, one barrier per slice).  A thread fetches 8 consecutive elements of
+// each operand per slice, as 16-byte vectors where the layout allows.
 constexpr int kGM = 128;  // output tile edge
-constexpr int kGK = 8;    // K per slice
+constexpr int kGK = 16;   // K per slice
 
 template <typename T>
 __device__ __forceinline__ float cl_ld(const T* p);
@@ -36,40 +37,64 @@ __device__ __forceinline__ float cl_ld<float>(const float* p) { return __ldg(p);
 template <>
 __device__ __forceinline__ float cl_ld<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
-// Four elements of a slice of an operand staged as [k][128]: `trans` says
-// whether the operand's rows are k (stored K x rows, ld) or the tile's
-// rows (stored rows x K, ld).  Out-of-range elements read as 0.
+// 8 consecutive elements at p (16-byte aligned for the vector forms)
+__device__ __forceinline__ void cl_ld8(const float* p, float v[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void cl_ld8(const __nv_bfloat16* p, float v[8]) {
+  const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    v[2 * u] = __uint_as_float(w[u] << 16);
+    v[2 * u + 1] = __uint_as_float(w[u] & 0xffff0000u);
+  }
+}
+
+// The thread's 8 elements of a slice of an operand staged as [k][128]:
+// `kmajor` operands are stored K x rows (a slice row is 128 contiguous
+// entries: the thread takes 8 of one k), the others rows x K (the thread
+// takes 8 consecutive k of one row).  Out-of-range elements read as 0;
+// `vec` says 16-byte loads are aligned for this operand.
 template <typename T>
-__device__ __forceinline__ void cl_fetch(const T* X, bool kmajor, int64_t ld, int row0, int rows, int k0, int K,
-                                         float v[4], int& kk, int& i0) {
+__device__ __forceinline__ void cl_fetch(const T* X, bool kmajor, bool vec, int64_t ld, int row0, int rows, int k0,
+                                         int K, float v[8], int& kk, int& i0) {
   const int t = threadIdx.x;
-  if (kmajor) {  // element (k, i) at X[k ld + i]: a slice row is 128 contiguous entries
-    kk = t >> 5;
-    i0 = (t & 31) * 4;
-    const int gk = k0 + kk;
+  if (kmajor) {
+    kk = t >> 4;
+    i0 = (t & 15) * 8;
+    const int gk = k0 + kk, gi = row0 + i0;
+    const T* p = X + static_cast<int64_t>(gk) * ld + gi;
+    if (vec && gk < K && gi + 8 <= rows) {
+      cl_ld8(p, v);
+    } else {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int gi = row0 + i0 + u;
-      v[u] = (gk < K && gi < rows) ? cl_ld<T>(X + static_cast<int64_t>(gk) * ld + gi) : 0.0f;
+      for (int u = 0; u < 8; ++u) v[u] = (gk < K && gi + u < rows) ? cl_ld<T>(p + u) : 0.0f;
     }
-  } else {  // element (k, i) at X[i ld + k]: 8 contiguous k per row
+  } else {
     i0 = t >> 1;
-    kk = (t & 1) * 4;
-    const int gi = row0 + i0;
+    kk = (t & 1) * 8;
+    const int gi = row0 + i0, gk = k0 + kk;
+    const T* p = X + static_cast<int64_t>(gi) * ld + gk;
+    if (vec && gi < rows && gk + 8 <= K) {
+      cl_ld8(p, v);
+    } else {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int gk = k0 + kk + u;
-      v[u] = (gk < K && gi < rows) ? cl_ld<T>(X + static_cast<int64_t>(gi) * ld + gk) : 0.0f;
+      for (int u = 0; u < 8; ++u) v[u] = (gi < rows && gk + u < K) ? cl_ld<T>(p + u) : 0.0f;
     }
   }
 }
 
-__device__ __forceinline__ void cl_stage(float (*S)[kGM], bool kmajor, const float v[4], int kk, int i0) {
+__device__ __forceinline__ void cl_stage(float (*S)[kGM], bool kmajor, const float v[8], int kk, int i0) {
   if (kmajor) {
     *reinterpret_cast<float4*>(&S[kk][i0]) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(&S[kk][i0 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
   } else {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) S[kk + u][i0] = v[u];
+    for (int u = 0; u < 8; ++u) S[kk + u][i0] = v[u];
   }
 }
 
@@ -89,10 +114,10 @@ __global__ void __launch_bounds__(256) k_cl_gemm(ClGemm g) {
   // k-major when stored K x N (not tb)
   const bool a_kmaj = g.ta != 0, b_kmaj = g.tb == 0;
   float acc[8][8] = {};
-  float va[4], vb[4];
+  float va[8], vb[8];
   int akk, ai0, bkk, bi0;
-  cl_fetch<TA>(A, a_kmaj, g.lda, m0, g.M, 0, g.K, va, akk, ai0);
-  cl_fetch<TB>(B, b_kmaj, g.ldb, n0, g.N, 0, g.K, vb, bkk, bi0);
+  cl_fetch<TA>(A, a_kmaj, g.a_vec, g.lda, m0, g.M, 0, g.K, va, akk, ai0);
+  cl_fetch<TB>(B, b_kmaj, g.b_vec, g.ldb, n0, g.N, 0, g.K, vb, bkk, bi0);
   cl_stage(As[0], a_kmaj, va, akk, ai0);
   cl_stage(Bs[0], b_kmaj, vb, bkk, bi0);
   __syncthreads();
@@ -100,8 +125,8 @@ __global__ void __launch_bounds__(256) k_cl_gemm(ClGemm g) {
   for (int k0 = 0; k0 < g.K; k0 += kGK) {
     const bool more = k0 + kGK < g.K;
     if (more) {
-      cl_fetch<TA>(A, a_kmaj, g.lda, m0, g.M, k0 + kGK, g.K, va, akk, ai0);
-      cl_fetch<TB>(B, b_kmaj, g.ldb, n0, g.N, k0 + kGK, g.K, vb, bkk, bi0);
+      cl_fetch<TA>(A, a_kmaj, g.a_vec, g.lda, m0, g.M, k0 + kGK, g.K, va, akk, ai0);
+      cl_fetch<TB>(B, b_kmaj, g.b_vec, g.ldb, n0, g.N, k0 + kGK, g.K, vb, bkk, bi0);
     }
 #pragma unroll
     for (int kk = 0; kk < kGK; ++kk) {
@@ -138,8 +163,18 @@ __global__ void __launch_bounds__(256) k_cl_gemm(ClGemm g) {
   }
 }
 
-cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st) {
-  if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return cudaSuccess;
+// 16-byte loads of 8 elements need the base, the leading dimension and the
+// batch stride to keep every run of 8 on a 16-byte boundary
+static int cl_vec_ok(const void* p, int bf16, int64_t ld, int64_t stride) {
+  const int64_t q = bf16 ? 8 : 4;  // elements per 16 bytes
+  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ld % q == 0 && stride % q == 0;
+}
+
+cudaError_t launch_cl_gemm(const ClGemm& g0, cudaStream_t st) {
+  if (g0.M <= 0 || g0.N <= 0 || g0.batch <= 0) return cudaSuccess;
+  ClGemm g = g0;
+  g.a_vec = cl_vec_ok(g.A, g.a_bf16, g.lda, g.sA);
+  g.b_vec = cl_vec_ok(g.B, g.b_bf16, g.ldb, g.sB);
   const dim3 grid((g.N + kGM - 1) / kGM, (g.M + kGM - 1) / kGM, g.batch);
   if (g.a_bf16 && g.b_bf16)
     k_cl_gemm<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(g);

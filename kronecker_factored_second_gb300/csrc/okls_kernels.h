@@ -124,6 +124,7 @@ struct ClGemm {
   int batch;
   float alpha, beta;
   const float* beta_dev;  // per-batch beta when not null
+  int a_vec, b_vec;       // set by launch_cl_gemm: 16-byte loads allowed
 };
 cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st);
 
