@@ -797,6 +797,8 @@ struct okls_handle_s {
   // the refreshed bases of a refresh step (workspace)
   float *MA = nullptr, *MB = nullptr, *vA = nullptr, *vB = nullptr, *vC = nullptr;
   float *ULn = nullptr, *URn = nullptr, *lamLn = nullptr, *lamRn = nullptr;
+  bool soap_large = false;   // SOAP past one CTA's shared memory (batched fp32 GEMMs)
+  SoapLarge sl;
   bool clean_large = false;  // Clean past one CTA's shared memory (batched fp32 GEMMs)
   ClLarge cl;                // its buffers (the state pointers above, plus workspace)
   float* scal = nullptr;
@@ -814,6 +816,14 @@ namespace {
 struct Layout {
   size_t state_bytes = 0, ws_bytes = 0;
 };
+
+// SOAP runs one CTA per matrix up to 128 x 128; past that (to 544), or with
+// OKLS_SOAP_LARGE=1, the batched-GEMM path.
+bool soap_large_path(const okls_config& c) {
+  const char* e = getenv("OKLS_SOAP_LARGE");
+  if (e && e[0] == '1') return true;
+  return c.m > 128 || c.n > 128;
+}
 
 // Clean runs one CTA per factor while a factor's panels fit its shared
 // memory (m, n <= 128, r + p <= 64); past that, or with OKLS_CLEAN_LARGE=1,
@@ -949,6 +959,24 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
   uint32_t* status = static_cast<uint32_t*>(wp.take(256));
   if (soap) {
     // SOAP keeps everything in the state; the workspace holds the status word
+    // (and, past one CTA, the batched path's buffers)
+    const bool large = soap_large_path(c);
+    SoapLarge sl;
+    memset(&sl, 0, sizeof(sl));
+    if (large) {
+      const int64_t dmax = m > n ? m : n;
+      const int64_t big = std::max(m * n, dmax * dmax);
+      auto f32 = [&](int64_t elems) { return static_cast<float*>(wp.take(static_cast<size_t>(elems * 4))); };
+      sl.Gf = f32(B * m * n);
+      sl.Gp = f32(B * m * n);
+      sl.Mp = f32(B * m * n);
+      sl.T = f32(B * big);
+      sl.Qh = f32(B * dmax * dmax);
+      sl.A = f32(B * dmax * dmax);
+      sl.P = f32(B * dmax * dmax);
+      sl.Wq = f32(B * dmax * dmax);
+      sl.KK = dmax > 128 ? f32(B * 2 * (dmax + 1) * (dmax + 1)) : nullptr;
+    }
     out->state_bytes = sp.off;
     out->ws_bytes = wp.off;
     if (h) {
@@ -961,6 +989,20 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
       h->scal = scal;
       h->status = status;
       h->maps = maps;
+      h->soap_large = large;
+      if (large) {
+        sl.batch = static_cast<int>(B);
+        sl.m = static_cast<int>(m);
+        sl.n = static_cast<int>(n);
+        sl.M = M;
+        sl.V = V;
+        sl.L = Sa;
+        sl.R = Sb;
+        sl.QL = Pa;
+        sl.QR = Pb;
+        sl.status = status;
+        h->sl = sl;
+      }
     }
     return OKLS_OK;
   }
@@ -1074,10 +1116,10 @@ okls_status validate(const okls_config* c) {
   } else if (c->rank != 0 || c->oversample != 0 || c->power_iters != 0) {
     return fail(OKLS_ERR_INVALID_ARG, "rank, oversample and power_iters are Clean's; leave them zero");
   }
-  if (c->method == OKLS_METHOD_SOAP && (c->m > 128 || c->n > 128))
+  if (c->method == OKLS_METHOD_SOAP && (c->m > kSoapLargeMax || c->n > kSoapLargeMax))
     return fail(OKLS_ERR_UNSUPPORTED,
-                "SOAP runs for m, n <= 128 in this build (one-CTA eigensolver); %lld x %lld needs the blocked one",
-                static_cast<long long>(c->m), static_cast<long long>(c->n));
+                "SOAP runs for m, n <= %d in this build (one-CTA Jacobi eigensolver); %lld x %lld needs a blocked one",
+                kSoapLargeMax, static_cast<long long>(c->m), static_cast<long long>(c->n));
   for (int i = 0; i < 3; ++i)
     if (c->reserved[i] != 0) return fail(OKLS_ERR_INVALID_ARG, "reserved fields must be zero");
   return OKLS_OK;
@@ -1114,9 +1156,30 @@ okls_status soap_step(okls_handle_s* h, void* W, const void* G, float lr, cudaSt
   A.bc1 = static_cast<float>(1.0 / (1.0 - std::pow(static_cast<double>(c.beta1), static_cast<double>(t1))));
   A.bc2 = static_cast<float>(1.0 / (1.0 - std::pow(static_cast<double>(c.beta2), static_cast<double>(t1))));
   A.status = h->status;
+  const int64_t every = c.root_every > 1 ? c.root_every : 1;
+  if (h->soap_large) {
+    SoapLarge S = h->sl;
+    S.G = G;
+    S.W = W;
+    S.g_bf16 = A.g_bf16;
+    S.w_bf16 = A.w_bf16;
+    S.beta1 = A.beta1;
+    S.beta2 = A.beta2;
+    S.eps = A.eps;
+    S.lr = A.lr;
+    S.decay = A.decay;
+    S.bc1 = A.bc1;
+    S.bc2 = A.bc2;
+    S.max_sweeps = 15;
+    S.tol2 = 1e-12f;
+    int launches = 0;
+    OKLS_CK(soap_large_step(S, t1 % every == 0, st, &launches));
+    note_kernels(launches);
+    h->t = t1;
+    return OKLS_OK;
+  }
   OKLS_CK(launch_soap_step(A, st));
   note_kernels(1);
-  const int64_t every = c.root_every > 1 ? c.root_every : 1;
   if (t1 % every == 0) {
     SoapRefreshArgs R;
     memset(&R, 0, sizeof(R));

@@ -104,6 +104,10 @@ template <typename TA, typename TB>
 __global__ void __launch_bounds__(256) k_cl_gemm(ClGemm g) {
   __shared__ __align__(16) float As[2][kGK][kGM];
   __shared__ __align__(16) float Bs[2][kGK][kGM];
+  // a GEMM that writes state is skipped once an earlier stage has flagged
+  if (g.status_guard &&
+      __syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<const volatile uint32_t*>(g.status_guard) != 0u))
+    return;
   const int b = blockIdx.z;
   const TA* A = static_cast<const TA*>(g.A) + static_cast<int64_t>(b) * g.sA;
   const TB* B = static_cast<const TB*>(g.B) + static_cast<int64_t>(b) * g.sB;
@@ -509,14 +513,16 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
     pr[j] = rank;
   }
   __syncthreads();
-  const float nub = nu[b];
+  // nu null: plain eigenvectors (no 1/sigma scaling) and eigenvalues
+  const bool unit = nu == nullptr;
+  const float nub = unit ? 0.0f : nu[b];
   float* W = WU + static_cast<int64_t>(b) * k * r;
   const float* Pb = P ? P + static_cast<int64_t>(b) * k * r : nullptr;
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
     const int c = pr[j];
     if (c >= r) continue;
     const float s2 = As[j * ld + j];
-    const float inv = s2 > 0.0f ? rsqrtf(s2) : 0.0f;
+    const float inv = unit ? 1.0f : (s2 > 0.0f ? rsqrtf(s2) : 0.0f);
     float sg = 1.0f;
     if (Pb) {
       float dot = 0.0f;
@@ -524,7 +530,7 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
       sg = dot < 0.0f ? -1.0f : 1.0f;
     }
     for (int l = 0; l < k; ++l) W[l * r + c] = sg * inv * Vs[l * ld + j];
-    lam[static_cast<int64_t>(b) * r + c] = fmaxf(0.0f, s2 - nub);
+    if (lam) lam[static_cast<int64_t>(b) * r + c] = unit ? s2 : fmaxf(0.0f, s2 - nub);
   }
 }
 
@@ -655,14 +661,16 @@ __global__ void __launch_bounds__(kLWide) k_cl_svd_packed(const float* Gram, con
     pr[j] = rank;
   }
   __syncthreads();
-  const float nub = nu[b];
+  // nu null: plain eigenvectors (no 1/sigma scaling) and eigenvalues
+  const bool unit = nu == nullptr;
+  const float nub = unit ? 0.0f : nu[b];
   float* W = WU + static_cast<int64_t>(b) * k * r;
   const float* Pb = P ? P + static_cast<int64_t>(b) * k * r : nullptr;
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
     const int c = pr[j];
     if (c >= r) continue;
     const float s2 = A[pk_idx(j, j, dp)];
-    const float inv = s2 > 0.0f ? rsqrtf(s2) : 0.0f;
+    const float inv = unit ? 1.0f : (s2 > 0.0f ? rsqrtf(s2) : 0.0f);
     const float* vj = Vt + static_cast<int64_t>(j) * dp;
     float sg = 1.0f;
     if (Pb) {
@@ -671,7 +679,7 @@ __global__ void __launch_bounds__(kLWide) k_cl_svd_packed(const float* Gram, con
       sg = dot < 0.0f ? -1.0f : 1.0f;
     }
     for (int l = 0; l < k; ++l) W[l * r + c] = sg * inv * vj[l];
-    lam[static_cast<int64_t>(b) * r + c] = fmaxf(0.0f, s2 - nub);
+    if (lam) lam[static_cast<int64_t>(b) * r + c] = unit ? s2 : fmaxf(0.0f, s2 - nub);
   }
 }
 
@@ -892,7 +900,7 @@ struct ClRun {
             int64_t sB, float* C, int64_t ldc, int64_t sC, int M, int N, int K, float alpha = 1.0f, float beta = 0.0f,
             const float* beta_dev = nullptr) {
     if (err != cudaSuccess) return;
-    ClGemm g;
+    ClGemm g{};
     g.A = A;
     g.B = B;
     g.C = C;
@@ -1050,6 +1058,29 @@ void cl_nystrom(ClRun& R, int side) {
 }
 
 }  // namespace
+
+cudaError_t launch_cl_eig(const float* A, const float* P, float* Wout, float* lam, int d, int batch, int max_sweeps,
+                          float tol2, float* scratch, uint32_t* status, cudaStream_t st) {
+  cudaError_t e = cl_attributes();
+  if (e != cudaSuccess) return e;
+  if (d > kLK && d <= kPackMaxK)
+    k_cl_svd_packed<<<batch, kLWide, packed_smem(d), st>>>(A, P, nullptr, Wout, lam, d, d, max_sweeps, tol2, scratch,
+                                                            status);
+  else
+    k_cl_svd<<<batch, kLThreads, kk_smem(d), st>>>(A, P, nullptr, Wout, lam, d, d, max_sweeps, tol2, scratch, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cl_prep(const void* G, int g_bf16, float* out, int64_t mn, int batch, uint32_t* status,
+                           cudaStream_t st) {
+  const int64_t gx = (mn + 255) / 256;
+  const dim3 grid(static_cast<unsigned>(gx < 256 ? (gx > 0 ? gx : 1) : 256), static_cast<unsigned>(batch));
+  if (g_bf16)
+    k_cl_prep<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(G), out, mn, status);
+  else
+    k_cl_prep<float><<<grid, 256, 0, st>>>(static_cast<const float*>(G), out, mn, status);
+  return cudaGetLastError();
+}
 
 cudaError_t clean_large_refresh(const ClLarge& L, cudaStream_t st, int* launches) {
   cudaError_t e = cl_attributes();

@@ -125,6 +125,7 @@ struct ClGemm {
   float alpha, beta;
   const float* beta_dev;  // per-batch beta when not null
   int a_vec, b_vec;       // set by launch_cl_gemm: 16-byte loads allowed
+  const uint32_t* status_guard;  // not null: skip the launch once the status word is set
 };
 cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st);
 
@@ -154,7 +155,35 @@ struct ClLarge {
 constexpr int kClParts = 64;
 constexpr int kClMaxK = 544;  // largest r + p of the batched-GEMM path
 cudaError_t clean_large_refresh(const ClLarge& L, cudaStream_t st, int* launches);
+// Eigenvectors of the batch of symmetric d x d matrices A (d <= kClMaxK),
+// reordered by decreasing eigenvalue into Wout (d x d, column c = the
+// eigenvector of rank c), each column's sign chosen so that its product with
+// column c of P (d x d: the previous basis seen through the current one) is
+// >= 0 (P null: signs as the solver leaves them); eigenvalues into lam (may be null).
+cudaError_t launch_cl_eig(const float* A, const float* P, float* Wout, float* lam, int d, int batch, int max_sweeps,
+                          float tol2, float* scratch, uint32_t* status, cudaStream_t st);
+cudaError_t launch_cl_prep(const void* G, int g_bf16, float* out, int64_t mn, int batch, uint32_t* status,
+                           cudaStream_t st);
 cudaError_t clean_large_step(const ClLarge& L, cudaStream_t st, int* launches);
+
+// SOAP for m, n <= kSoapLargeMax on the batched GEMM (okls_soap_large.cu).
+constexpr int kSoapLargeMax = kClMaxK;
+struct SoapLarge {
+  int batch, m, n;
+  const void* G;
+  void* W;
+  int g_bf16, w_bf16;
+  float *M, *V, *L, *R, *QL, *QR;       // state
+  float beta1, beta2, eps, lr, decay, bc1, bc2;
+  int max_sweeps;
+  float tol2;
+  uint32_t* status;
+  float *Gf, *Gp, *Mp;                  // workspace: m x n each
+  float* T;                             // max(m n, m^2, n^2)
+  float *Qh, *A, *P, *Wq;               // max(m, n)^2 each
+  float* KK;                            // eigensolver scratch past d = 128: 2 (d + 1)^2
+};
+cudaError_t soap_large_step(const SoapLarge& S, int refresh, cudaStream_t st, int* launches);
 
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_pair(const GemmLaunch& L, int num_sms, cudaStream_t stream);

@@ -127,14 +127,18 @@ def test_method_is_validated_and_sizes_the_workspace(lib):
 
 def test_soap_shapes_and_state(lib):
     """SOAP keeps M, L, R, Q_L, Q_R and V in the state and needs no binary16
-    workspace; this build takes m, n <= 128."""
+    workspace; this build takes m, n <= 544 (one CTA per matrix up to 128)."""
     c = L.config_default(3, 128, 64)
     c.method = L.METHOD_SOAP
     s, w = L.state_bytes(c)
     assert s >= 4 * 3 * (2 * 128 * 64 + 2 * 128 * 128 + 2 * 64 * 64)
     assert w < 1 << 20
-    c.m = 129
+    c.m = 545
     assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_UNSUPPORTED
+    # past 128 the batched-GEMM path adds its workspace
+    c.m = 300
+    s2, w2 = L.state_bytes(c)
+    assert w2 >= 4 * 3 * (3 * 300 * 64 + 4 * 300 * 300 + 300 * 300)
 
 
 def test_clean_shapes_and_validation(lib):

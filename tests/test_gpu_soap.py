@@ -8,7 +8,9 @@ the bases must be orthogonal and diagonalise L, R (1e-5), carry decreasing
 eigenvalues and agree in sign with the previous bases (orthogonality to
 1e-5 d in Frobenius norm: fp32 rotations), and every eigenvector
 whose eigenvalue is separated from its neighbours by more than 1e-3 of the
-spectrum must match the oracle's to 1e-3.
+spectrum must match the oracle's within 2e-6 ||L||_F / gap: twice the
+solver's stopping residual (1e-6 of the matrix in Frobenius norm) over the
+gap, the first-order bound on an eigenvector's error.
 """
 
 from __future__ import annotations
@@ -63,13 +65,31 @@ def _check_basis(Q, S, Q_prev, Q_ref):
         gaps[:-1] = np.minimum(gaps[:-1], w[:-1] - w[1:])
         gaps[1:] = np.minimum(gaps[1:], w[:-1] - w[1:])
     sel = gaps > 1e-3 * scale
-    out["vec"] = float(np.max(np.linalg.norm(Q[:, sel] - Q_ref[:, sel], axis=0))) if sel.any() else 0.0
+    err = np.linalg.norm(Q[:, sel] - Q_ref[:, sel], axis=0)
+    out["vec"] = float(np.max(err)) if sel.any() else 0.0
+    # first-order perturbation: ||dq_j|| <= ||dL|| / gap_j, and the solver
+    # stops at an off-diagonal residual of 1e-6 of the matrix in Frobenius
+    # norm: the error times the gap over ||L||_F is bounded by that residual
+    out["vec_gap"] = float(np.max(err * gaps[sel])) / max(float(np.linalg.norm(S)), 1e-30) if sel.any() else 0.0
     return out
 
 
 @pytest.mark.parametrize("B,m,n,dtype", [(1, 128, 64, torch.float32), (3, 40, 24, torch.float32),
                                          (2, 17, 33, torch.float32), (2, 64, 32, torch.bfloat16)])
 def test_teacher_forced_steps(B, m, n, dtype):
+    _teacher_forced(B, m, n, dtype)
+
+
+# the batched-GEMM path: m or n past 128 (or forced); eigensolves in shared
+# memory up to 128, as packed triangles up to 330, in L2 past that
+@pytest.mark.parametrize("B,m,n,dtype", [(2, 200, 150, torch.float32), (1, 300, 140, torch.float32),
+                                         (2, 96, 64, torch.float32), (1, 160, 340, torch.bfloat16)])
+def test_teacher_forced_steps_large_path(B, m, n, dtype, monkeypatch):
+    monkeypatch.setenv("OKLS_SOAP_LARGE", "1")
+    _teacher_forced(B, m, n, dtype)
+
+
+def _teacher_forced(B, m, n, dtype):
     lr, b1, b2, eps, f = 0.01, 0.9, 0.95, 1e-8, 2
     ob = _batch(B, m, n, param_dtype=dtype, lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=0.0, root_every=f)
     rng = np.random.default_rng(m + n)
@@ -109,7 +129,7 @@ def test_teacher_forced_steps(B, m, n, dtype):
     for side in ("QL", "QR"):
         assert worst[side + "_orth"] < 1e-5 and worst[side + "_offdiag"] < 1e-5, worst
         assert worst[side + "_order"] < 1e-6 and worst[side + "_sign"] == 0.0, worst
-        assert worst[side + "_vec"] < 1e-3, worst
+        assert worst[side + "_vec_gap"] < 2e-6, worst
     ob.close()
 
 
