@@ -534,9 +534,9 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
   }
 }
 
-// The same thin SVD for 128 < k <= kPackMaxK: Z^T Z kept in shared memory as
-// a packed upper triangle (padded to an even size dp), the eigenvectors as
-// V^T rows in the L2-resident scratch.  A round's d'/2 disjoint rotations
+// The same thin SVD for k > 128: Z^T Z kept as a packed upper triangle
+// (padded to an even size dp; in shared memory up to kPackMaxK, in the
+// L2-resident scratch past it), the eigenvectors as V^T rows in that scratch.  A round's d'/2 disjoint rotations
 // (J_pq acting on rows and columns p, q) are applied as one pass over the
 // 2 x 2 blocks A[{p1, q1}, {p2, q2}] of every two pairs of the round
 // (block <- J1^T block J2; each unordered index pair lies in exactly one
@@ -566,8 +566,10 @@ __global__ void __launch_bounds__(kLWide) k_cl_svd_packed(const float* Gram, con
   const float skip2 = tol2 / static_cast<float>(k);
   float* cs = sm;                                // 2 per pair
   int* pr = reinterpret_cast<int*>(sm + kLVec);  // 2 per pair, then ranks
-  float* A = sm + kLHead;                        // packed upper triangle, dp (dp + 1) / 2
   float* Vt = scratch + static_cast<int64_t>(b) * 2 * (k + 1) * (k + 1);  // dp x dp, row c = column c of V
+  // packed upper triangle, dp (dp + 1) / 2: in shared memory up to kPackMaxK,
+  // past it beside V^T in the L2-resident slice
+  float* A = k <= kPackMaxK ? sm + kLHead : Vt + static_cast<int64_t>(k + 1) * (k + 1);
   for (int j = threadIdx.x; j < dp; j += blockDim.x)
     for (int i = 0; i <= j; ++i)
       A[pk_idx(i, j, dp)] = (i < k && j < k) ? 0.5f * (Gb[i * k + j] + Gb[j * k + i]) : 0.0f;
@@ -685,7 +687,7 @@ __global__ void __launch_bounds__(kLWide) k_cl_svd_packed(const float* Gram, con
 
 inline int packed_smem(int k) {
   const int dp = k + (k & 1);
-  return (kLHead + dp * (dp + 1) / 2) * 4;
+  return k <= kPackMaxK ? (kLHead + dp * (dp + 1) / 2) * 4 : kLHead * 4;
 }
 
 // ------------------------------------------------------- element-wise kernels
@@ -1046,7 +1048,7 @@ void cl_nystrom(ClRun& R, int side) {
   R.gemm(Z, 0, 1, k, sP, Z, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
   if (L.warm) R.gemm(Z, 0, 1, k, sP, Uprev, 0, 0, r, sU, L.P, r, static_cast<int64_t>(k) * r, k, r, d);
   R.launch([&] {
-    if (k > kLK && k <= kPackMaxK)
+    if (k > kLK)
       k_cl_svd_packed<<<L.batch, kLWide, packed_smem(k), R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU,
                                                                      lamOut, k, r, L.max_sweeps, L.tol2, L.KK,
                                                                      L.status);
@@ -1063,7 +1065,7 @@ cudaError_t launch_cl_eig(const float* A, const float* P, float* Wout, float* la
                           float tol2, float* scratch, uint32_t* status, cudaStream_t st) {
   cudaError_t e = cl_attributes();
   if (e != cudaSuccess) return e;
-  if (d > kLK && d <= kPackMaxK)
+  if (d > kLK)
     k_cl_svd_packed<<<batch, kLWide, packed_smem(d), st>>>(A, P, nullptr, Wout, lam, d, d, max_sweeps, tol2, scratch,
                                                             status);
   else
