@@ -515,11 +515,12 @@ def run_okls(args):
             "state_gb": sum(ob.state.numel() for (_g, ob, _W, _G) in groups) / 1e9}
         del cnoise
 
-    def small_leg(method, **kw):
-        """One 128 x 64 matrix (the one-CTA methods take m, n <= 128 in this
-        build), 200 timed steps after 20 warm-up steps; Clean's Gaussian
-        draws are drawn up front and stay resident like the gradients."""
-        swl = workload("single128x64")
+    def small_leg(method, wl_name="single128x64", nsteps=200, **kw):
+        """A small workload for the SOAP and Clean modes (one 128 x 64 matrix
+        by default), `nsteps` timed steps after 20 warm-up steps; Clean's
+        Gaussian draws are drawn up front and stay resident like the
+        gradients."""
+        swl = workload(wl_name)
         sgs = GradientStream(swl, dev)
         sg = swl.groups[0]
         sob = OklsBatch(sg.batch, sg.m, sg.n, param_dtype=sg.dtype, method=method, beta1=0.95, beta2=0.95,
@@ -536,7 +537,6 @@ def run_okls(args):
         for k in range(20):
             st(k)
         torch.cuda.synchronize()
-        nsteps = 200
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for k in range(nsteps):
@@ -547,17 +547,26 @@ def run_okls(args):
             raise RuntimeError(f"device status flagged in the {method} leg")
         ms4 = a.elapsed_time(b)
         sob.close()
-        return {"workload": "single128x64: one 128 x 64 fp32 matrix", "steps": nsteps,
+        desc = {"single128x64": "single128x64: one 128 x 64 fp32 matrix",
+                "batch16x512": "batch16x512: 16 x 512 x 512 fp32 matrices"}[wl_name]
+        return {"workload": desc, "steps": nsteps,
                 "value": sg.batch * nsteps / (ms4 / 1e3), "unit": "matrices/s", "ms_per_step": ms4 / nsteps}
 
     soap_line = clean_line = None
     if args.also_soap and args.method == "okls":
         soap_line = {"method": "SOAP (Adam in the factors' eigenbasis), fp32, one CTA per matrix, Jacobi refresh "
-                               "every 10 steps; matrices up to 128 x 128 in this build", **small_leg("soap")}
+                               "every 10 steps", **small_leg("soap")}
+    soap512_line = clean512_line = None
+    if args.also_soap and args.method == "okls":
+        soap512_line = {"method": "SOAP as above on the batched-GEMM path (eigensolves as packed triangles in L2 "
+                                  "at d = 512), refresh every 10 steps", **small_leg("soap", "batch16x512", 50)}
+    if args.also_clean and args.method == "okls":
+        clean512_line = {"method": "Clean, rank 56 + oversampling 8, one power iteration, refresh every 10 steps, "
+                                   "batched-GEMM path",
+                         **small_leg("clean", "batch16x512", 50, rank=56, oversample=8, power_iters=1)}
     if args.also_clean and args.method == "okls":
         clean_line = {"method": "Clean (block Adam in rank-16 Nystrom bases, oversampling 8, one power iteration), "
-                                "fp32, one CTA per factor, refresh every 10 steps; matrices up to 128 x 128 and "
-                                "rank + oversampling <= 64 in this build",
+                                "fp32, one CTA per factor, refresh every 10 steps",
                       **small_leg("clean", rank=16, oversample=8, power_iters=1)}
 
     cpu = None
@@ -605,6 +614,10 @@ def run_okls(args):
             line["clean"] = clean_line
         if clean_large_line:
             line["clean_large"] = clean_large_line
+        if soap512_line:
+            line["soap_512"] = soap512_line
+        if clean512_line:
+            line["clean_512"] = clean512_line
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
