@@ -558,8 +558,8 @@ def run_okls(args):
                                "every 10 steps", **small_leg("soap")}
     soap512_line = clean512_line = None
     if args.also_soap and args.method == "okls":
-        soap512_line = {"method": "SOAP as above on the batched-GEMM path (eigensolves as packed triangles in L2 "
-                                  "at d = 512), refresh every 10 steps", **small_leg("soap", "batch16x512", 50)}
+        soap512_line = {"method": "SOAP as above on the batched-GEMM path (Jacobi eigensolves with logged rotations, "
+                                  "the matrix in L2 at d = 512), refresh every 10 steps", **small_leg("soap", "batch16x512", 50)}
     if args.also_clean and args.method == "okls":
         clean512_line = {"method": "Clean, rank 56 + oversampling 8, one power iteration, refresh every 10 steps, "
                                    "batched-GEMM path",

@@ -140,8 +140,10 @@ typedef enum okls_state_part {
  *                   t % root_every == 0 Q_L, Q_R <- eigenvectors of L, R
  *                   (decreasing eigenvalues, signs aligned with the previous
  *                   basis); eps is Adam's.  Q = I before the first refresh.
- *                   This build runs SOAP for m, n <= 128 only (one CTA per
- *                   matrix, fp32, Jacobi eigensolver); larger shapes return
+ *                   This build runs SOAP for m, n <= 544 (fp32 throughout,
+ *                   cyclic Jacobi eigensolver warm-started from the previous
+ *                   basis; one CTA per matrix up to 128 x 128, batched fp32
+ *                   GEMMs past that); larger shapes return
  *                   OKLS_ERR_UNSUPPORTED.
  *                   OKLS_METHOD_CLEAN (Clean page, Algorithm 1 with the
  *                   sketch of Eqn. (8) and Appendix A, Algorithm 3): at

@@ -887,7 +887,9 @@ okls_status plan_clean(const okls_config& c, uint8_t* state, uint8_t* ws, okls_h
     cl.Cb = f32(wp, B * m * n);
     cl.part = f32(wp, B * kClParts);
     cl.cden = f32(wp, B);
-    cl.KK = k > 128 ? f32(wp, B * 2 * (k + 1) * (k + 1)) : nullptr;
+    cl.KK = k > 128 ? f32(wp, B * std::max<int64_t>(2 * (k + 1) * (k + 1),
+                                                   static_cast<int64_t>(eig_scratch_floats(static_cast<int>(k)))))
+                    : nullptr;
   }
   out->state_bytes = sp.off;
   out->ws_bytes = wp.off;
@@ -971,11 +973,12 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
       sl.Gp = f32(B * m * n);
       sl.Mp = f32(B * m * n);
       sl.T = f32(B * big);
-      sl.Qh = f32(B * dmax * dmax);
-      sl.A = f32(B * dmax * dmax);
-      sl.P = f32(B * dmax * dmax);
-      sl.Wq = f32(B * dmax * dmax);
-      sl.KK = dmax > 128 ? f32(B * 2 * (dmax + 1) * (dmax + 1)) : nullptr;
+      sl.Qh = f32(B * (m * m + n * n));
+      sl.A = f32(B * (m * m + n * n));
+      sl.P = f32(B * (m * m + n * n));
+      sl.Wq = f32(B * (m * m + n * n));
+      sl.KKL = m > 128 ? f32(B * static_cast<int64_t>(eig_scratch_floats(static_cast<int>(m)))) : nullptr;
+      sl.KKR = n > 128 ? f32(B * static_cast<int64_t>(eig_scratch_floats(static_cast<int>(n)))) : nullptr;
     }
     out->state_bytes = sp.off;
     out->ws_bytes = wp.off;

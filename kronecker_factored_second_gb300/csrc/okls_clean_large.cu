@@ -9,7 +9,8 @@
 // double-buffered slices in shared memory); only k x k work (k = r + p) stays in
 // one CTA per matrix: the Cholesky factors and inverses of the thin QRs and
 // of Omega^T Y_nu, the norm estimate for nu, and the Jacobi eigensolve of
-// Z^T Z that yields the thin SVD.  The thin QRs are Cholesky-QR applied four
+// Z^T Z that yields the thin SVD (past k = 128 the logged-rotation solver of
+// okls_eig.cu, whose rotations of V spread over many CTAs).  The thin QRs are Cholesky-QR applied four
 // times, a pass shifted where its factorisation breaks down (the
 // power-iterated sketch is ill-conditioned), so they reduce to Gram
 // products, k x k factorisations and products again.
@@ -198,13 +199,13 @@ cudaError_t launch_cl_gemm(const ClGemm& g0, cudaStream_t st) {
 constexpr int kLK = 128;
 constexpr int kLP = kLK + 1;        // odd pitch of the staged k x k matrices
 constexpr int kLThreads = 256;
-constexpr int kLWide = 1024;  // the packed kernels: more of a round's work in flight
+constexpr int kLWide = 1024;  // the packed Cholesky: more of a step's work in flight
 constexpr int kLVec = 2 * kClMaxK;  // floats: vectors / rotation parameters
 constexpr int kLInts = 2 * kClMaxK; // ints: pairs, then ranks
 constexpr int kLHead = kLVec + kLInts;
 constexpr int kLSmallSmem = (kLHead + 2 * kLK * kLP) * 4;
-// up to here the k x k matrix of the Cholesky and eigensolve kernels fits
-// shared memory as a packed triangle
+// up to here the k x k matrix of the packed Cholesky kernel fits shared
+// memory as a packed triangle
 constexpr int kPackMaxK = 330;
 
 struct KkStore {
@@ -464,7 +465,8 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
         const float apq = As[pp * ld + qq];
         const float app = As[pp * ld + pp], aqq = As[qq * ld + qq];
         float c = 1.0f, sn = 0.0f;
-        // threshold Jacobi (see k_cl_svd_packed)
+        // threshold Jacobi: a pair already below tol2 / k of its diagonal is
+        // left alone (when every pair is, the sweep's stopping rule holds)
         if (apq * apq > tol2 / static_cast<float>(k) * fabsf(app * aqq)) {
           const float th = (aqq - app) / (2.0f * apq);
           const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
@@ -534,161 +536,6 @@ __global__ void __launch_bounds__(kLThreads) k_cl_svd(const float* Gram, const f
   }
 }
 
-// The same thin SVD for k > 128: Z^T Z kept as a packed upper triangle
-// (padded to an even size dp; in shared memory up to kPackMaxK, in the
-// L2-resident scratch past it), the eigenvectors as V^T rows in that scratch.  A round's d'/2 disjoint rotations
-// (J_pq acting on rows and columns p, q) are applied as one pass over the
-// 2 x 2 blocks A[{p1, q1}, {p2, q2}] of every two pairs of the round
-// (block <- J1^T block J2; each unordered index pair lies in exactly one
-// block) and over the V^T rows p, q: two barriers per round.
-__device__ __forceinline__ int pk_idx(int i, int j, int dp) {  // i <= j
-  return i * dp - (i * (i - 1)) / 2 + (j - i);
-}
-__device__ __forceinline__ float pk_get(const float* A, int i, int j, int dp) {
-  return i <= j ? A[pk_idx(i, j, dp)] : A[pk_idx(j, i, dp)];
-}
-__device__ __forceinline__ void pk_set(float* A, int i, int j, int dp, float v) {
-  if (i <= j)
-    A[pk_idx(i, j, dp)] = v;
-  else
-    A[pk_idx(j, i, dp)] = v;
-}
-
-__global__ void __launch_bounds__(kLWide) k_cl_svd_packed(const float* Gram, const float* P, const float* nu,
-                                                             float* WU, float* lam, int k, int r, int max_sweeps,
-                                                             float tol2, float* scratch, const uint32_t* status) {
-  extern __shared__ float sm[];
-  __shared__ float red[kLWide / 32];
-  if (cl_flagged(status)) return;
-  const int b = blockIdx.x;
-  const float* Gb = Gram + static_cast<int64_t>(b) * k * k;
-  const int dp = k + (k & 1), np = dp / 2;
-  const float skip2 = tol2 / static_cast<float>(k);
-  float* cs = sm;                                // 2 per pair
-  int* pr = reinterpret_cast<int*>(sm + kLVec);  // 2 per pair, then ranks
-  float* Vt = scratch + static_cast<int64_t>(b) * 2 * (k + 1) * (k + 1);  // dp x dp, row c = column c of V
-  // packed upper triangle, dp (dp + 1) / 2: in shared memory up to kPackMaxK,
-  // past it beside V^T in the L2-resident slice
-  float* A = k <= kPackMaxK ? sm + kLHead : Vt + static_cast<int64_t>(k + 1) * (k + 1);
-  for (int j = threadIdx.x; j < dp; j += blockDim.x)
-    for (int i = 0; i <= j; ++i)
-      A[pk_idx(i, j, dp)] = (i < k && j < k) ? 0.5f * (Gb[i * k + j] + Gb[j * k + i]) : 0.0f;
-  for (int e = threadIdx.x; e < dp * dp; e += blockDim.x) Vt[e] = (e / dp == e % dp) ? 1.0f : 0.0f;
-  __syncthreads();
-  for (int sweep = 0; sweep < max_sweeps; ++sweep) {
-    float off = 0.0f, dg = 0.0f;
-    for (int j = threadIdx.x; j < dp; j += blockDim.x)
-      for (int i = 0; i <= j; ++i) {
-        const float v = A[pk_idx(i, j, dp)];
-        if (i == j)
-          dg = fmaf(v, v, dg);
-        else
-          off = fmaf(2.0f * v, v, off);
-      }
-    const float offs = cl_block_sum(off, red);
-    const float dgs = cl_block_sum(dg, red);
-    if (!(offs > tol2 * dgs)) break;
-    for (int rd = 0; rd < dp - 1; ++rd) {
-      for (int q = threadIdx.x; q < np; q += blockDim.x) {
-        auto idx = [&](int pos) { return pos == 0 ? 0 : 1 + (pos - 1 + rd) % (dp - 1); };
-        int pp = idx(q), qq = idx(dp - 1 - q);
-        if (pp > qq) {
-          const int x = pp;
-          pp = qq;
-          qq = x;
-        }
-        const float apq = A[pk_idx(pp, qq, dp)];
-        const float app = A[pk_idx(pp, pp, dp)], aqq = A[pk_idx(qq, qq, dp)];
-        float c = 1.0f, sn = 0.0f;
-        // threshold Jacobi: a pair already below tol2 / k of its diagonal is
-        // left alone (when every pair is, the sweep's stopping rule holds)
-        if (apq * apq > skip2 * fabsf(app * aqq)) {
-          const float th = (aqq - app) / (2.0f * apq);
-          const float t = copysignf(1.0f, th) / (fabsf(th) + sqrtf(fmaf(th, th, 1.0f)));
-          c = rsqrtf(fmaf(t, t, 1.0f));
-          sn = t * c;
-        }
-        cs[2 * q] = c;
-        cs[2 * q + 1] = sn;
-        pr[2 * q] = pp;
-        pr[2 * q + 1] = qq;
-      }
-      __syncthreads();
-      // A <- J^T A J on the 2 x 2 blocks of pairs (u, v), u <= v
-      for (int e = threadIdx.x; e < np * np; e += blockDim.x) {
-        const int u = e / np, v = e % np;
-        if (u > v) continue;
-        const float c1 = cs[2 * u], s1 = cs[2 * u + 1], c2 = cs[2 * v], s2 = cs[2 * v + 1];
-        if (s1 == 0.0f && s2 == 0.0f) continue;  // both rotations are the identity
-        const int p1 = pr[2 * u], q1 = pr[2 * u + 1], p2 = pr[2 * v], q2 = pr[2 * v + 1];
-        const float a11 = pk_get(A, p1, p2, dp), a12 = pk_get(A, p1, q2, dp);
-        const float a21 = pk_get(A, q1, p2, dp), a22 = pk_get(A, q1, q2, dp);
-        // rows: J1^T = [[c1, -s1], [s1, c1]]
-        const float r11 = c1 * a11 - s1 * a21, r12 = c1 * a12 - s1 * a22;
-        const float r21 = s1 * a11 + c1 * a21, r22 = s1 * a12 + c1 * a22;
-        // columns: J2 = [[c2, s2], [-s2, c2]]
-        const float n11 = c2 * r11 - s2 * r12, n12 = s2 * r11 + c2 * r12;
-        const float n21 = c2 * r21 - s2 * r22, n22 = s2 * r21 + c2 * r22;
-        if (u == v) {
-          pk_set(A, p1, p1, dp, n11);
-          pk_set(A, p1, q1, dp, n12);
-          pk_set(A, q1, q1, dp, n22);
-        } else {
-          pk_set(A, p1, p2, dp, n11);
-          pk_set(A, p1, q2, dp, n12);
-          pk_set(A, q1, p2, dp, n21);
-          pk_set(A, q1, q2, dp, n22);
-        }
-      }
-      // V <- V J: rows p, q of V^T
-      for (int e = threadIdx.x; e < np * dp; e += blockDim.x) {
-        const int u = e / dp, l = e % dp;
-        const float c = cs[2 * u], sn = cs[2 * u + 1];
-        if (sn == 0.0f) continue;
-        const int pp = pr[2 * u], qq = pr[2 * u + 1];
-        const float vp = Vt[static_cast<int64_t>(pp) * dp + l], vq = Vt[static_cast<int64_t>(qq) * dp + l];
-        Vt[static_cast<int64_t>(pp) * dp + l] = c * vp - sn * vq;
-        Vt[static_cast<int64_t>(qq) * dp + l] = sn * vp + c * vq;
-      }
-      __syncthreads();
-    }
-  }
-  for (int j = threadIdx.x; j < k; j += blockDim.x) {
-    const float lj = A[pk_idx(j, j, dp)];
-    int rank = 0;
-    for (int i = 0; i < k; ++i) {
-      const float li = A[pk_idx(i, i, dp)];
-      rank += (li > lj) || (li == lj && i < j);
-    }
-    pr[j] = rank;
-  }
-  __syncthreads();
-  // nu null: plain eigenvectors (no 1/sigma scaling) and eigenvalues
-  const bool unit = nu == nullptr;
-  const float nub = unit ? 0.0f : nu[b];
-  float* W = WU + static_cast<int64_t>(b) * k * r;
-  const float* Pb = P ? P + static_cast<int64_t>(b) * k * r : nullptr;
-  for (int j = threadIdx.x; j < k; j += blockDim.x) {
-    const int c = pr[j];
-    if (c >= r) continue;
-    const float s2 = A[pk_idx(j, j, dp)];
-    const float inv = unit ? 1.0f : (s2 > 0.0f ? rsqrtf(s2) : 0.0f);
-    const float* vj = Vt + static_cast<int64_t>(j) * dp;
-    float sg = 1.0f;
-    if (Pb) {
-      float dot = 0.0f;
-      for (int l = 0; l < k; ++l) dot = fmaf(vj[l], Pb[l * r + c], dot);
-      sg = dot < 0.0f ? -1.0f : 1.0f;
-    }
-    for (int l = 0; l < k; ++l) W[l * r + c] = sg * inv * vj[l];
-    if (lam) lam[static_cast<int64_t>(b) * r + c] = unit ? s2 : fmaxf(0.0f, s2 - nub);
-  }
-}
-
-inline int packed_smem(int k) {
-  const int dp = k + (k & 1);
-  return k <= kPackMaxK ? (kLHead + dp * (dp + 1) / 2) * 4 : kLHead * 4;
-}
 
 // ------------------------------------------------------- element-wise kernels
 // Omega = [U_prev, Psi] (warm) or Psi (cold) for one side: rows row0.. of the
@@ -955,7 +802,6 @@ cudaError_t cl_attributes() {
   e = cudaFuncSetAttribute(k_cl_chol_inv, at, kLSmallSmem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_norm, at, kLSmallSmem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_svd, at, kLSmallSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_svd_packed, at, packed_smem(kPackMaxK));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_chol_inv_packed, at, packed_chol_smem(kPackMaxK));
   if (e == cudaSuccess) attr_dev = dev;
   return e;
@@ -1047,29 +893,30 @@ void cl_nystrom(ClRun& R, int side) {
   // thin SVD of Z from Z^T Z; signs against the previous basis
   R.gemm(Z, 0, 1, k, sP, Z, 0, 0, k, sP, L.Gram, k, sK, k, k, d);
   if (L.warm) R.gemm(Z, 0, 1, k, sP, Uprev, 0, 0, r, sU, L.P, r, static_cast<int64_t>(k) * r, k, r, d);
-  R.launch([&] {
-    if (k > kLK)
-      k_cl_svd_packed<<<L.batch, kLWide, packed_smem(k), R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU,
-                                                                     lamOut, k, r, L.max_sweeps, L.tol2, L.KK,
-                                                                     L.status);
-    else
+  if (k > kLK) {
+    EigPlan plan{};
+    plan.side[0] = EigSide{L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU, lamOut, L.KK, k, r, L.batch};
+    plan.max_sweeps = L.max_sweeps;
+    plan.tol2 = L.tol2;
+    plan.status = L.status;
+    if (R.err == cudaSuccess) R.err = launch_eig_rounds(plan, R.st, R.launches);
+  } else {
+    R.launch([&] {
       k_cl_svd<<<L.batch, kLThreads, kk_smem(k), R.st>>>(L.Gram, L.warm ? L.P : nullptr, L.nu, L.WU, lamOut, k, r,
                                                            L.max_sweeps, L.tol2, L.KK, L.status);
-  });
+    });
+  }
   R.gemm(Z, 0, 0, k, sP, L.WU, 0, 0, r, static_cast<int64_t>(k) * r, Uout, r, sU, d, r, k);
 }
 
 }  // namespace
 
 cudaError_t launch_cl_eig(const float* A, const float* P, float* Wout, float* lam, int d, int batch, int max_sweeps,
-                          float tol2, float* scratch, uint32_t* status, cudaStream_t st) {
+                          float tol2, uint32_t* status, cudaStream_t st) {
+  if (d > kLK) return cudaErrorInvalidValue;
   cudaError_t e = cl_attributes();
   if (e != cudaSuccess) return e;
-  if (d > kLK)
-    k_cl_svd_packed<<<batch, kLWide, packed_smem(d), st>>>(A, P, nullptr, Wout, lam, d, d, max_sweeps, tol2, scratch,
-                                                            status);
-  else
-    k_cl_svd<<<batch, kLThreads, kk_smem(d), st>>>(A, P, nullptr, Wout, lam, d, d, max_sweeps, tol2, scratch, status);
+  k_cl_svd<<<batch, kLThreads, kk_smem(d), st>>>(A, P, nullptr, Wout, lam, d, d, max_sweeps, tol2, nullptr, status);
   return cudaGetLastError();
 }
 

@@ -155,13 +155,35 @@ struct ClLarge {
 constexpr int kClParts = 64;
 constexpr int kClMaxK = 544;  // largest r + p of the batched-GEMM path
 cudaError_t clean_large_refresh(const ClLarge& L, cudaStream_t st, int* launches);
-// Eigenvectors of the batch of symmetric d x d matrices A (d <= kClMaxK),
-// reordered by decreasing eigenvalue into Wout (d x d, column c = the
-// eigenvector of rank c), each column's sign chosen so that its product with
-// column c of P (d x d: the previous basis seen through the current one) is
-// >= 0 (P null: signs as the solver leaves them); eigenvalues into lam (may be null).
+// Eigenvectors of the batch of symmetric d x d matrices A (d <= 128, one CTA
+// per matrix in shared memory), reordered by decreasing eigenvalue into Wout
+// (d x d, column c = the eigenvector of rank c), each column's sign chosen so
+// that its product with column c of P (d x d: the previous basis seen through
+// the current one) is >= 0 (P null: signs as the solver leaves them);
+// eigenvalues into lam (may be null).  Past 128: launch_eig_rounds.
 cudaError_t launch_cl_eig(const float* A, const float* P, float* Wout, float* lam, int d, int batch, int max_sweeps,
-                          float tol2, float* scratch, uint32_t* status, cudaStream_t st);
+                          float tol2, uint32_t* status, cudaStream_t st);
+// Eigenvectors of batches of symmetric k x k matrices, 128 < k <= kClMaxK
+// (okls_eig.cu): cyclic Jacobi sweeps on one CTA per matrix, the rotations of
+// each sweep logged and applied to V by a wide kernel.  Up to two batches
+// (sides) of different k in one set of launches.
+struct EigSide {
+  const float* A;      // count x k x k; its symmetric part is diagonalised
+  const float* P;      // count x k x r, or null: column c's sign makes v . P[:, c] >= 0
+  const float* nu;     // count, or null: W = eigenvectors, lam = eigenvalues
+  float* W;            // count x k x r: the eigenvectors of the r largest eigenvalues (/ sigma with nu)
+  float* lam;          // count x r, or null
+  float* scratch;      // count x eig_scratch_floats(k), 16-byte aligned
+  int k, r, count;     // count = 0: side unused
+};
+struct EigPlan {
+  EigSide side[2];
+  int max_sweeps;      // >= 1
+  float tol2;          // stop once the off-diagonal's squared norm <= tol2 x the diagonal's
+  const uint32_t* status;
+};
+size_t eig_scratch_floats(int k);
+cudaError_t launch_eig_rounds(const EigPlan& P, cudaStream_t st, int* launches);
 cudaError_t launch_cl_prep(const void* G, int g_bf16, float* out, int64_t mn, int batch, uint32_t* status,
                            cudaStream_t st);
 cudaError_t clean_large_step(const ClLarge& L, cudaStream_t st, int* launches);
@@ -180,8 +202,9 @@ struct SoapLarge {
   uint32_t* status;
   float *Gf, *Gp, *Mp;                  // workspace: m x n each
   float* T;                             // max(m n, m^2, n^2)
-  float *Qh, *A, *P, *Wq;               // max(m, n)^2 each
-  float* KK;                            // eigensolver scratch past d = 128: 2 (d + 1)^2
+  float *Qh, *A, *P, *Wq;               // batch (m^2 + n^2) each: side L, then side R
+  float *KKL, *KKR;                     // eigensolver scratch of a side with d > 128:
+                                        // batch x eig_scratch_floats(d)
 };
 cudaError_t soap_large_step(const SoapLarge& S, int refresh, cudaStream_t st, int* launches);
 

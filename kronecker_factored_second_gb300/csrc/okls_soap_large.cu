@@ -9,9 +9,9 @@
 // batched GEMM; the moments and the update are element-wise.  The refresh
 // (after steps t with t % root_every == 0) warm-starts from the previous
 // basis Q as the one-CTA kernel does: Q^ = Q (3 I - Q^T Q)/2, then the
-// eigenvectors of Q^^T L Q^ by cyclic Jacobi (one CTA per matrix: in shared
-// memory up to d = 128, as a packed triangle up to 330, in L2 up to 544),
-// ordered by decreasing eigenvalue and sign-aligned with Q, and
+// eigenvectors of Q^^T L Q^ by cyclic Jacobi (in shared memory up to d = 128;
+// past it the logged-rotation solver of okls_eig.cu, both sides in one set of
+// launches), ordered by decreasing eigenvalue and sign-aligned with Q, and
 // Q <- Q^ W.
 #include <cuda_bf16.h>
 
@@ -129,23 +129,75 @@ struct SlRun {
   }
 };
 
-// Refresh of one side: Q (d x d, state) from the factor F (d x d, state).
-void sl_refresh_side(SlRun& R, const float* F, float* Q, int d) {
+// Buffers of one side of the refresh: the side's slices of Qh, A, P, Wq.
+struct SlSide {
+  const float* F;  // the factor (d x d, state)
+  float* Q;        // the basis (d x d, state)
+  int d;
+  float *Qh, *A, *P, *Wq, *KK;
+};
+
+// Q^ = Q (1.5 I - 0.5 Q^T Q);  A = Q^^T F Q^;  P = Q^^T Q (for the signs)
+void sl_refresh_prep(SlRun& R, const SlSide& s) {
   const SoapLarge& S = R.S;
+  const int d = s.d;
   const int64_t sd = static_cast<int64_t>(d) * d;
-  // Q^ = Q (1.5 I - 0.5 Q^T Q)
-  R.gemm(Q, 1, d, sd, Q, 0, d, sd, S.P, d, sd, d, d, d);
-  R.launch([&] { k_sl_polar<<<sl_grid(sd, S.batch), 256, 0, R.st>>>(S.P, d); });
-  R.gemm(Q, 0, d, sd, S.P, 0, d, sd, S.Qh, d, sd, d, d, d);
-  // A = Q^^T F Q^;  P = Q^^T Q (for the signs)
-  R.gemm(F, 0, d, sd, S.Qh, 0, d, sd, S.T, d, sd, d, d, d);
-  R.gemm(S.Qh, 1, d, sd, S.T, 0, d, sd, S.A, d, sd, d, d, d);
-  R.gemm(S.Qh, 1, d, sd, Q, 0, d, sd, S.P, d, sd, d, d, d);
-  R.launch([&] {
-    launch_cl_eig(S.A, S.P, S.Wq, nullptr, d, S.batch, S.max_sweeps, S.tol2, S.KK, S.status, R.st);
-  });
-  // Q <- Q^ W (skipped once the status word is set)
-  R.gemm(S.Qh, 0, d, sd, S.Wq, 0, d, sd, Q, d, sd, d, d, d, 1.0f, 0.0f, S.status);
+  R.gemm(s.Q, 1, d, sd, s.Q, 0, d, sd, s.P, d, sd, d, d, d);
+  R.launch([&] { k_sl_polar<<<sl_grid(sd, S.batch), 256, 0, R.st>>>(s.P, d); });
+  R.gemm(s.Q, 0, d, sd, s.P, 0, d, sd, s.Qh, d, sd, d, d, d);
+  R.gemm(s.F, 0, d, sd, s.Qh, 0, d, sd, S.T, d, sd, d, d, d);
+  R.gemm(s.Qh, 1, d, sd, S.T, 0, d, sd, s.A, d, sd, d, d, d);
+  R.gemm(s.Qh, 1, d, sd, s.Q, 0, d, sd, s.P, d, sd, d, d, d);
+}
+
+// Q <- Q^ W (skipped once the status word is set)
+void sl_refresh_finish(SlRun& R, const SlSide& s) {
+  const int d = s.d;
+  const int64_t sd = static_cast<int64_t>(d) * d;
+  R.gemm(s.Qh, 0, d, sd, s.Wq, 0, d, sd, s.Q, d, sd, d, d, d, 1.0f, 0.0f, R.S.status);
+}
+
+EigSide eig_side(const SoapLarge& S, const SlSide& s) {
+  EigSide e{};
+  e.A = s.A;
+  e.P = s.P;
+  e.W = s.Wq;
+  e.scratch = s.KK;
+  e.k = s.d;
+  e.r = s.d;
+  e.count = S.batch;
+  return e;
+}
+
+// Both sides' bases: the eigen-decompositions of both sides go out in one
+// set of launches where both are past 128 (each is one CTA per matrix, so
+// this doubles the SMs at work).
+void sl_refresh(SlRun& R) {
+  const SoapLarge& S = R.S;
+  const int64_t mm = static_cast<int64_t>(S.m) * S.m;
+  const int64_t off = static_cast<int64_t>(S.batch) * mm;
+  const SlSide sL{S.L, S.QL, S.m, S.Qh, S.A, S.P, S.Wq, S.KKL};
+  const SlSide sR{S.R, S.QR, S.n, S.Qh + off, S.A + off, S.P + off, S.Wq + off, S.KKR};
+  sl_refresh_prep(R, sL);
+  sl_refresh_prep(R, sR);
+  EigPlan plan{};
+  plan.max_sweeps = S.max_sweeps;
+  plan.tol2 = S.tol2;
+  plan.status = S.status;
+  int nside = 0;
+  for (const SlSide* s : {&sL, &sR}) {
+    if (s->d > 128) {
+      plan.side[nside++] = eig_side(S, *s);
+    } else {
+      if (R.err == cudaSuccess) {
+        R.err = launch_cl_eig(s->A, s->P, s->Wq, nullptr, s->d, S.batch, S.max_sweeps, S.tol2, S.status, R.st);
+        ++*R.launches;
+      }
+    }
+  }
+  if (nside > 0 && R.err == cudaSuccess) R.err = launch_eig_rounds(plan, R.st, R.launches);
+  sl_refresh_finish(R, sL);
+  sl_refresh_finish(R, sR);
 }
 
 }  // namespace
@@ -180,10 +232,7 @@ cudaError_t soap_large_step(const SoapLarge& S, int refresh, cudaStream_t st, in
   // L <- b2 L + (1-b2) G G^T;  R <- b2 R + (1-b2) G^T G
   R.gemm(S.Gf, 0, n, mn, S.Gf, 1, n, mn, S.L, m, mm, m, m, n, 1.0f - S.beta2, S.beta2, S.status);
   R.gemm(S.Gf, 1, n, mn, S.Gf, 0, n, mn, S.R, n, nn, n, n, m, 1.0f - S.beta2, S.beta2, S.status);
-  if (refresh) {
-    sl_refresh_side(R, S.L, S.QL, m);
-    sl_refresh_side(R, S.R, S.QR, n);
-  }
+  if (refresh) sl_refresh(R);
   return R.err;
 }
 

@@ -175,6 +175,7 @@ LARGE_CASES = [
     (2, 260, 180, 131, 6, 1, 2, torch.float32, 0.0, "iid"),   # r + p = 137: packed eigensolve, odd k
     (1, 400, 300, 256, 8, 1, 2, torch.float32, 0.0, "iid"),   # the pages' rank 256 with oversampling 8
     (1, 420, 360, 332, 8, 0, 2, torch.float32, 0.0, "iid"),   # r + p = 340: the eigensolve's matrices in L2
+    (1, 600, 560, 536, 8, 0, 2, torch.float32, 0.0, "iid"),   # r + p = 544: the largest sketch
 ]
 
 

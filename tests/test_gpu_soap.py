@@ -1,4 +1,4 @@
-"""GPU parity of the SOAP mode (okls_config.method = SOAP, m, n <= 128)
+"""GPU parity of the SOAP mode (okls_config.method = SOAP, m, n <= 544)
 against the float64 oracle, through the C ABI.
 
 Teacher-forced: every step starts the oracle from the GPU's own state
@@ -6,7 +6,8 @@ Teacher-forced: every step starts the oracle from the GPU's own state
 N to 1e-4 (2e-2 with bf16 parameters, which round the new W); after a refresh
 the bases must be orthogonal and diagonalise L, R (1e-5), carry decreasing
 eigenvalues and agree in sign with the previous bases (orthogonality to
-1e-5 d in Frobenius norm: fp32 rotations), and every eigenvector
+1e-5 d in Frobenius norm, sqrt(d / 128) of that past d = 128: fp32
+rotations and d-deep fp32 sums, whose rounding grows like sqrt(d)), and every eigenvector
 whose eigenvalue is separated from its neighbours by more than 1e-3 of the
 spectrum must match the oracle's within 2e-6 ||L||_F / gap: twice the
 solver's stopping residual (1e-6 of the matrix in Frobenius norm, sqrt(d /
@@ -82,9 +83,11 @@ def test_teacher_forced_steps(B, m, n, dtype):
 
 
 # the batched-GEMM path: m or n past 128 (or forced); eigensolves in shared
-# memory up to 128, as packed triangles up to 330, in L2 past that
+# memory up to 128, past it by logged rotations (the matrix a packed triangle
+# in shared memory up to 330, a full one in L2 past that)
 @pytest.mark.parametrize("B,m,n,dtype", [(2, 200, 150, torch.float32), (1, 300, 140, torch.float32),
-                                         (2, 96, 64, torch.float32), (1, 160, 340, torch.bfloat16)])
+                                         (2, 96, 64, torch.float32), (1, 160, 340, torch.bfloat16),
+                                         (1, 544, 331, torch.float32)])  # the largest side; an odd one past 330
 def test_teacher_forced_steps_large_path(B, m, n, dtype, monkeypatch):
     monkeypatch.setenv("OKLS_SOAP_LARGE", "1")
     _teacher_forced(B, m, n, dtype)
@@ -128,10 +131,11 @@ def _teacher_forced(B, m, n, dtype):
     assert worst["N"] < (2e-2 if dtype == torch.bfloat16 else 1e-4), worst
     assert worst["Q_same"] == 0.0
     for side in ("QL", "QR"):
-        assert worst[side + "_orth"] < 1e-5 and worst[side + "_offdiag"] < 1e-5, worst
+        grow = max(1.0, (m if side == "QL" else n) / 128) ** 0.5
+        assert worst[side + "_orth"] < 1e-5 * grow and worst[side + "_offdiag"] < 1e-5, worst
         assert worst[side + "_order"] < 1e-6 and worst[side + "_sign"] == 0.0, worst
         # the solver's stopping residual is 1e-6 up to d = 128, sqrt(d / 128) of that past it
-        assert worst[side + "_vec_gap"] < 2e-6 * max(1.0, (m if side == "QL" else n) / 128) ** 0.5, worst
+        assert worst[side + "_vec_gap"] < 2e-6 * grow, worst
     ob.close()
 
 
