@@ -6,7 +6,7 @@
 // Eigenvectors(L, Q_L)) and by Clean's thin SVD of the sketch (Clean page,
 // Appendix A, Algorithm 3: the eigen-decomposition of Z^T Z).
 //
-// Per sweep, two launches:
+// Per sweep, two launches (three when a plan mixes both storage variants):
 //   k_eig_sweep  one CTA per matrix.  The matrix A sits as a packed upper
 //                triangle in shared memory up to kEigPackMaxK, and as a full
 //                symmetric dp x dp matrix in an L2-resident scratch slice past
@@ -30,6 +30,7 @@
 // block B with x's rows, and the item that owns the transposed block writes
 // the transpose of the same result.
 #include <algorithm>
+#include <cstdlib>
 
 #include "okls_internal.h"
 #include "okls_kernels.h"
@@ -144,11 +145,10 @@ __device__ __forceinline__ float2 jacobi_cs(float app, float aqq, float apq, flo
 
 }  // namespace
 
-// One sweep of cyclic Jacobi on one matrix per CTA.  kFull: A lives as a full
-// dp x dp matrix in the scratch slice; else as a packed triangle in shared
-// memory, loaded from / stored to the slice around the sweep.
-template <bool kFull>
-__device__ void sweep_body(const EigPlan& P, const EigSide& S, int b, int sweep, float* sm) {
+// One sweep on one matrix per CTA with A as a packed triangle in shared
+// memory (k <= kEigPackMaxK), loaded from / stored to the slice around the
+// sweep.
+__device__ void sweep_packed(const EigPlan& P, const EigSide& S, int b, int sweep, float* sm) {
   __shared__ float red[kEigThreads / 32];
   const int k = S.k;
   const int dp = k + (k & 1), np = dp / 2;
@@ -158,33 +158,24 @@ __device__ void sweep_body(const EigPlan& P, const EigSide& S, int b, int sweep,
     if (threadIdx.x == 0) sl.flags[1] = 0;
     return;
   }
-  float* cs = sm;                                   // 2 per pair
+  float* cs = sm;                                      // 2 per pair
   int* pr = reinterpret_cast<int*>(sm + 2 * kClMaxK);  // 2 per pair
-  float* A = kFull ? sl.A : sm + kEigHead;
+  float* A = sm + kEigHead;
   const int tid = threadIdx.x, nth = blockDim.x;
+  const int npk = dp * (dp + 1) / 2;
   if (sweep == 0) {
-    // the symmetric part of the input (bit-exactly symmetric), padded by a
-    // zero row and column when k is odd
+    // the symmetric part of the input, padded by a zero row and column when k is odd
     const float* G = S.A + static_cast<int64_t>(b) * k * k;
     for (int j = tid; j < dp; j += nth)
-      for (int i = 0; i <= j; ++i) {
-        const float v = (i < k && j < k) ? 0.5f * (G[i * k + j] + G[j * k + i]) : 0.0f;
-        if (kFull) {
-          A[static_cast<int64_t>(i) * dp + j] = v;
-          A[static_cast<int64_t>(j) * dp + i] = v;
-        } else {
-          A[pk(i, j, dp)] = v;
-        }
-      }
-  } else if (!kFull) {
-    const int npk = dp * (dp + 1) / 2;
+      for (int i = 0; i <= j; ++i) A[pk(i, j, dp)] = (i < k && j < k) ? 0.5f * (G[i * k + j] + G[j * k + i]) : 0.0f;
+  } else {
     for (int e = tid; e < npk; e += nth) A[e] = sl.A[e];
   }
   __syncthreads();
   float off = 0.0f, dg = 0.0f;
   for (int j = tid; j < dp; j += nth)
     for (int i = 0; i <= j; ++i) {
-      const float v = kFull ? A[static_cast<int64_t>(i) * dp + j] : A[pk(i, j, dp)];
+      const float v = A[pk(i, j, dp)];
       if (i == j)
         dg = fmaf(v, v, dg);
       else
@@ -203,17 +194,7 @@ __device__ void sweep_body(const EigPlan& P, const EigSide& S, int b, int sweep,
       for (int q = tid; q < np; q += nth) {
         int pp, qq;
         round_pair(q, rd, dp, pp, qq);
-        float app, aqq, apq;
-        if (kFull) {
-          app = A[static_cast<int64_t>(pp) * dp + pp];
-          aqq = A[static_cast<int64_t>(qq) * dp + qq];
-          apq = A[static_cast<int64_t>(pp) * dp + qq];
-        } else {
-          app = A[pk(pp, pp, dp)];
-          aqq = A[pk(qq, qq, dp)];
-          apq = A[pk(pp, qq, dp)];
-        }
-        const float2 r = jacobi_cs(app, aqq, apq, skip2);
+        const float2 r = jacobi_cs(A[pk(pp, pp, dp)], A[pk(qq, qq, dp)], A[pk(pp, qq, dp)], skip2);
         cs[2 * q] = r.x;
         cs[2 * q + 1] = r.y;
         pr[2 * q] = pp;
@@ -221,93 +202,173 @@ __device__ void sweep_body(const EigPlan& P, const EigSide& S, int b, int sweep,
         sl.log[static_cast<int64_t>(rd) * np + q] = r;
       }
       __syncthreads();
-      if (kFull) {
-        // every ordered pair of pairs (x, y): rows {p_x, q_x}, columns {p_y, q_y}
-        const int total = np * np;
-        int x = tid / np, y = tid - (tid / np) * np;
-        const int dx = nth / np, dy = nth - dx * np;
-        for (int e = tid; e < total; e += nth) {
-          const float c1 = cs[2 * x], s1 = cs[2 * x + 1], c2 = cs[2 * y], s2 = cs[2 * y + 1];
-          if (s1 != 0.0f || s2 != 0.0f) {
-            const int p1 = pr[2 * x], q1 = pr[2 * x + 1], p2 = pr[2 * y], q2 = pr[2 * y + 1];
-            float* r1 = A + static_cast<int64_t>(p1) * dp;
-            float* r2 = A + static_cast<int64_t>(q1) * dp;
-            const Blk C{r1[p2], r1[q2], r2[p2], r2[q2]};
-            if (x == y) {
-              const Blk n = rot2(C, c1, s1, c1, s1);
-              r1[p1] = n.a11;
-              r1[q1] = n.a12;
-              r2[p1] = n.a12;
-              r2[q1] = n.a22;
-            } else if (x < y) {
-              const Blk n = rot2(C, c1, s1, c2, s2);
-              r1[p2] = n.a11;
-              r1[q2] = n.a12;
-              r2[p2] = n.a21;
-              r2[q2] = n.a22;
-            } else {
-              // the block of {y, x} is C^T; write the transpose of its result
-              const Blk n = rot2(Blk{C.a11, C.a21, C.a12, C.a22}, c2, s2, c1, s1);
-              r1[p2] = n.a11;
-              r1[q2] = n.a21;
-              r2[p2] = n.a12;
-              r2[q2] = n.a22;
-            }
-          }
-          x += dx;
-          y += dy;
-          if (y >= np) {
-            y -= np;
-            ++x;
-          }
-        }
-      } else {
-        // the upper blocks (u <= v) of the packed triangle
-        for (int e = tid; e < np * np; e += nth) {
-          const int u = e / np, v = e - (e / np) * np;
-          if (u > v) continue;
-          const float c1 = cs[2 * u], s1 = cs[2 * u + 1], c2 = cs[2 * v], s2 = cs[2 * v + 1];
-          if (s1 == 0.0f && s2 == 0.0f) continue;
-          const int p1 = pr[2 * u], q1 = pr[2 * u + 1], p2 = pr[2 * v], q2 = pr[2 * v + 1];
-          auto get = [&](int i, int j) { return i <= j ? A[pk(i, j, dp)] : A[pk(j, i, dp)]; };
-          auto set = [&](int i, int j, float val) {
-            if (i <= j)
-              A[pk(i, j, dp)] = val;
-            else
-              A[pk(j, i, dp)] = val;
-          };
-          const Blk n = rot2(Blk{get(p1, p2), get(p1, q2), get(q1, p2), get(q1, q2)}, c1, s1, c2, s2);
-          if (u == v) {
-            set(p1, p1, n.a11);
-            set(p1, q1, n.a12);
-            set(q1, q1, n.a22);
-          } else {
-            set(p1, p2, n.a11);
-            set(p1, q2, n.a12);
-            set(q1, p2, n.a21);
-            set(q1, q2, n.a22);
-          }
+      // the upper blocks (u <= v)
+      for (int e = tid; e < np * np; e += nth) {
+        const int u = e / np, v = e - (e / np) * np;
+        if (u > v) continue;
+        const float c1 = cs[2 * u], s1 = cs[2 * u + 1], c2 = cs[2 * v], s2 = cs[2 * v + 1];
+        if (s1 == 0.0f && s2 == 0.0f) continue;
+        const int p1 = pr[2 * u], q1 = pr[2 * u + 1], p2 = pr[2 * v], q2 = pr[2 * v + 1];
+        auto get = [&](int i, int j) { return i <= j ? A[pk(i, j, dp)] : A[pk(j, i, dp)]; };
+        auto set = [&](int i, int j, float val) {
+          if (i <= j)
+            A[pk(i, j, dp)] = val;
+          else
+            A[pk(j, i, dp)] = val;
+        };
+        const Blk n = rot2(Blk{get(p1, p2), get(p1, q2), get(q1, p2), get(q1, q2)}, c1, s1, c2, s2);
+        if (u == v) {
+          set(p1, p1, n.a11);
+          set(p1, q1, n.a12);
+          set(q1, q1, n.a22);
+        } else {
+          set(p1, p2, n.a11);
+          set(p1, q2, n.a12);
+          set(q1, p2, n.a21);
+          set(q1, q2, n.a22);
         }
       }
       __syncthreads();
     }
   }
-  // the packed triangle goes back to the slice for the next sweep and the
-  // finishing kernel (at sweep 0 also when nothing rotated: it was built here)
-  if (!kFull && (more || sweep == 0)) {
-    const int npk = dp * (dp + 1) / 2;
+  // back to the slice for the next sweep and the finishing kernel (at sweep
+  // 0 also when nothing rotated: it was built here)
+  if (more || sweep == 0)
     for (int e = tid; e < npk; e += nth) sl.A[e] = A[e];
-  }
 }
 
-__global__ void __launch_bounds__(kEigThreads) k_eig_sweep(const __grid_constant__ EigPlan P, int sweep) {
+__global__ void __launch_bounds__(kEigThreads) k_eig_sweep_packed(const __grid_constant__ EigPlan P, int sweep) {
   extern __shared__ float sm[];
   if (eig_flagged(P.status)) return;
   const Where w = locate(P, 1, 1);
-  if (w.side->k > kEigPackMaxK)
-    sweep_body<true>(P, *w.side, w.b, sweep, sm);
+  sweep_packed(P, *w.side, w.b, sweep, sm);
+}
+
+__device__ __forceinline__ unsigned cl_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ unsigned cl_size() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster; global writes before it are
+// visible to the cluster's reads after it
+__device__ __forceinline__ void cl_barrier(unsigned nc) {
+  if (nc > 1)
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   else
-    sweep_body<false>(P, *w.side, w.b, sweep, sm);
+    __syncthreads();
+}
+
+// One sweep with A as a full symmetric dp x dp matrix in the L2-resident
+// slice, on a cluster of nc CTAs per matrix (nc = 1: a plain launch).  CTA c
+// of the cluster applies the blocks of the row pairs x in its share of
+// [0, dp / 2); every CTA forms all of a round's rotations itself (the same
+// numbers in each), and two cluster barriers per round separate the reads of
+// the rotation inputs from the pass's writes and the pass from the next
+// round.  A is read through L2 (ld.global.cg): other SMs write it.
+__global__ void __launch_bounds__(kEigThreads) k_eig_sweep_l2(const __grid_constant__ EigPlan P, int sweep) {
+  extern __shared__ float sm[];
+  __shared__ float red[kEigThreads / 32];
+  const unsigned nc = cl_size(), rank = cl_rank();
+  if (eig_flagged(P.status)) return;
+  const Where w = locate(P, static_cast<int>(nc), static_cast<int>(nc));
+  const EigSide& S = *w.side;
+  const int k = S.k, b = w.b;
+  const int dp = k + (k & 1), np = dp / 2;
+  const EigSlice sl = eig_slice(S.scratch, k, b);
+  if (sweep > 0 && __ldcg(sl.flags) == 0) {
+    if (rank == 0 && threadIdx.x == 0) sl.flags[1] = 0;
+    return;
+  }
+  float2* cs = reinterpret_cast<float2*>(sm);               // per pair
+  int2* pr = reinterpret_cast<int2*>(sm + 2 * kClMaxK);     // per pair
+  float* A = sl.A;
+  const int tid = threadIdx.x, nth = blockDim.x;
+  if (sweep == 0) {
+    const float* G = S.A + static_cast<int64_t>(b) * k * k;
+    for (int j = static_cast<int>(rank) * nth + tid; j < dp; j += static_cast<int>(nc) * nth)
+      for (int i = 0; i <= j; ++i) {
+        const float v = (i < k && j < k) ? 0.5f * (G[i * k + j] + G[j * k + i]) : 0.0f;
+        __stcg(A + i * dp + j, v);
+        __stcg(A + j * dp + i, v);
+      }
+    cl_barrier(nc);
+  }
+  float off = 0.0f, dg = 0.0f;
+  for (int j = tid; j < dp; j += nth)
+#pragma unroll 4
+    for (int i = 0; i <= j; ++i) {
+      const float v = __ldcg(A + i * dp + j);
+      if (i == j)
+        dg = fmaf(v, v, dg);
+      else
+        off = fmaf(2.0f * v, v, off);
+    }
+  const float offs = eig_block_sum(off, red);
+  const float dgs = eig_block_sum(dg, red);
+  // every CTA of the cluster reached the same decision from the same sums;
+  // the flags change only after all of them have read them
+  const bool more = offs > P.tol2 * dgs;
+  cl_barrier(nc);
+  if (rank == 0 && tid == 0) {
+    sl.flags[0] = more ? 1 : 0;
+    sl.flags[1] = more ? 1 : 0;
+  }
+  if (!more) return;
+  const float skip2 = P.tol2 / static_cast<float>(k);
+  const int x0 = static_cast<int>(rank) * np / static_cast<int>(nc);
+  const int x1 = (static_cast<int>(rank) + 1) * np / static_cast<int>(nc);
+  const int ng = (np + 31) >> 5;   // groups of 32 column pairs
+  const int ntask = ng * (x1 - x0);
+  const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
+  for (int rd = 0; rd < dp - 1; ++rd) {
+    for (int q = tid; q < np; q += nth) {
+      int pp, qq;
+      round_pair(q, rd, dp, pp, qq);
+      const float2 r = jacobi_cs(__ldcg(A + pp * dp + pp), __ldcg(A + qq * dp + qq), __ldcg(A + pp * dp + qq), skip2);
+      cs[q] = r;
+      pr[q] = make_int2(pp, qq);
+      if (rank == 0) sl.log[static_cast<int64_t>(rd) * np + q] = r;
+    }
+    __syncthreads();
+    cl_barrier(nc);
+    // task = (row pair x, 32 column pairs y); x is the same on every lane
+    for (int t = warp; t < ntask; t += nwarp) {
+      const int x = x0 + t / ng;
+      const int y = ((t - (t / ng) * ng) << 5) + lane;
+      if (y >= np) continue;
+      const float2 cx = cs[x], cy = cs[y];
+      if (cx.y == 0.0f && cy.y == 0.0f) continue;
+      const int2 px = pr[x], py = pr[y];
+      float* r1 = A + px.x * dp;
+      float* r2 = A + px.y * dp;
+      const float a11 = __ldcg(r1 + py.x), a12 = __ldcg(r1 + py.y);
+      const float a21 = __ldcg(r2 + py.x), a22 = __ldcg(r2 + py.y);
+      if (x == y) {
+        const Blk n = rot2(Blk{a11, a12, a21, a22}, cx.x, cx.y, cx.x, cx.y);
+        __stcg(r1 + px.x, n.a11);
+        __stcg(r1 + px.y, n.a12);
+        __stcg(r2 + px.x, n.a12);
+        __stcg(r2 + px.y, n.a22);
+      } else {
+        // the block of the unordered pair is formed from the lower index's
+        // rows: for x > y that is C^T, and the result is written transposed
+        const bool tr = x > y;
+        const Blk in = tr ? Blk{a11, a21, a12, a22} : Blk{a11, a12, a21, a22};
+        const float2 lo = tr ? cy : cx, hi = tr ? cx : cy;
+        const Blk n = rot2(in, lo.x, lo.y, hi.x, hi.y);
+        __stcg(r1 + py.x, n.a11);
+        __stcg(r1 + py.y, tr ? n.a21 : n.a12);
+        __stcg(r2 + py.x, tr ? n.a12 : n.a21);
+        __stcg(r2 + py.y, n.a22);
+      }
+    }
+    cl_barrier(nc);
+  }
 }
 
 // V <- V J for the rotations logged by sweep `sweep`, on a band of
@@ -386,7 +447,7 @@ __global__ void __launch_bounds__(kFinishThreads) k_eig_finish(const __grid_cons
   const int b = w.b, k = S.k, r = S.r;
   const int dp = k + (k & 1);
   const EigSlice sl = eig_slice(S.scratch, k, b);
-  const bool full = k > kEigPackMaxK;
+  const bool full = S.full != 0;
   const int tid = threadIdx.x, nth = blockDim.x;
   for (int j = tid; j < k; j += nth) dg[j] = full ? sl.A[static_cast<int64_t>(j) * dp + j] : sl.A[pk(j, j, dp)];
   __syncthreads();
@@ -432,10 +493,57 @@ cudaError_t eig_attributes() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || attr_dev == dev) return e;
   const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  e = cudaFuncSetAttribute(k_eig_sweep, at, sweep_smem(kEigPackMaxK));
+  e = cudaFuncSetAttribute(k_eig_sweep_packed, at, sweep_smem(kEigPackMaxK));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_eig_apply, at, kApplyRows * (kClMaxK + 1) * 4);
   if (e == cudaSuccess) attr_dev = dev;
   return e;
+}
+
+cudaLaunchConfig_t l2_config(int nb, int nc, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(nb * nc));
+  cfg.blockDim = dim3(kEigThreads);
+  cfg.dynamicSmemBytes = kEigHead * 4;
+  cfg.stream = st;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = static_cast<unsigned>(nc);
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = nc > 1 ? 1 : 0;
+  return cfg;
+}
+
+// CTAs per matrix for the L2 sweep: as many as keep every SM busy, up to a
+// cluster of 8, and no more than the device can co-schedule
+int cluster_size(int nb) {
+  static int dev_cached = -1, sms = 0, max_ok = 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev != dev_cached) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 1;
+    max_ok = 1;
+    for (int nc = 8; nc > 1; --nc) {
+      cudaLaunchAttribute attr;
+      cudaLaunchConfig_t cfg = l2_config(1, nc, nullptr, &attr);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_eig_sweep_l2), &cfg) == cudaSuccess &&
+          n >= 1) {
+        max_ok = nc;
+        break;
+      }
+    }
+    (void)cudaGetLastError();
+    dev_cached = dev;
+  }
+  int cap = max_ok;
+  // OKLS_EIG_CTAS=c caps the CTAs per matrix (tests run the one-CTA kernels
+  // on small batches with c = 1)
+  if (const char* env = getenv("OKLS_EIG_CTAS")) {
+    const int c = atoi(env);
+    if (c >= 1) cap = std::min(cap, c);
+  }
+  return std::max(1, std::min(cap, sms / std::max(nb, 1)));
 }
 
 }  // namespace
@@ -451,22 +559,38 @@ cudaError_t launch_eig_rounds(const EigPlan& P, cudaStream_t st, int* launches) 
   if (nb == 0) return cudaSuccess;
   cudaError_t e = eig_attributes();
   if (e != cudaSuccess) return e;
+  const int nc = cluster_size(nb);
   int smem = 0, dpmax = 0, bands[2] = {1, 1}, napply = 0;
+  bool any_large = false;
   for (int i = 0; i < 2; ++i) {
     const EigSide& S = P.side[i];
     if (S.count == 0) continue;
+    any_large |= S.k > kEigPackMaxK;
     smem = std::max(smem, sweep_smem(S.k));
     dpmax = std::max(dpmax, S.k + (S.k & 1));
     bands[i] = (S.k + kApplyRows - 1) / kApplyRows;
     napply += S.count * bands[i];
   }
+  // one CTA per matrix with A in shared memory where that fits and the
+  // batch fills the GPU; else clusters over A in L2 (every side alike, so
+  // that one launch covers both)
+  const bool l2 = nc > 1 || any_large;
+  EigPlan Q = P;
+  Q.side[0].full = Q.side[1].full = l2 ? 1 : 0;
   const int apply_smem = kApplyRows * dpmax * 4;
-  for (int s = 0; s < P.max_sweeps; ++s) {
-    k_eig_sweep<<<nb, kEigThreads, smem, st>>>(P, s);
-    k_eig_apply<<<napply, kApplyThreads, apply_smem, st>>>(P, s, bands[0], bands[1]);
+  for (int s = 0; s < Q.max_sweeps; ++s) {
+    if (l2) {
+      cudaLaunchAttribute attr;
+      const cudaLaunchConfig_t cfg = l2_config(nb, nc, st, &attr);
+      e = cudaLaunchKernelEx(&cfg, k_eig_sweep_l2, Q, s);
+      if (e != cudaSuccess) return e;
+    } else {
+      k_eig_sweep_packed<<<nb, kEigThreads, smem, st>>>(Q, s);
+    }
+    k_eig_apply<<<napply, kApplyThreads, apply_smem, st>>>(Q, s, bands[0], bands[1]);
   }
-  k_eig_finish<<<nb, kFinishThreads, 0, st>>>(P);
-  if (launches) *launches += 2 * P.max_sweeps + 1;
+  k_eig_finish<<<nb, kFinishThreads, 0, st>>>(Q);
+  if (launches) *launches += 2 * Q.max_sweeps + 1;
   return cudaGetLastError();
 }
 

@@ -175,6 +175,7 @@ struct EigSide {
   float* lam;          // count x r, or null
   float* scratch;      // count x eig_scratch_floats(k), 16-byte aligned
   int k, r, count;     // count = 0: side unused
+  int full;            // set by launch_eig_rounds: A kept as a full matrix in L2
 };
 struct EigPlan {
   EigSide side[2];

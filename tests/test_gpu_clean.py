@@ -193,6 +193,14 @@ def test_teacher_forced_steps_large_path(B, m, n, r, p, q, T, dtype, wd, spectru
     _teacher_forced(B, m, n, r, p, q, T, dtype, wd, spectrum)
 
 
+def test_rank256_one_cta_per_matrix(monkeypatch):
+    """The pages' rank 256 + 8 with the eigensolver on one CTA per matrix
+    (the packed-triangle kernel that full layer sets take)."""
+    monkeypatch.setenv("OKLS_CLEAN_LARGE", "1")
+    monkeypatch.setenv("OKLS_EIG_CTAS", "1")
+    _teacher_forced(1, 400, 300, 256, 8, 1, 2, torch.float32, 0.0, "iid")
+
+
 def _teacher_forced(B, m, n, r, p, q, T, dtype, wd, spectrum):
     lr, b1, b2, eps = 0.01, 0.95, 0.95, 1e-8
     ob = _batch(B, m, n, param_dtype=dtype, lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=wd, root_every=T,

@@ -93,6 +93,15 @@ def test_teacher_forced_steps_large_path(B, m, n, dtype, monkeypatch):
     _teacher_forced(B, m, n, dtype)
 
 
+# the eigensolver's one-CTA-per-matrix kernels, which batches that fill the
+# GPU take: packed triangle in shared memory (d <= 330), full matrix in L2
+@pytest.mark.parametrize("B,m,n,dtype", [(2, 200, 150, torch.float32), (1, 160, 340, torch.float32)])
+def test_large_path_one_cta_per_matrix(B, m, n, dtype, monkeypatch):
+    monkeypatch.setenv("OKLS_SOAP_LARGE", "1")
+    monkeypatch.setenv("OKLS_EIG_CTAS", "1")
+    _teacher_forced(B, m, n, dtype)
+
+
 def _teacher_forced(B, m, n, dtype):
     lr, b1, b2, eps, f = 0.01, 0.9, 0.95, 1e-8, 2
     ob = _batch(B, m, n, param_dtype=dtype, lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=0.0, root_every=f)
