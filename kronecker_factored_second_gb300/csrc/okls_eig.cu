@@ -42,6 +42,7 @@ namespace {
 constexpr int kEigPackMaxK = 330;  // packed triangle in shared memory up to here
 constexpr int kEigThreads = 1024;
 constexpr int kApplyRows = 32;
+constexpr int kApplyPitch = kApplyRows + 4;  // floats per column of a band (16-byte rows, banks staggered)
 constexpr int kApplyThreads = 256;
 constexpr int kFinishThreads = 512;
 constexpr int kEigHead = 4 * kClMaxK;  // floats: rotations (2 per pair), pairs (2 per pair)
@@ -263,6 +264,55 @@ __device__ __forceinline__ void cl_barrier(unsigned nc) {
     __syncthreads();
 }
 
+// The L2 pass's block item (x, y): load its four entries (false when the
+// item is out of range or both its rotations are the identity) ...
+__device__ __forceinline__ bool l2_load(const float* A, int dp, const float2* cs, const int2* pr, int x, int y, int np,
+                                        Blk& c) {
+  if (y >= np) return false;
+  if (cs[x].y == 0.0f && cs[y].y == 0.0f) return false;
+  const int2 px = pr[x], py = pr[y];
+  const float* r1 = A + px.x * dp;
+  const float* r2 = A + px.y * dp;
+  c = Blk{__ldcg(r1 + py.x), __ldcg(r1 + py.y), __ldcg(r2 + py.x), __ldcg(r2 + py.y)};
+  return true;
+}
+
+// ... and store its rotated entries.  The block of the unordered pair is
+// formed from the lower index's rows: for x > y that is C^T, and the result
+// is written transposed.
+__device__ __forceinline__ void l2_store(float* A, int dp, const float2* cs, const int2* pr, int x, int y,
+                                         const Blk c) {
+  const float2 cx = cs[x], cy = cs[y];
+  const int2 px = pr[x], py = pr[y];
+  float* r1 = A + px.x * dp;
+  float* r2 = A + px.y * dp;
+  if (x == y) {
+    const Blk n = rot2(c, cx.x, cx.y, cx.x, cx.y);
+    __stcg(r1 + px.x, n.a11);
+    __stcg(r1 + px.y, n.a12);
+    __stcg(r2 + px.x, n.a12);
+    __stcg(r2 + px.y, n.a22);
+  } else {
+    const bool tr = x > y;
+    const Blk in = tr ? Blk{c.a11, c.a21, c.a12, c.a22} : c;
+    const float2 lo = tr ? cy : cx, hi = tr ? cx : cy;
+    const Blk n = rot2(in, lo.x, lo.y, hi.x, hi.y);
+    __stcg(r1 + py.x, n.a11);
+    __stcg(r1 + py.y, tr ? n.a21 : n.a12);
+    __stcg(r2 + py.x, tr ? n.a12 : n.a21);
+    __stcg(r2 + py.y, n.a22);
+  }
+}
+
+__device__ __forceinline__ void next_task(int& xg, int& yg, int dxg, int dyg, int ng) {
+  xg += dxg;
+  yg += dyg;
+  if (yg >= ng) {
+    yg -= ng;
+    ++xg;
+  }
+}
+
 // One sweep with A as a full symmetric dp x dp matrix in the L2-resident
 // slice, on a cluster of nc CTAs per matrix (nc = 1: a plain launch).  CTA c
 // of the cluster applies the blocks of the row pairs x in its share of
@@ -323,8 +373,11 @@ __global__ void __launch_bounds__(kEigThreads) k_eig_sweep_l2(const __grid_const
   const int x0 = static_cast<int>(rank) * np / static_cast<int>(nc);
   const int x1 = (static_cast<int>(rank) + 1) * np / static_cast<int>(nc);
   const int ng = (np + 31) >> 5;   // groups of 32 column pairs
-  const int ntask = ng * (x1 - x0);
+  const int nx = x1 - x0;
   const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
+  // task counters (row pair, column group), advanced by nwarp tasks at a time
+  const int xg0 = warp / ng, yg0 = warp - (warp / ng) * ng;
+  const int dxg = nwarp / ng, dyg = nwarp - (nwarp / ng) * ng;
   for (int rd = 0; rd < dp - 1; ++rd) {
     for (int q = tid; q < np; q += nth) {
       int pp, qq;
@@ -336,46 +389,36 @@ __global__ void __launch_bounds__(kEigThreads) k_eig_sweep_l2(const __grid_const
     }
     __syncthreads();
     cl_barrier(nc);
-    // task = (row pair x, 32 column pairs y); x is the same on every lane
-    for (int t = warp; t < ntask; t += nwarp) {
-      const int x = x0 + t / ng;
-      const int y = ((t - (t / ng) * ng) << 5) + lane;
-      if (y >= np) continue;
-      const float2 cx = cs[x], cy = cs[y];
-      if (cx.y == 0.0f && cy.y == 0.0f) continue;
-      const int2 px = pr[x], py = pr[y];
-      float* r1 = A + px.x * dp;
-      float* r2 = A + px.y * dp;
-      const float a11 = __ldcg(r1 + py.x), a12 = __ldcg(r1 + py.y);
-      const float a21 = __ldcg(r2 + py.x), a22 = __ldcg(r2 + py.y);
-      if (x == y) {
-        const Blk n = rot2(Blk{a11, a12, a21, a22}, cx.x, cx.y, cx.x, cx.y);
-        __stcg(r1 + px.x, n.a11);
-        __stcg(r1 + px.y, n.a12);
-        __stcg(r2 + px.x, n.a12);
-        __stcg(r2 + px.y, n.a22);
-      } else {
-        // the block of the unordered pair is formed from the lower index's
-        // rows: for x > y that is C^T, and the result is written transposed
-        const bool tr = x > y;
-        const Blk in = tr ? Blk{a11, a21, a12, a22} : Blk{a11, a12, a21, a22};
-        const float2 lo = tr ? cy : cx, hi = tr ? cx : cy;
-        const Blk n = rot2(in, lo.x, lo.y, hi.x, hi.y);
-        __stcg(r1 + py.x, n.a11);
-        __stcg(r1 + py.y, tr ? n.a21 : n.a12);
-        __stcg(r2 + py.x, tr ? n.a12 : n.a21);
-        __stcg(r2 + py.y, n.a22);
-      }
+    // task = (row pair x, 32 column pairs y); x is the same on every lane.
+    // Two tasks per iteration: both tasks' loads are in flight together.
+    int xg = xg0, yg = yg0;
+    while (xg < nx) {
+      int xg2 = xg, yg2 = yg;
+      next_task(xg2, yg2, dxg, dyg, ng);
+      const int xa = x0 + xg, ya = (yg << 5) + lane;
+      const int xb = x0 + xg2, yb = (yg2 << 5) + lane;
+      Blk ca, cb;
+      const bool acta = l2_load(A, dp, cs, pr, xa, ya, np, ca);
+      const bool actb = xg2 < nx && l2_load(A, dp, cs, pr, xb, yb, np, cb);
+      if (acta) l2_store(A, dp, cs, pr, xa, ya, ca);
+      if (actb) l2_store(A, dp, cs, pr, xb, yb, cb);
+      next_task(xg2, yg2, dxg, dyg, ng);
+      xg = xg2;
+      yg = yg2;
     }
     cl_barrier(nc);
   }
 }
 
 // V <- V J for the rotations logged by sweep `sweep`, on a band of
-// kApplyRows rows of V per CTA (V = I before sweep 0).
+// kApplyRows rows of V per CTA (V = I before sweep 0).  The band sits in
+// shared memory column by column (pitch kApplyPitch), so that a rotation
+// moves four rows per 16-byte access; rows past the band's end are zeros
+// and are rotated along without being stored.
 __global__ void __launch_bounds__(kApplyThreads) k_eig_apply(const __grid_constant__ EigPlan P, int sweep,
                                                             int bands0, int bands1) {
-  extern __shared__ float vs[];
+  extern __shared__ float4 vs4[];
+  float* vs = reinterpret_cast<float*>(vs4);
   if (eig_flagged(P.status)) return;
   const Where w = locate(P, bands0, bands1);
   const int k = w.side->k;
@@ -390,7 +433,7 @@ __global__ void __launch_bounds__(kApplyThreads) k_eig_apply(const __grid_consta
     const int r = e / dp, j = e - (e / dp) * dp;
     float v = 0.0f;
     if (r < rows && j < k) v = sweep == 0 ? (l0 + r == j ? 1.0f : 0.0f) : sl.V[static_cast<int64_t>(l0 + r) * k + j];
-    vs[e] = v;
+    vs[j * kApplyPitch + r] = v;
   }
   __syncthreads();
   if (ran) {
@@ -414,11 +457,15 @@ __global__ void __launch_bounds__(kApplyThreads) k_eig_apply(const __grid_consta
         if (i < nq && q < np && sn != 0.0f) {
           int pp, qq;
           round_pair(q, rd, dp, pp, qq);
-          for (int r = 0; r < rows; ++r) {
-            float* row = vs + r * dp;
-            const float vp = row[pp], vq = row[qq];
-            row[pp] = fmaf(c, vp, -(sn * vq));
-            row[qq] = fmaf(sn, vp, c * vq);
+          float4* cp = vs4 + pp * (kApplyPitch / 4);
+          float4* cq = vs4 + qq * (kApplyPitch / 4);
+#pragma unroll
+          for (int r4 = 0; r4 < kApplyRows / 4; ++r4) {
+            const float4 a = cp[r4], b = cq[r4];
+            cp[r4] = make_float4(fmaf(c, a.x, -(sn * b.x)), fmaf(c, a.y, -(sn * b.y)), fmaf(c, a.z, -(sn * b.z)),
+                                 fmaf(c, a.w, -(sn * b.w)));
+            cq[r4] = make_float4(fmaf(sn, a.x, c * b.x), fmaf(sn, a.y, c * b.y), fmaf(sn, a.z, c * b.z),
+                                 fmaf(sn, a.w, c * b.w));
           }
         }
       }
@@ -429,7 +476,7 @@ __global__ void __launch_bounds__(kApplyThreads) k_eig_apply(const __grid_consta
   }
   for (int e = tid; e < rows * k; e += nth) {
     const int r = e / k, j = e - (e / k) * k;
-    sl.V[static_cast<int64_t>(l0 + r) * k + j] = vs[r * dp + j];
+    sl.V[static_cast<int64_t>(l0 + r) * k + j] = vs[j * kApplyPitch + r];
   }
 }
 
@@ -494,7 +541,7 @@ cudaError_t eig_attributes() {
   if (e != cudaSuccess || attr_dev == dev) return e;
   const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
   e = cudaFuncSetAttribute(k_eig_sweep_packed, at, sweep_smem(kEigPackMaxK));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_eig_apply, at, kApplyRows * (kClMaxK + 1) * 4);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_eig_apply, at, kApplyPitch * kClMaxK * 4);
   if (e == cudaSuccess) attr_dev = dev;
   return e;
 }
@@ -577,7 +624,7 @@ cudaError_t launch_eig_rounds(const EigPlan& P, cudaStream_t st, int* launches) 
   const bool l2 = nc > 1 || any_large;
   EigPlan Q = P;
   Q.side[0].full = Q.side[1].full = l2 ? 1 : 0;
-  const int apply_smem = kApplyRows * dpmax * 4;
+  const int apply_smem = kApplyPitch * dpmax * 4;
   for (int s = 0; s < Q.max_sweeps; ++s) {
     if (l2) {
       cudaLaunchAttribute attr;
