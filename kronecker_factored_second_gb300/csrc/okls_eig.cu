@@ -561,36 +561,36 @@ cudaLaunchConfig_t l2_config(int nb, int nc, cudaStream_t st, cudaLaunchAttribut
   return cfg;
 }
 
-// CTAs per matrix for the L2 sweep: as many as keep every SM busy, up to a
-// cluster of 8, and no more than the device can co-schedule
+// CTAs per matrix for the L2 sweep: 8, 4 or 2 where every matrix's cluster
+// is resident at once (cluster sizes that leave part of the grid to a second
+// wave measured slower than one CTA per matrix), else 1
 int cluster_size(int nb) {
-  static int dev_cached = -1, sms = 0, max_ok = 1;
+  static int dev_cached = -1;
+  static int active[9] = {0};  // co-resident clusters of each size
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   if (dev != dev_cached) {
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 1;
-    max_ok = 1;
-    for (int nc = 8; nc > 1; --nc) {
+    for (int nc = 2; nc <= 8; nc *= 2) {
       cudaLaunchAttribute attr;
       cudaLaunchConfig_t cfg = l2_config(1, nc, nullptr, &attr);
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_eig_sweep_l2), &cfg) == cudaSuccess &&
-          n >= 1) {
-        max_ok = nc;
-        break;
-      }
+      if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_eig_sweep_l2), &cfg) != cudaSuccess)
+        n = 0;
+      active[nc] = n;
     }
     (void)cudaGetLastError();
     dev_cached = dev;
   }
-  int cap = max_ok;
+  int cap = 8;
   // OKLS_EIG_CTAS=c caps the CTAs per matrix (tests run the one-CTA kernels
   // on small batches with c = 1)
   if (const char* env = getenv("OKLS_EIG_CTAS")) {
     const int c = atoi(env);
     if (c >= 1) cap = std::min(cap, c);
   }
-  return std::max(1, std::min(cap, sms / std::max(nb, 1)));
+  for (int nc = 8; nc >= 2; nc /= 2)
+    if (nc <= cap && nb <= active[nc]) return nc;
+  return 1;
 }
 
 }  // namespace
@@ -618,17 +618,19 @@ cudaError_t launch_eig_rounds(const EigPlan& P, cudaStream_t st, int* launches) 
     bands[i] = (S.k + kApplyRows - 1) / kApplyRows;
     napply += S.count * bands[i];
   }
-  // one CTA per matrix with A in shared memory where that fits and the
-  // batch fills the GPU; else clusters over A in L2 (every side alike, so
-  // that one launch covers both)
-  const bool l2 = nc > 1 || any_large;
+  // one CTA per matrix with A in shared memory where that fits, unless
+  // clusters of 4 or more CTAs per matrix fit at once (measured: 1.4-1.6x
+  // faster at k = 256-320 with 4); clusters over A in L2 past 330 (every
+  // side alike, so that one launch covers both)
+  const bool l2 = nc >= 4 || any_large;
+  const int ncl = l2 ? nc : 1;
   EigPlan Q = P;
   Q.side[0].full = Q.side[1].full = l2 ? 1 : 0;
   const int apply_smem = kApplyPitch * dpmax * 4;
   for (int s = 0; s < Q.max_sweeps; ++s) {
     if (l2) {
       cudaLaunchAttribute attr;
-      const cudaLaunchConfig_t cfg = l2_config(nb, nc, st, &attr);
+      const cudaLaunchConfig_t cfg = l2_config(nb, ncl, st, &attr);
       e = cudaLaunchKernelEx(&cfg, k_eig_sweep_l2, Q, s);
       if (e != cudaSuccess) return e;
     } else {

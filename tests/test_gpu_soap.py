@@ -93,12 +93,14 @@ def test_teacher_forced_steps_large_path(B, m, n, dtype, monkeypatch):
     _teacher_forced(B, m, n, dtype)
 
 
-# the eigensolver's one-CTA-per-matrix kernels, which batches that fill the
-# GPU take: packed triangle in shared memory (d <= 330), full matrix in L2
-@pytest.mark.parametrize("B,m,n,dtype", [(2, 200, 150, torch.float32), (1, 160, 340, torch.float32)])
-def test_large_path_one_cta_per_matrix(B, m, n, dtype, monkeypatch):
+# the eigensolver with fewer CTAs per matrix, as larger batches take it: one
+# CTA (packed triangle in shared memory for d <= 330, full matrix in L2
+# past it) and clusters of 2 over the matrix in L2
+@pytest.mark.parametrize("B,m,n,dtype,ctas", [(2, 200, 150, torch.float32, 1), (1, 160, 340, torch.float32, 1),
+                                              (1, 160, 340, torch.float32, 2)])
+def test_large_path_fewer_ctas_per_matrix(B, m, n, dtype, ctas, monkeypatch):
     monkeypatch.setenv("OKLS_SOAP_LARGE", "1")
-    monkeypatch.setenv("OKLS_EIG_CTAS", "1")
+    monkeypatch.setenv("OKLS_EIG_CTAS", str(ctas))
     _teacher_forced(B, m, n, dtype)
 
 
