@@ -611,20 +611,18 @@ constexpr int kCRotateSmem = kRotateFloats * 4;
 constexpr int kCStepSmem = kStepFloats * 4;
 
 static cudaError_t clean_attributes() {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || attr_dev == dev) return e;
-  const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  e = cudaFuncSetAttribute(k_clean_refresh<float>, at, kCRefreshSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_refresh<__nv_bfloat16>, at, kCRefreshSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_rotate, at, kCRotateSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<float, float>, at, kCStepSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<float, __nv_bfloat16>, at, kCStepSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<__nv_bfloat16, float>, at, kCStepSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<__nv_bfloat16, __nv_bfloat16>, at, kCStepSmem);
-  if (e == cudaSuccess) attr_dev = dev;
-  return e;
+  static PerDevice pd;
+  return once_per_device(pd, [](int) {
+    const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(k_clean_refresh<float>, at, kCRefreshSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_refresh<__nv_bfloat16>, at, kCRefreshSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_rotate, at, kCRotateSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<float, float>, at, kCStepSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<float, __nv_bfloat16>, at, kCStepSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<__nv_bfloat16, float>, at, kCStepSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_clean_step<__nv_bfloat16, __nv_bfloat16>, at, kCStepSmem);
+    return e;
+  });
 }
 
 cudaError_t launch_clean_refresh(const CleanArgs& A, cudaStream_t st) {

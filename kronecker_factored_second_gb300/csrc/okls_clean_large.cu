@@ -794,17 +794,15 @@ void cl_chol(const ClLarge& L, int k, int d, int adaptive, cudaStream_t st) {
 }
 
 cudaError_t cl_attributes() {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || attr_dev == dev) return e;
-  const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  e = cudaFuncSetAttribute(k_cl_chol_inv, at, kLSmallSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_norm, at, kLSmallSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_svd, at, kLSmallSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_chol_inv_packed, at, packed_chol_smem(kPackMaxK));
-  if (e == cudaSuccess) attr_dev = dev;
-  return e;
+  static PerDevice pd;
+  return once_per_device(pd, [](int) {
+    const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(k_cl_chol_inv, at, kLSmallSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_norm, at, kLSmallSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_svd, at, kLSmallSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_cl_chol_inv_packed, at, packed_chol_smem(kPackMaxK));
+    return e;
+  });
 }
 
 // Thin QR of the batch of d x k panels in `cur`: four Cholesky-QR passes,

@@ -6,17 +6,18 @@
 // Eigenvectors(L, Q_L)) and by Clean's thin SVD of the sketch (Clean page,
 // Appendix A, Algorithm 3: the eigen-decomposition of Z^T Z).
 //
-// Per sweep, two launches (three when a plan mixes both storage variants):
-//   k_eig_sweep  one CTA per matrix.  The matrix A sits as a packed upper
-//                triangle in shared memory up to kEigPackMaxK, and as a full
-//                symmetric dp x dp matrix in an L2-resident scratch slice past
-//                it (every access of a round is then a contiguous run of a
-//                row).  The sweep's stopping rule is checked first; then each
-//                of the dp - 1 rounds of the round-robin ordering computes its
-//                dp / 2 disjoint rotations (threshold Jacobi: a pair whose
-//                off-diagonal entry is already below tol2 / k of its diagonal
-//                is left alone), writes them to the sweep's log and applies
-//                J^T A J as one pass over the 2 x 2 blocks of every two pairs.
+// Per sweep, two launches:
+//   sweep        the sweep's stopping rule, then the dp - 1 rounds of the
+//                round-robin ordering: each computes its dp / 2 disjoint
+//                rotations (threshold Jacobi: a pair whose off-diagonal entry
+//                is already below tol2 / k of its diagonal is left alone),
+//                writes them to the sweep's log and applies J^T A J as one
+//                pass over the 2 x 2 blocks of every two pairs.  Two kernels:
+//                k_eig_sweep_l2 keeps A as a full symmetric dp x dp matrix in
+//                an L2-resident workspace slice and runs each matrix on a
+//                thread-block cluster of 1, 2, 4 or 8 CTAs (every access of a
+//                round is a contiguous run of a row); k_eig_sweep_packed keeps
+//                A as a packed triangle in one CTA's shared memory (k <= 330).
 //   k_eig_apply  V <- V J for every logged rotation, on rows of V: rows are
 //                independent under right multiplication, so each CTA keeps a
 //                band of rows in shared memory and runs all rounds on it, and
@@ -535,15 +536,13 @@ int sweep_smem(int k) {
 }
 
 cudaError_t eig_attributes() {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || attr_dev == dev) return e;
-  const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  e = cudaFuncSetAttribute(k_eig_sweep_packed, at, sweep_smem(kEigPackMaxK));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_eig_apply, at, kApplyPitch * kClMaxK * 4);
-  if (e == cudaSuccess) attr_dev = dev;
-  return e;
+  static PerDevice pd;
+  return once_per_device(pd, [](int) {
+    const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(k_eig_sweep_packed, at, sweep_smem(kEigPackMaxK));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_eig_apply, at, kApplyPitch * kClMaxK * 4);
+    return e;
+  });
 }
 
 cudaLaunchConfig_t l2_config(int nb, int nc, cudaStream_t st, cudaLaunchAttribute* attr) {
@@ -565,22 +564,22 @@ cudaLaunchConfig_t l2_config(int nb, int nc, cudaStream_t st, cudaLaunchAttribut
 // is resident at once (cluster sizes that leave part of the grid to a second
 // wave measured slower than one CTA per matrix), else 1
 int cluster_size(int nb) {
-  static int dev_cached = -1;
-  static int active[9] = {0};  // co-resident clusters of each size
+  static PerDevice pd;
+  static int active[64][9];  // per device: co-resident clusters of each size
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (dev != dev_cached) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 1;
+  once_per_device(pd, [](int d) {
     for (int nc = 2; nc <= 8; nc *= 2) {
       cudaLaunchAttribute attr;
       cudaLaunchConfig_t cfg = l2_config(1, nc, nullptr, &attr);
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_eig_sweep_l2), &cfg) != cudaSuccess)
         n = 0;
-      active[nc] = n;
+      active[d][nc] = n;
     }
     (void)cudaGetLastError();
-    dev_cached = dev;
-  }
+    return cudaSuccess;
+  });
   int cap = 8;
   // OKLS_EIG_CTAS=c caps the CTAs per matrix (tests run the one-CTA kernels
   // on small batches with c = 1)
@@ -589,7 +588,7 @@ int cluster_size(int nb) {
     if (c >= 1) cap = std::min(cap, c);
   }
   for (int nc = 8; nc >= 2; nc /= 2)
-    if (nc <= cap && nb <= active[nc]) return nc;
+    if (nc <= cap && nb <= active[dev][nc]) return nc;
   return 1;
 }
 

@@ -215,12 +215,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(okls_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice pd;
+  const cudaError_t e = once_per_device(pd, [](int) {
+    return cudaFuncSetAttribute(okls_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  });
+  if (e != cudaSuccess) return e;
   if (L.total_tiles <= 0) return cudaSuccess;
   const int grid = static_cast<int>(L.total_tiles < num_sms ? L.total_tiles : num_sms);
   okls_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(L);

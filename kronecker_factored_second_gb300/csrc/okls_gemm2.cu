@@ -221,15 +221,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 }
 
 cudaError_t launch_gemm_pair(const GemmLaunch& L, int num_sms, cudaStream_t stream) {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static PerDevice pd;
+  const cudaError_t e = once_per_device(pd, [](int) {
+    return cudaFuncSetAttribute(okls_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  });
   if (e != cudaSuccess) return e;
-  if (attr_dev != dev) {
-    e = cudaFuncSetAttribute(okls_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
   if (L.total_tiles <= 0) return cudaSuccess;
   const int64_t pairs = L.total_tiles < num_sms / 2 ? L.total_tiles : num_sms / 2;
   okls_gemm_pair_kernel<<<static_cast<int>(2 * pairs), kGemmThreads, kPairSmem, stream>>>(L);

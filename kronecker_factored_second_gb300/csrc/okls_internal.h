@@ -5,7 +5,30 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace okls {
+
+// Host-side set-up that must run once per device for one call site (the
+// kernels' shared-memory opt-ins, occupancy queries): `set(device)` runs for
+// the caller's current device unless it already succeeded there.  Safe to
+// call from several host threads; devices past 63 are set up on every call.
+struct PerDevice {
+  std::mutex mu;
+  uint64_t done = 0;  // bit d: device d is set up
+};
+template <class F>
+inline cudaError_t once_per_device(PerDevice& pd, F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  std::lock_guard<std::mutex> lock(pd.mu);
+  if (pd.done & bit) return cudaSuccess;
+  e = set(dev);
+  if (e == cudaSuccess) pd.done |= bit;
+  return e;
+}
 
 // ----------------------------------------------------------------- tiling
 constexpr int kBM = 128;        // output rows per tile (UMMA M, one TMEM lane each)

@@ -322,15 +322,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) okls_ns_small_kernel(const _
 }
 
 cudaError_t launch_ns_small(const SmallNsArgs& A, cudaStream_t st) {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static PerDevice pd;
+  const cudaError_t e = once_per_device(pd, [](int) {
+    return cudaFuncSetAttribute(okls_ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallSmem);
+  });
   if (e != cudaSuccess) return e;
-  if (attr_dev != dev) {
-    e = cudaFuncSetAttribute(okls_ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallSmem);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
   const int blocks = A.f[0].count + (A.nf > 1 ? A.f[1].count : 0);
   if (blocks <= 0) return cudaSuccess;
   okls_ns_small_kernel<<<blocks, kSmallThreads, kSmallSmem, st>>>(A);

@@ -363,24 +363,16 @@ cudaError_t launch_soap_reset(float* M, float* V, float* L, float* R, float* QL,
 
 // opt in to the large dynamic shared memory of both kernels, once per device
 static cudaError_t soap_attributes() {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || attr_dev == dev) return e;
-  e = cudaFuncSetAttribute(k_soap_step<float, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSoapStepSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_soap_step<float, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSoapStepSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_soap_step<__nv_bfloat16, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSoapStepSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_soap_step<__nv_bfloat16, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSoapStepSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_soap_refresh, cudaFuncAttributeMaxDynamicSharedMemorySize, kSoapRefreshSmem);
-  if (e == cudaSuccess) attr_dev = dev;
-  return e;
+  static PerDevice pd;
+  return once_per_device(pd, [](int) {
+    const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(k_soap_step<float, float>, at, kSoapStepSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_soap_step<float, __nv_bfloat16>, at, kSoapStepSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_soap_step<__nv_bfloat16, float>, at, kSoapStepSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_soap_step<__nv_bfloat16, __nv_bfloat16>, at, kSoapStepSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_soap_refresh, at, kSoapRefreshSmem);
+    return e;
+  });
 }
 
 cudaError_t launch_soap_step(const SoapArgs& A, cudaStream_t st) {
