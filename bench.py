@@ -33,6 +33,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "preconditioned matrices/s per okls_step (TFLOP/s vs GB300 FP16 peak alongside)"
+L2_BYTES = 129e6  # GB300 L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -574,30 +575,39 @@ def run_okls(args):
         cpu = oracle_sample(args.cpu_seconds)
 
     if rank == 0:
+        # SOAP's products run on CUDA-core GEMMs that the per-launch events do
+        # not time: no roofline object for that mode
+        roofline = None if args.method == "soap" else {
+            "bound": "tensor", "kernel": "okls_gemm_kernel (tcgen05, all products of the step)",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": (achieved / peak) if achieved else None, "traffic": gemm_traffic(),
+            "traffic_unit": "bytes per launch (dram read + write, ncu, full-size step)",
+            "peak_kind": f"{peak_kind} bf16 sustained (fp16 nominal ratio 1)",
+            "launches": prof["gemm_launches"], "ms_per_launch": prof["gemm_ms"] / max(1, prof["gemm_launches"]),
+            "ns_chain_tflops": ns_achieved,
+            "ns_chain_frac": (ns_achieved / peak) if ns_achieved else None}
         line = {
             "metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "fp32" if args.method == "soap" else "fp16", "data": "synthetic",
             "config": {
                 "workload": (f"{args.workload}: " + ", ".join(f"{g.batch} x {g.m}x{g.n} {g.name}" for g in wl.groups)
                              + f" = {matrices} matrices, {wl.groups[0].dtype} W and G, fp32 state, "
                              f"{wl.recipe} gradients (condition number {wl.cond:g})"),
                 "method": args.method,
-                "precision": f"binary16 Newton-Schulz operands, fp32 accumulation, split_iters={args.split}, "
-                             f"ridge={args.ridge:g}",
-                "l2": f"inputs larger than L2: {in_bytes / 1e9:.2f} GB of gradients and "
-                      f"{state_bytes / 1e9:.1f} GB of state per step",
+                "precision": ("fp32 throughout (batched CUDA-core GEMMs, Jacobi eigenbasis refresh every 10 "
+                              "steps)" if args.method == "soap" else
+                              f"binary16 Newton-Schulz operands, fp32 accumulation, split_iters={args.split}, "
+                              f"ridge={args.ridge:g}"),
+                "l2": (f"inputs larger than L2: {in_bytes / 1e9:.2f} GB of gradients and "
+                       f"{state_bytes / 1e9:.1f} GB of state per step"
+                       if in_bytes + state_bytes > L2_BYTES else
+                       f"inputs and state fit in L2 ({(in_bytes + state_bytes) / 1e6:.0f} MB); L2 not flushed "
+                       f"between steps"),
                 "parallelism": f"owner-computes replicas x{ws} (each rank a full layer set)"},
             "tflops": tflops,
             "tflops_frac_of_peak": tflops / peak,
-            "roofline": {"bound": "tensor", "kernel": "okls_gemm_kernel (tcgen05, all products of the step)",
-                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": (achieved / peak) if achieved else None, "traffic": gemm_traffic(),
-                         "traffic_unit": "bytes per launch (dram read + write, ncu, full-size step)",
-                         "peak_kind": f"{peak_kind} bf16 sustained (fp16 nominal ratio 1)",
-                         "launches": prof["gemm_launches"], "ms_per_launch": prof["gemm_ms"] / max(1, prof["gemm_launches"]),
-                         "ns_chain_tflops": ns_achieved,
-                         "ns_chain_frac": (ns_achieved / peak) if ns_achieved else None},
+            "roofline": roofline,
             "elementwise": elementwise,
             "cpu_baseline": cpu,
             "e2e": e2e,
