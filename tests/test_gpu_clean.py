@@ -1,5 +1,6 @@
-"""GPU parity of the Clean mode (okls_config.method = CLEAN, m, n <= 128,
-rank + oversample <= 64) against the float64 oracle, through the C ABI.
+"""GPU parity of the Clean mode (okls_config.method = CLEAN; one CTA per
+factor for m, n <= 128 and rank + oversample <= 64, batched GEMMs up to
+16384 and 544) against the float64 oracle, through the C ABI.
 
 Teacher-forced: every step starts the oracle from the GPU's own state.
 A refresh step is checked in two parts:
