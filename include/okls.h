@@ -143,8 +143,13 @@ typedef enum okls_state_part {
  *                   This build runs SOAP for m, n <= 544 (fp32 throughout,
  *                   cyclic Jacobi eigensolver warm-started from the previous
  *                   basis; one CTA per matrix up to 128 x 128, batched fp32
- *                   GEMMs past that); larger shapes return
- *                   OKLS_ERR_UNSUPPORTED.
+ *                   GEMMs past that).  On the batched path the workspace
+ *                   holds, per matrix, three m x n and one max(mn, m^2, n^2)
+ *                   fp32 buffers, four fp32 buffers of m^2 + n^2, and for
+ *                   each side d > 128 an eigensolver slice of about 3 d^2
+ *                   floats.  OKLS_SOAP_LARGE=1 selects that path for every
+ *                   shape, and OKLS_EIG_CTAS=c caps the eigensolver's CTAs
+ *                   per matrix.  Larger shapes return OKLS_ERR_UNSUPPORTED.
  *                   OKLS_METHOD_CLEAN (Clean page, Algorithm 1 with the
  *                   sketch of Eqn. (8) and Appendix A, Algorithm 3): at
  *                   steps t = 1, 1+T, 1+2T, ... (T = root_every) U_L,
