@@ -141,6 +141,29 @@ def test_soap_shapes_and_state(lib):
     assert w2 >= 4 * 3 * (3 * 300 * 64 + 4 * 300 * 300 + 300 * 300)
 
 
+def test_soap_batched_path_workspace(lib):
+    """The SOAP batched path's workspace is what the header documents: per
+    matrix three m x n and one max(mn, m^2, n^2) fp32 buffers, four of
+    m^2 + n^2, and for each side d > 128 an eigensolver slice of A (full,
+    dp x dp with dp = d rounded up to even), V (d x d) and one sweep's
+    rotation log ((dp - 1) x dp floats).  The fixed part (descriptor table,
+    scalars, status word, alignment) stays under 1 MiB."""
+    def r4(x):
+        return (x + 3) // 4 * 4
+
+    def eig(d):
+        dp = d + (d & 1)
+        return r4(dp * dp) + r4(d * d) + r4((dp - 1) * dp) + 4
+
+    for B, m, n in [(2, 544, 331), (3, 300, 100), (1, 129, 544)]:
+        c = L.config_default(B, m, n)
+        c.method = L.METHOD_SOAP
+        _s, w = L.state_bytes(c)
+        floats = B * (3 * m * n + max(m * n, m * m, n * n) + 4 * (m * m + n * n))
+        floats += sum(B * eig(d) for d in (m, n) if d > 128)
+        assert 4 * floats <= w <= 4 * floats + (1 << 20), (B, m, n, w, 4 * floats)
+
+
 def test_clean_shapes_and_validation(lib):
     """Clean keeps rank-r bases, their eigenvalues and the four blocks'
     moments (linear in m and n); this build takes m, n <= 16384 and
