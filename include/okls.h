@@ -376,28 +376,34 @@ okls_status okls_inv_root(const float *S_dev, float *P_dev, float *root_dev,
 /*
  * okls_inv_root without any device allocation.  The paper has no counterpart:
  * this entry point exists for callers that cannot allocate device memory
- * when they need a root — code running while a CUDA graph is being captured,
- * allocators that must not re-enter themselves, embedders whose device pool
- * is fixed at start-up.  It computes the same S^(-1/2) as okls_inv_root
- * (plain or split binary16 chain, same schedule, lo and ridge) but takes its
- * scratch from one static device array inside the library instead of a
- * workspace argument.
+ * when they need a root — allocators that must not re-enter themselves (a
+ * root computed from inside an allocation callback), embedders whose device
+ * pool is fixed at start-up and must not grow.  It computes the same
+ * S^(-1/2) as okls_inv_root (plain or split binary16 chain, same schedule,
+ * lo and ridge) but takes its scratch from one static device array inside
+ * the library instead of a workspace argument.
  *   S_dev, P_dev  as okls_inv_root (count x d x d fp32, caller-owned).
  *   Capacity      okls_inv_root_noalloc_capacity() bytes (32 MiB), held on
  *                 every GPU that loads the library until the process exits;
  *                 a request whose okls_inv_root_workspace_bytes exceeds it is
- *                 rejected with OKLS_ERR_UNSUPPORTED (e.g. d = 1024 fits one
- *                 matrix, d = 512 fits five).
+ *                 rejected with OKLS_ERR_UNSUPPORTED.  With 10 iterations:
+ *                 plain chain d = 1024 up to 2 matrices, d = 512 up to 10,
+ *                 d = 256 up to 42; split chain d = 1024 one matrix,
+ *                 d = 512 up to 5, d = 256 up to 21; d = 2048 never fits.
  *   First call    on each device looks up the array's device address
- *                 (cudaGetSymbolAddress); make that first call before any
- *                 stream capture.
+ *                 (cudaGetSymbolAddress).
+ *   Capture       not usable while `stream` is being captured into a CUDA
+ *                 graph: like okls_inv_root it uploads a host-side
+ *                 descriptor table and synchronises `stream` to read the
+ *                 device status word, and both break a capture.
  *   Sharing       every call on a device uses the same array, which keeps the
  *                 previous call's contents (the call clears what must start
  *                 at zero).  Calls whose work overlaps on the GPU — two
  *                 streams, two host threads — race on the array; serialise
  *                 them.
  * No cudaMalloc, cudaFree or other allocating routine is called.  The call
- * synchronises `stream` before returning, like okls_inv_root.
+ * synchronises `stream` before returning, on success and on every error, so
+ * no work of it is left queued on the shared array.
  */
 size_t okls_inv_root_noalloc_capacity(void);
 okls_status okls_inv_root_noalloc(const float *S_dev, float *P_dev, int64_t d,

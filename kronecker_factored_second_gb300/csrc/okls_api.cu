@@ -1864,12 +1864,12 @@ okls_status okls_inv_root(const float* S, float* P, float* root, uint16_t* trace
 
 // ===================================================== no-allocation variant
 // Some callers cannot allocate device memory at the moment they need an
-// inverse root: code running while a CUDA graph is being captured (a
-// cudaMalloc there breaks the capture), allocators that must not re-enter
-// themselves, and embedders whose memory pool is fixed at start-up.  For them
-// okls_inv_root_noalloc takes its scratch from this file-scope array instead
-// of a caller-provided workspace.  Every GPU that loads the library holds it
-// (32 MiB) until the process exits.
+// inverse root: allocators that must not re-enter themselves and embedders
+// whose memory pool is fixed at start-up.  For them okls_inv_root_noalloc
+// takes its scratch from this file-scope array instead of a caller-provided
+// workspace.  Every GPU that loads the library holds it (32 MiB) until the
+// process exits.  The call is not usable under stream capture: it uploads a
+// host-side descriptor table and synchronises the stream.
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
@@ -1917,8 +1917,14 @@ okls_status okls_inv_root_noalloc(const float* S, float* P, int64_t d, int64_t c
   if ((s = noalloc_scratch(&scratch)) != OKLS_OK) return s;
   // the shared scratch keeps the previous call's contents; okls_inv_root
   // clears the scalar sums and the status word it relies on
-  return okls_inv_root(S, P, nullptr, nullptr, d, count, iters, split_iters, lo, ridge, scratch,
-                       kNoAllocScratchBytes, stream);
+  s = okls_inv_root(S, P, nullptr, nullptr, d, count, iters, split_iters, lo, ridge, scratch, kNoAllocScratchBytes,
+                    stream);
+  // some error paths of okls_inv_root return before its final
+  // synchronisation: drain the stream so that no work of this call is still
+  // queued on the shared array when the next call starts (the error message
+  // of the failed call is kept)
+  if (s != OKLS_OK) (void)cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  return s;
 }
 
 }  // extern "C"
