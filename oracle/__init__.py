@@ -20,7 +20,9 @@ Parity status per function (the pins live in ``tests/test_oracle_pins.py``):
 * ``factor_ema``                           pinned (hand example L = G G^T,
   brute-force loops).
 * ``okls_step`` / ``okls_run``             pinned (square fixed-gradient polar
-  limit, descent sign, closed-form weight decay).
+  limit, descent sign, closed-form weight decay, the Nesterov combination
+  kappa_t (1 - b1^(t+1)) G of a constant gradient recovered through the
+  step's roots).
 * ``shampoo_step``                         pinned (the page's 2x3 gradient fed 1,
   4 and 100 times: step singular values 1 / 0.5 / 0.1; scale invariance of
   Problem 14; brute-force factor sums).
@@ -39,8 +41,9 @@ Parity status per function (the pins live in ``tests/test_oracle_pins.py``):
 * ``variance_correction``                  pinned by Monte Carlo against its
   definition (variance of the Nesterov combination for iid unit gradients);
   the *choice* of this reading is not printed on the pages.
-* AdamC correction factor lr/lr_peak       parity unpinned (closed-form scalar,
-  only the reading is documented; the G = 0 decay test fixes its arithmetic).
+* AdamC correction factor lr/lr_peak       parity unpinned by the pages (a
+  closed-form scalar whose reading the pages name without a formula; the
+  G = 0 decay test fixes its arithmetic, not the reading).
 """
 
 from .okls_oracle import *  # noqa: F401,F403

@@ -12,8 +12,7 @@ Sources (page title, then section / equation):
 * "Shampoo" chapter of the optim-book (section "2 x 3 gradient by hand" and
   Problem 14): worked numbers used as pins.
 
-Readings of points the pages leave open (each is listed, with its reason, in
-the design notes of the repository):
+Readings of points the pages leave open:
 
 r1  P_0 = I at the first step (the EMAs use the previous roots).
 r2  eps is added to both factors at initialisation (S_0 = eps*I) and at every

@@ -282,6 +282,37 @@ def test_variance_correction_monte_carlo():
     assert O.variance_correction(0.0, 5) == 1.0
 
 
+def test_nesterov_combination_for_a_constant_gradient():
+    """README bullet "Nesterov momentum with variance correction": for a
+    constant gradient G and M_0 = 0 the momentum is M_t = (1 - b1^t) G, and
+    the Nesterov combination N_t = kappa_t (b1 M_t + (1 - b1) G) sums to the
+    closed form kappa_t (1 - b1^(t+1)) G.  N is recovered from the change of
+    W through the step's own roots (U = P_a N P_b), so a combination built
+    from M_{t-1} (giving 1 - b1^t), a missing or misplaced kappa, or a wrong
+    sign of the update fails here."""
+    rng = np.random.default_rng(21)
+    m, n = 6, 4
+    G = rng.standard_normal((m, n))
+    hp = O.Hyper()
+    st = O.init_state(m, n, hp)
+    W = rng.standard_normal((m, n))
+    b1 = hp.beta1
+    decay = O.adamc_decay(hp.lr, hp.peak, hp.weight_decay)
+    c = O.c_shape(m, n)
+    for t in range(1, 6):
+        W_prev = W
+        st, W, U = O.okls_step(st, W, G, hp.lr, hp)
+        assert np.allclose(st.M, (1 - b1 ** t) * G, rtol=1e-13, atol=1e-15)
+        U_w = ((1 - decay) * W_prev - W) / (hp.lr * c)
+        N = np.linalg.solve(st.Pa, np.linalg.solve(st.Pb.T, U_w.T).T)
+        # kappa_t from its definition (variance of the unrolled combination
+        # for iid unit gradients), summed here term by term
+        v = (1 - b1) ** 2 * (1 + b1) ** 2 + sum((1 - b1) ** 2 * b1 ** (2 * k) for k in range(2, t + 1))
+        want = (1 - b1 ** (t + 1)) / math.sqrt(v) * G
+        assert O.rel_fro(N, want) < 1e-9, t
+        assert O.rel_fro(U_w, U) < 1e-9
+
+
 def test_hyperparameter_defaults_are_the_readme_table():
     hp = O.Hyper()
     assert (hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay) == \
