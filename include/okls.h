@@ -303,6 +303,26 @@ okls_status okls_set_state(okls_handle h, int32_t part, const void *src_dev,
 okls_status okls_get_step(okls_handle h, int64_t *t);
 okls_status okls_set_step(okls_handle h, int64_t t);
 
+/*
+ * Limit of the bounded waits inside the step's tcgen05 GEMM launches, and a
+ * test hook for the failure path.  The pages have no counterpart (they
+ * describe no failure handling); it serves the OKLS_DEV_TIMEOUT contract of
+ * the status word above.
+ *   cycles         SM clock cycles a pipeline wait may spin before it raises
+ *                  OKLS_DEV_TIMEOUT (0: the default, ~4e9 cycles, ~2 s).
+ *   unloaded_tile  -1: none.  >= 0: in every GEMM launch of the following
+ *                  steps the producer stops before that linear output tile,
+ *                  so its consumers' waits run out with none of that CTA's
+ *                  copies or MMAs in flight: the launch raises
+ *                  OKLS_DEV_TIMEOUT, every later launch of the step returns
+ *                  at once, and okls_query_status reports OKLS_ERR_TIMEOUT.
+ *                  W, S and P keep their previous values (the momentum M has
+ *                  already advanced when the first GEMM launch fails).
+ * Applies to the steps launched after the call, until the next call.
+ */
+okls_status okls_set_wait_limit(okls_handle h, int64_t cycles,
+                                int64_t unloaded_tile);
+
 /* Release the handle (its descriptor table lives in the caller's workspace,
  * so nothing on the device is freed).  The caller must not free state or
  * workspace while work of this handle is still queued.  NULL is accepted. */

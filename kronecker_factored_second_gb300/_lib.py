@@ -114,6 +114,7 @@ _SIGS = {
     "okls_set_step": (_I32, [_P, _I64]),
     "okls_destroy": (_I32, [_P]),
     "okls_profile_enable": (_I32, [_P, _I32]),
+    "okls_set_wait_limit": (_I32, [_P, _I64, _I64]),
     "okls_profile_read": (_I32, [_P, ctypes.POINTER(okls_profile)]),
     "okls_ns_schedule": (_I32, [_I32, ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                                 ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I32)]),

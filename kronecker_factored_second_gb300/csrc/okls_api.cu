@@ -115,41 +115,22 @@ constexpr size_t kMapTableBytes = kMaxMaps * sizeof(CUtensorMap);
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-// Output tiles are tile_rows x 256: 128 rows for one CTA (default), 256 for
-// a CTA pair (okls_gemm2.cu, enabled with OKLS_GEMM_PAIR=1 for launches with a
-// problem taller than 128 rows).  On the power-capped GB300 the pair kernel
-// does ~10% more work per clock but runs ~10% lower clocks; end to end the
-// one-CTA kernel measured 2% faster on the 1.2B-shaped set.
-bool pair_enabled() {
-  static const bool on = [] {
-    const char* e = getenv("OKLS_GEMM_PAIR");
-    return e && e[0] == '1';
-  }();
-  return on;
-}
-
-bool use_pair(int64_t max_rows) { return pair_enabled() && max_rows > kBM; }
-
-// tiles of a symmetric (upper-triangle) d x d product: row block tm holds
-// column blocks floor(tm * tile_rows / 256) .. tiles_n-1
-int64_t sym_tiles(int64_t d, int tile_rows) {
-  const int64_t tm_n = (d + tile_rows - 1) / tile_rows, tn_n = (d + kBN - 1) / kBN;
-  const int div = kBN / tile_rows;
+// tiles (128 x 256) of a symmetric (upper-triangle) d x d product: row
+// block tm holds column blocks floor(tm / 2) .. tiles_n-1
+int64_t sym_tiles(int64_t d) {
+  const int64_t tm_n = (d + kBM - 1) / kBM, tn_n = (d + kBN - 1) / kBN;
+  constexpr int div = kBN / kBM;
   int64_t c = 0;
   for (int64_t tm = 0; tm < tm_n; ++tm) c += tn_n - tm / div;
   return c;
 }
 
 // partial sums of S^2 one symmetric product writes: 4 epilogue warps per tile
-// (one CTA) or 8 (a pair)
-int64_t syrk_parts(int64_t d, bool pair) { return pair ? 8 * sym_tiles(d, 256) : 4 * sym_tiles(d, kBM); }
+int64_t syrk_parts(int64_t d) { return 4 * sym_tiles(d); }
 
-// fixed partial slots per matrix for ||S||_F^2 (either tiling, or the
+// fixed partial slots per matrix for ||S||_F^2 (the product's tiles, or the
 // blocks of the standalone reduction)
-int64_t factor_parts(int64_t d) {
-  int64_t a = syrk_parts(d, false), b = syrk_parts(d, true), c = sumsq_parts(d * d);
-  return std::max(a, std::max(b, c));
-}
+int64_t factor_parts(int64_t d) { return std::max(syrk_parts(d), static_cast<int64_t>(sumsq_parts(d * d))); }
 
 // A batch of binary16 matrices (rows x cols, row pitch ld) with two TMA
 // descriptors: box 128 rows (A operand) and box 256 rows (B operand).
@@ -345,6 +326,20 @@ struct BoxScope {
   ~BoxScope() { g_boxes = nullptr; }
 };
 
+// Wait limit of the GEMM launches of the current call (0: the kernels'
+// default) and the test hook that leaves one tile's operands unloaded
+// (okls_set_wait_limit).
+struct WaitSetting {
+  int64_t cycles = 0;
+  int64_t unloaded_tile = -1;
+};
+thread_local WaitSetting g_wait;
+
+struct WaitScope {
+  explicit WaitScope(const WaitSetting& w) { g_wait = w; }
+  ~WaitScope() { g_wait = WaitSetting(); }
+};
+
 // ------------------------------------------------------------ GEMM launches
 // Output buffers must cover the problem's rows x cols (and cols x rows for the
 // transposed copy, which shares the pitch); a violation is a planning bug.
@@ -362,18 +357,14 @@ struct LaunchBuilder {
     memset(&p, 0, sizeof(p));
     p.bmn = bmn ? 1 : 0;
     auto bm = [&](const Buf& x) { return bmn ? x.mapMN : x.mapB; };
-    auto bp = [&](const Buf& x) { return bmn ? x.mapMN : x.mapA; };
     p.nseg = split ? 3 : 1;
     p.amap[0] = A[0].mapA;
     p.bmap[0] = bm(B[0]);
-    p.bmap_pair[0] = bp(B[0]);
     if (split) {
       p.amap[1] = A[0].mapA;
       p.bmap[1] = bm(B[1]);
-      p.bmap_pair[1] = bp(B[1]);
       p.amap[2] = A[1].mapA;
       p.bmap[2] = bm(B[0]);
-      p.bmap_pair[2] = bp(B[0]);
     }
     p.rows = rows;
     p.cols = cols;
@@ -392,7 +383,6 @@ struct LaunchBuilder {
       p.nseg = 2;
       p.amap[1] = A.mapA;
       p.bmap[1] = bmn ? B[1].mapMN : B[1].mapB;
-      p.bmap_pair[1] = bmn ? B[1].mapMN : B[1].mapA;
     }
     return p;
   }
@@ -405,7 +395,6 @@ struct LaunchBuilder {
       p.nseg = 2;
       p.amap[1] = A[1].mapA;
       p.bmap[1] = p.bmap[0];
-      p.bmap_pair[1] = p.bmap_pair[0];
     }
     return p;
   }
@@ -426,30 +415,24 @@ struct LaunchBuilder {
     std::stable_sort(L.prob, L.prob + L.nprob, [](const GemmProblem& x, const GemmProblem& y) {
       return static_cast<int64_t>(x.K) * x.nseg > static_cast<int64_t>(y.K) * y.nseg;
     });
-    int64_t max_rows = 0;
-    for (int i = 0; i < L.nprob; ++i) max_rows = std::max<int64_t>(max_rows, L.prob[i].rows);
-    const bool pair = use_pair(max_rows);
     // every TMA box must match the ring slot it lands in
     if (g_boxes) {
       const int nb = static_cast<int>(g_boxes->size());
       auto box = [&](int idx) { return (idx >= 0 && idx < nb) ? (*g_boxes)[idx] : -1; };
       for (int i = 0; i < L.nprob; ++i)
         for (int sg = 0; sg < L.prob[i].nseg; ++sg)
-          if (box(L.prob[i].amap[sg]) != kBM ||
-              box(L.prob[i].bmap[sg]) != (L.prob[i].bmn ? kMNBox : kBN) ||
-              box(L.prob[i].bmap_pair[sg]) != (L.prob[i].bmn ? kMNBox : kBM))
+          if (box(L.prob[i].amap[sg]) != kBM || box(L.prob[i].bmap[sg]) != (L.prob[i].bmn ? kMNBox : kBN))
             return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: descriptor box sizes");
     } else {
       return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: descriptor table not bound");
     }
-    const int tile_rows = pair ? 256 : kBM;
     int64_t t = 0;
     for (int i = 0; i < L.nprob; ++i) {
       GemmProblem& p = L.prob[i];
-      p.tiles_m = (p.rows + tile_rows - 1) / tile_rows;
+      p.tiles_m = (p.rows + kBM - 1) / kBM;
       p.tiles_n = (p.cols + kBN - 1) / kBN;
-      p.tiles_per_mat = p.sym ? sym_tiles(p.rows, tile_rows) : static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-      if (p.epi == EPI_SYRK && (p.part == nullptr || p.part_ld < syrk_parts(p.rows, pair)))
+      p.tiles_per_mat = p.sym ? sym_tiles(p.rows) : static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+      if (p.epi == EPI_SYRK && (p.part == nullptr || p.part_ld < syrk_parts(p.rows)))
         return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: partial-sum slots");
       p.tile_begin = t;
       t += p.tiles_per_mat * p.batch;
@@ -461,6 +444,8 @@ struct LaunchBuilder {
     L.total_tiles = t;
     L.maps = maps;
     L.status = status;
+    L.wait_cycles = g_wait.cycles;
+    L.unloaded_tile = g_wait.unloaded_tile;
     Prof* pf = g_prof;
     double flops = 0.0;
     for (int i = 0; i < L.nprob; ++i) {
@@ -475,7 +460,7 @@ struct LaunchBuilder {
       eb = pf->next_event();
       if (ea) OKLS_CK(cudaEventRecord(ea, st));
     }
-    OKLS_CK(pair ? launch_gemm_pair(L, sms, st) : launch_gemm(L, sms, st));
+    OKLS_CK(launch_gemm(L, sms, st));
     if (pf) {
       if (ea && eb) {
         OKLS_CK(cudaEventRecord(eb, st));
@@ -809,6 +794,7 @@ struct okls_handle_s {
   int64_t part_g_ld = 0, part_a_ld = 0, part_b_ld = 0;
   int64_t t = 0;
   Prof prof;
+  WaitSetting wait;  // okls_set_wait_limit
 };
 
 namespace {
@@ -1443,6 +1429,7 @@ okls_status step_impl(okls_handle h, void* W, const void* G, float lr, const flo
   okls_status s;
   ProfScope scope(&h->prof);
   BoxScope boxes(&h->boxes);
+  WaitScope waits(h->wait);
 
   // 1-2. momentum, statistics, packed binary16 operands
   OKLS_CK(cudaMemsetAsync(h->scal, 0, static_cast<size_t>(4 * B * 4), st));  // SC_SUMSQ_* slots
@@ -1519,11 +1506,9 @@ okls_status step_impl(okls_handle h, void* W, const void* G, float lr, const flo
   // new roots are committed only after the chain has run.
   const int64_t every = c.root_every > 1 ? c.root_every : 1;
   const bool fresh = ((t1 - 1) % every) == 0;
-  // the factor products ran as one launch: pair tiles iff either factor is taller than 128
-  const bool syrk_pair = use_pair(std::max(m, n));
   if (fresh) {
     OKLS_CK(launch_coeffs_post(B, c.ridge, zK, zK1, h->scal, sld, kPostRoots, h->status, h->part_a, h->part_a_ld,
-                               syrk_parts(m, syrk_pair), h->part_b, h->part_b_ld, syrk_parts(n, syrk_pair), st));
+                               syrk_parts(m), h->part_b, h->part_b_ld, syrk_parts(n), st));
     note_kernels(1);
     if (shampoo) {
       // L^-1/4 = (L^1/2)^-1/2: the first chain (ridge on L) forms only the
@@ -1719,6 +1704,14 @@ okls_status okls_set_step(okls_handle h, int64_t t) {
 
 okls_status okls_destroy(okls_handle h) {
   delete h;
+  return OKLS_OK;
+}
+
+okls_status okls_set_wait_limit(okls_handle h, int64_t cycles, int64_t unloaded_tile) {
+  if (!h) return fail(OKLS_ERR_INVALID_ARG, "handle is NULL");
+  if (cycles < 0 || unloaded_tile < -1) return fail(OKLS_ERR_INVALID_ARG, "cycles >= 0, unloaded_tile >= -1");
+  h->wait.cycles = cycles;
+  h->wait.unloaded_tile = unloaded_tile;
   return OKLS_OK;
 }
 

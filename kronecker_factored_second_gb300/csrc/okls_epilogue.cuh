@@ -1,5 +1,4 @@
-// Tile decoding and the fused OKLS epilogues shared by the one-CTA and the
-// CTA-pair tcgen05 GEMM kernels.
+// Tile decoding and the fused OKLS epilogues of the tcgen05 GEMM kernel.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -14,9 +13,9 @@ struct TileCoord {
   int64_t lt;  // tile index within its matrix
 };
 
-// Tile t of the launch's linear tile space.  Output tiles are tile_rows x 256
-// (tile_rows = 128 for one CTA, 256 for a CTA pair); symmetric problems keep
-// the tiles that touch the upper triangle: column block >= floor(tm * tile_rows / 256).
+// Tile t of the launch's linear tile space.  Output tiles are kTileRows x 256
+// (128 x 256 for one CTA); symmetric problems keep the tiles that touch the
+// upper triangle: column block >= floor(tm * kTileRows / 256).
 template <int kTileRows>
 __device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t) {
   constexpr int kDiv = kBN / kTileRows;

@@ -12,7 +12,11 @@
 //   warps 2-5        epilogue: tcgen05.ld of their 32 TMEM lanes, the fused
 //                    OKLS arithmetic, global stores.
 // The two accumulators let the epilogue of tile i overlap the main loop of
-// tile i+1.  All waits are bounded (okls_ptx.cuh).
+// tile i+1.  All waits are bounded (okls_ptx.cuh) by the launch's limit;
+// when one expires the kernel raises kStTimeout, every thread leaves its
+// loop, the producer waits for its own copies still landing and the MMA
+// thread for its own MMAs (neither of those two waits stops early because
+// of another thread's timeout), and TMEM is freed before the CTA exits.
 //
 // Where each epilogue comes from (page "Online KL Shampoo", "How it works"):
 //   EPI_SYRK      the factor EMAs S <- beta2 S + (1-beta2)/n X X^T (+ eps I)
@@ -42,6 +46,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const long long lim = L.wait_cycles > 0 ? static_cast<long long>(L.wait_cycles) : kTimeoutCycles;
 
   // An earlier stage of the step failed: leave W, S and P untouched.
   if (threadIdx.x == 0) *skip = (*reinterpret_cast<volatile uint32_t*>(L.status) != 0u);
@@ -81,6 +86,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
       int64_t issued = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x) {
+        // test hook: this tile's operands are never loaded, so its consumers'
+        // waits run out with nothing of this CTA in flight
+        if (t == L.unloaded_tile) break;
         const TileCoord tc = decode_tile<kBM>(L, t);
         const GemmProblem& P = L.prob[tc.p];
         const int nkb = (P.K + kBK - 1) / kBK;
@@ -88,7 +96,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
           const CUtensorMap* am = L.maps + P.amap[sg];
           const CUtensorMap* bm = L.maps + P.bmap[sg];
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, L.status)) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, L.status, lim)) {
               ok = false;
               break;
             }
@@ -113,12 +121,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         }
       }
       // make sure no bulk copy is still landing in shared memory at exit
+      // (waits on this thread's own copies: the default limit, whatever the
+      // status word says)
       const int64_t back = issued < kStages ? issued : kStages;
       for (int64_t q = 1; q <= back; ++q) {
         const int64_t idx = issued - q;
         const uint32_t s = static_cast<uint32_t>(idx % kStages);
         const uint32_t ph = static_cast<uint32_t>((idx / kStages) & 1);
-        if (!mbar_wait(&full[s], ph, L.status)) break;
+        if (!mbar_wait_own(&full[s], ph, L.status)) break;
       }
     }
     __syncwarp();
@@ -146,7 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         const int nkb = ((P.K + kBK - 1) / kBK) * P.nseg;
         const uint32_t buf = it & 1u;
         const uint32_t aph = (it >> 1) & 1u;
-        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, L.status)) break;
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, L.status, lim)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kBN;
         const bool half_n = P.cols - tc.tn * kBN <= kBN / 2;
@@ -155,7 +165,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         // K16 step of B: 16 rows of 128 B (MN-major) or 32 B (K-major)
         const uint64_t bstep = P.bmn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, L.status)) {
+          if (!mbar_wait(&full[stage], phase, L.status, lim)) {
             ok = false;
             break;
           }
@@ -169,9 +179,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         }
         if (ok) umma_commit(&acc_full[buf]);
       }
-      // all MMAs retired before TMEM is released
+      // all MMAs retired before TMEM is released (this thread's own MMAs:
+      // the default limit, whatever the status word says)
       umma_commit(drain);
-      mbar_wait(drain, 0, L.status);
+      mbar_wait_own(drain, 0, L.status);
     }
     __syncwarp();
   } else {
@@ -185,7 +196,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
       const GemmProblem& P = L.prob[tc.p];
       const uint32_t buf = it & 1u;
       const uint32_t aph = (it >> 1) & 1u;
-      if (!mbar_wait(&acc_full[buf], aph, L.status)) break;
+      if (!mbar_wait(&acc_full[buf], aph, L.status, lim)) break;
       tc_fence_after();
       const int i = tc.tm * kBM + row_in_tile;
       float sumsq = 0.0f;

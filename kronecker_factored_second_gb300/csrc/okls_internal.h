@@ -93,9 +93,8 @@ struct GemmProblem {
   // B: box 256 rows) into the handle's descriptor table
   int32_t nseg;
   int32_t amap[kMaxSeg];        // A descriptors, 128-row boxes
-  int32_t bmap[kMaxSeg];        // B descriptors: K-major 256-row boxes (one CTA per tile), or
-                                // MN-major 64x64 boxes when bmn
-  int32_t bmap_pair[kMaxSeg];   // B descriptors for CTA pairs: K-major 128-row boxes, or MN-major
+  int32_t bmap[kMaxSeg];        // B descriptors: K-major 256-row boxes, or MN-major 64x64 boxes
+                                // when bmn
   int32_t bmn;                  // 1: B is stored K x N row-major (MN-major operand)
   int32_t rows, cols, K;        // output rows (A rows), cols (B rows), K
   int32_t batch;
@@ -151,6 +150,8 @@ struct GemmLaunch {
   int64_t total_tiles;
   const CUtensorMap* maps;      // device table of descriptors (64-byte aligned)
   uint32_t* status;
+  int64_t wait_cycles;          // limit of every pipeline wait (<= 0: the default, ~2 s of SM clock)
+  int64_t unloaded_tile;        // test hook: the producer stops before this linear tile (-1: none)
 };
 
 }  // namespace okls

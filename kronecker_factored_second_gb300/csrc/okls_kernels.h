@@ -210,7 +210,6 @@ struct SoapLarge {
 cudaError_t soap_large_step(const SoapLarge& S, int refresh, cudaStream_t st, int* launches);
 
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
-cudaError_t launch_gemm_pair(const GemmLaunch& L, int num_sms, cudaStream_t stream);
 
 // Reductions are deterministic: kernels write per-block (or per-tile) partials
 // into fixed slots and a single thread per matrix sums them in order.

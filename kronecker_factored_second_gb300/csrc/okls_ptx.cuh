@@ -49,9 +49,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
-// false (and raises kStTimeout) when the wait expires or another thread of
-// the grid already reported a timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// false (and raises kStTimeout) when the wait expires after `limit` cycles or
+// another thread of the grid already reported a timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          long long limit = kTimeoutCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   uint32_t n = 0;
@@ -59,10 +60,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     if (mbar_try_wait(bar, parity)) return true;
     if (((++n) & 127u) == 0u) {
       if (*reinterpret_cast<volatile uint32_t*>(status) & kStTimeout) return false;
-      if (clock64() - t0 > kTimeoutCycles) {
+      if (clock64() - t0 > limit) {
         atomicOr(status, kStTimeout);
         return false;
       }
+    }
+  }
+}
+
+// Wait for this thread's own operations in flight (its bulk copies, its
+// MMAs) before the CTA moves on to exit or to free TMEM: unlike mbar_wait it
+// does not give up when another thread has reported a timeout, only after
+// `limit` cycles of its own (and then raises kStTimeout).
+__device__ __forceinline__ bool mbar_wait_own(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                              long long limit = kTimeoutCycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) {
+      atomicOr(status, kStTimeout);
+      return false;
     }
   }
 }
@@ -243,7 +261,8 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                  long long limit = kTimeoutCycles) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const long long t0 = clock64();
   uint32_t n = 0;
@@ -251,10 +270,24 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (((++n) & 127u) == 0u) {
       if (*reinterpret_cast<volatile uint32_t*>(status) & kStTimeout) return false;
-      if (clock64() - t0 > kTimeoutCycles) {
+      if (clock64() - t0 > limit) {
         atomicOr(status, kStTimeout);
         return false;
       }
+    }
+  }
+}
+
+// mbar_wait_own for barriers that receive arrivals from the peer CTA
+__device__ __forceinline__ bool mbar_wait_own_cluster(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                      long long limit = kTimeoutCycles) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (clock64() - t0 > limit) {
+      atomicOr(status, kStTimeout);
+      return false;
     }
   }
 }

@@ -179,6 +179,12 @@ class OklsBatch:
     def t(self, value: int):
         L.check(L.lib().okls_set_step(self._h, int(value)))
 
+    def set_wait_limit(self, cycles: int = 0, unloaded_tile: int = -1):
+        """Wait limit of the GEMM launches of later steps (0: the default)
+        and the failure-path test hook (a tile whose operands are never
+        loaded; -1: none)."""
+        L.check(L.lib().okls_set_wait_limit(self._h, int(cycles), int(unloaded_tile)))
+
     def profile(self, timing: bool = True):
         """Enable event timing of the GEMM launches of later steps."""
         L.check(L.lib().okls_profile_enable(self._h, int(timing)))

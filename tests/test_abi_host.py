@@ -79,6 +79,7 @@ def test_null_arguments(lib):
     assert lib.okls_step(None, None, None, ctypes.c_float(0.1), None) == L.OKLS_ERR_INVALID_ARG
     assert lib.okls_destroy(None) == L.OKLS_OK
     assert lib.okls_ns_schedule(0, 1e-3, None, None, None) == L.OKLS_ERR_INVALID_ARG
+    assert lib.okls_set_wait_limit(None, 0, -1) == L.OKLS_ERR_INVALID_ARG
 
 
 def test_schedule_matches_oracle_definition(lib):

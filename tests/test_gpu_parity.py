@@ -312,6 +312,35 @@ def test_nonfinite_gradient_leaves_state_and_weights():
     assert ob.query_status() == 0
 
 
+def test_expired_wait_raises_timeout_and_leaves_state():
+    """Failure detection by bounded waits, with no GPU fault: a short wait
+    limit and a tile whose operands the producer never loads make the first
+    GEMM launch's waits run out.  The status word reports OKLS_DEV_TIMEOUT,
+    every later launch of the step returns at once (W, S and P keep their
+    values), and after the hook is removed the handle steps normally."""
+    okls = _okls()
+    ob = okls.OklsBatch(2, 256, 192)
+    torch.manual_seed(3)
+    W = torch.randn(2, 256, 192, device="cuda") * 0.01
+    G = torch.randn_like(W)
+    ob.step(W, G, 0.05)
+    assert ob.query_status() == 0
+    pre = snapshot(ob)
+    W1 = W.clone()
+    ob.set_wait_limit(cycles=20000, unloaded_tile=0)
+    ob.step(W, torch.randn_like(W), 0.05)
+    code, st = ob.status_nothrow()
+    assert code == L.OKLS_ERR_TIMEOUT and (st & L.DEV_TIMEOUT), (code, st)
+    post = snapshot(ob)
+    assert torch.equal(W, W1)
+    for k in ("Sa", "Sb", "Pa", "Pb"):
+        assert np.array_equal(pre[k], post[k]), k
+    ob.set_wait_limit(0, -1)
+    ob.step(W, G, 0.05)
+    assert ob.query_status() == 0
+    assert torch.isfinite(W).all() and not torch.equal(W, W1)
+
+
 def test_zero_lr_keeps_weights():
     okls = _okls()
     ob = okls.OklsBatch(1, 48, 48)
