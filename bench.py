@@ -55,28 +55,29 @@ GEMM_SOURCES = ["kronecker_factored_second_gb300/csrc/okls_gemm.cu",
                 "kronecker_factored_second_gb300/csrc/okls_epilogue.cuh",
                 "kronecker_factored_second_gb300/csrc/okls_ptx.cuh",
                 "kronecker_factored_second_gb300/csrc/okls_internal.h"]
-TRAFFIC_PROFILE = "profiles/okls_gemm_kernel__llama1.2b_dram_per_launch.md"
+TRAFFIC_RECORD = "profiles/okls_gemm_kernel__llama1.2b_dram.json"
+
+
+def gemm_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def gemm_traffic() -> float | None:
-    """DRAM bytes per GEMM launch from the committed ncu summary, or None
-    when the kernel sources changed since those counters were taken."""
-    import hashlib
+    """DRAM bytes (read + write) per GEMM launch of the headline step, from
+    the committed ncu record, or None when the kernel's sources changed since
+    those counters were taken."""
     try:
-        h = hashlib.sha256()
-        for f in GEMM_SOURCES:
-            with open(os.path.join(ROOT, f), "rb") as fh:
-                h.update(fh.read())
-        rec = {}
-        with open(os.path.join(ROOT, TRAFFIC_PROFILE)) as fh:
-            for line in fh:
-                if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch", "source_sha256"):
-                    k, v = line.split(":", 1)
-                    rec[k.strip()] = v.strip()
-        if rec.get("source_sha256") != h.hexdigest():
+        with open(os.path.join(ROOT, TRAFFIC_RECORD)) as fh:
+            rec = json.load(fh)
+        if rec.get("source_sha256") != gemm_sources_sha256():
             return None
         return float(rec["traffic_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 
@@ -196,64 +197,100 @@ def sum_over_ranks(x: float, ws: int, device) -> float:
 
 
 # ------------------------------------------------------------ CPU baseline
-def oracle_sample(seconds: float = 20.0, reps_max: int = 3) -> dict:
-    """The float64 oracle as it stands, one q/k/v/o-shaped (2048 x 2048)
-    matrix step per sample, repeated while within `seconds`."""
-    import numpy as np
+def _oracle_threads() -> int:
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
 
-    import oracle as O
-    rng = np.random.default_rng(7)
-    m = n = 2048
-    hp = O.Hyper(ridge=1e-3)
-    st = O.init_state(m, n, hp)
-    W = rng.standard_normal((m, n)) * 1e-3
-    times = []
-    t_end = time.perf_counter() + seconds
-    for i in range(reps_max):
-        G = rng.standard_normal((m, n))
-        t0 = time.perf_counter()
-        st, W, _U = O.okls_step(st, W, G, hp.lr, hp)
-        times.append(time.perf_counter() - t0)
-        if time.perf_counter() > t_end:
-            break
-    t = statistics.median(times)
-    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
-    return {"value": 1.0 / t, "unit": "matrices/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(times)} float64 oracle step(s) of one 2048x2048 q/k/v/o-shaped matrix "
-                      f"(eigendecomposition roots), median {t:.2f} s per matrix"}
+
+class OracleShapes:
+    """The float64 oracle as it stands, one matrix per distinct shape of the
+    workload, each with its own state carried from step to step.  A step of
+    the whole workload is extrapolated as sum over shapes of (matrices of
+    that shape) x (time of one oracle step on that shape): the oracle's cost
+    is that of its eigendecompositions and products, which do not depend on
+    the values, so iid N(0, 1) gradients of the same shapes stand in."""
+
+    def __init__(self, wl, seed: int = 7):
+        import numpy as np
+
+        import oracle as O
+        self.O = O
+        self.np = np
+        self.rng = np.random.default_rng(seed)
+        self.hp = O.Hyper(ridge=1e-3)
+        self.shapes = []
+        for g in wl.groups:
+            m, n = g.m, g.n
+            st = O.init_state(m, n, self.hp)
+            W = self.rng.standard_normal((m, n)) * 1e-3
+            self.shapes.append([g, st, W])
+        self.matrices = wl.matrices
+
+    def step(self) -> tuple[float, list]:
+        """One oracle step per shape; returns the extrapolated seconds of one
+        step of the whole workload and the per-shape seconds."""
+        per = []
+        total = 0.0
+        for item in self.shapes:
+            g, st, W = item
+            G = self.rng.standard_normal((g.m, g.n))
+            t0 = time.perf_counter()
+            st, W, _U = self.O.okls_step(st, W, G, self.hp.lr, self.hp)
+            dt = time.perf_counter() - t0
+            item[1], item[2] = st, W
+            per.append(dt)
+            total += g.batch * dt
+        return total, per
+
+    def describe(self, per: list) -> str:
+        return ("extrapolation: one float64 oracle step (eigendecomposition roots) per distinct shape, "
+                + ", ".join(f"{g.m}x{g.n} {dt:.2f} s x {g.batch}" for (g, _s, _W), dt in zip(self.shapes, per))
+                + f" = {sum(g.batch * dt for (g, _s, _W), dt in zip(self.shapes, per)):.1f} s per step of "
+                  f"{self.matrices} matrices (iid N(0,1) gradients of the same shapes)")
+
+
+def oracle_sample(wl) -> dict:
+    """cpu_baseline: one oracle step per distinct shape, extrapolated to the
+    workload's step (about 10-20 s of host CPU work on the 1.2B-shaped set)."""
+    orc = OracleShapes(wl)
+    total, per = orc.step()
+    return {"value": orc.matrices / total, "unit": "matrices/s", "cores": _oracle_threads(), "kind": "oracle",
+            "sample": orc.describe(per)}
 
 
 def run_reference(args):
-    """`--impl reference`: the float64 CPU oracle timed on the host cores on
-    a bounded sample of the same workload (one 2048x2048 matrix per step)."""
+    """`--impl reference`: the float64 CPU oracle timed on the host cores,
+    each step one oracle step per distinct shape of the workload,
+    extrapolated to the whole step (OracleShapes)."""
     ws, rank, _ = dist_info()
     if rank != 0:
         return
-    import numpy as np
-
-    import oracle as O
-    rng = np.random.default_rng(11)
-    m = n = 2048
-    hp = O.Hyper(ridge=1e-3)
-    st = O.init_state(m, n, hp)
-    W = rng.standard_normal((m, n)) * 1e-3
-    Gs = [rng.standard_normal((m, n)) for _ in range(2)]
-    for i in range(args.warmup):
-        st, W, _ = O.okls_step(st, W, Gs[i % 2], hp.lr, hp)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        st, W, _ = O.okls_step(st, W, Gs[i % 2], hp.lr, hp)
-    dt = (time.perf_counter() - t0) / max(args.steps, 1)
-    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
-    v = 1.0 / dt
+    from kronecker_factored_second_gb300.workloads import workload
+    wl = workload(args.workload, layers=args.layers)
+    orc = OracleShapes(wl, seed=11)
+    for _ in range(args.warmup):
+        orc.step()
+    tot, pers = 0.0, []
+    for _ in range(args.steps):
+        t, per = orc.step()
+        tot += t
+        pers.append(per)
+    dt = tot / max(args.steps, 1)
+    per_mean = [sum(p[i] for p in pers) / len(pers) for i in range(len(orc.shapes))]
+    v = orc.matrices / dt
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "matrices/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "llama1.2b (bounded sample: one 2048x2048 q/k/v/o-shaped matrix per step)"},
-            "cpu_baseline": {"value": v, "unit": "matrices/s", "cores": cores, "kind": "oracle",
-                             "sample": "one float64 oracle step of one 2048x2048 matrix per timed step"},
+            "config": {"workload": workload_desc(wl)},
+            "cpu_baseline": {"value": v, "unit": "matrices/s", "cores": _oracle_threads(), "kind": "oracle",
+                             "sample": orc.describe(per_mean)},
             "e2e": {"value": v, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def workload_desc(wl) -> str:
+    return (f"{wl.name}: " + ", ".join(f"{g.batch} x {g.m}x{g.n} {g.name}" for g in wl.groups)
+            + f" = {wl.matrices} matrices, {wl.groups[0].dtype} W and G, fp32 state, "
+            f"{wl.recipe} gradients (condition number {wl.cond:g})")
 
 
 # --------------------------------------------------------------- GPU arm
@@ -572,7 +609,7 @@ def run_okls(args):
 
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline:
-        cpu = oracle_sample(args.cpu_seconds)
+        cpu = oracle_sample(wl)
 
     if rank == 0:
         # SOAP's products run on CUDA-core GEMMs that the per-launch events do
@@ -591,9 +628,7 @@ def run_okls(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp32" if args.method == "soap" else "fp16", "data": "synthetic",
             "config": {
-                "workload": (f"{args.workload}: " + ", ".join(f"{g.batch} x {g.m}x{g.n} {g.name}" for g in wl.groups)
-                             + f" = {matrices} matrices, {wl.groups[0].dtype} W and G, fp32 state, "
-                             f"{wl.recipe} gradients (condition number {wl.cond:g})"),
+                "workload": workload_desc(wl),
                 "method": args.method,
                 "precision": ("fp32 throughout (batched CUDA-core GEMMs, Jacobi eigenbasis refresh every 10 "
                               "steps)" if args.method == "soap" else
@@ -654,7 +689,6 @@ def main():
     ap.add_argument("--also-clean-large", type=int, default=1)
     ap.add_argument("--method", choices=["okls", "shampoo", "soap"], default="okls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "okls":
         print("note: at least 3 warm-up steps are used", file=sys.stderr)

@@ -345,6 +345,43 @@ struct WaitScope {
 // transposed copy, which shares the pitch); a violation is a planning bug.
 thread_local bool g_plan_error = false;
 
+// Raster group height of a non-symmetric problem (see kRasterL2Bytes): the
+// largest height, in groups of equal size, for which the group's A row
+// panels and the B column panels one wave of `sms` tiles spans fit the L2
+// budget.  OKLS_GROUP_M=<rows> overrides it (tuning experiments).
+int env_group_m() {
+  static const int v = [] {
+    const char* e = getenv("OKLS_GROUP_M");
+    return e ? atoi(e) : 0;
+  }();
+  return v;
+}
+
+void raster_plan(GemmProblem& p, int sms) {
+  const int tm = p.tiles_m;
+  int gm = 0;
+  if (env_group_m() > 0) {
+    gm = std::min(env_group_m(), tm);
+  } else {
+    const double a_panel = static_cast<double>(kBM) * p.K * 2.0 * p.nseg;  // one row block of A
+    const double b_panel = static_cast<double>(kBN) * p.K * 2.0 * p.nseg;  // one column block of B
+    for (int groups = 1; groups <= tm && gm == 0; ++groups) {
+      const int h = (tm + groups - 1) / groups;
+      const int wave_cols = (sms + h - 1) / h;
+      if (h * a_panel + std::min(wave_cols, p.tiles_n) * b_panel <= kRasterL2Bytes) gm = h;
+    }
+    // nothing fits: the height whose wave footprint h a + (sms / h) b is
+    // smallest, h = sqrt(sms b / a) = sqrt(2 sms)
+    if (gm == 0) gm = std::min(tm, static_cast<int>(std::lround(std::sqrt(2.0 * sms))));
+  }
+  if (gm < 1) gm = 1;
+  p.group_m = gm;
+  p.last_gm = tm % gm == 0 ? gm : tm % gm;
+  fastdiv_make(static_cast<uint32_t>(gm * p.tiles_n), &p.span_mul, &p.span_shift);
+  fastdiv_make(static_cast<uint32_t>(gm), &p.gm_mul, &p.gm_shift);
+  fastdiv_make(static_cast<uint32_t>(p.last_gm), &p.lgm_mul, &p.lgm_shift);
+}
+
 struct LaunchBuilder {
   GemmLaunch L;
   LaunchBuilder() { memset(&L, 0, sizeof(L)); }
@@ -437,7 +474,7 @@ struct LaunchBuilder {
       p.tile_begin = t;
       t += p.tiles_per_mat * p.batch;
       fastdiv_make(static_cast<uint32_t>(p.tiles_per_mat), &p.tpm_mul, &p.tpm_shift);
-      fastdiv_make(static_cast<uint32_t>(kGroupM * p.tiles_n), &p.span_mul, &p.span_shift);
+      raster_plan(p, sms);
     }
     // the kernels decode tile indices in 32 bits
     if (t >= (int64_t(1) << 31)) return fail(OKLS_ERR_UNSUPPORTED, "more than 2^31 output tiles in one launch");

@@ -19,7 +19,6 @@ struct TileCoord {
 template <int kTileRows>
 __device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t) {
   constexpr int kDiv = kBN / kTileRows;
-  static_assert((kGroupM & (kGroupM - 1)) == 0, "raster group height must be a power of two");
   TileCoord c;
   int p = 0;
   while (p + 1 < L.nprob && t >= L.prob[p + 1].tile_begin) ++p;
@@ -44,15 +43,16 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t)
     c.tn = tm / kDiv + static_cast<int>(r);
   } else {
     const uint32_t g = fastdiv(r, P.span_mul, P.span_shift);
-    const int first = static_cast<int>(g) * kGroupM;
-    const int gm = min(kGroupM, P.tiles_m - first);
-    const uint32_t rr = r - g * static_cast<uint32_t>(kGroupM * P.tiles_n);
-    if (gm == kGroupM) {
-      c.tm = first + static_cast<int>(rr & (kGroupM - 1));
-      c.tn = static_cast<int>(rr / kGroupM);
+    const int first = static_cast<int>(g) * P.group_m;
+    const uint32_t rr = r - g * static_cast<uint32_t>(P.group_m * P.tiles_n);
+    if (P.tiles_m - first >= P.group_m) {
+      const uint32_t col = fastdiv(rr, P.gm_mul, P.gm_shift);
+      c.tm = first + static_cast<int>(rr - col * static_cast<uint32_t>(P.group_m));
+      c.tn = static_cast<int>(col);
     } else {  // the last, shorter group of row blocks
-      c.tm = first + static_cast<int>(rr % static_cast<uint32_t>(gm));
-      c.tn = static_cast<int>(rr / static_cast<uint32_t>(gm));
+      const uint32_t col = fastdiv(rr, P.lgm_mul, P.lgm_shift);
+      c.tm = first + static_cast<int>(rr - col * static_cast<uint32_t>(P.last_gm));
+      c.tn = static_cast<int>(col);
     }
   }
   return c;

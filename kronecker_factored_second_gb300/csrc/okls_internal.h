@@ -44,7 +44,13 @@ constexpr int kTmemCols = 512;                // two 256-column fp32 accumulator
 constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int kMaxProblems = 6;
 constexpr int kMaxSeg = 3;                    // K segments (split mode: hi*hi, hi*lo, lo*hi)
-constexpr int kGroupM = 8;                    // raster group height (tiles) for L2 reuse
+// Raster of non-symmetric products: output tiles go in groups of group_m
+// row blocks, column by column inside a group, so a group's A row panels stay
+// in L2 while its columns pass and each B column panel is read once per
+// group.  group_m is chosen per problem on the host: the largest height
+// (groups of equal size) whose A panels plus the B panels of one wave of
+// tiles fit kRasterL2Bytes.
+constexpr double kRasterL2Bytes = 64.0 * 1024 * 1024;
 
 // Binary16 operand headroom (power of two) of the Newton-Schulz iterates.
 constexpr int kHeadroom = 12;
@@ -103,9 +109,12 @@ struct GemmProblem {
   int32_t epi;
   int64_t tiles_per_mat;
   int64_t tile_begin;           // first linear tile of this problem in the launch
-  // exact division of tile indices (< 2^31) by tiles_per_mat and by the raster
-  // group span kGroupM * tiles_n: q = (n * mul) >> shift (host-computed)
+  // exact division of tile indices (< 2^31) by tiles_per_mat, by the raster
+  // group span group_m * tiles_n, by group_m and by the height of the last
+  // (shorter) group: q = (n * mul) >> shift (host-computed)
   uint32_t tpm_mul, tpm_shift, span_mul, span_shift;
+  int32_t group_m, last_gm;
+  uint32_t gm_mul, gm_shift, lgm_mul, lgm_shift;
   // epilogue
   void* out_hi;                 // fp16 row-major
   void* out_hi_t;               // fp16 transposed (may be null)

@@ -39,7 +39,7 @@ import numpy as np
 
 __all__ = [
     "Hyper", "OklsState", "c_shape", "variance_correction", "adamc_decay",
-    "sym_power", "inv_root_exact", "cans_schedule", "ns_exponents",
+    "sym_power", "inv_root_exact", "inv_roots_exact", "cans_schedule", "ns_exponents",
     "ns_scalar_map", "ns_exact", "ns_matrix_float64", "f16", "split16",
     "ns_replay", "ns_replay_iteration", "factor_ema", "init_state",
     "okls_step", "okls_run", "rel_fro", "NS_HEADROOM", "NS_MARGIN",
@@ -159,6 +159,22 @@ def inv_root_exact(S: np.ndarray, ridge: float = 0.0) -> np.ndarray:
     return sym_power(S + ridge * c * np.eye(S.shape[0]), -0.5)
 
 
+def inv_roots_exact(S: np.ndarray, ridges) -> list:
+    """inv_root_exact(S, rho) for each rho in `ridges` from one
+    eigendecomposition of S (for large factors, where eigh dominates)."""
+    S = _sym(S)
+    c = math.sqrt(float(np.sum(S * S)))
+    lam, Q = np.linalg.eigh(S)
+    out = []
+    for rho in ridges:
+        mu = np.maximum(lam + rho * c, 0.0)
+        f = np.zeros_like(mu)
+        keep = mu > 0.0
+        f[keep] = mu[keep] ** -0.5
+        out.append((Q * f) @ Q.T)
+    return out
+
+
 # -------------------------------------------------- Newton-Schulz schedule ---
 
 def cans_schedule(iters: int = 10, lo: float = 1e-3, hi: float = 1.0):
@@ -262,16 +278,25 @@ def _ns_consts(schedule, headroom=NS_HEADROOM):
     return z, headroom, headroom, headroom
 
 
-def _prod(A, B, split: bool):
+def _mm(A, B, acc32: bool):
+    """A @ B in float64, or (acc32) with float32 operands and a float32
+    result accumulated in the BLAS's own order (binary16 operands are exact
+    in float32)."""
+    if not acc32:
+        return A @ B
+    return (np.asarray(A, np.float32) @ np.asarray(B, np.float32)).astype(np.float64)
+
+
+def _prod(A, B, split: bool, acc32: bool = False):
     """A @ B for stored operands; in split mode A, B are (hi, lo) pairs and
     the product keeps hi*hi + hi*lo + lo*hi (lo*lo is below the precision)."""
     if not split:
-        return A @ B
-    return A[0] @ B[0] + A[0] @ B[1] + A[1] @ B[0]
+        return _mm(A, B, acc32)
+    return _mm(A[0], B[0], acc32) + _mm(A[0], B[1], acc32) + _mm(A[1], B[0], acc32)
 
 
 def ns_replay(S: np.ndarray, schedule, ridge: float = 0.0, rounding: bool = True,
-              trace: bool = False, split_iters: int = 0):
+              trace: bool = False, split_iters: int = 0, accumulate: str = "float64"):
     """Float64 replay of the coupled iteration as the GPU orders it, with every
     GEMM operand rounded to binary16 (rounding=False keeps float64 operands).
 
@@ -290,6 +315,12 @@ def ns_replay(S: np.ndarray, schedule, ridge: float = 0.0, rounding: bool = True
 
     split_iters > 0: the operands of iterations k < split_iters are (hi, lo)
     binary16 pairs (``split16``) and each product is hi*hi + hi*lo + lo*hi.
+
+    accumulate="float32": every product is summed in float32 (in the BLAS's
+    order) instead of float64.  Two float32 accumulation orders give two
+    different chains: the distance between this replay and the float64 one
+    measures how far accumulation order alone moves the result, the floor
+    any fp32-accumulating implementation meets end to end.
 
     Returns dict with P, P_hat (binary16 copy of Z_K^), pi (P ~ pi * P_hat),
     c_prime, root (S^1/2 ~ Y_K sqrt(c') = (Y^_{K-1} T^_{K-1}) 2^(-2h) sqrt(c'))
@@ -316,6 +347,9 @@ def ns_replay(S: np.ndarray, schedule, ridge: float = 0.0, rounding: bool = True
     I = np.eye(d)
     cp, Y0 = _normaliser(S, ridge)
     Ys, Zs, Ts = [], [], []
+    a32 = accumulate == "float32"
+    if accumulate not in ("float64", "float32"):
+        raise ValueError(accumulate)
     sp = split_iters > 0
     Yh = rs(Y0 * 2.0 ** h, sp)
     a0, b0 = schedule[0][0], schedule[0][1]
@@ -323,7 +357,7 @@ def ns_replay(S: np.ndarray, schedule, ridge: float = 0.0, rounding: bool = True
     sp1 = split_iters > 1
     Zh = rs(val(Th) * 2.0 ** (-z[1]), sp1)
     Ys.append(Yh); Zs.append(None); Ts.append(Th)
-    Yh = rs(_prod(Yh, Th, sp) * 2.0 ** -h, sp1)
+    Yh = rs(_prod(Yh, Th, sp, a32) * 2.0 ** -h, sp1)
     Zacc = None
     for k in range(1, K):
         spk = split_iters > k
@@ -331,10 +365,10 @@ def ns_replay(S: np.ndarray, schedule, ridge: float = 0.0, rounding: bool = True
         a, b = schedule[k][0], schedule[k][1]
         Ys.append(Yh); Zs.append(Zh)
         Mfac = b * 2.0 ** (z[k] - h)
-        Th = rs(2.0 ** h * a * I + Mfac * _prod(Zh, Yh, spk), spk)
+        Th = rs(2.0 ** h * a * I + Mfac * _prod(Zh, Yh, spk, a32), spk)
         Ts.append(Th)
-        Zacc = _prod(Th, Zh, spk)
-        Yacc = _prod(Yh, Th, spk)
+        Zacc = _prod(Th, Zh, spk, a32)
+        Yacc = _prod(Yh, Th, spk, a32)
         if k < K - 1:
             Yh = rs(Yacc * 2.0 ** -h, spn)
             Zh = rs(Zacc * 2.0 ** (z[k] - z[k + 1] - h), spn)

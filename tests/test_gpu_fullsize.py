@@ -1,16 +1,22 @@
 """Parity at the workloads' full sizes, in the launch configuration bench.py
 times (whole batches of every shape group on one GPU), on sampled outputs.
 
-For one matrix of each shape group, step 2 is checked teacher-forced from the
-GPU's own state after step 1 (so the factor products see a non-trivial P):
+For one matrix of each shape group the workload's LAST step (t = 50 for the
+16 x 512^2 batch, 10 for the 1.2B-shaped set and the rectangular set, 5 for
+the 7B-shaped slice) is checked teacher-forced from the GPU's own state after
+step t - 1, in both precision modes (plain binary16 with ridge 1e-3; the
+first three iterations split with ridge 1e-4):
   M            every entry, 1e-6
   S_a, S_b     a 32 x 32 block: rows of G P_b / P_a G computed in float64
                from the GPU's previous roots, 1e-3
   P_a, P_b     against the eigendecomposition root of the GPU's own ridged S
-               (float64 on the host), 1e-2
+               (float64 on the host), 1e-2; the distance to the root of the
+               unridged S is reported beside it
   U            64 sampled entries (from the change of W) against P_a N P_b with
                the exact roots of the GPU's S and N from the float64 momentum,
                2e-2; and against the same product with the GPU's own roots, 2e-2
+A per-iteration replay of the binary16 chain runs on one full-size 2048^2 and
+one 5504^2 factor of the 1.2B-shaped set.
 """
 
 from __future__ import annotations
@@ -27,6 +33,9 @@ from gpu_helpers import PARTS, hyper_of
 from kronecker_factored_second_gb300.workloads import GradientStream, workload
 
 pytestmark = pytest.mark.gpu
+
+LAST_STEP = {"batch16x512": 50, "llama1.2b": 10, "rect8192": 10, "llama7b_slice": 5}
+MODES = [pytest.param((0, 1e-3), id="fp16-ridge1e-3"), pytest.param((3, 1e-4), id="split3-ridge1e-4")]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,16 +54,18 @@ def _matrix_state(ob, b: int) -> dict:
     return out
 
 
-def _check_group(wl_name, gi, g, gs, b, rng):
+def _check_group(wl_name, gi, g, gs, b, rng, t_last, mode):
     from kronecker_factored_second_gb300.okls import OklsBatch
-    ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype)
+    split, ridge = mode
+    ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=split, ridge=ridge)
     hp = hyper_of(ob)
     W = gs.init_weights(gi)
-    ob.step(W, gs.grad(gi, 1), hp.lr)
+    for t in range(1, t_last):
+        ob.step(W, gs.grad(gi, t), hp.lr)
     assert ob.query_status() == 0
     pre = _matrix_state(ob, b)
     Wp = W[b].double().cpu().numpy()
-    G = gs.grad(gi, 2)
+    G = gs.grad(gi, t_last)
     ob.step(W, G, hp.lr)
     assert ob.query_status() == 0
     post = _matrix_state(ob, b)
@@ -81,28 +92,30 @@ def _check_group(wl_name, gi, g, gs, b, rng):
     Xa_i, Xa_j = pre["Pa"] @ Gb[:, ib], pre["Pa"] @ Gb[:, jb]
     Sb_blk = b2 * pre["Sb"][np.ix_(ib, jb)] + (1 - b2) / m * (Xa_i.T @ Xa_j) + hp.eps * (ib[:, None] == jb[None, :])
     err["Sb"] = O.rel_fro(post["Sb"][np.ix_(ib, jb)], Sb_blk)
-    # roots against the exact root of the GPU's own ridged factors
+    # roots against the exact root of the GPU's own ridged factors (and, for
+    # the record, of the unridged ones)
     t0 = time.time()
-    Pa_x = O.inv_root_exact(post["Sa"], hp.ridge)
-    Pb_x = O.inv_root_exact(post["Sb"], hp.ridge)
+    Pa_x, Pa_0 = O.inv_roots_exact(post["Sa"], [hp.ridge, 0.0])
+    Pb_x, Pb_0 = O.inv_roots_exact(post["Sb"], [hp.ridge, 0.0])
     t_eigh = time.time() - t0
     err["Pa"] = O.rel_fro(post["Pa"], Pa_x)
     err["Pb"] = O.rel_fro(post["Pb"], Pb_x)
+    err["Pa_plain"] = O.rel_fro(post["Pa"], Pa_0)
+    err["Pb_plain"] = O.rel_fro(post["Pb"], Pb_0)
     # sampled U entries
-    kappa = O.variance_correction(b1, 2)
+    kappa = O.variance_correction(b1, t_last)
     N = kappa * (b1 * M + (1 - b1) * Gb)
     ri = rng.choice(m, size=64)
     ci = rng.choice(n, size=64)
     decay = O.adamc_decay(hp.lr, hp.peak, hp.weight_decay)
     c = O.c_shape(m, n)
     U_gpu = ((1 - decay) * Wp[ri, ci] - Wn[ri, ci]) / (hp.lr * c)
-    left_x = Pa_x[ri] @ N
-    U_x = np.einsum("ij,ji->i", left_x, Pb_x[:, ci])
-    left_g = post["Pa"][ri] @ N
-    U_tf = np.einsum("ij,ji->i", left_g, post["Pb"][:, ci])
+    U_x = np.einsum("ij,ji->i", Pa_x[ri] @ N, Pb_x[:, ci])
+    U_tf = np.einsum("ij,ji->i", post["Pa"][ri] @ N, post["Pb"][:, ci])
     err["U"] = float(np.linalg.norm(U_gpu - U_x) / np.linalg.norm(U_x))
     err["U_tf"] = float(np.linalg.norm(U_gpu - U_tf) / np.linalg.norm(U_tf))
-    print(f"{wl_name}/{g.name} b={b} ({m}x{n}) eigh {t_eigh:.1f}s", {k: f"{v:.2e}" for k, v in err.items()})
+    print(f"{wl_name}/{g.name} t={t_last} split={split} ridge={ridge:g} b={b} ({m}x{n}) eigh {t_eigh:.1f}s",
+          {k: f"{v:.2e}" for k, v in err.items()})
     bf16 = g.dtype == torch.bfloat16
     assert err["M"] < 1e-6, err
     assert err["Sa"] < 1e-3 and err["Sb"] < 1e-3, err
@@ -112,14 +125,66 @@ def _check_group(wl_name, gi, g, gs, b, rng):
     assert err["U"] < u_tol and err["U_tf"] < u_tol, err
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name", ["batch16x512", "llama1.2b", "rect8192", "llama7b_slice"])
-def test_full_size_sampled_parity(name):
+def test_full_size_last_step_parity(name, mode):
     wl = workload(name)
     gs = GradientStream(wl, "cuda")
     rng = np.random.default_rng(31)
     for gi, g in enumerate(wl.groups):
         b = (7 * gi + 3) % g.batch
-        _check_group(name, gi, g, gs, b, rng)
+        _check_group(name, gi, g, gs, b, rng, LAST_STEP[name], mode)
+
+
+@pytest.mark.parametrize("gi", [0, 1])
+def test_full_size_per_iteration_replay(gi):
+    """The 1.2B-shaped set's left factor after three steps: 2048^2 (q/k/v/o)
+    and 5504^2 (gate/up).  The GPU's stored iterates (Y^_k, Z^_k) are fed to
+    one float64 step of the binary16 replay; T^_k, Y^_k+1, Z^_k+1 must agree
+    to 1e-3.  The end-to-end distance to the replay is reported beside the
+    float32-accumulation-order floor."""
+    from kronecker_factored_second_gb300 import okls
+    from kronecker_factored_second_gb300 import _lib as L
+    wl = workload("llama1.2b")
+    g = wl.groups[gi]
+    gs = GradientStream(wl, "cuda")
+    ob = okls.OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype)
+    hp = hyper_of(ob)
+    W = gs.init_weights(gi)
+    for t in range(1, 4):
+        ob.step(W, gs.grad(gi, t), hp.lr)
+    assert ob.query_status() == 0
+    Sfull = ob.get_state(L.STATE_SA)
+    S = Sfull[2:3].clone()
+    del Sfull, W
+    ob.close()
+    del ob
+    torch.cuda.empty_cache()
+    out = okls.inv_root(S, ridge=hp.ridge, want_trace=True)
+    tr = out["trace"][:, 0].float().cpu().numpy().astype(np.float64)
+    P = out["P"][0].double().cpu().numpy()
+    S64 = S[0].double().cpu().numpy()
+    sch = O.cans_schedule(10, 1e-3)
+    t0 = time.time()
+    rep = O.ns_replay(S64, sch, hp.ridge, trace=True)
+    assert O.rel_fro(tr[0], rep["Y"][0]) < 1e-3
+    assert O.rel_fro(tr[2], rep["T"][0]) < 1e-3
+    worst = 0.0
+    for k in range(1, 10):
+        Yk, Zk, Tk = tr[3 * k], tr[3 * k + 1], tr[3 * k + 2]
+        T1, Y1, Z1 = O.ns_replay_iteration(k, Yk, Zk, sch)
+        errs = [O.rel_fro(Tk, T1)]
+        Znext = tr[3 * (k + 1) + 1] if k < 9 else tr[30]
+        errs.append(O.rel_fro(Znext, Z1))
+        if k < 9:
+            errs.append(O.rel_fro(tr[3 * (k + 1)], Y1))
+        worst = max(worst, max(errs))
+        assert max(errs) < 1e-3, (k, errs)
+    e_rep = O.rel_fro(P, rep["P"])
+    e_exact = O.rel_fro(P, O.inv_root_exact(S64, hp.ridge))
+    print(f"full-size replay d={g.m}: worst per-iteration {worst:.2e}, end-to-end vs replay {e_rep:.2e}, "
+          f"vs exact {e_exact:.2e}, host {time.time() - t0:.1f}s")
+    assert e_exact < 1e-2
 
 
 def _check_group_shampoo(wl_name, gi, g, gs, b, rng):

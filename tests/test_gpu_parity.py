@@ -114,10 +114,13 @@ def test_inv_root_per_iteration_replay(d, count, cond):
         e_exact = O.rel_fro(P[b], O.inv_root_exact(S32[b]))
         e_rep = O.rel_fro(P[b], rep["P"])
         assert e_exact < 1e-2, e_exact
-        # end to end the chain amplifies accumulation-order noise (fp32 sums on
-        # the GPU, float64 in the replay): a few 1e-3 at most for cond <= 1e2
+        # end to end the chain amplifies accumulation-order noise: the same
+        # replay summed in float32 (another order) moves as far from the
+        # float64 replay, so that distance is the floor the bar allows for
+        e_floor = O.rel_fro(O.ns_replay(S32[b], sch, accumulate="float32")["P"], rep["P"])
+        print(f"inv_root d={d} b={b}: end-to-end vs replay {e_rep:.2e}, float32-order floor {e_floor:.2e}")
         if cond <= 100:
-            assert e_rep < 3e-3, e_rep
+            assert e_rep < max(1e-3, 1.5 * e_floor), (e_rep, e_floor)
     print(f"inv_root d={d}: worst per-iteration {worst:.2e}")
 
 
@@ -148,6 +151,10 @@ def test_inv_root_root_output():
 # ------------------------------------------------------------ whole steps
 
 MODES = [pytest.param((0, 1e-3), id="fp16-ridge1e-3"), pytest.param((3, 1e-4), id="split3-ridge1e-4")]
+# every Newton-Schulz iteration on (hi, lo) binary16 pairs: the mode that
+# holds the main bars on factors of a few rows, whose ridge-level eigenvalues
+# a single binary16 copy of Y_0 resolves only to a few percent
+FULL_SPLIT = pytest.param((10, 1e-3), id="split10-ridge1e-3")
 
 
 def _run(wl, steps, mode=(0, 1e-3), sample=None, lr_sched=None, root_every=1, check_stale=False):
@@ -193,15 +200,18 @@ def _run(wl, steps, mode=(0, 1e-3), sample=None, lr_sched=None, root_every=1, ch
     return worst
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES + [FULL_SPLIT])
 def test_step_single128x64_twenty_steps(mode):
     """The 128 x 64 workload at full size, all 20 steps, every step checked."""
     _run(workload("single128x64"), 20, mode)
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES + [FULL_SPLIT])
 def test_step_hand_example_matrix(mode):
-    """The optim-book's 2 x 3 gradient as a parameter, fed four times."""
+    """The optim-book's 2 x 3 gradient as a parameter, fed four times (the
+    hand example of the 128 x 64 workload).  With every iteration split it
+    holds the main bars (P 1e-2, U 2e-2); the other two modes are held to
+    the bar for degenerate tiny factors."""
     okls = _okls()
     G = torch.tensor([[3.0, 0.0, 1.0], [1.0, 2.0, 0.0]]).reshape(1, 2, 3)
     ob = okls.OklsBatch(1, 2, 3, ns_split_iters=mode[0], ridge=mode[1])
@@ -219,7 +229,21 @@ def test_step_hand_example_matrix(mode):
         for k, v in e.items():
             worst[k] = max(worst.get(k, 0.0), v)
     print("hand example step", mode, {k: f"{v:.2e}" for k, v in worst.items()})
-    _degenerate_bar(worst, mode)
+    if mode[0] >= 10:
+        _main_bar(worst)
+    else:
+        _degenerate_bar(worst, mode)
+
+
+def _main_bar(worst):
+    """The stated bars: M 1e-6, S 1e-3, P 1e-2 against the exact root of the
+    GPU's own ridged factor, U 2e-2 against the oracle's float64 step and
+    against the whitening with the GPU's own roots."""
+    assert worst["M"] < 1e-6, worst
+    assert worst["Sa"] < 1e-3 and worst["Sb"] < 1e-3, worst
+    assert worst["Pa_exact"] < 1e-2 and worst["Pb_exact"] < 1e-2, worst
+    assert worst["U"] < 2e-2 and worst["U_tf"] < 2e-2, worst
+    assert all(np.isfinite(v) for v in worst.values())
 
 
 def _degenerate_bar(worst, mode):
@@ -375,7 +399,7 @@ def test_state_roundtrip_and_resume():
                      Wa.double().cpu().numpy() - W.double().cpu().numpy()) < 2e-2
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES + [FULL_SPLIT])
 def test_ragged_shapes_and_tiny_dims(mode):
     for (B, m, n) in [(3, 200, 72), (1, 2, 3), (2, 1, 5), (1, 260, 260), (2, 4, 3)]:
         okls = _okls()
@@ -397,12 +421,10 @@ def test_ragged_shapes_and_tiny_dims(mode):
                 for k, v in e.items():
                     worst[k] = max(worst.get(k, 0.0), v)
         print("ragged", mode, (B, m, n), {k: f"{v:.2e}" for k, v in worst.items()})
-        if min(m, n) <= 5:
+        if min(m, n) <= 5 and mode[0] < 10:
             _degenerate_bar(worst, mode)
         else:
-            assert worst["Sa"] < 1e-3 and worst["Sb"] < 1e-3, worst
-            assert worst["Pa_exact"] < 1e-2 and worst["Pb_exact"] < 1e-2, worst
-            assert worst["U"] < 2e-2 and worst["U_tf"] < 2e-2, worst
+            _main_bar(worst)
 
 
 def test_bitwise_reproducible():

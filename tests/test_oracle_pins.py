@@ -177,6 +177,13 @@ def test_ridge_is_root_of_shifted_matrix():
     assert O.rel_fro(O.ns_exact(S, O.cans_schedule(10, 1e-3), rho)[0], want) < 2e-5
 
 
+def test_roots_for_several_ridges_from_one_decomposition():
+    S = _spd(40, 1e3, 12)
+    got = O.inv_roots_exact(S, [0.0, 1e-4, 1e-3])
+    for P, rho in zip(got, [0.0, 1e-4, 1e-3]):
+        assert O.rel_fro(P, O.inv_root_exact(S, rho)) < 1e-12
+
+
 def test_replay_without_rounding_is_the_float64_iteration():
     S = _spd(48, 1e3, 5)
     sch = O.cans_schedule(10, 1e-3)
@@ -197,6 +204,24 @@ def test_replay_with_binary16_rounding_is_accurate_when_well_conditioned():
     e0 = O.rel_fro(O.ns_replay(S4, sch)["P"], O.inv_root_exact(S4))
     e3 = O.rel_fro(O.ns_replay(S4, sch, split_iters=3)["P"], O.inv_root_exact(S4))
     assert e3 < 1e-2 and e3 < 0.5 * e0
+
+
+def test_replay_float32_accumulation_is_the_same_chain():
+    """accumulate="float32" changes only the summation precision: without
+    binary16 rounding it is the float64 iteration to float32 accuracy; with
+    rounding it still reaches the exact root, and it moves the end-to-end
+    result by a small but non-zero amount (the accumulation-order floor)."""
+    sch = O.cans_schedule(10, 1e-3)
+    S = _spd(96, 1e2, 9)
+    r64 = O.ns_replay(S, sch, rounding=False)
+    r32 = O.ns_replay(S, sch, rounding=False, accumulate="float32")
+    assert O.rel_fro(r32["P"], r64["P"]) < 1e-5
+    q64 = O.ns_replay(S, sch)
+    q32 = O.ns_replay(S, sch, accumulate="float32")
+    assert O.rel_fro(q32["P"], O.inv_root_exact(S)) < 1e-2
+    assert 0.0 < O.rel_fro(q32["P"], q64["P"]) < 5e-3
+    with pytest.raises(ValueError):
+        O.ns_replay(S, sch, accumulate="float16")
 
 
 def test_replay_iteration_matches_trace():
