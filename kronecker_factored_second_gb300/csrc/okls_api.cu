@@ -436,7 +436,9 @@ struct LaunchBuilder {
     return p;
   }
 
-  okls_status go(const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st) {
+  // Validate the problems, order them (longest K first) and lay out their
+  // tiles from linear tile `base` on; *flops gets their algorithmic FLOPs.
+  okls_status prepare(int sms, int64_t base, double* flops) {
     if (g_plan_error) {
       g_plan_error = false;
       return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: output buffer smaller than a GEMM problem");
@@ -463,7 +465,7 @@ struct LaunchBuilder {
     } else {
       return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: descriptor table not bound");
     }
-    int64_t t = 0;
+    int64_t t = base;
     for (int i = 0; i < L.nprob; ++i) {
       GemmProblem& p = L.prob[i];
       p.tiles_m = (p.rows + kBM - 1) / kBM;
@@ -479,18 +481,26 @@ struct LaunchBuilder {
     // the kernels decode tile indices in 32 bits
     if (t >= (int64_t(1) << 31)) return fail(OKLS_ERR_UNSUPPORTED, "more than 2^31 output tiles in one launch");
     L.total_tiles = t;
+    double f = 0.0;
+    for (int i = 0; i < L.nprob; ++i) {
+      const GemmProblem& p = L.prob[i];
+      const double mn =
+          p.sym ? static_cast<double>(p.rows) * (p.rows + 1) * 0.5 : static_cast<double>(p.rows) * p.cols;
+      f += 2.0 * mn * p.K * p.batch * p.nseg;
+    }
+    *flops = f;
+    return OKLS_OK;
+  }
+
+  okls_status go(const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st) {
+    double flops = 0.0;
+    okls_status s0 = prepare(sms, 0, &flops);
+    if (s0 != OKLS_OK) return s0;
     L.maps = maps;
     L.status = status;
     L.wait_cycles = g_wait.cycles;
     L.unloaded_tile = g_wait.unloaded_tile;
     Prof* pf = g_prof;
-    double flops = 0.0;
-    for (int i = 0; i < L.nprob; ++i) {
-      const GemmProblem& p = L.prob[i];
-      const double mn =
-          p.sym ? static_cast<double>(p.rows) * (p.rows + 1) * 0.5 : static_cast<double>(p.rows) * p.cols;
-      flops += 2.0 * mn * p.K * p.batch * p.nseg;
-    }
     cudaEvent_t ea = nullptr, eb = nullptr;
     if (pf && pf->timing) {
       ea = pf->next_event();
@@ -536,6 +546,16 @@ void set_out16(GemmProblem& p, const Buf& hi, const Buf* hiT, const Buf* lo, con
   p.split_out = lo ? 1 : 0;
 }
 
+// The GEMM stages of the coupled Newton-Schulz chain for 1 or 2 factors,
+// handed to `sink` in order (one LaunchBuilder per stage: stage 0 is
+// Y_1 = Y_0 T_0, then per iteration k >= 1 the T_k stage and the Y/Z stage).
+// The stable order is kept: M_k = Z_k Y_k, Y_{k+1} = Y_k T_k,
+// Z_{k+1} = T_k Z_k.  root_only: the last iteration forms only the square
+// root (every factor must have root32), not P, its binary16 copy or their
+// scales.  Each problem carries the counter slot of its factor (factor q's
+// matrices use slots sum_{q' < q} batch_q' + b) for chain launches.  With a
+// trace, the iterates of factor 0 are copied out between stages (per-stage
+// launches only).
 struct TraceOut {
   uint16_t* base = nullptr;  // [(3K+1)][count][d][d]
   int64_t count = 0, d = 0;
@@ -555,13 +575,256 @@ okls_status trace_copy(const TraceOut& tr, int slice, const Buf* b, cudaStream_t
   return OKLS_OK;
 }
 
-// Normalisation and the coupled Newton-Schulz chain for 1 or 2 factors.
-// The stable order is kept: M_k = Z_k Y_k, Y_{k+1} = Y_k T_k, Z_{k+1} = T_k Z_k.
-// root_only: the last iteration forms only the square root (every factor
-// must have root32), not P, its binary16 copy or their scales.
-okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
-                        int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
-                        const TraceOut* tr, bool root_only);
+template <class Sink>
+okls_status ns_stages(Factor* const* fs, int nf, const Sched& sc, int split, float* scal, int scal_ld,
+                      bool root_only, const TraceOut* tr, cudaStream_t st, Sink&& sink) {
+  const int K = sc.iters;
+  const int h = kHeadroom;
+  int slot0[2] = {0, 0};
+  for (int q = 1; q < nf; ++q) slot0[q] = slot0[q - 1] + fs[q - 1]->batch;
+  okls_status s;
+  // k = 0: Y_1 = Y_0 T_0 (Z_1 = T_0 written by the normaliser)
+  {
+    LaunchBuilder lb;
+    const bool sp = split > 0, spo = split > 1;
+    for (int q = 0; q < nf; ++q) {
+      Factor& f = *fs[q];
+      GemmProblem& p = lb.add(f.Y[0], f.T, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
+      set_out16(p, f.Y[1][0], nullptr, spo ? &f.Y[1][1] : nullptr, nullptr);
+      p.alpha = std::ldexp(1.0f, -h);
+      p.dep_slot = slot0[q];
+    }
+    if ((s = sink(lb)) != OKLS_OK) return s;
+  }
+  for (int k = 1; k < K; ++k) {
+    const int cur = k & 1, nxt = cur ^ 1;
+    const bool sp = split > k;       // operands of this iteration are pairs
+    const bool spo = split > k + 1;  // outputs feed a split iteration
+    {
+      LaunchBuilder lb;  // T_k = a_k I + b_k Z_k Y_k
+      for (int q = 0; q < nf; ++q) {
+        Factor& f = *fs[q];
+        GemmProblem& p = lb.add(f.Z[cur], f.Y[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_T, false, true);
+        set_out16(p, f.T[0], nullptr, sp ? &f.T[1] : nullptr, nullptr);
+        p.alpha = static_cast<float>(std::ldexp(sc.a[k], h));
+        p.beta = static_cast<float>(std::ldexp(sc.b[k], sc.z[k] - h));
+        p.dep_slot = slot0[q];
+      }
+      if ((s = sink(lb)) != OKLS_OK) return s;
+    }
+    if (tr && tr->base) {
+      if ((s = trace_copy(*tr, 3 * k, &fs[0]->Y[cur][0], st)) != OKLS_OK) return s;
+      if ((s = trace_copy(*tr, 3 * k + 1, &fs[0]->Z[cur][0], st)) != OKLS_OK) return s;
+      if ((s = trace_copy(*tr, 3 * k + 2, &fs[0]->T[0], st)) != OKLS_OK) return s;
+    }
+    LaunchBuilder lb;
+    for (int q = 0; q < nf; ++q) {
+      Factor& f = *fs[q];
+      if (k < K - 1) {
+        GemmProblem& py = lb.add(f.Y[cur], f.T, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
+        set_out16(py, f.Y[nxt][0], nullptr, spo ? &f.Y[nxt][1] : nullptr, nullptr);
+        py.alpha = std::ldexp(1.0f, -h);
+        py.dep_slot = slot0[q];
+        GemmProblem& pz = lb.add(f.T, f.Z[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
+        set_out16(pz, f.Z[nxt][0], nullptr, spo ? &f.Z[nxt][1] : nullptr, nullptr);
+        pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
+        pz.dep_slot = slot0[q];
+      } else {
+        if (!root_only) {
+          GemmProblem& pz = lb.add(f.T, f.Z[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_LAST, false, true);
+          // in split mode the copy of P read by the X and whitening products
+          // is a (hi, lo) pair as well
+          set_out16(pz, f.Ph[0], nullptr, f.split ? &f.Ph[1] : nullptr, nullptr);
+          pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
+          pz.out32 = f.P32;
+          pz.ld32 = f.d;
+          pz.mat32 = static_cast<int64_t>(f.d) * f.d;
+          pz.scal = scal;
+          pz.scal_ld = scal_ld;
+          pz.scal_slot = f.slot_pscale;
+          pz.pi_slot = f.slot_pi;
+          pz.cp_slot = f.slot_cprime;
+          pz.pi_exp = sc.z[K] - h;
+          pz.dep_slot = slot0[q];
+        }
+        if (f.root32) {
+          GemmProblem& pr = lb.add(f.Y[cur], f.T, sp, f.d, f.d, f.d, f.batch, EPI_ROOT, false, true);
+          pr.out32 = f.root32;
+          pr.ld32 = f.d;
+          pr.mat32 = static_cast<int64_t>(f.d) * f.d;
+          pr.scal = scal;
+          pr.scal_ld = scal_ld;
+          pr.scal_slot = f.slot_rscale;
+          pr.dep_slot = slot0[q];
+        }
+      }
+    }
+    if ((s = sink(lb)) != OKLS_OK) return s;
+  }
+  return OKLS_OK;
+}
+
+// A whole Newton-Schulz chain (its GEMM stages) as one persistent launch:
+// the problem table and the completion counters live in the workspace; the
+// table is built and uploaded once, when the handle is created (every
+// pointer and constant in it is fixed for the handle's life).
+struct ChainProgram {
+  bool ready = false;
+  GemmProblem* table = nullptr;  // device, kChainMaxProblems entries reserved
+  uint32_t* done = nullptr;      // device, [stages][nslot]
+  int nprob = 0, nstage = 0, nslot = 0;
+  int64_t total_tiles = 0;
+  double flops = 0.0;
+};
+
+constexpr int kChainMaxStages = 64;
+// Chains run for factors of at most this size; past it the per-stage
+// launches' fixed costs are small beside the products.
+constexpr int kChainMaxD = 1024;
+
+bool chain_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("OKLS_NS_CHAIN");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+size_t chain_table_bytes() { return static_cast<size_t>(kChainMaxProblems) * sizeof(GemmProblem); }
+size_t chain_done_bytes(int nslot) { return static_cast<size_t>(kChainMaxStages) * nslot * 4; }
+
+// Build the chain program of the GEMM stages for the factors `fs` and upload
+// its table (synchronously; called when the handle is created).
+okls_status build_chain(ChainProgram& cp, Factor* const* fs, int nf, const Sched& sc, int split, float* scal,
+                        int scal_ld, bool root_only, int sms) {
+  std::vector<GemmProblem> probs;
+  std::vector<std::vector<int64_t>> need;  // per stage, per factor: completions of one matrix
+  int stage = 0;
+  int64_t base = 0;
+  double flops = 0.0;
+  okls_status s = ns_stages(fs, nf, sc, split, scal, scal_ld, root_only, nullptr, nullptr, [&](LaunchBuilder& lb) {
+    double f = 0.0;
+    okls_status s0 = lb.prepare(sms, base, &f);
+    if (s0 != OKLS_OK) return s0;
+    base = lb.L.total_tiles;
+    flops += f;
+    need.emplace_back(nf, 0);
+    for (int i = 0; i < lb.L.nprob; ++i) {
+      GemmProblem p = lb.L.prob[i];
+      // factor index from the slot base
+      int q = 0, acc = 0;
+      for (; q < nf; ++q) {
+        if (p.dep_slot == acc) break;
+        acc += fs[q]->batch;
+      }
+      if (q == nf) return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: chain slot");
+      p.stage = stage;
+      p.dep_need = 0;
+      if (stage > 0) {
+        const int64_t nd = need[stage - 1][q];
+        if (nd <= 0 || nd > 0x7fffffff) return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: chain dependency");
+        p.dep_need = static_cast<int32_t>(nd);
+      }
+      need[stage][q] += 4 * p.tiles_per_mat;
+      probs.push_back(p);
+    }
+    ++stage;
+    return OKLS_OK;
+  });
+  if (s != OKLS_OK) return s;
+  if (static_cast<int>(probs.size()) > kChainMaxProblems || stage > kChainMaxStages)
+    return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: chain too long");
+  int nslot = 0;
+  for (int q = 0; q < nf; ++q) nslot += fs[q]->batch;
+  if (nslot != cp.nslot) return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: chain slots");
+  cp.nprob = static_cast<int>(probs.size());
+  cp.nstage = stage;
+  cp.total_tiles = base;
+  cp.flops = flops;
+  cudaError_t e = cudaMemcpy(cp.table, probs.data(), probs.size() * sizeof(GemmProblem), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(OKLS_ERR_CUDA, "chain table upload: %s", cudaGetErrorString(e));
+  cp.ready = true;
+  return OKLS_OK;
+}
+
+okls_status run_chain(const ChainProgram& cp, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st) {
+  OKLS_CK(cudaMemsetAsync(cp.done, 0, static_cast<size_t>(cp.nstage) * cp.nslot * 4, st));
+  ChainLaunch C;
+  memset(&C, 0, sizeof(C));
+  C.prob = cp.table;
+  C.nprob = cp.nprob;
+  C.nslot = cp.nslot;
+  C.total_tiles = cp.total_tiles;
+  C.done = cp.done;
+  C.maps = maps;
+  C.status = status;
+  C.wait_cycles = g_wait.cycles;
+  C.unloaded_tile = g_wait.unloaded_tile;
+  Prof* pf = g_prof;
+  cudaEvent_t ea = nullptr, eb = nullptr;
+  if (pf && pf->timing) {
+    ea = pf->next_event();
+    eb = pf->next_event();
+    if (ea) OKLS_CK(cudaEventRecord(ea, st));
+  }
+  OKLS_CK(launch_chain(C, sms, st));
+  if (pf) {
+    if (ea && eb) {
+      OKLS_CK(cudaEventRecord(eb, st));
+      pf->recs.push_back({ea, eb, cp.flops, true, false});
+    }
+    pf->kernels += 1;
+    pf->gemm_launches += 1;
+    pf->gemm_flops += cp.flops;
+    pf->ns_launches += 1;
+    pf->ns_flops += cp.flops;
+  }
+  return OKLS_OK;
+}
+
+// Normalisation of the factors (k_normalise: Y_0, T_0, Z_1 and, for a
+// factor-product output, S's mirrored lower triangle).
+okls_status ns_normalise(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
+                         int scal_ld, uint32_t* status, cudaStream_t st) {
+  for (int q = 0; q < nf; ++q) {
+    Factor& f = *fs[q];
+    NormaliseArgs A;
+    memset(&A, 0, sizeof(A));
+    A.S = f.S;
+    A.upper_only = f.S_upper_only ? 1 : 0;
+    A.d = f.d;
+    A.ld16 = f.Y[0][0].ld;
+    A.mat16 = f.Y[0][0].mat();
+    A.Y = f.Y[0][0].p;
+    A.T = f.T[0].p;
+    A.Z = f.Z[1][0].p;
+    A.split_y = split > 0;
+    A.split_t = split > 0;
+    A.split_z = split > 1;
+    if (A.split_y) {
+      A.Ylo = f.Y[0][1].p;
+      A.Tlo = f.T[1].p;
+    }
+    if (A.split_z) A.Zlo = f.Z[1][1].p;
+    A.a0 = static_cast<float>(sc.a[0]);
+    A.b0 = static_cast<float>(sc.b[0]);
+    A.z1 = sc.z[1];
+    A.ridge = ridge;
+    A.scal = scal;
+    A.scal_ld = scal_ld;
+    A.slot_cprime = f.slot_cprime;
+    A.slot_sumsq = f.slot_sumsq;
+    A.status = status;
+    // per element: the upper triangle of S read and its mirror written
+    // (upper-only input) or all of S read (full input); Y_0, T_0, Z_1 (and
+    // low halves) written
+    const double per = 4.0 + 6.0 + 2.0 * (A.split_y + A.split_t + A.split_z);
+    okls_status s0 = bw_launch(per * f.batch * static_cast<double>(f.d) * f.d, st,
+                               [&] { return launch_normalise(A, f.batch, st); });
+    if (s0 != OKLS_OK) return s0;
+  }
+  return OKLS_OK;
+}
 
 // Factors with d <= 128 run the whole chain in one fused on-chip kernel
 // (plain binary16 mode); OKLS_NS_SMALL=0 sends them through the general path.
@@ -573,6 +836,8 @@ bool small_enabled() {
   }();
   return on;
 }
+
+bool takes_small(const Factor& f, int split) { return split == 0 && small_enabled() && f.d <= kSmallMaxD; }
 
 okls_status run_ns_small(Factor* const* fs, int nf, const Sched& sc, float ridge, float* scal, int scal_ld,
                          uint32_t* status, cudaStream_t st, const TraceOut* tr, bool root_only) {
@@ -635,20 +900,21 @@ okls_status run_ns_small(Factor* const* fs, int nf, const Sched& sc, float ridge
   return OKLS_OK;
 }
 
+// Normalisation and the Newton-Schulz chain of 1 or 2 factors: factors with
+// d <= 128 (plain mode) in the fused kernel, the rest as one chain launch when
+// `chain` holds their program, else as one launch per stage.  A trace is
+// taken from factor 0 only, so a traced run keeps factor 0 on one path.
 okls_status run_ns(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
                    int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
-                   const TraceOut* tr, bool root_only = false) {
+                   const TraceOut* tr, bool root_only = false, const ChainProgram* chain = nullptr) {
   for (int q = 0; q < nf && root_only; ++q)
     if (!fs[q]->root32) return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: square-root output");
   if (sc.iters > kSmallMaxIters) return fail(OKLS_ERR_UNSUPPORTED, "more than %d Newton-Schulz steps", kSmallMaxIters);
-  // the small factors go to the fused kernel, the rest to the GEMM chain;
-  // a trace is taken from factor 0 only, so a traced run keeps factor 0 on
-  // one path
   Factor* small[2];
   Factor* big[2];
   int ns = 0, nb = 0;
   for (int q = 0; q < nf; ++q) {
-    if (split == 0 && small_enabled() && fs[q]->d <= kSmallMaxD)
+    if (takes_small(*fs[q], split))
       small[ns++] = fs[q];
     else
       big[nb++] = fs[q];
@@ -660,146 +926,21 @@ okls_status run_ns(Factor* const* fs, int nf, const Sched& sc, int split, float 
         OKLS_OK)
       return s;
   }
-  if (nb > 0) {
-    const bool tr_big = tr && tr->base && big[0] == fs[0];
-    g_in_ns = true;
-    s = run_ns_body(big, nb, sc, split, ridge, scal, scal_ld, maps, status, sms, st, tr_big ? tr : nullptr,
-                    root_only);
-    g_in_ns = false;
-  }
-  return s;
-}
-
-okls_status run_ns_body(Factor* const* fs, int nf, const Sched& sc, int split, float ridge, float* scal,
-                        int scal_ld, const CUtensorMap* maps, uint32_t* status, int sms, cudaStream_t st,
-                        const TraceOut* tr, bool root_only) {
-  const int K = sc.iters;
-  const int h = kHeadroom;
-  for (int q = 0; q < nf; ++q) {
-    Factor& f = *fs[q];
-    NormaliseArgs A;
-    memset(&A, 0, sizeof(A));
-    A.S = f.S;
-    A.upper_only = f.S_upper_only ? 1 : 0;
-    A.d = f.d;
-    A.ld16 = f.Y[0][0].ld;
-    A.mat16 = f.Y[0][0].mat();
-    A.Y = f.Y[0][0].p;
-
-    A.T = f.T[0].p;
-
-    A.Z = f.Z[1][0].p;
-
-    A.split_y = split > 0;
-    A.split_t = split > 0;
-    A.split_z = split > 1;
-    if (A.split_y) {
-      A.Ylo = f.Y[0][1].p;
-
-      A.Tlo = f.T[1].p;
-
-    }
-    if (A.split_z) {
-      A.Zlo = f.Z[1][1].p;
-
-    }
-    A.a0 = static_cast<float>(sc.a[0]);
-    A.b0 = static_cast<float>(sc.b[0]);
-    A.z1 = sc.z[1];
-    A.ridge = ridge;
-    A.scal = scal;
-    A.scal_ld = scal_ld;
-    A.slot_cprime = f.slot_cprime;
-    A.slot_sumsq = f.slot_sumsq;
-    A.status = status;
-    // per element: the upper triangle of S read and its mirror written
-    // (upper-only input) or all of S read (full input); Y_0, T_0, Z_1 (and
-    // low halves) written
-    const double per = 4.0 + 6.0 + 2.0 * (A.split_y + A.split_t + A.split_z);
-    okls_status s0 = bw_launch(per * f.batch * static_cast<double>(f.d) * f.d, st,
-                               [&] { return launch_normalise(A, f.batch, st); });
-    if (s0 != OKLS_OK) return s0;
-  }
-  if (tr && tr->base) {
-    okls_status s;
-    if ((s = trace_copy(*tr, 0, &fs[0]->Y[0][0], st)) != OKLS_OK) return s;
+  if (nb == 0) return OKLS_OK;
+  const bool tr_big = tr && tr->base && big[0] == fs[0];
+  if ((s = ns_normalise(big, nb, sc, split, ridge, scal, scal_ld, status, st)) != OKLS_OK) return s;
+  if (chain && chain->ready && !tr_big) return run_chain(*chain, maps, status, sms, st);
+  if (tr_big) {
+    if ((s = trace_copy(*tr, 0, &big[0]->Y[0][0], st)) != OKLS_OK) return s;
     if ((s = trace_copy(*tr, 1, nullptr, st)) != OKLS_OK) return s;
-    if ((s = trace_copy(*tr, 2, &fs[0]->T[0], st)) != OKLS_OK) return s;
+    if ((s = trace_copy(*tr, 2, &big[0]->T[0], st)) != OKLS_OK) return s;
   }
-  // k = 0: Y_1 = Y_0 T_0 (Z_1 = T_0 written by the normaliser)
-  {
-    LaunchBuilder lb;
-    const bool sp = split > 0, spo = split > 1;
-    for (int q = 0; q < nf; ++q) {
-      Factor& f = *fs[q];
-      GemmProblem& p = lb.add(f.Y[0], f.T, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
-      set_out16(p, f.Y[1][0], nullptr, spo ? &f.Y[1][1] : nullptr, nullptr);
-      p.alpha = std::ldexp(1.0f, -h);
-    }
-    okls_status s = lb.go(maps, status, sms, st);
-    if (s != OKLS_OK) return s;
-  }
-  for (int k = 1; k < K; ++k) {
-    const int cur = k & 1, nxt = cur ^ 1;
-    const bool sp = split > k;       // operands of this iteration are pairs
-    const bool spo = split > k + 1;  // outputs feed a split iteration
-    {
-      LaunchBuilder lb;  // T_k = a_k I + b_k Z_k Y_k
-      for (int q = 0; q < nf; ++q) {
-        Factor& f = *fs[q];
-        GemmProblem& p = lb.add(f.Z[cur], f.Y[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_T, false, true);
-        set_out16(p, f.T[0], nullptr, sp ? &f.T[1] : nullptr, nullptr);
-        p.alpha = static_cast<float>(std::ldexp(sc.a[k], h));
-        p.beta = static_cast<float>(std::ldexp(sc.b[k], sc.z[k] - h));
-      }
-      okls_status s = lb.go(maps, status, sms, st);
-      if (s != OKLS_OK) return s;
-    }
-    if (tr && tr->base) {
-      okls_status s;
-      if ((s = trace_copy(*tr, 3 * k, &fs[0]->Y[cur][0], st)) != OKLS_OK) return s;
-      if ((s = trace_copy(*tr, 3 * k + 1, &fs[0]->Z[cur][0], st)) != OKLS_OK) return s;
-      if ((s = trace_copy(*tr, 3 * k + 2, &fs[0]->T[0], st)) != OKLS_OK) return s;
-    }
-    LaunchBuilder lb;
-    for (int q = 0; q < nf; ++q) {
-      Factor& f = *fs[q];
-      if (k < K - 1) {
-        GemmProblem& py = lb.add(f.Y[cur], f.T, sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
-        set_out16(py, f.Y[nxt][0], nullptr, spo ? &f.Y[nxt][1] : nullptr, nullptr);
-        py.alpha = std::ldexp(1.0f, -h);
-        GemmProblem& pz = lb.add(f.T, f.Z[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_SCALE, false, true);
-        set_out16(pz, f.Z[nxt][0], nullptr, spo ? &f.Z[nxt][1] : nullptr, nullptr);
-        pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
-      } else {
-        if (!root_only) {
-          GemmProblem& pz = lb.add(f.T, f.Z[cur], sp, f.d, f.d, f.d, f.batch, EPI_NS_LAST, false, true);
-          // in split mode the copy of P read by the X and whitening products
-          // is a (hi, lo) pair as well
-          set_out16(pz, f.Ph[0], nullptr, f.split ? &f.Ph[1] : nullptr, nullptr);
-          pz.alpha = std::ldexp(1.0f, sc.z[k] - sc.z[k + 1] - h);
-          pz.out32 = f.P32;
-          pz.ld32 = f.d;
-          pz.mat32 = static_cast<int64_t>(f.d) * f.d;
-          pz.scal = scal;
-          pz.scal_ld = scal_ld;
-          pz.scal_slot = f.slot_pscale;
-        }
-        if (f.root32) {
-          GemmProblem& pr = lb.add(f.Y[cur], f.T, sp, f.d, f.d, f.d, f.batch, EPI_ROOT, false, true);
-          pr.out32 = f.root32;
-          pr.ld32 = f.d;
-          pr.mat32 = static_cast<int64_t>(f.d) * f.d;
-          pr.scal = scal;
-          pr.scal_ld = scal_ld;
-          pr.scal_slot = f.slot_rscale;
-        }
-      }
-    }
-    okls_status s = lb.go(maps, status, sms, st);
-    if (s != OKLS_OK) return s;
-  }
-  if (tr && tr->base && !root_only) return trace_copy(*tr, 3 * K, &fs[0]->Ph[0], st);
+  g_in_ns = true;
+  s = ns_stages(big, nb, sc, split, scal, scal_ld, root_only, tr_big ? tr : nullptr, st,
+                [&](LaunchBuilder& lb) { return lb.go(maps, status, sms, st); });
+  g_in_ns = false;
+  if (s != OKLS_OK) return s;
+  if (tr_big && !root_only) return trace_copy(*tr, 3 * sc.iters, &big[0]->Ph[0], st);
   return OKLS_OK;
 }
 
@@ -832,6 +973,11 @@ struct okls_handle_s {
   int64_t t = 0;
   Prof prof;
   WaitSetting wait;  // okls_set_wait_limit
+  // Newton-Schulz chains as single persistent launches (factors up to
+  // kChainMaxD): OKLS uses chain[0]; Shampoo chain[0] (square roots) and
+  // chain[1] (inverse square roots of those)
+  ChainProgram chain[2];
+  int nchain = 0;
 };
 
 namespace {
@@ -965,6 +1111,30 @@ okls_status plan_clean(const okls_config& c, uint8_t* state, uint8_t* ws, okls_h
 }
 
 // Lays out state and workspace; with bases set, fills the handle too.
+// A step's Newton-Schulz GEMM stages run as one chain launch when every
+// factor that does not take the fused small kernel has d <= kChainMaxD
+// (OKLS_NS_CHAIN=0: always one launch per stage).
+bool chain_eligible(const okls_config& c) {
+  if (!chain_enabled()) return false;
+  if (c.method != OKLS_METHOD_OKLS && c.method != OKLS_METHOD_SHAMPOO) return false;
+  const int split = c.ns_split_iters;
+  bool any = false;
+  for (int64_t d : {c.m, c.n}) {
+    if (split == 0 && small_enabled() && d <= kSmallMaxD) continue;
+    if (d > kChainMaxD) return false;
+    any = true;
+  }
+  return any;
+}
+
+// counter slots of a step's chain: the batch of each factor that runs in it
+int chain_slots(const okls_config& c) {
+  int n = 0;
+  for (int64_t d : {c.m, c.n})
+    if (!(c.ns_split_iters == 0 && small_enabled() && d <= kSmallMaxD)) n += static_cast<int>(c.batch);
+  return n;
+}
+
 okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_s* h, Layout* out) {
   const int64_t B = c.batch, m = c.m, n = c.n;
   if (c.method == OKLS_METHOD_CLEAN) return plan_clean(c, state, ws, h, out);
@@ -1049,6 +1219,14 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
   const bool split = c.ns_split_iters > 0;
   plan_factor(wp, fa, static_cast<int>(m), static_cast<int>(B), split);
   plan_factor(wp, fb, static_cast<int>(n), static_cast<int>(B), split);
+  // chain programs: the problem tables and completion counters
+  const int nchain = chain_eligible(c) ? (shampoo ? 2 : 1) : 0;
+  ChainProgram chains[2];
+  for (int i = 0; i < nchain; ++i) {
+    chains[i].nslot = chain_slots(c);
+    chains[i].table = static_cast<GemmProblem*>(wp.take(chain_table_bytes()));
+    chains[i].done = static_cast<uint32_t*>(wp.take(chain_done_bytes(chains[i].nslot)));
+  }
   if (wp.err != OKLS_OK) return wp.err;
   out->state_bytes = sp.off;
   out->ws_bytes = wp.off;
@@ -1093,6 +1271,8 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
     h->part_a_ld = pa_ld;
     h->part_b_ld = pb_ld;
     h->boxes = wp.boxes;
+    h->nchain = nchain;
+    for (int i = 0; i < nchain; ++i) h->chain[i] = chains[i];
     // upload the descriptor table once
     if (!wp.maps.empty()) {
       cudaError_t e = cudaMemcpy(maps, wp.maps.data(), wp.maps.size() * sizeof(CUtensorMap),
@@ -1326,6 +1506,44 @@ okls_status clean_step(okls_handle_s* h, void* W, const void* G, float lr, const
 
 okls_status step_impl(okls_handle h, void* W, const void* G, float lr, const float* noise, void* stream);
 
+// The factors of a step's chain: those that do not take the fused small
+// kernel, in the order run_ns hands them on.
+int chain_factor_list(Factor* const* fs, int nf, int split, Factor** out) {
+  int n = 0;
+  for (int q = 0; q < nf; ++q)
+    if (!takes_small(*fs[q], split)) out[n++] = fs[q];
+  return n;
+}
+
+// Build the handle's chain programs (once, at creation): the same factor
+// set-ups as the step's run_ns calls.
+okls_status build_chains(okls_handle_s* h) {
+  const okls_config& c = h->cfg;
+  BoxScope boxes(&h->boxes);
+  const int sld = static_cast<int>(c.batch);
+  Factor* big[2];
+  if (c.method == OKLS_METHOD_SHAMPOO) {
+    Factor ra = h->fa, rb = h->fb;
+    ra.root32 = h->sq_a;
+    rb.root32 = h->sq_b;
+    Factor* f1[2] = {&ra, &rb};
+    int nb = chain_factor_list(f1, 2, c.ns_split_iters, big);
+    okls_status s = build_chain(h->chain[0], big, nb, h->sched, c.ns_split_iters, h->scal, sld, true, h->sms);
+    if (s != OKLS_OK) return s;
+    Factor qa = h->fa, qb = h->fb;
+    qa.S = h->sq_a;
+    qa.S_upper_only = false;
+    qb.S = h->sq_b;
+    qb.S_upper_only = false;
+    Factor* f2[2] = {&qa, &qb};
+    nb = chain_factor_list(f2, 2, c.ns_split_iters, big);
+    return build_chain(h->chain[1], big, nb, h->sched, c.ns_split_iters, h->scal, sld, false, h->sms);
+  }
+  Factor* fs[2] = {&h->fa, &h->fb};
+  const int nb = chain_factor_list(fs, 2, c.ns_split_iters, big);
+  return build_chain(h->chain[0], big, nb, h->sched, c.ns_split_iters, h->scal, sld, false, h->sms);
+}
+
 }  // namespace
 
 // ================================================================== C entries
@@ -1390,6 +1608,7 @@ okls_status okls_create(const okls_config* cfg, void* state_dev, size_t state_by
   h->sms = sms;
   h->sched = make_schedule(cfg->ns_iters, cfg->ns_lo);
   s = plan(*cfg, static_cast<uint8_t*>(state_dev), static_cast<uint8_t*>(workspace_dev), h, &lay);
+  if (s == OKLS_OK && h->nchain > 0) s = build_chains(h);
   if (s != OKLS_OK) {
     delete h;
     return s;
@@ -1555,7 +1774,7 @@ okls_status step_impl(okls_handle h, void* W, const void* G, float lr, const flo
       rb.root32 = h->sq_b;
       Factor* f1[2] = {&ra, &rb};
       if ((s = run_ns(f1, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
-                      nullptr, /*root_only=*/true)) != OKLS_OK)
+                      nullptr, /*root_only=*/true, h->nchain > 0 ? &h->chain[0] : nullptr)) != OKLS_OK)
         return s;
       if ((s = bw_launch(4.0 * B * static_cast<double>(m) * m, st, [&] {
              return launch_sumsq(h->sq_a, B, static_cast<int64_t>(m) * m, h->part_a, h->part_a_ld, st);
@@ -1576,12 +1795,12 @@ okls_status step_impl(okls_handle h, void* W, const void* G, float lr, const flo
       qb.S_upper_only = false;
       Factor* f2[2] = {&qa, &qb};
       if ((s = run_ns(f2, 2, h->sched, c.ns_split_iters, 0.0f, h->scal, sld, h->maps, h->status, h->sms, st,
-                      nullptr)) != OKLS_OK)
+                      nullptr, false, h->nchain > 1 ? &h->chain[1] : nullptr)) != OKLS_OK)
         return s;
     } else {
       Factor* fs[2] = {&h->fa, &h->fb};
       if ((s = run_ns(fs, 2, h->sched, c.ns_split_iters, c.ridge, h->scal, sld, h->maps, h->status, h->sms, st,
-                      nullptr)) != OKLS_OK)
+                      nullptr, false, h->nchain > 0 ? &h->chain[0] : nullptr)) != OKLS_OK)
         return s;
     }
     OKLS_CK(launch_coeffs_post(B, c.ridge, zK, zK1, h->scal, sld, kPostCommit | kPostUpdate, h->status, nullptr, 0,

@@ -13,16 +13,16 @@ struct TileCoord {
   int64_t lt;  // tile index within its matrix
 };
 
-// Tile t of the launch's linear tile space.  Output tiles are kTileRows x 256
-// (128 x 256 for one CTA); symmetric problems keep the tiles that touch the
-// upper triangle: column block >= floor(tm * kTileRows / 256).
-template <int kTileRows>
-__device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int64_t t) {
-  constexpr int kDiv = kBN / kTileRows;
+// Tile t of the launch's linear tile space.  Output tiles are kBM x kBN
+// (128 x 256); symmetric problems keep the tiles that touch the upper
+// triangle: column block >= floor(tm * kBM / kBN).  `p` is the caller's
+// running problem index: tiles are visited in increasing order, so the
+// search only moves forward.
+__device__ __forceinline__ TileCoord decode_tile(const GemmProblem* probs, int nprob, int64_t t, int& p) {
+  constexpr int kDiv = kBN / kBM;
   TileCoord c;
-  int p = 0;
-  while (p + 1 < L.nprob && t >= L.prob[p + 1].tile_begin) ++p;
-  const GemmProblem& P = L.prob[p];
+  while (p + 1 < nprob && t >= probs[p + 1].tile_begin) ++p;
+  const GemmProblem& P = probs[p];
   // tile indices of a launch stay below 2^31 (checked on the host), so the
   // divisions run in 32 bits by multiplication
   const uint32_t local = static_cast<uint32_t>(t - P.tile_begin);

@@ -33,7 +33,25 @@
 
 namespace okls {
 
-__global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid_constant__ GemmLaunch L) {
+// The kernel body, shared by the two schedules:
+//   kChain = false  one launch of up to kMaxProblems independent problems
+//                   (okls_gemm_kernel; the problems in the parameter block);
+//   kChain = true   a chain of dependent stages in one persistent launch
+//                   (okls_chain_kernel; the problems in a device table): the
+//                   producer waits, before loading a tile of stage s > 0,
+//                   until its matrix's slot of stage s - 1 has dep_need
+//                   completions, and each epilogue warp publishes its
+//                   stores and adds one completion to its slot of stage s.
+//                   Any status bit stops the chain: later stages must not
+//                   run after a failure, as later launches skip it.
+// Tiles go to CTAs with a static stride and each CTA visits them in
+// increasing order; a tile only depends on tiles of earlier stages, which
+// have lower indices, so the lowest unfinished tile can always proceed once
+// every CTA is resident (the chain is launched cooperatively).
+template <bool kChain>
+__device__ __forceinline__ void gemm_body(const GemmProblem* probs, int nprob, int64_t total_tiles,
+                                          const CUtensorMap* maps, uint32_t* status, int64_t wait_cycles,
+                                          int64_t unloaded_tile, uint32_t* done, int nslot) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -46,10 +64,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const long long lim = L.wait_cycles > 0 ? static_cast<long long>(L.wait_cycles) : kTimeoutCycles;
+  const long long lim = wait_cycles > 0 ? static_cast<long long>(wait_cycles) : kTimeoutCycles;
+  const uint32_t abort_mask = kChain ? 0xFFFFFFFFu : kStTimeout;
 
   // An earlier stage of the step failed: leave W, S and P untouched.
-  if (threadIdx.x == 0) *skip = (*reinterpret_cast<volatile uint32_t*>(L.status) != 0u);
+  if (threadIdx.x == 0) *skip = (*reinterpret_cast<volatile uint32_t*>(status) != 0u);
   __syncthreads();
   if (*skip) return;
 
@@ -77,26 +96,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      for (int p = 0; p < L.nprob; ++p)
-        for (int s = 0; s < L.prob[p].nseg; ++s) {
-          prefetch_tmap(L.maps + L.prob[p].amap[s]);
-          prefetch_tmap(L.maps + L.prob[p].bmap[s]);
-        }
+      if (!kChain)
+        for (int p = 0; p < nprob; ++p)
+          for (int s = 0; s < probs[p].nseg; ++s) {
+            prefetch_tmap(maps + probs[p].amap[s]);
+            prefetch_tmap(maps + probs[p].bmap[s]);
+          }
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
+      int pi = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x) {
+      for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         // test hook: this tile's operands are never loaded, so its consumers'
         // waits run out with nothing of this CTA in flight
-        if (t == L.unloaded_tile) break;
-        const TileCoord tc = decode_tile<kBM>(L, t);
-        const GemmProblem& P = L.prob[tc.p];
+        if (t == unloaded_tile) break;
+        const TileCoord tc = decode_tile(probs, nprob, t, pi);
+        const GemmProblem& P = probs[tc.p];
+        if (kChain) {
+          if (*reinterpret_cast<volatile uint32_t*>(status) != 0u) break;
+          if (P.dep_need > 0) {
+            const uint32_t* ctr = done + static_cast<int64_t>(P.stage - 1) * nslot + P.dep_slot + tc.mat;
+            if (!counter_wait(ctr, static_cast<uint32_t>(P.dep_need), status, lim)) break;
+            // the operands were written by other CTAs' epilogues
+            fence_proxy_async_global();
+          }
+        }
         const int nkb = (P.K + kBK - 1) / kBK;
         for (int sg = 0; sg < P.nseg && ok; ++sg) {
-          const CUtensorMap* am = L.maps + P.amap[sg];
-          const CUtensorMap* bm = L.maps + P.bmap[sg];
+          const CUtensorMap* am = maps + P.amap[sg];
+          const CUtensorMap* bm = maps + P.bmap[sg];
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, L.status, lim)) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, status, lim, abort_mask)) {
               ok = false;
               break;
             }
@@ -128,7 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         const int64_t idx = issued - q;
         const uint32_t s = static_cast<uint32_t>(idx % kStages);
         const uint32_t ph = static_cast<uint32_t>((idx / kStages) & 1);
-        if (!mbar_wait_own(&full[s], ph, L.status)) break;
+        if (!mbar_wait_own(&full[s], ph, status)) break;
       }
     }
     __syncwarp();
@@ -149,14 +179,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
       const uint64_t bdesc0_mn = sw128_mn_desc(s0 + kStageABytes);
       constexpr uint64_t kStageDesc = kStageBytes >> 4;
       uint32_t stage = 0, phase = 0, it = 0;
+      int pi = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x, ++it) {
-        const TileCoord tc = decode_tile<kBM>(L, t);
-        const GemmProblem& P = L.prob[tc.p];
+      for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++it) {
+        const TileCoord tc = decode_tile(probs, nprob, t, pi);
+        const GemmProblem& P = probs[tc.p];
         const int nkb = ((P.K + kBK - 1) / kBK) * P.nseg;
         const uint32_t buf = it & 1u;
         const uint32_t aph = (it >> 1) & 1u;
-        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, L.status, lim)) break;
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, status, lim, abort_mask)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kBN;
         const bool half_n = P.cols - tc.tn * kBN <= kBN / 2;
@@ -165,7 +196,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         // K16 step of B: 16 rows of 128 B (MN-major) or 32 B (K-major)
         const uint64_t bstep = P.bmn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, L.status, lim)) {
+          if (!mbar_wait(&full[stage], phase, status, lim, abort_mask)) {
             ok = false;
             break;
           }
@@ -182,7 +213,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
       // all MMAs retired before TMEM is released (this thread's own MMAs:
       // the default limit, whatever the status word says)
       umma_commit(drain);
-      mbar_wait_own(drain, 0, L.status);
+      mbar_wait_own(drain, 0, status);
     }
     __syncwarp();
   } else {
@@ -191,12 +222,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
     const int row_in_tile = q * 32 + lane;
     uint32_t it = 0;
     uint32_t flags = 0;
-    for (int64_t t = blockIdx.x; t < L.total_tiles; t += gridDim.x, ++it) {
-      const TileCoord tc = decode_tile<kBM>(L, t);
-      const GemmProblem& P = L.prob[tc.p];
+    int pi = 0;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      const TileCoord tc = decode_tile(probs, nprob, t, pi);
+      const GemmProblem& P = probs[tc.p];
       const uint32_t buf = it & 1u;
       const uint32_t aph = (it >> 1) & 1u;
-      if (!mbar_wait(&acc_full[buf], aph, L.status, lim)) break;
+      if (!mbar_wait(&acc_full[buf], aph, status, lim, abort_mask)) break;
       tc_fence_after();
       const int i = tc.tm * kBM + row_in_tile;
       float sumsq = 0.0f;
@@ -213,16 +245,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid
         for (int o = 16; o > 0; o >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, o);
         if (lane == 0) P.part[static_cast<int64_t>(tc.mat) * P.part_ld + tc.lt * 4 + q] = sumsq;
       }
+      if (P.epi == EPI_NS_LAST && tc.tm == 0 && tc.tn == 0 && q == 0 && lane == 0) {
+        // the new root's scale, computed as the commit after the chain does
+        const double cp = static_cast<double>(P.scal[static_cast<int64_t>(P.cp_slot) * P.scal_ld + tc.mat]);
+        P.scal[static_cast<int64_t>(P.pi_slot) * P.scal_ld + tc.mat] = static_cast<float>(ldexp(1.0 / sqrt(cp), P.pi_exp));
+      }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
+      if (kChain) {
+        // publish this warp's stores to the other CTAs' TMA loads, then
+        // count the warp's quarter of the tile as done
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          red_release_gpu_add(done + static_cast<int64_t>(P.stage) * nslot + P.dep_slot + tc.mat, 1u);
+      }
     }
-    if (flags) atomicOr(L.status, flags);
+    if (flags) atomicOr(status, flags);
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) okls_gemm_kernel(const __grid_constant__ GemmLaunch L) {
+  gemm_body<false>(L.prob, L.nprob, L.total_tiles, L.maps, L.status, L.wait_cycles, L.unloaded_tile, nullptr, 0);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) okls_chain_kernel(const __grid_constant__ ChainLaunch C) {
+  gemm_body<true>(C.prob, C.nprob, C.total_tiles, C.maps, C.status, C.wait_cycles, C.unloaded_tile, C.done,
+                  C.nslot);
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream) {
@@ -235,6 +290,30 @@ cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream) {
   const int grid = static_cast<int>(L.total_tiles < num_sms ? L.total_tiles : num_sms);
   okls_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(L);
   return cudaGetLastError();
+}
+
+// The chain's CTAs wait on one another's tiles, so all of them must be
+// resident at once: a cooperative launch of at most one CTA per SM (the
+// kernel's shared memory admits no second one) guarantees it or fails.
+cudaError_t launch_chain(const ChainLaunch& C, int num_sms, cudaStream_t stream) {
+  static PerDevice pd;
+  const cudaError_t e = once_per_device(pd, [](int) {
+    return cudaFuncSetAttribute(okls_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  });
+  if (e != cudaSuccess) return e;
+  if (C.total_tiles <= 0) return cudaSuccess;
+  const int grid = static_cast<int>(C.total_tiles < num_sms ? C.total_tiles : num_sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, okls_chain_kernel, C);
 }
 
 }  // namespace okls

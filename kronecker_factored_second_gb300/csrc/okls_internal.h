@@ -134,6 +134,18 @@ struct GemmProblem {
   float alpha, beta, gamma, delta;  // kind-specific constants
   int32_t split_out;            // 1: also write lo halves
   int32_t check_finite;         // 1: raise kStNonfiniteIter on non-finite acc
+  // EPI_NS_LAST: the root's scale pi = 2^pi_exp / sqrt(c') is written with
+  // the root (slot pi_slot, c' from slot cp_slot) by the tile at (0, 0), so
+  // a matrix's binary16 root and its scale always change together
+  int32_t pi_slot, cp_slot, pi_exp;
+  // chain launches (okls_chain_kernel) only: the problem's stage, the
+  // completion-counter slot of its matrix 0 (a factor's matrix b uses
+  // dep_slot + b), and how many completions (4 per tile, one per epilogue
+  // warp) that slot must reach in the previous stage before a tile of this
+  // problem may load its operands (0: no dependency)
+  int32_t stage;
+  int32_t dep_slot;
+  int32_t dep_need;
 };
 
 // Division by an invariant d >= 1 for dividends n < 2^31: with
@@ -152,6 +164,24 @@ __host__ __device__ inline void fastdiv_make(uint32_t d, uint32_t* mul, uint32_t
 __host__ __device__ __forceinline__ uint32_t fastdiv(uint32_t n, uint32_t mul, uint32_t shift) {
   return static_cast<uint32_t>((static_cast<unsigned long long>(n) * mul) >> shift);
 }
+
+// A chain of dependent GEMM stages in one persistent launch: the stages'
+// problems live in a device table (stage-major, tile_begin counting through
+// all stages); a tile of stage s > 0 waits until its matrix's slot of stage
+// s - 1 has reached dep_need completions, and every epilogue warp adds one
+// completion to its slot of stage s when its stores are done.
+constexpr int kChainMaxProblems = 256;
+struct ChainLaunch {
+  const GemmProblem* prob;      // device table
+  int32_t nprob;
+  int32_t nslot;                // counter slots per stage
+  int64_t total_tiles;
+  uint32_t* done;               // [stages][nslot] completion counters, zero when the launch starts
+  const CUtensorMap* maps;
+  uint32_t* status;
+  int64_t wait_cycles;          // as GemmLaunch
+  int64_t unloaded_tile;
+};
 
 struct GemmLaunch {
   GemmProblem prob[kMaxProblems];

@@ -210,6 +210,7 @@ struct SoapLarge {
 cudaError_t soap_large_step(const SoapLarge& S, int refresh, cudaStream_t st, int* launches);
 
 cudaError_t launch_gemm(const GemmLaunch& L, int num_sms, cudaStream_t stream);
+cudaError_t launch_chain(const ChainLaunch& C, int num_sms, cudaStream_t stream);
 
 // Reductions are deterministic: kernels write per-block (or per-tile) partials
 // into fixed slots and a single thread per matrix sums them in order.

@@ -49,17 +49,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
-// false (and raises kStTimeout) when the wait expires after `limit` cycles or
-// another thread of the grid already reported a timeout.
+// false (and raises kStTimeout) when the wait expires after `limit` cycles, or
+// false at once when another thread of the grid already raised a status bit
+// of `abort_mask` (a timeout by default).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                          long long limit = kTimeoutCycles) {
+                                          long long limit = kTimeoutCycles, uint32_t abort_mask = kStTimeout) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   uint32_t n = 0;
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (((++n) & 127u) == 0u) {
-      if (*reinterpret_cast<volatile uint32_t*>(status) & kStTimeout) return false;
+      if (*reinterpret_cast<volatile uint32_t*>(status) & abort_mask) return false;
       if (clock64() - t0 > limit) {
         atomicOr(status, kStTimeout);
         return false;
@@ -78,6 +79,43 @@ __device__ __forceinline__ bool mbar_wait_own(uint64_t* bar, uint32_t parity, ui
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) {
+      atomicOr(status, kStTimeout);
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------ cross-CTA completion counters
+// Generic-proxy stores by one CTA are later read by another CTA's TMA loads
+// (the async proxy): the writer orders its stores for the async proxy
+// (fence.proxy.async) and publishes them with a release add on a counter;
+// the reader acquires the counter and fences again before issuing the copy.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *ctr >= need.  Returns false (and raises kStTimeout) after
+// `limit` cycles, or at once when another thread of the grid has already
+// reported a failure (any status bit: the producing tiles may never finish).
+__device__ __forceinline__ bool counter_wait(const uint32_t* ctr, uint32_t need, uint32_t* status,
+                                             long long limit = kTimeoutCycles) {
+  if (ld_acquire_gpu(ctr) >= need) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(ctr) >= need) return true;
+    if (*reinterpret_cast<volatile uint32_t*>(status) != 0u) return false;
     if (clock64() - t0 > limit) {
       atomicOr(status, kStTimeout);
       return false;
