@@ -504,6 +504,16 @@ def run_okls(args):
                       "unit": "matrices/s", "ms_per_step": ms2 / args.steps,
                       "tflops_dense_27": sum_over_ranks(flops_step * args.steps, ws, dev) / (ms2 / 1e3) / 1e12,
                       "gemm_tflops_executed": gt}
+    plain_line = None
+    if args.also_plain and args.split == 0 and args.method == "okls":
+        rebuild(ns_split_iters=10, ridge=0.0)
+        ms6, gt = timed()
+        plain_line = {"mode": "every iteration split (hi/lo binary16), no ridge: the root of the unridged factor "
+                              "(81 binary16 products per factor)",
+                      "value": sum_over_ranks(matrices * args.steps, ws, dev) / (ms6 / 1e3),
+                      "unit": "matrices/s", "ms_per_step": ms6 / args.steps,
+                      "tflops_dense_27": sum_over_ranks(flops_step * args.steps, ws, dev) / (ms6 / 1e3) / 1e12,
+                      "gemm_tflops_executed": gt}
     shampoo_line = None
     if args.also_shampoo and args.method == "okls":
         rebuild(ridge=args.ridge, method="shampoo", lr=args.lr, weight_decay=0.0)
@@ -651,6 +661,8 @@ def run_okls(args):
         }
         if split_line:
             line["split_mode"] = split_line
+        if plain_line:
+            line["plain_root_mode"] = plain_line
         if shampoo_line:
             line["shampoo"] = shampoo_line
         if soap_line:
@@ -683,6 +695,7 @@ def main():
     ap.add_argument("--distinct", type=int, default=4, help="distinct gradient batches kept on the device")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--also-split", type=int, default=1)
+    ap.add_argument("--also-plain", type=int, default=1)
     ap.add_argument("--also-shampoo", type=int, default=1)
     ap.add_argument("--also-soap", type=int, default=1)
     ap.add_argument("--also-clean", type=int, default=1)

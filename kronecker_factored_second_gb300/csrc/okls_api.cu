@@ -685,7 +685,7 @@ constexpr int kChainMaxD = 1024;
 bool chain_enabled() {
   static const bool on = [] {
     const char* e = getenv("OKLS_NS_CHAIN");
-    return e && e[0] == '1';
+    return !(e && e[0] == '0');
   }();
   return on;
 }
