@@ -125,8 +125,8 @@ int64_t sym_tiles(int64_t d) {
   return c;
 }
 
-// partial sums of S^2 one symmetric product writes: 4 epilogue warps per tile
-int64_t syrk_parts(int64_t d) { return 4 * sym_tiles(d); }
+// partial sums of S^2 one symmetric product writes: 8 epilogue warps per tile
+int64_t syrk_parts(int64_t d) { return 8 * sym_tiles(d); }
 
 // fixed partial slots per matrix for ||S||_F^2 (the product's tiles, or the
 // blocks of the standalone reduction)
@@ -725,7 +725,7 @@ okls_status build_chain(ChainProgram& cp, Factor* const* fs, int nf, const Sched
         if (nd <= 0 || nd > 0x7fffffff) return fail(OKLS_ERR_UNSUPPORTED, "internal plan error: chain dependency");
         p.dep_need = static_cast<int32_t>(nd);
       }
-      need[stage][q] += 4 * p.tiles_per_mat;
+      need[stage][q] += 8 * p.tiles_per_mat;
       probs.push_back(p);
     }
     ++stage;

@@ -9,8 +9,9 @@
 //                    swizzle, into a kStages-deep shared-memory ring;
 //   warp 1 / lane 0  MMA issuer: four tcgen05.mma (M128 N256 K16) per stage
 //                    into one of two 256-column TMEM accumulators;
-//   warps 2-5        epilogue: tcgen05.ld of their 32 TMEM lanes, the fused
-//                    OKLS arithmetic, global stores.
+//   warps 2-9        epilogue: tcgen05.ld of their 32 TMEM lanes and 128
+//                    of the 256 columns, the fused OKLS arithmetic, global
+//                    stores.
 // The two accumulators let the epilogue of tile i overlap the main loop of
 // tile i+1.  All waits are bounded (okls_ptx.cuh) by the launch's limit;
 // when one expires the kernel raises kStTimeout, every thread leaves its
@@ -79,7 +80,7 @@ __device__ __forceinline__ void gemm_body(const GemmProblem* probs, int nprob, i
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 128);
+      mbar_init(&acc_empty[b], 256);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -218,7 +219,11 @@ __device__ __forceinline__ void gemm_body(const GemmProblem* probs, int nprob, i
     __syncwarp();
   } else {
     // -------------------------------------------------- epilogue warps
+    // two warps per TMEM lane quarter (a warp reaches only the lanes of
+    // quarter warp % 4), each taking 128 of the tile's 256 columns: short
+    // tiles (K = 512) are bound by the epilogue, which this halves
     const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;        // which 128 of the tile's 256 columns
     const int row_in_tile = q * 32 + lane;
     uint32_t it = 0;
     uint32_t flags = 0;
@@ -233,7 +238,7 @@ __device__ __forceinline__ void gemm_body(const GemmProblem* probs, int nprob, i
       const int i = tc.tm * kBM + row_in_tile;
       float sumsq = 0.0f;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = half * 4; c < half * 4 + 4; ++c) {
         float v[32];
         tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + c * 32, v);
         epilogue_chunk(P, tc, i, tc.tn * kBN + c * 32, v, flags, sumsq);
@@ -243,9 +248,9 @@ __device__ __forceinline__ void gemm_body(const GemmProblem* probs, int nprob, i
         // slots is taken later in a fixed order, so ||S||_F is reproducible
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, o);
-        if (lane == 0) P.part[static_cast<int64_t>(tc.mat) * P.part_ld + tc.lt * 4 + q] = sumsq;
+        if (lane == 0) P.part[static_cast<int64_t>(tc.mat) * P.part_ld + tc.lt * 8 + half * 4 + q] = sumsq;
       }
-      if (P.epi == EPI_NS_LAST && tc.tm == 0 && tc.tn == 0 && q == 0 && lane == 0) {
+      if (P.epi == EPI_NS_LAST && tc.tm == 0 && tc.tn == 0 && q == 0 && half == 0 && lane == 0) {
         // the new root's scale, computed as the commit after the chain does
         const double cp = static_cast<double>(P.scal[static_cast<int64_t>(P.cp_slot) * P.scal_ld + tc.mat]);
         P.scal[static_cast<int64_t>(P.pi_slot) * P.scal_ld + tc.mat] = static_cast<float>(ldexp(1.0 / sqrt(cp), P.pi_exp));
@@ -254,7 +259,7 @@ __device__ __forceinline__ void gemm_body(const GemmProblem* probs, int nprob, i
       mbar_arrive(&acc_empty[buf]);
       if (kChain) {
         // publish this warp's stores to the other CTAs' TMA loads, then
-        // count the warp's quarter of the tile as done
+        // count the warp's eighth of the tile as done
         fence_proxy_async_global();
         __threadfence();
         __syncwarp();

@@ -39,7 +39,7 @@ constexpr int kStages = 4;      // smem ring depth
 constexpr int kStageABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kStageBBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kStageBytes = kStageABytes + kStageBBytes;
-constexpr int kGemmThreads = 192;             // warp0 TMA, warp1 MMA, warps2-5 epilogue
+constexpr int kGemmThreads = 320;             // warp0 TMA, warp1 MMA, warps2-9 epilogue
 constexpr int kTmemCols = 512;                // two 256-column fp32 accumulators
 constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int kMaxProblems = 6;
@@ -140,7 +140,7 @@ struct GemmProblem {
   int32_t pi_slot, cp_slot, pi_exp;
   // chain launches (okls_chain_kernel) only: the problem's stage, the
   // completion-counter slot of its matrix 0 (a factor's matrix b uses
-  // dep_slot + b), and how many completions (4 per tile, one per epilogue
+  // dep_slot + b), and how many completions (8 per tile, one per epilogue
   // warp) that slot must reach in the previous stage before a tile of this
   // problem may load its operands (0: no dependency)
   int32_t stage;
