@@ -262,7 +262,15 @@ okls_status okls_reset_state(okls_handle h, void *stream);
  * run their whole Newton-Schulz chain in one fused launch, one CTA per
  * matrix: there a matrix whose chain overflowed keeps its previous root,
  * while the other matrices of that launch commit their new roots; a root
- * and its scale are always committed together.
+ * and its scale are always committed together.  Factors of 129 to 1024
+ * rows run the chain's 19 GEMM stages as one persistent launch whose tiles
+ * wait on per-matrix completion counters in the workspace; it is a
+ * cooperative launch (all its CTAs, one per SM, resident at once), and it
+ * stops at the first status bit, so after a failure inside it some
+ * matrices may already hold their new root (with its scale) and others the
+ * previous one.  Larger factors run one launch per stage.  The environment
+ * variable OKLS_NS_CHAIN=0, read once per process, selects one launch per
+ * stage for every size (the results are bit-identical).
  */
 okls_status okls_step(okls_handle h, void *W_dev, const void *G_dev, float lr,
                       void *stream);
