@@ -140,16 +140,24 @@ typedef enum okls_state_part {
  *                   t % root_every == 0 Q_L, Q_R <- eigenvectors of L, R
  *                   (decreasing eigenvalues, signs aligned with the previous
  *                   basis); eps is Adam's.  Q = I before the first refresh.
- *                   This build runs SOAP for m, n <= 544 (fp32 throughout,
- *                   cyclic Jacobi eigensolver warm-started from the previous
- *                   basis; one CTA per matrix up to 128 x 128, batched fp32
- *                   GEMMs past that).  On the batched path the workspace
- *                   holds, per matrix, three m x n and one max(mn, m^2, n^2)
- *                   fp32 buffers, four fp32 buffers of m^2 + n^2, and for
- *                   each side d > 128 an eigensolver slice of about 3 d^2
- *                   floats.  OKLS_SOAP_LARGE=1 selects that path for every
- *                   shape, and OKLS_EIG_CTAS=c caps the eigensolver's CTAs
- *                   per matrix.  Larger shapes return OKLS_ERR_UNSUPPORTED.
+ *                   This build runs SOAP for m, n <= 16384 (fp32
+ *                   throughout; the eigensolver is warm-started from the
+ *                   previous basis: cyclic Jacobi in one CTA per matrix up
+ *                   to 128 x 128, batched fp32 GEMMs past that, with a
+ *                   logged-rotation Jacobi for sides up to 544 and a
+ *                   blocked Jacobi (64 x 64 pair subproblems, rotations
+ *                   applied as fp32 panel products) past 544).  On the
+ *                   batched path the workspace holds, per matrix, three
+ *                   m x n and one max(mn, m^2, n^2) fp32 buffers, and per
+ *                   side d two d x d buffers plus, for d <= 544, two more
+ *                   and (d > 128) an eigensolver slice of about 3 d^2
+ *                   floats, or, past 544, a blocked-Jacobi slice of about
+ *                   4 kp^2 floats (kp = d rounded up to a multiple of 64).
+ *                   OKLS_SOAP_LARGE=1 selects the batched path for every
+ *                   shape, OKLS_SOAP_BLOCKED=1 the blocked solver for every
+ *                   side past 128, and OKLS_EIG_CTAS=c caps the
+ *                   logged-rotation solver's CTAs per matrix.  Larger
+ *                   shapes return OKLS_ERR_UNSUPPORTED.
  *                   OKLS_METHOD_CLEAN (Clean page, Algorithm 1 with the
  *                   sketch of Eqn. (8) and Appendix A, Algorithm 3): at
  *                   steps t = 1, 1+T, 1+2T, ... (T = root_every) U_L,

@@ -994,6 +994,15 @@ bool soap_large_path(const okls_config& c) {
   return c.m > 128 || c.n > 128;
 }
 
+// A SOAP side's refresh runs the blocked Jacobi solver past the logged-rotation
+// solver's range, or past 128 with OKLS_SOAP_BLOCKED=1 (tests run the blocked
+// solver at sizes the oracle finishes quickly).
+bool soap_blocked_side(int64_t d) {
+  if (d > kClMaxK) return true;
+  const char* e = getenv("OKLS_SOAP_BLOCKED");
+  return e && e[0] == '1' && d > 128;
+}
+
 // Clean runs one CTA per factor while a factor's panels fit its shared
 // memory (m, n <= 128, r + p <= 64); past that, or with OKLS_CLEAN_LARGE=1,
 // the batched-GEMM path.
@@ -1166,12 +1175,20 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
       sl.Gp = f32(B * m * n);
       sl.Mp = f32(B * m * n);
       sl.T = f32(B * big);
-      sl.Qh = f32(B * (m * m + n * n));
-      sl.A = f32(B * (m * m + n * n));
-      sl.P = f32(B * (m * m + n * n));
-      sl.Wq = f32(B * (m * m + n * n));
-      sl.KKL = m > 128 ? f32(B * static_cast<int64_t>(eig_scratch_floats(static_cast<int>(m)))) : nullptr;
-      sl.KKR = n > 128 ? f32(B * static_cast<int64_t>(eig_scratch_floats(static_cast<int>(n)))) : nullptr;
+      for (int side = 0; side < 2; ++side) {
+        const int64_t d = side == 0 ? m : n;
+        SoapSideBufs& sb = side == 0 ? sl.sideL : sl.sideR;
+        sb.blocked = soap_blocked_side(d) ? 1 : 0;
+        sb.Qh = f32(B * d * d);
+        sb.A = f32(B * d * d);
+        if (sb.blocked) {
+          sb.BJ = f32(B * static_cast<int64_t>(bj_scratch_floats(static_cast<int>(d))));
+        } else {
+          sb.P = f32(B * d * d);
+          sb.Wq = f32(B * d * d);
+          if (d > 128) sb.KK = f32(B * static_cast<int64_t>(eig_scratch_floats(static_cast<int>(d))));
+        }
+      }
     }
     out->state_bytes = sp.off;
     out->ws_bytes = wp.off;
@@ -1323,9 +1340,8 @@ okls_status validate(const okls_config* c) {
     return fail(OKLS_ERR_INVALID_ARG, "rank, oversample and power_iters are Clean's; leave them zero");
   }
   if (c->method == OKLS_METHOD_SOAP && (c->m > kSoapLargeMax || c->n > kSoapLargeMax))
-    return fail(OKLS_ERR_UNSUPPORTED,
-                "SOAP runs for m, n <= %d in this build (one-CTA Jacobi eigensolver); %lld x %lld needs a blocked one",
-                kSoapLargeMax, static_cast<long long>(c->m), static_cast<long long>(c->n));
+    return fail(OKLS_ERR_UNSUPPORTED, "SOAP runs for m, n <= %d in this build; got %lld x %lld", kSoapLargeMax,
+                static_cast<long long>(c->m), static_cast<long long>(c->n));
   for (int i = 0; i < 3; ++i)
     if (c->reserved[i] != 0) return fail(OKLS_ERR_INVALID_ARG, "reserved fields must be zero");
   return OKLS_OK;
@@ -1377,9 +1393,8 @@ okls_status soap_step(okls_handle_s* h, void* W, const void* G, float lr, cudaSt
     S.bc1 = A.bc1;
     S.bc2 = A.bc2;
     S.max_sweeps = 15;
-    // the off-diagonal that fp32 rotations leave grows like 2^-24 sqrt(d) of
-    // the matrix: the stopping rule keeps above that floor
-    S.tol2 = 1e-12f * std::max(1.0f, static_cast<float>(std::max(c.m, c.n)) / 128.0f);
+    // one rule for the sides solved together; a blocked side takes its own
+    S.tol2 = soap_tol2(std::max(c.m, c.n));
     int launches = 0;
     OKLS_CK(soap_large_step(S, t1 % every == 0, st, &launches));
     note_kernels(launches);

@@ -189,8 +189,38 @@ cudaError_t launch_cl_prep(const void* G, int g_bf16, float* out, int64_t mn, in
                            cudaStream_t st);
 cudaError_t clean_large_step(const ClLarge& L, cudaStream_t st, int* launches);
 
-// SOAP for m, n <= kSoapLargeMax on the batched GEMM (okls_soap_large.cu).
-constexpr int kSoapLargeMax = kClMaxK;
+// Blocked Jacobi for the SOAP refresh of sides past kClMaxK (okls_bjacobi.cu):
+// diagonalises the symmetric part of A (= Qh^T F Qh) and writes Qout = Qh W,
+// columns by decreasing eigenvalue, each column's sign making its product
+// with the same column of Qprev >= 0.  Qout may be Qprev.
+struct BjSide {
+  const float* A;      // count x d x d
+  const float* Qh;     // count x d x d
+  const float* Qprev;  // count x d x d
+  float* Qout;         // count x d x d
+  float* scratch;      // count x bj_scratch_floats(d), 16-byte aligned
+  int d, count;        // d > 64
+};
+size_t bj_scratch_floats(int d);
+cudaError_t launch_bjacobi(const BjSide& S, int max_sweeps, float tol2, uint32_t* status, cudaStream_t st,
+                           int* launches);
+
+// SOAP past one CTA on the batched GEMM (okls_soap_large.cu): m, n up to
+// kSoapLargeMax; a side's eigensolve runs in shared memory up to 128, by
+// logged rotations up to kClMaxK and by blocked Jacobi past that.
+constexpr int kSoapLargeMax = 16384;
+// The eigensolvers' stopping rule for a d x d factor: the off-diagonal's
+// squared norm at most this times the diagonal's.  The off-diagonal that fp32
+// rotations leave grows like 2^-24 sqrt(d) of the matrix, so the rule keeps
+// above that floor.
+inline float soap_tol2(int64_t d) { return 1e-12f * (d > 128 ? static_cast<float>(d) / 128.0f : 1.0f); }
+struct SoapSideBufs {
+  float *Qh, *A;  // batch x d x d each
+  float *P, *Wq;  // batch x d x d each (sides up to kClMaxK)
+  float* KK;      // eigensolver scratch for 128 < d <= kClMaxK: batch x eig_scratch_floats(d)
+  float* BJ;      // blocked Jacobi scratch (blocked sides): batch x bj_scratch_floats(d)
+  int blocked;    // the side's refresh runs the blocked solver
+};
 struct SoapLarge {
   int batch, m, n;
   const void* G;
@@ -203,9 +233,7 @@ struct SoapLarge {
   uint32_t* status;
   float *Gf, *Gp, *Mp;                  // workspace: m x n each
   float* T;                             // max(m n, m^2, n^2)
-  float *Qh, *A, *P, *Wq;               // batch (m^2 + n^2) each: side L, then side R
-  float *KKL, *KKR;                     // eigensolver scratch of a side with d > 128:
-                                        // batch x eig_scratch_floats(d)
+  SoapSideBufs sideL, sideR;
 };
 cudaError_t soap_large_step(const SoapLarge& S, int refresh, cudaStream_t st, int* launches);
 

@@ -1,5 +1,5 @@
-// SOAP for m, n up to 544 (sm_103a): the one-CTA kernels' method on batched
-// fp32 GEMMs.
+// SOAP past one CTA (sm_103a): the one-CTA kernels' method on batched fp32
+// GEMMs, for m, n up to 16384.
 //
 // Page "Clean: Second-order LLM Training at Linear Memory Cost via Nystrom
 // Sketching", Appendix C, Algorithm 4 (SOAP), with the KPOP page's section on
@@ -10,9 +10,9 @@
 // (after steps t with t % root_every == 0) warm-starts from the previous
 // basis Q as the one-CTA kernel does: Q^ = Q (3 I - Q^T Q)/2, then the
 // eigenvectors of Q^^T L Q^ by cyclic Jacobi (in shared memory up to d = 128;
-// past it the logged-rotation solver of okls_eig.cu, both sides in one set of
-// launches), ordered by decreasing eigenvalue and sign-aligned with Q, and
-// Q <- Q^ W.
+// up to 544 the logged-rotation solver of okls_eig.cu, both sides in one set
+// of launches; past that the blocked Jacobi of okls_bjacobi.cu), ordered by
+// decreasing eigenvalue and sign-aligned with Q, and Q <- Q^ W.
 #include <cuda_bf16.h>
 
 #include "okls_internal.h"
@@ -129,55 +129,58 @@ struct SlRun {
   }
 };
 
-// Buffers of one side of the refresh: the side's slices of Qh, A, P, Wq.
+// One side of the refresh: the factor, the basis and the side's buffers.
 struct SlSide {
   const float* F;  // the factor (d x d, state)
   float* Q;        // the basis (d x d, state)
   int d;
-  float *Qh, *A, *P, *Wq, *KK;
+  const SoapSideBufs* buf;
 };
 
-// Q^ = Q (1.5 I - 0.5 Q^T Q);  A = Q^^T F Q^;  P = Q^^T Q (for the signs)
+// Q^ = Q (1.5 I - 0.5 Q^T Q);  A = Q^^T F Q^;  P = Q^^T Q (for the signs; the
+// blocked solver takes them from Q directly).  The blocked side keeps no P:
+// T holds Q^T Q for the polar step.
 void sl_refresh_prep(SlRun& R, const SlSide& s) {
   const SoapLarge& S = R.S;
+  const SoapSideBufs& B = *s.buf;
   const int d = s.d;
   const int64_t sd = static_cast<int64_t>(d) * d;
-  R.gemm(s.Q, 1, d, sd, s.Q, 0, d, sd, s.P, d, sd, d, d, d);
-  R.launch([&] { k_sl_polar<<<sl_grid(sd, S.batch), 256, 0, R.st>>>(s.P, d); });
-  R.gemm(s.Q, 0, d, sd, s.P, 0, d, sd, s.Qh, d, sd, d, d, d);
-  R.gemm(s.F, 0, d, sd, s.Qh, 0, d, sd, S.T, d, sd, d, d, d);
-  R.gemm(s.Qh, 1, d, sd, S.T, 0, d, sd, s.A, d, sd, d, d, d);
-  R.gemm(s.Qh, 1, d, sd, s.Q, 0, d, sd, s.P, d, sd, d, d, d);
+  float* QtQ = B.blocked ? S.T : B.P;
+  R.gemm(s.Q, 1, d, sd, s.Q, 0, d, sd, QtQ, d, sd, d, d, d);
+  R.launch([&] { k_sl_polar<<<sl_grid(sd, S.batch), 256, 0, R.st>>>(QtQ, d); });
+  R.gemm(s.Q, 0, d, sd, QtQ, 0, d, sd, B.Qh, d, sd, d, d, d);
+  R.gemm(s.F, 0, d, sd, B.Qh, 0, d, sd, S.T, d, sd, d, d, d);
+  R.gemm(B.Qh, 1, d, sd, S.T, 0, d, sd, B.A, d, sd, d, d, d);
+  if (!B.blocked) R.gemm(B.Qh, 1, d, sd, s.Q, 0, d, sd, B.P, d, sd, d, d, d);
 }
 
 // Q <- Q^ W (skipped once the status word is set)
 void sl_refresh_finish(SlRun& R, const SlSide& s) {
   const int d = s.d;
   const int64_t sd = static_cast<int64_t>(d) * d;
-  R.gemm(s.Qh, 0, d, sd, s.Wq, 0, d, sd, s.Q, d, sd, d, d, d, 1.0f, 0.0f, R.S.status);
+  R.gemm(s.buf->Qh, 0, d, sd, s.buf->Wq, 0, d, sd, s.Q, d, sd, d, d, d, 1.0f, 0.0f, R.S.status);
 }
 
 EigSide eig_side(const SoapLarge& S, const SlSide& s) {
   EigSide e{};
-  e.A = s.A;
-  e.P = s.P;
-  e.W = s.Wq;
-  e.scratch = s.KK;
+  e.A = s.buf->A;
+  e.P = s.buf->P;
+  e.W = s.buf->Wq;
+  e.scratch = s.buf->KK;
   e.k = s.d;
   e.r = s.d;
   e.count = S.batch;
   return e;
 }
 
-// Both sides' bases: the eigen-decompositions of both sides go out in one
-// set of launches where both are past 128 (each is one CTA per matrix, so
-// this doubles the SMs at work).
+// Both sides' bases: where both are in the logged-rotation solver's range
+// their eigen-decompositions go out in one set of launches (each is one CTA
+// per matrix, so this doubles the SMs at work); a blocked side runs its own
+// rounds and writes its basis itself.
 void sl_refresh(SlRun& R) {
   const SoapLarge& S = R.S;
-  const int64_t mm = static_cast<int64_t>(S.m) * S.m;
-  const int64_t off = static_cast<int64_t>(S.batch) * mm;
-  const SlSide sL{S.L, S.QL, S.m, S.Qh, S.A, S.P, S.Wq, S.KKL};
-  const SlSide sR{S.R, S.QR, S.n, S.Qh + off, S.A + off, S.P + off, S.Wq + off, S.KKR};
+  const SlSide sL{S.L, S.QL, S.m, &S.sideL};
+  const SlSide sR{S.R, S.QR, S.n, &S.sideR};
   sl_refresh_prep(R, sL);
   sl_refresh_prep(R, sR);
   EigPlan plan{};
@@ -186,18 +189,28 @@ void sl_refresh(SlRun& R) {
   plan.status = S.status;
   int nside = 0;
   for (const SlSide* s : {&sL, &sR}) {
-    if (s->d > 128) {
+    if (R.err != cudaSuccess) break;
+    const SoapSideBufs& B = *s->buf;
+    if (B.blocked) {
+      BjSide bj{};
+      bj.A = B.A;
+      bj.Qh = B.Qh;
+      bj.Qprev = s->Q;
+      bj.Qout = s->Q;
+      bj.scratch = B.BJ;
+      bj.d = s->d;
+      bj.count = S.batch;
+      R.err = launch_bjacobi(bj, S.max_sweeps, soap_tol2(s->d), S.status, R.st, R.launches);
+    } else if (s->d > 128) {
       plan.side[nside++] = eig_side(S, *s);
     } else {
-      if (R.err == cudaSuccess) {
-        R.err = launch_cl_eig(s->A, s->P, s->Wq, nullptr, s->d, S.batch, S.max_sweeps, S.tol2, S.status, R.st);
-        ++*R.launches;
-      }
+      R.err = launch_cl_eig(B.A, B.P, B.Wq, nullptr, s->d, S.batch, S.max_sweeps, S.tol2, S.status, R.st);
+      ++*R.launches;
     }
   }
   if (nside > 0 && R.err == cudaSuccess) R.err = launch_eig_rounds(plan, R.st, R.launches);
-  sl_refresh_finish(R, sL);
-  sl_refresh_finish(R, sR);
+  if (!S.sideL.blocked) sl_refresh_finish(R, sL);
+  if (!S.sideR.blocked) sl_refresh_finish(R, sR);
 }
 
 }  // namespace

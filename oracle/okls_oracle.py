@@ -640,7 +640,8 @@ def soap_step(state: SoapState, W: np.ndarray, G: np.ndarray, lr: float, beta1: 
 # (the update), Appendix A Algorithm 3 (warm-started Nystrom with subspace
 # iteration).  Readings:
 #   c1  Algorithm 3 orthonormalises the starting sketch in both branches
-#       (warm start [U_prev, Psi] and cold start): the listing's line 5 QR.
+#       (warm start [U_prev, Psi] and cold start) with a thin QR before the
+#       power iterations.
 #   c2  eps(x) is the spacing of binary64 numbers at x: 2^(floor(log2 x) - 52);
 #       norm(Y, 2) is the spectral norm.
 #   c3  Y_nu / C is right division, Y_nu C^-1, with C the upper Cholesky

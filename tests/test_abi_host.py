@@ -128,14 +128,16 @@ def test_method_is_validated_and_sizes_the_workspace(lib):
 
 def test_soap_shapes_and_state(lib):
     """SOAP keeps M, L, R, Q_L, Q_R and V in the state and needs no binary16
-    workspace; this build takes m, n <= 544 (one CTA per matrix up to 128)."""
+    workspace; this build takes m, n <= 16384 (one CTA per matrix up to 128)."""
     c = L.config_default(3, 128, 64)
     c.method = L.METHOD_SOAP
     s, w = L.state_bytes(c)
     assert s >= 4 * 3 * (2 * 128 * 64 + 2 * 128 * 128 + 2 * 64 * 64)
     assert w < 1 << 20
-    c.m = 545
+    c.m = 16385
     assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_ERR_UNSUPPORTED
+    c.m = 16384
+    assert lib.okls_state_bytes(ctypes.byref(c), None, None) == L.OKLS_OK
     # past 128 the batched-GEMM path adds its workspace
     c.m = 300
     s2, w2 = L.state_bytes(c)
@@ -144,11 +146,13 @@ def test_soap_shapes_and_state(lib):
 
 def test_soap_batched_path_workspace(lib):
     """The SOAP batched path's workspace is what the header documents: per
-    matrix three m x n and one max(mn, m^2, n^2) fp32 buffers, four of
-    m^2 + n^2, and for each side d > 128 an eigensolver slice of A (full,
-    dp x dp with dp = d rounded up to even), V (d x d) and one sweep's
-    rotation log ((dp - 1) x dp floats).  The fixed part (descriptor table,
-    scalars, status word, alignment) stays under 1 MiB."""
+    matrix three m x n and one max(mn, m^2, n^2) fp32 buffers, and per side
+    d two d x d buffers; up to d = 544 two more and, for d > 128, an
+    eigensolver slice of A (full, dp x dp with dp = d rounded up to even), V
+    (d x d) and one sweep's rotation log ((dp - 1) x dp floats); past 544 the
+    blocked Jacobi slice (four kp x kp buffers, kp = d rounded up to 64, the
+    pair rotations and small per-position arrays).  The fixed part
+    (descriptor table, scalars, status word, alignment) stays under 1 MiB."""
     def r4(x):
         return (x + 3) // 4 * 4
 
@@ -156,12 +160,23 @@ def test_soap_batched_path_workspace(lib):
         dp = d + (d & 1)
         return r4(dp * dp) + r4(d * d) + r4((dp - 1) * dp) + 4
 
-    for B, m, n in [(2, 544, 331), (3, 300, 100), (1, 129, 544)]:
+    def blocked(d):
+        # A and A P, the basis panels (two), pair rotations, flags and
+        # per-position arrays, the stopping rule's partials
+        kp = (d + 63) // 64 * 64
+        return 4 * kp * kp + (kp // 64) * 64 * 64 + r4(kp // 64) + 4 * r4(kp) + 4 * 32 + 4
+
+    for B, m, n in [(2, 544, 331), (3, 300, 100), (1, 129, 544), (2, 600, 100), (1, 2048, 5504), (1, 545, 700)]:
         c = L.config_default(B, m, n)
         c.method = L.METHOD_SOAP
         _s, w = L.state_bytes(c)
-        floats = B * (3 * m * n + max(m * n, m * m, n * n) + 4 * (m * m + n * n))
-        floats += sum(B * eig(d) for d in (m, n) if d > 128)
+        floats = B * (3 * m * n + max(m * n, m * m, n * n))
+        for d in (m, n):
+            floats += B * 2 * d * d
+            if d > 544:
+                floats += B * blocked(d)
+            else:
+                floats += B * 2 * d * d + (B * eig(d) if d > 128 else 0)
         assert 4 * floats <= w <= 4 * floats + (1 << 20), (B, m, n, w, 4 * floats)
 
 

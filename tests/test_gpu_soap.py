@@ -1,5 +1,7 @@
-"""GPU parity of the SOAP mode (okls_config.method = SOAP, m, n <= 544)
-against the float64 oracle, through the C ABI.
+"""GPU parity of the SOAP mode (okls_config.method = SOAP) against the
+float64 oracle, through the C ABI: the one-CTA kernels, the batched path with
+the logged-rotation eigensolver (sides up to 544) and with the blocked Jacobi
+(past 544, or forced past 128).
 
 Teacher-forced: every step starts the oracle from the GPU's own state
 (M, V, L, R, Q_L, Q_R).  Bars: M, V, L, R to 1e-5 (fp32 arithmetic), the step
@@ -104,6 +106,21 @@ def test_large_path_fewer_ctas_per_matrix(B, m, n, dtype, ctas, monkeypatch):
     _teacher_forced(B, m, n, dtype)
 
 
+# the blocked Jacobi refresh (sides past 544; forced past 128 here so that the
+# oracle stays quick): padded sides (140 -> 192, 340 -> 384, 600 -> 640), a
+# side of 64-multiple size, and one that stays on the one-CTA solver
+@pytest.mark.parametrize("B,m,n,dtype,force", [(2, 200, 150, torch.float32, True),
+                                               (1, 300, 140, torch.float32, True),
+                                               (1, 160, 340, torch.bfloat16, True),
+                                               (1, 600, 100, torch.float32, False),
+                                               (1, 576, 640, torch.float32, False)])
+def test_teacher_forced_steps_blocked_solver(B, m, n, dtype, force, monkeypatch):
+    monkeypatch.setenv("OKLS_SOAP_LARGE", "1")
+    if force:
+        monkeypatch.setenv("OKLS_SOAP_BLOCKED", "1")
+    _teacher_forced(B, m, n, dtype)
+
+
 def _teacher_forced(B, m, n, dtype):
     lr, b1, b2, eps, f = 0.01, 0.9, 0.95, 1e-8, 2
     ob = _batch(B, m, n, param_dtype=dtype, lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=0.0, root_every=f)
@@ -188,3 +205,78 @@ def test_optimizer_class_matches_the_batch_api():
     torch.cuda.synchronize()
     assert torch.equal(p.detach(), W)
     ob.close()
+
+
+def _snap_one(ob, b):
+    torch.cuda.synchronize()
+    return {k: ob.get_state(p)[b].double().cpu().numpy() for k, p in PARTS}
+
+
+@pytest.mark.parametrize("gi", [0, 1, 2])
+def test_full_size_layer_shapes(gi):
+    """SOAP on the 1.2B-shaped layer set's shape groups at full size (2048^2,
+    5504 x 2048 and 2048 x 5504, bf16 W and G; one layer's batch of each):
+    four steps with a refresh every two, so that the first refresh starts
+    from the identity and the second from the previous bases.  One matrix per
+    group is checked teacher-forced at every step (M, V, L, R, N) and at the
+    refreshes its bases (orthogonality, diagonalisation, order, signs and the
+    gapped eigenvectors against float64 eigenvectors of the GPU's L, R), with
+    the bars of the smaller shapes (sqrt(d / 128) where they grow with d; the
+    diagonalisation bar, 1e-5 up to d = 2048, grows like d past it)."""
+    from kronecker_factored_second_gb300.okls import OklsBatch
+    from kronecker_factored_second_gb300.workloads import GradientStream, workload
+    import time
+
+    wl = workload("llama1.2b", layers=1)
+    g = wl.groups[gi]
+    gs = GradientStream(wl, "cuda")
+    lr, b1, b2, eps, f = 0.01, 0.95, 0.95, 1e-8, 2
+    ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, method="soap", lr=lr, beta1=b1, beta2=b2, eps=eps,
+                   weight_decay=0.0, root_every=f)
+    W = gs.init_weights(gi)
+    b = g.batch - 1
+    m, n = g.m, g.n
+    worst = {}
+    for t in range(1, 5):
+        pre = _snap_one(ob, b)
+        Wp = W[b].double().cpu().numpy()
+        G = gs.grad(gi, t)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        ob.step(W, G, lr)
+        assert ob.query_status() == 0
+        torch.cuda.synchronize()
+        dt = time.time() - t0
+        post = _snap_one(ob, b)
+        Wn = W[b].double().cpu().numpy()
+        Gd = G[b].double().cpu().numpy()
+        st = O.SoapState(M=pre["M"], V=pre["V"], L=pre["L"], R=pre["R"], QL=pre["QL"], QR=pre["QR"], t=t - 1)
+        # the oracle's own refresh is not needed here: the bases are checked
+        # against float64 eigenvectors of the GPU's factors below
+        ost, _Wo, No = O.soap_step(st, Wp, Gd, lr, b1, b2, eps, 10 ** 9)
+        err = {k: O.rel_fro(post[k], getattr(ost, k)) for k in ("M", "V", "L", "R")}
+        err["N"] = O.rel_fro((Wp - Wn) / lr, No)
+        if t % f == 0:
+            for side, S in (("QL", post["L"]), ("QR", post["R"])):
+                ref = O.eigenvectors_aligned(S, pre[side])
+                for k, v in _check_basis(post[side], S, pre[side], ref).items():
+                    err[side + "_" + k] = v
+        print(f"soap {g.name} {m}x{n} t={t} step {dt * 1e3:.0f} ms", {k: f"{v:.1e}" for k, v in err.items()})
+        for k, v in err.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    ob.close()
+    for k in ("M", "V", "L", "R"):
+        assert worst[k] < 1e-5, (k, worst)
+    # bf16 parameters round the new W to 8 bits
+    assert worst["N"] < 2e-2, worst
+    for side in ("QL", "QR"):
+        grow = max(1.0, (m if side == "QL" else n) / 128) ** 0.5
+        # the diagonalisation bar grows with d past 2048: the blocked solver
+        # tracks Q^T L Q through sweeps of d / 32 - 1 rounds of 64-deep fp32
+        # panel products, whose rounding adds up round after round (measured
+        # 6-7e-6 at d = 2048, 1.3-2.1e-5 at d = 5504); the eigenvector bar
+        # below keeps its sqrt(d / 128) growth
+        d = m if side == "QL" else n
+        assert worst[side + "_orth"] < 1e-5 * grow and worst[side + "_offdiag"] < 1e-5 * max(1.0, d / 2048), worst
+        assert worst[side + "_order"] < 1e-6 and worst[side + "_sign"] == 0.0, worst
+        assert worst[side + "_vec_gap"] < 2e-6 * grow, worst
