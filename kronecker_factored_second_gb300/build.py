@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libokls.so")
 SOURCES = ["okls_api.cu", "okls_gemm.cu", "okls_elementwise.cu", "okls_ns_small.cu",
            "okls_soap.cu", "okls_clean.cu", "okls_clean_large.cu",
-           "okls_soap_large.cu", "okls_eig.cu", "okls_bjacobi.cu"]
+           "okls_soap_large.cu", "okls_eig.cu", "okls_bjacobi.cu", "okls_tc3.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -180,6 +180,7 @@ cudaError_t launch_cl_gemm(const ClGemm& g0, cudaStream_t st) {
   ClGemm g = g0;
   g.a_vec = cl_vec_ok(g.A, g.a_bf16, g.lda, g.sA);
   g.b_vec = cl_vec_ok(g.B, g.b_bf16, g.ldb, g.sB);
+  if (t3_gemm_eligible(g)) return launch_t3_gemm(g, st);
   const dim3 grid((g.N + kGM - 1) / kGM, (g.M + kGM - 1) / kGM, g.batch);
   if (g.a_bf16 && g.b_bf16)
     k_cl_gemm<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(g);
@@ -770,6 +771,7 @@ struct ClRun {
     g.alpha = alpha;
     g.beta = beta;
     g.beta_dev = beta_dev;
+    g.status = L.status;
     err = launch_cl_gemm(g, st);
     ++*launches;
   }

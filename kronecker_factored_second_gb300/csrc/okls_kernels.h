@@ -126,8 +126,13 @@ struct ClGemm {
   const float* beta_dev;  // per-batch beta when not null
   int a_vec, b_vec;       // set by launch_cl_gemm: 16-byte loads allowed
   const uint32_t* status_guard;  // not null: skip the launch once the status word is set
+  uint32_t* status;       // not null: the tensor-core path may run (its bounded waits report here)
 };
+// fp32 products: on the tensor cores (okls_tc3.cu, three-term bf16 split)
+// where t3_gemm_eligible holds, else on the CUDA cores (k_cl_gemm).
 cudaError_t launch_cl_gemm(const ClGemm& g, cudaStream_t st);
+bool t3_gemm_eligible(const ClGemm& g);
+cudaError_t launch_t3_gemm(const ClGemm& g, cudaStream_t st);
 
 // Device buffers of the large Clean path; every array is batch-strided.
 struct ClLarge {

@@ -117,6 +117,7 @@ struct SlRun {
     g.alpha = alpha;
     g.beta = beta;
     g.status_guard = guard;
+    g.status = S.status;
     err = launch_cl_gemm(g, st);
     ++*launches;
   }
