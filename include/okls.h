@@ -145,14 +145,15 @@ typedef enum okls_state_part {
  *                   previous basis: cyclic Jacobi in one CTA per matrix up
  *                   to 128 x 128, batched fp32 GEMMs past that, with a
  *                   logged-rotation Jacobi for sides up to 544 and a
- *                   blocked Jacobi (64 x 64 pair subproblems, rotations
- *                   applied as fp32 panel products) past 544).  On the
+ *                   blocked Jacobi (128 x 128 pair subproblems, rotations
+ *                   applied as fp32-accurate panel products on the tensor
+ *                   cores) past 544).  On the
  *                   batched path the workspace holds, per matrix, three
  *                   m x n and one max(mn, m^2, n^2) fp32 buffers, and per
- *                   side d two d x d buffers plus, for d <= 544, two more
+ *                   side d three d x d buffers plus, for d <= 544, one more
  *                   and (d > 128) an eigensolver slice of about 3 d^2
  *                   floats, or, past 544, a blocked-Jacobi slice of about
- *                   4 kp^2 floats (kp = d rounded up to a multiple of 64).
+ *                   4 kp^2 floats (kp = d rounded up to a multiple of 128).
  *                   OKLS_SOAP_LARGE=1 selects the batched path for every
  *                   shape, OKLS_SOAP_BLOCKED=1 the blocked solver for every
  *                   side past 128, and OKLS_EIG_CTAS=c caps the

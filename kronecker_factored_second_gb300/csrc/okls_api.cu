@@ -1181,10 +1181,10 @@ okls_status plan(const okls_config& c, uint8_t* state, uint8_t* ws, okls_handle_
         sb.blocked = soap_blocked_side(d) ? 1 : 0;
         sb.Qh = f32(B * d * d);
         sb.A = f32(B * d * d);
+        sb.P = f32(B * d * d);
         if (sb.blocked) {
           sb.BJ = f32(B * static_cast<int64_t>(bj_scratch_floats(static_cast<int>(d))));
         } else {
-          sb.P = f32(B * d * d);
           sb.Wq = f32(B * d * d);
           if (d > 128) sb.KK = f32(B * static_cast<int64_t>(eig_scratch_floats(static_cast<int>(d))));
         }

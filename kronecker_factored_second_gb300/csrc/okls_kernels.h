@@ -221,7 +221,8 @@ constexpr int kSoapLargeMax = 16384;
 inline float soap_tol2(int64_t d) { return 1e-12f * (d > 128 ? static_cast<float>(d) / 128.0f : 1.0f); }
 struct SoapSideBufs {
   float *Qh, *A;  // batch x d x d each
-  float *P, *Wq;  // batch x d x d each (sides up to kClMaxK)
+  float* P;       // batch x d x d: Q^^T Q, or (blocked) the previous basis
+  float* Wq;      // batch x d x d (sides up to kClMaxK)
   float* KK;      // eigensolver scratch for 128 < d <= kClMaxK: batch x eig_scratch_floats(d)
   float* BJ;      // blocked Jacobi scratch (blocked sides): batch x bj_scratch_floats(d)
   int blocked;    // the side's refresh runs the blocked solver

@@ -139,8 +139,8 @@ struct SlSide {
 };
 
 // Q^ = Q (1.5 I - 0.5 Q^T Q);  A = Q^^T F Q^;  P = Q^^T Q (for the signs; the
-// blocked solver takes them from Q directly).  The blocked side keeps no P:
-// T holds Q^T Q for the polar step.
+// blocked solver takes them from the previous basis directly, which it keeps
+// in P: T holds Q^T Q for its polar step).
 void sl_refresh_prep(SlRun& R, const SlSide& s) {
   const SoapLarge& S = R.S;
   const SoapSideBufs& B = *s.buf;
@@ -174,6 +174,38 @@ EigSide eig_side(const SoapLarge& S, const SlSide& s) {
   return e;
 }
 
+// The blocked sides: the sweeps from the polar-corrected previous basis, then
+// a refinement -- Q^^T F Q^ formed anew from the basis just found (through
+// the polar step again) and up to two more sweeps on it.  The solver tracks
+// Q^T F Q through hundreds of rounds of fp32 panel products, whose rounding
+// adds up; the refinement's sweeps start from the matrix itself, so what is
+// left is one sweep's rounding.
+void refine_blocked_passes(SlRun& R, const SlSide& sL, const SlSide& sR) {
+  const SoapLarge& S = R.S;
+  // both passes order and sign the columns against the previous basis (kept
+  // in P: near-equal eigenvalues may rank differently in the two passes)
+  for (const SlSide* s : {&sL, &sR}) {
+    if (R.err != cudaSuccess || !s->buf->blocked) continue;
+    R.err = cudaMemcpyAsync(s->buf->P, s->Q, static_cast<size_t>(S.batch) * s->d * s->d * sizeof(float),
+                            cudaMemcpyDeviceToDevice, R.st);
+  }
+  for (int pass = 0; pass < 2; ++pass) {
+    for (const SlSide* s : {&sL, &sR}) {
+      if (R.err != cudaSuccess || !s->buf->blocked) continue;
+      if (pass == 1) sl_refresh_prep(R, *s);
+      BjSide bj{};
+      bj.A = s->buf->A;
+      bj.Qh = s->buf->Qh;
+      bj.Qprev = s->buf->P;
+      bj.Qout = s->Q;
+      bj.scratch = s->buf->BJ;
+      bj.d = s->d;
+      bj.count = S.batch;
+      R.err = launch_bjacobi(bj, pass == 0 ? S.max_sweeps : 2, soap_tol2(s->d), S.status, R.st, R.launches);
+    }
+  }
+}
+
 // Both sides' bases: where both are in the logged-rotation solver's range
 // their eigen-decompositions go out in one set of launches (each is one CTA
 // per matrix, so this doubles the SMs at work); a blocked side runs its own
@@ -184,6 +216,7 @@ void sl_refresh(SlRun& R) {
   const SlSide sR{S.R, S.QR, S.n, &S.sideR};
   sl_refresh_prep(R, sL);
   sl_refresh_prep(R, sR);
+  refine_blocked_passes(R, sL, sR);
   EigPlan plan{};
   plan.max_sweeps = S.max_sweeps;
   plan.tol2 = S.tol2;
@@ -193,15 +226,7 @@ void sl_refresh(SlRun& R) {
     if (R.err != cudaSuccess) break;
     const SoapSideBufs& B = *s->buf;
     if (B.blocked) {
-      BjSide bj{};
-      bj.A = B.A;
-      bj.Qh = B.Qh;
-      bj.Qprev = s->Q;
-      bj.Qout = s->Q;
-      bj.scratch = B.BJ;
-      bj.d = s->d;
-      bj.count = S.batch;
-      R.err = launch_bjacobi(bj, S.max_sweeps, soap_tol2(s->d), S.status, R.st, R.launches);
+      continue;  // solved (and refined) above
     } else if (s->d > 128) {
       plan.side[nside++] = eig_side(S, *s);
     } else {

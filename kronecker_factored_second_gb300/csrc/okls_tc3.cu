@@ -32,6 +32,7 @@
 // products into registers and store the tile.  Every wait is bounded.
 #include <cuda_bf16.h>
 
+#include "okls_bj.cuh"
 #include "okls_internal.h"
 #include "okls_kernels.h"
 #include "okls_ptx.cuh"
@@ -435,7 +436,90 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_t3_gemm(const __grid_constant
       });
 }
 
+// ------------------------------------------------- blocked Jacobi panels
+// One CTA per (128-column tile, pair q, matrix x target): out (128 x 128) =
+// V_q^T (src rows 128q.., the tile's columns), K = 128, written by the
+// target's mode (okls_bj.cuh); a pair that was not rotated is copied (the
+// transposing copy through shared memory).
+__global__ void __launch_bounds__(kT3Threads, 1) k_t3_panel(const __grid_constant__ bj::Args P, int rd,
+                                                           bj::Panel t0, bj::Panel t1, int ntarget) {
+  extern __shared__ uint8_t t3_raw[];
+  const int b = blockIdx.z / ntarget, which = blockIdx.z % ntarget;
+  const bj::Panel T = which == 0 ? t0 : t1;
+  const int q = blockIdx.y, c0 = blockIdx.x * kT3N;
+  const bj::Mat M = bj::mat(P, b);
+  if (bj::skip(P, M)) return;
+  const int kp = P.kp, nb = P.nb;
+  const float* src = bj::buf(M, T.src_buf) + static_cast<int64_t>(q) * bj::kP * kp + c0;
+  float* dst = bj::buf(M, T.dst_buf);
+  if (M.flags[q] == 0) {
+    const int tid = threadIdx.x;
+    if (T.mode == 0) {
+      float* tile = reinterpret_cast<float*>(t3_raw);  // [i][c], pitch 129
+      for (int e = tid; e < bj::kP * kT3N; e += kT3Threads) {
+        const int i = e / kT3N, c = e % kT3N;
+        tile[i * (kT3N + 1) + c] = src[static_cast<int64_t>(i) * kp + c];
+      }
+      __syncthreads();
+      for (int e = tid; e < bj::kP * kT3N; e += kT3Threads) {
+        const int c = e / bj::kP, i = e % bj::kP;
+        dst[bj::panel_dst(0, q, i, c0 + c, rd, nb, kp)] = tile[i * (kT3N + 1) + c];
+      }
+    } else {
+      for (int e = tid; e < bj::kP * kT3N; e += kT3Threads) {
+        const int i = e / kT3N, c = e % kT3N;
+        dst[bj::panel_dst(T.mode, q, i, c0 + c, rd, nb, kp)] = src[static_cast<int64_t>(i) * kp + c];
+      }
+    }
+    return;
+  }
+  T3Src sa, sb;
+  sa.p = M.vv + static_cast<int64_t>(q) * bj::kP * bj::kP;  // element (i, l) of V^T at V[l][i]
+  sa.ld = bj::kP;
+  sa.rows = bj::kP;
+  sa.K = bj::kP;
+  sa.kmajor = 0;
+  sa.bf16 = 0;
+  sa.vec = 1;
+  sb.p = src;  // element (c, l) at src[l][c]
+  sb.ld = kp;
+  sb.rows = kT3N;
+  sb.K = bj::kP;
+  sb.kmajor = 0;
+  sb.bf16 = 0;
+  sb.vec = 1;
+  t3_tile(
+      t3_raw, bj::kP / kT3K, P.status_w,
+      [&](int kb, uint8_t* pa, uint8_t* pb) {
+        t3_fill(sa, kb * kT3K, pa);
+        t3_fill(sb, kb * kT3K, pb);
+      },
+      [&](int r, int cl, const float (&v)[32]) {
+        if (T.mode == 0) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dst[bj::panel_dst(0, q, r, c0 + cl + j, rd, nb, kp)] = v[j];
+        } else {
+          // 32 consecutive columns inside one 64-column block
+          float4* out = reinterpret_cast<float4*>(dst + bj::panel_dst(T.mode, q, r, c0 + cl, rd, nb, kp));
+#pragma unroll
+          for (int u = 0; u < 8; ++u) out[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        }
+      });
+}
+
 }  // namespace
+
+cudaError_t launch_t3_panels(const bj::Args& P, int rd, bj::Panel t0, bj::Panel t1, int ntarget, cudaStream_t st) {
+  static PerDevice pd;
+  cudaError_t e = once_per_device(pd, [](int) {
+    return cudaFuncSetAttribute(k_t3_panel, cudaFuncAttributeMaxDynamicSharedMemorySize, kT3Smem);
+  });
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(P.kp / kT3N), static_cast<unsigned>(P.nb / 2),
+                  static_cast<unsigned>(P.count * ntarget));
+  k_t3_panel<<<grid, kT3Threads, kT3Smem, st>>>(P, rd, t0, t1, ntarget);
+  return cudaGetLastError();
+}
 
 bool t3_gemm_eligible(const ClGemm& g) {
   if (!g.status) return false;

@@ -147,10 +147,10 @@ def test_soap_shapes_and_state(lib):
 def test_soap_batched_path_workspace(lib):
     """The SOAP batched path's workspace is what the header documents: per
     matrix three m x n and one max(mn, m^2, n^2) fp32 buffers, and per side
-    d two d x d buffers; up to d = 544 two more and, for d > 128, an
+    d three d x d buffers; up to d = 544 one more and, for d > 128, an
     eigensolver slice of A (full, dp x dp with dp = d rounded up to even), V
     (d x d) and one sweep's rotation log ((dp - 1) x dp floats); past 544 the
-    blocked Jacobi slice (four kp x kp buffers, kp = d rounded up to 64, the
+    blocked Jacobi slice (four kp x kp buffers, kp = d rounded up to 128, the
     pair rotations and small per-position arrays).  The fixed part
     (descriptor table, scalars, status word, alignment) stays under 1 MiB."""
     def r4(x):
@@ -161,10 +161,10 @@ def test_soap_batched_path_workspace(lib):
         return r4(dp * dp) + r4(d * d) + r4((dp - 1) * dp) + 4
 
     def blocked(d):
-        # A and A P, the basis panels (two), pair rotations, flags and
-        # per-position arrays, the stopping rule's partials
-        kp = (d + 63) // 64 * 64
-        return 4 * kp * kp + (kp // 64) * 64 * 64 + r4(kp // 64) + 4 * r4(kp) + 4 * 32 + 4
+        # A and A P, the basis panels (two), pair rotations (128 x 128 each),
+        # flags and per-position arrays, the stopping rule's partials
+        kp = (d + 127) // 128 * 128
+        return 4 * kp * kp + (kp // 128) * 128 * 128 + r4(kp // 128) + 4 * r4(kp) + 4 * 32 + 4
 
     for B, m, n in [(2, 544, 331), (3, 300, 100), (1, 129, 544), (2, 600, 100), (1, 2048, 5504), (1, 545, 700)]:
         c = L.config_default(B, m, n)
@@ -172,11 +172,11 @@ def test_soap_batched_path_workspace(lib):
         _s, w = L.state_bytes(c)
         floats = B * (3 * m * n + max(m * n, m * m, n * n))
         for d in (m, n):
-            floats += B * 2 * d * d
+            floats += B * 3 * d * d
             if d > 544:
                 floats += B * blocked(d)
             else:
-                floats += B * 2 * d * d + (B * eig(d) if d > 128 else 0)
+                floats += B * d * d + (B * eig(d) if d > 128 else 0)
         assert 4 * floats <= w <= 4 * floats + (1 << 20), (B, m, n, w, 4 * floats)
 
 

@@ -221,8 +221,7 @@ def test_full_size_layer_shapes(gi):
     group is checked teacher-forced at every step (M, V, L, R, N) and at the
     refreshes its bases (orthogonality, diagonalisation, order, signs and the
     gapped eigenvectors against float64 eigenvectors of the GPU's L, R), with
-    the bars of the smaller shapes (sqrt(d / 128) where they grow with d; the
-    diagonalisation bar, 1e-5 up to d = 2048, grows like d past it)."""
+    the bars of the smaller shapes (sqrt(d / 128) where they grow with d)."""
     from kronecker_factored_second_gb300.okls import OklsBatch
     from kronecker_factored_second_gb300.workloads import GradientStream, workload
     import time
@@ -271,12 +270,6 @@ def test_full_size_layer_shapes(gi):
     assert worst["N"] < 2e-2, worst
     for side in ("QL", "QR"):
         grow = max(1.0, (m if side == "QL" else n) / 128) ** 0.5
-        # the diagonalisation bar grows with d past 2048: the blocked solver
-        # tracks Q^T L Q through sweeps of d / 32 - 1 rounds of 64-deep fp32
-        # panel products, whose rounding adds up round after round (measured
-        # 6-7e-6 at d = 2048, 1.3-2.1e-5 at d = 5504); the eigenvector bar
-        # below keeps its sqrt(d / 128) growth
-        d = m if side == "QL" else n
-        assert worst[side + "_orth"] < 1e-5 * grow and worst[side + "_offdiag"] < 1e-5 * max(1.0, d / 2048), worst
+        assert worst[side + "_orth"] < 1e-5 * grow and worst[side + "_offdiag"] < 1e-5, worst
         assert worst[side + "_order"] < 1e-6 and worst[side + "_sign"] == 0.0, worst
         assert worst[side + "_vec_gap"] < 2e-6 * grow, worst
