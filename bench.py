@@ -313,7 +313,7 @@ def run_okls(args):
     extra = {}
     if args.method == "soap":
         # SOAP's Adam hyperparameters; the eigenbases are refreshed every 10 steps
-        extra = dict(beta1=0.95, beta2=0.95, eps=1e-8, weight_decay=0.0, root_every=10)
+        extra = dict(beta1=0.95, beta2=0.95, eps=1e-8, weight_decay=0.0, root_every=args.root_every)
     for gi, g in enumerate(wl.groups):
         ob = OklsBatch(g.batch, g.m, g.n, param_dtype=g.dtype, ns_split_iters=args.split, ridge=args.ridge,
                        method=args.method, device=dev, **extra)
@@ -640,8 +640,9 @@ def run_okls(args):
             "config": {
                 "workload": workload_desc(wl),
                 "method": args.method,
-                "precision": ("fp32 throughout (batched CUDA-core GEMMs, Jacobi eigenbasis refresh every 10 "
-                              "steps)" if args.method == "soap" else
+                "precision": ("fp32-accurate throughout (products on the tensor cores as three-term bf16 splits "
+                              "with fp32 accumulation; blocked Jacobi eigenbasis refresh every "
+                              f"{args.root_every} steps)" if args.method == "soap" else
                               f"binary16 Newton-Schulz operands, fp32 accumulation, split_iters={args.split}, "
                               f"ridge={args.ridge:g}"),
                 "l2": (f"inputs larger than L2: {in_bytes / 1e9:.2f} GB of gradients and "
@@ -701,6 +702,7 @@ def main():
     ap.add_argument("--also-clean", type=int, default=1)
     ap.add_argument("--also-clean-large", type=int, default=1)
     ap.add_argument("--method", choices=["okls", "shampoo", "soap"], default="okls")
+    ap.add_argument("--root-every", type=int, default=10, help="SOAP: eigenbasis refresh interval")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "okls":

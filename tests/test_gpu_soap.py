@@ -167,10 +167,15 @@ def _teacher_forced(B, m, n, dtype):
     ob.close()
 
 
-def test_without_refresh_the_step_is_adam():
+@pytest.mark.parametrize("B,m,n,large", [(2, 24, 16, False), (2, 320, 192, True)])
+def test_without_refresh_the_step_is_adam(B, m, n, large, monkeypatch):
     """Before any refresh the bases are the identity: SOAP is Adam with both
-    moments bias-corrected."""
-    B, m, n = 2, 24, 16
+    moments bias-corrected.  On the batched path (320 x 192) the rotations
+    are tensor-core products of three-term bf16 splits: the identity's split
+    is exact, so the rotations return G and N' to within fp32 rounding (an
+    fp32 value's three terms hold it to 2^-27)."""
+    if large:
+        monkeypatch.setenv("OKLS_SOAP_LARGE", "1")
     lr, b1, b2, eps = 0.02, 0.9, 0.99, 1e-8
     ob = _batch(B, m, n, lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=0.0, root_every=1000)
     rng = np.random.default_rng(3)
