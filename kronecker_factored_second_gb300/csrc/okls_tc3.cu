@@ -112,19 +112,22 @@ struct T3Src {
   int kmajor, bf16, vec;
 };
 
-__device__ __forceinline__ float t3_ld(const T3Src& s, int64_t i) {
-  return s.bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(s.p)[i])
-                : __ldg(reinterpret_cast<const float*>(s.p) + i);
+template <bool kBf16>
+__device__ __forceinline__ float t3_ld(const void* p, int64_t i) {
+  if constexpr (kBf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  else return __ldg(reinterpret_cast<const float*>(p) + i);
 }
 
 // 4 consecutive elements at element offset i (16-byte fp32 or 8-byte bf16 load)
-__device__ __forceinline__ float4 t3_ld4(const T3Src& s, int64_t i) {
-  if (s.bf16) {
-    const uint2 q = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(s.p) + i));
+template <bool kBf16>
+__device__ __forceinline__ float4 t3_ld4(const void* p, int64_t i) {
+  if constexpr (kBf16) {
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i));
     return make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u), __uint_as_float(q.y << 16),
                        __uint_as_float(q.y & 0xffff0000u));
+  } else {
+    return __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + i));
   }
-  return __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(s.p) + i));
 }
 
 constexpr int kT3KItems = (kT3M * 8 + kT3Prod - 1) / kT3Prod;        // K-contiguous: (row, chunk) items per thread
@@ -132,26 +135,28 @@ constexpr int kT3MItems = (kT3M / 4 * 8 + kT3Prod - 1) / kT3Prod;    // row-cont
 
 // all producer threads: the stage's tile of one operand, K columns k0..k0+63.
 // Every load of the thread is issued before the first split, so a stage
-// waits for memory once.
-__device__ __forceinline__ void t3_fill(const T3Src& s, int k0, uint8_t* part0) {
+// waits for memory once.  A whole tile in range with aligned rows takes the
+// vector path without per-element checks.
+template <bool kKmajor, bool kBf16>
+__device__ __forceinline__ void t3_fill_t(const T3Src& s, int k0, uint8_t* part0) {
   const int tid = threadIdx.x - kT3Drain;
-  if (s.kmajor) {
+  const bool whole = s.vec && s.rows >= kT3M && k0 + kT3K <= s.K;
+  if constexpr (kKmajor) {
     // item (row r, chunk kc): 8 consecutive k of one row; 8 lanes per row
     float v[kT3KItems][8];
 #pragma unroll
     for (int it = 0; it < kT3KItems; ++it) {
       const int idx = tid + it * kT3Prod;
       const int r = idx >> 3, k = k0 + 8 * (idx & 7);
-      if (idx < kT3M * 8 && r < s.rows && k + 8 <= s.K && s.vec) {
-        const int64_t o = static_cast<int64_t>(r) * s.ld + k;
-        const float4 a = t3_ld4(s, o), b = t3_ld4(s, o + 4);
+      const int64_t o = static_cast<int64_t>(r) * s.ld + k;
+      if (idx < kT3M * 8 && (whole || (s.vec && r < s.rows && k + 8 <= s.K))) {
+        const float4 a = t3_ld4<kBf16>(s.p, o), b = t3_ld4<kBf16>(s.p, o + 4);
         v[it][0] = a.x; v[it][1] = a.y; v[it][2] = a.z; v[it][3] = a.w;
         v[it][4] = b.x; v[it][5] = b.y; v[it][6] = b.z; v[it][7] = b.w;
       } else {
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          v[it][u] = (idx < kT3M * 8 && r < s.rows && k + u < s.K) ? t3_ld(s, static_cast<int64_t>(r) * s.ld + k + u)
-                                                                    : 0.0f;
+          v[it][u] = (idx < kT3M * 8 && r < s.rows && k + u < s.K) ? t3_ld<kBf16>(s.p, o + u) : 0.0f;
       }
     }
 #pragma unroll
@@ -168,21 +173,33 @@ __device__ __forceinline__ void t3_fill(const T3Src& s, int k0, uint8_t* part0) 
     for (int it = 0; it < kT3MItems; ++it) {
       const int idx = tid + it * kT3Prod;
       const int kc = idx & 7, r = 4 * (idx >> 3);
-      const bool quad = idx < kT3M * 2 && r + 4 <= s.rows && s.vec;
+      const int64_t o0 = static_cast<int64_t>(k0 + 8 * kc) * s.ld + r;
+      if (idx < kT3M * 2 && whole) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int k = k0 + 8 * kc + u;
-        const int64_t o = static_cast<int64_t>(k) * s.ld + r;
-        if (quad) {
-          const float4 a = k < s.K ? t3_ld4(s, o) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < 8; ++u) {
+          const float4 a = t3_ld4<kBf16>(s.p, o0 + u * s.ld);
           v[it][4 * u] = a.x;
           v[it][4 * u + 1] = a.y;
           v[it][4 * u + 2] = a.z;
           v[it][4 * u + 3] = a.w;
-        } else {
+        }
+      } else {
+        const bool quad = idx < kT3M * 2 && r + 4 <= s.rows && s.vec;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            v[it][4 * u + i] = (idx < kT3M * 2 && r + i < s.rows && k < s.K) ? t3_ld(s, o + i) : 0.0f;
+        for (int u = 0; u < 8; ++u) {
+          const int k = k0 + 8 * kc + u;
+          const int64_t o = o0 + u * s.ld;
+          if (quad) {
+            const float4 a = k < s.K ? t3_ld4<kBf16>(s.p, o) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[it][4 * u] = a.x;
+            v[it][4 * u + 1] = a.y;
+            v[it][4 * u + 2] = a.z;
+            v[it][4 * u + 3] = a.w;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              v[it][4 * u + i] = (idx < kT3M * 2 && r + i < s.rows && k < s.K) ? t3_ld<kBf16>(s.p, o + i) : 0.0f;
+          }
         }
       }
     }
@@ -199,6 +216,18 @@ __device__ __forceinline__ void t3_fill(const T3Src& s, int k0, uint8_t* part0) 
         t3_store(part0, r + i, kc, w);
       }
     }
+  }
+}
+
+// the operand's layout and element type are uniform over the grid: one
+// specialised fill per combination
+__device__ __forceinline__ void t3_fill(const T3Src& s, int k0, uint8_t* part0) {
+  if (s.kmajor) {
+    if (s.bf16) t3_fill_t<true, true>(s, k0, part0);
+    else t3_fill_t<true, false>(s, k0, part0);
+  } else {
+    if (s.bf16) t3_fill_t<false, true>(s, k0, part0);
+    else t3_fill_t<false, false>(s, k0, part0);
   }
 }
 
