@@ -278,3 +278,32 @@ def test_full_size_layer_shapes(gi):
         assert worst[side + "_orth"] < 1e-5 * grow and worst[side + "_offdiag"] < 1e-5, worst
         assert worst[side + "_order"] < 1e-6 and worst[side + "_sign"] == 0.0, worst
         assert worst[side + "_vec_gap"] < 2e-6 * grow, worst
+
+
+_CUDA_CORE_SCRIPT = r"""
+import os, sys
+sys.path.insert(0, os.path.join(os.environ["OKLS_ROOT"], "tests"))
+sys.path.insert(0, os.environ["OKLS_ROOT"])
+import torch
+import test_gpu_soap as T
+torch.cuda.set_device(0)
+os.environ["OKLS_SOAP_LARGE"] = "1"
+os.environ["OKLS_SOAP_BLOCKED"] = "1"
+T._teacher_forced(1, 300, 140, torch.float32)   # blocked solver, padded side
+os.environ["OKLS_SOAP_BLOCKED"] = "0"
+T._teacher_forced(1, 544, 331, torch.float32)   # logged-rotation solver, 544-deep products
+"""
+
+
+def test_cuda_core_products_subprocess():
+    """With OKLS_TC3=0 (read once per process, hence a separate one) every
+    fp32 product runs on the CUDA cores (k_cl_gemm) and the blocked solver's
+    panels on k_bj_rows; the same teacher-forced bars hold there."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, OKLS_TC3="0", OKLS_ROOT=root)
+    r = subprocess.run([sys.executable, "-c", _CUDA_CORE_SCRIPT], env=env, timeout=900, capture_output=True, text=True)
+    print(r.stdout[-2000:])
+    assert r.returncode == 0, r.stderr[-4000:]
