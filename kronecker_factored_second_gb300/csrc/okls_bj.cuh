@@ -19,8 +19,13 @@ __host__ __device__ inline int64_t r4(int64_t x) { return (x + 3) & ~int64_t(3);
 // image A P, the basis panels (two: they alternate round by round), the pair
 // rotations, flags, the per-position arrays of the finish and the partials
 struct Layout {
-  int64_t kk, a0, a1, q0, q1, vv, flags, lam, inv, orig, sign, parts, misc, total;
+  int64_t kk, a0, a1, q0, q1, vv, vimg, flags, lam, inv, orig, sign, parts, misc, total;
 };
+
+// V^T of a pair as the tensor-core panel product's A operand: for each of the
+// two 64-deep K-blocks the three bf16 terms, each a 128-row x 128-byte image
+// in the 128-byte-swizzled K-major layout (16 KB): 96 KB per pair
+constexpr int kVimgFloats = 2 * 3 * kP * 64 / 2;
 
 __host__ __device__ inline Layout layout(int kp) {
   Layout L;
@@ -31,7 +36,8 @@ __host__ __device__ inline Layout layout(int kp) {
   L.q0 = L.a1 + L.kk;
   L.q1 = L.q0 + L.kk;
   L.vv = L.q1 + L.kk;
-  L.flags = L.vv + np * kP * kP;
+  L.vimg = L.vv + np * kP * kP;
+  L.flags = L.vimg + np * kVimgFloats;
   L.lam = L.flags + r4(np);
   L.inv = L.lam + r4(kp);
   L.orig = L.inv + r4(kp);
@@ -57,7 +63,7 @@ struct Args {
 };
 
 struct Mat {
-  float *a0, *a1, *q0, *q1, *vv, *lam, *sign;
+  float *a0, *a1, *q0, *q1, *vv, *vimg, *lam, *sign;
   int *flags, *inv, *orig;
   double* parts;
   int* misc;
@@ -73,6 +79,7 @@ __device__ __forceinline__ Mat mat(const Args& P, int b) {
   M.q0 = s + L.q0;
   M.q1 = s + L.q1;
   M.vv = s + L.vv;
+  M.vimg = s + L.vimg;
   M.flags = reinterpret_cast<int*>(s + L.flags);
   M.lam = s + L.lam;
   M.inv = reinterpret_cast<int*>(s + L.inv);

@@ -43,6 +43,8 @@
 // would meet the stopping rule (tol2 d2 / d^2, d2 the diagonal's squared
 // norm), so entries at the rounding floor of a large row are not rotated
 // again and again.
+#include <cuda_bf16.h>
+
 #include <cstdlib>
 
 #include "okls_bj.cuh"
@@ -58,7 +60,7 @@ namespace {
 constexpr int kT = 32;              // tile edge of the transposing copies
 constexpr int kPitch = kP + 1;      // odd pitch of the subproblem in shared memory
 constexpr int kSolveThreads = 512;
-constexpr int kSolveSmem = 2 * kP * kPitch * 4;
+constexpr int kSolveSmem = 2 * kP * kPitch * 4 + kP * kP * 4;  // A, V, and the polar-corrected V
 constexpr int kInner = 2;           // Jacobi sweeps per subproblem at most (more do not cut the outer sweeps)
 constexpr int kThreads = 256;
 constexpr int kRowCols = 64;        // columns per CTA of the CUDA-core panel product
@@ -268,12 +270,40 @@ __global__ void __launch_bounds__(kSolveThreads) k_bj_solve(Args P) {
       Xs[a * kPitch + c] = (a == c ? 1.5f : 0.0f) - 0.5f * x;
     }
     __syncthreads();
+    float* Vc = sm + 2 * kP * kPitch;  // the corrected V, row-major
     float* V = M.vv + static_cast<int64_t>(q) * kP * kP;
     for (int e = threadIdx.x; e < kP * kP; e += blockDim.x) {
       const int i = e / kP, c = e % kP;
       float v = 0.0f;
       for (int l = 0; l < kP; ++l) v = fmaf(Vs[i * kPitch + l], Xs[l * kPitch + c], v);
       V[e] = v;
+      Vc[e] = v;
+    }
+    __syncthreads();
+    // V^T as the panel product's A operand (row r = i, k = l: V[l][i]), split
+    // into three bf16 terms and laid out as the tensor core reads it: K-block
+    // kb, term j, row r, 16-byte chunk kc at (kc ^ (r % 8)) * 16
+    uint8_t* img = reinterpret_cast<uint8_t*>(M.vimg + static_cast<int64_t>(q) * kVimgFloats);
+    constexpr int kPart = kP * 128;  // bytes of one term's image
+    for (int e = threadIdx.x; e < kP * 2 * 8; e += blockDim.x) {
+      const int r = e & (kP - 1), kc = (e >> 7) & 7, kb = e >> 10;
+      uint32_t w[3][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int l = 64 * kb + 8 * kc + 2 * u;
+        const float x0 = Vc[l * kP + r], x1 = Vc[(l + 1) * kP + r];
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x0, x1);
+        const float r0 = x0 - __low2float(a), r1 = x1 - __high2float(a);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
+        const __nv_bfloat162 c = __floats2bfloat162_rn(r0 - __low2float(b), r1 - __high2float(b));
+        w[0][u] = *reinterpret_cast<const uint32_t*>(&a);
+        w[1][u] = *reinterpret_cast<const uint32_t*>(&b);
+        w[2][u] = *reinterpret_cast<const uint32_t*>(&c);
+      }
+      const uint32_t off = static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(kc) ^ (r & 7u)) << 4);
+#pragma unroll
+      for (int j = 0; j < 3; ++j)
+        *reinterpret_cast<uint4*>(img + (kb * 3 + j) * kPart + off) = make_uint4(w[j][0], w[j][1], w[j][2], w[j][3]);
     }
   }
 }

@@ -502,14 +502,9 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_t3_panel(const __grid_constan
     }
     return;
   }
-  T3Src sa, sb;
-  sa.p = M.vv + static_cast<int64_t>(q) * bj::kP * bj::kP;  // element (i, l) of V^T at V[l][i]
-  sa.ld = bj::kP;
-  sa.rows = bj::kP;
-  sa.K = bj::kP;
-  sa.kmajor = 0;
-  sa.bf16 = 0;
-  sa.vec = 1;
+  // A: V_q^T, split once by the solve kernel into the three terms' images
+  const uint4* vimg = reinterpret_cast<const uint4*>(M.vimg + static_cast<int64_t>(q) * bj::kVimgFloats);
+  T3Src sb;
   sb.p = src;  // element (c, l) at src[l][c]
   sb.ld = kp;
   sb.rows = kT3N;
@@ -520,7 +515,9 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_t3_panel(const __grid_constan
   t3_tile(
       t3_raw, bj::kP / kT3K, P.status_w,
       [&](int kb, uint8_t* pa, uint8_t* pb) {
-        t3_fill(sa, kb * kT3K, pa);
+        const uint4* in = vimg + kb * (3 * kT3Part / 16);
+        uint4* out = reinterpret_cast<uint4*>(pa);
+        for (int i = threadIdx.x - kT3Drain; i < 3 * kT3Part / 16; i += kT3Prod) out[i] = __ldg(in + i);
         t3_fill(sb, kb * kT3K, pb);
       },
       [&](int r, int cl, const float (&v)[32]) {

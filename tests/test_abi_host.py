@@ -164,7 +164,8 @@ def test_soap_batched_path_workspace(lib):
         # A and A P, the basis panels (two), pair rotations (128 x 128 each),
         # flags and per-position arrays, the stopping rule's partials
         kp = (d + 127) // 128 * 128
-        return 4 * kp * kp + (kp // 128) * 128 * 128 + r4(kp // 128) + 4 * r4(kp) + 4 * 32 + 4
+        # (the rotations also as the tensor core's bf16 images: 96 KB per pair)
+        return 4 * kp * kp + (kp // 128) * (128 * 128 + 24576) + r4(kp // 128) + 4 * r4(kp) + 4 * 32 + 4
 
     for B, m, n in [(2, 544, 331), (3, 300, 100), (1, 129, 544), (2, 600, 100), (1, 2048, 5504), (1, 545, 700)]:
         c = L.config_default(B, m, n)
