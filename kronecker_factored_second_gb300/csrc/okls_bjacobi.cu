@@ -61,7 +61,7 @@ constexpr int kT = 32;              // tile edge of the transposing copies
 constexpr int kPitch = kP + 1;      // odd pitch of the subproblem in shared memory
 constexpr int kSolveThreads = 512;
 constexpr int kSolveSmem = 2 * kP * kPitch * 4 + kP * kP * 4;  // A, V, and the polar-corrected V
-constexpr int kInner = 2;           // Jacobi sweeps per subproblem at most (more do not cut the outer sweeps)
+constexpr int kInner = 2;           // Jacobi sweeps per subproblem at most (more do not cut the outer sweeps; one is faster on small batches, slower on the 1.2B layer set)
 constexpr int kThreads = 256;
 constexpr int kRowCols = 64;        // columns per CTA of the CUDA-core panel product
 constexpr int kRowSmem = (kP * kP + kP * kRowCols) * 4;
