@@ -563,6 +563,44 @@ def run_okls(args):
             "state_gb": sum(ob.state.numel() for (_g, ob, _W, _G) in groups) / 1e9}
         del cnoise
 
+    soap_large_line = None
+    if args.also_soap_large and args.method == "okls" and args.workload == "llama1.2b":
+        # SOAP over the same layer set (betas 0.95, refresh every 10 steps): the
+        # warm-up holds the first refresh (from the identity), the timed steps
+        # one refresh warm-started from the previous bases
+        try:
+            rebuild(method="soap", root_every=10, beta1=0.95, beta2=0.95, eps=1e-8, weight_decay=0.0, lr=args.lr)
+
+            def soap_step(k):
+                for (_g, ob, W, Gs) in groups:
+                    ob.step(W, Gs[k % len(Gs)], args.lr)
+            for k in range(10):
+                soap_step(k)
+            torch.cuda.synchronize()
+            ssteps = 10
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k in range(ssteps):
+                soap_step(10 + k)
+            b.record(stream)
+            torch.cuda.synchronize()
+            for (_g, ob, _W, _G) in groups:
+                if ob.status_nothrow()[1]:
+                    raise RuntimeError("device status flagged in the SOAP leg")
+            ms6 = max_over_ranks(a.elapsed_time(b), ws, dev)
+            fs = sum(g.batch * dense_flops(g.m, g.n, "soap") for g in wl.groups)
+            soap_large_line = {
+                "method": "SOAP (Adam in the factors' eigenbases, refresh every 10 steps, betas 0.95); "
+                          "fp32-accurate products on the tensor cores (three-term bf16 split), blocked Jacobi "
+                          "refresh", "workload": "the same 168-matrix layer set, bf16 W and G, fp32 state",
+                "steps": ssteps, "warmup": 10,
+                "value": sum_over_ranks(matrices * ssteps, ws, dev) / (ms6 / 1e3), "unit": "matrices/s",
+                "ms_per_step": ms6 / ssteps,
+                "tflops_products": sum_over_ranks(fs * ssteps, ws, dev) / (ms6 / 1e3) / 1e12,
+                "state_gb": sum(ob.state.numel() for (_g, ob, _W, _G) in groups) / 1e9}
+        except Exception as e:  # the headline line is printed either way
+            soap_large_line = {"error": str(e)[:300]}
+
     def small_leg(method, wl_name="single128x64", nsteps=200, **kw):
         """A small workload for the SOAP and Clean modes (one 128 x 64 matrix
         by default), `nsteps` timed steps after 20 warm-up steps; Clean's
@@ -622,8 +660,8 @@ def run_okls(args):
         cpu = oracle_sample(wl)
 
     if rank == 0:
-        # SOAP's products run on CUDA-core GEMMs that the per-launch events do
-        # not time: no roofline object for that mode
+        # SOAP's products run on other kernels than the per-launch events
+        # time: no roofline object for that mode
         roofline = None if args.method == "soap" else {
             "bound": "tensor", "kernel": "okls_gemm_kernel (tcgen05, all products of the step)",
             "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -672,6 +710,8 @@ def run_okls(args):
             line["clean"] = clean_line
         if clean_large_line:
             line["clean_large"] = clean_large_line
+        if soap_large_line:
+            line["soap_large"] = soap_large_line
         if soap512_line:
             line["soap_512"] = soap512_line
         if clean512_line:
@@ -701,6 +741,7 @@ def main():
     ap.add_argument("--also-soap", type=int, default=1)
     ap.add_argument("--also-clean", type=int, default=1)
     ap.add_argument("--also-clean-large", type=int, default=1)
+    ap.add_argument("--also-soap-large", type=int, default=1)
     ap.add_argument("--method", choices=["okls", "shampoo", "soap"], default="okls")
     ap.add_argument("--root-every", type=int, default=10, help="SOAP: eigenbasis refresh interval")
     ap.add_argument("--no-cpu-baseline", action="store_true")
