@@ -10,7 +10,7 @@
 `Shampoo`          the classic Shampoo step (summed factors, -1/4 roots)
                    over the same kernels (method="shampoo").
 `SOAP`             Adam in the factors' eigenbasis (method="soap"; matrices up
-                   to 544 x 544 in this build).
+                   to 16384 x 16384 in this build).
 `Clean`            block-wise Adam in Nystrom low-rank bases (method="clean";
                    matrices up to 16384 x 16384 and rank + oversample <= 544
                    in this build); the sketch's Gaussian draws come from a
@@ -320,8 +320,8 @@ class Shampoo(torch.optim.Optimizer):
 
 class SOAP(torch.optim.Optimizer):
     """SOAP (Clean page, Appendix C, Algorithm 4) over 2-D and 3-D CUDA
-    parameters with both dimensions <= 544: Adam run in the eigenbases of the
-    factor EMAs L, R, refreshed every `precondition_frequency` steps."""
+    parameters with both dimensions <= 16384: Adam run in the eigenbases of
+    the factor EMAs L, R, refreshed every `precondition_frequency` steps."""
 
     def __init__(self, params, lr: float = 3e-3, betas=(0.95, 0.95), eps: float = 1e-8,
                  weight_decay: float = 0.0, precondition_frequency: int = 10):
