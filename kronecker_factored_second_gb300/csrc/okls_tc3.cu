@@ -11,13 +11,16 @@
 // the CUDA cores runs at ~1/50 of the tensor rate.
 //
 // The split: x = b1 + b2 + b3 with b1 = bf16(x), b2 = bf16(x - b1),
-// b3 = bf16(x - b1 - b2) (round to nearest; each difference is exact in fp32),
-// which holds x to 2^-27 of itself.  A product of two split values keeps
-// the six terms down to 2^-18 of the leading one,
-//   b1 c1 + b1 c2 + b2 c1 + b1 c3 + b3 c1 + b2 c2,
-// each product of two bf16 values exact in the fp32 accumulator; what is
-// left out is below 2^-26 of |x c|.  The accumulation is fp32 in TMEM, so the
-// result carries the rounding of an fp32 product with K-deep sums.  A value
+// b3 = bf16(x - b1 - b2) (round to nearest; each difference is exact in
+// fp32), and the three terms hold x exactly (|b2| <= 2^-8 |x|,
+// |b3| <= 2^-17 |x|: three 8-bit terms with signed rounding cover fp32's
+// 24-bit significand).  A product of two split values keeps six terms,
+//   b1 c1 + b1 c2 + b2 c1 + b1 c3 + b3 c1 + b2 c2
+// (down to 2^-15 of the leading one), each product of two bf16 values exact
+// in the fp32 accumulator; what is left out (b2 c3 + b3 c2 + b3 c3) is at
+// most 2^-24 of |x c|, fp32's unit roundoff.  The accumulation is fp32 in
+// TMEM, so the result carries the rounding of an fp32 product with K-deep
+// sums.  A value
 // that bf16 holds exactly (an identity rotation, a bf16 gradient) has
 // b2 = b3 = 0 and its products are exact: multiplying by the identity
 // reproduces the other operand bit for bit.

@@ -173,7 +173,7 @@ def test_without_refresh_the_step_is_adam(B, m, n, large, monkeypatch):
     moments bias-corrected.  On the batched path (320 x 192) the rotations
     are tensor-core products of three-term bf16 splits: the identity's split
     is exact, so the rotations return G and N' to within fp32 rounding (an
-    fp32 value's three terms hold it to 2^-27)."""
+    fp32 value's three terms hold it exactly)."""
     if large:
         monkeypatch.setenv("OKLS_SOAP_LARGE", "1")
     lr, b1, b2, eps = 0.02, 0.9, 0.99, 1e-8
