@@ -7,9 +7,9 @@
 // polar-corrected previous basis Q^; this file diagonalises A and writes
 // Q^ W, reordered and sign-aligned, over the previous basis.
 //
-// The method: two-sided block Jacobi.  A (padded to kp, a multiple of 64, by
-// zero rows and columns that no rotation ever touches) is split into
-// nb = kp / 64 blocks of 64 (kp a multiple of 128); a sweep is the nb - 1
+// The method: two-sided block Jacobi.  A (padded to kp, a multiple of 128,
+// by zero rows and columns that no rotation ever touches) is split into
+// nb = kp / 64 blocks of 64; a sweep is the nb - 1
 // rounds of the round-robin pairing of the blocks, and a round diagonalises
 // each of its nb / 2 pair subproblems (128 x 128, one CTA each, cyclic Jacobi
 // in shared memory with the threshold rule, then one polar step on V) and
@@ -39,10 +39,11 @@
 // Accuracy: the rotations are fp32-accurate panel products with 128-deep
 // sums; the threshold rule skips a pair whose off-diagonal entry is below
 // tol2 / d of its diagonal product or below the level at which every entry
-// together
-// would meet the stopping rule (tol2 d2 / d^2, d2 the diagonal's squared
-// norm), so entries at the rounding floor of a large row are not rotated
-// again and again.
+// together would meet the stopping rule (tol2 d2 / d^2, d2 the diagonal's
+// squared norm), so entries at the rounding floor of a large row are not
+// rotated again and again.  After the sweeps the caller forms Q^T F Q anew
+// from the basis found and runs up to two more sweeps on it (the tracked
+// matrix gathers the rounding of hundreds of rounds).
 #include <cuda_bf16.h>
 
 #include <cstdlib>

@@ -20,10 +20,9 @@
 // in the fp32 accumulator; what is left out (b2 c3 + b3 c2 + b3 c3) is at
 // most 2^-24 of |x c|, fp32's unit roundoff.  The accumulation is fp32 in
 // TMEM, so the result carries the rounding of an fp32 product with K-deep
-// sums.  A value
-// that bf16 holds exactly (an identity rotation, a bf16 gradient) has
-// b2 = b3 = 0 and its products are exact: multiplying by the identity
-// reproduces the other operand bit for bit.
+// sums.  A value that bf16 holds exactly (an identity rotation, a bf16
+// gradient) has b2 = b3 = 0 and its products are exact: multiplying by the
+// identity reproduces the other operand bit for bit.
 //
 // The kernel: one CTA per 128 x 128 output tile, K in stages of 64 (one
 // 128-byte bf16 row per operand row, the SWIZZLE_128B K-major layout that
